@@ -1,0 +1,280 @@
+"""Checks that pin the CPU oracle to facts outside itself.
+
+Each ``check_*`` function takes the oracle module and raises AssertionError
+when the oracle disagrees with a brute-force computation, a textbook or
+library routine, an invariant of the method or a value printed on the source
+pages.  The pin tests call them on the real oracle; the mutation tests plant
+plausible mistakes in the oracle and expect them to fail.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+import scipy.special
+import torch
+import torch.nn.functional as F
+
+import workloads
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _brute_topk(L, k):
+    """Python sort with key (-logit, index): the lower index wins a tie."""
+    T, E = L.shape
+    ids = np.zeros((T, k), dtype=np.int64)
+    w = np.zeros((T, k))
+    for t in range(T):
+        order = sorted(range(E), key=lambda e: (-L[t, e], e))[:k]
+        ids[t] = order
+        m = L[t, order[0]]
+        z = [math.exp(L[t, e] - m) for e in order]
+        w[t] = [v / sum(z) for v in z]
+    return ids, w
+
+
+def check_topk_brute_force(o):
+    rng = _rng(1)
+    for E, k in [(7, 3), (8, 2), (16, 5), (5, 5), (9, 1)]:
+        # small integer logits force many exact ties
+        L = rng.integers(-3, 4, size=(60, E)).astype(np.float64) * 0.5
+        ids, w = o.topk_softmax(L, k)
+        bids, bw = _brute_topk(L, k)
+        assert np.array_equal(ids, bids), "top-k ids differ from brute force"
+        assert np.allclose(w, bw, rtol=0, atol=1e-15), "top-k weights differ from brute force"
+        L2 = rng.standard_normal((40, E))
+        ids, w = o.topk_softmax(L2, k)
+        bids, bw = _brute_topk(L2, k)
+        assert np.array_equal(ids, bids)
+        assert np.allclose(w, bw, rtol=0, atol=1e-15)
+
+
+def check_topk_all_equal(o):
+    L = np.zeros((4, 12))
+    ids, w = o.topk_softmax(L, 5)
+    assert np.array_equal(ids, np.tile(np.arange(5), (4, 1))), "all-equal logits must give ids 0..k-1"
+    assert np.allclose(w, 0.2, rtol=0, atol=1e-15)
+
+
+def check_topk_full_softmax(o):
+    """k = E reduces renormalised top-k gating to the textbook softmax."""
+    rng = _rng(2)
+    L = rng.standard_normal((30, 9)) * 3
+    ids, w = o.topk_softmax(L, 9)
+    p = scipy.special.softmax(L, axis=1)
+    assert np.allclose(np.take_along_axis(p, ids.astype(np.int64), 1), w, rtol=0, atol=1e-15)
+    # without renormalisation the weights are the full softmax probabilities
+    ids3, w3 = o.topk_softmax(L, 3, renormalize=False)
+    assert np.allclose(np.take_along_axis(p, ids3.astype(np.int64), 1), w3, rtol=0, atol=1e-15)
+
+
+def check_topk_weight_invariants(o):
+    rng = _rng(3)
+    L = rng.standard_normal((200, 64)) * 2
+    for k in (1, 2, 8, 10):
+        ids, w = o.topk_softmax(L, k)
+        assert np.allclose(w.sum(1), 1.0, rtol=0, atol=1e-14), "renormalised weights must sum to 1"
+        assert (np.diff(w, axis=1) <= 1e-15).all(), "weights must be non-increasing in slot order"
+        assert (w > 0).all()
+        sel = np.take_along_axis(L, ids.astype(np.int64), 1)
+        assert (np.diff(sel, axis=1) <= 0).all(), "ids must be ordered by descending logit"
+
+
+def check_routing_brute_force(o):
+    rng = _rng(4)
+    for T, E, k in [(50, 6, 2), (17, 33, 4), (1, 4, 1), (64, 8, 8)]:
+        ids = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+        r = o.init_routing(ids, E)
+        flat = ids.reshape(-1)
+        R = T * k
+        want = sorted(range(R), key=lambda q: (flat[q], q))
+        assert list(r["sorted_rows"]) == want, "sorted_rows must be the stable sort by expert"
+        cnt = [int((flat == e).sum()) for e in range(E)]
+        assert list(r["counts"]) == cnt
+        assert r["offsets"][0] == 0 and r["offsets"][-1] == R
+        assert all(r["offsets"][e + 1] - r["offsets"][e] == cnt[e] for e in range(E))
+        assert np.array_equal(r["dest"][r["sorted_rows"]], np.arange(R)), "dest must invert sorted_rows"
+        for e in range(E):
+            seg = r["sorted_rows"][r["offsets"][e]:r["offsets"][e + 1]]
+            assert (flat[seg] == e).all()
+
+
+def check_permute_round_trip(o):
+    rng = _rng(5)
+    T, D, E, k = 40, 12, 7, 3
+    x = rng.standard_normal((T, D))
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(T)])
+    r = o.init_routing(ids, E)
+    xp = o.permute(x, r["sorted_rows"], k)
+    assert xp.shape == (T * k, D)
+    for t in range(T):
+        for j in range(k):
+            assert np.array_equal(xp[r["dest"][t * k + j]], x[t]), "un-permute(permute(x)) must be x"
+
+
+def check_swiglu_golden(o):
+    g = json.load(open(os.path.join(GOLDEN, "swiglu_chunk_example.json")))
+    for case in g["cases"]:
+        gu = np.array(case["gate_up"], dtype=np.float64)[None, :]
+        I = gu.shape[1] // 2
+        # an identity down projection exposes h itself
+        W13 = np.eye(2 * I)
+        W2 = np.eye(I)
+        h, y = o.expert_ffn(gu, W13, W2, o.ACT_SWIGLU)
+        assert np.allclose(h[0], case["h"], rtol=0, atol=1e-15), f"swiglu chunk example {case}"
+        assert np.allclose(y[0], case["h"], rtol=0, atol=1e-15)
+
+
+def check_activations_library(o):
+    g = np.linspace(-30, 30, 2001)
+    tg = torch.from_numpy(g)
+    assert np.allclose(o.activation(g, o.ACT_SWIGLU), F.silu(tg).numpy(), rtol=1e-14, atol=1e-300)
+    # 1 + tanh(.) cancels for very negative g: both sides are exact to ~1e-16 absolute there
+    assert np.allclose(o.activation(g, o.ACT_GEGLU_TANH), F.gelu(tg, approximate="tanh").numpy(),
+                       rtol=1e-13, atol=1e-14)
+
+
+def _dense_mlp_torch(x, W13, W2, act):
+    """Dense gated MLP with torch fp64: chunk(x W13, 2) -> act(first) * second -> W2."""
+    tx, t13, t2 = (torch.from_numpy(np.asarray(a, np.float64)) for a in (x, W13, W2))
+    gate, up = torch.chunk(tx @ t13, 2, dim=-1)
+    a = F.silu(gate) if act == "swiglu" else F.gelu(gate, approximate="tanh")
+    return ((a * up) @ t2).numpy()
+
+
+def check_single_expert_is_dense_mlp(o):
+    """E = 1, k = 1: the layer reduces to one dense gated MLP (weight 1)."""
+    rng = _rng(6)
+    T, D, I = 23, 16, 10
+    for act in (o.ACT_SWIGLU, o.ACT_GEGLU_TANH):
+        x = rng.standard_normal((T, D))
+        W13 = rng.standard_normal((1, D, 2 * I)) * 0.3
+        W2 = rng.standard_normal((1, I, D)) * 0.3
+        inp = {"x": x, "Wg": rng.standard_normal((D, 1)), "W13": W13, "W2": W2}
+        out = o.moe_layer(inp, 1, act)["out"]
+        ref = _dense_mlp_torch(x, W13[0], W2[0], act)
+        assert np.allclose(out, ref, rtol=1e-12, atol=1e-12), "E=1,k=1 must equal the dense MLP"
+
+
+def _tiny_layer(rng, T=19, D=12, E=6, k=3, I=5, Is=4, fp8=False):
+    x = rng.standard_normal((T, D))
+    inp = {
+        "x": x,
+        "Wg": rng.standard_normal((D, E)) * 0.5,
+        "logit_bias": rng.standard_normal(E) * 0.1,
+        "W13": rng.standard_normal((E, D, 2 * I)) * 0.3,
+        "W2": rng.standard_normal((E, I, D)) * 0.3,
+    }
+    if Is:
+        inp["W13s"] = rng.standard_normal((D, 2 * Is)) * 0.3
+        inp["W2s"] = rng.standard_normal((Is, D)) * 0.3
+    if fp8:
+        inp["s13"] = rng.uniform(0.5, 2.0, (E, 2 * I))
+        inp["s2"] = rng.uniform(0.5, 2.0, (E, D))
+        if Is:
+            inp["s13s"] = rng.uniform(0.5, 2.0, 2 * Is)
+            inp["s2s"] = rng.uniform(0.5, 2.0, D)
+    return inp
+
+
+def _brute_dense_layer(inp, k, act):
+    """Every expert on every token, then masked by the brute-force gates."""
+    x = np.asarray(inp["x"], np.float64)
+    E = inp["W13"].shape[0]
+    L = x @ inp["Wg"] + inp.get("logit_bias", 0.0)
+    ids, w = _brute_topk(L, k)
+    gates = np.zeros((x.shape[0], E))
+    for t in range(x.shape[0]):
+        for j in range(k):
+            gates[t, ids[t, j]] = w[t, j]
+
+    def w_eff(W, s):
+        return W if s is None else W * np.asarray(s)[None, :]
+
+    out = np.zeros_like(x)
+    for e in range(E):
+        W13 = w_eff(inp["W13"][e], None if inp.get("s13") is None else inp["s13"][e])
+        W2 = w_eff(inp["W2"][e], None if inp.get("s2") is None else inp["s2"][e])
+        out += gates[:, e:e + 1] * _dense_mlp_torch(x, W13, W2, act)
+    if inp.get("W13s") is not None:
+        out += _dense_mlp_torch(x, w_eff(inp["W13s"], inp.get("s13s")), w_eff(inp["W2s"], inp.get("s2s")), act)
+    return out
+
+
+def check_layer_vs_dense_then_mask(o):
+    rng = _rng(7)
+    for act in (o.ACT_SWIGLU, o.ACT_GEGLU_TANH):
+        for fp8 in (False, True):
+            for (E, k, Is) in [(6, 3, 4), (8, 1, 0), (5, 5, 3)]:
+                inp = _tiny_layer(rng, E=E, k=k, Is=Is, fp8=fp8)
+                out = o.moe_layer(inp, k, act)["out"]
+                ref = _brute_dense_layer(inp, k, act)
+                assert np.allclose(out, ref, rtol=1e-11, atol=1e-12), \
+                    f"layer != dense-then-mask (act={act}, fp8={fp8}, E={E}, k={k})"
+
+
+def check_identical_experts(o):
+    """All experts equal + renormalised gates: out = FFN(x) + shared(x) whatever the routing."""
+    rng = _rng(8)
+    inp = _tiny_layer(rng, T=31, E=7, k=3)
+    inp["W13"] = np.repeat(inp["W13"][:1], 7, axis=0)
+    inp["W2"] = np.repeat(inp["W2"][:1], 7, axis=0)
+    out = o.moe_layer(inp, 3, o.ACT_SWIGLU)["out"]
+    ref = _dense_mlp_torch(inp["x"], inp["W13"][0], inp["W2"][0], "swiglu") + \
+        _dense_mlp_torch(inp["x"], inp["W13s"], inp["W2s"], "swiglu")
+    assert np.allclose(out, ref, rtol=1e-11, atol=1e-12), "identical-experts invariant broken"
+
+
+def check_shared_only(o):
+    """Zero routed down projections leave exactly the shared expert's output."""
+    rng = _rng(9)
+    inp = _tiny_layer(rng)
+    inp["W2"] = np.zeros_like(inp["W2"])
+    out = o.moe_layer(inp, 3, o.ACT_SWIGLU)["out"]
+    ref = _dense_mlp_torch(inp["x"], inp["W13s"], inp["W2s"], "swiglu")
+    assert np.allclose(out, ref, rtol=1e-12, atol=1e-13), "shared expert must be added ungated"
+
+
+def check_fp8_scale_identity(o):
+    """(sum_k x q) * s[n] equals sum_k x (q * s[n]) for per-column scales."""
+    rng = _rng(10)
+    w = torch.from_numpy(rng.standard_normal((64, 48)) * 0.02).float()
+    q, s = workloads.quantize_fp8_per_column(w)
+    qf, sf = o.to_f64(q), o.to_f64(s)
+    x = rng.standard_normal((9, 64))
+    a = o.scaled_projection(x, qf, sf)
+    b = x @ (qf * sf[None, :])
+    assert np.allclose(a, b, rtol=1e-12, atol=1e-15), "per-channel scale must apply to output columns"
+    # and the dequantised weights approximate the fp32 weights to e4m3 precision
+    assert np.max(np.abs(qf * sf[None, :] - w.double().numpy())) <= 2 ** -4 * np.max(np.abs(w.numpy()))
+
+
+def check_subset_matches_full(o):
+    rng = _rng(11)
+    inp = _tiny_layer(rng, T=25)
+    full = o.moe_layer(inp, 3, o.ACT_SWIGLU)["out"]
+    tok = np.array([0, 7, 24, 3])
+    sub = o.moe_layer_tokens(inp, tok, 3, o.ACT_SWIGLU)
+    assert np.allclose(sub, full[tok], rtol=1e-13, atol=1e-14)
+
+
+def check_counts_sum(o):
+    rng = _rng(12)
+    inp = _tiny_layer(rng, T=33, E=6, k=4)
+    res = o.moe_layer(inp, 4, o.ACT_SWIGLU)
+    assert res["counts"].sum() == 33 * 4, "per-expert counts must sum to T*k"
+
+
+ALL_CHECKS = [
+    check_topk_brute_force, check_topk_all_equal, check_topk_full_softmax, check_topk_weight_invariants,
+    check_routing_brute_force, check_permute_round_trip, check_swiglu_golden, check_activations_library,
+    check_single_expert_is_dense_mlp, check_layer_vs_dense_then_mask, check_identical_experts,
+    check_shared_only, check_fp8_scale_identity, check_subset_matches_full, check_counts_sum,
+]

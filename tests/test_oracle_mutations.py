@@ -1,0 +1,103 @@
+"""Plant plausible mistakes in the CPU oracle and check that the pins catch
+each one.  Every mistake lives in the oracle, on the CPU."""
+import numpy as np
+import pytest
+
+import oracle.moe_oracle as o
+from tests import _pins
+
+_orig = {name: getattr(o, name) for name in
+         ("topk_softmax", "init_routing", "expert_ffn", "finalize", "activation",
+          "scaled_projection", "router_logits", "permute")}
+
+
+def _swap_gate_up(rows, W13_e, W2_e, act, s13_e=None, s2_e=None):
+    W13_e, W2_e = o.to_f64(W13_e), o.to_f64(W2_e)
+    I = W2_e.shape[0]
+    gu = o.scaled_projection(rows, W13_e, o.to_f64(s13_e))
+    h = o.activation(gu[:, I:], act) * gu[:, :I]
+    return h, o.scaled_projection(h, W2_e, o.to_f64(s2_e))
+
+
+def _ties_to_high_index(L, k, renormalize=True):
+    L = np.asarray(L, np.float64)
+    E = L.shape[1]
+    ids_rev, w = _orig["topk_softmax"](L[:, ::-1], k, renormalize)
+    return (E - 1 - ids_rev).astype(np.int32), w
+
+
+def _no_renormalize(L, k, renormalize=True):
+    return _orig["topk_softmax"](L, k, False)
+
+
+def _drop_shared(y_perm, dest, w, s=None):
+    return _orig["finalize"](y_perm, dest, w, None)
+
+
+def _unweighted_combine(y_perm, dest, w, s=None):
+    return _orig["finalize"](y_perm, dest, np.ones_like(np.asarray(w, np.float64)), s)
+
+
+def _scale_reversed_channels(A, W, scale):
+    return _orig["scaled_projection"](A, W, None if scale is None else scale[::-1])
+
+
+def _reverse_within_expert(ids, E):
+    r = _orig["init_routing"](ids, E)
+    flat = np.asarray(ids).reshape(-1)
+    R = flat.size
+    sr = np.array(sorted(range(R), key=lambda q: (flat[q], -q)), dtype=np.int64)
+    dest = np.empty(R, dtype=np.int64)
+    dest[sr] = np.arange(R)
+    r.update(sorted_rows=sr, dest=dest)
+    return r
+
+
+def _dest_not_inverted(ids, E):
+    r = _orig["init_routing"](ids, E)
+    r["dest"] = r["sorted_rows"].copy()
+    return r
+
+
+def _erf_gelu(g, act):
+    if act == o.ACT_GEGLU_TANH:
+        import scipy.special
+        return 0.5 * g * (1.0 + scipy.special.erf(g / np.sqrt(2.0)))
+    return _orig["activation"](g, act)
+
+
+def _bias_dropped(x, Wg, logit_bias=None):
+    return _orig["router_logits"](x, Wg, None)
+
+
+def _permute_off_by_one(x, sorted_rows, k):
+    xx = o.to_f64(x)
+    return xx[(np.asarray(sorted_rows) + 1) % (xx.shape[0] * k) // k]
+
+
+MUTATIONS = {
+    "gate_up_swapped": ("expert_ffn", _swap_gate_up),
+    "ties_to_high_index": ("topk_softmax", _ties_to_high_index),
+    "no_renormalize": ("topk_softmax", _no_renormalize),
+    "shared_dropped": ("finalize", _drop_shared),
+    "combine_unweighted": ("finalize", _unweighted_combine),
+    "scale_channel_order": ("scaled_projection", _scale_reversed_channels),
+    "unstable_within_expert": ("init_routing", _reverse_within_expert),
+    "dest_not_inverted": ("init_routing", _dest_not_inverted),
+    "erf_instead_of_tanh_gelu": ("activation", _erf_gelu),
+    "router_bias_dropped": ("router_logits", _bias_dropped),
+    "permute_off_by_one": ("permute", _permute_off_by_one),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_pins_catch_planted_mistake(name, monkeypatch):
+    fn_name, bad = MUTATIONS[name]
+    monkeypatch.setattr(o, fn_name, bad)
+    caught = []
+    for check in _pins.ALL_CHECKS:
+        try:
+            check(o)
+        except AssertionError:
+            caught.append(check.__name__)
+    assert caught, f"no pin caught the planted mistake {name}"
