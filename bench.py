@@ -1,0 +1,404 @@
+"""Benchmark of the GB300 MoE layer: one JSON line on rank 0.
+
+A step is one whole moe_layer call (router projection, top-k softmax,
+init_routing, permutation gather, grouped gate/up + activation, grouped down
+projection, shared expert when present, finalize) over one batch of T tokens
+already resident in HBM.  Default workload: the Qwen3-MoE-style prefill layer
+(T=4096, D=2048, E=128, top-8, I=768, bf16).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--impl ours|reference] [--no-cpu-baseline]
+
+Multi-GPU runs (torchrun, one rank per GPU) are independent replicas: the
+layer has no exchange step on one GPU's worth of tokens, so every rank runs
+its own batch (weak scaling) and only the timing uses a barrier and a max.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "MoE-layer tokens/s; % of HBM (decode) or tensor (prefill) roofline"
+PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
+PROFILES = os.path.join(ROOT, "profiles")
+KERNEL_SOURCES = [os.path.join(ROOT, "mixture_experts_layer_gating_gb300", "csrc", f)
+                  for f in ("gemm_sm103.cu", "sm103_ptx.cuh")]
+
+
+# ------------------------------------------------------------------ helpers
+def peaks():
+    try:
+        p = json.load(open(PEAKS_PATH))
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha1()
+    for f in KERNEL_SOURCES:
+        h.update(open(f, "rb").read())
+    return h.hexdigest()[:12]
+
+
+def profiled_traffic(kernel_tag: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    path = os.path.join(PROFILES, f"{kernel_tag}_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    txt = open(path).read()
+    m_hash = re.search(r"kernel_source_sha1:\s*([0-9a-f]+)", txt)
+    m_b = re.search(r"dram_bytes_per_launch_full_size:\s*([0-9.eE+]+)", txt)
+    if not m_hash or not m_b or m_hash.group(1) != kernel_source_hash():
+        return None
+    return float(m_b.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t_start = self.t_end = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.th = threading.Thread(target=self._read, daemon=True)
+            self.th.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, which):
+        if which == "start":
+            self.t_start = time.time()
+        else:
+            self.t_end = time.time()
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.lines:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"]}
+        inside = [l for (t, l) in self.lines if self.t_start and self.t_end and self.t_start <= t <= self.t_end + 0.15]
+        used = inside if inside else [l for (_, l) in self.lines]
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in used:
+            parts = [p.strip() for p in l.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                sm.append(float(parts[2]))
+                smax.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[6:10]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons),
+                "samples": len(sm),
+                "window": "timed region" if inside else "whole run (timed region shorter than the sampling period)"}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch.distributed as dist
+
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ oracle timing
+def time_oracle(shape, inp_cpu, n_tokens: int, seed: int = 1):
+    """The CPU oracle, as it stands, on the first n_tokens tokens of the batch."""
+    import oracle
+
+    sub = dict(inp_cpu)
+    sub["x"] = inp_cpu["x"][:n_tokens]
+    t0 = time.perf_counter()
+    oracle.moe_layer(sub, shape.k, shape.act, shape.renormalize)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(shape, inp_cpu, budget_s: float = 15.0):
+    """Time the oracle on a bounded token sample sized to about budget_s."""
+    n = min(shape.T, 64)
+    dt = time_oracle(shape, inp_cpu, n)
+    if dt < budget_s / 4 and n < shape.T:
+        n2 = int(min(shape.T, max(n + 1, n * budget_s / 2 / max(dt, 1e-3))))
+        dt = time_oracle(shape, inp_cpu, n2)
+        n = n2
+    return {"value": n / dt, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"first {n} of {shape.T} tokens of {shape.name}, one oracle.moe_layer call "
+                      f"(numpy fp64, per-expert loop, BLAS threads = host cores), {dt:.1f} s"}
+
+
+# ------------------------------------------------------------------ arms
+def run_reference(args, world, rank):
+    shape = workloads.CONFIGS[args.workload]
+    if rank != 0:
+        return
+    inp = workloads.make_inputs(shape, seed=0, device="cpu") if not torch.cuda.is_available() else \
+        {k: (v.cpu() if isinstance(v, torch.Tensor) else v)
+         for k, v in workloads.make_inputs(shape, seed=0, device="cuda").items()}
+    # each step: the oracle on a bounded sample so the whole run stays within minutes
+    n = min(shape.T, args.ref_tokens)
+    for _ in range(args.warmup):
+        time_oracle(shape, inp, n)
+    times = [time_oracle(shape, inp, n) for _ in range(args.steps)]
+    tot = sum(times)
+    value = n * args.steps / tot
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded Gaussian inputs of the workload's shapes)",
+        "config": dict(workloads.config_summary(shape), sample_tokens_per_step=n),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": f"first {n} of {shape.T} tokens per step"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, world, rank, local):
+    import mixture_experts_layer_gating_gb300 as moe
+    from mixture_experts_layer_gating_gb300 import _build
+
+    if rank == 0 or not os.path.exists(moe.LIB_PATH):
+        _build.build()
+    barrier(world)
+    moe.load_library()
+    shape = workloads.CONFIGS[args.workload]
+    dev = torch.device("cuda", local)
+    inp = workloads.make_inputs(shape, seed=rank, device=dev, weights_seed=0)
+    cfg = moe.config_from_shape(shape)
+    ws = moe.alloc_workspace(cfg, device=dev)
+    out = torch.empty((shape.T, shape.D), dtype=workloads.torch_dtype(shape.act_dtype), device=dev)
+    stream = torch.cuda.current_stream(dev)
+    args_layer = (inp["x"], inp["Wg"], inp["logit_bias"], inp["W13"], inp["s13"], inp["W2"], inp["s2"],
+                  inp["W13s"], inp["s13s"], inp["W2s"], inp["s2s"])
+
+    def step(x=None):
+        a = list(args_layer)
+        if x is not None:
+            a[0] = x
+        moe.moe_layer(cfg, *a, out, ws, stream)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    flags = moe.moe_read_device_status(ws)
+    if flags:
+        raise RuntimeError(f"device error flags {flags:#x}")
+
+    # ---- device-resident timed region
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler.mark("start")
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    sampler.mark("end")
+    barrier(world)
+    t_ms = ev0.elapsed_time(ev1)
+    t_ms = max_over_ranks(t_ms, world)
+    ms_step = t_ms / args.steps
+    value = shape.T * world / (t_ms / 1e3 / args.steps)
+
+    # ---- per-kernel durations (instrumented pass, same work, after the timed region)
+    L = moe.moe_layer_launch_count(cfg)
+    names = ["router_gemm", "topk_softmax", "route_hist", "route_scan", "route_scatter",
+             "permute_gather", "w13_gate_up", "w2_down"]
+    if shape.I_shared:
+        names += ["shared_w13", "shared_w2"]
+    names += ["finalize"]
+    assert len(names) == L
+    per = [[] for _ in range(L)]
+    for _ in range(args.steps):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(L + 1)]
+        moe.moe_set_trace_events(evs)
+        step()
+        moe.moe_set_trace_events(None)
+        torch.cuda.synchronize()
+        for i in range(L):
+            per[i].append(evs[i].elapsed_time(evs[i + 1]))
+    kernels_us = {n: 1e3 * statistics.mean(v) for n, v in zip(names, per)}
+
+    # ---- end to end through the public API with host buffers
+    x_host = inp["x"].cpu().pin_memory()
+    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    x_dev = torch.empty_like(inp["x"])
+    for _ in range(2):
+        x_dev.copy_(x_host, non_blocking=True)
+        step(x_dev)
+        out_host.copy_(out, non_blocking=True)
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        x_dev.copy_(x_host, non_blocking=True)
+        step(x_dev)
+        out_host.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    sampler.stop()
+
+    # ---- roofline of the dominant kernel
+    counts = moe.workspace_view(ws, cfg, "counts", (shape.E,), torch.int32).cpu()
+    active = int((counts > 0).sum())
+    pk = peaks()
+    R, D, I = shape.R, shape.D, shape.I
+    wb = {"f32": 4, "bf16": 2, "fp8_e4m3": 1}[shape.w_dtype]
+    ab = 4 if shape.act_dtype == "f32" else 2
+    w13_flops = 2.0 * R * D * 2 * I
+    w13_bytes = active * D * 2 * I * wb + R * D * ab + R * I * ab
+    w2_flops = 2.0 * R * I * D
+    w2_bytes = active * I * D * wb + R * I * ab + R * D * ab
+    cand = {"w13_gate_up": (w13_flops, w13_bytes), "w2_down": (w2_flops, w2_bytes)}
+    dom = max(cand, key=lambda n: kernels_us[n])
+    flops, nbytes = cand[dom]
+    t_s = kernels_us[dom] / 1e6
+    t_tensor = flops / (pk["bf16_tflops"] * 1e12)
+    t_hbm = nbytes / (pk["hbm_gbs"] * 1e9)
+    if t_tensor >= t_hbm:
+        roof = {"bound": "tensor", "achieved": flops / t_s / 1e12, "peak": pk["bf16_tflops"], "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": nbytes / t_s / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    tr = profiled_traffic(dom, args.workload)
+    roof.update({"traffic": tr, "kernel": dom, "kernel_us": kernels_us[dom],
+                 "algorithmic_flops": flops, "algorithmic_bytes": nbytes,
+                 "tensor_frac": (flops / t_s / 1e12) / pk["bf16_tflops"],
+                 "hbm_frac": (nbytes / t_s / 1e9) / pk["hbm_gbs"],
+                 "peak_source": f"{pk['source']} (MEASURED_PEAKS.json burst figures)"})
+    layer_flops = workloads.layer_flops(shape)
+    layer_bytes = workloads.layer_bytes(shape, active_experts=active)
+    t_roof = max(layer_flops / (pk["bf16_tflops"] * 1e12), layer_bytes / (pk["hbm_gbs"] * 1e9))
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if shape.act_dtype == "bf16" else "f32",
+        "data": "synthetic (seeded Gaussian x ~ N(0,1), weights ~ N(0,0.02), random init)",
+        "config": dict(workloads.config_summary(shape), parallelism=f"replicas x{world}",
+                       l2="inputs larger than L2: %.2f GB of expert weights per step" %
+                          (shape.E * workloads.expert_weight_bytes(shape.D, shape.I, shape.w_dtype) / 1e9),
+                       active_experts=active),
+        "roofline": roof,
+        "layer_roofline": {"t_roofline_us": t_roof * 1e6, "t_measured_us": ms_step * 1e3,
+                           "frac": t_roof / (ms_step / 1e3), "flops": layer_flops, "bytes": layer_bytes},
+        "kernels_us": kernels_us,
+        "e2e": {"value": shape.T * world / (e2e_ms / 1e3 / args.steps), "unit": "tokens/s",
+                "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
+                "d2h_bytes_per_step": out_host.numel() * out_host.element_size()},
+        "gpu_launches": L * args.steps,
+        "clocks": sampler.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu_inp = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+        line["cpu_baseline"] = cpu_baseline(shape, cpu_inp, budget_s=args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="qwen3_prefill", choices=sorted(workloads.CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--ref-tokens", type=int, default=64)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

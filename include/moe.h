@@ -1,0 +1,209 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) sparse Mixture-of-Experts FFN layer.
+ *
+ * The layer, as the source pages state it:
+ *   logits = x W_g                                   (router projection)
+ *   (ids, w) = top-k of softmax(logits), renormalised (gating_top_k_softmax)
+ *   rows grouped by expert                            (init_routing)
+ *   h_e = act(x W13_e[:, :I]) * (x W13_e[:, I:])      (grouped matmul + swiglu)
+ *   y_e = h_e W2_e                                    (grouped matmul)
+ *   out = sum_j w_j y_{ids_j} + SharedExpert(x)       (finalize_routing)
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - All tensors are device pointers, row-major and contiguous, owned by the
+ *   caller.  The library allocates no device memory; scratch space comes from
+ *   the caller's workspace `ws` of at least moe_workspace_size(cfg) bytes
+ *   (256-byte aligned).  The first 256 bytes of `ws` are a control block that
+ *   holds the device error word.
+ * - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call is
+ *   asynchronous on that stream and returns after enqueueing its kernels.
+ * - Return value: MOE_OK or a negative moe_status_t.  Argument errors are
+ *   detected on the host before anything is enqueued.  Data errors found on
+ *   the device (an expert id outside [0, E), non-monotone offsets, a permuted
+ *   position outside [0, T*k), non-finite router logits) never fault: the
+ *   offending element is skipped or clamped and a code is recorded in the
+ *   device error word, which moe_read_device_status() reads.
+ * - Pointers must be 16-byte aligned and every row pitch a multiple of 16
+ *   bytes, which makes D, I and I_shared multiples of 8 (16 for fp8 weights).
+ * - Dtypes: act_dtype applies to x, W_g, the permuted rows, h, the expert
+ *   outputs, the shared-expert output and out.  w_dtype applies to W13, W2 and
+ *   the shared expert's weights.  Supported pairs: (F32, F32), (BF16, BF16),
+ *   (BF16, FP8_E4M3).  Router logits and gate weights are always fp32.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_FP8_E4M3 = 2 } moe_dtype_t;
+
+/* SwiGLU: SiLU(gate) * up.  GEGLU: tanh-approximated GELU(gate) * up. */
+typedef enum { MOE_ACT_SWIGLU = 0, MOE_ACT_GEGLU_TANH = 1 } moe_act_t;
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = -1,  /* null pointer, bad shape, misalignment, k > E, E > 512 */
+  MOE_ERR_UNSUPPORTED = -2,  /* dtype / activation combination not built */
+  MOE_ERR_CUDA = -3,         /* a CUDA runtime or driver call failed */
+  MOE_ERR_DEVICE_CHECK = -4, /* the device error word is set (see moe_read_device_status) */
+  MOE_ERR_WORKSPACE = -5     /* workspace missing, misaligned or too small */
+} moe_status_t;
+
+/* Codes stored in the device error word (bit flags, OR-ed together). */
+#define MOE_DEV_BAD_EXPERT_ID 0x1   /* an id outside [0, E) reached routing */
+#define MOE_DEV_BAD_OFFSETS 0x2     /* offsets not monotone or beyond T*k */
+#define MOE_DEV_BAD_DEST 0x4        /* a permuted position outside [0, T*k) */
+#define MOE_DEV_NONFINITE_LOGIT 0x8 /* NaN / Inf router logit (treated as -Inf) */
+#define MOE_DEV_WAIT_TIMEOUT 0x10   /* a bounded pipeline wait gave up */
+
+typedef struct {
+  int32_t T;           /* tokens */
+  int32_t D;           /* hidden size */
+  int32_t E;           /* routed experts, 1..512 */
+  int32_t k;           /* experts per token, 1..min(E, 16) */
+  int32_t I;           /* routed expert intermediate size */
+  int32_t I_shared;    /* shared expert / dense MLP intermediate, 0 = none */
+  int32_t act;         /* moe_act_t */
+  int32_t act_dtype;   /* moe_dtype_t: MOE_F32 or MOE_BF16 */
+  int32_t w_dtype;     /* moe_dtype_t: MOE_F32, MOE_BF16 or MOE_FP8_E4M3 */
+  int32_t renormalize; /* 1: gate weights renormalised over the k chosen experts */
+} moe_config_t;
+
+/* Bytes of workspace that every call below accepts for this configuration
+ * (moe_layer needs all of it; the stage calls use the control block and
+ * their own scratch).  Returns 0 for an invalid configuration. */
+size_t moe_workspace_size(const moe_config_t* cfg);
+
+/* Router projection and gating_top_k_softmax.
+ * Pages: "千问 3.5 MoE 在 TPU 上的系统优化实战" (routed MoE paragraph: the
+ * router projects each token and picks the top 10 experts by softmax);
+ * "CANN/cann-recipes-infer：Qwen3-MoE优化", section "GMM使能和Routing优化"
+ * (npu_moe_gating_top_k_softmax fuses top-k and softmax) and section
+ * "融合RMSNorm + Cast" (the gate is computed in fp32).
+ *   x          [T, D] act_dtype, or NULL: then `logits` is an input.
+ *   Wg         [D, E] act_dtype (ignored when x is NULL).
+ *   logit_bias [E] fp32 or NULL, added to x W_g (must be NULL when x is NULL).
+ *   logits     [T, E] fp32: x W_g + bias with fp32 accumulation (output), or
+ *              the input logits when x is NULL.
+ *   topk_ids   [T, k] int32 out: experts by descending logit, the lower index
+ *              first among equal logits.
+ *   topk_w     [T, k] fp32 out: softmax over the k chosen logits when
+ *              cfg->renormalize, else the full-softmax probabilities. */
+int moe_route(const moe_config_t* cfg, const void* x, const void* Wg, const float* logit_bias,
+              float* logits, int32_t* topk_ids, float* topk_w, void* ws, size_t ws_bytes,
+              void* stream);
+
+/* init_routing + compute_expert_tokens + the permutation gather.
+ * Pages: "CANN/cann-recipes-infer：Qwen3-MoE优化", section "GMM使能和Routing优化"
+ * (npu_moe_init_routing orders rows by expert; npu_moe_compute_expert_tokens
+ * counts tokens per expert); "千问 3.5 MoE 在 TPU 上的系统优化实战", SparseCore
+ * paragraph (gather rows by routing index into one contiguous unpadded buffer).
+ * Expanded row r = t*k + j is token t's j-th choice.
+ *   topk_ids    [T, k] int32 in.
+ *   x           [T, D] act_dtype in (may be NULL: no gather, x_perm unused).
+ *   counts      [E] int32 out: rows per expert.
+ *   offsets     [E+1] int32 out: exclusive scan of counts; offsets[E] = T*k.
+ *   sorted_rows [T*k] int32 out: expanded row at each permuted position,
+ *               grouped by expert, ascending r inside an expert (stable).
+ *   dest        [T*k] int32 out: permuted position of each expanded row
+ *               (inverse of sorted_rows; -1 for a row with an invalid id).
+ *   x_perm      [T*k, D] act_dtype out: x_perm[p] = x[sorted_rows[p] / k]. */
+int moe_permute(const moe_config_t* cfg, const int32_t* topk_ids, const void* x, int32_t* counts,
+                int32_t* offsets, int32_t* sorted_rows, int32_t* dest, void* x_perm, void* ws,
+                size_t ws_bytes, void* stream);
+
+/* Grouped matmul over expert segments, with the gate/up activation epilogue,
+ * plus the shared expert (or dense MLP) over all tokens.
+ * Pages: "CANN/cann-recipes-infer：Qwen3-MoE优化", sections "MoE TP优化 /
+ * 计算分解" (w13 = [gate | up], swiglu = SiLU(first half) * second half) and
+ * "GMM使能和Routing优化" (npu_grouped_matmul); "Gemma-4 模型优化报告" §2
+ * (GEGLU experts; dense MLP added to the MoE output); "用SGLang-JAX在TPU上优化
+ * Ling-2.6-1T" §5 "逐通道 direct_scaled_dot" (per-output-channel fp8 scale
+ * applied after the K reduction).
+ *   x_perm  [T*k, D] act_dtype: expert-ordered rows.
+ *   offsets [E+1] int32: segment bounds (from moe_permute).
+ *   W13     [E, D, 2I] w_dtype: columns [0, I) gate, [I, 2I) up.
+ *   s13     [E, 2I] fp32 per-column scales (fp8 only, else NULL).
+ *   W2      [E, I, D] w_dtype;   s2 [E, D] fp32 (fp8 only, else NULL).
+ *   h       [T*k, I] act_dtype out: act(gate) * up.
+ *   y_perm  [T*k, D] act_dtype out: h W2 per segment.
+ *   x, W13s [D, 2*I_shared], s13s [2*I_shared], W2s [I_shared, D], s2s [D]:
+ *           the shared expert; x NULL (or I_shared == 0) skips it.
+ *   h_s     [T, I_shared] act_dtype out (shared intermediate).
+ *   s_out   [T, D] act_dtype out: shared expert output. */
+int moe_grouped_ffn(const moe_config_t* cfg, const void* x_perm, const int32_t* offsets,
+                    const void* W13, const float* s13, const void* W2, const float* s2, void* h,
+                    void* y_perm, const void* x, const void* W13s, const float* s13s,
+                    const void* W2s, const float* s2s, void* h_s, void* s_out, void* ws,
+                    size_t ws_bytes, void* stream);
+
+/* finalize_routing fused with the shared-expert add.
+ * Pages: "CANN/cann-recipes-infer：Qwen3-MoE优化", section "GMM使能和Routing优化"
+ * (npu_moe_finalize_routing restores token order and takes the weighted sum);
+ * "千问 3.5 MoE 在 TPU 上的系统优化实战": y = Router(x) + SharedExpert(x).
+ *   out[t] = round( sum_{j<k} w[t, j] * y_perm[dest[t*k + j]] + s[t] ),
+ *   accumulated in fp32 with j ascending, the shared row added last, one
+ *   rounding to act_dtype.
+ *   y_perm [T*k, D], dest [T*k] int32, topk_w [T, k] fp32,
+ *   s [T, D] act_dtype or NULL, out [T, D] act_dtype. */
+int moe_finalize(const moe_config_t* cfg, const void* y_perm, const int32_t* dest,
+                 const float* topk_w, const void* s, void* out, void* ws, size_t ws_bytes,
+                 void* stream);
+
+/* The whole layer: moe_route, moe_permute, moe_grouped_ffn, moe_finalize on
+ * one stream, with every intermediate carved from `ws`.  Arguments as above;
+ * the shared-expert weights may be NULL when cfg->I_shared == 0. */
+int moe_layer(const moe_config_t* cfg, const void* x, const void* Wg, const float* logit_bias,
+              const void* W13, const float* s13, const void* W2, const float* s2,
+              const void* W13s, const float* s13s, const void* W2s, const float* s2s, void* out,
+              void* ws, size_t ws_bytes, void* stream);
+
+/* Device byte offsets inside `ws` where moe_layer keeps its intermediates,
+ * for inspection (logits, ids, weights, counts, offsets, sorted_rows, dest,
+ * x_perm, h, y_perm, h_s, s).  `which` is one of the MOE_WS_* indices;
+ * returns (size_t)-1 for an unknown index or an invalid configuration. */
+#define MOE_WS_LOGITS 0
+#define MOE_WS_TOPK_IDS 1
+#define MOE_WS_TOPK_W 2
+#define MOE_WS_COUNTS 3
+#define MOE_WS_OFFSETS 4
+#define MOE_WS_SORTED_ROWS 5
+#define MOE_WS_DEST 6
+#define MOE_WS_X_PERM 7
+#define MOE_WS_H 8
+#define MOE_WS_Y_PERM 9
+#define MOE_WS_H_SHARED 10
+#define MOE_WS_S 11
+size_t moe_workspace_offset(const moe_config_t* cfg, int which);
+
+/* Synchronises `stream`, reads and clears the device error word of `ws`.
+ * Returns MOE_OK, MOE_ERR_DEVICE_CHECK (flags written to *flags when not
+ * NULL) or MOE_ERR_CUDA. */
+int moe_read_device_status(void* ws, void* stream, int32_t* flags);
+
+/* Human-readable text of a moe_status_t. */
+const char* moe_status_string(int status);
+
+/* Kernel launches one moe_layer call enqueues for this configuration. */
+int moe_layer_launch_count(const moe_config_t* cfg);
+
+/* Per-kernel timing hook (process-wide, off by default).  `events` holds
+ * n_events cudaEvent_t handles created by the caller; while set, each
+ * moe_layer call records events[i] on its stream right before its i-th kernel
+ * launch and events[L] after the last one (L = moe_layer_launch_count), so
+ * consecutive events bracket exactly one kernel.  Calls with fewer than L+1
+ * events record nothing.  Pass NULL / 0 to switch it off.  Not thread-safe:
+ * set it from the thread that calls moe_layer.  Returns MOE_OK. */
+int moe_set_trace_events(void* const* events, int n_events);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

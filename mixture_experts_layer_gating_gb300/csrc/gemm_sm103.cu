@@ -1,0 +1,539 @@
+// Grouped GEMM over variable-length expert segments on the sm_103a tensor
+// core (tcgen05 + TMEM), fed by TMA.
+//
+// What it computes (per group g with rows [start_g, start_g + cnt_g) of A):
+//   gate/up pass : acc = A_g [gate | up]; out = act(gate * s) * (up * s)
+//   store pass   : out = (A_g B_g) * s              (bf16 out)
+//   router pass  : out = A B + bias                 (fp32 out, one group)
+// This is the grouped matmul of "CANN/cann-recipes-infer：Qwen3-MoE优化"
+// (section "GMM使能和Routing优化": one op computes every expert instead of a
+// per-expert loop), with the swiglu of section "MoE TP优化 / 计算分解" fused
+// into the epilogue of the gate/up pass (the "千问 3.5 MoE 在 TPU 上的系统优化
+// 实战" page fuses SwiGLU into the GMM main loop the same way) and the
+// per-output-channel fp8 scale of "用SGLang-JAX在TPU上优化Ling-2.6-1T" §5
+// applied after the full K reduction.  Segments are unpadded: a tile that runs
+// past its segment computes rows of the next segment and masks their stores
+// (the Qwen3.5 page's dynamic bounded slices with minimal padding).
+//
+// Kernel structure (one persistent CTA per SM, 192 threads):
+//   warp 0      : TMA producer (one lane) -- A tile 128 x 64 (K-major) and
+//                 B tile 64 x 256 (N-major) per stage, 4-stage mbarrier ring.
+//   warp 1      : TMEM allocator + single-lane tcgen05.mma issuer,
+//                 M=128 N=256 K=16 per instruction, fp32 accumulators in TMEM,
+//                 two accumulator buffers (2 x 256 columns).
+//   warps 2..5  : epilogue -- tcgen05.ld 32 lanes x 32 columns, activation /
+//                 scale, masked bf16 or fp32 stores; one row per thread.
+// Tiles are ordered (group, column tile, row tile) so that the row tiles that
+// share a weight slice run at the same time and reuse it from L2.  The tile
+// schedule is built on the device from the group offsets, so no host
+// synchronisation is needed between routing and the GEMM.
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "moe_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int BN_MAX = 256;
+constexpr int STAGES = 4;
+constexpr int A_TILE_BYTES = BM * BK * 2;    // 16 KB
+constexpr int B_BOX_BYTES = 64 * BK * 2;     // one 64-column x 64-row bf16 box, 8 KB
+constexpr int B_TILE_BYTES = BN_MAX * BK * 2; // 32 KB
+constexpr int MAX_G = 512;
+constexpr int THREADS = 192;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t ACC_STRIDE = 256;  // TMEM columns per accumulator buffer
+
+struct Ctrl {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint32_t tmem_slot;
+  int abort;
+  int grp_start[MAX_G];
+  int grp_cnt[MAX_G];
+  int tile_start[MAX_G + 1];
+};
+
+constexpr size_t SMEM_BYTES = 1024 + STAGES * (A_TILE_BYTES + B_TILE_BYTES) + sizeof(Ctrl);
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+
+struct KParams {
+  const int32_t* group_offsets;
+  int G;
+  int M;
+  int K;
+  int N;              // output columns
+  int n_tiles;        // column tiles
+  int bn;             // MMA N (accumulator columns per tile)
+  int cols_per_tile;  // output columns per tile
+  void* out;
+  const float* b_scale;
+  const float* bias;
+  int act;
+  int32_t* err;
+};
+
+struct TileInfo {
+  int g, row0, rows, n0;
+};
+
+__device__ __forceinline__ TileInfo decode_tile(const Ctrl* c, int G, int t, int n_tiles,
+                                                int cols_per_tile) {
+  const int q = t / n_tiles;
+  int lo = 0, hi = G - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (c->tile_start[mid] <= q) lo = mid; else hi = mid - 1;
+  }
+  TileInfo ti;
+  ti.g = lo;
+  const int mt_g = c->tile_start[lo + 1] - c->tile_start[lo];
+  const int local = t - c->tile_start[lo] * n_tiles;
+  const int nt = local / mt_g;
+  const int mt = local - nt * mt_g;
+  ti.row0 = c->grp_start[lo] + mt * BM;
+  ti.rows = min(BM, c->grp_cnt[lo] - mt * BM);
+  ti.n0 = nt * cols_per_tile;
+  return ti;
+}
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
+__device__ __forceinline__ float gelu_tanh_f(float g) {
+  const float c = 0.7978845608028654f;  // sqrt(2/pi)
+  return 0.5f * g * (1.0f + tanhf(c * (g + 0.044715f * g * g * g)));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(THREADS, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                        const __grid_constant__ CUtensorMap tmap_b, const KParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sa = base;
+  uint8_t* sb = base + STAGES * A_TILE_BYTES;
+  Ctrl* ctrl = reinterpret_cast<Ctrl*>(sb + STAGES * B_TILE_BYTES);
+  volatile int* abort_flag = &ctrl->abort;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int G = p.G;
+
+  // ---------------------------------------------------------------- set-up
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&ctrl->full[s], 1);
+      mbar_init(&ctrl->empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&ctrl->tfull[a], 1);
+      mbar_init(&ctrl->tempty[a], 128);
+    }
+    ctrl->abort = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmap_a);
+    tma_prefetch_desc(&tmap_b);
+  }
+  if (warp == 1) {
+    tmem_alloc(&ctrl->tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == 2) {
+    // Row-tile schedule: tile_start[g] = sum_{g' < g} ceil(cnt_g' / BM).
+    const int per = (G + 31) / 32;
+    const int g0 = min(G, lane * per), g1 = min(G, g0 + per);
+    int local = 0;
+    bool bad = false;
+    for (int g = g0; g < g1; ++g) {
+      int a, b;
+      if (p.group_offsets) {
+        a = p.group_offsets[g];
+        b = p.group_offsets[g + 1];
+      } else {
+        a = 0;
+        b = p.M;
+      }
+      if (a < 0 || b < a || b > p.M) {
+        bad = true;
+        a = 0;
+        b = 0;
+      }
+      ctrl->grp_start[g] = a;
+      ctrl->grp_cnt[g] = b - a;
+      local += (b - a + BM - 1) / BM;
+    }
+    int incl = local;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += v;
+    }
+    int run = incl - local;
+    for (int g = g0; g < g1; ++g) {
+      ctrl->tile_start[g] = run;
+      run += (ctrl->grp_cnt[g] + BM - 1) / BM;
+    }
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    if (lane == 0) ctrl->tile_start[G] = total;
+    if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.err, MOE_DEV_BAD_OFFSETS);
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+
+  const uint32_t tmem_base = ctrl->tmem_slot;
+  const int total_tiles = ctrl->tile_start[G] * p.n_tiles;
+  const int KB = (p.K + BK - 1) / BK;
+  const int nbox = p.bn / 64;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol = l2_policy_evict_normal();
+      const uint32_t tx = A_TILE_BYTES + nbox * B_BOX_BYTES;
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+        const TileInfo ti = decode_tile(ctrl, G, t, p.n_tiles, p.cols_per_tile);
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(&ctrl->empty[stage], phase ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&ctrl->full[stage], tx);
+          uint8_t* a_dst = sa + stage * A_TILE_BYTES;
+          uint8_t* b_dst = sb + stage * B_TILE_BYTES;
+          tma_load_2d(a_dst, &tmap_a, &ctrl->full[stage], kb * BK, ti.row0, pol);
+          if (EPI == kEpiGateUpAct) {
+            // gate columns n0..n0+127 into boxes 0,1; up columns into boxes 2,3
+            for (int j = 0; j < 2; ++j) {
+              tma_load_4d(b_dst + j * B_BOX_BYTES, &tmap_b, &ctrl->full[stage], ti.n0 + 64 * j, 0,
+                          kb * BK, ti.g, pol);
+              tma_load_4d(b_dst + (2 + j) * B_BOX_BYTES, &tmap_b, &ctrl->full[stage],
+                          ti.n0 + 64 * j, 1, kb * BK, ti.g, pol);
+            }
+          } else {
+            for (int j = 0; j < nbox; ++j)
+              tma_load_3d(b_dst + j * B_BOX_BYTES, &tmap_b, &ctrl->full[stage], ti.n0 + 64 * j,
+                          kb * BK, ti.g, pol);
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        ctrl->abort = 1;
+        atomicOr(p.err, MOE_DEV_WAIT_TIMEOUT);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = make_idesc_bf16_f32(BM, p.bn, 0, 1);
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+        if (!mbar_wait(&ctrl->tempty[acc], acc_phase ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + acc * ACC_STRIDE;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(&ctrl->full[stage], phase, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t a_addr = smem_u32(sa + stage * A_TILE_BYTES);
+          const uint32_t b_addr = smem_u32(sb + stage * B_TILE_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            // A: K-major, 128-byte rows; a K step of 16 bf16 is 32 bytes.
+            const uint64_t adesc = make_smem_desc_sw128(a_addr + kk * 32, 16, 1024);
+            // B: N-major, 64-column boxes 8 KB apart; a K step of 16 rows is 2 KB.
+            const uint64_t bdesc = make_smem_desc_sw128(b_addr + kk * 2048, B_BOX_BYTES, 1024);
+            tc_mma_f16(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0);
+          }
+          tc_commit(&ctrl->empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(&ctrl->tfull[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      if (!ok) {
+        ctrl->abort = 1;
+        atomicOr(p.err, MOE_DEV_WAIT_TIMEOUT);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;  // TMEM lanes [32*quarter, 32*quarter + 32)
+    const int row_in_tile = quarter * 32 + lane;
+    uint32_t acc = 0, acc_phase = 0;
+    for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
+      const TileInfo ti = decode_tile(ctrl, G, t, p.n_tiles, p.cols_per_tile);
+      if (!mbar_wait(&ctrl->tfull[acc], acc_phase, abort_flag)) {
+        if (lane == 0) {
+          ctrl->abort = 1;
+          atomicOr(p.err, MOE_DEV_WAIT_TIMEOUT);
+        }
+        break;
+      }
+      __syncwarp();
+      tc_fence_after_sync();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * ACC_STRIDE;
+      const bool valid = row_in_tile < ti.rows;
+      const size_t out_row = static_cast<size_t>(ti.row0 + row_in_tile);
+
+      if (EPI == kEpiGateUpAct) {
+        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
+        const float* sg = p.b_scale ? p.b_scale + static_cast<size_t>(ti.g) * 2 * p.N : nullptr;
+#pragma unroll 1
+        for (int c = 0; c < 128; c += 32) {
+          uint32_t gr[32], ur[32];
+          tmem_ld_32x32b_x32(taddr + c, gr);
+          tmem_ld_32x32b_x32(taddr + 128 + c, ur);
+          tc_wait_ld();
+          const int col = ti.n0 + c;
+          if (valid) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              const int cc = col + 8 * v;
+              if (cc < p.N) {
+                uint32_t packed[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  float hv[2];
+#pragma unroll
+                  for (int h2 = 0; h2 < 2; ++h2) {
+                    const int idx = 8 * v + 2 * i + h2;
+                    float g = __uint_as_float(gr[idx]);
+                    float u = __uint_as_float(ur[idx]);
+                    if (sg) {
+                      g *= sg[cc + 2 * i + h2];
+                      u *= sg[p.N + cc + 2 * i + h2];
+                    }
+                    const float a = (p.act == MOE_ACT_SWIGLU) ? silu_f(g) : gelu_tanh_f(g);
+                    hv[h2] = a * u;
+                  }
+                  packed[i] = pack_bf16x2(hv[0], hv[1]);
+                }
+                *reinterpret_cast<uint4*>(out + out_row * p.N + cc) =
+                    make_uint4(packed[0], packed[1], packed[2], packed[3]);
+              }
+            }
+          }
+        }
+      } else if (EPI == kEpiStoreBf16) {
+        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
+        const float* sc = p.b_scale ? p.b_scale + static_cast<size_t>(ti.g) * p.N : nullptr;
+#pragma unroll 1
+        for (int c = 0; c < p.bn; c += 32) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(taddr + c, r);
+          tc_wait_ld();
+          const int col = ti.n0 + c;
+          if (valid) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              const int cc = col + 8 * v;
+              if (cc < p.N) {
+                uint32_t packed[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  float a = __uint_as_float(r[8 * v + 2 * i]);
+                  float b = __uint_as_float(r[8 * v + 2 * i + 1]);
+                  if (sc) {
+                    a *= sc[cc + 2 * i];
+                    b *= sc[cc + 2 * i + 1];
+                  }
+                  packed[i] = pack_bf16x2(a, b);
+                }
+                *reinterpret_cast<uint4*>(out + out_row * p.N + cc) =
+                    make_uint4(packed[0], packed[1], packed[2], packed[3]);
+              }
+            }
+          }
+        }
+      } else {  // kEpiStoreF32
+        float* out = reinterpret_cast<float*>(p.out);
+#pragma unroll 1
+        for (int c = 0; c < p.bn; c += 32) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(taddr + c, r);
+          tc_wait_ld();
+          const int col = ti.n0 + c;
+          if (valid) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const int cc = col + i;
+              if (cc < p.N) {
+                float v = __uint_as_float(r[i]);
+                if (p.bias) v += p.bias[cc];
+                out[out_row * p.N + cc] = v;
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before_sync();
+      mbar_arrive(&ctrl->tempty[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+    __syncwarp();
+  }
+
+  // ---------------------------------------------------------------- teardown
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+bool encode_tmap(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims,
+                 const uint64_t* strides_bytes, const uint32_t* box) {
+  auto fn = get_encode_fn();
+  if (!fn) return false;
+  cuuint64_t gd[5];
+  cuuint64_t gs[4];
+  cuuint32_t bx[5];
+  cuuint32_t es[5];
+  for (int i = 0; i < rank; ++i) {
+    gd[i] = dims[i];
+    bx[i] = box[i];
+    es[i] = 1;
+  }
+  for (int i = 0; i < rank - 1; ++i) gs[i] = strides_bytes[i];
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), gd, gs, bx, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int EPI>
+cudaError_t launch_epi(const CUtensorMap& ta, const CUtensorMap& tb, const KParams& kp, int grid,
+                       cudaStream_t s) {
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(grouped_gemm_kernel<EPI>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(SMEM_BYTES));
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  grouped_gemm_kernel<EPI><<<grid, THREADS, SMEM_BYTES, s>>>(ta, tb, kp);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int device_sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  static int cached[64] = {0};
+  if (dev >= 0 && dev < 64 && cached[dev]) return cached[dev];
+  int n = 1;
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  if (dev >= 0 && dev < 64) cached[dev] = n;
+  return n;
+}
+
+cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
+  if (a.M <= 0) return cudaSuccess;
+  if (a.b_fp8) return cudaErrorNotSupported;
+  if (a.G < 1 || a.G > MAX_G) return cudaErrorInvalidValue;
+  CUtensorMap ta, tb;
+  {
+    const uint64_t dims[2] = {static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.M)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(a.K) * 2};
+    const uint32_t box[2] = {BK, BM};
+    if (!encode_tmap(&ta, a.A, 2, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  KParams kp;
+  kp.group_offsets = a.group_offsets;
+  kp.G = a.G;
+  kp.M = a.M;
+  kp.K = a.K;
+  kp.N = a.N;
+  kp.out = a.out;
+  kp.b_scale = a.b_scale;
+  kp.bias = a.bias;
+  kp.act = a.act;
+  kp.err = a.err;
+  const uint64_t N = static_cast<uint64_t>(a.N), K = static_cast<uint64_t>(a.K);
+  if (a.epilogue == kEpiGateUpAct) {
+    const uint64_t dims[4] = {N, 2, K, static_cast<uint64_t>(a.G)};
+    const uint64_t strides[3] = {N * 2, 2 * N * 2, K * 2 * N * 2};
+    const uint32_t box[4] = {64, 1, BK, 1};
+    if (!encode_tmap(&tb, a.B, 4, dims, strides, box)) return cudaErrorInvalidValue;
+    kp.bn = 256;
+    kp.cols_per_tile = 128;
+  } else {
+    const uint64_t dims[3] = {N, K, static_cast<uint64_t>(a.G)};
+    const uint64_t strides[2] = {N * 2, K * N * 2};
+    const uint32_t box[3] = {64, BK, 1};
+    if (!encode_tmap(&tb, a.B, 3, dims, strides, box)) return cudaErrorInvalidValue;
+    kp.bn = static_cast<int>(std::min<uint64_t>(BN_MAX, (N + 63) / 64 * 64));
+    kp.cols_per_tile = kp.bn;
+  }
+  kp.n_tiles = (a.N + kp.cols_per_tile - 1) / kp.cols_per_tile;
+  const long long max_tiles =
+      (static_cast<long long>((a.M + BM - 1) / BM) + a.G) * static_cast<long long>(kp.n_tiles);
+  const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(device_sm_count(), max_tiles)));
+  switch (a.epilogue) {
+    case kEpiGateUpAct: return launch_epi<kEpiGateUpAct>(ta, tb, kp, grid, s);
+    case kEpiStoreBf16: return launch_epi<kEpiStoreBf16>(ta, tb, kp, grid, s);
+    case kEpiStoreF32: return launch_epi<kEpiStoreF32>(ta, tb, kp, grid, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace moe

@@ -1,0 +1,383 @@
+// C ABI of the MoE layer (include/moe.h): argument validation, workspace
+// layout and the order of kernel launches on the caller's stream.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+
+#include "moe_internal.h"
+
+using namespace moe;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+// Optional per-kernel trace events (moe_set_trace_events).
+void* const* g_trace_events = nullptr;
+int g_trace_n = 0;
+int g_trace_next = -1;  // next event index during a traced moe_layer call, -1 = off
+
+inline void trace_mark(cudaStream_t s) {
+  if (g_trace_next >= 0 && g_trace_next < g_trace_n)
+    cudaEventRecord(static_cast<cudaEvent_t>(g_trace_events[g_trace_next++]), s);
+}
+
+inline size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Layout {
+  size_t off[12];
+  size_t seg_scratch;
+  size_t total;
+};
+
+bool cfg_valid(const moe_config_t* c) {
+  if (!c) return false;
+  if (c->T < 0 || c->D < 8 || c->E < 1 || c->E > 512 || c->k < 1 || c->k > 16 || c->k > c->E ||
+      c->I < 8 || c->I_shared < 0)
+    return false;
+  if (c->D % 8 || c->I % 8 || c->I_shared % 8) return false;
+  if (c->act != MOE_ACT_SWIGLU && c->act != MOE_ACT_GEGLU_TANH) return false;
+  if (c->act_dtype != MOE_F32 && c->act_dtype != MOE_BF16) return false;
+  if (c->w_dtype != MOE_F32 && c->w_dtype != MOE_BF16 && c->w_dtype != MOE_FP8_E4M3) return false;
+  if (c->w_dtype == MOE_FP8_E4M3 && (c->D % 16 || c->I % 16 || c->I_shared % 16)) return false;
+  const long long R = static_cast<long long>(c->T) * c->k;
+  if (R > (1ll << 30)) return false;
+  return true;
+}
+
+bool combo_supported(const moe_config_t* c) {
+  if (c->act_dtype == MOE_F32) return c->w_dtype == MOE_F32;
+  return c->w_dtype == MOE_BF16 || c->w_dtype == MOE_FP8_E4M3;
+}
+
+Layout make_layout(const moe_config_t* c) {
+  Layout L{};
+  const size_t T = c->T, E = c->E, R = static_cast<size_t>(c->T) * c->k, D = c->D, I = c->I,
+               Is = c->I_shared;
+  const size_t ab = act_bytes(c->act_dtype);
+  size_t cur = sizeof(ControlBlock);
+  auto take = [&](size_t bytes) {
+    const size_t o = cur;
+    cur = align_up(cur + bytes);
+    return o;
+  };
+  L.off[MOE_WS_LOGITS] = take(T * E * 4);
+  L.off[MOE_WS_TOPK_IDS] = take(R * 4);
+  L.off[MOE_WS_TOPK_W] = take(R * 4);
+  L.off[MOE_WS_COUNTS] = take(E * 4);
+  L.off[MOE_WS_OFFSETS] = take((E + 1) * 4);
+  L.off[MOE_WS_SORTED_ROWS] = take(R * 4);
+  L.off[MOE_WS_DEST] = take(R * 4);
+  L.seg_scratch = take(E * static_cast<size_t>(route_segments(static_cast<long long>(R))) * 4 + 4);
+  L.off[MOE_WS_X_PERM] = take(R * D * ab);
+  L.off[MOE_WS_H] = take(R * I * ab);
+  L.off[MOE_WS_Y_PERM] = take(R * D * ab);
+  L.off[MOE_WS_H_SHARED] = take(T * Is * ab);
+  L.off[MOE_WS_S] = take(T * D * ab);
+  L.total = cur;
+  return L;
+}
+
+int check_ws(const moe_config_t* c, void* ws, size_t ws_bytes) {
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) % kAlign)) return MOE_ERR_WORKSPACE;
+  if (ws_bytes < make_layout(c).total) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+inline int32_t* err_word(void* ws) { return &static_cast<ControlBlock*>(ws)->err; }
+inline uint8_t* ws_at(void* ws, size_t off) { return static_cast<uint8_t*>(ws) + off; }
+
+inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+int common_checks(const moe_config_t* cfg, void* ws, size_t ws_bytes) {
+  if (!cfg_valid(cfg)) return MOE_ERR_INVALID_ARG;
+  if (!combo_supported(cfg)) return MOE_ERR_UNSUPPORTED;
+  return check_ws(cfg, ws, ws_bytes);
+}
+
+// ------------------------------------------------------------------ stages
+int do_route(const moe_config_t* c, const void* x, const void* Wg, const float* bias,
+             float* logits, int32_t* ids, float* w, int32_t* err, cudaStream_t s) {
+  cudaError_t e = cudaSuccess;
+  if (x) {
+    trace_mark(s);
+    if (c->act_dtype == MOE_F32) {
+      e = launch_simt_router(static_cast<const float*>(x), static_cast<const float*>(Wg), bias,
+                             logits, c->T, c->D, c->E, s);
+    } else {
+      GroupedGemmArgs a{};
+      a.epilogue = kEpiStoreF32;
+      a.A = x;
+      a.M = c->T;
+      a.K = c->D;
+      a.group_offsets = nullptr;
+      a.G = 1;
+      a.B = Wg;
+      a.N = c->E;
+      a.bias = bias;
+      a.out = logits;
+      a.err = err;
+      e = launch_grouped_gemm(a, s);
+    }
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  trace_mark(s);
+  return cuda_status(launch_topk_softmax(logits, c->T, c->E, c->k, c->renormalize, ids, w, err, s));
+}
+
+int do_permute(const moe_config_t* c, const int32_t* ids, const void* x, int32_t* counts,
+               int32_t* offsets, int32_t* sorted_rows, int32_t* dest, void* x_perm,
+               int32_t* seg_scratch, int32_t* err, cudaStream_t s) {
+  const int R = c->T * c->k;
+  cudaError_t e = launch_init_routing(ids, R, c->E, counts, offsets, sorted_rows, dest, seg_scratch,
+                                      err, s, g_trace_next >= 0 ? trace_mark : nullptr);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  if (x && x_perm) {
+    trace_mark(s);
+    e = launch_permute_gather(x, sorted_rows, R, c->k, c->T,
+                              static_cast<size_t>(c->D) * act_bytes(c->act_dtype), x_perm, err, s);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+// One gated FFN (gate/up + act, then down) over grouped rows.
+int do_ffn(const moe_config_t* c, const void* A, int M, const int32_t* offsets, int G,
+           const void* W13, const float* s13, const void* W2, const float* s2, int I, void* h,
+           void* y, int32_t* err, cudaStream_t s) {
+  if (M <= 0) return MOE_OK;
+  cudaError_t e;
+  trace_mark(s);
+  if (c->act_dtype == MOE_F32) {
+    e = launch_simt_gate_up(static_cast<const float*>(A), offsets, G, M, c->D,
+                            static_cast<const float*>(W13), I, c->act, static_cast<float*>(h), err,
+                            s);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    trace_mark(s);
+    e = launch_simt_down(static_cast<const float*>(h), offsets, G, M, I,
+                         static_cast<const float*>(W2), c->D, static_cast<float*>(y), err, s);
+    return cuda_status(e);
+  }
+  GroupedGemmArgs a{};
+  a.epilogue = kEpiGateUpAct;
+  a.A = A;
+  a.M = M;
+  a.K = c->D;
+  a.group_offsets = offsets;
+  a.G = G;
+  a.B = W13;
+  a.b_fp8 = c->w_dtype == MOE_FP8_E4M3;
+  a.N = I;
+  a.b_scale = s13;
+  a.out = h;
+  a.act = c->act;
+  a.err = err;
+  e = launch_grouped_gemm(a, s);
+  if (e != cudaSuccess) return e == cudaErrorNotSupported ? MOE_ERR_UNSUPPORTED : MOE_ERR_CUDA;
+  GroupedGemmArgs b = a;
+  b.epilogue = kEpiStoreBf16;
+  b.A = h;
+  b.K = I;
+  b.B = W2;
+  b.N = c->D;
+  b.b_scale = s2;
+  b.out = y;
+  trace_mark(s);
+  e = launch_grouped_gemm(b, s);
+  if (e != cudaSuccess) return e == cudaErrorNotSupported ? MOE_ERR_UNSUPPORTED : MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+int do_grouped_ffn(const moe_config_t* c, const void* x_perm, const int32_t* offsets,
+                   const void* W13, const float* s13, const void* W2, const float* s2, void* h,
+                   void* y_perm, const void* x, const void* W13s, const float* s13s,
+                   const void* W2s, const float* s2s, void* h_s, void* s_out, int32_t* err,
+                   cudaStream_t s) {
+  const int R = c->T * c->k;
+  int st = do_ffn(c, x_perm, R, offsets, c->E, W13, s13, W2, s2, c->I, h, y_perm, err, s);
+  if (st != MOE_OK) return st;
+  if (x && c->I_shared > 0)
+    st = do_ffn(c, x, c->T, nullptr, 1, W13s, s13s, W2s, s2s, c->I_shared, h_s, s_out, err, s);
+  return st;
+}
+
+bool fp8_scales_ok(const moe_config_t* c, const float* s13, const float* s2) {
+  const bool fp8 = c->w_dtype == MOE_FP8_E4M3;
+  return fp8 ? (s13 && s2) : (!s13 && !s2);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t moe_workspace_size(const moe_config_t* cfg) {
+  if (!cfg_valid(cfg)) return 0;
+  return make_layout(cfg).total;
+}
+
+size_t moe_workspace_offset(const moe_config_t* cfg, int which) {
+  if (!cfg_valid(cfg) || which < 0 || which > MOE_WS_S) return static_cast<size_t>(-1);
+  return make_layout(cfg).off[which];
+}
+
+int moe_route(const moe_config_t* cfg, const void* x, const void* Wg, const float* logit_bias,
+              float* logits, int32_t* topk_ids, float* topk_w, void* ws, size_t ws_bytes,
+              void* stream) {
+  int st = common_checks(cfg, ws, ws_bytes);
+  if (st != MOE_OK) return st;
+  if (!logits || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
+  if (x && (!Wg || !aligned16(x) || !aligned16(Wg))) return MOE_ERR_INVALID_ARG;
+  if (!x && logit_bias) return MOE_ERR_INVALID_ARG;
+  if (cfg->act_dtype == MOE_BF16 && x && (cfg->E % 8)) return MOE_ERR_INVALID_ARG;
+  if (cfg->T == 0) return MOE_OK;
+  return do_route(cfg, x, Wg, logit_bias, logits, topk_ids, topk_w, err_word(ws),
+                  static_cast<cudaStream_t>(stream));
+}
+
+int moe_permute(const moe_config_t* cfg, const int32_t* topk_ids, const void* x, int32_t* counts,
+                int32_t* offsets, int32_t* sorted_rows, int32_t* dest, void* x_perm, void* ws,
+                size_t ws_bytes, void* stream) {
+  int st = common_checks(cfg, ws, ws_bytes);
+  if (st != MOE_OK) return st;
+  if (!topk_ids || !counts || !offsets || !sorted_rows || !dest) return MOE_ERR_INVALID_ARG;
+  if (x && (!x_perm || !aligned16(x) || !aligned16(x_perm))) return MOE_ERR_INVALID_ARG;
+  const Layout L = make_layout(cfg);
+  return do_permute(cfg, topk_ids, x, counts, offsets, sorted_rows, dest, x_perm,
+                    reinterpret_cast<int32_t*>(ws_at(ws, L.seg_scratch)), err_word(ws),
+                    static_cast<cudaStream_t>(stream));
+}
+
+int moe_grouped_ffn(const moe_config_t* cfg, const void* x_perm, const int32_t* offsets,
+                    const void* W13, const float* s13, const void* W2, const float* s2, void* h,
+                    void* y_perm, const void* x, const void* W13s, const float* s13s,
+                    const void* W2s, const float* s2s, void* h_s, void* s_out, void* ws,
+                    size_t ws_bytes, void* stream) {
+  int st = common_checks(cfg, ws, ws_bytes);
+  if (st != MOE_OK) return st;
+  if (!x_perm || !offsets || !W13 || !W2 || !h || !y_perm) return MOE_ERR_INVALID_ARG;
+  for (const void* p : {x_perm, W13, W2, static_cast<const void*>(h), static_cast<const void*>(y_perm)})
+    if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
+  if (!fp8_scales_ok(cfg, s13, s2)) return MOE_ERR_INVALID_ARG;
+  const bool shared = x && cfg->I_shared > 0;
+  if (shared) {
+    if (!W13s || !W2s || !h_s || !s_out) return MOE_ERR_INVALID_ARG;
+    for (const void* p : {x, W13s, W2s, static_cast<const void*>(h_s), static_cast<const void*>(s_out)})
+      if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
+    if (!fp8_scales_ok(cfg, s13s, s2s)) return MOE_ERR_INVALID_ARG;
+  }
+  if (cfg->T == 0) return MOE_OK;
+  return do_grouped_ffn(cfg, x_perm, offsets, W13, s13, W2, s2, h, y_perm, x, W13s, s13s, W2s, s2s,
+                        h_s, s_out, err_word(ws), static_cast<cudaStream_t>(stream));
+}
+
+int moe_finalize(const moe_config_t* cfg, const void* y_perm, const int32_t* dest,
+                 const float* topk_w, const void* s, void* out, void* ws, size_t ws_bytes,
+                 void* stream) {
+  int st = common_checks(cfg, ws, ws_bytes);
+  if (st != MOE_OK) return st;
+  if (!y_perm || !dest || !topk_w || !out) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(y_perm) || !aligned16(out) || (s && !aligned16(s))) return MOE_ERR_INVALID_ARG;
+  if (cfg->T == 0) return MOE_OK;
+  return cuda_status(launch_finalize(cfg->act_dtype, y_perm, dest, topk_w, s, out, cfg->T, cfg->k,
+                                     cfg->D, cfg->T * cfg->k, err_word(ws),
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+int moe_layer(const moe_config_t* cfg, const void* x, const void* Wg, const float* logit_bias,
+              const void* W13, const float* s13, const void* W2, const float* s2,
+              const void* W13s, const float* s13s, const void* W2s, const float* s2s, void* out,
+              void* ws, size_t ws_bytes, void* stream) {
+  int st = common_checks(cfg, ws, ws_bytes);
+  if (st != MOE_OK) return st;
+  if (!x || !Wg || !W13 || !W2 || !out) return MOE_ERR_INVALID_ARG;
+  for (const void* p : {x, Wg, W13, W2, static_cast<const void*>(out)})
+    if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
+  if (!fp8_scales_ok(cfg, s13, s2)) return MOE_ERR_INVALID_ARG;
+  const bool shared = cfg->I_shared > 0;
+  if (shared) {
+    if (!W13s || !W2s || !aligned16(W13s) || !aligned16(W2s)) return MOE_ERR_INVALID_ARG;
+    if (!fp8_scales_ok(cfg, s13s, s2s)) return MOE_ERR_INVALID_ARG;
+  }
+  if (cfg->act_dtype == MOE_BF16 && (cfg->E % 8)) return MOE_ERR_INVALID_ARG;
+  if (cfg->T == 0) return MOE_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const Layout L = make_layout(cfg);
+  int32_t* err = err_word(ws);
+  float* logits = reinterpret_cast<float*>(ws_at(ws, L.off[MOE_WS_LOGITS]));
+  int32_t* ids = reinterpret_cast<int32_t*>(ws_at(ws, L.off[MOE_WS_TOPK_IDS]));
+  float* w = reinterpret_cast<float*>(ws_at(ws, L.off[MOE_WS_TOPK_W]));
+  int32_t* counts = reinterpret_cast<int32_t*>(ws_at(ws, L.off[MOE_WS_COUNTS]));
+  int32_t* offsets = reinterpret_cast<int32_t*>(ws_at(ws, L.off[MOE_WS_OFFSETS]));
+  int32_t* sorted_rows = reinterpret_cast<int32_t*>(ws_at(ws, L.off[MOE_WS_SORTED_ROWS]));
+  int32_t* dest = reinterpret_cast<int32_t*>(ws_at(ws, L.off[MOE_WS_DEST]));
+  int32_t* seg = reinterpret_cast<int32_t*>(ws_at(ws, L.seg_scratch));
+  void* x_perm = ws_at(ws, L.off[MOE_WS_X_PERM]);
+  void* h = ws_at(ws, L.off[MOE_WS_H]);
+  void* y_perm = ws_at(ws, L.off[MOE_WS_Y_PERM]);
+  void* h_s = ws_at(ws, L.off[MOE_WS_H_SHARED]);
+  void* s_out = ws_at(ws, L.off[MOE_WS_S]);
+
+  const bool traced = g_trace_events && g_trace_n >= moe_layer_launch_count(cfg) + 1;
+  g_trace_next = traced ? 0 : -1;
+  st = do_route(cfg, x, Wg, logit_bias, logits, ids, w, err, s);
+  if (st != MOE_OK) return (g_trace_next = -1, st);
+  st = do_permute(cfg, ids, x, counts, offsets, sorted_rows, dest, x_perm, seg, err, s);
+  if (st != MOE_OK) return (g_trace_next = -1, st);
+  st = do_grouped_ffn(cfg, x_perm, offsets, W13, s13, W2, s2, h, y_perm, shared ? x : nullptr,
+                      W13s, s13s, W2s, s2s, h_s, s_out, err, s);
+  if (st != MOE_OK) return (g_trace_next = -1, st);
+  trace_mark(s);
+  st = cuda_status(launch_finalize(cfg->act_dtype, y_perm, dest, w, shared ? s_out : nullptr, out,
+                                   cfg->T, cfg->k, cfg->D, cfg->T * cfg->k, err, s));
+  trace_mark(s);
+  g_trace_next = -1;
+  return st;
+}
+
+int moe_read_device_status(void* ws, void* stream, int32_t* flags) {
+  if (!ws) return MOE_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, err_word(ws), sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemsetAsync(err_word(ws), 0, sizeof(int32_t), s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (flags) *flags = v;
+  return v ? MOE_ERR_DEVICE_CHECK : MOE_OK;
+}
+
+const char* moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument (null pointer, shape, alignment or range)";
+    case MOE_ERR_UNSUPPORTED: return "unsupported dtype / activation combination";
+    case MOE_ERR_CUDA: return "CUDA runtime or driver error";
+    case MOE_ERR_DEVICE_CHECK: return "device data check failed (see the device error flags)";
+    case MOE_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    default: return "unknown status";
+  }
+}
+
+int moe_set_trace_events(void* const* events, int n_events) {
+  g_trace_events = (events && n_events > 0) ? events : nullptr;
+  g_trace_n = g_trace_events ? n_events : 0;
+  return MOE_OK;
+}
+
+int moe_layer_launch_count(const moe_config_t* cfg) {
+  if (!cfg_valid(cfg) || cfg->T == 0) return 0;
+  int n = 0;
+  n += 1;  // router projection
+  n += 1;  // top-k softmax
+  n += 3;  // histogram, scan, stable scatter
+  n += 1;  // permutation gather
+  n += 2;  // routed gate/up, down
+  if (cfg->I_shared > 0) n += 2;  // shared gate/up, down
+  n += 1;  // finalize
+  return n;
+}
+
+}  // extern "C"

@@ -1,0 +1,82 @@
+// Internal interfaces between the C ABI (moe_api.cu) and the kernel files.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "moe.h"
+
+namespace moe {
+
+// Control block at the start of every workspace.
+struct ControlBlock {
+  int32_t err;       // device error word (MOE_DEV_* flags)
+  int32_t reserved[63];
+};
+static_assert(sizeof(ControlBlock) == 256, "control block is 256 bytes");
+
+inline size_t act_bytes(int dt) { return dt == MOE_F32 ? 4 : 2; }
+inline size_t w_bytes(int dt) { return dt == MOE_F32 ? 4 : (dt == MOE_BF16 ? 2 : 1); }
+
+// ---------------------------------------------------------------- routing.cu
+// Segment size (expanded rows) handled by one warp of the stable scatter.
+constexpr int kRouteSeg = 1024;
+inline int route_segments(long long R) { return static_cast<int>((R + kRouteSeg - 1) / kRouteSeg); }
+
+cudaError_t launch_topk_softmax(const float* logits, int T, int E, int k, int renorm, int32_t* ids,
+                                float* w, int32_t* err, cudaStream_t s);
+// `mark`, when not null, is called on the stream right before each of the
+// three launches (trace hook of moe_layer).
+cudaError_t launch_init_routing(const int32_t* ids, int R, int E, int32_t* counts, int32_t* offsets,
+                                int32_t* sorted_rows, int32_t* dest, int32_t* seg_scratch,
+                                int32_t* err, cudaStream_t s, void (*mark)(cudaStream_t) = nullptr);
+cudaError_t launch_permute_gather(const void* x, const int32_t* sorted_rows, int R, int k, int T,
+                                  size_t row_bytes, void* x_perm, int32_t* err, cudaStream_t s);
+cudaError_t launch_finalize(int act_dtype, const void* y_perm, const int32_t* dest, const float* w,
+                            const void* s_rows, void* out, int T, int k, int D, int R,
+                            int32_t* err, cudaStream_t s);
+
+// ---------------------------------------------------------------- simt_fp32.cu
+// fp32 path (exact-fp32 configurations): plain CUDA-core kernels.
+cudaError_t launch_simt_router(const float* x, const float* Wg, const float* bias, float* logits,
+                               int T, int D, int E, cudaStream_t s);
+// Gate/up projection + activation over groups (offsets == nullptr: one group of M rows).
+cudaError_t launch_simt_gate_up(const float* A, const int32_t* offsets, int G, int M, int K,
+                                const float* W13, int I, int act, float* h, int32_t* err,
+                                cudaStream_t s);
+cudaError_t launch_simt_down(const float* h, const int32_t* offsets, int G, int M, int I,
+                             const float* W2, int N, float* y, int32_t* err, cudaStream_t s);
+
+// ---------------------------------------------------------------- gemm_sm103.cu
+enum GemmEpilogue : int {
+  kEpiGateUpAct = 0,  // W13 pass: acc = [gate | up] -> act(gate) * up, bf16
+  kEpiStoreBf16 = 1,  // W2 pass: acc -> (scale) -> bf16
+  kEpiStoreF32 = 2,   // router: acc (+ bias) -> fp32
+};
+
+struct GroupedGemmArgs {
+  int epilogue;                  // GemmEpilogue
+  const void* A;                 // [M, K] bf16, K contiguous
+  int M;                         // rows of A (and of the output)
+  int K;
+  const int32_t* group_offsets;  // [G+1] device, or nullptr for one group of M rows
+  int G;
+  const void* B;                 // [G, K, 2*N] (gate/up) or [G, K, N]; bf16 or e4m3
+  int b_fp8;                     // 1: B is e4m3 (converted to bf16 on chip)
+  int N;                         // output columns (I for gate/up)
+  const float* b_scale;          // [G, 2N] or [G, N] per-column scales (fp8), or nullptr
+  const float* bias;             // [N] fp32 (router), or nullptr
+  void* out;                     // [M, N] bf16 or fp32
+  int act;                       // moe_act_t (gate/up epilogue)
+  int32_t* err;
+};
+
+cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s);
+
+// Shared helper: SM count of the current device (cached).
+int device_sm_count();
+
+}  // namespace moe

@@ -1,0 +1,418 @@
+// Routing-side kernels of the MoE layer: gating top-k softmax, init_routing
+// (histogram, exclusive scan, stable scatter), the permutation gather and the
+// finalize (weighted un-permute + shared-expert add).  All are memory-bound;
+// they move 16-byte vectors and keep every index bounds-checked so that bad
+// input data is reported through the error word instead of faulting.
+#include <cuda_bf16.h>
+
+#include <cfloat>
+#include <climits>
+
+#include "moe_internal.h"
+
+namespace moe {
+namespace {
+
+constexpr unsigned FULL = 0xffffffffu;
+constexpr int kMaxTopK = 16;
+
+// ------------------------------------------------------------------------
+// gating_top_k_softmax ("CANN/cann-recipes-infer：Qwen3-MoE优化", section
+// "GMM使能和Routing优化"; "Gemma-4 模型优化报告" §6 MoE Router row).
+// One warp per token; lane l holds experts l, l+32, ... (E <= 512).  k rounds
+// of a warp arg-max with the order (higher logit, then lower index).  Weights:
+// softmax over the k chosen logits (renormalised) or full-softmax probabilities.
+template <int EPL>
+__global__ void topk_softmax_kernel(const float* __restrict__ logits, int T, int E, int k,
+                                    int renorm, int32_t* __restrict__ ids, float* __restrict__ w,
+                                    int32_t* err) {
+  const int warps_per_block = blockDim.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const long long t = static_cast<long long>(blockIdx.x) * warps_per_block + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const float* row = logits + t * E;
+  float v[EPL];
+  bool nonfinite = false;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const int e = lane + 32 * i;
+    float x = -INFINITY;
+    if (e < E) {
+      x = row[e];
+      if (!isfinite(x)) {
+        nonfinite = true;
+        x = -INFINITY;
+      }
+    }
+    v[i] = x;
+  }
+  if (__any_sync(FULL, nonfinite) && lane == 0) atomicOr(err, MOE_DEV_NONFINITE_LOGIT);
+
+  uint32_t taken = 0;
+  float my_v = -INFINITY;
+  int my_e = 0;
+  for (int j = 0; j < k; ++j) {
+    float bv = -INFINITY;
+    int be = INT_MAX;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && !((taken >> i) & 1u)) {
+        if (v[i] > bv || (v[i] == bv && e < be)) {
+          bv = v[i];
+          be = e;
+        }
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(FULL, bv, off);
+      const int oe = __shfl_xor_sync(FULL, be, off);
+      if (ov > bv || (ov == bv && oe < be)) {
+        bv = ov;
+        be = oe;
+      }
+    }
+    if ((be & 31) == lane) taken |= 1u << (be >> 5);
+    if (lane == j) {
+      my_v = bv;
+      my_e = be;
+    }
+  }
+  const float m = __shfl_sync(FULL, my_v, 0);
+  float z = 0.0f;
+  float denom;
+  if (m == -INFINITY) {  // every logit non-finite: uniform weights
+    z = lane < k ? 1.0f : 0.0f;
+    denom = static_cast<float>(k);
+  } else if (renorm) {
+    z = lane < k ? expf(my_v - m) : 0.0f;
+    denom = z;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) denom += __shfl_xor_sync(FULL, denom, off);
+  } else {
+    z = lane < k ? expf(my_v - m) : 0.0f;
+    float s = 0.0f;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) s += (lane + 32 * i < E) ? expf(v[i] - m) : 0.0f;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(FULL, s, off);
+    denom = s;
+  }
+  if (lane < k) {
+    ids[t * k + lane] = my_e;
+    w[t * k + lane] = z / denom;
+  }
+}
+
+// ------------------------------------------------------------------------
+// init_routing ("CANN/cann-recipes-infer：Qwen3-MoE优化", section
+// "GMM使能和Routing优化": npu_moe_init_routing + npu_moe_compute_expert_tokens).
+// A stable counting sort of the expanded rows r = t*k + j by expert id:
+//  1. per-segment histograms (segments of kRouteSeg rows),
+//  2. one exclusive scan over (expert, segment) in expert-major order,
+//  3. per-segment stable scatter: one warp walks its segment in order, 32 rows
+//     per step, ranking equal ids inside the step with __match_any_sync.
+__global__ void route_hist_kernel(const int32_t* __restrict__ ids, int R, int E, int nseg,
+                                  int32_t* __restrict__ seg_hist, int32_t* err) {
+  extern __shared__ int32_t cnt[];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
+  __syncthreads();
+  const int s = blockIdx.x;
+  const int r0 = s * kRouteSeg, r1 = min(R, r0 + kRouteSeg);
+  bool bad = false;
+  for (int r = r0 + threadIdx.x; r < r1; r += blockDim.x) {
+    const int e = ids[r];
+    if (e < 0 || e >= E) bad = true;
+    else atomicAdd(&cnt[e], 1);
+  }
+  if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(err, MOE_DEV_BAD_EXPERT_ID);
+  for (int e = threadIdx.x; e < E; e += blockDim.x) seg_hist[static_cast<size_t>(e) * nseg + s] = cnt[e];
+}
+
+// Single-block exclusive scan of seg_hist (expert-major, E*nseg entries) in
+// place, plus counts and offsets.
+__global__ void route_scan_kernel(int32_t* __restrict__ seg_hist, int E, int nseg,
+                                  int32_t* __restrict__ counts, int32_t* __restrict__ offsets) {
+  constexpr int ITEMS = 8;
+  __shared__ int32_t warp_sums[32];
+  __shared__ int32_t carry_s;
+  const int n = E * nseg;
+  const int chunk = blockDim.x * ITEMS;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  if (threadIdx.x == 0) carry_s = 0;
+  __syncthreads();
+  for (int base = 0; base < n; base += chunk) {
+    int vals[ITEMS];
+    int local = 0;
+    const int i0 = base + threadIdx.x * ITEMS;
+#pragma unroll
+    for (int i = 0; i < ITEMS; ++i) {
+      vals[i] = (i0 + i < n) ? seg_hist[i0 + i] : 0;
+      local += vals[i];
+    }
+    int incl = local;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int y = __shfl_up_sync(FULL, incl, d);
+      if (lane >= d) incl += y;
+    }
+    if (lane == 31) warp_sums[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+      int ws = lane < nw ? warp_sums[lane] : 0;
+      int wi = ws;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int y = __shfl_up_sync(FULL, wi, d);
+        if (lane >= d) wi += y;
+      }
+      if (lane < nw) warp_sums[lane] = wi - ws;  // exclusive warp prefix
+    }
+    __syncthreads();
+    int run = carry_s + warp_sums[wid] + incl - local;
+#pragma unroll
+    for (int i = 0; i < ITEMS; ++i) {
+      if (i0 + i < n) {
+        const int idx = i0 + i;
+        const int e = idx / nseg;
+        if (idx % nseg == 0) offsets[e] = run;
+        seg_hist[idx] = run;
+      }
+      run += vals[i];
+    }
+    __syncthreads();
+    if (threadIdx.x == blockDim.x - 1) carry_s = run;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) offsets[E] = carry_s;
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const int next = (e + 1 < E) ? seg_hist[static_cast<size_t>(e + 1) * nseg] : carry_s;
+    counts[e] = next - seg_hist[static_cast<size_t>(e) * nseg];
+  }
+}
+
+__global__ void route_scatter_kernel(const int32_t* __restrict__ ids, int R, int E, int nseg,
+                                     const int32_t* __restrict__ seg_base,
+                                     int32_t* __restrict__ sorted_rows, int32_t* __restrict__ dest) {
+  extern __shared__ int32_t run[];  // [warps_per_block][E]
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int s = blockIdx.x * (blockDim.x >> 5) + wid;
+  int32_t* my = run + wid * E;
+  for (int e = lane; e < E; e += 32) my[e] = 0;
+  __syncwarp();
+  if (s >= nseg) return;
+  const int r0 = s * kRouteSeg, r1 = min(R, r0 + kRouteSeg);
+  const unsigned lt = (1u << lane) - 1u;
+  for (int rb = r0; rb < r1; rb += 32) {
+    const int r = rb + lane;
+    const bool in = r < r1;
+    int e = in ? ids[r] : -1;
+    const bool valid = in && e >= 0 && e < E;
+    if (in && !valid) dest[r] = -1;
+    const int key = valid ? e : -1 - lane;  // invalid rows never match anything
+    const unsigned peers = __match_any_sync(FULL, key);
+    if (valid) {
+      const int rank = __popc(peers & lt);
+      const int pos = seg_base[static_cast<size_t>(e) * nseg + s] + my[e] + rank;
+      sorted_rows[pos] = r;
+      dest[r] = pos;
+    }
+    __syncwarp();
+    if (valid && (peers & lt) == 0) my[e] += __popc(peers);
+    __syncwarp();
+  }
+}
+
+// ------------------------------------------------------------------------
+// Permutation gather (the "千问 3.5 MoE 在 TPU 上的系统优化实战" SparseCore
+// paragraph: rows gathered by routing index into one contiguous buffer).
+// One warp per permuted row, 16-byte vectors.
+__global__ void permute_gather_kernel(const uint4* __restrict__ x,
+                                      const int32_t* __restrict__ sorted_rows, int R, int k, int T,
+                                      int vec_per_row, uint4* __restrict__ x_perm, int32_t* err) {
+  const int lane = threadIdx.x & 31;
+  const long long wstride = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+  for (long long p = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       p < R; p += wstride) {
+    const int r = sorted_rows[p];
+    const int t = r / k;
+    uint4* dst = x_perm + p * vec_per_row;
+    if (r < 0 || t >= T) {
+      if (lane == 0) atomicOr(err, MOE_DEV_BAD_DEST);
+      for (int v = lane; v < vec_per_row; v += 32) dst[v] = make_uint4(0, 0, 0, 0);
+      continue;
+    }
+    const uint4* src = x + static_cast<long long>(t) * vec_per_row;
+    int v = lane;
+    for (; v + 96 < vec_per_row; v += 128) {
+      const uint4 a = src[v], b = src[v + 32], c = src[v + 64], d = src[v + 96];
+      dst[v] = a;
+      dst[v + 32] = b;
+      dst[v + 64] = c;
+      dst[v + 96] = d;
+    }
+    for (; v < vec_per_row; v += 32) dst[v] = src[v];
+  }
+}
+
+// ------------------------------------------------------------------------
+// finalize_routing ("CANN/cann-recipes-infer：Qwen3-MoE优化", section
+// "GMM使能和Routing优化") fused with the shared-expert add ("千问 3.5 MoE 在
+// TPU 上的系统优化实战": y = Router(x) + SharedExpert(x)).  One warp per
+// token; fp32 accumulation with j ascending, shared row last, one rounding.
+__device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&f)[8]) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 v = __bfloat1622float2(h[i]);
+    f[2 * i] = v.x;
+    f[2 * i + 1] = v.y;
+  }
+}
+__device__ __forceinline__ void load8(const float* p, float (&f)[8]) {
+  const float4 a = *reinterpret_cast<const float4*>(p);
+  const float4 b = *reinterpret_cast<const float4*>(p + 4);
+  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+  f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+__device__ __forceinline__ void store8(__nv_bfloat16* p, const float (&f)[8]) {
+  uint4 u;
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+  *reinterpret_cast<uint4*>(p) = u;
+}
+__device__ __forceinline__ void store8(float* p, const float (&f)[8]) {
+  *reinterpret_cast<float4*>(p) = make_float4(f[0], f[1], f[2], f[3]);
+  *reinterpret_cast<float4*>(p + 4) = make_float4(f[4], f[5], f[6], f[7]);
+}
+
+template <typename Tt>
+__global__ void finalize_kernel(const Tt* __restrict__ y_perm, const int32_t* __restrict__ dest,
+                                const float* __restrict__ w, const Tt* __restrict__ s_rows,
+                                Tt* __restrict__ out, int T, int k, int D, int R, int32_t* err) {
+  const int lane = threadIdx.x & 31;
+  const long long wstride = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+  const int nchunk = D / 8;
+  for (long long t = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       t < T; t += wstride) {
+    int my_p = -1;
+    float my_w = 0.0f;
+    if (lane < k) {
+      my_p = dest[t * k + lane];
+      my_w = w[t * k + lane];
+      if (my_p < 0 || my_p >= R) {
+        atomicOr(err, MOE_DEV_BAD_DEST);
+        my_p = -1;
+      }
+    }
+    // every lane gets all k (position, weight) pairs before the chunk loop
+    int pj[kMaxTopK];
+    float wj[kMaxTopK];
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+      pj[j] = __shfl_sync(FULL, my_p, j);
+      wj[j] = __shfl_sync(FULL, my_w, j);
+    }
+    for (int c = lane; c < nchunk; c += 32) {
+      float acc[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+#pragma unroll
+      for (int j = 0; j < kMaxTopK; ++j) {
+        if (j < k && pj[j] >= 0) {
+          float f[8];
+          load8(y_perm + static_cast<long long>(pj[j]) * D + c * 8, f);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj[j], f[i], acc[i]);
+        }
+      }
+      if (s_rows) {
+        float f[8];
+        load8(s_rows + t * D + c * 8, f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] += f[i];
+      }
+      store8(out + t * D + c * 8, acc);
+    }
+  }
+}
+
+int blocks_for(long long work_items, int per_block, int cap) {
+  long long b = (work_items + per_block - 1) / per_block;
+  if (b < 1) b = 1;
+  if (b > cap) b = cap;
+  return static_cast<int>(b);
+}
+
+}  // namespace
+
+cudaError_t launch_topk_softmax(const float* logits, int T, int E, int k, int renorm, int32_t* ids,
+                                float* w, int32_t* err, cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
+  const int threads = 256, wpb = threads / 32;
+  const int blocks = (T + wpb - 1) / wpb;
+  const int epl = (E + 31) / 32;
+  if (epl <= 4)
+    topk_softmax_kernel<4><<<blocks, threads, 0, s>>>(logits, T, E, k, renorm, ids, w, err);
+  else if (epl <= 8)
+    topk_softmax_kernel<8><<<blocks, threads, 0, s>>>(logits, T, E, k, renorm, ids, w, err);
+  else
+    topk_softmax_kernel<16><<<blocks, threads, 0, s>>>(logits, T, E, k, renorm, ids, w, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_init_routing(const int32_t* ids, int R, int E, int32_t* counts, int32_t* offsets,
+                                int32_t* sorted_rows, int32_t* dest, int32_t* seg_scratch,
+                                int32_t* err, cudaStream_t s, void (*mark)(cudaStream_t)) {
+  if (R <= 0) {
+    cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, s);
+    if (e != cudaSuccess) return e;
+    return cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (E + 1), s);
+  }
+  const int nseg = route_segments(R);
+  if (mark) mark(s);
+  route_hist_kernel<<<nseg, 256, E * sizeof(int32_t), s>>>(ids, R, E, nseg, seg_scratch, err);
+  if (mark) mark(s);
+  route_scan_kernel<<<1, 1024, 0, s>>>(seg_scratch, E, nseg, counts, offsets);
+  const int wpb = 4;
+  if (mark) mark(s);
+  route_scatter_kernel<<<(nseg + wpb - 1) / wpb, 32 * wpb, wpb * E * sizeof(int32_t), s>>>(
+      ids, R, E, nseg, seg_scratch, sorted_rows, dest);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_permute_gather(const void* x, const int32_t* sorted_rows, int R, int k, int T,
+                                  size_t row_bytes, void* x_perm, int32_t* err, cudaStream_t s) {
+  if (R <= 0) return cudaSuccess;
+  const int vec = static_cast<int>(row_bytes / 16);
+  const int threads = 256;
+  const int blocks = blocks_for(R, threads / 32, device_sm_count() * 16);
+  permute_gather_kernel<<<blocks, threads, 0, s>>>(static_cast<const uint4*>(x), sorted_rows, R, k,
+                                                   T, vec, static_cast<uint4*>(x_perm), err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_finalize(int act_dtype, const void* y_perm, const int32_t* dest, const float* w,
+                            const void* s_rows, void* out, int T, int k, int D, int R,
+                            int32_t* err, cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
+  const int threads = 256;
+  const int blocks = blocks_for(T, threads / 32, device_sm_count() * 16);
+  if (act_dtype == MOE_BF16) {
+    finalize_kernel<__nv_bfloat16><<<blocks, threads, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(y_perm), dest, w,
+        static_cast<const __nv_bfloat16*>(s_rows), static_cast<__nv_bfloat16*>(out), T, k, D, R,
+        err);
+  } else {
+    finalize_kernel<float><<<blocks, threads, 0, s>>>(static_cast<const float*>(y_perm), dest, w,
+                                                      static_cast<const float*>(s_rows),
+                                                      static_cast<float*>(out), T, k, D, R, err);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace moe

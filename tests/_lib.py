@@ -1,0 +1,29 @@
+"""Shared helpers of the test suite: build/load the library, run the oracle,
+compare results."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import mixture_experts_layer_gating_gb300 as moe
+from mixture_experts_layer_gating_gb300 import _build
+
+
+def ensure_library():
+    _build.build()
+    return moe.load_library()
+
+
+def rms(a) -> float:
+    a = np.asarray(a, np.float64)
+    return float(np.sqrt(np.mean(a * a))) if a.size else 0.0
+
+
+def tol_factor(shape) -> float:
+    """Layer-output tolerance as a fraction of RMS(out): 2e-2 for bf16 / fp32
+    weights, 6e-2 for fp8 weights."""
+    return 6e-2 if shape.w_dtype == "fp8_e4m3" else 2e-2
+
+
+def to_device(inp, device="cuda"):
+    return {k: (v.to(device) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}

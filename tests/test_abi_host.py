@@ -1,0 +1,109 @@
+"""The C-ABI library loads, exports every symbol include/moe.h declares, and
+its host-side logic (workspace sizing, argument validation, status text)
+behaves as documented.  No GPU needed: nothing here reaches a CUDA call."""
+import ctypes
+
+import pytest
+
+import mixture_experts_layer_gating_gb300 as moe
+import workloads
+from tests._lib import ensure_library
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return ensure_library()
+
+
+def test_exports_every_header_symbol(lib):
+    names = moe.header_symbols()
+    assert {"moe_route", "moe_permute", "moe_grouped_ffn", "moe_finalize", "moe_layer",
+            "moe_workspace_size"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/moe.h but not exported"
+
+
+@pytest.mark.parametrize("name", sorted(workloads.CONFIGS))
+def test_workspace_size_covers_intermediates(lib, name):
+    shape = workloads.CONFIGS[name]
+    cfg = moe.config_from_shape(shape)
+    n = moe.moe_workspace_size(cfg)
+    ab = 4 if shape.act_dtype == "f32" else 2
+    R = shape.R
+    need = R * shape.D * ab * 2 + R * shape.I * ab + shape.T * shape.E * 4
+    assert n >= need
+    offs = [moe.moe_workspace_offset(cfg, i) for i in range(len(moe.WS_SLOTS))]
+    assert all(o % 256 == 0 for o in offs)
+    assert offs == sorted(offs) and offs[-1] < n
+    assert moe.moe_layer_launch_count(cfg) == (11 if shape.I_shared else 9)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(k=0), dict(k=9, E=8), dict(E=513, k=8), dict(D=12), dict(I=100), dict(T=-1),
+    dict(act=7), dict(k=17, E=64), dict(D=8, w_dtype="fp8_e4m3"),
+])
+def test_invalid_configs_rejected(lib, bad):
+    base = dict(T=64, D=256, E=8, k=2, I=128)
+    acts = {"act": bad.pop("act")} if "act" in bad else {}
+    base.update(bad)
+    cfg = moe.make_config(**{k: v for k, v in base.items()})
+    if acts:
+        cfg.act = acts["act"]
+    assert moe.moe_workspace_size(cfg) == 0
+    assert moe.moe_layer_launch_count(cfg) == 0
+
+
+def _call_layer(lib, cfg, ptrs, ws, ws_bytes):
+    return lib.moe_layer(ctypes.byref(cfg), *ptrs, ws, ws_bytes, None)
+
+
+def test_host_validation_codes(lib):
+    cfg = moe.make_config(64, 256, 8, 2, 128)
+    n = moe.moe_workspace_size(cfg)
+    good = 1 << 20  # a fake, aligned device address: validation fails before any use
+    ptrs = [good, good, None, good, None, good, None, None, None, None, None, good]
+    # workspace problems
+    assert _call_layer(lib, cfg, ptrs, None, n) == -5
+    assert _call_layer(lib, cfg, ptrs, good + 16, n) == -5
+    assert _call_layer(lib, cfg, ptrs, good, n - 1) == -5
+    # null / misaligned tensors
+    bad = list(ptrs); bad[0] = None
+    assert _call_layer(lib, cfg, bad, good, n) == -1
+    bad = list(ptrs); bad[3] = good + 8
+    assert _call_layer(lib, cfg, bad, good, n) == -1
+    # fp8 weights need scales; bf16 weights must not get them
+    cfg8 = moe.make_config(64, 256, 8, 2, 128, w_dtype="fp8_e4m3")
+    assert _call_layer(lib, cfg8, ptrs, good, moe.moe_workspace_size(cfg8)) == -1
+    bad = list(ptrs); bad[4] = good
+    assert _call_layer(lib, cfg, bad, good, n) == -1
+    # unsupported dtype pair
+    cfg_mix = moe.make_config(64, 256, 8, 2, 128, act_dtype="f32", w_dtype="bf16")
+    assert _call_layer(lib, cfg_mix, ptrs, good, moe.moe_workspace_size(cfg_mix)) == -2
+    # shared expert weights required when I_shared > 0
+    cfg_s = moe.make_config(64, 256, 8, 2, 128, I_shared=64)
+    assert _call_layer(lib, cfg_s, ptrs, good, moe.moe_workspace_size(cfg_s)) == -1
+    # T == 0 is a no-op that touches nothing
+    cfg0 = moe.make_config(0, 256, 8, 2, 128)
+    assert _call_layer(lib, cfg0, ptrs, good, moe.moe_workspace_size(cfg0)) == 0
+
+
+def test_status_strings(lib):
+    for st in (0, -1, -2, -3, -4, -5):
+        assert moe.moe_status_string(st)
+    assert "unknown" in moe.moe_status_string(12345)
+
+
+def test_stage_validation(lib):
+    cfg = moe.make_config(64, 256, 8, 2, 128)
+    n = moe.moe_workspace_size(cfg)
+    g = 1 << 20
+    # moe_route: bias without x is rejected; missing outputs rejected
+    assert lib.moe_route(ctypes.byref(cfg), None, None, g, g, g, g, g, n, None) == -1
+    assert lib.moe_route(ctypes.byref(cfg), g, g, None, None, g, g, g, n, None) == -1
+    # moe_permute: gather requested without destination
+    assert lib.moe_permute(ctypes.byref(cfg), g, g, g, g, g, g, None, g, n, None) == -1
+    # moe_finalize: missing weights
+    assert lib.moe_finalize(ctypes.byref(cfg), g, g, None, None, g, g, n, None) == -1
+    # moe_grouped_ffn: misaligned h
+    assert lib.moe_grouped_ffn(ctypes.byref(cfg), g, g, g, None, g, None, g + 4, g, None, None,
+                               None, None, None, None, None, g, n, None) == -1

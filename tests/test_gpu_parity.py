@@ -1,0 +1,271 @@
+"""GPU parity: every stage and the whole layer, through the C ABI, against the
+CPU fp64 oracle on the same seeded inputs.
+
+Bars: routing ids / counts / offsets / permutation bit-exact given the same
+fp32 router logits; gate weights within 1e-6; layer outputs within
+2e-2 * RMS(out) (bf16, fp32) or 6e-2 * RMS(out) (fp8), with tokens whose k-th
+and (k+1)-th oracle logits lie within 1e-4 left out of the output and id
+comparisons.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import mixture_experts_layer_gating_gb300 as moe
+import oracle
+import workloads
+from tests._lib import ensure_library, rms, tol_factor
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return ensure_library()
+
+
+def _cpu(d):
+    return {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+
+
+def run_layer(shape, inp):
+    cfg = moe.config_from_shape(shape)
+    ws = moe.alloc_workspace(cfg)
+    out = torch.empty((shape.T, shape.D), dtype=workloads.torch_dtype(shape.act_dtype), device="cuda")
+    moe.moe_layer(cfg, inp["x"], inp["Wg"], inp["logit_bias"], inp["W13"], inp["s13"], inp["W2"],
+                  inp["s2"], inp["W13s"], inp["s13s"], inp["W2s"], inp["s2s"], out, ws)
+    flags = moe.moe_read_device_status(ws)
+    assert flags == 0, f"device error flags {flags:#x}"
+    R = shape.R
+    view = lambda slot, shp, dt: moe.workspace_view(ws, cfg, slot, shp, dt).cpu()  # noqa: E731
+    adt = workloads.torch_dtype(shape.act_dtype)
+    res = {
+        "out": out.cpu(),
+        "logits": view("logits", (shape.T, shape.E), torch.float32),
+        "ids": view("topk_ids", (shape.T, shape.k), torch.int32),
+        "w": view("topk_w", (shape.T, shape.k), torch.float32),
+        "counts": view("counts", (shape.E,), torch.int32),
+        "offsets": view("offsets", (shape.E + 1,), torch.int32),
+        "sorted_rows": view("sorted_rows", (R,), torch.int32),
+        "dest": view("dest", (R,), torch.int32),
+        "x_perm": view("x_perm", (R, shape.D), adt),
+    }
+    return res
+
+
+def check_layer(shape, seed=0):
+    inp = workloads.make_inputs(shape, seed=seed, device="cuda")
+    g = run_layer(shape, inp)
+    cinp = _cpu(inp)
+    k, E = shape.k, shape.E
+
+    # 1. routing, given the GPU's own fp32 logits: bit-exact ids, weights to 1e-6
+    L_gpu = g["logits"].double().numpy()
+    ids_o, w_o = oracle.topk_softmax(L_gpu, k, shape.renormalize)
+    assert np.array_equal(g["ids"].numpy(), ids_o), "top-k ids differ (same logits)"
+    assert np.max(np.abs(g["w"].double().numpy() - w_o)) <= 1e-6
+    r = oracle.init_routing(g["ids"].numpy(), E)
+    assert np.array_equal(g["counts"].numpy(), r["counts"])
+    assert np.array_equal(g["offsets"].numpy(), r["offsets"])
+    assert np.array_equal(g["sorted_rows"].numpy(), r["sorted_rows"])
+    assert np.array_equal(g["dest"].numpy(), r["dest"])
+    xs = cinp["x"][torch.from_numpy(r["sorted_rows"] // k)]
+    assert torch.equal(g["x_perm"], xs), "permutation gather must copy rows bit-exactly"
+
+    # 2. router projection against the fp64 definition
+    L_ref = oracle.router_logits(cinp["x"], cinp["Wg"], cinp["logit_bias"])
+    assert np.max(np.abs(L_gpu - L_ref)) <= 1e-3 * max(1.0, rms(L_ref))
+
+    # 3. the layer output against the fp64 oracle (its own logits)
+    ref = oracle.moe_layer(cinp, k, shape.act, shape.renormalize)
+    ties = oracle.near_tie_tokens(ref["logits"], k)
+    same = (ref["ids"] == g["ids"].numpy()).all(axis=1)
+    assert (same | ties).all(), "ids differ on a token without a near tie"
+    keep = ~ties
+    out_g = g["out"].double().numpy()
+    err = np.abs(out_g - ref["out"])[keep]
+    scale = rms(ref["out"])
+    assert np.isfinite(out_g).all()
+    assert err.max() <= tol_factor(shape) * scale, \
+        f"max|err| {err.max():.3e} > {tol_factor(shape)} * RMS {scale:.3e} ({int(ties.sum())} near-tie tokens left out)"
+    return {"max_err_over_rms": float(err.max() / scale), "near_ties": int(ties.sum())}
+
+
+C = workloads.CONFIGS
+LAYER_CASES = {
+    "toy": C["toy"],
+    "qwen3_T512": C["qwen3_prefill"].with_tokens(512),
+    "qwen3_T1": C["qwen3_decode"].with_tokens(1),
+    "qwen3_T64_decode": C["qwen3_decode"],
+    "qwen3_zipf_T384": dataclasses.replace(C["qwen3_prefill"].with_tokens(384), zipf=1.1, name="qwen3_zipf"),
+    "gemma4_T256": C["gemma4_prefill"].with_tokens(256),
+    "gemma4_T8_decode": C["gemma4_decode"],
+    "qwen35_T64": C["qwen35_decode64"],
+}
+
+
+@pytest.mark.parametrize("case", sorted(LAYER_CASES))
+def test_layer_parity(case):
+    check_layer(LAYER_CASES[case])
+
+
+def test_layer_parity_full_qwen3_prefill():
+    """The benchmarked workload at full size (T=4096), every token checked."""
+    check_layer(C["qwen3_prefill"])
+
+
+# ------------------------------------------------------------------ stages
+def _ws_for(cfg):
+    return moe.alloc_workspace(cfg)
+
+
+@pytest.mark.parametrize("E,k,renorm", [(128, 8, True), (512, 10, True), (8, 2, True), (64, 5, False), (33, 33, True)])
+def test_route_from_logits_bit_exact(E, k, renorm):
+    T = 777
+    gen = torch.Generator(device="cuda").manual_seed(E * 31 + k)
+    L = torch.randn((T, E), generator=gen, device="cuda")
+    L[: T // 3] = torch.round(L[: T // 3] * 2) / 2  # many exact ties
+    L[5] = 0.0  # a token whose logits are all equal
+    cfg = moe.make_config(T, 64, E, k, 64, renormalize=renorm)
+    ws = _ws_for(cfg)
+    ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    moe.moe_route(cfg, None, None, None, L, ids, w, ws)
+    assert moe.moe_read_device_status(ws) == 0
+    ids_o, w_o = oracle.topk_softmax(L.cpu().double().numpy(), k, renorm)
+    assert np.array_equal(ids.cpu().numpy(), ids_o)
+    assert np.max(np.abs(w.cpu().double().numpy() - w_o)) <= 1e-6
+    assert np.array_equal(ids[5].cpu().numpy(), np.arange(k))
+
+
+@pytest.mark.parametrize("T,E,k,pattern", [
+    (1000, 128, 8, "uniform"), (3000, 512, 10, "uniform"), (129, 8, 2, "one_hot"),
+    (4096, 256, 8, "skew"), (1, 4, 1, "uniform"), (2500, 64, 6, "empty_half"),
+])
+def test_permute_bit_exact(T, E, k, pattern):
+    gen = np.random.default_rng(T + E + k)
+    if pattern == "one_hot":  # expert 3 and 5 take every token
+        ids = np.tile(np.array([3, 5]), (T, 1))
+    elif pattern == "skew":
+        p = 1.0 / np.arange(1, E + 1) ** 1.2
+        ids = np.stack([gen.choice(E, k, replace=False, p=p / p.sum()) for _ in range(T)])
+    elif pattern == "empty_half":
+        ids = np.stack([gen.permutation(E // 2)[:k] * 2 for _ in range(T)])
+    else:
+        ids = np.stack([gen.permutation(E)[:k] for _ in range(T)])
+    D = 136
+    cfg = moe.make_config(T, D, E, k, 64)
+    ws = _ws_for(cfg)
+    tids = torch.from_numpy(ids.astype(np.int32)).cuda()
+    x = torch.randn((T, D), device="cuda").to(torch.bfloat16)
+    R = T * k
+    counts = torch.empty(E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    sr = torch.empty(R, dtype=torch.int32, device="cuda")
+    dest = torch.empty(R, dtype=torch.int32, device="cuda")
+    xp = torch.empty((R, D), dtype=torch.bfloat16, device="cuda")
+    moe.moe_permute(cfg, tids, x, counts, offsets, sr, dest, xp, ws)
+    assert moe.moe_read_device_status(ws) == 0
+    r = oracle.init_routing(ids, E)
+    assert np.array_equal(counts.cpu().numpy(), r["counts"])
+    assert np.array_equal(offsets.cpu().numpy(), r["offsets"])
+    assert np.array_equal(sr.cpu().numpy(), r["sorted_rows"])
+    assert np.array_equal(dest.cpu().numpy(), r["dest"])
+    assert torch.equal(xp.cpu(), x.cpu()[torch.from_numpy(r["sorted_rows"] // k)])
+    # un-permute(permute(x)) is the identity
+    assert torch.equal(xp[dest.long()].view(T, k, D)[:, 0], x)
+
+
+def test_permute_flags_bad_ids_without_fault():
+    T, E, k, D = 300, 16, 2, 64
+    ids = torch.randint(0, E, (T, k), dtype=torch.int32, device="cuda")
+    ids[7, 1] = E
+    ids[100, 0] = -3
+    cfg = moe.make_config(T, D, E, k, 64)
+    ws = _ws_for(cfg)
+    R = T * k
+    counts = torch.empty(E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    sr = torch.full((R,), -1, dtype=torch.int32, device="cuda")
+    dest = torch.empty(R, dtype=torch.int32, device="cuda")
+    x = torch.randn((T, D), device="cuda").to(torch.bfloat16)
+    xp = torch.empty((R, D), dtype=torch.bfloat16, device="cuda")
+    moe.moe_permute(cfg, ids, x, counts, offsets, sr, dest, xp, ws)
+    flags = moe.moe_read_device_status(ws)
+    assert flags & moe.MOE_DEV_BAD_EXPERT_ID
+    assert int(offsets[E]) == R - 2
+    d = dest.cpu().numpy()
+    assert d[7 * k + 1] == -1 and d[100 * k] == -1
+    assert moe.moe_read_device_status(ws) == 0  # reading clears the word
+
+
+def _grouped_case(E, counts, D, I, act, seed):
+    gen = torch.Generator(device="cuda").manual_seed(seed)
+    R = int(sum(counts))
+    offsets = np.zeros(E + 1, dtype=np.int32)
+    offsets[1:] = np.cumsum(counts)
+    xp = torch.randn((R, D), generator=gen, device="cuda").to(torch.bfloat16)
+    W13 = (torch.randn((E, D, 2 * I), generator=gen, device="cuda") * 0.02).to(torch.bfloat16)
+    W2 = (torch.randn((E, I, D), generator=gen, device="cuda") * 0.02).to(torch.bfloat16)
+    return xp, offsets, W13, W2
+
+
+@pytest.mark.parametrize("E,counts,D,I,act", [
+    (4, [300, 0, 129, 1], 256, 128, "swiglu"),            # empty expert, ragged tails
+    (3, [1, 2, 3], 192, 64, "geglu_tanh"),                # tiny segments, K not a multiple of 64*4
+    (2, [1000, 24], 2816, 704, "geglu_tanh"),             # Gemma widths: ragged column tile
+    (8, [0, 0, 0, 513, 0, 0, 0, 0], 2048, 768, "swiglu"),  # one expert takes everything
+    (1, [77], 72, 40, "swiglu"),                          # K < 64, N < 64
+])
+def test_grouped_ffn_parity(E, counts, D, I, act):
+    xp, offsets, W13, W2 = _grouped_case(E, counts, D, I, act, seed=E * 7 + D)
+    R = xp.shape[0]
+    T = R  # k = 1 view
+    cfg = moe.make_config(T, D, E, 1, I, act=act)
+    ws = _ws_for(cfg)
+    h = torch.empty((R, I), dtype=torch.bfloat16, device="cuda")
+    y = torch.empty((R, D), dtype=torch.bfloat16, device="cuda")
+    toff = torch.from_numpy(offsets).cuda()
+    moe.moe_grouped_ffn(cfg, xp, toff, W13, None, W2, None, h, y, ws=ws)
+    assert moe.moe_read_device_status(ws) == 0
+    h_o, y_o = oracle.grouped_ffn(oracle.to_f64(xp.cpu()), offsets, W13.cpu(), W2.cpu(), act)
+    eh = np.abs(h.cpu().double().numpy() - h_o).max()
+    ey = np.abs(y.cpu().double().numpy() - y_o).max()
+    assert eh <= 2e-2 * rms(h_o), f"h max err {eh:.3e} vs RMS {rms(h_o):.3e}"
+    assert ey <= 2e-2 * rms(y_o), f"y max err {ey:.3e} vs RMS {rms(y_o):.3e}"
+
+
+def test_grouped_ffn_flags_bad_offsets_without_fault():
+    E, D, I = 3, 128, 64
+    xp, offsets, W13, W2 = _grouped_case(E, [10, 10, 10], D, I, "swiglu", seed=3)
+    bad = torch.tensor([0, 20, 10, 30], dtype=torch.int32, device="cuda")  # not monotone
+    cfg = moe.make_config(30, D, E, 1, I)
+    ws = _ws_for(cfg)
+    h = torch.zeros((30, I), dtype=torch.bfloat16, device="cuda")
+    y = torch.zeros((30, D), dtype=torch.bfloat16, device="cuda")
+    moe.moe_grouped_ffn(cfg, xp, bad, W13, None, W2, None, h, y, ws=ws)
+    assert moe.moe_read_device_status(ws) & moe.MOE_DEV_BAD_OFFSETS
+
+
+@pytest.mark.parametrize("T,k,D,shared", [(513, 8, 2048, False), (64, 10, 4096, True), (3, 1, 264, True)])
+def test_finalize_parity(T, k, D, shared):
+    gen = torch.Generator(device="cuda").manual_seed(T + k)
+    R = T * k
+    y = torch.randn((R, D), generator=gen, device="cuda").to(torch.bfloat16)
+    perm = torch.randperm(R, generator=gen, device="cuda").to(torch.int32)
+    w = torch.rand((T, k), generator=gen, device="cuda")
+    w = w / w.sum(1, keepdim=True)
+    s = torch.randn((T, D), generator=gen, device="cuda").to(torch.bfloat16) if shared else None
+    out = torch.empty((T, D), dtype=torch.bfloat16, device="cuda")
+    cfg = moe.make_config(T, D, 16, k, 64)
+    ws = _ws_for(cfg)
+    moe.moe_finalize(cfg, y, perm, w, s, out, ws)
+    assert moe.moe_read_device_status(ws) == 0
+    ref = oracle.finalize(oracle.to_f64(y.cpu()), perm.cpu().numpy(), w.cpu().double().numpy(),
+                          None if s is None else oracle.to_f64(s.cpu()))
+    got = out.cpu().double().numpy()
+    # fp32 accumulation then one bf16 rounding: within one bf16 ulp of the exact sum
+    assert (np.abs(got - ref) <= np.abs(ref) * 2.0 ** -8 + 1e-5).all()
