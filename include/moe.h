@@ -26,10 +26,14 @@
  *   device error word, which moe_read_device_status() reads.
  * - Pointers must be 16-byte aligned and every row pitch a multiple of 16
  *   bytes, which makes D, I and I_shared multiples of 8 (16 for fp8 weights).
- * - Dtypes: act_dtype applies to x, W_g, the permuted rows, h, the expert
- *   outputs, the shared-expert output and out.  w_dtype applies to W13, W2 and
- *   the shared expert's weights.  Supported pairs: (F32, F32), (BF16, BF16),
- *   (BF16, FP8_E4M3).  Router logits and gate weights are always fp32.
+ * - Dtypes: act_dtype applies to x, W_g, the permuted rows and out.  w_dtype
+ *   applies to W13, W2 and the shared expert's weights.  Supported pairs:
+ *   (F32, F32), (BF16, BF16), (BF16, FP8_E4M3).  Router logits, gate weights,
+ *   the expert outputs y_perm and the shared-expert output are always fp32.
+ *   The intermediate h uses 4 bytes per element: fp32 for fp32 layers, and for
+ *   bf16 layers two bf16 planes [M, I] -- h_hi = bf16(h) followed by
+ *   h_lo = bf16(h - h_hi) -- which the down projection consumes as two bf16
+ *   tensor-core products, so that h keeps about 16 significant bits.
  */
 #ifndef MOE_GB300_H
 #define MOE_GB300_H
@@ -131,12 +135,13 @@ int moe_permute(const moe_config_t* cfg, const int32_t* topk_ids, const void* x,
  *   W13     [E, D, 2I] w_dtype: columns [0, I) gate, [I, 2I) up.
  *   s13     [E, 2I] fp32 per-column scales (fp8 only, else NULL).
  *   W2      [E, I, D] w_dtype;   s2 [E, D] fp32 (fp8 only, else NULL).
- *   h       [T*k, I] act_dtype out: act(gate) * up.
- *   y_perm  [T*k, D] act_dtype out: h W2 per segment.
+ *   h       out: act(gate) * up, [T*k, I] fp32 (fp32 layers) or the bf16 pair
+ *           [2, T*k, I] (hi plane, then lo plane) for bf16 layers.
+ *   y_perm  [T*k, D] fp32 out: h W2 per segment (times s2 for fp8).
  *   x, W13s [D, 2*I_shared], s13s [2*I_shared], W2s [I_shared, D], s2s [D]:
  *           the shared expert; x NULL (or I_shared == 0) skips it.
- *   h_s     [T, I_shared] act_dtype out (shared intermediate).
- *   s_out   [T, D] act_dtype out: shared expert output. */
+ *   h_s     shared intermediate, same layout as h with T rows.
+ *   s_out   [T, D] fp32 out: shared expert output. */
 int moe_grouped_ffn(const moe_config_t* cfg, const void* x_perm, const int32_t* offsets,
                     const void* W13, const float* s13, const void* W2, const float* s2, void* h,
                     void* y_perm, const void* x, const void* W13s, const float* s13s,
@@ -150,8 +155,8 @@ int moe_grouped_ffn(const moe_config_t* cfg, const void* x_perm, const int32_t* 
  *   out[t] = round( sum_{j<k} w[t, j] * y_perm[dest[t*k + j]] + s[t] ),
  *   accumulated in fp32 with j ascending, the shared row added last, one
  *   rounding to act_dtype.
- *   y_perm [T*k, D], dest [T*k] int32, topk_w [T, k] fp32,
- *   s [T, D] act_dtype or NULL, out [T, D] act_dtype. */
+ *   y_perm [T*k, D] fp32, dest [T*k] int32, topk_w [T, k] fp32,
+ *   s [T, D] fp32 or NULL, out [T, D] act_dtype. */
 int moe_finalize(const moe_config_t* cfg, const void* y_perm, const int32_t* dest,
                  const float* topk_w, const void* s, void* out, void* ws, size_t ws_bytes,
                  void* stream);

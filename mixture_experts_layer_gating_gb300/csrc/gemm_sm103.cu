@@ -2,8 +2,10 @@
 // core (tcgen05 + TMEM), fed by TMA.
 //
 // What it computes (per group g with rows [start_g, start_g + cnt_g) of A):
-//   gate/up pass : acc = A_g [gate | up]; out = act(gate * s) * (up * s)
-//   store pass   : out = (A_g B_g) * s              (bf16 out)
+//   gate/up pass : acc = A_g [gate | up]; h = act(gate * s) * (up * s), stored
+//                  as a bf16 pair h_hi = bf16(h), h_lo = bf16(h - h_hi)
+//   down pass    : out = ((A_hi + A_lo)_g B_g) * s   (fp32 out; two MMAs per
+//                  K step so h keeps ~16 significant bits through the GEMM)
 //   router pass  : out = A B + bias                 (fp32 out, one group)
 // This is the grouped matmul of "CANN/cann-recipes-infer：Qwen3-MoE优化"
 // (section "GMM使能和Routing优化": one op computes every expert instead of a
@@ -16,13 +18,14 @@
 // (the Qwen3.5 page's dynamic bounded slices with minimal padding).
 //
 // Kernel structure (one persistent CTA per SM, 192 threads):
-//   warp 0      : TMA producer (one lane) -- A tile 128 x 64 (K-major) and
-//                 B tile 64 x 256 (N-major) per stage, 4-stage mbarrier ring.
+//   warp 0      : TMA producer (one lane) -- A tile 128 x 64 (K-major; two
+//                 of them, hi and lo, in the down pass) and B tile 64 x 256
+//                 (N-major) per stage, 4-stage (3 in the down pass) ring.
 //   warp 1      : TMEM allocator + single-lane tcgen05.mma issuer,
 //                 M=128 N=256 K=16 per instruction, fp32 accumulators in TMEM,
 //                 two accumulator buffers (2 x 256 columns).
 //   warps 2..5  : epilogue -- tcgen05.ld 32 lanes x 32 columns, activation /
-//                 scale, masked bf16 or fp32 stores; one row per thread.
+//                 scale, masked stores; one row per thread.
 // Tiles are ordered (group, column tile, row tile) so that the row tiles that
 // share a weight slice run at the same time and reuse it from L2.  The tile
 // schedule is built on the device from the group offsets, so no host
@@ -42,18 +45,25 @@ namespace {
 constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int BN_MAX = 256;
-constexpr int STAGES = 4;
 constexpr int A_TILE_BYTES = BM * BK * 2;    // 16 KB
 constexpr int B_BOX_BYTES = 64 * BK * 2;     // one 64-column x 64-row bf16 box, 8 KB
 constexpr int B_TILE_BYTES = BN_MAX * BK * 2; // 32 KB
+constexpr int MAX_STAGES = 4;
 constexpr int MAX_G = 512;
 constexpr int THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_STRIDE = 256;  // TMEM columns per accumulator buffer
 
+template <bool SPLIT>
+struct StageCfg {
+  static constexpr int kStages = SPLIT ? 3 : 4;
+  static constexpr int kABytes = (SPLIT ? 2 : 1) * A_TILE_BYTES;  // hi (+ lo) A tiles
+  static constexpr int kStageBytes = kABytes + B_TILE_BYTES;
+};
+
 struct Ctrl {
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
+  uint64_t full[MAX_STAGES];
+  uint64_t empty[MAX_STAGES];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint32_t tmem_slot;
@@ -63,8 +73,12 @@ struct Ctrl {
   int tile_start[MAX_G + 1];
 };
 
-constexpr size_t SMEM_BYTES = 1024 + STAGES * (A_TILE_BYTES + B_TILE_BYTES) + sizeof(Ctrl);
-static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+template <bool SPLIT>
+constexpr size_t smem_bytes() {
+  return 1024 + StageCfg<SPLIT>::kStages * StageCfg<SPLIT>::kStageBytes + sizeof(Ctrl);
+}
+static_assert(smem_bytes<false>() <= 227 * 1024, "shared memory budget");
+static_assert(smem_bytes<true>() <= 227 * 1024, "shared memory budget");
 
 struct KParams {
   const int32_t* group_offsets;
@@ -76,6 +90,7 @@ struct KParams {
   int bn;             // MMA N (accumulator columns per tile)
   int cols_per_tile;  // output columns per tile
   void* out;
+  void* out_lo;  // gate/up pass: h_lo
   const float* b_scale;
   const float* bias;
   int act;
@@ -117,16 +132,21 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-template <int EPI>
+template <int EPI, bool SPLIT>
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                        const __grid_constant__ CUtensorMap tmap_a_lo,
                         const __grid_constant__ CUtensorMap tmap_b, const KParams p) {
+  constexpr int STAGES = StageCfg<SPLIT>::kStages;
+  constexpr int STAGE_BYTES = StageCfg<SPLIT>::kStageBytes;
+  constexpr int A_BYTES = StageCfg<SPLIT>::kABytes;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* sa = base;
-  uint8_t* sb = base + STAGES * A_TILE_BYTES;
-  Ctrl* ctrl = reinterpret_cast<Ctrl*>(sb + STAGES * B_TILE_BYTES);
+  // stage s: [A hi | A lo (SPLIT) | B], every tile 1024-byte aligned
+  auto stage_a = [&](int st) { return base + st * STAGE_BYTES; };
+  auto stage_b = [&](int st) { return base + st * STAGE_BYTES + A_BYTES; };
+  Ctrl* ctrl = reinterpret_cast<Ctrl*>(base + STAGES * STAGE_BYTES);
   volatile int* abort_flag = &ctrl->abort;
 
   const int warp = threadIdx.x >> 5;
@@ -148,6 +168,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmap_a);
+    if (SPLIT) tma_prefetch_desc(&tmap_a_lo);
     tma_prefetch_desc(&tmap_b);
   }
   if (warp == 1) {
@@ -206,7 +227,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const uint64_t pol = l2_policy_evict_normal();
-      const uint32_t tx = A_TILE_BYTES + nbox * B_BOX_BYTES;
+      const uint32_t tx = A_BYTES + nbox * B_BOX_BYTES;
       uint32_t stage = 0, phase = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
@@ -217,9 +238,12 @@ __global__ void __launch_bounds__(THREADS, 1)
             break;
           }
           mbar_arrive_expect_tx(&ctrl->full[stage], tx);
-          uint8_t* a_dst = sa + stage * A_TILE_BYTES;
-          uint8_t* b_dst = sb + stage * B_TILE_BYTES;
+          uint8_t* a_dst = stage_a(stage);
+          uint8_t* b_dst = stage_b(stage);
           tma_load_2d(a_dst, &tmap_a, &ctrl->full[stage], kb * BK, ti.row0, pol);
+          if (SPLIT)
+            tma_load_2d(a_dst + A_TILE_BYTES, &tmap_a_lo, &ctrl->full[stage], kb * BK, ti.row0,
+                        pol);
           if (EPI == kEpiGateUpAct) {
             // gate columns n0..n0+127 into boxes 0,1; up columns into boxes 2,3
             for (int j = 0; j < 2; ++j) {
@@ -264,8 +288,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             break;
           }
           tc_fence_after_sync();
-          const uint32_t a_addr = smem_u32(sa + stage * A_TILE_BYTES);
-          const uint32_t b_addr = smem_u32(sb + stage * B_TILE_BYTES);
+          const uint32_t a_addr = smem_u32(stage_a(stage));
+          const uint32_t b_addr = smem_u32(stage_b(stage));
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             // A: K-major, 128-byte rows; a K step of 16 bf16 is 32 bytes.
@@ -273,6 +297,11 @@ __global__ void __launch_bounds__(THREADS, 1)
             // B: N-major, 64-column boxes 8 KB apart; a K step of 16 rows is 2 KB.
             const uint64_t bdesc = make_smem_desc_sw128(b_addr + kk * 2048, B_BOX_BYTES, 1024);
             tc_mma_f16(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0);
+            if (SPLIT) {
+              const uint64_t adesc_lo =
+                  make_smem_desc_sw128(a_addr + A_TILE_BYTES + kk * 32, 16, 1024);
+              tc_mma_f16(d_tmem, adesc_lo, bdesc, idesc, 1);
+            }
           }
           tc_commit(&ctrl->empty[stage]);
           if (++stage == STAGES) {
@@ -315,6 +344,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
       if (EPI == kEpiGateUpAct) {
         __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
+        __nv_bfloat16* out_lo = reinterpret_cast<__nv_bfloat16*>(p.out_lo);
         const float* sg = p.b_scale ? p.b_scale + static_cast<size_t>(ti.g) * 2 * p.N : nullptr;
 #pragma unroll 1
         for (int c = 0; c < 128; c += 32) {
@@ -328,10 +358,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int v = 0; v < 4; ++v) {
               const int cc = col + 8 * v;
               if (cc < p.N) {
-                uint32_t packed[4];
+                uint32_t packed[4], packed_lo[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                  float hv[2];
+                  float hv[2], lo[2];
 #pragma unroll
                   for (int h2 = 0; h2 < 2; ++h2) {
                     const int idx = 8 * v + 2 * i + h2;
@@ -342,49 +372,25 @@ __global__ void __launch_bounds__(THREADS, 1)
                       u *= sg[p.N + cc + 2 * i + h2];
                     }
                     const float a = (p.act == MOE_ACT_SWIGLU) ? silu_f(g) : gelu_tanh_f(g);
-                    hv[h2] = a * u;
+                    const float hf = a * u;
+                    hv[h2] = __bfloat162float(__float2bfloat16_rn(hf));
+                    lo[h2] = hf - hv[h2];  // exact in fp32
                   }
                   packed[i] = pack_bf16x2(hv[0], hv[1]);
+                  packed_lo[i] = pack_bf16x2(lo[0], lo[1]);
                 }
                 *reinterpret_cast<uint4*>(out + out_row * p.N + cc) =
                     make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                *reinterpret_cast<uint4*>(out_lo + out_row * p.N + cc) =
+                    make_uint4(packed_lo[0], packed_lo[1], packed_lo[2], packed_lo[3]);
               }
             }
           }
         }
-      } else if (EPI == kEpiStoreBf16) {
-        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
-        const float* sc = p.b_scale ? p.b_scale + static_cast<size_t>(ti.g) * p.N : nullptr;
-#pragma unroll 1
-        for (int c = 0; c < p.bn; c += 32) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(taddr + c, r);
-          tc_wait_ld();
-          const int col = ti.n0 + c;
-          if (valid) {
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              const int cc = col + 8 * v;
-              if (cc < p.N) {
-                uint32_t packed[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                  float a = __uint_as_float(r[8 * v + 2 * i]);
-                  float b = __uint_as_float(r[8 * v + 2 * i + 1]);
-                  if (sc) {
-                    a *= sc[cc + 2 * i];
-                    b *= sc[cc + 2 * i + 1];
-                  }
-                  packed[i] = pack_bf16x2(a, b);
-                }
-                *reinterpret_cast<uint4*>(out + out_row * p.N + cc) =
-                    make_uint4(packed[0], packed[1], packed[2], packed[3]);
-              }
-            }
-          }
-        }
-      } else {  // kEpiStoreF32
+      } else {  // kEpiStoreF32: (acc * scale[col]) + bias[col]
         float* out = reinterpret_cast<float*>(p.out);
+        const float* sc = p.b_scale ? p.b_scale + static_cast<size_t>(ti.g) * p.N : nullptr;
+        const bool vec = (p.N % 4) == 0;
 #pragma unroll 1
         for (int c = 0; c < p.bn; c += 32) {
           uint32_t r[32];
@@ -392,13 +398,25 @@ __global__ void __launch_bounds__(THREADS, 1)
           tc_wait_ld();
           const int col = ti.n0 + c;
           if (valid) {
+            float* orow = out + out_row * p.N;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const int cc = col + i;
-              if (cc < p.N) {
-                float v = __uint_as_float(r[i]);
-                if (p.bias) v += p.bias[cc];
-                out[out_row * p.N + cc] = v;
+            for (int q = 0; q < 8; ++q) {
+              const int cc = col + 4 * q;
+              float v[4];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                v[i] = __uint_as_float(r[4 * q + i]);
+                if (cc + i < p.N) {
+                  if (sc) v[i] *= sc[cc + i];
+                  if (p.bias) v[i] += p.bias[cc + i];
+                }
+              }
+              if (vec && cc + 4 <= p.N) {
+                *reinterpret_cast<float4*>(orow + cc) = make_float4(v[0], v[1], v[2], v[3]);
+              } else {
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                  if (cc + i < p.N) orow[cc + i] = v[i];
               }
             }
           }
@@ -458,18 +476,22 @@ bool encode_tmap(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims
   return r == CUDA_SUCCESS;
 }
 
-template <int EPI>
-cudaError_t launch_epi(const CUtensorMap& ta, const CUtensorMap& tb, const KParams& kp, int grid,
-                       cudaStream_t s) {
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(grouped_gemm_kernel<EPI>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(SMEM_BYTES));
-  });
-  if (attr_err != cudaSuccess) return attr_err;
-  grouped_gemm_kernel<EPI><<<grid, THREADS, SMEM_BYTES, s>>>(ta, tb, kp);
+template <int EPI, bool SPLIT>
+cudaError_t launch_epi(const CUtensorMap& ta, const CUtensorMap& ta_lo, const CUtensorMap& tb,
+                       const KParams& kp, int grid, cudaStream_t s) {
+  constexpr size_t smem = smem_bytes<SPLIT>();
+  // the attribute is per device: set it once for each device this process uses
+  static bool done[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !done[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI, SPLIT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) done[dev] = true;
+  }
+  grouped_gemm_kernel<EPI, SPLIT><<<grid, THREADS, smem, s>>>(ta, ta_lo, tb, kp);
   return cudaGetLastError();
 }
 
@@ -490,12 +512,14 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
   if (a.M <= 0) return cudaSuccess;
   if (a.b_fp8) return cudaErrorNotSupported;
   if (a.G < 1 || a.G > MAX_G) return cudaErrorInvalidValue;
-  CUtensorMap ta, tb;
+  CUtensorMap ta, ta_lo, tb;
   {
     const uint64_t dims[2] = {static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.M)};
     const uint64_t strides[1] = {static_cast<uint64_t>(a.K) * 2};
     const uint32_t box[2] = {BK, BM};
     if (!encode_tmap(&ta, a.A, 2, dims, strides, box)) return cudaErrorInvalidValue;
+    if (a.A_lo && !encode_tmap(&ta_lo, a.A_lo, 2, dims, strides, box)) return cudaErrorInvalidValue;
+    if (!a.A_lo) ta_lo = ta;
   }
   KParams kp;
   kp.group_offsets = a.group_offsets;
@@ -504,6 +528,7 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
   kp.K = a.K;
   kp.N = a.N;
   kp.out = a.out;
+  kp.out_lo = a.out_lo;
   kp.b_scale = a.b_scale;
   kp.bias = a.bias;
   kp.act = a.act;
@@ -528,12 +553,15 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
   const long long max_tiles =
       (static_cast<long long>((a.M + BM - 1) / BM) + a.G) * static_cast<long long>(kp.n_tiles);
   const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(device_sm_count(), max_tiles)));
-  switch (a.epilogue) {
-    case kEpiGateUpAct: return launch_epi<kEpiGateUpAct>(ta, tb, kp, grid, s);
-    case kEpiStoreBf16: return launch_epi<kEpiStoreBf16>(ta, tb, kp, grid, s);
-    case kEpiStoreF32: return launch_epi<kEpiStoreF32>(ta, tb, kp, grid, s);
-    default: return cudaErrorInvalidValue;
+  if (a.epilogue == kEpiGateUpAct) {
+    if (!a.out_lo || a.A_lo) return cudaErrorInvalidValue;
+    return launch_epi<kEpiGateUpAct, false>(ta, ta_lo, tb, kp, grid, s);
   }
+  if (a.epilogue == kEpiStoreF32) {
+    return a.A_lo ? launch_epi<kEpiStoreF32, true>(ta, ta_lo, tb, kp, grid, s)
+                  : launch_epi<kEpiStoreF32, false>(ta, ta_lo, tb, kp, grid, s);
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace moe

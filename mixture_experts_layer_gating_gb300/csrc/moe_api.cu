@@ -72,10 +72,10 @@ Layout make_layout(const moe_config_t* c) {
   L.off[MOE_WS_DEST] = take(R * 4);
   L.seg_scratch = take(E * static_cast<size_t>(route_segments(static_cast<long long>(R))) * 4 + 4);
   L.off[MOE_WS_X_PERM] = take(R * D * ab);
-  L.off[MOE_WS_H] = take(R * I * ab);
-  L.off[MOE_WS_Y_PERM] = take(R * D * ab);
-  L.off[MOE_WS_H_SHARED] = take(T * Is * ab);
-  L.off[MOE_WS_S] = take(T * D * ab);
+  L.off[MOE_WS_H] = take(R * I * 4);         // fp32, or bf16 (hi, lo) planes
+  L.off[MOE_WS_Y_PERM] = take(R * D * 4);    // fp32
+  L.off[MOE_WS_H_SHARED] = take(T * Is * 4);
+  L.off[MOE_WS_S] = take(T * D * 4);
   L.total = cur;
   return L;
 }
@@ -160,6 +160,8 @@ int do_ffn(const moe_config_t* c, const void* A, int M, const int32_t* offsets, 
                          static_cast<const float*>(W2), c->D, static_cast<float*>(y), err, s);
     return cuda_status(e);
   }
+  // h is two bf16 planes [M, I]: h_hi then h_lo (h ~= h_hi + h_lo)
+  void* h_lo = static_cast<uint8_t*>(h) + static_cast<size_t>(M) * I * 2;
   GroupedGemmArgs a{};
   a.epilogue = kEpiGateUpAct;
   a.A = A;
@@ -172,18 +174,21 @@ int do_ffn(const moe_config_t* c, const void* A, int M, const int32_t* offsets, 
   a.N = I;
   a.b_scale = s13;
   a.out = h;
+  a.out_lo = h_lo;
   a.act = c->act;
   a.err = err;
   e = launch_grouped_gemm(a, s);
   if (e != cudaSuccess) return e == cudaErrorNotSupported ? MOE_ERR_UNSUPPORTED : MOE_ERR_CUDA;
   GroupedGemmArgs b = a;
-  b.epilogue = kEpiStoreBf16;
+  b.epilogue = kEpiStoreF32;
   b.A = h;
+  b.A_lo = h_lo;
   b.K = I;
   b.B = W2;
   b.N = c->D;
   b.b_scale = s2;
   b.out = y;
+  b.out_lo = nullptr;
   trace_mark(s);
   e = launch_grouped_gemm(b, s);
   if (e != cudaSuccess) return e == cudaErrorNotSupported ? MOE_ERR_UNSUPPORTED : MOE_ERR_CUDA;

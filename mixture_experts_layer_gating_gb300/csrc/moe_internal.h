@@ -35,6 +35,7 @@ cudaError_t launch_init_routing(const int32_t* ids, int R, int E, int32_t* count
                                 int32_t* err, cudaStream_t s, void (*mark)(cudaStream_t) = nullptr);
 cudaError_t launch_permute_gather(const void* x, const int32_t* sorted_rows, int R, int k, int T,
                                   size_t row_bytes, void* x_perm, int32_t* err, cudaStream_t s);
+// y_perm and s_rows are fp32; out is act_dtype.
 cudaError_t launch_finalize(int act_dtype, const void* y_perm, const int32_t* dest, const float* w,
                             const void* s_rows, void* out, int T, int k, int D, int R,
                             int32_t* err, cudaStream_t s);
@@ -52,14 +53,14 @@ cudaError_t launch_simt_down(const float* h, const int32_t* offsets, int G, int 
 
 // ---------------------------------------------------------------- gemm_sm103.cu
 enum GemmEpilogue : int {
-  kEpiGateUpAct = 0,  // W13 pass: acc = [gate | up] -> act(gate) * up, bf16
-  kEpiStoreBf16 = 1,  // W2 pass: acc -> (scale) -> bf16
-  kEpiStoreF32 = 2,   // router: acc (+ bias) -> fp32
+  kEpiGateUpAct = 0,  // W13 pass: acc = [gate | up] -> act(gate) * up as a bf16 (hi, lo) pair
+  kEpiStoreF32 = 2,   // down pass / router: acc (* scale) (+ bias) -> fp32
 };
 
 struct GroupedGemmArgs {
   int epilogue;                  // GemmEpilogue
   const void* A;                 // [M, K] bf16, K contiguous
+  const void* A_lo;              // [M, K] bf16 low part of a split operand, or nullptr
   int M;                         // rows of A (and of the output)
   int K;
   const int32_t* group_offsets;  // [G+1] device, or nullptr for one group of M rows
@@ -69,7 +70,8 @@ struct GroupedGemmArgs {
   int N;                         // output columns (I for gate/up)
   const float* b_scale;          // [G, 2N] or [G, N] per-column scales (fp8), or nullptr
   const float* bias;             // [N] fp32 (router), or nullptr
-  void* out;                     // [M, N] bf16 or fp32
+  void* out;                     // [M, N] fp32, or bf16 h_hi (gate/up pass)
+  void* out_lo;                  // [M, N] bf16 h_lo (gate/up pass)
   int act;                       // moe_act_t (gate/up epilogue)
   int32_t* err;
 };

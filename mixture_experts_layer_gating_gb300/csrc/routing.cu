@@ -261,7 +261,8 @@ __global__ void permute_gather_kernel(const uint4* __restrict__ x,
 // finalize_routing ("CANN/cann-recipes-infer：Qwen3-MoE优化", section
 // "GMM使能和Routing优化") fused with the shared-expert add ("千问 3.5 MoE 在
 // TPU 上的系统优化实战": y = Router(x) + SharedExpert(x)).  One warp per
-// token; fp32 accumulation with j ascending, shared row last, one rounding.
+// token; fp32 expert rows and shared row, fp32 accumulation with j ascending,
+// shared row last, one rounding to the output type.
 __device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&f)[8]) {
   const uint4 u = *reinterpret_cast<const uint4*>(p);
   const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
@@ -291,8 +292,8 @@ __device__ __forceinline__ void store8(float* p, const float (&f)[8]) {
 }
 
 template <typename Tt>
-__global__ void finalize_kernel(const Tt* __restrict__ y_perm, const int32_t* __restrict__ dest,
-                                const float* __restrict__ w, const Tt* __restrict__ s_rows,
+__global__ void finalize_kernel(const float* __restrict__ y_perm, const int32_t* __restrict__ dest,
+                                const float* __restrict__ w, const float* __restrict__ s_rows,
                                 Tt* __restrict__ out, int T, int k, int D, int R, int32_t* err) {
   const int lane = threadIdx.x & 31;
   const long long wstride = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
@@ -402,16 +403,14 @@ cudaError_t launch_finalize(int act_dtype, const void* y_perm, const int32_t* de
   if (T <= 0) return cudaSuccess;
   const int threads = 256;
   const int blocks = blocks_for(T, threads / 32, device_sm_count() * 16);
-  if (act_dtype == MOE_BF16) {
+  const float* y = static_cast<const float*>(y_perm);
+  const float* sr = static_cast<const float*>(s_rows);
+  if (act_dtype == MOE_BF16)
     finalize_kernel<__nv_bfloat16><<<blocks, threads, 0, s>>>(
-        static_cast<const __nv_bfloat16*>(y_perm), dest, w,
-        static_cast<const __nv_bfloat16*>(s_rows), static_cast<__nv_bfloat16*>(out), T, k, D, R,
-        err);
-  } else {
-    finalize_kernel<float><<<blocks, threads, 0, s>>>(static_cast<const float*>(y_perm), dest, w,
-                                                      static_cast<const float*>(s_rows),
-                                                      static_cast<float*>(out), T, k, D, R, err);
-  }
+        y, dest, w, sr, static_cast<__nv_bfloat16*>(out), T, k, D, R, err);
+  else
+    finalize_kernel<float><<<blocks, threads, 0, s>>>(y, dest, w, sr, static_cast<float*>(out), T,
+                                                      k, D, R, err);
   return cudaGetLastError();
 }
 
