@@ -122,6 +122,31 @@ int moe_permute(const moe_config_t* cfg, const int32_t* topk_ids, const void* x,
                 int32_t* offsets, int32_t* sorted_rows, int32_t* dest, void* x_perm, void* ws,
                 size_t ws_bytes, void* stream);
 
+/* moe_permute for callers that cannot allocate device memory.  The source
+ * pages have no counterpart: this is an interface for hosts that hand an
+ * operator only its input and output buffers and forbid device allocation
+ * while a request runs (a serving runtime that plans all device memory at
+ * start-up, a plugin interface without a workspace argument), so they cannot
+ * provide the workspace moe_permute takes.
+ *   Same arguments and results as moe_permute, without ws / ws_bytes.  Its
+ *   scratch (the per-expert, per-1024-row-segment histogram) is a fixed
+ *   256 KiB array in the library's device memory, held on every GPU that
+ *   loads the library until the process exits.  Limit: E * ceil(T*k / 1024)
+ *   <= 65536 (e.g. E = 512 up to T*k = 131072); larger sizes return
+ *   MOE_ERR_INVALID_ARG before anything is enqueued.
+ *   The first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture.  Nothing is allocated or freed, by this call
+ *   or by any library routine it uses.
+ *   Every call shares the one array, and it keeps the last call's contents:
+ *   calls that overlap on the GPU (different streams, or different host
+ *   threads, without ordering between them) race on it.
+ *   There is no error word to read: a row with an id outside [0, E) gets
+ *   dest = -1, is left out of sorted_rows, and offsets[E] < T*k. */
+int moe_permute_noalloc(const moe_config_t* cfg, const int32_t* topk_ids, const void* x,
+                        int32_t* counts, int32_t* offsets, int32_t* sorted_rows, int32_t* dest,
+                        void* x_perm, void* stream);
+
 /* Grouped matmul over expert segments, with the gate/up activation epilogue,
  * plus the shared expert (or dense MLP) over all tokens.
  * Pages: "CANN/cann-recipes-infer：Qwen3-MoE优化", sections "MoE TP优化 /

@@ -60,6 +60,7 @@ _SIGS = {
     "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "moe_layer_launch_count": (ctypes.c_int, [ctypes.POINTER(MoEConfig)]),
     "moe_set_trace_events": (ctypes.c_int, [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]),
+    "moe_permute_noalloc": (ctypes.c_int, [ctypes.POINTER(MoEConfig)] + [_P] * 7 + [_P]),
 }
 
 
@@ -175,6 +176,15 @@ def moe_permute(cfg, topk_ids, x, counts, offsets, sorted_rows, dest, x_perm, ws
     _check("moe_permute", load_library().moe_permute(
         ctypes.byref(cfg), _ptr(topk_ids), _ptr(x), _ptr(counts), _ptr(offsets), _ptr(sorted_rows),
         _ptr(dest), _ptr(x_perm), wp, wb, _stream(stream)))
+
+
+def moe_permute_noalloc(cfg, topk_ids, x, counts, offsets, sorted_rows, dest, x_perm, stream=None):
+    """moe_permute without a workspace, for callers that cannot allocate device
+    memory: its scratch is a fixed array inside the library (see include/moe.h
+    for the size limit and the rule that overlapping calls race)."""
+    _check("moe_permute_noalloc", load_library().moe_permute_noalloc(
+        ctypes.byref(cfg), _ptr(topk_ids), _ptr(x), _ptr(counts), _ptr(offsets), _ptr(sorted_rows),
+        _ptr(dest), _ptr(x_perm), _stream(stream)))
 
 
 def moe_grouped_ffn(cfg, x_perm, offsets, W13, s13, W2, s2, h, y_perm, x=None, W13s=None,
