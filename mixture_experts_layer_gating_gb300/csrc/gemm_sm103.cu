@@ -19,13 +19,17 @@
 //
 // Kernel structure (one persistent CTA per SM, 192 threads):
 //   warp 0      : TMA producer (one lane) -- A tile 128 x 64 (K-major; two
-//                 of them, hi and lo, in the down pass) and B tile 64 x 256
-//                 (N-major) per stage, 4-stage (3 in the down pass) ring.
+//                 of them, hi and lo, in the bf16 down pass) and B tile 64 x 256
+//                 (N-major) per stage, 4-stage (3 in the split / fp8 passes) ring.
 //   warp 1      : TMEM allocator + single-lane tcgen05.mma issuer,
 //                 M=128 N=256 K=16 per instruction, fp32 accumulators in TMEM,
 //                 two accumulator buffers (2 x 256 columns).
 //   warps 2..5  : epilogue -- tcgen05.ld 32 lanes x 32 columns, activation /
 //                 scale, masked stores; one row per thread.
+//   warps 6..9  : (fp8 weights only) converters -- TMA brings the raw e4m3
+//                 weight boxes; these warps expand them exactly to bf16 in the
+//                 swizzled N-major layout the MMA reads, then arrive on the
+//                 stage's full barrier (W8A16: activations stay bf16).
 // Tiles are ordered (group, column tile, row tile) so that the row tiles that
 // share a weight slice run at the same time and reuse it from L2.  The tile
 // schedule is built on the device from the group offsets, so no host
@@ -50,20 +54,27 @@ constexpr int B_BOX_BYTES = 64 * BK * 2;     // one 64-column x 64-row bf16 box,
 constexpr int B_TILE_BYTES = BN_MAX * BK * 2; // 32 KB
 constexpr int MAX_STAGES = 4;
 constexpr int MAX_G = 512;
-constexpr int THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_STRIDE = 256;  // TMEM columns per accumulator buffer
 
-template <bool SPLIT>
+constexpr int RAW_BOX_BYTES = 128 * BK;        // one 128-column x 64-row e4m3 box, 8 KB
+constexpr int RAW_TILE_BYTES = 2 * RAW_BOX_BYTES;
+
+template <bool SPLIT, bool FP8>
 struct StageCfg {
-  static constexpr int kStages = SPLIT ? 3 : 4;
+  static_assert(!(SPLIT && FP8), "fp8 layers use an unsplit h");
+  static constexpr int kStages = (SPLIT || FP8) ? 3 : 4;
   static constexpr int kABytes = (SPLIT ? 2 : 1) * A_TILE_BYTES;  // hi (+ lo) A tiles
-  static constexpr int kStageBytes = kABytes + B_TILE_BYTES;
+  static constexpr int kRawBytes = FP8 ? RAW_TILE_BYTES : 0;
+  // stage layout: [A (+ A lo) | B (bf16, MMA operand) | raw e4m3 B]
+  static constexpr int kStageBytes = kABytes + B_TILE_BYTES + kRawBytes;
+  static constexpr int kThreads = FP8 ? 320 : 192;
 };
 
 struct Ctrl {
   uint64_t full[MAX_STAGES];
   uint64_t empty[MAX_STAGES];
+  uint64_t raw_full[MAX_STAGES];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint32_t tmem_slot;
@@ -73,12 +84,13 @@ struct Ctrl {
   int tile_start[MAX_G + 1];
 };
 
-template <bool SPLIT>
+template <bool SPLIT, bool FP8>
 constexpr size_t smem_bytes() {
-  return 1024 + StageCfg<SPLIT>::kStages * StageCfg<SPLIT>::kStageBytes + sizeof(Ctrl);
+  return 1024 + StageCfg<SPLIT, FP8>::kStages * StageCfg<SPLIT, FP8>::kStageBytes + sizeof(Ctrl);
 }
-static_assert(smem_bytes<false>() <= 227 * 1024, "shared memory budget");
-static_assert(smem_bytes<true>() <= 227 * 1024, "shared memory budget");
+static_assert(smem_bytes<false, false>() <= 227 * 1024, "shared memory budget");
+static_assert(smem_bytes<true, false>() <= 227 * 1024, "shared memory budget");
+static_assert(smem_bytes<false, true>() <= 227 * 1024, "shared memory budget");
 
 struct KParams {
   const int32_t* group_offsets;
@@ -132,20 +144,39 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-template <int EPI, bool SPLIT>
-__global__ void __launch_bounds__(THREADS, 1)
+// Four e4m3 values (bytes of w, low byte first) to four bf16, exactly.
+// The e4m3 sign / exponent / mantissa bits are placed in an fp32 with the
+// exponent in the low bits of the fp32 exponent field: that fp32 equals the
+// e4m3 value times 2^-120 (an e4m3 subnormal becomes an fp32 subnormal), so one
+// multiplication by 2^120 (exact, subnormals kept: no flush-to-zero build
+// flag) gives the value; it has at most 4 significant bits, so the bf16
+// rounding is exact too.  The NaN encoding (S.1111.111) is not produced by
+// the saturating quantisation and is not handled.
+__device__ __forceinline__ uint2 e4m3x4_to_bf16x4(uint32_t w) {
+  float f[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t b = (w >> (8 * i)) & 0xFFu;
+    f[i] = __uint_as_float(((b & 0x80u) << 24) | ((b & 0x7Fu) << 20)) * 0x1p120f;
+  }
+  return make_uint2(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]));
+}
+
+template <int EPI, bool SPLIT, bool FP8>
+__global__ void __launch_bounds__(StageCfg<SPLIT, FP8>::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                         const __grid_constant__ CUtensorMap tmap_a_lo,
                         const __grid_constant__ CUtensorMap tmap_b, const KParams p) {
-  constexpr int STAGES = StageCfg<SPLIT>::kStages;
-  constexpr int STAGE_BYTES = StageCfg<SPLIT>::kStageBytes;
-  constexpr int A_BYTES = StageCfg<SPLIT>::kABytes;
+  constexpr int STAGES = StageCfg<SPLIT, FP8>::kStages;
+  constexpr int STAGE_BYTES = StageCfg<SPLIT, FP8>::kStageBytes;
+  constexpr int A_BYTES = StageCfg<SPLIT, FP8>::kABytes;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   // stage s: [A hi | A lo (SPLIT) | B], every tile 1024-byte aligned
   auto stage_a = [&](int st) { return base + st * STAGE_BYTES; };
   auto stage_b = [&](int st) { return base + st * STAGE_BYTES + A_BYTES; };
+  auto stage_raw = [&](int st) { return base + st * STAGE_BYTES + A_BYTES + B_TILE_BYTES; };
   Ctrl* ctrl = reinterpret_cast<Ctrl*>(base + STAGES * STAGE_BYTES);
   volatile int* abort_flag = &ctrl->abort;
 
@@ -156,8 +187,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   // ---------------------------------------------------------------- set-up
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&ctrl->full[s], 1);
+      // fp8: the stage is full once the A bytes landed and all 128 converter
+      // threads stored their part of the bf16 B tile
+      mbar_init(&ctrl->full[s], FP8 ? 1 + 128 : 1);
       mbar_init(&ctrl->empty[s], 1);
+      mbar_init(&ctrl->raw_full[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&ctrl->tfull[a], 1);
@@ -227,7 +261,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const uint64_t pol = l2_policy_evict_normal();
-      const uint32_t tx = A_BYTES + nbox * B_BOX_BYTES;
+      const uint32_t tx = FP8 ? A_BYTES : A_BYTES + nbox * B_BOX_BYTES;
+      const int nraw = (p.bn + 127) / 128;  // raw e4m3 boxes per stage (fp8)
       uint32_t stage = 0, phase = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
@@ -244,7 +279,19 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (SPLIT)
             tma_load_2d(a_dst + A_TILE_BYTES, &tmap_a_lo, &ctrl->full[stage], kb * BK, ti.row0,
                         pol);
-          if (EPI == kEpiGateUpAct) {
+          if (FP8) {
+            uint8_t* r_dst = stage_raw(stage);
+            mbar_arrive_expect_tx(&ctrl->raw_full[stage], nraw * RAW_BOX_BYTES);
+            if (EPI == kEpiGateUpAct) {
+              tma_load_4d(r_dst, &tmap_b, &ctrl->raw_full[stage], ti.n0, 0, kb * BK, ti.g, pol);
+              tma_load_4d(r_dst + RAW_BOX_BYTES, &tmap_b, &ctrl->raw_full[stage], ti.n0, 1,
+                          kb * BK, ti.g, pol);
+            } else {
+              for (int j = 0; j < nraw; ++j)
+                tma_load_3d(r_dst + j * RAW_BOX_BYTES, &tmap_b, &ctrl->raw_full[stage],
+                            ti.n0 + 128 * j, kb * BK, ti.g, pol);
+            }
+          } else if (EPI == kEpiGateUpAct) {
             // gate columns n0..n0+127 into boxes 0,1; up columns into boxes 2,3
             for (int j = 0; j < 2; ++j) {
               tma_load_4d(b_dst + j * B_BOX_BYTES, &tmap_b, &ctrl->full[stage], ti.n0 + 64 * j, 0,
@@ -322,6 +369,51 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
     }
     __syncwarp();
+  } else if (warp >= 6) {
+    // ------------------------------------------------------------ fp8 converters
+    if (FP8) {
+      const int tid = threadIdx.x - 6 * 32;  // 0..127
+      const int nraw = (p.bn + 127) / 128;
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(&ctrl->raw_full[stage], phase, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint8_t* raw = stage_raw(stage);
+          uint8_t* dst = stage_b(stage);
+          // raw box b: 64 rows x 128 bytes (128 e4m3 columns), 128-byte swizzled;
+          // each thread expands 16-byte raw chunks into two 16-byte bf16 chunks of
+          // the N-major bf16 boxes (64 columns each) the MMA descriptor reads.
+          for (int q = tid; q < nraw * 512; q += 128) {
+            const int b = q >> 9, r = (q >> 3) & 63, cc = q & 7;
+            const uint4 v = *reinterpret_cast<const uint4*>(raw + b * RAW_BOX_BYTES + r * 128 +
+                                                            ((cc ^ (r & 7)) << 4));
+            const uint2 o0 = e4m3x4_to_bf16x4(v.x), o1 = e4m3x4_to_bf16x4(v.y);
+            const uint2 o2 = e4m3x4_to_bf16x4(v.z), o3 = e4m3x4_to_bf16x4(v.w);
+            const int j = 2 * b + (cc >> 2);  // bf16 box
+            const int lc = 2 * (cc & 3);      // first logical 16-byte chunk in the row
+            uint8_t* row = dst + j * B_BOX_BYTES + r * 128;
+            *reinterpret_cast<uint4*>(row + ((lc ^ (r & 7)) << 4)) = make_uint4(o0.x, o0.y, o1.x, o1.y);
+            *reinterpret_cast<uint4*>(row + (((lc + 1) ^ (r & 7)) << 4)) =
+                make_uint4(o2.x, o2.y, o3.x, o3.y);
+          }
+          fence_proxy_async_smem();  // generic-proxy stores -> tensor core reads
+          mbar_arrive(&ctrl->full[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok && tid == 0) {
+        ctrl->abort = 1;
+        atomicOr(p.err, MOE_DEV_WAIT_TIMEOUT);
+      }
+    }
+    __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;  // TMEM lanes [32*quarter, 32*quarter + 32)
@@ -381,8 +473,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 *reinterpret_cast<uint4*>(out + out_row * p.N + cc) =
                     make_uint4(packed[0], packed[1], packed[2], packed[3]);
-                *reinterpret_cast<uint4*>(out_lo + out_row * p.N + cc) =
-                    make_uint4(packed_lo[0], packed_lo[1], packed_lo[2], packed_lo[3]);
+                if (out_lo)
+                  *reinterpret_cast<uint4*>(out_lo + out_row * p.N + cc) =
+                      make_uint4(packed_lo[0], packed_lo[1], packed_lo[2], packed_lo[3]);
               }
             }
           }
@@ -457,7 +550,8 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
 }
 
 bool encode_tmap(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims,
-                 const uint64_t* strides_bytes, const uint32_t* box) {
+                 const uint64_t* strides_bytes, const uint32_t* box,
+                 CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   auto fn = get_encode_fn();
   if (!fn) return false;
   cuuint64_t gd[5];
@@ -470,28 +564,29 @@ bool encode_tmap(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims
     es[i] = 1;
   }
   for (int i = 0; i < rank - 1; ++i) gs[i] = strides_bytes[i];
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), gd, gs, bx, es,
+  CUresult r = fn(m, dt, rank, const_cast<void*>(ptr), gd, gs, bx, es,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
-template <int EPI, bool SPLIT>
+template <int EPI, bool SPLIT, bool FP8>
 cudaError_t launch_epi(const CUtensorMap& ta, const CUtensorMap& ta_lo, const CUtensorMap& tb,
                        const KParams& kp, int grid, cudaStream_t s) {
-  constexpr size_t smem = smem_bytes<SPLIT>();
+  constexpr size_t smem = smem_bytes<SPLIT, FP8>();
+  constexpr int threads = StageCfg<SPLIT, FP8>::kThreads;
   // the attribute is per device: set it once for each device this process uses
   static bool done[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || !done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI, SPLIT>,
+    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI, SPLIT, FP8>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) done[dev] = true;
   }
-  grouped_gemm_kernel<EPI, SPLIT><<<grid, THREADS, smem, s>>>(ta, ta_lo, tb, kp);
+  grouped_gemm_kernel<EPI, SPLIT, FP8><<<grid, threads, smem, s>>>(ta, ta_lo, tb, kp);
   return cudaGetLastError();
 }
 
@@ -510,7 +605,7 @@ int device_sm_count() {
 
 cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
   if (a.M <= 0) return cudaSuccess;
-  if (a.b_fp8) return cudaErrorNotSupported;
+  if (a.b_fp8 && a.A_lo) return cudaErrorNotSupported;
   if (a.G < 1 || a.G > MAX_G) return cudaErrorInvalidValue;
   CUtensorMap ta, ta_lo, tb;
   {
@@ -534,19 +629,24 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
   kp.act = a.act;
   kp.err = a.err;
   const uint64_t N = static_cast<uint64_t>(a.N), K = static_cast<uint64_t>(a.K);
+  const uint64_t eb = a.b_fp8 ? 1 : 2;  // weight element bytes
+  const CUtensorMapDataType bdt =
+      a.b_fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const uint32_t box_n = a.b_fp8 ? 128 : 64;  // 128 bytes of columns either way
   if (a.epilogue == kEpiGateUpAct) {
     const uint64_t dims[4] = {N, 2, K, static_cast<uint64_t>(a.G)};
-    const uint64_t strides[3] = {N * 2, 2 * N * 2, K * 2 * N * 2};
-    const uint32_t box[4] = {64, 1, BK, 1};
-    if (!encode_tmap(&tb, a.B, 4, dims, strides, box)) return cudaErrorInvalidValue;
+    const uint64_t strides[3] = {N * eb, 2 * N * eb, K * 2 * N * eb};
+    const uint32_t box[4] = {box_n, 1, BK, 1};
+    if (!encode_tmap(&tb, a.B, 4, dims, strides, box, bdt)) return cudaErrorInvalidValue;
     kp.bn = 256;
     kp.cols_per_tile = 128;
   } else {
     const uint64_t dims[3] = {N, K, static_cast<uint64_t>(a.G)};
-    const uint64_t strides[2] = {N * 2, K * N * 2};
-    const uint32_t box[3] = {64, BK, 1};
-    if (!encode_tmap(&tb, a.B, 3, dims, strides, box)) return cudaErrorInvalidValue;
-    kp.bn = static_cast<int>(std::min<uint64_t>(BN_MAX, (N + 63) / 64 * 64));
+    const uint64_t strides[2] = {N * eb, K * N * eb};
+    const uint32_t box[3] = {box_n, BK, 1};
+    if (!encode_tmap(&tb, a.B, 3, dims, strides, box, bdt)) return cudaErrorInvalidValue;
+    const uint64_t gran = a.b_fp8 ? 128 : 64;
+    kp.bn = static_cast<int>(std::min<uint64_t>(BN_MAX, (N + gran - 1) / gran * gran));
     kp.cols_per_tile = kp.bn;
   }
   kp.n_tiles = (a.N + kp.cols_per_tile - 1) / kp.cols_per_tile;
@@ -554,12 +654,14 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
       (static_cast<long long>((a.M + BM - 1) / BM) + a.G) * static_cast<long long>(kp.n_tiles);
   const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(device_sm_count(), max_tiles)));
   if (a.epilogue == kEpiGateUpAct) {
-    if (!a.out_lo || a.A_lo) return cudaErrorInvalidValue;
-    return launch_epi<kEpiGateUpAct, false>(ta, ta_lo, tb, kp, grid, s);
+    if (a.A_lo) return cudaErrorInvalidValue;
+    return a.b_fp8 ? launch_epi<kEpiGateUpAct, false, true>(ta, ta_lo, tb, kp, grid, s)
+                   : launch_epi<kEpiGateUpAct, false, false>(ta, ta_lo, tb, kp, grid, s);
   }
   if (a.epilogue == kEpiStoreF32) {
-    return a.A_lo ? launch_epi<kEpiStoreF32, true>(ta, ta_lo, tb, kp, grid, s)
-                  : launch_epi<kEpiStoreF32, false>(ta, ta_lo, tb, kp, grid, s);
+    if (a.b_fp8) return launch_epi<kEpiStoreF32, false, true>(ta, ta_lo, tb, kp, grid, s);
+    return a.A_lo ? launch_epi<kEpiStoreF32, true, false>(ta, ta_lo, tb, kp, grid, s)
+                  : launch_epi<kEpiStoreF32, false, false>(ta, ta_lo, tb, kp, grid, s);
   }
   return cudaErrorInvalidValue;
 }

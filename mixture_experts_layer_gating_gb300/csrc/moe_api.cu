@@ -160,8 +160,11 @@ int do_ffn(const moe_config_t* c, const void* A, int M, const int32_t* offsets, 
                          static_cast<const float*>(W2), c->D, static_cast<float*>(y), err, s);
     return cuda_status(e);
   }
-  // h is two bf16 planes [M, I]: h_hi then h_lo (h ~= h_hi + h_lo)
-  void* h_lo = static_cast<uint8_t*>(h) + static_cast<size_t>(M) * I * 2;
+  // bf16 weights: h is two bf16 planes [M, I], h_hi then h_lo (h ~= h_hi + h_lo),
+  // and the down pass multiplies both.  fp8 weights (tolerance 6e-2 RMS): h is
+  // the hi plane alone.
+  const bool fp8 = c->w_dtype == MOE_FP8_E4M3;
+  void* h_lo = fp8 ? nullptr : static_cast<uint8_t*>(h) + static_cast<size_t>(M) * I * 2;
   GroupedGemmArgs a{};
   a.epilogue = kEpiGateUpAct;
   a.A = A;
@@ -170,7 +173,7 @@ int do_ffn(const moe_config_t* c, const void* A, int M, const int32_t* offsets, 
   a.group_offsets = offsets;
   a.G = G;
   a.B = W13;
-  a.b_fp8 = c->w_dtype == MOE_FP8_E4M3;
+  a.b_fp8 = fp8;
   a.N = I;
   a.b_scale = s13;
   a.out = h;

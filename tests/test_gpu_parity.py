@@ -104,6 +104,11 @@ LAYER_CASES = {
     "gemma4_T256": C["gemma4_prefill"].with_tokens(256),
     "gemma4_T8_decode": C["gemma4_decode"],
     "qwen35_T64": C["qwen35_decode64"],
+    "fp8_small_T300": workloads.MoEShape("fp8_small", 300, 512, 16, 4, 256, I_shared=256,
+                                         w_dtype="fp8_e4m3"),
+    "fp8_small_geglu_T77": workloads.MoEShape("fp8_small_geglu", 77, 384, 24, 3, 320, I_shared=128,
+                                              act=workloads.ACT_GEGLU_TANH, w_dtype="fp8_e4m3"),
+    "ling_T64": C["ling_decode"].with_tokens(64),
 }
 
 
@@ -210,15 +215,18 @@ def check_close(name, got, ref, rel, rms_slack):
                            f"{np.abs(got - ref).max():.3e} (RMS {rms(ref):.3e})")
 
 
-def _grouped_case(E, counts, D, I, act, seed):
+def _grouped_case(E, counts, D, I, act, seed, fp8=False):
     gen = torch.Generator(device="cuda").manual_seed(seed)
     R = int(sum(counts))
     offsets = np.zeros(E + 1, dtype=np.int32)
     offsets[1:] = np.cumsum(counts)
     xp = torch.randn((R, D), generator=gen, device="cuda").to(torch.bfloat16)
-    W13 = (torch.randn((E, D, 2 * I), generator=gen, device="cuda") * 0.02).to(torch.bfloat16)
-    W2 = (torch.randn((E, I, D), generator=gen, device="cuda") * 0.02).to(torch.bfloat16)
-    return xp, offsets, W13, W2
+    W13 = torch.randn((E, D, 2 * I), generator=gen, device="cuda") * 0.02
+    W2 = torch.randn((E, I, D), generator=gen, device="cuda") * 0.02
+    if fp8:
+        (W13, s13), (W2, s2) = workloads.quantize_fp8_per_column(W13), workloads.quantize_fp8_per_column(W2)
+        return xp, offsets, W13, W2, s13, s2
+    return xp, offsets, W13.to(torch.bfloat16), W2.to(torch.bfloat16)
 
 
 @pytest.mark.parametrize("E,counts,D,I,act", [
@@ -246,6 +254,29 @@ def test_grouped_ffn_parity(E, counts, D, I, act):
     check_close("h_hi+h_lo", (hc[0] + hc[1]).numpy(), h_o, 2.0 ** -15, 1e-4)
     # y is fp32: only fp32 accumulation differs from the exact value
     check_close("y", y.cpu().double().numpy(), y_o, 1e-4, 1e-4)
+
+
+@pytest.mark.parametrize("E,counts,D,I,act", [
+    (4, [300, 0, 129, 1], 256, 128, "swiglu"),
+    (2, [200, 57], 512, 384, "geglu_tanh"),   # column tile past I: zero-filled raw boxes
+    (3, [5, 140, 0], 128, 64, "swiglu"),      # N < 128: one partly filled raw box
+])
+def test_grouped_ffn_fp8_parity(E, counts, D, I, act):
+    """W8A16: e4m3 weights expanded exactly on chip, per-column scales after
+    the K reduction; h is a single bf16 plane for fp8 layers."""
+    xp, offsets, W13, W2, s13, s2 = _grouped_case(E, counts, D, I, act, seed=E + D + I, fp8=True)
+    R = xp.shape[0]
+    cfg = moe.make_config(R, D, E, 1, I, act=act, w_dtype="fp8_e4m3")
+    ws = _ws_for(cfg)
+    h = torch.empty((R, I), dtype=torch.bfloat16, device="cuda")
+    y = torch.empty((R, D), dtype=torch.float32, device="cuda")
+    moe.moe_grouped_ffn(cfg, xp, torch.from_numpy(offsets).cuda(), W13, s13, W2, s2, h, y, ws=ws)
+    assert moe.moe_read_device_status(ws) == 0
+    h_o, y_o = oracle.grouped_ffn(oracle.to_f64(xp.cpu()), offsets, W13.cpu(), W2.cpu(), act,
+                                  s13.cpu(), s2.cpu())
+    check_close("h", h.cpu().double().numpy(), h_o, 2.0 ** -8, 1e-4)
+    # y from a bf16 h: one bf16 rounding of h feeds the down projection
+    check_close("y", y.cpu().double().numpy(), y_o, 2.0 ** -7, 1e-2)
 
 
 def test_grouped_ffn_flags_bad_offsets_without_fault():
