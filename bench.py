@@ -280,7 +280,7 @@ def run_ours(args, world, rank, local):
 
     # ---- per-kernel durations (instrumented pass, same work, after the timed region)
     L = moe.moe_layer_launch_count(cfg)
-    names = ["router_gemm", "topk_softmax", "route_hist", "route_scan", "route_scatter",
+    names = ["router_gemm", "topk_softmax", "route_hist", "route_scan_scatter",
              "permute_gather", "w13_gate_up", "w2_down"]
     if shape.I_shared:
         names += ["shared_w13", "shared_w2"]

@@ -131,11 +131,11 @@ int moe_permute(const moe_config_t* cfg, const int32_t* topk_ids, const void* x,
  * start-up, a plugin interface without a workspace argument), so they cannot
  * provide the workspace moe_permute takes.
  *   Same arguments and results as moe_permute, without ws / ws_bytes.  Its
- *   scratch (the per-expert, per-1024-row-segment histogram) is a fixed
- *   256 KiB array in the library's device memory, held on every GPU that
- *   loads the library until the process exits.  Limit: E * ceil(T*k / 1024)
- *   <= 65536 (e.g. E = 512 up to T*k = 131072); larger sizes return
- *   MOE_ERR_INVALID_ARG before anything is enqueued.
+ *   scratch (one expert histogram per routing segment: E <= 512 experts times
+ *   at most 128 segments) is a fixed 256 KiB array in the library's device
+ *   memory, held on every GPU that loads the library until the process exits.
+ *   Limit: T*k <= 2^30 expanded rows, the same as every other call; larger
+ *   sizes return MOE_ERR_INVALID_ARG before anything is enqueued.
  *   The first call on each device looks up the array's device address
  *   (cudaGetSymbolAddress) with that device current; make that first call
  *   before any stream capture.  Nothing is allocated or freed, by this call

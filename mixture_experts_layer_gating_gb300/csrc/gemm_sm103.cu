@@ -106,6 +106,8 @@ struct KParams {
   const float* b_scale;
   const float* bias;
   int act;
+  int ksplit;  // K split into ksplit parts, each writing its own fp32 output plane
+  int kbs;     // k-blocks per split
   int32_t* err;
 };
 
@@ -145,21 +147,22 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 // Four e4m3 values (bytes of w, low byte first) to four bf16, exactly.
-// The e4m3 sign / exponent / mantissa bits are placed in an fp32 with the
-// exponent in the low bits of the fp32 exponent field: that fp32 equals the
-// e4m3 value times 2^-120 (an e4m3 subnormal becomes an fp32 subnormal), so one
-// multiplication by 2^120 (exact, subnormals kept: no flush-to-zero build
-// flag) gives the value; it has at most 4 significant bits, so the bf16
-// rounding is exact too.  The NaN encoding (S.1111.111) is not produced by
-// the saturating quantisation and is not handled.
+// Each byte's sign goes to the bf16 sign bit and its 4-bit exponent and 3-bit
+// mantissa to the low exponent bits and top mantissa bits: that bf16 equals
+// the e4m3 value times 2^-120 (an e4m3 subnormal becomes a bf16 subnormal).
+// One bf16x2 multiplication by 2^120 -- exact, bf16 arithmetic keeps
+// subnormal inputs -- gives the value.  The NaN encoding (S.1111.111) is not
+// produced by the saturating quantisation and is not handled.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t u /* [0, b1, 0, b0] */) {
+  const uint32_t bits = ((u << 8) & 0x80008000u) | ((u & 0x007F007Fu) << 4);
+  __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&bits);
+  const __nv_bfloat162 k = __floats2bfloat162_rn(0x1p120f, 0x1p120f);
+  v = __hmul2(v, k);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
 __device__ __forceinline__ uint2 e4m3x4_to_bf16x4(uint32_t w) {
-  float f[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint32_t b = (w >> (8 * i)) & 0xFFu;
-    f[i] = __uint_as_float(((b & 0x80u) << 24) | ((b & 0x7Fu) << 20)) * 0x1p120f;
-  }
-  return make_uint2(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]));
+  return make_uint2(e4m3x2_to_bf16x2(__byte_perm(w, 0u, 0x4140)),
+                    e4m3x2_to_bf16x2(__byte_perm(w, 0u, 0x4342)));
 }
 
 template <int EPI, bool SPLIT, bool FP8>
@@ -253,8 +256,13 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8>::kThreads, 1)
   tc_fence_after_sync();
 
   const uint32_t tmem_base = ctrl->tmem_slot;
-  const int total_tiles = ctrl->tile_start[G] * p.n_tiles;
+  const int total_tiles = ctrl->tile_start[G] * p.n_tiles * p.ksplit;
   const int KB = (p.K + BK - 1) / BK;
+  // work item t = (output tile t / ksplit, K split t % ksplit)
+  auto kb_range = [&](int t, int& kb0, int& kb1) {
+    kb0 = (t % p.ksplit) * p.kbs;
+    kb1 = min(KB, kb0 + p.kbs);
+  };
   const int nbox = p.bn / 64;
 
   if (warp == 0) {
@@ -266,8 +274,10 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8>::kThreads, 1)
       uint32_t stage = 0, phase = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
-        const TileInfo ti = decode_tile(ctrl, G, t, p.n_tiles, p.cols_per_tile);
-        for (int kb = 0; kb < KB; ++kb) {
+        const TileInfo ti = decode_tile(ctrl, G, t / p.ksplit, p.n_tiles, p.cols_per_tile);
+        int kb0, kb1;
+        kb_range(t, kb0, kb1);
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&ctrl->empty[stage], phase ^ 1u, abort_flag)) {
             ok = false;
             break;
@@ -329,7 +339,9 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8>::kThreads, 1)
         }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + acc * ACC_STRIDE;
-        for (int kb = 0; kb < KB; ++kb) {
+        int kb0, kb1;
+        kb_range(t, kb0, kb1);
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&ctrl->full[stage], phase, abort_flag)) {
             ok = false;
             break;
@@ -343,7 +355,7 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8>::kThreads, 1)
             const uint64_t adesc = make_smem_desc_sw128(a_addr + kk * 32, 16, 1024);
             // B: N-major, 64-column boxes 8 KB apart; a K step of 16 rows is 2 KB.
             const uint64_t bdesc = make_smem_desc_sw128(b_addr + kk * 2048, B_BOX_BYTES, 1024);
-            tc_mma_f16(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0);
+            tc_mma_f16(d_tmem, adesc, bdesc, idesc, ((kb - kb0) | kk) != 0);
             if (SPLIT) {
               const uint64_t adesc_lo =
                   make_smem_desc_sw128(a_addr + A_TILE_BYTES + kk * 32, 16, 1024);
@@ -377,7 +389,9 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8>::kThreads, 1)
       uint32_t stage = 0, phase = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
-        for (int kb = 0; kb < KB; ++kb) {
+        int kb0, kb1;
+        kb_range(t, kb0, kb1);
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&ctrl->raw_full[stage], phase, abort_flag)) {
             ok = false;
             break;
@@ -420,7 +434,8 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8>::kThreads, 1)
     const int row_in_tile = quarter * 32 + lane;
     uint32_t acc = 0, acc_phase = 0;
     for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
-      const TileInfo ti = decode_tile(ctrl, G, t, p.n_tiles, p.cols_per_tile);
+      const TileInfo ti = decode_tile(ctrl, G, t / p.ksplit, p.n_tiles, p.cols_per_tile);
+      const size_t plane = static_cast<size_t>(t % p.ksplit) * p.M * p.N;
       if (!mbar_wait(&ctrl->tfull[acc], acc_phase, abort_flag)) {
         if (lane == 0) {
           ctrl->abort = 1;
@@ -481,7 +496,7 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8>::kThreads, 1)
           }
         }
       } else {  // kEpiStoreF32: (acc * scale[col]) + bias[col]
-        float* out = reinterpret_cast<float*>(p.out);
+        float* out = reinterpret_cast<float*>(p.out) + plane;
         const float* sc = p.b_scale ? p.b_scale + static_cast<size_t>(ti.g) * p.N : nullptr;
         const bool vec = (p.N % 4) == 0;
 #pragma unroll 1
@@ -592,6 +607,16 @@ cudaError_t launch_epi(const CUtensorMap& ta, const CUtensorMap& ta_lo, const CU
 
 }  // namespace
 
+int router_k_split(int T, int E, int D) {
+  // aim for about 148 work items (the SM count of a GB300) without making a
+  // split shorter than 4 k-blocks; at most 8 partial planes
+  const int tiles = ((T + BM - 1) / BM) * ((E + BN_MAX - 1) / BN_MAX);
+  const int KB = (D + BK - 1) / BK;
+  int ks = std::max(1, std::min({8, 148 / std::max(1, tiles), KB / 4}));
+  const int kbs = (KB + ks - 1) / ks;
+  return (KB + kbs - 1) / kbs;
+}
+
 int device_sm_count() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 1;
@@ -628,6 +653,14 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
   kp.bias = a.bias;
   kp.act = a.act;
   kp.err = a.err;
+  {
+    const int KB = (a.K + BK - 1) / BK;
+    int ks = std::max(1, std::min(a.ksplit, KB));
+    if (a.epilogue != kEpiStoreF32) ks = 1;
+    kp.kbs = (KB + ks - 1) / ks;
+    kp.ksplit = (KB + kp.kbs - 1) / kp.kbs;  // no empty split
+    if (kp.ksplit != ks && a.ksplit > 1) return cudaErrorInvalidValue;
+  }
   const uint64_t N = static_cast<uint64_t>(a.N), K = static_cast<uint64_t>(a.K);
   const uint64_t eb = a.b_fp8 ? 1 : 2;  // weight element bytes
   const CUtensorMapDataType bdt =
@@ -650,8 +683,8 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
     kp.cols_per_tile = kp.bn;
   }
   kp.n_tiles = (a.N + kp.cols_per_tile - 1) / kp.cols_per_tile;
-  const long long max_tiles =
-      (static_cast<long long>((a.M + BM - 1) / BM) + a.G) * static_cast<long long>(kp.n_tiles);
+  const long long max_tiles = (static_cast<long long>((a.M + BM - 1) / BM) + a.G) *
+                              static_cast<long long>(kp.n_tiles) * kp.ksplit;
   const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(device_sm_count(), max_tiles)));
   if (a.epilogue == kEpiGateUpAct) {
     if (a.A_lo) return cudaErrorInvalidValue;

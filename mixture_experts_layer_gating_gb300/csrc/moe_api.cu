@@ -28,6 +28,7 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 struct Layout {
   size_t off[12];
+  size_t router_partials;  // split-K planes of the router projection (0 = none)
   size_t seg_scratch;
   size_t total;
 };
@@ -64,6 +65,10 @@ Layout make_layout(const moe_config_t* c) {
     return o;
   };
   L.off[MOE_WS_LOGITS] = take(T * E * 4);
+  {
+    const int ks = router_k_split(c->T, c->E, c->D);
+    L.router_partials = ks > 1 ? take(static_cast<size_t>(ks) * T * E * 4) : 0;
+  }
   L.off[MOE_WS_TOPK_IDS] = take(R * 4);
   L.off[MOE_WS_TOPK_W] = take(R * 4);
   L.off[MOE_WS_COUNTS] = take(E * 4);
@@ -98,15 +103,22 @@ int common_checks(const moe_config_t* cfg, void* ws, size_t ws_bytes) {
 }
 
 // ------------------------------------------------------------------ stages
+// `partials`: workspace room for the router's split-K planes (may be null when
+// the configuration does not split).
 int do_route(const moe_config_t* c, const void* x, const void* Wg, const float* bias,
-             float* logits, int32_t* ids, float* w, int32_t* err, cudaStream_t s) {
+             float* logits, int32_t* ids, float* w, float* partials, int32_t* err,
+             cudaStream_t s) {
   cudaError_t e = cudaSuccess;
+  const float* src = logits;
+  int nsplit = 1;
   if (x) {
     trace_mark(s);
     if (c->act_dtype == MOE_F32) {
       e = launch_simt_router(static_cast<const float*>(x), static_cast<const float*>(Wg), bias,
                              logits, c->T, c->D, c->E, s);
+      bias = nullptr;  // added by the projection
     } else {
+      nsplit = partials ? router_k_split(c->T, c->E, c->D) : 1;
       GroupedGemmArgs a{};
       a.epilogue = kEpiStoreF32;
       a.A = x;
@@ -116,15 +128,20 @@ int do_route(const moe_config_t* c, const void* x, const void* Wg, const float* 
       a.G = 1;
       a.B = Wg;
       a.N = c->E;
-      a.bias = bias;
-      a.out = logits;
+      a.bias = nullptr;  // added, after the split planes, by the top-k kernel
+      a.ksplit = nsplit;
+      a.out = nsplit > 1 ? partials : logits;
       a.err = err;
       e = launch_grouped_gemm(a, s);
+      src = nsplit > 1 ? partials : logits;
     }
     if (e != cudaSuccess) return MOE_ERR_CUDA;
+  } else {
+    bias = nullptr;
   }
   trace_mark(s);
-  return cuda_status(launch_topk_softmax(logits, c->T, c->E, c->k, c->renormalize, ids, w, err, s));
+  return cuda_status(launch_topk_softmax(src, nsplit, bias, logits, c->T, c->E, c->k,
+                                         c->renormalize, ids, w, err, s));
 }
 
 int do_permute(const moe_config_t* c, const int32_t* ids, const void* x, int32_t* counts,
@@ -240,7 +257,9 @@ int moe_route(const moe_config_t* cfg, const void* x, const void* Wg, const floa
   if (!x && logit_bias) return MOE_ERR_INVALID_ARG;
   if (cfg->act_dtype == MOE_BF16 && x && (cfg->E % 8)) return MOE_ERR_INVALID_ARG;
   if (cfg->T == 0) return MOE_OK;
-  return do_route(cfg, x, Wg, logit_bias, logits, topk_ids, topk_w, err_word(ws),
+  const Layout L = make_layout(cfg);
+  float* partials = L.router_partials ? reinterpret_cast<float*>(ws_at(ws, L.router_partials)) : nullptr;
+  return do_route(cfg, x, Wg, logit_bias, logits, topk_ids, topk_w, partials, err_word(ws),
                   static_cast<cudaStream_t>(stream));
 }
 
@@ -329,7 +348,8 @@ int moe_layer(const moe_config_t* cfg, const void* x, const void* Wg, const floa
 
   const bool traced = g_trace_events && g_trace_n >= moe_layer_launch_count(cfg) + 1;
   g_trace_next = traced ? 0 : -1;
-  st = do_route(cfg, x, Wg, logit_bias, logits, ids, w, err, s);
+  float* partials = L.router_partials ? reinterpret_cast<float*>(ws_at(ws, L.router_partials)) : nullptr;
+  st = do_route(cfg, x, Wg, logit_bias, logits, ids, w, partials, err, s);
   if (st != MOE_OK) return (g_trace_next = -1, st);
   st = do_permute(cfg, ids, x, counts, offsets, sorted_rows, dest, x_perm, seg, err, s);
   if (st != MOE_OK) return (g_trace_next = -1, st);
@@ -380,7 +400,7 @@ int moe_layer_launch_count(const moe_config_t* cfg) {
   int n = 0;
   n += 1;  // router projection
   n += 1;  // top-k softmax
-  n += 3;  // histogram, scan, stable scatter
+  n += 2;  // histogram, scan + stable scatter
   n += 1;  // permutation gather
   n += 2;  // routed gate/up, down
   if (cfg->I_shared > 0) n += 2;  // shared gate/up, down

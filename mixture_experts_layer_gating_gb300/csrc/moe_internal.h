@@ -22,12 +22,28 @@ inline size_t act_bytes(int dt) { return dt == MOE_F32 ? 4 : 2; }
 inline size_t w_bytes(int dt) { return dt == MOE_F32 ? 4 : (dt == MOE_BF16 ? 2 : 1); }
 
 // ---------------------------------------------------------------- routing.cu
-// Segment size (expanded rows) handled by one warp of the stable scatter.
-constexpr int kRouteSeg = 1024;
-inline int route_segments(long long R) { return static_cast<int>((R + kRouteSeg - 1) / kRouteSeg); }
+// Expanded rows per init_routing segment: 512, raised for large R so that
+// there are at most 128 segments (each scatter block reads all segments'
+// histograms).
+inline int route_segment_rows(long long R) {
+  long long seg = 512;
+  while ((R + seg - 1) / seg > 128) seg *= 2;
+  return static_cast<int>(seg);
+}
+inline int route_segments(long long R) {
+  const int seg = route_segment_rows(R);
+  return static_cast<int>((R + seg - 1) / seg);
+}
 
-cudaError_t launch_topk_softmax(const float* logits, int T, int E, int k, int renorm, int32_t* ids,
-                                float* w, int32_t* err, cudaStream_t s);
+// Router logits = sum of nsplit fp32 partial planes [nsplit, T, E] (+ bias),
+// written to `logits` when nsplit > 1 or bias != nullptr; then top-k softmax.
+cudaError_t launch_topk_softmax(const float* partials, int nsplit, const float* bias, float* logits,
+                                int T, int E, int k, int renorm, int32_t* ids, float* w,
+                                int32_t* err, cudaStream_t s);
+
+// Split-K factor of the router projection (a pure function of the shape, so
+// the workspace size does not depend on the device).
+int router_k_split(int T, int E, int D);
 // `mark`, when not null, is called on the stream right before each of the
 // three launches (trace hook of moe_layer).
 cudaError_t launch_init_routing(const int32_t* ids, int R, int E, int32_t* counts, int32_t* offsets,
@@ -70,6 +86,7 @@ struct GroupedGemmArgs {
   int N;                         // output columns (I for gate/up)
   const float* b_scale;          // [G, 2N] or [G, N] per-column scales (fp8), or nullptr
   const float* bias;             // [N] fp32 (router), or nullptr
+  int ksplit;                    // >1: K split into planes out[s] = partial sums (fp32 store only)
   void* out;                     // [M, N] fp32, or bf16 h_hi (gate/up pass)
   void* out_lo;                  // [M, N] bf16 h_lo (gate/up pass)
   int act;                       // moe_act_t (gate/up epilogue)

@@ -22,8 +22,9 @@
 
 namespace {
 
-// Per-(expert, 1024-row segment) histogram entries the array holds.  One more
-// int at the front is the error word the routing kernels write to.
+// Per-(expert, routing segment) histogram entries the array holds: at most
+// 512 experts times 128 segments.  One more int at the front is the error word
+// the routing kernels write to.
 constexpr int kMaxScratchInts = 65536;
 
 static __device__ __align__(256) int32_t g_permute_scratch[1 + kMaxScratchInts];
@@ -61,7 +62,8 @@ extern "C" int moe_permute_noalloc(const moe_config_t* cfg, const int32_t* topk_
     return MOE_ERR_INVALID_ARG;
   const long long R = static_cast<long long>(cfg->T) * cfg->k;
   if (R > (1ll << 30)) return MOE_ERR_INVALID_ARG;
-  // the histogram needs E * ceil(R / 1024) entries; larger problems are refused
+  // the histogram needs E * route_segments(R) entries (never more than the
+  // array holds while R <= 2^30); the check stays as a guard
   if (static_cast<long long>(cfg->E) * moe::route_segments(R) > kMaxScratchInts)
     return MOE_ERR_INVALID_ARG;
   int32_t* scratch = scratch_on_current_device();

@@ -22,23 +22,43 @@ constexpr int kMaxTopK = 16;
 // One warp per token; lane l holds experts l, l+32, ... (E <= 512).  k rounds
 // of a warp arg-max with the order (higher logit, then lower index).  Weights:
 // softmax over the k chosen logits (renormalised) or full-softmax probabilities.
+// The router projection may arrive as nsplit fp32 partial planes [nsplit, T, E]
+// (split-K); they are summed in plane order, the bias added last, and the final
+// logits written to `logits` (which may alias plane 0).
 template <int EPL>
-__global__ void topk_softmax_kernel(const float* __restrict__ logits, int T, int E, int k,
-                                    int renorm, int32_t* __restrict__ ids, float* __restrict__ w,
-                                    int32_t* err) {
+__global__ void topk_softmax_kernel(const float* __restrict__ partials, int nsplit,
+                                    const float* __restrict__ bias, float* logits, int T, int E,
+                                    int k, int renorm, int32_t* __restrict__ ids,
+                                    float* __restrict__ w, int32_t* err) {
   const int warps_per_block = blockDim.x >> 5;
   const int lane = threadIdx.x & 31;
   const long long t = static_cast<long long>(blockIdx.x) * warps_per_block + (threadIdx.x >> 5);
   if (t >= T) return;
-  const float* row = logits + t * E;
+  const size_t plane = static_cast<size_t>(T) * E;
   float v[EPL];
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = e < E ? partials[t * E + e] : 0.0f;
+  }
+  // planes summed in order; each plane's loads are issued together
+  for (int sp = 1; sp < nsplit; ++sp) {
+    const float* pl = partials + sp * plane + t * E;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E) v[i] += pl[e];
+    }
+  }
   bool nonfinite = false;
 #pragma unroll
   for (int i = 0; i < EPL; ++i) {
     const int e = lane + 32 * i;
     float x = -INFINITY;
     if (e < E) {
-      x = row[e];
+      x = v[i];
+      if (bias) x += bias[e];
+      if (nsplit > 1 || bias) logits[t * E + e] = x;
       if (!isfinite(x)) {
         nonfinite = true;
         x = -INFINITY;
@@ -108,18 +128,24 @@ __global__ void topk_softmax_kernel(const float* __restrict__ logits, int T, int
 // ------------------------------------------------------------------------
 // init_routing ("CANN/cann-recipes-infer：Qwen3-MoE优化", section
 // "GMM使能和Routing优化": npu_moe_init_routing + npu_moe_compute_expert_tokens).
-// A stable counting sort of the expanded rows r = t*k + j by expert id:
-//  1. per-segment histograms (segments of kRouteSeg rows),
-//  2. one exclusive scan over (expert, segment) in expert-major order,
-//  3. per-segment stable scatter: one warp walks its segment in order, 32 rows
-//     per step, ranking equal ids inside the step with __match_any_sync.
-__global__ void route_hist_kernel(const int32_t* __restrict__ ids, int R, int E, int nseg,
+// A stable counting sort of the expanded rows r = t*k + j by expert id, in two
+// kernels over segments of `seg` consecutive rows:
+//  1. route_hist_kernel: one block per segment writes its expert histogram
+//     seg_hist[s][e] (segment-major).
+//  2. route_scatter_kernel: one block per segment sums the histograms of all
+//     segments (counts), scans them over experts (offsets; block 0 publishes
+//     both), adds the histograms of earlier segments (its base position per
+//     expert), and scatters its rows in order: the segment is cut into one
+//     contiguous piece per warp, per-warp expert counts give each warp's start,
+//     and inside a warp equal ids of a 32-row step are ranked with
+//     __match_any_sync.  Rows with an id outside [0, E) are skipped (dest -1).
+__global__ void route_hist_kernel(const int32_t* __restrict__ ids, int R, int E, int seg,
                                   int32_t* __restrict__ seg_hist, int32_t* err) {
   extern __shared__ int32_t cnt[];
   for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
   __syncthreads();
   const int s = blockIdx.x;
-  const int r0 = s * kRouteSeg, r1 = min(R, r0 + kRouteSeg);
+  const int r0 = s * seg, r1 = min(R, r0 + seg);
   bool bad = false;
   for (int r = r0 + threadIdx.x; r < r1; r += blockDim.x) {
     const int e = ids[r];
@@ -127,95 +153,112 @@ __global__ void route_hist_kernel(const int32_t* __restrict__ ids, int R, int E,
     else atomicAdd(&cnt[e], 1);
   }
   if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(err, MOE_DEV_BAD_EXPERT_ID);
-  for (int e = threadIdx.x; e < E; e += blockDim.x) seg_hist[static_cast<size_t>(e) * nseg + s] = cnt[e];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) seg_hist[static_cast<size_t>(s) * E + e] = cnt[e];
 }
 
-// Single-block exclusive scan of seg_hist (expert-major, E*nseg entries) in
-// place, plus counts and offsets.
-__global__ void route_scan_kernel(int32_t* __restrict__ seg_hist, int E, int nseg,
-                                  int32_t* __restrict__ counts, int32_t* __restrict__ offsets) {
-  constexpr int ITEMS = 8;
-  __shared__ int32_t warp_sums[32];
-  __shared__ int32_t carry_s;
-  const int n = E * nseg;
-  const int chunk = blockDim.x * ITEMS;
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  if (threadIdx.x == 0) carry_s = 0;
-  __syncthreads();
-  for (int base = 0; base < n; base += chunk) {
-    int vals[ITEMS];
-    int local = 0;
-    const int i0 = base + threadIdx.x * ITEMS;
+constexpr int kScatterWarps = 8;
+
+__global__ void __launch_bounds__(kScatterWarps * 32)
+    route_scatter_kernel(const int32_t* __restrict__ ids, int R, int E, int seg, int nseg,
+                         const int32_t* __restrict__ seg_hist, int32_t* __restrict__ counts,
+                         int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_rows,
+                         int32_t* __restrict__ dest) {
+  extern __shared__ int32_t sm[];
+  int32_t* base = sm;                    // [E] first position of this segment's rows of e
+  int32_t* wcnt = sm + E;                // [kScatterWarps][E] per-warp counts, then starts
+  __shared__ int32_t warp_tot[32];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int s = blockIdx.x;
+  const int nthr = blockDim.x;
+
+  // (a) per expert: rows in earlier segments and in all segments
+  int tot_local[2], pre_local[2];  // E <= 512 and 256 threads: at most 2 experts per thread
+  const int per = (E + nthr - 1) / nthr;
 #pragma unroll
-    for (int i = 0; i < ITEMS; ++i) {
-      vals[i] = (i0 + i < n) ? seg_hist[i0 + i] : 0;
-      local += vals[i];
+  for (int i = 0; i < 2; ++i) {
+    if (i >= per) break;
+    const int e = threadIdx.x + i * nthr;
+    int pre = 0, tot = 0;
+    if (e < E) {
+      for (int q = 0; q < nseg; ++q) {
+        const int v = seg_hist[static_cast<size_t>(q) * E + e];
+        if (q < s) pre += v;
+        tot += v;
+      }
     }
-    int incl = local;
+    pre_local[i] = pre;
+    tot_local[i] = tot;
+  }
+  // (b) exclusive scan of tot over e (thread-major: e = tid + i * nthr)
+  //     done as a scan over the flattened order e = 0..E-1 with per = 1 or 2
+  //     items per thread; items are visited in e order by a two-pass scan.
+  int carry = 0;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    if (i >= per) break;
+    const int e = threadIdx.x + i * nthr;
+    const int v = (e < E) ? tot_local[i] : 0;
+    int incl = v;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
       const int y = __shfl_up_sync(FULL, incl, d);
       if (lane >= d) incl += y;
     }
-    if (lane == 31) warp_sums[wid] = incl;
+    if (lane == 31) warp_tot[wid] = incl;
     __syncthreads();
-    if (wid == 0) {
-      int ws = lane < nw ? warp_sums[lane] : 0;
-      int wi = ws;
-#pragma unroll
-      for (int d = 1; d < 32; d <<= 1) {
-        const int y = __shfl_up_sync(FULL, wi, d);
-        if (lane >= d) wi += y;
-      }
-      if (lane < nw) warp_sums[lane] = wi - ws;  // exclusive warp prefix
+    int wbase = 0, all = 0;
+    for (int w = 0; w < nthr / 32; ++w) {
+      const int t = warp_tot[w];
+      if (w < wid) wbase += t;
+      all += t;
     }
-    __syncthreads();
-    int run = carry_s + warp_sums[wid] + incl - local;
-#pragma unroll
-    for (int i = 0; i < ITEMS; ++i) {
-      if (i0 + i < n) {
-        const int idx = i0 + i;
-        const int e = idx / nseg;
-        if (idx % nseg == 0) offsets[e] = run;
-        seg_hist[idx] = run;
+    const int excl = carry + wbase + incl - v;
+    if (e < E) {
+      base[e] = excl + pre_local[i];
+      if (s == 0) {
+        counts[e] = v;
+        offsets[e] = excl;
       }
-      run += vals[i];
     }
-    __syncthreads();
-    if (threadIdx.x == blockDim.x - 1) carry_s = run;
+    carry += all;
     __syncthreads();
   }
-  if (threadIdx.x == 0) offsets[E] = carry_s;
-  __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    const int next = (e + 1 < E) ? seg_hist[static_cast<size_t>(e + 1) * nseg] : carry_s;
-    counts[e] = next - seg_hist[static_cast<size_t>(e) * nseg];
-  }
-}
+  if (s == 0 && threadIdx.x == 0) offsets[E] = carry;
 
-__global__ void route_scatter_kernel(const int32_t* __restrict__ ids, int R, int E, int nseg,
-                                     const int32_t* __restrict__ seg_base,
-                                     int32_t* __restrict__ sorted_rows, int32_t* __restrict__ dest) {
-  extern __shared__ int32_t run[];  // [warps_per_block][E]
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  const int s = blockIdx.x * (blockDim.x >> 5) + wid;
-  int32_t* my = run + wid * E;
-  for (int e = lane; e < E; e += 32) my[e] = 0;
-  __syncwarp();
-  if (s >= nseg) return;
-  const int r0 = s * kRouteSeg, r1 = min(R, r0 + kRouteSeg);
+  // (c) per-warp counts inside this segment, then per-warp start positions
+  for (int i = threadIdx.x; i < kScatterWarps * E; i += nthr) wcnt[i] = 0;
+  __syncthreads();
+  const int r0 = s * seg, r1 = min(R, r0 + seg);
+  const int piece = (seg + kScatterWarps - 1) / kScatterWarps;
+  const int w0 = min(r1, r0 + wid * piece), w1 = min(r1, w0 + piece);
+  for (int r = w0 + lane; r < w1; r += 32) {
+    const int e = ids[r];
+    if (e >= 0 && e < E) atomicAdd(&wcnt[wid * E + e], 1);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += nthr) {
+    int run = base[e];
+    for (int w = 0; w < kScatterWarps; ++w) {
+      const int c = wcnt[w * E + e];
+      wcnt[w * E + e] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+
+  // (d) ordered scatter of each warp's piece
+  int32_t* my = wcnt + wid * E;
   const unsigned lt = (1u << lane) - 1u;
-  for (int rb = r0; rb < r1; rb += 32) {
+  for (int rb = w0; rb < w1; rb += 32) {
     const int r = rb + lane;
-    const bool in = r < r1;
-    int e = in ? ids[r] : -1;
+    const bool in = r < w1;
+    const int e = in ? ids[r] : -1;
     const bool valid = in && e >= 0 && e < E;
     if (in && !valid) dest[r] = -1;
     const int key = valid ? e : -1 - lane;  // invalid rows never match anything
     const unsigned peers = __match_any_sync(FULL, key);
     if (valid) {
-      const int rank = __popc(peers & lt);
-      const int pos = seg_base[static_cast<size_t>(e) * nseg + s] + my[e] + rank;
+      const int pos = my[e] + __popc(peers & lt);
       sorted_rows[pos] = r;
       dest[r] = pos;
     }
@@ -291,52 +334,70 @@ __device__ __forceinline__ void store8(float* p, const float (&f)[8]) {
   *reinterpret_cast<float4*>(p + 4) = make_float4(f[4], f[5], f[6], f[7]);
 }
 
-template <typename Tt>
+template <typename Tt, int KMAX>
 __global__ void finalize_kernel(const float* __restrict__ y_perm, const int32_t* __restrict__ dest,
                                 const float* __restrict__ w, const float* __restrict__ s_rows,
                                 Tt* __restrict__ out, int T, int k, int D, int R, int32_t* err) {
   const int lane = threadIdx.x & 31;
   const long long wstride = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
-  const int nchunk = D / 8;
+  const int nchunk = D / 8;  // 8 output elements per chunk
   for (long long t = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
        t < T; t += wstride) {
-    int my_p = -1;
+    // lanes < k fetch one (position, weight) pair each; a bad position is
+    // flagged and replaced by row 0 with weight 0 so every load stays in bounds
+    int my_p = 0;
     float my_w = 0.0f;
     if (lane < k) {
       my_p = dest[t * k + lane];
       my_w = w[t * k + lane];
       if (my_p < 0 || my_p >= R) {
         atomicOr(err, MOE_DEV_BAD_DEST);
-        my_p = -1;
+        my_p = 0;
+        my_w = 0.0f;
       }
     }
-    // every lane gets all k (position, weight) pairs before the chunk loop
-    int pj[kMaxTopK];
-    float wj[kMaxTopK];
+    int pj[KMAX];
+    float wj[KMAX];
 #pragma unroll
-    for (int j = 0; j < kMaxTopK; ++j) {
+    for (int j = 0; j < KMAX; ++j) {
       pj[j] = __shfl_sync(FULL, my_p, j);
       wj[j] = __shfl_sync(FULL, my_w, j);
     }
     for (int c = lane; c < nchunk; c += 32) {
+      // issue all k row loads before any arithmetic so they are in flight together
+      float4 a[KMAX], b[KMAX];
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j) {
+        if (j < k) {
+          const float4* src = reinterpret_cast<const float4*>(y_perm + static_cast<long long>(pj[j]) * D) + 2 * c;
+          a[j] = __ldcs(src);
+          b[j] = __ldcs(src + 1);
+        }
+      }
+      float4 sa = make_float4(0.f, 0.f, 0.f, 0.f), sb = sa;
+      if (s_rows) {
+        const float4* src = reinterpret_cast<const float4*>(s_rows + t * D) + 2 * c;
+        sa = __ldcs(src);
+        sb = __ldcs(src + 1);
+      }
       float acc[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
 #pragma unroll
-      for (int j = 0; j < kMaxTopK; ++j) {
-        if (j < k && pj[j] >= 0) {
-          float f[8];
-          load8(y_perm + static_cast<long long>(pj[j]) * D + c * 8, f);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj[j], f[i], acc[i]);
+      for (int j = 0; j < KMAX; ++j) {
+        if (j < k) {
+          acc[0] = fmaf(wj[j], a[j].x, acc[0]);
+          acc[1] = fmaf(wj[j], a[j].y, acc[1]);
+          acc[2] = fmaf(wj[j], a[j].z, acc[2]);
+          acc[3] = fmaf(wj[j], a[j].w, acc[3]);
+          acc[4] = fmaf(wj[j], b[j].x, acc[4]);
+          acc[5] = fmaf(wj[j], b[j].y, acc[5]);
+          acc[6] = fmaf(wj[j], b[j].z, acc[6]);
+          acc[7] = fmaf(wj[j], b[j].w, acc[7]);
         }
       }
-      if (s_rows) {
-        float f[8];
-        load8(s_rows + t * D + c * 8, f);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] += f[i];
-      }
+      acc[0] += sa.x; acc[1] += sa.y; acc[2] += sa.z; acc[3] += sa.w;
+      acc[4] += sb.x; acc[5] += sb.y; acc[6] += sb.z; acc[7] += sb.w;
       store8(out + t * D + c * 8, acc);
     }
   }
@@ -351,18 +412,22 @@ int blocks_for(long long work_items, int per_block, int cap) {
 
 }  // namespace
 
-cudaError_t launch_topk_softmax(const float* logits, int T, int E, int k, int renorm, int32_t* ids,
-                                float* w, int32_t* err, cudaStream_t s) {
+cudaError_t launch_topk_softmax(const float* partials, int nsplit, const float* bias, float* logits,
+                                int T, int E, int k, int renorm, int32_t* ids, float* w,
+                                int32_t* err, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
   const int threads = 256, wpb = threads / 32;
   const int blocks = (T + wpb - 1) / wpb;
   const int epl = (E + 31) / 32;
   if (epl <= 4)
-    topk_softmax_kernel<4><<<blocks, threads, 0, s>>>(logits, T, E, k, renorm, ids, w, err);
+    topk_softmax_kernel<4><<<blocks, threads, 0, s>>>(partials, nsplit, bias, logits, T, E, k,
+                                                      renorm, ids, w, err);
   else if (epl <= 8)
-    topk_softmax_kernel<8><<<blocks, threads, 0, s>>>(logits, T, E, k, renorm, ids, w, err);
+    topk_softmax_kernel<8><<<blocks, threads, 0, s>>>(partials, nsplit, bias, logits, T, E, k,
+                                                      renorm, ids, w, err);
   else
-    topk_softmax_kernel<16><<<blocks, threads, 0, s>>>(logits, T, E, k, renorm, ids, w, err);
+    topk_softmax_kernel<16><<<blocks, threads, 0, s>>>(partials, nsplit, bias, logits, T, E, k,
+                                                       renorm, ids, w, err);
   return cudaGetLastError();
 }
 
@@ -374,15 +439,14 @@ cudaError_t launch_init_routing(const int32_t* ids, int R, int E, int32_t* count
     if (e != cudaSuccess) return e;
     return cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (E + 1), s);
   }
-  const int nseg = route_segments(R);
+  const int seg = route_segment_rows(R);
+  const int nseg = (R + seg - 1) / seg;
   if (mark) mark(s);
-  route_hist_kernel<<<nseg, 256, E * sizeof(int32_t), s>>>(ids, R, E, nseg, seg_scratch, err);
+  route_hist_kernel<<<nseg, 256, E * sizeof(int32_t), s>>>(ids, R, E, seg, seg_scratch, err);
   if (mark) mark(s);
-  route_scan_kernel<<<1, 1024, 0, s>>>(seg_scratch, E, nseg, counts, offsets);
-  const int wpb = 4;
-  if (mark) mark(s);
-  route_scatter_kernel<<<(nseg + wpb - 1) / wpb, 32 * wpb, wpb * E * sizeof(int32_t), s>>>(
-      ids, R, E, nseg, seg_scratch, sorted_rows, dest);
+  const size_t smem = (1 + kScatterWarps) * E * sizeof(int32_t);
+  route_scatter_kernel<<<nseg, kScatterWarps * 32, smem, s>>>(ids, R, E, seg, nseg, seg_scratch,
+                                                               counts, offsets, sorted_rows, dest);
   return cudaGetLastError();
 }
 
@@ -405,12 +469,21 @@ cudaError_t launch_finalize(int act_dtype, const void* y_perm, const int32_t* de
   const int blocks = blocks_for(T, threads / 32, device_sm_count() * 16);
   const float* y = static_cast<const float*>(y_perm);
   const float* sr = static_cast<const float*>(s_rows);
-  if (act_dtype == MOE_BF16)
-    finalize_kernel<__nv_bfloat16><<<blocks, threads, 0, s>>>(
-        y, dest, w, sr, static_cast<__nv_bfloat16*>(out), T, k, D, R, err);
-  else
-    finalize_kernel<float><<<blocks, threads, 0, s>>>(y, dest, w, sr, static_cast<float*>(out), T,
-                                                      k, D, R, err);
+#define MOE_FIN(KM)                                                                           \
+  do {                                                                                        \
+    if (act_dtype == MOE_BF16)                                                                \
+      finalize_kernel<__nv_bfloat16, KM><<<blocks, threads, 0, s>>>(                          \
+          y, dest, w, sr, static_cast<__nv_bfloat16*>(out), T, k, D, R, err);                 \
+    else                                                                                      \
+      finalize_kernel<float, KM><<<blocks, threads, 0, s>>>(y, dest, w, sr,                   \
+                                                            static_cast<float*>(out), T, k, D, R, err); \
+  } while (0)
+  if (k <= 2) MOE_FIN(2);
+  else if (k <= 4) MOE_FIN(4);
+  else if (k <= 8) MOE_FIN(8);
+  else if (k <= 10) MOE_FIN(10);
+  else MOE_FIN(16);
+#undef MOE_FIN
   return cudaGetLastError();
 }
 

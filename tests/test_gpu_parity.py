@@ -279,6 +279,47 @@ def test_grouped_ffn_fp8_parity(E, counts, D, I, act):
     check_close("y", y.cpu().double().numpy(), y_o, 2.0 ** -7, 1e-2)
 
 
+def test_fp8_weight_expansion_is_exact_including_subnormals():
+    """Weight codes drawn mostly from the e4m3 subnormal range (|q| < 2^-6):
+    a conversion that flushed them would zero whole outputs.  y is checked
+    against the GPU's own h times the dequantised W2 in fp64 (fp32-accumulation
+    tolerance), h against act(x W13) from the dequantised W13."""
+    E, D, I = 2, 256, 128
+    counts = [150, 90]
+    R = sum(counts)
+    gen = torch.Generator(device="cuda").manual_seed(11)
+    codes = torch.tensor([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=torch.uint8)
+    sub = torch.tensor([c for c in range(256) if (c & 0x78) == 0 and (c & 7) != 0], dtype=torch.uint8)
+
+    def draw(shape):
+        pick_sub = torch.rand(shape, generator=gen, device="cuda") < 0.8
+        a = sub.cuda()[torch.randint(0, len(sub), shape, generator=gen, device="cuda")]
+        b = codes.cuda()[torch.randint(0, len(codes), shape, generator=gen, device="cuda")]
+        return torch.where(pick_sub, a, b).view(torch.float8_e4m3fn)
+
+    W13, W2 = draw((E, D, 2 * I)), draw((E, I, D))
+    s13 = torch.rand((E, 2 * I), generator=gen, device="cuda") * 0.01 + 0.001
+    s2 = torch.rand((E, D), generator=gen, device="cuda") * 0.01 + 0.001
+    xp = torch.randn((R, D), generator=gen, device="cuda").to(torch.bfloat16)
+    offsets = np.array([0, counts[0], R], dtype=np.int32)
+    cfg = moe.make_config(R, D, E, 1, I, w_dtype="fp8_e4m3")
+    ws = _ws_for(cfg)
+    h = torch.empty((R, I), dtype=torch.bfloat16, device="cuda")
+    y = torch.empty((R, D), dtype=torch.float32, device="cuda")
+    moe.moe_grouped_ffn(cfg, xp, torch.from_numpy(offsets).cuda(), W13, s13, W2, s2, h, y, ws=ws)
+    assert moe.moe_read_device_status(ws) == 0
+    h_o, _ = oracle.grouped_ffn(oracle.to_f64(xp.cpu()), offsets, W13.cpu(), W2.cpu(), "swiglu",
+                                s13.cpu(), s2.cpu())
+    check_close("h", h.cpu().double().numpy(), h_o, 2.0 ** -8, 1e-4)
+    hg = h.cpu().double().numpy()
+    y_ref = np.zeros((R, D))
+    for e in range(E):
+        a, b = offsets[e], offsets[e + 1]
+        y_ref[a:b] = oracle.scaled_projection(hg[a:b], oracle.to_f64(W2[e].cpu()), oracle.to_f64(s2[e].cpu()))
+    check_close("y", y.cpu().double().numpy(), y_ref, 1e-5, 1e-5)
+    assert rms(y_ref) > 0
+
+
 def test_grouped_ffn_flags_bad_offsets_without_fault():
     E, D, I = 3, 128, 64
     xp, offsets, W13, W2 = _grouped_case(E, [10, 10, 10], D, I, "swiglu", seed=3)

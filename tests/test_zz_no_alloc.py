@@ -64,8 +64,8 @@ def test_noalloc_permute_matches_workspace_permute_twice():
 
 def test_noalloc_permute_rejects_sizes_beyond_its_scratch():
     ensure_library()
-    # E * ceil(T*k / 1024) must stay <= 65536
-    cfg = moe.make_config(20000, 64, 512, 8, 64)  # 512 * 157 segments > 65536
+    # at most 2^30 expanded rows
+    cfg = moe.make_config(1 << 28, 64, 512, 8, 64)  # T*k = 2^31
     d = torch.empty(1, dtype=torch.int32, device="cuda")
     with pytest.raises(moe.MoEError) as ei:
         moe.moe_permute_noalloc(cfg, d, None, d, d, d, d, None)
