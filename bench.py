@@ -201,8 +201,19 @@ def cpu_baseline(shape, inp_cpu, budget_s: float = 15.0):
 
 
 # ------------------------------------------------------------------ arms
-def run_reference(args, world, rank):
+def workload_shape(args):
+    import dataclasses
+
     shape = workloads.CONFIGS[args.workload]
+    if args.tokens:
+        shape = shape.with_tokens(args.tokens)
+    if args.experts:
+        shape = dataclasses.replace(shape, E=args.experts, name=f"{shape.name}@E{args.experts}")
+    return shape
+
+
+def run_reference(args, world, rank):
+    shape = workload_shape(args)
     if rank != 0:
         return
     inp = workloads.make_inputs(shape, seed=0, device="cpu") if not torch.cuda.is_available() else \
@@ -236,7 +247,9 @@ def run_ours(args, world, rank, local):
         _build.build()
     barrier(world)
     moe.load_library()
-    shape = workloads.CONFIGS[args.workload]
+    if args.pair_tiles:
+        moe.moe_set_option(moe.MOE_OPT_PAIR_TILES, 1)
+    shape = workload_shape(args)
     dev = torch.device("cuda", local)
     inp = workloads.make_inputs(shape, seed=rank, device=dev, weights_seed=0)
     cfg = moe.config_from_shape(shape)
@@ -280,8 +293,10 @@ def run_ours(args, world, rank, local):
 
     # ---- per-kernel durations (instrumented pass, same work, after the timed region)
     L = moe.moe_layer_launch_count(cfg)
-    names = ["router_gemm", "topk_softmax", "route_hist", "route_scan_scatter",
-             "permute_gather", "w13_gate_up", "w2_down"]
+    names = ["router_gemm", "topk_softmax"]
+    if shape.w_dtype == "fp8_e4m3":
+        names += ["x_to_fp16"]
+    names += ["route_hist", "route_scan_scatter", "permute_gather", "w13_gate_up", "w2_down"]
     if shape.I_shared:
         names += ["shared_w13", "shared_w2"]
     names += ["finalize"]
@@ -386,6 +401,12 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--ref-tokens", type=int, default=64)
+    ap.add_argument("--pair-tiles", action="store_true",
+                    help="grouped GEMMs on 2-CTA clusters (moe_set_option MOE_OPT_PAIR_TILES)")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="override T of the workload (smaller cases for profiling)")
+    ap.add_argument("--experts", type=int, default=None,
+                    help="override E of the workload (smaller cases for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

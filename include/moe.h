@@ -200,7 +200,8 @@ int moe_layer(const moe_config_t* cfg, const void* x, const void* Wg, const floa
 /* Device byte offsets inside `ws` where moe_layer keeps its intermediates,
  * for inspection (logits, ids, weights, counts, offsets, sorted_rows, dest,
  * x_perm, h, y_perm, h_s, s).  `which` is one of the MOE_WS_* indices;
- * returns (size_t)-1 for an unknown index or an invalid configuration. */
+ * returns (size_t)-1 for an unknown index, an invalid configuration, or an
+ * fp8-only region of a layer without fp8 weights. */
 #define MOE_WS_LOGITS 0
 #define MOE_WS_TOPK_IDS 1
 #define MOE_WS_TOPK_W 2
@@ -213,6 +214,12 @@ int moe_layer(const moe_config_t* cfg, const void* x, const void* Wg, const floa
 #define MOE_WS_Y_PERM 9
 #define MOE_WS_H_SHARED 10
 #define MOE_WS_S 11
+/* fp8-weight layers only (the fp16 tensor-core path): x as fp16 rows times
+ * exact powers of two [T, D], their inverse scales per token [T] and per
+ * permuted row [T*k] (fp32); for these layers MOE_WS_X_PERM holds fp16 rows. */
+#define MOE_WS_X16 12
+#define MOE_WS_TOK_INV 13
+#define MOE_WS_ROW_INV 14
 size_t moe_workspace_offset(const moe_config_t* cfg, int which);
 
 /* Synchronises `stream`, reads and clears the device error word of `ws`.
@@ -225,6 +232,16 @@ const char* moe_status_string(int status);
 
 /* Kernel launches one moe_layer call enqueues for this configuration. */
 int moe_layer_launch_count(const moe_config_t* cfg);
+
+/* Kernel-variant options (process-wide; set them from the thread that
+ * launches, between calls).  Returns the previous value, or
+ * MOE_ERR_INVALID_ARG for an unknown option.
+ *   MOE_OPT_PAIR_TILES: 1 = grouped GEMMs with a full 256-column B tile use
+ *   2-CTA clusters (tcgen05 cta_group::2, M = 256 rows per tile, each CTA
+ *   loading half of B); 0 (default) = one CTA per 128-row tile.  Results are
+ *   the same up to fp32 summation order. */
+#define MOE_OPT_PAIR_TILES 1
+int moe_set_option(int option, int value);
 
 /* Per-kernel timing hook (process-wide, off by default).  `events` holds
  * n_events cudaEvent_t handles created by the caller; while set, each

@@ -26,7 +26,7 @@ MOE_DEV_BAD_DEST = 0x4
 MOE_DEV_NONFINITE_LOGIT = 0x8
 MOE_DEV_WAIT_TIMEOUT = 0x10
 WS_SLOTS = ["logits", "topk_ids", "topk_w", "counts", "offsets", "sorted_rows", "dest",
-            "x_perm", "h", "y_perm", "h_shared", "s"]
+            "x_perm", "h", "y_perm", "h_shared", "s", "x16", "tok_inv", "row_inv"]
 
 _DTYPES = {"f32": MOE_F32, "bf16": MOE_BF16, "fp8_e4m3": MOE_FP8_E4M3}
 _ACTS = {"swiglu": MOE_ACT_SWIGLU, "geglu_tanh": MOE_ACT_GEGLU_TANH}
@@ -61,7 +61,9 @@ _SIGS = {
     "moe_layer_launch_count": (ctypes.c_int, [ctypes.POINTER(MoEConfig)]),
     "moe_set_trace_events": (ctypes.c_int, [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]),
     "moe_permute_noalloc": (ctypes.c_int, [ctypes.POINTER(MoEConfig)] + [_P] * 7 + [_P]),
+    "moe_set_option": (ctypes.c_int, [ctypes.c_int, ctypes.c_int]),
 }
+MOE_OPT_PAIR_TILES = 1
 
 
 def load_library(path: Optional[str] = None) -> ctypes.CDLL:
@@ -158,6 +160,14 @@ def moe_set_trace_events(events) -> None:
     arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
     moe_set_trace_events._keep = arr
     lib.moe_set_trace_events(arr, len(events))
+
+
+def moe_set_option(option: int, value: int) -> int:
+    """Set a kernel-variant option (e.g. MOE_OPT_PAIR_TILES); returns the old value."""
+    r = int(load_library().moe_set_option(option, value))
+    if r < 0:
+        raise MoEError("moe_set_option", r, moe_status_string(r))
+    return r
 
 
 def moe_status_string(status: int) -> str:

@@ -17,7 +17,10 @@
 // past its segment computes rows of the next segment and masks their stores
 // (the Qwen3.5 page's dynamic bounded slices with minimal padding).
 //
-// Kernel structure (one persistent CTA per SM, 192 threads):
+// Kernel structure (one persistent CTA per SM, 192 threads; or, in PAIR mode,
+// one persistent 2-CTA cluster per SM pair that computes M=256 row tiles with
+// tcgen05.mma.cta_group::2 -- each CTA loads its own 128 A rows and half of the
+// B columns, so per-SM operand traffic for a 256x256 tile drops by a third):
 //   warp 0      : TMA producer (one lane) -- A tile 128 x 64 (K-major; two
 //                 of them, hi and lo, in the bf16 down pass) and B tile 64 x 256
 //                 (N-major) per stage, 4-stage (3 in the split / fp8 passes) ring.
@@ -27,9 +30,14 @@
 //   warps 2..5  : epilogue -- tcgen05.ld 32 lanes x 32 columns, activation /
 //                 scale, masked stores; one row per thread.
 //   warps 6..9  : (fp8 weights only) converters -- TMA brings the raw e4m3
-//                 weight boxes; these warps expand them exactly to bf16 in the
-//                 swizzled N-major layout the MMA reads, then arrive on the
-//                 stage's full barrier (W8A16: activations stay bf16).
+//                 weight boxes; these warps expand them exactly to 16-bit
+//                 floats in the swizzled N-major layout the MMA reads, then
+//                 arrive on the stage's full barrier (W8A16).  The gate/up pass
+//                 runs on the fp16 kind: e4m3 -> fp16 is one hardware convert
+//                 per pair, and the activations arrive as fp16 rows carrying an
+//                 exact power-of-two row scale that the epilogue removes.  The
+//                 down pass keeps bf16 (h can leave fp16's range), with e4m3 ->
+//                 bf16 done by bit placement and one bf16x2 multiply.
 // Tiles are ordered (group, column tile, row tile) so that the row tiles that
 // share a weight slice run at the same time and reuse it from L2.  The tile
 // schedule is built on the device from the group offsets, so no host
@@ -52,7 +60,8 @@ constexpr int BN_MAX = 256;
 constexpr int A_TILE_BYTES = BM * BK * 2;    // 16 KB
 constexpr int B_BOX_BYTES = 64 * BK * 2;     // one 64-column x 64-row bf16 box, 8 KB
 constexpr int B_TILE_BYTES = BN_MAX * BK * 2; // 32 KB
-constexpr int MAX_STAGES = 4;
+constexpr int MAX_STAGES = 8;
+constexpr int STAGE_BUDGET = 200 * 1024;
 constexpr int MAX_G = 512;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_STRIDE = 256;  // TMEM columns per accumulator buffer
@@ -60,15 +69,19 @@ constexpr uint32_t ACC_STRIDE = 256;  // TMEM columns per accumulator buffer
 constexpr int RAW_BOX_BYTES = 128 * BK;        // one 128-column x 64-row e4m3 box, 8 KB
 constexpr int RAW_TILE_BYTES = 2 * RAW_BOX_BYTES;
 
-template <bool SPLIT, bool FP8>
+template <bool SPLIT, bool FP8, bool PAIR>
 struct StageCfg {
   static_assert(!(SPLIT && FP8), "fp8 layers use an unsplit h");
-  static constexpr int kStages = (SPLIT || FP8) ? 3 : 4;
   static constexpr int kABytes = (SPLIT ? 2 : 1) * A_TILE_BYTES;  // hi (+ lo) A tiles
-  static constexpr int kRawBytes = FP8 ? RAW_TILE_BYTES : 0;
+  // this CTA's share of the bf16 B tile (all 256 columns, or 128 in a pair)
+  static constexpr int kBBytes = PAIR ? B_TILE_BYTES / 2 : B_TILE_BYTES;
+  static constexpr int kRawBytes = FP8 ? (PAIR ? RAW_BOX_BYTES : RAW_TILE_BYTES) : 0;
   // stage layout: [A (+ A lo) | B (bf16, MMA operand) | raw e4m3 B]
-  static constexpr int kStageBytes = kABytes + B_TILE_BYTES + kRawBytes;
+  static constexpr int kStageBytes = kABytes + kBBytes + kRawBytes;
+  static constexpr int kStages =
+      STAGE_BUDGET / kStageBytes > MAX_STAGES ? MAX_STAGES : STAGE_BUDGET / kStageBytes;
   static constexpr int kThreads = FP8 ? 320 : 192;
+  static constexpr int kTileM = PAIR ? 2 * BM : BM;  // rows per scheduled tile
 };
 
 struct Ctrl {
@@ -84,13 +97,17 @@ struct Ctrl {
   int tile_start[MAX_G + 1];
 };
 
-template <bool SPLIT, bool FP8>
+template <bool SPLIT, bool FP8, bool PAIR>
 constexpr size_t smem_bytes() {
-  return 1024 + StageCfg<SPLIT, FP8>::kStages * StageCfg<SPLIT, FP8>::kStageBytes + sizeof(Ctrl);
+  return 1024 + StageCfg<SPLIT, FP8, PAIR>::kStages * StageCfg<SPLIT, FP8, PAIR>::kStageBytes +
+         sizeof(Ctrl);
 }
-static_assert(smem_bytes<false, false>() <= 227 * 1024, "shared memory budget");
-static_assert(smem_bytes<true, false>() <= 227 * 1024, "shared memory budget");
-static_assert(smem_bytes<false, true>() <= 227 * 1024, "shared memory budget");
+static_assert(smem_bytes<false, false, false>() <= 227 * 1024, "shared memory budget");
+static_assert(smem_bytes<true, false, false>() <= 227 * 1024, "shared memory budget");
+static_assert(smem_bytes<false, true, false>() <= 227 * 1024, "shared memory budget");
+static_assert(smem_bytes<false, false, true>() <= 227 * 1024, "shared memory budget");
+static_assert(smem_bytes<true, false, true>() <= 227 * 1024, "shared memory budget");
+static_assert(smem_bytes<false, true, true>() <= 227 * 1024, "shared memory budget");
 
 struct KParams {
   const int32_t* group_offsets;
@@ -105,6 +122,7 @@ struct KParams {
   void* out_lo;  // gate/up pass: h_lo
   const float* b_scale;
   const float* bias;
+  const float* a_row_scale;  // per-row factor on the accumulator (fp16 A rows), or nullptr
   int act;
   int ksplit;  // K split into ksplit parts, each writing its own fp32 output plane
   int kbs;     // k-blocks per split
@@ -115,6 +133,7 @@ struct TileInfo {
   int g, row0, rows, n0;
 };
 
+template <int TILE_M>
 __device__ __forceinline__ TileInfo decode_tile(const Ctrl* c, int G, int t, int n_tiles,
                                                 int cols_per_tile) {
   const int q = t / n_tiles;
@@ -129,8 +148,8 @@ __device__ __forceinline__ TileInfo decode_tile(const Ctrl* c, int G, int t, int
   const int local = t - c->tile_start[lo] * n_tiles;
   const int nt = local / mt_g;
   const int mt = local - nt * mt_g;
-  ti.row0 = c->grp_start[lo] + mt * BM;
-  ti.rows = min(BM, c->grp_cnt[lo] - mt * BM);
+  ti.row0 = c->grp_start[lo] + mt * TILE_M;
+  ti.rows = min(TILE_M, c->grp_cnt[lo] - mt * TILE_M);
   ti.n0 = nt * cols_per_tile;
   return ti;
 }
@@ -165,40 +184,63 @@ __device__ __forceinline__ uint2 e4m3x4_to_bf16x4(uint32_t w) {
                     e4m3x2_to_bf16x2(__byte_perm(w, 0u, 0x4342)));
 }
 
-template <int EPI, bool SPLIT, bool FP8>
-__global__ void __launch_bounds__(StageCfg<SPLIT, FP8>::kThreads, 1)
+// Four e4m3 values to four fp16 (exact: every e4m3 value is an fp16 value),
+// one hardware conversion per pair; element order is kept (low byte first).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
+  return r;
+}
+__device__ __forceinline__ uint2 e4m3x4_to_f16x4(uint32_t w) {
+  return make_uint2(e4m3x2_to_f16x2(static_cast<uint16_t>(w & 0xFFFFu)),
+                    e4m3x2_to_f16x2(static_cast<uint16_t>(w >> 16)));
+}
+
+template <int EPI, bool SPLIT, bool FP8, bool PAIR>
+__global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                         const __grid_constant__ CUtensorMap tmap_a_lo,
                         const __grid_constant__ CUtensorMap tmap_b, const KParams p) {
-  constexpr int STAGES = StageCfg<SPLIT, FP8>::kStages;
-  constexpr int STAGE_BYTES = StageCfg<SPLIT, FP8>::kStageBytes;
-  constexpr int A_BYTES = StageCfg<SPLIT, FP8>::kABytes;
+  using Cfg = StageCfg<SPLIT, FP8, PAIR>;
+  // fp8 gate/up pass: fp16 operands; everything else: bf16 operands
+  constexpr bool F16 = FP8 && EPI == kEpiGateUpAct;
+  constexpr int STAGES = Cfg::kStages;
+  constexpr int STAGE_BYTES = Cfg::kStageBytes;
+  constexpr int A_BYTES = Cfg::kABytes;
+  constexpr int TILE_M = Cfg::kTileM;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   // stage s: [A hi | A lo (SPLIT) | B], every tile 1024-byte aligned
   auto stage_a = [&](int st) { return base + st * STAGE_BYTES; };
   auto stage_b = [&](int st) { return base + st * STAGE_BYTES + A_BYTES; };
-  auto stage_raw = [&](int st) { return base + st * STAGE_BYTES + A_BYTES + B_TILE_BYTES; };
+  auto stage_raw = [&](int st) { return base + st * STAGE_BYTES + A_BYTES + Cfg::kBBytes; };
   Ctrl* ctrl = reinterpret_cast<Ctrl*>(base + STAGES * STAGE_BYTES);
   volatile int* abort_flag = &ctrl->abort;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int G = p.G;
+  // PAIR: rank 0 (the leader) issues the MMAs; both CTAs load, convert and drain.
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
+  const int work0 = PAIR ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
+  const int work_stride = PAIR ? static_cast<int>(nclusters_x()) : static_cast<int>(gridDim.x);
 
   // ---------------------------------------------------------------- set-up
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       // fp8: the stage is full once the A bytes landed and all 128 converter
       // threads stored their part of the bf16 B tile
-      mbar_init(&ctrl->full[s], FP8 ? 1 + 128 : 1);
+      // (one arrival per converter warp; in a pair both CTAs' converters and
+      // A loads report to the leader's barrier)
+      mbar_init(&ctrl->full[s], FP8 ? 1 + 4 * (PAIR ? 2 : 1) : 1);
       mbar_init(&ctrl->empty[s], 1);
       mbar_init(&ctrl->raw_full[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&ctrl->tfull[a], 1);
-      mbar_init(&ctrl->tempty[a], 128);
+      mbar_init(&ctrl->tempty[a], 128 * (PAIR ? 2 : 1));
     }
     ctrl->abort = 0;
     fence_mbarrier_init();
@@ -209,8 +251,13 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8>::kThreads, 1)
     tma_prefetch_desc(&tmap_b);
   }
   if (warp == 1) {
-    tmem_alloc(&ctrl->tmem_slot, TMEM_COLS);
-    tmem_relinquish();
+    if (PAIR) {  // collective over one warp of each CTA of the pair
+      tmem_alloc_pair(&ctrl->tmem_slot, TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(&ctrl->tmem_slot, TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   if (warp == 2) {
     // Row-tile schedule: tile_start[g] = sum_{g' < g} ceil(cnt_g' / BM).
@@ -234,7 +281,7 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8>::kThreads, 1)
       }
       ctrl->grp_start[g] = a;
       ctrl->grp_cnt[g] = b - a;
-      local += (b - a + BM - 1) / BM;
+      local += (b - a + TILE_M - 1) / TILE_M;
     }
     int incl = local;
 #pragma unroll
@@ -245,7 +292,7 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8>::kThreads, 1)
     int run = incl - local;
     for (int g = g0; g < g1; ++g) {
       ctrl->tile_start[g] = run;
-      run += (ctrl->grp_cnt[g] + BM - 1) / BM;
+      run += (ctrl->grp_cnt[g] + TILE_M - 1) / TILE_M;
     }
     const int total = __shfl_sync(0xffffffffu, incl, 31);
     if (lane == 0) ctrl->tile_start[G] = total;
@@ -253,6 +300,7 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8>::kThreads, 1)
   }
   tc_fence_before_sync();
   __syncthreads();
+  if (PAIR) cluster_sync();  // the peer's barriers exist before anyone signals them
   tc_fence_after_sync();
 
   const uint32_t tmem_base = ctrl->tmem_slot;
@@ -264,17 +312,22 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8>::kThreads, 1)
     kb1 = min(KB, kb0 + p.kbs);
   };
   const int nbox = p.bn / 64;
+  const int nbox_cta = PAIR ? nbox / 2 : nbox;  // bf16 B boxes this CTA loads
+  // barrier addresses in the leader CTA (cluster window) for the pair protocol
+  auto leader_bar = [&](uint64_t* bar) { return PAIR ? mapa_shared(bar, 0) : smem_u32(bar); };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const uint64_t pol = l2_policy_evict_normal();
-      const uint32_t tx = FP8 ? A_BYTES : A_BYTES + nbox * B_BOX_BYTES;
-      const int nraw = (p.bn + 127) / 128;  // raw e4m3 boxes per stage (fp8)
+      // bytes the (leader's) full barrier waits for: A (+ bf16 B) of every CTA
+      const uint32_t tx = (PAIR ? 2u : 1u) * (FP8 ? A_BYTES : A_BYTES + nbox_cta * B_BOX_BYTES);
+      const int nraw = PAIR ? 1 : (p.bn + 127) / 128;  // raw e4m3 boxes this CTA loads (fp8)
       uint32_t stage = 0, phase = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
-        const TileInfo ti = decode_tile(ctrl, G, t / p.ksplit, p.n_tiles, p.cols_per_tile);
+      for (int t = work0; t < total_tiles && ok; t += work_stride) {
+        const TileInfo ti = decode_tile<TILE_M>(ctrl, G, t / p.ksplit, p.n_tiles, p.cols_per_tile);
+        const int my_row0 = ti.row0 + static_cast<int>(rank) * BM;
         int kb0, kb1;
         kb_range(t, kb0, kb1);
         for (int kb = kb0; kb < kb1; ++kb) {
@@ -282,37 +335,64 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8>::kThreads, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&ctrl->full[stage], tx);
+          if (leader) mbar_arrive_expect_tx(&ctrl->full[stage], tx);
+          const uint32_t fbar = leader_bar(&ctrl->full[stage]);
           uint8_t* a_dst = stage_a(stage);
           uint8_t* b_dst = stage_b(stage);
-          tma_load_2d(a_dst, &tmap_a, &ctrl->full[stage], kb * BK, ti.row0, pol);
-          if (SPLIT)
-            tma_load_2d(a_dst + A_TILE_BYTES, &tmap_a_lo, &ctrl->full[stage], kb * BK, ti.row0,
-                        pol);
+          if (PAIR) {
+            tma_load_2d_pair(a_dst, &tmap_a, fbar, kb * BK, my_row0, pol);
+            if (SPLIT)
+              tma_load_2d_pair(a_dst + A_TILE_BYTES, &tmap_a_lo, fbar, kb * BK, my_row0, pol);
+          } else {
+            tma_load_2d(a_dst, &tmap_a, &ctrl->full[stage], kb * BK, my_row0, pol);
+            if (SPLIT)
+              tma_load_2d(a_dst + A_TILE_BYTES, &tmap_a_lo, &ctrl->full[stage], kb * BK, my_row0,
+                          pol);
+          }
           if (FP8) {
+            // raw e4m3 boxes land on this CTA's own barrier for its converters
             uint8_t* r_dst = stage_raw(stage);
             mbar_arrive_expect_tx(&ctrl->raw_full[stage], nraw * RAW_BOX_BYTES);
             if (EPI == kEpiGateUpAct) {
-              tma_load_4d(r_dst, &tmap_b, &ctrl->raw_full[stage], ti.n0, 0, kb * BK, ti.g, pol);
-              tma_load_4d(r_dst + RAW_BOX_BYTES, &tmap_b, &ctrl->raw_full[stage], ti.n0, 1,
-                          kb * BK, ti.g, pol);
+              if (PAIR) {  // rank 0: gate half, rank 1: up half
+                tma_load_4d(r_dst, &tmap_b, &ctrl->raw_full[stage], ti.n0, static_cast<int>(rank),
+                            kb * BK, ti.g, pol);
+              } else {
+                tma_load_4d(r_dst, &tmap_b, &ctrl->raw_full[stage], ti.n0, 0, kb * BK, ti.g, pol);
+                tma_load_4d(r_dst + RAW_BOX_BYTES, &tmap_b, &ctrl->raw_full[stage], ti.n0, 1,
+                            kb * BK, ti.g, pol);
+              }
             } else {
+              const int c0 = ti.n0 + (PAIR ? 128 * static_cast<int>(rank) : 0);
               for (int j = 0; j < nraw; ++j)
                 tma_load_3d(r_dst + j * RAW_BOX_BYTES, &tmap_b, &ctrl->raw_full[stage],
-                            ti.n0 + 128 * j, kb * BK, ti.g, pol);
+                            c0 + 128 * j, kb * BK, ti.g, pol);
             }
           } else if (EPI == kEpiGateUpAct) {
-            // gate columns n0..n0+127 into boxes 0,1; up columns into boxes 2,3
-            for (int j = 0; j < 2; ++j) {
-              tma_load_4d(b_dst + j * B_BOX_BYTES, &tmap_b, &ctrl->full[stage], ti.n0 + 64 * j, 0,
-                          kb * BK, ti.g, pol);
-              tma_load_4d(b_dst + (2 + j) * B_BOX_BYTES, &tmap_b, &ctrl->full[stage],
-                          ti.n0 + 64 * j, 1, kb * BK, ti.g, pol);
+            if (PAIR) {  // rank 0: gate columns n0..n0+127, rank 1: up columns
+              for (int j = 0; j < 2; ++j)
+                tma_load_4d_pair(b_dst + j * B_BOX_BYTES, &tmap_b, fbar, ti.n0 + 64 * j,
+                                 static_cast<int>(rank), kb * BK, ti.g, pol);
+            } else {
+              // gate columns n0..n0+127 into boxes 0,1; up columns into boxes 2,3
+              for (int j = 0; j < 2; ++j) {
+                tma_load_4d(b_dst + j * B_BOX_BYTES, &tmap_b, &ctrl->full[stage], ti.n0 + 64 * j,
+                            0, kb * BK, ti.g, pol);
+                tma_load_4d(b_dst + (2 + j) * B_BOX_BYTES, &tmap_b, &ctrl->full[stage],
+                            ti.n0 + 64 * j, 1, kb * BK, ti.g, pol);
+              }
             }
           } else {
-            for (int j = 0; j < nbox; ++j)
-              tma_load_3d(b_dst + j * B_BOX_BYTES, &tmap_b, &ctrl->full[stage], ti.n0 + 64 * j,
-                          kb * BK, ti.g, pol);
+            if (PAIR) {  // rank r: columns n0 + r*bn/2 ...
+              const int c0 = ti.n0 + static_cast<int>(rank) * 64 * nbox_cta;
+              for (int j = 0; j < nbox_cta; ++j)
+                tma_load_3d_pair(b_dst + j * B_BOX_BYTES, &tmap_b, fbar, c0 + 64 * j, kb * BK,
+                                 ti.g, pol);
+            } else {
+              for (int j = 0; j < nbox; ++j)
+                tma_load_3d(b_dst + j * B_BOX_BYTES, &tmap_b, &ctrl->full[stage], ti.n0 + 64 * j,
+                            kb * BK, ti.g, pol);
+            }
           }
           if (++stage == STAGES) {
             stage = 0;
@@ -328,11 +408,12 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8>::kThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t idesc = make_idesc_bf16_f32(BM, p.bn, 0, 1);
+    if (lane == 0 && leader) {
+      const uint32_t idesc = F16 ? make_idesc_f16_f32(TILE_M, p.bn, 0, 1)
+                                 : make_idesc_bf16_f32(TILE_M, p.bn, 0, 1);
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+      for (int t = work0; t < total_tiles && ok; t += work_stride) {
         if (!mbar_wait(&ctrl->tempty[acc], acc_phase ^ 1u, abort_flag)) {
           ok = false;
           break;
@@ -355,21 +436,25 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8>::kThreads, 1)
             const uint64_t adesc = make_smem_desc_sw128(a_addr + kk * 32, 16, 1024);
             // B: N-major, 64-column boxes 8 KB apart; a K step of 16 rows is 2 KB.
             const uint64_t bdesc = make_smem_desc_sw128(b_addr + kk * 2048, B_BOX_BYTES, 1024);
-            tc_mma_f16(d_tmem, adesc, bdesc, idesc, ((kb - kb0) | kk) != 0);
+            if (PAIR) tc_mma_f16_pair(d_tmem, adesc, bdesc, idesc, ((kb - kb0) | kk) != 0);
+            else tc_mma_f16(d_tmem, adesc, bdesc, idesc, ((kb - kb0) | kk) != 0);
             if (SPLIT) {
               const uint64_t adesc_lo =
                   make_smem_desc_sw128(a_addr + A_TILE_BYTES + kk * 32, 16, 1024);
-              tc_mma_f16(d_tmem, adesc_lo, bdesc, idesc, 1);
+              if (PAIR) tc_mma_f16_pair(d_tmem, adesc_lo, bdesc, idesc, 1);
+              else tc_mma_f16(d_tmem, adesc_lo, bdesc, idesc, 1);
             }
           }
-          tc_commit(&ctrl->empty[stage]);
+          if (PAIR) tc_commit_pair_multicast(&ctrl->empty[stage], 0x3);
+          else tc_commit(&ctrl->empty[stage]);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        tc_commit(&ctrl->tfull[acc]);
+        if (PAIR) tc_commit_pair_multicast(&ctrl->tfull[acc], 0x3);
+        else tc_commit(&ctrl->tfull[acc]);
         if (++acc == 2) {
           acc = 0;
           acc_phase ^= 1u;
@@ -385,10 +470,10 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8>::kThreads, 1)
     // ------------------------------------------------------------ fp8 converters
     if (FP8) {
       const int tid = threadIdx.x - 6 * 32;  // 0..127
-      const int nraw = (p.bn + 127) / 128;
+      const int nraw = PAIR ? 1 : (p.bn + 127) / 128;
       uint32_t stage = 0, phase = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+      for (int t = work0; t < total_tiles && ok; t += work_stride) {
         int kb0, kb1;
         kb_range(t, kb0, kb1);
         for (int kb = kb0; kb < kb1; ++kb) {
@@ -405,8 +490,18 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8>::kThreads, 1)
             const int b = q >> 9, r = (q >> 3) & 63, cc = q & 7;
             const uint4 v = *reinterpret_cast<const uint4*>(raw + b * RAW_BOX_BYTES + r * 128 +
                                                             ((cc ^ (r & 7)) << 4));
-            const uint2 o0 = e4m3x4_to_bf16x4(v.x), o1 = e4m3x4_to_bf16x4(v.y);
-            const uint2 o2 = e4m3x4_to_bf16x4(v.z), o3 = e4m3x4_to_bf16x4(v.w);
+            uint2 o0, o1, o2, o3;
+            if (F16) {
+              o0 = e4m3x4_to_f16x4(v.x);
+              o1 = e4m3x4_to_f16x4(v.y);
+              o2 = e4m3x4_to_f16x4(v.z);
+              o3 = e4m3x4_to_f16x4(v.w);
+            } else {
+              o0 = e4m3x4_to_bf16x4(v.x);
+              o1 = e4m3x4_to_bf16x4(v.y);
+              o2 = e4m3x4_to_bf16x4(v.z);
+              o3 = e4m3x4_to_bf16x4(v.w);
+            }
             const int j = 2 * b + (cc >> 2);  // bf16 box
             const int lc = 2 * (cc & 3);      // first logical 16-byte chunk in the row
             uint8_t* row = dst + j * B_BOX_BYTES + r * 128;
@@ -415,7 +510,11 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8>::kThreads, 1)
                 make_uint4(o2.x, o2.y, o3.x, o3.y);
           }
           fence_proxy_async_smem();  // generic-proxy stores -> tensor core reads
-          mbar_arrive(&ctrl->full[stage]);
+          __syncwarp();
+          if (lane == 0) {
+            if (PAIR) mbar_arrive_cluster(leader_bar(&ctrl->full[stage]));
+            else mbar_arrive(&ctrl->full[stage]);
+          }
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -433,8 +532,10 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8>::kThreads, 1)
     const int quarter = warp & 3;  // TMEM lanes [32*quarter, 32*quarter + 32)
     const int row_in_tile = quarter * 32 + lane;
     uint32_t acc = 0, acc_phase = 0;
-    for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
-      const TileInfo ti = decode_tile(ctrl, G, t / p.ksplit, p.n_tiles, p.cols_per_tile);
+    for (int t = work0; t < total_tiles; t += work_stride) {
+      TileInfo ti = decode_tile<TILE_M>(ctrl, G, t / p.ksplit, p.n_tiles, p.cols_per_tile);
+      ti.row0 += static_cast<int>(rank) * BM;  // this CTA's 128 rows of the tile
+      ti.rows -= static_cast<int>(rank) * BM;
       const size_t plane = static_cast<size_t>(t % p.ksplit) * p.M * p.N;
       if (!mbar_wait(&ctrl->tfull[acc], acc_phase, abort_flag)) {
         if (lane == 0) {
@@ -453,6 +554,7 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8>::kThreads, 1)
         __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
         __nv_bfloat16* out_lo = reinterpret_cast<__nv_bfloat16*>(p.out_lo);
         const float* sg = p.b_scale ? p.b_scale + static_cast<size_t>(ti.g) * 2 * p.N : nullptr;
+        const float rs = (p.a_row_scale && valid) ? p.a_row_scale[out_row] : 1.0f;
 #pragma unroll 1
         for (int c = 0; c < 128; c += 32) {
           uint32_t gr[32], ur[32];
@@ -472,8 +574,8 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8>::kThreads, 1)
 #pragma unroll
                   for (int h2 = 0; h2 < 2; ++h2) {
                     const int idx = 8 * v + 2 * i + h2;
-                    float g = __uint_as_float(gr[idx]);
-                    float u = __uint_as_float(ur[idx]);
+                    float g = __uint_as_float(gr[idx]) * rs;
+                    float u = __uint_as_float(ur[idx]) * rs;
                     if (sg) {
                       g *= sg[cc + 2 * i + h2];
                       u *= sg[p.N + cc + 2 * i + h2];
@@ -531,7 +633,8 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8>::kThreads, 1)
         }
       }
       tc_fence_before_sync();
-      mbar_arrive(&ctrl->tempty[acc]);
+      if (PAIR) mbar_arrive_cluster(leader_bar(&ctrl->tempty[acc]));
+      else mbar_arrive(&ctrl->tempty[acc]);
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1u;
@@ -543,9 +646,13 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8>::kThreads, 1)
   // ---------------------------------------------------------------- teardown
   tc_fence_before_sync();
   __syncthreads();
+  // a pair finishes together: the leader's MMAs read the peer's shared memory
+  // and the peer arrives on the leader's barriers
+  if (PAIR) cluster_sync();
   if (warp == 1) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    if (PAIR) tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    else tmem_dealloc(tmem_base, TMEM_COLS);
   }
 }
 
@@ -585,27 +692,61 @@ bool encode_tmap(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims
   return r == CUDA_SUCCESS;
 }
 
-template <int EPI, bool SPLIT, bool FP8>
+template <int EPI, bool SPLIT, bool FP8, bool PAIR>
 cudaError_t launch_epi(const CUtensorMap& ta, const CUtensorMap& ta_lo, const CUtensorMap& tb,
-                       const KParams& kp, int grid, cudaStream_t s) {
-  constexpr size_t smem = smem_bytes<SPLIT, FP8>();
-  constexpr int threads = StageCfg<SPLIT, FP8>::kThreads;
+                       const KParams& kp, long long max_tiles, cudaStream_t s) {
+  constexpr size_t smem = smem_bytes<SPLIT, FP8, PAIR>();
+  constexpr int threads = StageCfg<SPLIT, FP8, PAIR>::kThreads;
+  auto kern = grouped_gemm_kernel<EPI, SPLIT, FP8, PAIR>;
   // the attribute is per device: set it once for each device this process uses
   static bool done[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || !done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI, SPLIT, FP8>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) done[dev] = true;
   }
-  grouped_gemm_kernel<EPI, SPLIT, FP8><<<grid, threads, smem, s>>>(ta, ta_lo, tb, kp);
+  if (!PAIR) {
+    const int grid =
+        static_cast<int>(std::max<long long>(1, std::min<long long>(device_sm_count(), max_tiles)));
+    kern<<<grid, threads, smem, s>>>(ta, ta_lo, tb, kp);
+    return cudaGetLastError();
+  }
+  // one persistent 2-CTA cluster per SM pair that can hold one
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(threads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  static int max_clusters[64] = {0};
+  if (dev < 0 || dev >= 64 || max_clusters[dev] == 0) {
+    cfg.gridDim = dim3(2 * (device_sm_count() / 2), 1, 1);
+    int n = 0;
+    cudaError_t e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+    if (e != cudaSuccess || n < 1) n = device_sm_count() / 2;
+    if (dev >= 0 && dev < 64) max_clusters[dev] = n;
+    else max_clusters[0] = n;
+  }
+  const int nclu = static_cast<int>(std::max<long long>(
+      1, std::min<long long>(max_clusters[(dev >= 0 && dev < 64) ? dev : 0], max_tiles)));
+  cfg.gridDim = dim3(2 * nclu, 1, 1);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, ta_lo, tb, kp);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
 }  // namespace
+
+int g_pair_tiles = 0;  // set through moe_set_option(MOE_OPT_PAIR_TILES, .)
+bool pair_tiles_requested() { return g_pair_tiles != 0; }
 
 int router_k_split(int T, int E, int D) {
   // aim for about 148 work items (the SM count of a GB300) without making a
@@ -631,13 +772,17 @@ int device_sm_count() {
 cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
   if (a.M <= 0) return cudaSuccess;
   if (a.b_fp8 && a.A_lo) return cudaErrorNotSupported;
+  // fp16 A rows exactly when the gate/up pass has fp8 weights
+  if ((a.a_fp16 != 0) != (a.b_fp8 && a.epilogue == kEpiGateUpAct)) return cudaErrorInvalidValue;
   if (a.G < 1 || a.G > MAX_G) return cudaErrorInvalidValue;
   CUtensorMap ta, ta_lo, tb;
   {
     const uint64_t dims[2] = {static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.M)};
     const uint64_t strides[1] = {static_cast<uint64_t>(a.K) * 2};
     const uint32_t box[2] = {BK, BM};
-    if (!encode_tmap(&ta, a.A, 2, dims, strides, box)) return cudaErrorInvalidValue;
+    const CUtensorMapDataType adt =
+        a.a_fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    if (!encode_tmap(&ta, a.A, 2, dims, strides, box, adt)) return cudaErrorInvalidValue;
     if (a.A_lo && !encode_tmap(&ta_lo, a.A_lo, 2, dims, strides, box)) return cudaErrorInvalidValue;
     if (!a.A_lo) ta_lo = ta;
   }
@@ -651,6 +796,7 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
   kp.out_lo = a.out_lo;
   kp.b_scale = a.b_scale;
   kp.bias = a.bias;
+  kp.a_row_scale = a.a_row_scale;
   kp.act = a.act;
   kp.err = a.err;
   {
@@ -683,19 +829,26 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
     kp.cols_per_tile = kp.bn;
   }
   kp.n_tiles = (a.N + kp.cols_per_tile - 1) / kp.cols_per_tile;
-  const long long max_tiles = (static_cast<long long>((a.M + BM - 1) / BM) + a.G) *
+  // 2-CTA tiles need a full 256-column B tile and no split-K.  They are used
+  // only when requested with moe_set_option(MOE_OPT_PAIR_TILES, 1) (measured
+  // slower than 1-CTA tiles on the configured workloads, where 256-row tiles
+  // leave more rows empty).
+  const bool pair = a.pair_ok && kp.bn == 256 && kp.ksplit == 1 && pair_tiles_requested();
+  const int tile_m = pair ? 2 * BM : BM;
+  const long long max_tiles = (static_cast<long long>((a.M + tile_m - 1) / tile_m) + a.G) *
                               static_cast<long long>(kp.n_tiles) * kp.ksplit;
-  const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(device_sm_count(), max_tiles)));
+#define MOE_LAUNCH(E_, S_, F_)                                                          \
+  (pair ? launch_epi<E_, S_, F_, true>(ta, ta_lo, tb, kp, max_tiles, s)                  \
+        : launch_epi<E_, S_, F_, false>(ta, ta_lo, tb, kp, max_tiles, s))
   if (a.epilogue == kEpiGateUpAct) {
     if (a.A_lo) return cudaErrorInvalidValue;
-    return a.b_fp8 ? launch_epi<kEpiGateUpAct, false, true>(ta, ta_lo, tb, kp, grid, s)
-                   : launch_epi<kEpiGateUpAct, false, false>(ta, ta_lo, tb, kp, grid, s);
+    return a.b_fp8 ? MOE_LAUNCH(kEpiGateUpAct, false, true) : MOE_LAUNCH(kEpiGateUpAct, false, false);
   }
   if (a.epilogue == kEpiStoreF32) {
-    if (a.b_fp8) return launch_epi<kEpiStoreF32, false, true>(ta, ta_lo, tb, kp, grid, s);
-    return a.A_lo ? launch_epi<kEpiStoreF32, true, false>(ta, ta_lo, tb, kp, grid, s)
-                  : launch_epi<kEpiStoreF32, false, false>(ta, ta_lo, tb, kp, grid, s);
+    if (a.b_fp8) return MOE_LAUNCH(kEpiStoreF32, false, true);
+    return a.A_lo ? MOE_LAUNCH(kEpiStoreF32, true, false) : MOE_LAUNCH(kEpiStoreF32, false, false);
   }
+#undef MOE_LAUNCH
   return cudaErrorInvalidValue;
 }
 

@@ -29,6 +29,9 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 struct Layout {
   size_t off[12];
   size_t router_partials;  // split-K planes of the router projection (0 = none)
+  // fp8-weight layers: x as fp16 rows with exact power-of-two scales, the
+  // inverse scales per token and per permuted row (0 = none)
+  size_t x16, tok_inv, row_inv;
   size_t seg_scratch;
   size_t total;
 };
@@ -81,6 +84,11 @@ Layout make_layout(const moe_config_t* c) {
   L.off[MOE_WS_Y_PERM] = take(R * D * 4);    // fp32
   L.off[MOE_WS_H_SHARED] = take(T * Is * 4);
   L.off[MOE_WS_S] = take(T * D * 4);
+  if (c->w_dtype == MOE_FP8_E4M3) {
+    L.x16 = take(T * D * 2);
+    L.tok_inv = take(T * 4);
+    L.row_inv = take(R * 4);
+  }
   L.total = cur;
   return L;
 }
@@ -146,7 +154,8 @@ int do_route(const moe_config_t* c, const void* x, const void* Wg, const float* 
 
 int do_permute(const moe_config_t* c, const int32_t* ids, const void* x, int32_t* counts,
                int32_t* offsets, int32_t* sorted_rows, int32_t* dest, void* x_perm,
-               int32_t* seg_scratch, int32_t* err, cudaStream_t s) {
+               int32_t* seg_scratch, int32_t* err, cudaStream_t s,
+               const float* tok_scale = nullptr, float* row_scale = nullptr) {
   const int R = c->T * c->k;
   cudaError_t e = launch_init_routing(ids, R, c->E, counts, offsets, sorted_rows, dest, seg_scratch,
                                       err, s, g_trace_next >= 0 ? trace_mark : nullptr);
@@ -154,16 +163,18 @@ int do_permute(const moe_config_t* c, const int32_t* ids, const void* x, int32_t
   if (x && x_perm) {
     trace_mark(s);
     e = launch_permute_gather(x, sorted_rows, R, c->k, c->T,
-                              static_cast<size_t>(c->D) * act_bytes(c->act_dtype), x_perm, err, s);
+                              static_cast<size_t>(c->D) * act_bytes(c->act_dtype), x_perm, err, s,
+                              tok_scale, row_scale);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   }
   return MOE_OK;
 }
 
-// One gated FFN (gate/up + act, then down) over grouped rows.
-int do_ffn(const moe_config_t* c, const void* A, int M, const int32_t* offsets, int G,
-           const void* W13, const float* s13, const void* W2, const float* s2, int I, void* h,
-           void* y, int32_t* err, cudaStream_t s) {
+// One gated FFN (gate/up + act, then down) over grouped rows.  For fp8
+// weights A holds fp16 rows and a_row_scale their inverse power-of-two scales.
+int do_ffn(const moe_config_t* c, const void* A, const float* a_row_scale, int M,
+           const int32_t* offsets, int G, const void* W13, const float* s13, const void* W2,
+           const float* s2, int I, void* h, void* y, int32_t* err, cudaStream_t s) {
   if (M <= 0) return MOE_OK;
   cudaError_t e;
   trace_mark(s);
@@ -191,11 +202,14 @@ int do_ffn(const moe_config_t* c, const void* A, int M, const int32_t* offsets, 
   a.G = G;
   a.B = W13;
   a.b_fp8 = fp8;
+  a.a_fp16 = fp8;
+  a.a_row_scale = a_row_scale;
   a.N = I;
   a.b_scale = s13;
   a.out = h;
   a.out_lo = h_lo;
   a.act = c->act;
+  a.pair_ok = 1;
   a.err = err;
   e = launch_grouped_gemm(a, s);
   if (e != cudaSuccess) return e == cudaErrorNotSupported ? MOE_ERR_UNSUPPORTED : MOE_ERR_CUDA;
@@ -207,6 +221,8 @@ int do_ffn(const moe_config_t* c, const void* A, int M, const int32_t* offsets, 
   b.B = W2;
   b.N = c->D;
   b.b_scale = s2;
+  b.a_fp16 = 0;
+  b.a_row_scale = nullptr;
   b.out = y;
   b.out_lo = nullptr;
   trace_mark(s);
@@ -215,16 +231,20 @@ int do_ffn(const moe_config_t* c, const void* A, int M, const int32_t* offsets, 
   return MOE_OK;
 }
 
-int do_grouped_ffn(const moe_config_t* c, const void* x_perm, const int32_t* offsets,
-                   const void* W13, const float* s13, const void* W2, const float* s2, void* h,
-                   void* y_perm, const void* x, const void* W13s, const float* s13s,
-                   const void* W2s, const float* s2s, void* h_s, void* s_out, int32_t* err,
-                   cudaStream_t s) {
+// x_perm / x: the routed and shared A rows (fp16 with inverse row scales
+// xp_scale / x_scale for fp8 weights, else act_dtype and null scales).
+int do_grouped_ffn(const moe_config_t* c, const void* x_perm, const float* xp_scale,
+                   const int32_t* offsets, const void* W13, const float* s13, const void* W2,
+                   const float* s2, void* h, void* y_perm, const void* x, const float* x_scale,
+                   const void* W13s, const float* s13s, const void* W2s, const float* s2s,
+                   void* h_s, void* s_out, int32_t* err, cudaStream_t s) {
   const int R = c->T * c->k;
-  int st = do_ffn(c, x_perm, R, offsets, c->E, W13, s13, W2, s2, c->I, h, y_perm, err, s);
+  int st = do_ffn(c, x_perm, xp_scale, R, offsets, c->E, W13, s13, W2, s2, c->I, h, y_perm, err,
+                  s);
   if (st != MOE_OK) return st;
   if (x && c->I_shared > 0)
-    st = do_ffn(c, x, c->T, nullptr, 1, W13s, s13s, W2s, s2s, c->I_shared, h_s, s_out, err, s);
+    st = do_ffn(c, x, x_scale, c->T, nullptr, 1, W13s, s13s, W2s, s2s, c->I_shared, h_s, s_out,
+                err, s);
   return st;
 }
 
@@ -243,8 +263,11 @@ size_t moe_workspace_size(const moe_config_t* cfg) {
 }
 
 size_t moe_workspace_offset(const moe_config_t* cfg, int which) {
-  if (!cfg_valid(cfg) || which < 0 || which > MOE_WS_S) return static_cast<size_t>(-1);
-  return make_layout(cfg).off[which];
+  if (!cfg_valid(cfg) || which < 0 || which > MOE_WS_ROW_INV) return static_cast<size_t>(-1);
+  const Layout L = make_layout(cfg);
+  if (which <= MOE_WS_S) return L.off[which];
+  if (cfg->w_dtype != MOE_FP8_E4M3) return static_cast<size_t>(-1);
+  return which == MOE_WS_X16 ? L.x16 : which == MOE_WS_TOK_INV ? L.tok_inv : L.row_inv;
 }
 
 int moe_route(const moe_config_t* cfg, const void* x, const void* Wg, const float* logit_bias,
@@ -295,8 +318,29 @@ int moe_grouped_ffn(const moe_config_t* cfg, const void* x_perm, const int32_t* 
     if (!fp8_scales_ok(cfg, s13s, s2s)) return MOE_ERR_INVALID_ARG;
   }
   if (cfg->T == 0) return MOE_OK;
-  return do_grouped_ffn(cfg, x_perm, offsets, W13, s13, W2, s2, h, y_perm, x, W13s, s13s, W2s, s2s,
-                        h_s, s_out, err_word(ws), static_cast<cudaStream_t>(stream));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cfg->w_dtype == MOE_FP8_E4M3) {
+    // fp8 weights run on the fp16 tensor-core kind: convert the bf16 rows to
+    // fp16 rows with exact power-of-two scales in the workspace first
+    const Layout L = make_layout(cfg);
+    const int R = cfg->T * cfg->k;
+    void* xp16 = ws_at(ws, L.off[MOE_WS_X_PERM]);
+    float* row_inv = reinterpret_cast<float*>(ws_at(ws, L.row_inv));
+    if (launch_rows_to_fp16(x_perm, R, cfg->D, xp16, row_inv, s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    void* x16 = nullptr;
+    float* tok_inv = nullptr;
+    if (shared) {
+      x16 = ws_at(ws, L.x16);
+      tok_inv = reinterpret_cast<float*>(ws_at(ws, L.tok_inv));
+      if (launch_rows_to_fp16(x, cfg->T, cfg->D, x16, tok_inv, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    }
+    return do_grouped_ffn(cfg, xp16, row_inv, offsets, W13, s13, W2, s2, h, y_perm, x16, tok_inv,
+                          W13s, s13s, W2s, s2s, h_s, s_out, err_word(ws), s);
+  }
+  return do_grouped_ffn(cfg, x_perm, nullptr, offsets, W13, s13, W2, s2, h, y_perm, x, nullptr,
+                        W13s, s13s, W2s, s2s, h_s, s_out, err_word(ws), s);
 }
 
 int moe_finalize(const moe_config_t* cfg, const void* y_perm, const int32_t* dest,
@@ -351,10 +395,27 @@ int moe_layer(const moe_config_t* cfg, const void* x, const void* Wg, const floa
   float* partials = L.router_partials ? reinterpret_cast<float*>(ws_at(ws, L.router_partials)) : nullptr;
   st = do_route(cfg, x, Wg, logit_bias, logits, ids, w, partials, err, s);
   if (st != MOE_OK) return (g_trace_next = -1, st);
-  st = do_permute(cfg, ids, x, counts, offsets, sorted_rows, dest, x_perm, seg, err, s);
+  const bool fp8 = cfg->w_dtype == MOE_FP8_E4M3;
+  const void* x_rows = x;  // what the gather and the shared expert read
+  float* tok_inv = nullptr;
+  float* row_inv = nullptr;
+  if (fp8) {
+    // fp16 tensor-core kind for fp8 weights: x once to fp16 rows with exact
+    // power-of-two scales; the gather then carries the scales per row
+    void* x16 = ws_at(ws, L.x16);
+    tok_inv = reinterpret_cast<float*>(ws_at(ws, L.tok_inv));
+    row_inv = reinterpret_cast<float*>(ws_at(ws, L.row_inv));
+    trace_mark(s);
+    if (launch_rows_to_fp16(x, cfg->T, cfg->D, x16, tok_inv, s) != cudaSuccess)
+      return (g_trace_next = -1, MOE_ERR_CUDA);
+    x_rows = x16;
+  }
+  st = do_permute(cfg, ids, x_rows, counts, offsets, sorted_rows, dest, x_perm, seg, err, s,
+                  tok_inv, row_inv);
   if (st != MOE_OK) return (g_trace_next = -1, st);
-  st = do_grouped_ffn(cfg, x_perm, offsets, W13, s13, W2, s2, h, y_perm, shared ? x : nullptr,
-                      W13s, s13s, W2s, s2s, h_s, s_out, err, s);
+  st = do_grouped_ffn(cfg, x_perm, row_inv, offsets, W13, s13, W2, s2, h, y_perm,
+                      shared ? x_rows : nullptr, tok_inv, W13s, s13s, W2s, s2s, h_s, s_out, err,
+                      s);
   if (st != MOE_OK) return (g_trace_next = -1, st);
   trace_mark(s);
   st = cuda_status(launch_finalize(cfg->act_dtype, y_perm, dest, w, shared ? s_out : nullptr, out,
@@ -389,6 +450,17 @@ const char* moe_status_string(int status) {
   }
 }
 
+int moe_set_option(int option, int value) {
+  switch (option) {
+    case MOE_OPT_PAIR_TILES: {
+      const int old = g_pair_tiles;
+      g_pair_tiles = value ? 1 : 0;
+      return old;
+    }
+    default: return MOE_ERR_INVALID_ARG;
+  }
+}
+
 int moe_set_trace_events(void* const* events, int n_events) {
   g_trace_events = (events && n_events > 0) ? events : nullptr;
   g_trace_n = g_trace_events ? n_events : 0;
@@ -400,6 +472,7 @@ int moe_layer_launch_count(const moe_config_t* cfg) {
   int n = 0;
   n += 1;  // router projection
   n += 1;  // top-k softmax
+  if (cfg->w_dtype == MOE_FP8_E4M3) n += 1;  // x to fp16 rows (fp16 tensor-core path)
   n += 2;  // histogram, scan + stable scatter
   n += 1;  // permutation gather
   n += 2;  // routed gate/up, down

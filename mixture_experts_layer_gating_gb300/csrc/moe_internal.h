@@ -49,8 +49,14 @@ int router_k_split(int T, int E, int D);
 cudaError_t launch_init_routing(const int32_t* ids, int R, int E, int32_t* counts, int32_t* offsets,
                                 int32_t* sorted_rows, int32_t* dest, int32_t* seg_scratch,
                                 int32_t* err, cudaStream_t s, void (*mark)(cudaStream_t) = nullptr);
+// tok_scale / row_scale (optional): row_scale[p] = tok_scale[sorted_rows[p] / k].
 cudaError_t launch_permute_gather(const void* x, const int32_t* sorted_rows, int R, int k, int T,
-                                  size_t row_bytes, void* x_perm, int32_t* err, cudaStream_t s);
+                                  size_t row_bytes, void* x_perm, int32_t* err, cudaStream_t s,
+                                  const float* tok_scale = nullptr, float* row_scale = nullptr);
+// bf16 rows -> fp16 rows times an exact power of two (max |row| < 2^14);
+// inv_scale[r] = the inverse power of two.
+cudaError_t launch_rows_to_fp16(const void* x, int rows, int D, void* x16, float* inv_scale,
+                                cudaStream_t s);
 // y_perm and s_rows are fp32; out is act_dtype.
 cudaError_t launch_finalize(int act_dtype, const void* y_perm, const int32_t* dest, const float* w,
                             const void* s_rows, void* out, int T, int k, int D, int R,
@@ -86,7 +92,10 @@ struct GroupedGemmArgs {
   int N;                         // output columns (I for gate/up)
   const float* b_scale;          // [G, 2N] or [G, N] per-column scales (fp8), or nullptr
   const float* bias;             // [N] fp32 (router), or nullptr
+  const float* a_row_scale;      // [M] fp32 per-A-row factor on the accumulator, or nullptr
+  int a_fp16;                    // 1: A is fp16 (gate/up pass of fp8 layers), B expanded to fp16
   int ksplit;                    // >1: K split into planes out[s] = partial sums (fp32 store only)
+  int pair_ok;                   // 1: 2-CTA (M=256) tiles may be used
   void* out;                     // [M, N] fp32, or bf16 h_hi (gate/up pass)
   void* out_lo;                  // [M, N] bf16 h_lo (gate/up pass)
   int act;                       // moe_act_t (gate/up epilogue)
@@ -94,6 +103,9 @@ struct GroupedGemmArgs {
 };
 
 cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s);
+
+// Kernel-variant options (moe_set_option).
+extern int g_pair_tiles;
 
 // Shared helper: SM count of the current device (cached).
 int device_sm_count();

@@ -4,6 +4,7 @@
 // they move 16-byte vectors and keep every index bounds-checked so that bad
 // input data is reported through the error word instead of faulting.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include <cfloat>
 #include <climits>
@@ -274,7 +275,9 @@ __global__ void __launch_bounds__(kScatterWarps * 32)
 // One warp per permuted row, 16-byte vectors.
 __global__ void permute_gather_kernel(const uint4* __restrict__ x,
                                       const int32_t* __restrict__ sorted_rows, int R, int k, int T,
-                                      int vec_per_row, uint4* __restrict__ x_perm, int32_t* err) {
+                                      int vec_per_row, uint4* __restrict__ x_perm,
+                                      const float* __restrict__ tok_scale,
+                                      float* __restrict__ row_scale, int32_t* err) {
   const int lane = threadIdx.x & 31;
   const long long wstride = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
   for (long long p = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -283,10 +286,14 @@ __global__ void permute_gather_kernel(const uint4* __restrict__ x,
     const int t = r / k;
     uint4* dst = x_perm + p * vec_per_row;
     if (r < 0 || t >= T) {
-      if (lane == 0) atomicOr(err, MOE_DEV_BAD_DEST);
+      if (lane == 0) {
+        atomicOr(err, MOE_DEV_BAD_DEST);
+        if (row_scale) row_scale[p] = 0.0f;
+      }
       for (int v = lane; v < vec_per_row; v += 32) dst[v] = make_uint4(0, 0, 0, 0);
       continue;
     }
+    if (row_scale && lane == 0) row_scale[p] = tok_scale[t];
     const uint4* src = x + static_cast<long long>(t) * vec_per_row;
     int v = lane;
     for (; v + 96 < vec_per_row; v += 128) {
@@ -297,6 +304,60 @@ __global__ void permute_gather_kernel(const uint4* __restrict__ x,
       dst[v + 96] = d;
     }
     for (; v < vec_per_row; v += 32) dst[v] = src[v];
+  }
+}
+
+// ------------------------------------------------------------------------
+// bf16 rows to fp16 rows with an exact power-of-two row scale, for the fp16
+// tensor-core path of fp8-weight layers: row t is multiplied by 2^e_t with
+// max_d |x[t, d]| * 2^e_t < 2^14, so every bf16 value in the range that
+// matters converts exactly (bf16's 8 significant bits fit in fp16's 11), and
+// inv_scale[t] = 2^-e_t undoes it exactly after the GEMM.  One warp per row.
+__device__ __forceinline__ float exp2_int(int e) {  // exact 2^e for e in [-126, 127]
+  return __int_as_float((e + 127) << 23);
+}
+
+__global__ void rows_to_fp16_kernel(const __nv_bfloat16* __restrict__ x, int rows, int D,
+                                    __half* __restrict__ x16, float* __restrict__ inv_scale) {
+  const int lane = threadIdx.x & 31;
+  const long long wstride = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+  const int nvec = D / 8;
+  for (long long r = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       r < rows; r += wstride) {
+    const uint4* src = reinterpret_cast<const uint4*>(x + r * D);
+    float m = 0.0f;
+    for (int v = lane; v < nvec; v += 32) {
+      const uint4 u = src[v];
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(h[i]);
+        m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(FULL, m, off));
+    int e = 0;
+    if (m > 0.0f && isfinite(m)) {
+      int ex;
+      frexpf(m, &ex);  // m < 2^ex
+      e = min(100, max(-100, 14 - ex));
+    }
+    const float sc = exp2_int(e);
+    if (lane == 0) inv_scale[r] = exp2_int(-e);
+    uint4* dst = reinterpret_cast<uint4*>(x16 + r * D);
+    for (int v = lane; v < nvec; v += 32) {
+      const uint4 u = src[v];
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+      uint4 o;
+      __half2* oh = reinterpret_cast<__half2*>(&o);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(h[i]);
+        oh[i] = __floats2half2_rn(f.x * sc, f.y * sc);
+      }
+      dst[v] = o;
+    }
   }
 }
 
@@ -451,13 +512,25 @@ cudaError_t launch_init_routing(const int32_t* ids, int R, int E, int32_t* count
 }
 
 cudaError_t launch_permute_gather(const void* x, const int32_t* sorted_rows, int R, int k, int T,
-                                  size_t row_bytes, void* x_perm, int32_t* err, cudaStream_t s) {
+                                  size_t row_bytes, void* x_perm, int32_t* err, cudaStream_t s,
+                                  const float* tok_scale, float* row_scale) {
   if (R <= 0) return cudaSuccess;
   const int vec = static_cast<int>(row_bytes / 16);
   const int threads = 256;
   const int blocks = blocks_for(R, threads / 32, device_sm_count() * 16);
   permute_gather_kernel<<<blocks, threads, 0, s>>>(static_cast<const uint4*>(x), sorted_rows, R, k,
-                                                   T, vec, static_cast<uint4*>(x_perm), err);
+                                                   T, vec, static_cast<uint4*>(x_perm), tok_scale,
+                                                   row_scale, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rows_to_fp16(const void* x, int rows, int D, void* x16, float* inv_scale,
+                                cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  const int threads = 256;
+  const int blocks = blocks_for(rows, threads / 32, device_sm_count() * 16);
+  rows_to_fp16_kernel<<<blocks, threads, 0, s>>>(static_cast<const __nv_bfloat16*>(x), rows, D,
+                                                 static_cast<__half*>(x16), inv_scale);
   return cudaGetLastError();
 }
 

@@ -53,6 +53,8 @@ def run_layer(shape, inp):
         "dest": view("dest", (R,), torch.int32),
         "x_perm": view("x_perm", (R, shape.D), adt),
     }
+    if shape.w_dtype == "fp8_e4m3":
+        res["row_inv"] = view("row_inv", (R,), torch.float32)
     return res
 
 
@@ -73,7 +75,13 @@ def check_layer(shape, seed=0):
     assert np.array_equal(g["sorted_rows"].numpy(), r["sorted_rows"])
     assert np.array_equal(g["dest"].numpy(), r["dest"])
     xs = cinp["x"][torch.from_numpy(r["sorted_rows"] // k)]
-    assert torch.equal(g["x_perm"], xs), "permutation gather must copy rows bit-exactly"
+    if shape.w_dtype == "fp8_e4m3":
+        # fp16 rows times exact powers of two: scaling back gives x bit-exactly
+        xp16 = g["x_perm"].view(torch.float16).float()
+        inv = g["row_inv"].float()[:, None]
+        assert torch.equal((xp16 * inv).to(torch.bfloat16), xs), "fp16 row-scaled gather must be exact"
+    else:
+        assert torch.equal(g["x_perm"], xs), "permutation gather must copy rows bit-exactly"
 
     # 2. router projection against the fp64 definition
     L_ref = oracle.router_logits(cinp["x"], cinp["Wg"], cinp["logit_bias"])
@@ -117,7 +125,7 @@ def test_layer_parity(case):
     check_layer(LAYER_CASES[case])
 
 
-def test_layer_parity_full_qwen3_prefill():
+def test_layer_parity_full_qwen3_prefill(tile_mode):
     """The benchmarked workload at full size (T=4096), every token checked."""
     check_layer(C["qwen3_prefill"])
 
@@ -229,14 +237,26 @@ def _grouped_case(E, counts, D, I, act, seed, fp8=False):
     return xp, offsets, W13.to(torch.bfloat16), W2.to(torch.bfloat16)
 
 
+@pytest.fixture(params=[0, 1], ids=["cta1", "pair"])
+def tile_mode(request):
+    """Run a grouped-GEMM test with 1-CTA tiles and again with 2-CTA tiles."""
+    old = moe.moe_set_option(moe.MOE_OPT_PAIR_TILES, request.param)
+    yield request.param
+    moe.moe_set_option(moe.MOE_OPT_PAIR_TILES, old)
+
+
 @pytest.mark.parametrize("E,counts,D,I,act", [
     (4, [300, 0, 129, 1], 256, 128, "swiglu"),            # empty expert, ragged tails
     (3, [1, 2, 3], 192, 64, "geglu_tanh"),                # tiny segments, K not a multiple of 64*4
     (2, [1000, 24], 2816, 704, "geglu_tanh"),             # Gemma widths: ragged column tile
     (8, [0, 0, 0, 513, 0, 0, 0, 0], 2048, 768, "swiglu"),  # one expert takes everything
     (1, [77], 72, 40, "swiglu"),                          # K < 64, N < 64
+    # >= 192 rows per group: 2-CTA (M = 256) tiles, with a peer CTA that has
+    # a partial or no row range in the last tile of a group
+    (2, [700, 300], 256, 128, "swiglu"),
+    (3, [1000, 0, 560], 2048, 768, "geglu_tanh"),
 ])
-def test_grouped_ffn_parity(E, counts, D, I, act):
+def test_grouped_ffn_parity(E, counts, D, I, act, tile_mode):
     xp, offsets, W13, W2 = _grouped_case(E, counts, D, I, act, seed=E * 7 + D)
     R = xp.shape[0]
     T = R  # k = 1 view
@@ -260,8 +280,9 @@ def test_grouped_ffn_parity(E, counts, D, I, act):
     (4, [300, 0, 129, 1], 256, 128, "swiglu"),
     (2, [200, 57], 512, 384, "geglu_tanh"),   # column tile past I: zero-filled raw boxes
     (3, [5, 140, 0], 128, 64, "swiglu"),      # N < 128: one partly filled raw box
+    (2, [600, 129], 512, 256, "swiglu"),      # 2-CTA tiles with fp8 weights
 ])
-def test_grouped_ffn_fp8_parity(E, counts, D, I, act):
+def test_grouped_ffn_fp8_parity(E, counts, D, I, act, tile_mode):
     """W8A16: e4m3 weights expanded exactly on chip, per-column scales after
     the K reduction; h is a single bf16 plane for fp8 layers."""
     xp, offsets, W13, W2, s13, s2 = _grouped_case(E, counts, D, I, act, seed=E + D + I, fp8=True)
@@ -279,7 +300,7 @@ def test_grouped_ffn_fp8_parity(E, counts, D, I, act):
     check_close("y", y.cpu().double().numpy(), y_o, 2.0 ** -7, 1e-2)
 
 
-def test_fp8_weight_expansion_is_exact_including_subnormals():
+def test_fp8_weight_expansion_is_exact_including_subnormals(tile_mode):
     """Weight codes drawn mostly from the e4m3 subnormal range (|q| < 2^-6):
     a conversion that flushed them would zero whole outputs.  y is checked
     against the GPU's own h times the dequantised W2 in fp64 (fp32-accumulation
