@@ -296,9 +296,12 @@ def run_ours(args, world, rank, local):
     names = ["router_gemm", "topk_softmax"]
     if shape.w_dtype == "fp8_e4m3":
         names += ["x_to_fp16"]
-    names += ["route_hist", "route_scan_scatter", "permute_gather", "w13_gate_up", "w2_down"]
+    fp8 = shape.w_dtype == "fp8_e4m3"
+    names += ["route_hist", "route_scan_scatter", "permute_gather", "w13_gate_up"]
+    names += ["h_to_fp16"] if fp8 else []
+    names += ["w2_down"]
     if shape.I_shared:
-        names += ["shared_w13", "shared_w2"]
+        names += ["shared_w13"] + (["shared_h_to_fp16"] if fp8 else []) + ["shared_w2"]
     names += ["finalize"]
     assert len(names) == L
     per = [[] for _ in range(L)]

@@ -30,12 +30,15 @@
  *   applies to W13, W2 and the shared expert's weights.  Supported pairs:
  *   (F32, F32), (BF16, BF16), (BF16, FP8_E4M3).  Router logits, gate weights,
  *   the expert outputs y_perm and the shared-expert output are always fp32.
- *   The intermediate h takes 4 bytes per element of space: fp32 for fp32
- *   layers; for bf16 weights two bf16 planes [M, I] -- h_hi = bf16(h) followed
- *   by h_lo = bf16(h - h_hi) -- which the down projection consumes as two bf16
- *   tensor-core products, so that h keeps about 16 significant bits; for fp8
- *   weights (looser tolerance) the h_hi plane alone.  fp8 weights are
- *   expanded exactly to bf16 on chip (W8A16).
+ *   The intermediate h takes 4 bytes per element: fp32 for fp32 layers and
+ *   for fp8 weights; for bf16 weights two bf16 planes [M, I] -- h_hi =
+ *   bf16(h) followed by h_lo = bf16(h - h_hi) -- which the down projection
+ *   consumes as two bf16 tensor-core products, so that h keeps about 16
+ *   significant bits.  fp8 weights (W8A16) run on the fp16 tensor-core kind:
+ *   e4m3 expands exactly to fp16, and the A rows (x, then h) are fp16 rows
+ *   times exact powers of two, so the result equals the bf16-activation
+ *   product up to fp32 summation order (x exactly; h rounded once to 11
+ *   significant bits relative to its row).
  */
 #ifndef MOE_GB300_H
 #define MOE_GB300_H
@@ -162,9 +165,9 @@ int moe_permute_noalloc(const moe_config_t* cfg, const int32_t* topk_ids, const 
  *   W13     [E, D, 2I] w_dtype: columns [0, I) gate, [I, 2I) up.
  *   s13     [E, 2I] fp32 per-column scales (fp8 only, else NULL).
  *   W2      [E, I, D] w_dtype;   s2 [E, D] fp32 (fp8 only, else NULL).
- *   h       out: act(gate) * up, [T*k, I] fp32 (fp32 layers), the bf16 pair
- *           [2, T*k, I] (hi plane, then lo plane) for bf16 weights, or the
- *           hi plane [T*k, I] bf16 for fp8 weights (allocate 4 bytes/element).
+ *   h       out: act(gate) * up, [T*k, I] fp32 (fp32 layers and fp8 weights)
+ *           or the bf16 pair [2, T*k, I] (hi plane, then lo plane) for bf16
+ *           weights.
  *   y_perm  [T*k, D] fp32 out: h W2 per segment (times s2 for fp8).
  *   x, W13s [D, 2*I_shared], s13s [2*I_shared], W2s [I_shared, D], s2s [D]:
  *           the shared expert; x NULL (or I_shared == 0) skips it.

@@ -32,12 +32,10 @@
 //   warps 6..9  : (fp8 weights only) converters -- TMA brings the raw e4m3
 //                 weight boxes; these warps expand them exactly to 16-bit
 //                 floats in the swizzled N-major layout the MMA reads, then
-//                 arrive on the stage's full barrier (W8A16).  The gate/up pass
-//                 runs on the fp16 kind: e4m3 -> fp16 is one hardware convert
-//                 per pair, and the activations arrive as fp16 rows carrying an
-//                 exact power-of-two row scale that the epilogue removes.  The
-//                 down pass keeps bf16 (h can leave fp16's range), with e4m3 ->
-//                 bf16 done by bit placement and one bf16x2 multiply.
+//                 arrive on the stage's full barrier (W8A16).  Both passes run
+//                 on the fp16 kind: e4m3 -> fp16 is one hardware convert per
+//                 pair, and the A rows (x, or h) arrive as fp16 rows carrying
+//                 an exact power-of-two row scale that the epilogue removes.
 // Tiles are ordered (group, column tile, row tile) so that the row tiles that
 // share a weight slice run at the same time and reuse it from L2.  The tile
 // schedule is built on the device from the group offsets, so no host
@@ -123,6 +121,7 @@ struct KParams {
   const float* b_scale;
   const float* bias;
   const float* a_row_scale;  // per-row factor on the accumulator (fp16 A rows), or nullptr
+  int h_fp32;                // gate/up pass: store h as fp32
   int act;
   int ksplit;  // K split into ksplit parts, each writing its own fp32 output plane
   int kbs;     // k-blocks per split
@@ -202,8 +201,8 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
                         const __grid_constant__ CUtensorMap tmap_a_lo,
                         const __grid_constant__ CUtensorMap tmap_b, const KParams p) {
   using Cfg = StageCfg<SPLIT, FP8, PAIR>;
-  // fp8 gate/up pass: fp16 operands; everything else: bf16 operands
-  constexpr bool F16 = FP8 && EPI == kEpiGateUpAct;
+  // fp8 weights: fp16 operands; everything else: bf16 operands
+  constexpr bool F16 = FP8;
   constexpr int STAGES = Cfg::kStages;
   constexpr int STAGE_BYTES = Cfg::kStageBytes;
   constexpr int A_BYTES = Cfg::kABytes;
@@ -568,6 +567,7 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
               const int cc = col + 8 * v;
               if (cc < p.N) {
                 uint32_t packed[4], packed_lo[4];
+                float hfull[8];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                   float hv[2], lo[2];
@@ -582,17 +582,25 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
                     }
                     const float a = (p.act == MOE_ACT_SWIGLU) ? silu_f(g) : gelu_tanh_f(g);
                     const float hf = a * u;
+                    hfull[2 * i + h2] = hf;
                     hv[h2] = __bfloat162float(__float2bfloat16_rn(hf));
                     lo[h2] = hf - hv[h2];  // exact in fp32
                   }
                   packed[i] = pack_bf16x2(hv[0], hv[1]);
                   packed_lo[i] = pack_bf16x2(lo[0], lo[1]);
                 }
-                *reinterpret_cast<uint4*>(out + out_row * p.N + cc) =
-                    make_uint4(packed[0], packed[1], packed[2], packed[3]);
-                if (out_lo)
-                  *reinterpret_cast<uint4*>(out_lo + out_row * p.N + cc) =
-                      make_uint4(packed_lo[0], packed_lo[1], packed_lo[2], packed_lo[3]);
+                if (p.h_fp32) {
+                  float4* o = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) +
+                                                        out_row * p.N + cc);
+                  o[0] = make_float4(hfull[0], hfull[1], hfull[2], hfull[3]);
+                  o[1] = make_float4(hfull[4], hfull[5], hfull[6], hfull[7]);
+                } else {
+                  *reinterpret_cast<uint4*>(out + out_row * p.N + cc) =
+                      make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                  if (out_lo)
+                    *reinterpret_cast<uint4*>(out_lo + out_row * p.N + cc) =
+                        make_uint4(packed_lo[0], packed_lo[1], packed_lo[2], packed_lo[3]);
+                }
               }
             }
           }
@@ -600,6 +608,7 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
       } else {  // kEpiStoreF32: (acc * scale[col]) + bias[col]
         float* out = reinterpret_cast<float*>(p.out) + plane;
         const float* sc = p.b_scale ? p.b_scale + static_cast<size_t>(ti.g) * p.N : nullptr;
+        const float rs = (p.a_row_scale && valid) ? p.a_row_scale[out_row] : 1.0f;
         const bool vec = (p.N % 4) == 0;
 #pragma unroll 1
         for (int c = 0; c < p.bn; c += 32) {
@@ -615,7 +624,7 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
               float v[4];
 #pragma unroll
               for (int i = 0; i < 4; ++i) {
-                v[i] = __uint_as_float(r[4 * q + i]);
+                v[i] = __uint_as_float(r[4 * q + i]) * rs;
                 if (cc + i < p.N) {
                   if (sc) v[i] *= sc[cc + i];
                   if (p.bias) v[i] += p.bias[cc + i];
@@ -772,8 +781,8 @@ int device_sm_count() {
 cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
   if (a.M <= 0) return cudaSuccess;
   if (a.b_fp8 && a.A_lo) return cudaErrorNotSupported;
-  // fp16 A rows exactly when the gate/up pass has fp8 weights
-  if ((a.a_fp16 != 0) != (a.b_fp8 && a.epilogue == kEpiGateUpAct)) return cudaErrorInvalidValue;
+  // fp16 A rows exactly when the weights are fp8
+  if ((a.a_fp16 != 0) != (a.b_fp8 != 0)) return cudaErrorInvalidValue;
   if (a.G < 1 || a.G > MAX_G) return cudaErrorInvalidValue;
   CUtensorMap ta, ta_lo, tb;
   {
@@ -797,6 +806,7 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
   kp.b_scale = a.b_scale;
   kp.bias = a.bias;
   kp.a_row_scale = a.a_row_scale;
+  kp.h_fp32 = a.h_fp32;
   kp.act = a.act;
   kp.err = a.err;
   {

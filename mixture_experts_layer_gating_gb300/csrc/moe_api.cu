@@ -32,6 +32,8 @@ struct Layout {
   // fp8-weight layers: x as fp16 rows with exact power-of-two scales, the
   // inverse scales per token and per permuted row (0 = none)
   size_t x16, tok_inv, row_inv;
+  // fp8-weight layers: h (routed, shared) as fp16 rows with inverse scales
+  size_t h16, h_inv, hs16, hs_inv;
   size_t seg_scratch;
   size_t total;
 };
@@ -88,6 +90,10 @@ Layout make_layout(const moe_config_t* c) {
     L.x16 = take(T * D * 2);
     L.tok_inv = take(T * 4);
     L.row_inv = take(R * 4);
+    L.h16 = take(R * I * 2);
+    L.h_inv = take(R * 4);
+    L.hs16 = take(T * Is * 2);
+    L.hs_inv = take(T * 4);
   }
   L.total = cur;
   return L;
@@ -171,10 +177,12 @@ int do_permute(const moe_config_t* c, const int32_t* ids, const void* x, int32_t
 }
 
 // One gated FFN (gate/up + act, then down) over grouped rows.  For fp8
-// weights A holds fp16 rows and a_row_scale their inverse power-of-two scales.
+// weights A holds fp16 rows and a_row_scale their inverse power-of-two scales;
+// h is written in fp32 and converted to fp16 rows (h16, h_inv) for the down pass.
 int do_ffn(const moe_config_t* c, const void* A, const float* a_row_scale, int M,
            const int32_t* offsets, int G, const void* W13, const float* s13, const void* W2,
-           const float* s2, int I, void* h, void* y, int32_t* err, cudaStream_t s) {
+           const float* s2, int I, void* h, void* y, void* h16, float* h_inv, int32_t* err,
+           cudaStream_t s) {
   if (M <= 0) return MOE_OK;
   cudaError_t e;
   trace_mark(s);
@@ -189,8 +197,7 @@ int do_ffn(const moe_config_t* c, const void* A, const float* a_row_scale, int M
     return cuda_status(e);
   }
   // bf16 weights: h is two bf16 planes [M, I], h_hi then h_lo (h ~= h_hi + h_lo),
-  // and the down pass multiplies both.  fp8 weights (tolerance 6e-2 RMS): h is
-  // the hi plane alone.
+  // and the down pass multiplies both.  fp8 weights: h in fp32, then fp16 rows.
   const bool fp8 = c->w_dtype == MOE_FP8_E4M3;
   void* h_lo = fp8 ? nullptr : static_cast<uint8_t*>(h) + static_cast<size_t>(M) * I * 2;
   GroupedGemmArgs a{};
@@ -208,21 +215,28 @@ int do_ffn(const moe_config_t* c, const void* A, const float* a_row_scale, int M
   a.b_scale = s13;
   a.out = h;
   a.out_lo = h_lo;
+  a.h_fp32 = fp8;
   a.act = c->act;
   a.pair_ok = 1;
   a.err = err;
   e = launch_grouped_gemm(a, s);
   if (e != cudaSuccess) return e == cudaErrorNotSupported ? MOE_ERR_UNSUPPORTED : MOE_ERR_CUDA;
+  if (fp8) {
+    trace_mark(s);
+    if (launch_rows_to_fp16(h, M, I, h16, h_inv, s, /*src_f32=*/true) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
   GroupedGemmArgs b = a;
   b.epilogue = kEpiStoreF32;
-  b.A = h;
+  b.A = fp8 ? h16 : h;
   b.A_lo = h_lo;
   b.K = I;
   b.B = W2;
   b.N = c->D;
   b.b_scale = s2;
-  b.a_fp16 = 0;
-  b.a_row_scale = nullptr;
+  b.a_fp16 = fp8;
+  b.a_row_scale = fp8 ? h_inv : nullptr;
+  b.h_fp32 = 0;
   b.out = y;
   b.out_lo = nullptr;
   trace_mark(s);
@@ -237,14 +251,18 @@ int do_grouped_ffn(const moe_config_t* c, const void* x_perm, const float* xp_sc
                    const int32_t* offsets, const void* W13, const float* s13, const void* W2,
                    const float* s2, void* h, void* y_perm, const void* x, const float* x_scale,
                    const void* W13s, const float* s13s, const void* W2s, const float* s2s,
-                   void* h_s, void* s_out, int32_t* err, cudaStream_t s) {
+                   void* h_s, void* s_out, void* ws, int32_t* err, cudaStream_t s) {
   const int R = c->T * c->k;
-  int st = do_ffn(c, x_perm, xp_scale, R, offsets, c->E, W13, s13, W2, s2, c->I, h, y_perm, err,
-                  s);
+  const Layout L = make_layout(c);
+  const bool fp8 = c->w_dtype == MOE_FP8_E4M3;
+  int st = do_ffn(c, x_perm, xp_scale, R, offsets, c->E, W13, s13, W2, s2, c->I, h, y_perm,
+                  fp8 ? ws_at(ws, L.h16) : nullptr,
+                  fp8 ? reinterpret_cast<float*>(ws_at(ws, L.h_inv)) : nullptr, err, s);
   if (st != MOE_OK) return st;
   if (x && c->I_shared > 0)
     st = do_ffn(c, x, x_scale, c->T, nullptr, 1, W13s, s13s, W2s, s2s, c->I_shared, h_s, s_out,
-                err, s);
+                fp8 ? ws_at(ws, L.hs16) : nullptr,
+                fp8 ? reinterpret_cast<float*>(ws_at(ws, L.hs_inv)) : nullptr, err, s);
   return st;
 }
 
@@ -337,10 +355,10 @@ int moe_grouped_ffn(const moe_config_t* cfg, const void* x_perm, const int32_t* 
         return MOE_ERR_CUDA;
     }
     return do_grouped_ffn(cfg, xp16, row_inv, offsets, W13, s13, W2, s2, h, y_perm, x16, tok_inv,
-                          W13s, s13s, W2s, s2s, h_s, s_out, err_word(ws), s);
+                          W13s, s13s, W2s, s2s, h_s, s_out, ws, err_word(ws), s);
   }
   return do_grouped_ffn(cfg, x_perm, nullptr, offsets, W13, s13, W2, s2, h, y_perm, x, nullptr,
-                        W13s, s13s, W2s, s2s, h_s, s_out, err_word(ws), s);
+                        W13s, s13s, W2s, s2s, h_s, s_out, ws, err_word(ws), s);
 }
 
 int moe_finalize(const moe_config_t* cfg, const void* y_perm, const int32_t* dest,
@@ -414,8 +432,8 @@ int moe_layer(const moe_config_t* cfg, const void* x, const void* Wg, const floa
                   tok_inv, row_inv);
   if (st != MOE_OK) return (g_trace_next = -1, st);
   st = do_grouped_ffn(cfg, x_perm, row_inv, offsets, W13, s13, W2, s2, h, y_perm,
-                      shared ? x_rows : nullptr, tok_inv, W13s, s13s, W2s, s2s, h_s, s_out, err,
-                      s);
+                      shared ? x_rows : nullptr, tok_inv, W13s, s13s, W2s, s2s, h_s, s_out, ws,
+                      err, s);
   if (st != MOE_OK) return (g_trace_next = -1, st);
   trace_mark(s);
   st = cuda_status(launch_finalize(cfg->act_dtype, y_perm, dest, w, shared ? s_out : nullptr, out,
@@ -472,7 +490,10 @@ int moe_layer_launch_count(const moe_config_t* cfg) {
   int n = 0;
   n += 1;  // router projection
   n += 1;  // top-k softmax
-  if (cfg->w_dtype == MOE_FP8_E4M3) n += 1;  // x to fp16 rows (fp16 tensor-core path)
+  if (cfg->w_dtype == MOE_FP8_E4M3) {
+    n += 1;                          // x to fp16 rows (fp16 tensor-core path)
+    n += cfg->I_shared > 0 ? 2 : 1;  // h to fp16 rows, routed (and shared)
+  }
   n += 2;  // histogram, scan + stable scatter
   n += 1;  // permutation gather
   n += 2;  // routed gate/up, down

@@ -53,10 +53,10 @@ cudaError_t launch_init_routing(const int32_t* ids, int R, int E, int32_t* count
 cudaError_t launch_permute_gather(const void* x, const int32_t* sorted_rows, int R, int k, int T,
                                   size_t row_bytes, void* x_perm, int32_t* err, cudaStream_t s,
                                   const float* tok_scale = nullptr, float* row_scale = nullptr);
-// bf16 rows -> fp16 rows times an exact power of two (max |row| < 2^14);
-// inv_scale[r] = the inverse power of two.
+// bf16 (or fp32 when src_f32) rows -> fp16 rows times an exact power of two
+// (max |row| < 2^14); inv_scale[r] = the inverse power of two.
 cudaError_t launch_rows_to_fp16(const void* x, int rows, int D, void* x16, float* inv_scale,
-                                cudaStream_t s);
+                                cudaStream_t s, bool src_f32 = false);
 // y_perm and s_rows are fp32; out is act_dtype.
 cudaError_t launch_finalize(int act_dtype, const void* y_perm, const int32_t* dest, const float* w,
                             const void* s_rows, void* out, int T, int k, int D, int R,
@@ -93,7 +93,8 @@ struct GroupedGemmArgs {
   const float* b_scale;          // [G, 2N] or [G, N] per-column scales (fp8), or nullptr
   const float* bias;             // [N] fp32 (router), or nullptr
   const float* a_row_scale;      // [M] fp32 per-A-row factor on the accumulator, or nullptr
-  int a_fp16;                    // 1: A is fp16 (gate/up pass of fp8 layers), B expanded to fp16
+  int a_fp16;                    // 1: A is fp16 (fp8 layers), B e4m3 expanded to fp16
+  int h_fp32;                    // gate/up pass: store h as fp32 (no lo plane)
   int ksplit;                    // >1: K split into planes out[s] = partial sums (fp32 store only)
   int pair_ok;                   // 1: 2-CTA (M=256) tiles may be used
   void* out;                     // [M, N] fp32, or bf16 h_hi (gate/up pass)

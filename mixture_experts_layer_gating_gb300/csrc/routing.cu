@@ -317,23 +317,41 @@ __device__ __forceinline__ float exp2_int(int e) {  // exact 2^e for e in [-126,
   return __int_as_float((e + 127) << 23);
 }
 
-__global__ void rows_to_fp16_kernel(const __nv_bfloat16* __restrict__ x, int rows, int D,
+// 8 consecutive elements of a bf16 or fp32 row as floats
+__device__ __forceinline__ void load8f(const __nv_bfloat16* row, int v, float (&f)[8]) {
+  const uint4 u = reinterpret_cast<const uint4*>(row)[v];
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 t = __bfloat1622float2(h[i]);
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+__device__ __forceinline__ void load8f(const float* row, int v, float (&f)[8]) {
+  const float4 a = reinterpret_cast<const float4*>(row)[2 * v];
+  const float4 b = reinterpret_cast<const float4*>(row)[2 * v + 1];
+  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+  f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+
+// Source rows bf16 (exact conversion) or fp32 (rounded once to fp16's 11
+// significant bits, relative to the row maximum's scale).
+template <typename Tin>
+__global__ void rows_to_fp16_kernel(const Tin* __restrict__ x, int rows, int D,
                                     __half* __restrict__ x16, float* __restrict__ inv_scale) {
   const int lane = threadIdx.x & 31;
   const long long wstride = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
   const int nvec = D / 8;
   for (long long r = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
        r < rows; r += wstride) {
-    const uint4* src = reinterpret_cast<const uint4*>(x + r * D);
+    const Tin* src = x + r * D;
     float m = 0.0f;
     for (int v = lane; v < nvec; v += 32) {
-      const uint4 u = src[v];
-      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+      float f[8];
+      load8f(src, v, f);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 f = __bfloat1622float2(h[i]);
-        m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
-      }
+      for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(f[i]));
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(FULL, m, off));
@@ -347,15 +365,12 @@ __global__ void rows_to_fp16_kernel(const __nv_bfloat16* __restrict__ x, int row
     if (lane == 0) inv_scale[r] = exp2_int(-e);
     uint4* dst = reinterpret_cast<uint4*>(x16 + r * D);
     for (int v = lane; v < nvec; v += 32) {
-      const uint4 u = src[v];
-      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+      float f[8];
+      load8f(src, v, f);
       uint4 o;
       __half2* oh = reinterpret_cast<__half2*>(&o);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 f = __bfloat1622float2(h[i]);
-        oh[i] = __floats2half2_rn(f.x * sc, f.y * sc);
-      }
+      for (int i = 0; i < 4; ++i) oh[i] = __floats2half2_rn(f[2 * i] * sc, f[2 * i + 1] * sc);
       dst[v] = o;
     }
   }
@@ -525,12 +540,16 @@ cudaError_t launch_permute_gather(const void* x, const int32_t* sorted_rows, int
 }
 
 cudaError_t launch_rows_to_fp16(const void* x, int rows, int D, void* x16, float* inv_scale,
-                                cudaStream_t s) {
+                                cudaStream_t s, bool src_f32) {
   if (rows <= 0) return cudaSuccess;
   const int threads = 256;
   const int blocks = blocks_for(rows, threads / 32, device_sm_count() * 16);
-  rows_to_fp16_kernel<<<blocks, threads, 0, s>>>(static_cast<const __nv_bfloat16*>(x), rows, D,
-                                                 static_cast<__half*>(x16), inv_scale);
+  if (src_f32)
+    rows_to_fp16_kernel<float><<<blocks, threads, 0, s>>>(static_cast<const float*>(x), rows, D,
+                                                          static_cast<__half*>(x16), inv_scale);
+  else
+    rows_to_fp16_kernel<__nv_bfloat16><<<blocks, threads, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(x), rows, D, static_cast<__half*>(x16), inv_scale);
   return cudaGetLastError();
 }
 
