@@ -59,7 +59,12 @@ constexpr int A_TILE_BYTES = BM * BK * 2;    // 16 KB
 constexpr int B_BOX_BYTES = 64 * BK * 2;     // one 64-column x 64-row bf16 box, 8 KB
 constexpr int B_TILE_BYTES = BN_MAX * BK * 2; // 32 KB
 constexpr int MAX_STAGES = 8;
-constexpr int STAGE_BUDGET = 200 * 1024;
+constexpr int STAGE_BUDGET = 192 * 1024;
+// epilogue staging of the fp32 store pass: one padded 32 x 36 fp32 tile per
+// epilogue warp turns a row per thread into 128-byte row segments per store
+constexpr int EPI_STAGE_LD = 36;  // padded row (144 bytes: 16-byte aligned rows)
+constexpr int EPI_STAGE_FLOATS = 32 * EPI_STAGE_LD;
+constexpr int EPI_STAGE_BYTES = 4 * EPI_STAGE_FLOATS * 4;
 constexpr int MAX_G = 512;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_STRIDE = 256;  // TMEM columns per accumulator buffer
@@ -98,7 +103,7 @@ struct Ctrl {
 template <bool SPLIT, bool FP8, bool PAIR>
 constexpr size_t smem_bytes() {
   return 1024 + StageCfg<SPLIT, FP8, PAIR>::kStages * StageCfg<SPLIT, FP8, PAIR>::kStageBytes +
-         sizeof(Ctrl);
+         sizeof(Ctrl) + EPI_STAGE_BYTES;
 }
 static_assert(smem_bytes<false, false, false>() <= 227 * 1024, "shared memory budget");
 static_assert(smem_bytes<true, false, false>() <= 227 * 1024, "shared memory budget");
@@ -215,6 +220,7 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
   auto stage_b = [&](int st) { return base + st * STAGE_BYTES + A_BYTES; };
   auto stage_raw = [&](int st) { return base + st * STAGE_BYTES + A_BYTES + Cfg::kBBytes; };
   Ctrl* ctrl = reinterpret_cast<Ctrl*>(base + STAGES * STAGE_BYTES);
+  float* epi_stage = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ctrl) + sizeof(Ctrl));
   volatile int* abort_flag = &ctrl->abort;
 
   const int warp = threadIdx.x >> 5;
@@ -549,6 +555,10 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
       const bool valid = row_in_tile < ti.rows;
       const size_t out_row = static_cast<size_t>(ti.row0 + row_in_tile);
 
+      // per-warp staging tile: stg[row_in_warp * 33 + col]
+      float* stg = epi_stage + (warp - 2) * EPI_STAGE_FLOATS;
+      const int wrow0 = ti.row0 + quarter * 32;                 // first row of this warp
+      const int wrows = min(32, max(0, ti.rows - quarter * 32));  // valid rows of this warp
       if (EPI == kEpiGateUpAct) {
         __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
         __nv_bfloat16* out_lo = reinterpret_cast<__nv_bfloat16*>(p.out_lo);
@@ -605,10 +615,13 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
             }
           }
         }
-      } else {  // kEpiStoreF32: (acc * scale[col]) + bias[col]
+      } else {  // kEpiStoreF32: (acc * row scale * scale[col]) + bias[col]
         float* out = reinterpret_cast<float*>(p.out) + plane;
         const float* sc = p.b_scale ? p.b_scale + static_cast<size_t>(ti.g) * p.N : nullptr;
         const float rs = (p.a_row_scale && valid) ? p.a_row_scale[out_row] : 1.0f;
+        // after the transpose lane l owns 4 columns (4 * (l % 8) ..) of rows
+        // l / 8, l / 8 + 4, ...: one warp store writes 4 rows x 128 bytes
+        const int sub = lane >> 3, c4 = (lane & 7) * 4;
         const bool vec = (p.N % 4) == 0;
 #pragma unroll 1
         for (int c = 0; c < p.bn; c += 32) {
@@ -616,27 +629,36 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
           tmem_ld_32x32b_x32(taddr + c, r);
           tc_wait_ld();
           const int col = ti.n0 + c;
-          if (valid) {
-            float* orow = out + out_row * p.N;
+          if (col >= p.N) continue;  // warp-uniform
+          __syncwarp();
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              const int cc = col + 4 * q;
-              float v[4];
+          for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<float4*>(stg + lane * EPI_STAGE_LD + 4 * j) =
+                make_float4(__uint_as_float(r[4 * j]) * rs, __uint_as_float(r[4 * j + 1]) * rs,
+                            __uint_as_float(r[4 * j + 2]) * rs, __uint_as_float(r[4 * j + 3]) * rs);
+          __syncwarp();
+          const int cl = col + c4;
+          float cs[4] = {1.f, 1.f, 1.f, 1.f}, cb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                v[i] = __uint_as_float(r[4 * q + i]) * rs;
-                if (cc + i < p.N) {
-                  if (sc) v[i] *= sc[cc + i];
-                  if (p.bias) v[i] += p.bias[cc + i];
-                }
-              }
-              if (vec && cc + 4 <= p.N) {
-                *reinterpret_cast<float4*>(orow + cc) = make_float4(v[0], v[1], v[2], v[3]);
-              } else {
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                  if (cc + i < p.N) orow[cc + i] = v[i];
-              }
+          for (int i = 0; i < 4; ++i) {
+            if (cl + i < p.N) {
+              if (sc) cs[i] = sc[cl + i];
+              if (p.bias) cb[i] = p.bias[cl + i];
+            }
+          }
+#pragma unroll 2
+          for (int rr = sub; rr < wrows; rr += 4) {
+            const float4 v = *reinterpret_cast<const float4*>(stg + rr * EPI_STAGE_LD + c4);
+            float* orow = out + static_cast<size_t>(wrow0 + rr) * p.N;
+            const float o0 = v.x * cs[0] + cb[0], o1 = v.y * cs[1] + cb[1];
+            const float o2 = v.z * cs[2] + cb[2], o3 = v.w * cs[3] + cb[3];
+            if (vec && cl + 4 <= p.N) {
+              *reinterpret_cast<float4*>(orow + cl) = make_float4(o0, o1, o2, o3);
+            } else {
+              if (cl < p.N) orow[cl] = o0;
+              if (cl + 1 < p.N) orow[cl + 1] = o1;
+              if (cl + 2 < p.N) orow[cl + 2] = o2;
+              if (cl + 3 < p.N) orow[cl + 3] = o3;
             }
           }
         }
