@@ -249,6 +249,8 @@ def run_ours(args, world, rank, local):
     moe.load_library()
     if args.pair_tiles:
         moe.moe_set_option(moe.MOE_OPT_PAIR_TILES, 1)
+    if args.gather_a:
+        moe.moe_set_option(moe.MOE_OPT_GATHER_A, 1)
     shape = workload_shape(args)
     dev = torch.device("cuda", local)
     inp = workloads.make_inputs(shape, seed=rank, device=dev, weights_seed=0)
@@ -297,7 +299,9 @@ def run_ours(args, world, rank, local):
     if shape.w_dtype == "fp8_e4m3":
         names += ["x_to_fp16"]
     fp8 = shape.w_dtype == "fp8_e4m3"
-    names += ["route_hist", "route_scan_scatter", "permute_gather", "w13_gate_up"]
+    names += ["route_hist", "route_scan_scatter"]
+    names += ["permute_gather"] if (shape.act_dtype == "f32" or not args.gather_a) else []
+    names += ["w13_gate_up"]
     names += ["h_to_fp16"] if fp8 else []
     names += ["w2_down"]
     if shape.I_shared:
@@ -406,6 +410,8 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=64)
     ap.add_argument("--pair-tiles", action="store_true",
                     help="grouped GEMMs on 2-CTA clusters (moe_set_option MOE_OPT_PAIR_TILES)")
+    ap.add_argument("--gather-a", action="store_true",
+                    help="routed gate/up GEMM gathers x rows itself (moe_set_option MOE_OPT_GATHER_A)")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override T of the workload (smaller cases for profiling)")
     ap.add_argument("--experts", type=int, default=None,

@@ -244,6 +244,11 @@ int moe_layer_launch_count(const moe_config_t* cfg);
  *   loading half of B); 0 (default) = one CTA per 128-row tile.  Results are
  *   the same up to fp32 summation order. */
 #define MOE_OPT_PAIR_TILES 1
+/*   MOE_OPT_GATHER_A: 1 = moe_layer does not materialise the permuted rows;
+ *   the routed gate/up GEMM gathers its A rows from x with TMA tile::gather4
+ *   loads (measured slower on GB300 than the streaming gather kernel); 0
+ *   (default) = gather kernel, then tiled loads.  Same results. */
+#define MOE_OPT_GATHER_A 2
 int moe_set_option(int option, int value);
 
 /* Per-kernel timing hook (process-wide, off by default).  `events` holds

@@ -64,6 +64,7 @@ _SIGS = {
     "moe_set_option": (ctypes.c_int, [ctypes.c_int, ctypes.c_int]),
 }
 MOE_OPT_PAIR_TILES = 1
+MOE_OPT_GATHER_A = 2
 
 
 def load_library(path: Optional[str] = None) -> ctypes.CDLL:

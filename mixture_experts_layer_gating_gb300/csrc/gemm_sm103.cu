@@ -126,6 +126,9 @@ struct KParams {
   const float* b_scale;
   const float* bias;
   const float* a_row_scale;  // per-row factor on the accumulator (fp16 A rows), or nullptr
+  const int32_t* a_gather;   // gather mode: A row of output row r is a_gather[r] / gather_k
+  int gather_k;
+  int a_rows;                // rows of the A tensor (gather mode)
   int h_fp32;                // gate/up pass: store h as fp32
   int act;
   int ksplit;  // K split into ksplit parts, each writing its own fp32 output plane
@@ -323,7 +326,11 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    // Lane 0 waits for free stages, arms the full barrier and loads B (and A,
+    // except in gather mode, where every lane fetches 4 of the tile's 128 A
+    // rows straight from x with one tile::gather4 per k-block).
+    {
+      const bool gather = p.a_gather != nullptr;
       const uint64_t pol = l2_policy_evict_normal();
       // bytes the (leader's) full barrier waits for: A (+ bf16 B) of every CTA
       const uint32_t tx = (PAIR ? 2u : 1u) * (FP8 ? A_BYTES : A_BYTES + nbox_cta * B_BOX_BYTES);
@@ -333,26 +340,43 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
       for (int t = work0; t < total_tiles && ok; t += work_stride) {
         const TileInfo ti = decode_tile<TILE_M>(ctrl, G, t / p.ksplit, p.n_tiles, p.cols_per_tile);
         const int my_row0 = ti.row0 + static_cast<int>(rank) * BM;
+        // gather mode: the source rows of this lane's 4 tile rows (rows past the
+        // group repeat the tile's first row; their results are never stored)
+        int tr[4] = {0, 0, 0, 0};
+        if (gather) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int q = 4 * lane + i;
+            const int src = p.a_gather[ti.row0 + (q < ti.rows ? q : 0)] / p.gather_k;
+            tr[i] = min(max(src, 0), p.a_rows - 1);
+          }
+        }
         int kb0, kb1;
         kb_range(t, kb0, kb1);
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait(&ctrl->empty[stage], phase ^ 1u, abort_flag)) {
-            ok = false;
-            break;
-          }
-          if (leader) mbar_arrive_expect_tx(&ctrl->full[stage], tx);
+          if (lane == 0) ok = mbar_wait(&ctrl->empty[stage], phase ^ 1u, abort_flag);
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+          if (lane == 0 && leader) mbar_arrive_expect_tx(&ctrl->full[stage], tx);
+          __syncwarp();
           const uint32_t fbar = leader_bar(&ctrl->full[stage]);
           uint8_t* a_dst = stage_a(stage);
           uint8_t* b_dst = stage_b(stage);
-          if (PAIR) {
-            tma_load_2d_pair(a_dst, &tmap_a, fbar, kb * BK, my_row0, pol);
-            if (SPLIT)
-              tma_load_2d_pair(a_dst + A_TILE_BYTES, &tmap_a_lo, fbar, kb * BK, my_row0, pol);
-          } else {
-            tma_load_2d(a_dst, &tmap_a, &ctrl->full[stage], kb * BK, my_row0, pol);
-            if (SPLIT)
-              tma_load_2d(a_dst + A_TILE_BYTES, &tmap_a_lo, &ctrl->full[stage], kb * BK, my_row0,
-                          pol);
+          if (gather)
+            tma_gather4_2d(a_dst + lane * 4 * 128, &tmap_a, &ctrl->full[stage], kb * BK, tr[0],
+                           tr[1], tr[2], tr[3], pol);
+          if (lane == 0) {
+          if (!gather) {
+            if (PAIR) {
+              tma_load_2d_pair(a_dst, &tmap_a, fbar, kb * BK, my_row0, pol);
+              if (SPLIT)
+                tma_load_2d_pair(a_dst + A_TILE_BYTES, &tmap_a_lo, fbar, kb * BK, my_row0, pol);
+            } else {
+              tma_load_2d(a_dst, &tmap_a, &ctrl->full[stage], kb * BK, my_row0, pol);
+              if (SPLIT)
+                tma_load_2d(a_dst + A_TILE_BYTES, &tmap_a_lo, &ctrl->full[stage], kb * BK,
+                            my_row0, pol);
+            }
           }
           if (FP8) {
             // raw e4m3 boxes land on this CTA's own barrier for its converters
@@ -399,13 +423,14 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
                             kb * BK, ti.g, pol);
             }
           }
+          }  // lane 0
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
       }
-      if (!ok) {
+      if (!ok && lane == 0) {
         ctrl->abort = 1;
         atomicOr(p.err, MOE_DEV_WAIT_TIMEOUT);
       }
@@ -563,7 +588,10 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
         __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
         __nv_bfloat16* out_lo = reinterpret_cast<__nv_bfloat16*>(p.out_lo);
         const float* sg = p.b_scale ? p.b_scale + static_cast<size_t>(ti.g) * 2 * p.N : nullptr;
-        const float rs = (p.a_row_scale && valid) ? p.a_row_scale[out_row] : 1.0f;
+        const float rs =
+            (p.a_row_scale && valid)
+                ? p.a_row_scale[p.a_gather ? p.a_gather[out_row] / p.gather_k : out_row]
+                : 1.0f;
 #pragma unroll 1
         for (int c = 0; c < 128; c += 32) {
           uint32_t gr[32], ur[32];
@@ -813,7 +841,15 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
     const uint32_t box[2] = {BK, BM};
     const CUtensorMapDataType adt =
         a.a_fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    if (!encode_tmap(&ta, a.A, 2, dims, strides, box, adt)) return cudaErrorInvalidValue;
+    if (a.a_gather) {
+      // row gather from an [a_rows, K] tensor: one-row boxes, 4 rows per load
+      if (a.A_lo || a.a_rows < 1 || a.gather_k < 1) return cudaErrorInvalidValue;
+      const uint64_t gdims[2] = {static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.a_rows)};
+      const uint32_t gbox[2] = {BK, 1};
+      if (!encode_tmap(&ta, a.A, 2, gdims, strides, gbox, adt)) return cudaErrorInvalidValue;
+    } else if (!encode_tmap(&ta, a.A, 2, dims, strides, box, adt)) {
+      return cudaErrorInvalidValue;
+    }
     if (a.A_lo && !encode_tmap(&ta_lo, a.A_lo, 2, dims, strides, box)) return cudaErrorInvalidValue;
     if (!a.A_lo) ta_lo = ta;
   }
@@ -828,6 +864,9 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
   kp.b_scale = a.b_scale;
   kp.bias = a.bias;
   kp.a_row_scale = a.a_row_scale;
+  kp.a_gather = a.a_gather;
+  kp.gather_k = a.gather_k;
+  kp.a_rows = a.a_rows;
   kp.h_fp32 = a.h_fp32;
   kp.act = a.act;
   kp.err = a.err;
@@ -865,7 +904,8 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
   // only when requested with moe_set_option(MOE_OPT_PAIR_TILES, 1) (measured
   // slower than 1-CTA tiles on the configured workloads, where 256-row tiles
   // leave more rows empty).
-  const bool pair = a.pair_ok && kp.bn == 256 && kp.ksplit == 1 && pair_tiles_requested();
+  const bool pair = a.pair_ok && !a.a_gather && kp.bn == 256 && kp.ksplit == 1 &&
+                    pair_tiles_requested();
   const int tile_m = pair ? 2 * BM : BM;
   const long long max_tiles = (static_cast<long long>((a.M + tile_m - 1) / tile_m) + a.G) *
                               static_cast<long long>(kp.n_tiles) * kp.ksplit;

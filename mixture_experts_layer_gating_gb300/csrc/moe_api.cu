@@ -13,6 +13,8 @@ namespace {
 
 constexpr size_t kAlign = 256;
 
+int g_gather_a = 0;  // moe_set_option(MOE_OPT_GATHER_A, .)
+
 // Optional per-kernel trace events (moe_set_trace_events).
 void* const* g_trace_events = nullptr;
 int g_trace_n = 0;
@@ -179,10 +181,12 @@ int do_permute(const moe_config_t* c, const int32_t* ids, const void* x, int32_t
 // One gated FFN (gate/up + act, then down) over grouped rows.  For fp8
 // weights A holds fp16 rows and a_row_scale their inverse power-of-two scales;
 // h is written in fp32 and converted to fp16 rows (h16, h_inv) for the down pass.
+// When a_gather is given, the gate/up pass reads A row a_gather[r] / k of an
+// [a_rows, D] A for output row r (a_row_scale then indexed by that A row).
 int do_ffn(const moe_config_t* c, const void* A, const float* a_row_scale, int M,
            const int32_t* offsets, int G, const void* W13, const float* s13, const void* W2,
            const float* s2, int I, void* h, void* y, void* h16, float* h_inv, int32_t* err,
-           cudaStream_t s) {
+           cudaStream_t s, const int32_t* a_gather = nullptr, int a_rows = 0) {
   if (M <= 0) return MOE_OK;
   cudaError_t e;
   trace_mark(s);
@@ -211,6 +215,9 @@ int do_ffn(const moe_config_t* c, const void* A, const float* a_row_scale, int M
   a.b_fp8 = fp8;
   a.a_fp16 = fp8;
   a.a_row_scale = a_row_scale;
+  a.a_gather = a_gather;
+  a.gather_k = c->k;
+  a.a_rows = a_rows;
   a.N = I;
   a.b_scale = s13;
   a.out = h;
@@ -236,6 +243,7 @@ int do_ffn(const moe_config_t* c, const void* A, const float* a_row_scale, int M
   b.b_scale = s2;
   b.a_fp16 = fp8;
   b.a_row_scale = fp8 ? h_inv : nullptr;
+  b.a_gather = nullptr;
   b.h_fp32 = 0;
   b.out = y;
   b.out_lo = nullptr;
@@ -247,17 +255,21 @@ int do_ffn(const moe_config_t* c, const void* A, const float* a_row_scale, int M
 
 // x_perm / x: the routed and shared A rows (fp16 with inverse row scales
 // xp_scale / x_scale for fp8 weights, else act_dtype and null scales).
+// gather: when not null, x_perm is x itself ([T, D]) and the routed gate/up
+// pass gathers row gather[p] / k for permuted row p (xp_scale indexed by token).
 int do_grouped_ffn(const moe_config_t* c, const void* x_perm, const float* xp_scale,
                    const int32_t* offsets, const void* W13, const float* s13, const void* W2,
                    const float* s2, void* h, void* y_perm, const void* x, const float* x_scale,
                    const void* W13s, const float* s13s, const void* W2s, const float* s2s,
-                   void* h_s, void* s_out, void* ws, int32_t* err, cudaStream_t s) {
+                   void* h_s, void* s_out, void* ws, int32_t* err, cudaStream_t s,
+                   const int32_t* gather = nullptr) {
   const int R = c->T * c->k;
   const Layout L = make_layout(c);
   const bool fp8 = c->w_dtype == MOE_FP8_E4M3;
   int st = do_ffn(c, x_perm, xp_scale, R, offsets, c->E, W13, s13, W2, s2, c->I, h, y_perm,
                   fp8 ? ws_at(ws, L.h16) : nullptr,
-                  fp8 ? reinterpret_cast<float*>(ws_at(ws, L.h_inv)) : nullptr, err, s);
+                  fp8 ? reinterpret_cast<float*>(ws_at(ws, L.h_inv)) : nullptr, err, s, gather,
+                  gather ? c->T : 0);
   if (st != MOE_OK) return st;
   if (x && c->I_shared > 0)
     st = do_ffn(c, x, x_scale, c->T, nullptr, 1, W13s, s13s, W2s, s2s, c->I_shared, h_s, s_out,
@@ -419,7 +431,7 @@ int moe_layer(const moe_config_t* cfg, const void* x, const void* Wg, const floa
   float* row_inv = nullptr;
   if (fp8) {
     // fp16 tensor-core kind for fp8 weights: x once to fp16 rows with exact
-    // power-of-two scales; the gather then carries the scales per row
+    // power-of-two scales; the gather carries the inverse scale per row
     void* x16 = ws_at(ws, L.x16);
     tok_inv = reinterpret_cast<float*>(ws_at(ws, L.tok_inv));
     row_inv = reinterpret_cast<float*>(ws_at(ws, L.row_inv));
@@ -428,12 +440,17 @@ int moe_layer(const moe_config_t* cfg, const void* x, const void* Wg, const floa
       return (g_trace_next = -1, MOE_ERR_CUDA);
     x_rows = x16;
   }
-  st = do_permute(cfg, ids, x_rows, counts, offsets, sorted_rows, dest, x_perm, seg, err, s,
-                  tok_inv, row_inv);
+  // Default: a permuted copy of x (the gather kernel streams at HBM speed).
+  // With MOE_OPT_GATHER_A the routed gate/up pass instead gathers its rows from
+  // x (or its fp16 copy) with TMA tile::gather4 loads (slower on GB300: 32
+  // four-row requests per 16 KB A tile).
+  const bool gather = g_gather_a && cfg->act_dtype != MOE_F32;
+  st = do_permute(cfg, ids, gather ? nullptr : x_rows, counts, offsets, sorted_rows, dest,
+                  gather ? nullptr : x_perm, seg, err, s, tok_inv, row_inv);
   if (st != MOE_OK) return (g_trace_next = -1, st);
-  st = do_grouped_ffn(cfg, x_perm, row_inv, offsets, W13, s13, W2, s2, h, y_perm,
-                      shared ? x_rows : nullptr, tok_inv, W13s, s13s, W2s, s2s, h_s, s_out, ws,
-                      err, s);
+  st = do_grouped_ffn(cfg, gather ? x_rows : x_perm, gather ? tok_inv : row_inv, offsets, W13, s13,
+                      W2, s2, h, y_perm, shared ? x_rows : nullptr, tok_inv, W13s, s13s, W2s, s2s,
+                      h_s, s_out, ws, err, s, gather ? sorted_rows : nullptr);
   if (st != MOE_OK) return (g_trace_next = -1, st);
   trace_mark(s);
   st = cuda_status(launch_finalize(cfg->act_dtype, y_perm, dest, w, shared ? s_out : nullptr, out,
@@ -475,6 +492,11 @@ int moe_set_option(int option, int value) {
       g_pair_tiles = value ? 1 : 0;
       return old;
     }
+    case MOE_OPT_GATHER_A: {
+      const int old = g_gather_a;
+      g_gather_a = value ? 1 : 0;
+      return old;
+    }
     default: return MOE_ERR_INVALID_ARG;
   }
 }
@@ -495,7 +517,7 @@ int moe_layer_launch_count(const moe_config_t* cfg) {
     n += cfg->I_shared > 0 ? 2 : 1;  // h to fp16 rows, routed (and shared)
   }
   n += 2;  // histogram, scan + stable scatter
-  n += 1;  // permutation gather
+  if (cfg->act_dtype == MOE_F32 || !g_gather_a) n += 1;  // permutation gather
   n += 2;  // routed gate/up, down
   if (cfg->I_shared > 0) n += 2;  // shared gate/up, down
   n += 1;  // finalize

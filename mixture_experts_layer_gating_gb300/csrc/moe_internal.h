@@ -92,7 +92,11 @@ struct GroupedGemmArgs {
   int N;                         // output columns (I for gate/up)
   const float* b_scale;          // [G, 2N] or [G, N] per-column scales (fp8), or nullptr
   const float* bias;             // [N] fp32 (router), or nullptr
-  const float* a_row_scale;      // [M] fp32 per-A-row factor on the accumulator, or nullptr
+  const float* a_row_scale;      // per-A-row factor on the accumulator ([M], or [a_rows] when
+                                 // gathering), or nullptr
+  const int32_t* a_gather;       // [M] row gather: output row r reads A row a_gather[r] / gather_k
+  int gather_k;
+  int a_rows;                    // rows of A when gathering
   int a_fp16;                    // 1: A is fp16 (fp8 layers), B e4m3 expanded to fp16
   int h_fp32;                    // gate/up pass: store h as fp32 (no lo plane)
   int ksplit;                    // >1: K split into planes out[s] = partial sums (fp32 store only)

@@ -105,6 +105,20 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* m, uin
       : "memory");
 }
 
+// Row gather: rows r0..r3 (any order, any rows) of a 2-D tensor whose map has
+// a one-row box, columns [c0, c0 + box width), written as 4 consecutive rows
+// at dst (128B swizzle follows the destination address as for tiled loads).
+__device__ __forceinline__ void tma_gather4_2d(void* dst, const CUtensorMap* m, uint64_t* bar,
+                                               int32_t c0, int32_t r0, int32_t r1, int32_t r2,
+                                               int32_t r3, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes."
+      "L2::cache_hint [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(c0), "r"(r0), "r"(r1), "r"(r2),
+      "r"(r3), "l"(policy)
+      : "memory");
+}
+
 // 2-CTA (cta_group::2) loads: the destination is this CTA's shared memory and
 // the transaction bytes complete on `bar_cluster`, a shared::cluster address
 // that may name the barrier of the peer CTA of the pair (see mapa_shared).

@@ -39,7 +39,8 @@ def test_workspace_size_covers_intermediates(lib, name):
     assert all(o % 256 == 0 for o in offs)
     assert offs == sorted(offs) and offs[-1] < n
     fp8_extra = (1 + (2 if shape.I_shared else 1)) if shape.w_dtype == "fp8_e4m3" else 0
-    assert moe.moe_layer_launch_count(cfg) == (10 if shape.I_shared else 8) + fp8_extra
+    gather = 1  # the permutation gather kernel (default MOE_OPT_GATHER_A = 0)
+    assert moe.moe_layer_launch_count(cfg) == (9 if shape.I_shared else 7) + fp8_extra + gather
 
 
 @pytest.mark.parametrize("bad", [

@@ -54,7 +54,8 @@ def run_layer(shape, inp):
         "x_perm": view("x_perm", (R, shape.D), adt),
     }
     if shape.w_dtype == "fp8_e4m3":
-        res["row_inv"] = view("row_inv", (R,), torch.float32)
+        res["x16"] = view("x16", (shape.T, shape.D), torch.float16)
+        res["tok_inv"] = view("tok_inv", (shape.T,), torch.float32)
     return res
 
 
@@ -74,14 +75,21 @@ def check_layer(shape, seed=0):
     assert np.array_equal(g["offsets"].numpy(), r["offsets"])
     assert np.array_equal(g["sorted_rows"].numpy(), r["sorted_rows"])
     assert np.array_equal(g["dest"].numpy(), r["dest"])
-    xs = cinp["x"][torch.from_numpy(r["sorted_rows"] // k)]
+    gathered = moe.moe_set_option(moe.MOE_OPT_GATHER_A, 0)
+    moe.moe_set_option(moe.MOE_OPT_GATHER_A, gathered)
+    if not gathered or shape.act_dtype == "f32":
+        # materialised permuted rows: a bit-exact copy of x (fp8: of its fp16 rows)
+        xs = cinp["x"][torch.from_numpy(r["sorted_rows"] // k)]
+        if shape.w_dtype == "fp8_e4m3":
+            xs = g["x16"][torch.from_numpy(r["sorted_rows"] // k)]
+            assert torch.equal(g["x_perm"].view(torch.float16), xs)
+        else:
+            assert torch.equal(g["x_perm"], xs), "permutation gather must copy rows bit-exactly"
     if shape.w_dtype == "fp8_e4m3":
         # fp16 rows times exact powers of two: scaling back gives x bit-exactly
-        xp16 = g["x_perm"].view(torch.float16).float()
-        inv = g["row_inv"].float()[:, None]
-        assert torch.equal((xp16 * inv).to(torch.bfloat16), xs), "fp16 row-scaled gather must be exact"
-    else:
-        assert torch.equal(g["x_perm"], xs), "permutation gather must copy rows bit-exactly"
+        x16 = g["x16"].float()
+        inv = g["tok_inv"].float()[:, None]
+        assert torch.equal((x16 * inv).to(torch.bfloat16), cinp["x"]), "fp16 row scaling must be exact"
 
     # 2. router projection against the fp64 definition
     L_ref = oracle.router_logits(cinp["x"], cinp["Wg"], cinp["logit_bias"])
@@ -128,6 +136,16 @@ def test_layer_parity(case):
 def test_layer_parity_full_qwen3_prefill(tile_mode):
     """The benchmarked workload at full size (T=4096), every token checked."""
     check_layer(C["qwen3_prefill"])
+
+
+@pytest.mark.parametrize("case", ["qwen3_T512", "fp8_small_T300", "gemma4_T256"])
+def test_layer_parity_gemm_gathers_rows(case):
+    """MOE_OPT_GATHER_A: the routed gate/up GEMM reads x rows with TMA gather4."""
+    old = moe.moe_set_option(moe.MOE_OPT_GATHER_A, 1)
+    try:
+        check_layer(LAYER_CASES[case])
+    finally:
+        moe.moe_set_option(moe.MOE_OPT_GATHER_A, old)
 
 
 # ------------------------------------------------------------------ stages
