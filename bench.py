@@ -251,6 +251,8 @@ def run_ours(args, world, rank, local):
         moe.moe_set_option(moe.MOE_OPT_PAIR_TILES, 1)
     if args.gather_a:
         moe.moe_set_option(moe.MOE_OPT_GATHER_A, 1)
+    if args.decode_kernel is not None:
+        moe.moe_set_option(moe.MOE_OPT_DECODE_KERNEL, args.decode_kernel)
     shape = workload_shape(args)
     dev = torch.device("cuda", local)
     inp = workloads.make_inputs(shape, seed=rank, device=dev, weights_seed=0)
@@ -410,6 +412,8 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=64)
     ap.add_argument("--pair-tiles", action="store_true",
                     help="grouped GEMMs on 2-CTA clusters (moe_set_option MOE_OPT_PAIR_TILES)")
+    ap.add_argument("--decode-kernel", type=int, default=None, choices=[0, 1, 2],
+                    help="moe_set_option MOE_OPT_DECODE_KERNEL (0 off, 1 auto, 2 always)")
     ap.add_argument("--gather-a", action="store_true",
                     help="routed gate/up GEMM gathers x rows itself (moe_set_option MOE_OPT_GATHER_A)")
     ap.add_argument("--tokens", type=int, default=None,

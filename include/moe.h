@@ -249,6 +249,14 @@ int moe_layer_launch_count(const moe_config_t* cfg);
  *   loads (measured slower on GB300 than the streaming gather kernel); 0
  *   (default) = gather kernel, then tiled loads.  Same results. */
 #define MOE_OPT_GATHER_A 2
+/*   MOE_OPT_DECODE_KERNEL: 1 (default) = the swap-AB decode kernel (weights
+ *   as the 128-row MMA operand, 16 or 64 rows per tile, each active expert's
+ *   weights streamed once) for decode-size passes where it is faster: at most
+ *   one row per group on average, a single group (shared expert) of at most
+ *   64 rows, or fp8 weights at up to 16 rows per group; 0 = always the 128-row-tile kernel; 2 = the decode kernel
+ *   for every routed or shared FFN pass (testing).  Same results up to fp32
+ *   summation order. */
+#define MOE_OPT_DECODE_KERNEL 3
 int moe_set_option(int option, int value);
 
 /* Per-kernel timing hook (process-wide, off by default).  `events` holds

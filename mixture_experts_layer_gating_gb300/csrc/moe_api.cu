@@ -225,6 +225,7 @@ int do_ffn(const moe_config_t* c, const void* A, const float* a_row_scale, int M
   a.h_fp32 = fp8;
   a.act = c->act;
   a.pair_ok = 1;
+  a.decode_ok = 1;
   a.err = err;
   e = launch_grouped_gemm(a, s);
   if (e != cudaSuccess) return e == cudaErrorNotSupported ? MOE_ERR_UNSUPPORTED : MOE_ERR_CUDA;
@@ -490,6 +491,11 @@ int moe_set_option(int option, int value) {
     case MOE_OPT_PAIR_TILES: {
       const int old = g_pair_tiles;
       g_pair_tiles = value ? 1 : 0;
+      return old;
+    }
+    case MOE_OPT_DECODE_KERNEL: {
+      const int old = g_decode_kernel;
+      g_decode_kernel = value < 0 ? 0 : (value > 2 ? 2 : value);
       return old;
     }
     case MOE_OPT_GATHER_A: {

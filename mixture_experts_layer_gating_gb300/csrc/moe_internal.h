@@ -101,6 +101,7 @@ struct GroupedGemmArgs {
   int h_fp32;                    // gate/up pass: store h as fp32 (no lo plane)
   int ksplit;                    // >1: K split into planes out[s] = partial sums (fp32 store only)
   int pair_ok;                   // 1: 2-CTA (M=256) tiles may be used
+  int decode_ok;                 // 1: the swap-AB decode kernel may be used
   void* out;                     // [M, N] fp32, or bf16 h_hi (gate/up pass)
   void* out_lo;                  // [M, N] bf16 h_lo (gate/up pass)
   int act;                       // moe_act_t (gate/up epilogue)
@@ -111,6 +112,7 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s);
 
 // Kernel-variant options (moe_set_option).
 extern int g_pair_tiles;
+extern int g_decode_kernel;
 
 // Shared helper: SM count of the current device (cached).
 int device_sm_count();

@@ -300,6 +300,11 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
       : "r"(taddr));
 }
 
+// Named barrier for `nthreads` threads (a multiple of 32) with id `id` (1..15).
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 // Shared-memory matrix descriptor for a 128-byte-swizzled operand tile.
 //   lbo: leading byte offset  (MN-major: stride between 64-element MN groups;
 //        K-major swizzled: unused, pass 16)

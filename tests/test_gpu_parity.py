@@ -133,6 +133,16 @@ def test_layer_parity(case):
     check_layer(LAYER_CASES[case])
 
 
+@pytest.mark.parametrize("case", ["qwen3_T64_decode", "gemma4_T8_decode", "ling_T64", "qwen35_T64"])
+def test_layer_parity_decode_sizes_on_tile_kernel(case):
+    """Decode-size layers with the swap-AB kernel switched off (128-row tiles)."""
+    old = moe.moe_set_option(moe.MOE_OPT_DECODE_KERNEL, 0)
+    try:
+        check_layer(LAYER_CASES[case])
+    finally:
+        moe.moe_set_option(moe.MOE_OPT_DECODE_KERNEL, old)
+
+
 def test_layer_parity_full_qwen3_prefill(tile_mode):
     """The benchmarked workload at full size (T=4096), every token checked."""
     check_layer(C["qwen3_prefill"])
@@ -255,12 +265,15 @@ def _grouped_case(E, counts, D, I, act, seed, fp8=False):
     return xp, offsets, W13.to(torch.bfloat16), W2.to(torch.bfloat16)
 
 
-@pytest.fixture(params=[0, 1], ids=["cta1", "pair"])
+@pytest.fixture(params=["cta1", "pair", "decode"])
 def tile_mode(request):
-    """Run a grouped-GEMM test with 1-CTA tiles and again with 2-CTA tiles."""
-    old = moe.moe_set_option(moe.MOE_OPT_PAIR_TILES, request.param)
+    """Run a grouped-GEMM test on 128-row 1-CTA tiles, on 2-CTA (256-row)
+    tiles, and on the swap-AB decode kernel."""
+    pair = moe.moe_set_option(moe.MOE_OPT_PAIR_TILES, 1 if request.param == "pair" else 0)
+    dec = moe.moe_set_option(moe.MOE_OPT_DECODE_KERNEL, 2 if request.param == "decode" else 0)
     yield request.param
-    moe.moe_set_option(moe.MOE_OPT_PAIR_TILES, old)
+    moe.moe_set_option(moe.MOE_OPT_PAIR_TILES, pair)
+    moe.moe_set_option(moe.MOE_OPT_DECODE_KERNEL, dec)
 
 
 @pytest.mark.parametrize("E,counts,D,I,act", [
