@@ -227,9 +227,20 @@ def run_reference(args, world, rank):
     inp = workloads.make_inputs(shape, seed=0, device="cpu") if not torch.cuda.is_available() else \
         {k: (v.cpu() if isinstance(v, torch.Tensor) else v)
          for k, v in workloads.make_inputs(shape, seed=0, device="cuda").items()}
-    # each step: the oracle on a bounded sample so the whole run stays within minutes
-    n = min(shape.T, args.ref_tokens)
-    for _ in range(args.warmup):
+    # each step: the oracle on a bounded sample so the whole run stays within
+    # minutes -- the first n tokens, n grown from 64 (one call is also the first
+    # warm-up) while a call stays under --ref-step-s and n < T
+    if args.ref_tokens:
+        n = min(shape.T, args.ref_tokens)
+        done = 0
+    else:
+        n = min(shape.T, 64)
+        dt = time_oracle(shape, inp, n)
+        while n < shape.T and dt < 0.5 * args.ref_step_s:
+            n = min(shape.T, 2 * n)
+            dt = time_oracle(shape, inp, n)
+        done = 1
+    for _ in range(max(0, args.warmup - done)):
         time_oracle(shape, inp, n)
     times = [time_oracle(shape, inp, n) for _ in range(args.steps)]
     tot = sum(times)
@@ -417,7 +428,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
-    ap.add_argument("--ref-tokens", type=int, default=64)
+    ap.add_argument("--ref-tokens", type=int, default=0,
+                    help="reference arm: tokens per step (0: grown until one step takes ~--ref-step-s)")
+    ap.add_argument("--ref-step-s", type=float, default=2.0)
     ap.add_argument("--pair-tiles", action="store_true",
                     help="grouped GEMMs on 2-CTA clusters (moe_set_option MOE_OPT_PAIR_TILES)")
     ap.add_argument("--decode-kernel", type=int, default=None, choices=[0, 1, 2],
