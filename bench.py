@@ -320,8 +320,11 @@ def run_ours(args, world, rank, local):
     if shape.w_dtype == "fp8_e4m3":
         names += ["x_to_fp16"]
     fp8 = shape.w_dtype == "fp8_e4m3"
-    names += ["route_hist", "route_scan_scatter"]
-    names += ["permute_gather"] if (shape.act_dtype == "f32" or not args.gather_a) else []
+    if shape.R <= 8192:  # small batches: init_routing + gather in one kernel
+        names += ["route_permute"]
+    else:
+        names += ["route_hist", "route_scan_scatter"]
+        names += ["permute_gather"] if (shape.act_dtype == "f32" or not args.gather_a) else []
     names += ["w13_gate_up"]
     names += ["h_to_fp16"] if fp8 else []
     names += ["w2_down"]

@@ -165,6 +165,14 @@ int do_permute(const moe_config_t* c, const int32_t* ids, const void* x, int32_t
                int32_t* seg_scratch, int32_t* err, cudaStream_t s,
                const float* tok_scale = nullptr, float* row_scale = nullptr) {
   const int R = c->T * c->k;
+  if (small_route(R, c->E)) {  // one launch: sort + gather
+    trace_mark(s);
+    const bool gather = x && x_perm;
+    return cuda_status(launch_route_permute_small(
+        ids, R, c->E, c->k, c->T, counts, offsets, sorted_rows, dest, gather ? x : nullptr,
+        static_cast<size_t>(c->D) * act_bytes(c->act_dtype), gather ? x_perm : nullptr, tok_scale,
+        row_scale, err, s));
+  }
   cudaError_t e = launch_init_routing(ids, R, c->E, counts, offsets, sorted_rows, dest, seg_scratch,
                                       err, s, g_trace_next >= 0 ? trace_mark : nullptr);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
@@ -522,8 +530,12 @@ int moe_layer_launch_count(const moe_config_t* cfg) {
     n += 1;                          // x to fp16 rows (fp16 tensor-core path)
     n += cfg->I_shared > 0 ? 2 : 1;  // h to fp16 rows, routed (and shared)
   }
-  n += 2;  // histogram, scan + stable scatter
-  if (cfg->act_dtype == MOE_F32 || !g_gather_a) n += 1;  // permutation gather
+  if (small_route(static_cast<long long>(cfg->T) * cfg->k, cfg->E)) {
+    n += 1;  // init_routing + permutation gather in one kernel
+  } else {
+    n += 2;  // histogram, scan + stable scatter
+    if (cfg->act_dtype == MOE_F32 || !g_gather_a) n += 1;  // permutation gather
+  }
   n += 2;  // routed gate/up, down
   if (cfg->I_shared > 0) n += 2;  // shared gate/up, down
   n += 1;  // finalize

@@ -35,6 +35,16 @@ inline int route_segments(long long R) {
   return static_cast<int>((R + seg - 1) / seg);
 }
 
+// Batches of at most kSmallRouteRows expanded rows use the one-launch
+// init_routing + gather kernel (every CTA sorts all rows in shared memory).
+constexpr int kSmallRouteRows = 8192;
+inline bool small_route(long long R, int E) { return R > 0 && R <= kSmallRouteRows && E <= 512; }
+cudaError_t launch_route_permute_small(const int32_t* ids, int R, int E, int k, int T,
+                                       int32_t* counts, int32_t* offsets, int32_t* sorted_rows,
+                                       int32_t* dest, const void* x, size_t row_bytes,
+                                       void* x_perm, const float* tok_scale, float* row_scale,
+                                       int32_t* err, cudaStream_t s);
+
 // Router logits = sum of nsplit fp32 partial planes [nsplit, T, E] (+ bias),
 // written to `logits` when nsplit > 1 or bias != nullptr; then top-k softmax.
 cudaError_t launch_topk_softmax(const float* partials, int nsplit, const float* bias, float* logits,

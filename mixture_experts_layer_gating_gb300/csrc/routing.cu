@@ -270,6 +270,144 @@ __global__ void __launch_bounds__(kScatterWarps * 32)
 }
 
 // ------------------------------------------------------------------------
+// init_routing and the permutation gather in one launch, for small batches
+// (R <= kSmallRouteRows expanded rows; decode).  Every CTA loads all R expert
+// ids into shared memory and repeats the whole stable counting sort there --
+// per-warp histograms over contiguous pieces of the rows, per-expert prefix
+// over warps, exclusive scan over experts, ordered scatter with
+// __match_any_sync inside each warp -- which at these sizes costs less than
+// a kernel boundary.  CTA 0 writes counts / offsets / sorted_rows / dest;
+// then all CTAs copy their share of the permuted rows, taking the order from
+// their own shared-memory copy.  Same results as route_hist_kernel +
+// route_scatter_kernel + permute_gather_kernel (positions past the last
+// valid row, which exist only when ids were invalid, get zero rows).
+constexpr int kSmallRouteThreads = 1024;
+
+__global__ void __launch_bounds__(kSmallRouteThreads, 1)
+    route_permute_small_kernel(const int32_t* __restrict__ ids, int R, int E, int k, int T,
+                               int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                               int32_t* __restrict__ sorted_rows, int32_t* __restrict__ dest,
+                               const uint4* __restrict__ x, int vec_per_row,
+                               uint4* __restrict__ x_perm, const float* __restrict__ tok_scale,
+                               float* __restrict__ row_scale, int32_t* err) {
+  extern __shared__ int32_t sm[];
+  int32_t* ids_s = sm;               // [R] expert of each row (-1: invalid)
+  int32_t* sorted_s = sm + R;        // [R] row at each permuted position
+  int32_t* wcnt = sm + 2 * R;        // [32][E] per-warp counts, then per-warp starts
+  int32_t* off_s = wcnt + 32 * E;    // [E + 1] expert offsets
+  __shared__ int32_t warp_tot[32];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const bool writer = blockIdx.x == 0;
+
+  for (int i = threadIdx.x; i < 32 * E; i += blockDim.x) wcnt[i] = 0;
+  bool bad = false;
+  for (int r = threadIdx.x; r < R; r += blockDim.x) {
+    int e = ids[r];
+    if (e < 0 || e >= E) {
+      bad = true;
+      e = -1;
+    }
+    ids_s[r] = e;
+  }
+  if (__syncthreads_or(bad) && writer && threadIdx.x == 0) atomicOr(err, MOE_DEV_BAD_EXPERT_ID);
+  // (a) warp w counts rows [w0, w1) per expert
+  const int piece = (R + 31) / 32;
+  const int w0 = min(R, wid * piece), w1 = min(R, w0 + piece);
+  for (int r = w0 + lane; r < w1; r += 32) {
+    const int e = ids_s[r];
+    if (e >= 0) atomicAdd(&wcnt[wid * E + e], 1);
+  }
+  __syncthreads();
+  // (b) per expert: start of each warp's rows among the expert's rows; total
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = 0;
+    for (int w = 0; w < 32; ++w) {
+      const int c = wcnt[w * E + e];
+      wcnt[w * E + e] = run;
+      run += c;
+    }
+    off_s[e] = run;
+  }
+  __syncthreads();
+  // (c) exclusive scan of the totals over experts (E <= blockDim.x)
+  {
+    const int e = threadIdx.x;
+    const int v = e < E ? off_s[e] : 0;
+    int incl = v;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int y = __shfl_up_sync(FULL, incl, d);
+      if (lane >= d) incl += y;
+    }
+    if (lane == 31) warp_tot[wid] = incl;
+    __syncthreads();
+    int wbase = 0;
+    for (int w = 0; w < wid; ++w) wbase += warp_tot[w];
+    if (e < E) {
+      off_s[e] = wbase + incl - v;
+      if (writer) {
+        counts[e] = v;
+        offsets[e] = wbase + incl - v;
+      }
+    }
+    if (e == E - 1) {
+      off_s[E] = wbase + incl;
+      if (writer) offsets[E] = wbase + incl;
+    }
+  }
+  __syncthreads();
+  // (d) ordered scatter of each warp's piece
+  const unsigned lt = (1u << lane) - 1u;
+  int32_t* my = wcnt + wid * E;
+  for (int rb = w0; rb < w1; rb += 32) {
+    const int r = rb + lane;
+    const bool in = r < w1;
+    const int e = in ? ids_s[r] : -1;
+    const bool valid = e >= 0;
+    if (in && !valid && writer) dest[r] = -1;
+    const int key = valid ? e : -1 - lane;  // invalid rows never match anything
+    const unsigned peers = __match_any_sync(FULL, key);
+    if (valid) {
+      const int pos = off_s[e] + my[e] + __popc(peers & lt);
+      sorted_s[pos] = r;
+      if (writer) {
+        sorted_rows[pos] = r;
+        dest[r] = pos;
+      }
+    }
+    __syncwarp();
+    if (valid && (peers & lt) == 0) my[e] += __popc(peers);
+    __syncwarp();
+  }
+  __syncthreads();
+  if (!x) return;
+  // (e) gather: one warp per permuted row, grid-strided over all CTAs
+  const int nvalid = off_s[E];
+  const long long wstride = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+  for (long long p = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + wid; p < R;
+       p += wstride) {
+    uint4* dst = x_perm + p * vec_per_row;
+    if (p >= nvalid) {
+      if (row_scale && lane == 0) row_scale[p] = 0.0f;
+      for (int v = lane; v < vec_per_row; v += 32) dst[v] = make_uint4(0, 0, 0, 0);
+      continue;
+    }
+    const int t = sorted_s[p] / k;  // a valid row: t < T
+    if (row_scale && lane == 0) row_scale[p] = tok_scale[t];
+    const uint4* src = x + static_cast<long long>(t) * vec_per_row;
+    int v = lane;
+    for (; v + 96 < vec_per_row; v += 128) {
+      const uint4 a = src[v], b = src[v + 32], c = src[v + 64], d = src[v + 96];
+      dst[v] = a;
+      dst[v + 32] = b;
+      dst[v + 64] = c;
+      dst[v + 96] = d;
+    }
+    for (; v < vec_per_row; v += 32) dst[v] = src[v];
+  }
+}
+
+// ------------------------------------------------------------------------
 // Permutation gather (the "千问 3.5 MoE 在 TPU 上的系统优化实战" SparseCore
 // paragraph: rows gathered by routing index into one contiguous buffer).
 // One warp per permuted row, 16-byte vectors.
@@ -380,7 +518,8 @@ __global__ void rows_to_fp16_kernel(const Tin* __restrict__ x, int rows, int D,
 // finalize_routing ("CANN/cann-recipes-infer：Qwen3-MoE优化", section
 // "GMM使能和Routing优化") fused with the shared-expert add ("千问 3.5 MoE 在
 // TPU 上的系统优化实战": y = Router(x) + SharedExpert(x)).  One warp per
-// token; fp32 expert rows and shared row, fp32 accumulation with j ascending,
+// (token, 256-column slice), so that small batches still spread over every
+// SM; fp32 expert rows and shared row, fp32 accumulation with j ascending,
 // shared row last, one rounding to the output type.
 __device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&f)[8]) {
   const uint4 u = *reinterpret_cast<const uint4*>(p);
@@ -416,9 +555,13 @@ __global__ void finalize_kernel(const float* __restrict__ y_perm, const int32_t*
                                 Tt* __restrict__ out, int T, int k, int D, int R, int32_t* err) {
   const int lane = threadIdx.x & 31;
   const long long wstride = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
-  const int nchunk = D / 8;  // 8 output elements per chunk
-  for (long long t = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
-       t < T; t += wstride) {
+  const int nchunk = D / 8;              // 8 output elements per lane and chunk
+  const int nslice = (nchunk + 31) / 32;  // one warp item: a token x 256 columns
+  const long long items = static_cast<long long>(T) * nslice;
+  for (long long it = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       it < items; it += wstride) {
+    const long long t = it / nslice;
+    const int c = static_cast<int>(it - t * nslice) * 32 + lane;
     // lanes < k fetch one (position, weight) pair each; a bad position is
     // flagged and replaced by row 0 with weight 0 so every load stays in bounds
     int my_p = 0;
@@ -439,7 +582,7 @@ __global__ void finalize_kernel(const float* __restrict__ y_perm, const int32_t*
       pj[j] = __shfl_sync(FULL, my_p, j);
       wj[j] = __shfl_sync(FULL, my_w, j);
     }
-    for (int c = lane; c < nchunk; c += 32) {
+    if (c < nchunk) {
       // issue all k row loads before any arithmetic so they are in flight together
       float4 a[KMAX], b[KMAX];
 #pragma unroll
@@ -526,6 +669,31 @@ cudaError_t launch_init_routing(const int32_t* ids, int R, int E, int32_t* count
   return cudaGetLastError();
 }
 
+cudaError_t launch_route_permute_small(const int32_t* ids, int R, int E, int k, int T,
+                                       int32_t* counts, int32_t* offsets, int32_t* sorted_rows,
+                                       int32_t* dest, const void* x, size_t row_bytes,
+                                       void* x_perm, const float* tok_scale, float* row_scale,
+                                       int32_t* err, cudaStream_t s) {
+  if (R <= 0 || !small_route(R, E)) return cudaErrorInvalidValue;
+  const size_t smem = (2 * static_cast<size_t>(R) + 33 * static_cast<size_t>(E) + 1) * sizeof(int32_t);
+  static bool attr_done[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+  if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+    const size_t max_smem = (2 * static_cast<size_t>(kSmallRouteRows) + 33 * 512 + 1) * sizeof(int32_t);
+    cudaError_t e = cudaFuncSetAttribute(route_permute_small_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(max_smem));
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_done[dev] = true;
+  }
+  const int blocks = x ? blocks_for(R, 32, device_sm_count()) : 1;
+  route_permute_small_kernel<<<blocks, kSmallRouteThreads, smem, s>>>(
+      ids, R, E, k, T, counts, offsets, sorted_rows, dest, static_cast<const uint4*>(x),
+      static_cast<int>(row_bytes / 16), static_cast<uint4*>(x_perm), tok_scale, row_scale, err);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_permute_gather(const void* x, const int32_t* sorted_rows, int R, int k, int T,
                                   size_t row_bytes, void* x_perm, int32_t* err, cudaStream_t s,
                                   const float* tok_scale, float* row_scale) {
@@ -558,7 +726,8 @@ cudaError_t launch_finalize(int act_dtype, const void* y_perm, const int32_t* de
                             int32_t* err, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
   const int threads = 256;
-  const int blocks = blocks_for(T, threads / 32, device_sm_count() * 16);
+  const long long items = static_cast<long long>(T) * ((D / 8 + 31) / 32);
+  const int blocks = blocks_for(items, threads / 32, device_sm_count() * 16);
   const float* y = static_cast<const float*>(y_perm);
   const float* sr = static_cast<const float*>(s_rows);
 #define MOE_FIN(KM)                                                                           \

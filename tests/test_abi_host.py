@@ -39,8 +39,12 @@ def test_workspace_size_covers_intermediates(lib, name):
     assert all(o % 256 == 0 for o in offs)
     assert offs == sorted(offs) and offs[-1] < n
     fp8_extra = (1 + (2 if shape.I_shared else 1)) if shape.w_dtype == "fp8_e4m3" else 0
-    gather = 1  # the permutation gather kernel (default MOE_OPT_GATHER_A = 0)
-    assert moe.moe_layer_launch_count(cfg) == (9 if shape.I_shared else 7) + fp8_extra + gather
+    if shape.T * shape.k <= 8192:
+        routing = 1  # small batches: init_routing and the gather in one kernel
+    else:
+        routing = 3  # histogram, scan + scatter, gather (default MOE_OPT_GATHER_A = 0)
+    base = 7 if shape.I_shared else 5  # router, top-k, 2 (+2 shared) GEMMs, finalize
+    assert moe.moe_layer_launch_count(cfg) == base + fp8_extra + routing
 
 
 @pytest.mark.parametrize("bad", [
@@ -112,3 +116,19 @@ def test_stage_validation(lib):
     # moe_grouped_ffn: misaligned h
     assert lib.moe_grouped_ffn(ctypes.byref(cfg), g, g, g, None, g, None, g + 4, g, None, None,
                                None, None, None, None, None, g, n, None) == -1
+
+
+def test_set_option_values():
+    """moe_set_option returns the previous value, clamps ranges, rejects unknown options."""
+    ensure_library()
+    with pytest.raises(moe.MoEError):
+        moe.moe_set_option(99, 1)
+    cases = [
+        (moe.MOE_OPT_PAIR_TILES, 5, 1),
+        (moe.MOE_OPT_GATHER_A, 1, 1),
+        (moe.MOE_OPT_DECODE_KERNEL, 7, 2),
+        (moe.MOE_OPT_DECODE_KERNEL, -3, 0),
+    ]
+    for opt, value, stored in cases:
+        old = moe.moe_set_option(opt, value)
+        assert moe.moe_set_option(opt, old) == stored

@@ -185,6 +185,8 @@ def test_route_from_logits_bit_exact(E, k, renorm):
 @pytest.mark.parametrize("T,E,k,pattern", [
     (1000, 128, 8, "uniform"), (3000, 512, 10, "uniform"), (129, 8, 2, "one_hot"),
     (4096, 256, 8, "skew"), (1, 4, 1, "uniform"), (2500, 64, 6, "empty_half"),
+    # either side of the one-launch small-batch path (at most 8192 expanded rows)
+    (1024, 512, 8, "uniform"), (8193, 16, 1, "skew"), (64, 128, 8, "skew"),
 ])
 def test_permute_bit_exact(T, E, k, pattern):
     gen = np.random.default_rng(T + E + k)
@@ -220,8 +222,9 @@ def test_permute_bit_exact(T, E, k, pattern):
     assert torch.equal(xp[dest.long()].view(T, k, D)[:, 0], x)
 
 
-def test_permute_flags_bad_ids_without_fault():
-    T, E, k, D = 300, 16, 2, 64
+@pytest.mark.parametrize("T", [300, 5000])  # small-batch and segmented routing
+def test_permute_flags_bad_ids_without_fault(T):
+    E, k, D = 16, 2, 64
     ids = torch.randint(0, E, (T, k), dtype=torch.int32, device="cuda")
     ids[7, 1] = E
     ids[100, 0] = -3
