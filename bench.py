@@ -272,6 +272,8 @@ def run_ours(args, world, rank, local):
         moe.moe_set_option(moe.MOE_OPT_GATHER_A, 1)
     if args.decode_kernel is not None:
         moe.moe_set_option(moe.MOE_OPT_DECODE_KERNEL, args.decode_kernel)
+    if args.no_pdl:
+        moe.moe_set_option(moe.MOE_OPT_PDL, 0)
     shape = workload_shape(args)
     dev = torch.device("cuda", local)
     inp = workloads.make_inputs(shape, seed=rank, device=dev, weights_seed=0)
@@ -440,6 +442,8 @@ def main():
                     help="moe_set_option MOE_OPT_DECODE_KERNEL (0 off, 1 auto, 2 always)")
     ap.add_argument("--gather-a", action="store_true",
                     help="routed gate/up GEMM gathers x rows itself (moe_set_option MOE_OPT_GATHER_A)")
+    ap.add_argument("--no-pdl", action="store_true",
+                    help="plain stream order instead of programmatic dependent launch (MOE_OPT_PDL 0)")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override T of the workload (smaller cases for profiling)")
     ap.add_argument("--experts", type=int, default=None,

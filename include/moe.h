@@ -257,6 +257,12 @@ int moe_layer_launch_count(const moe_config_t* cfg);
  *   for every routed or shared FFN pass (testing).  Same results up to fp32
  *   summation order. */
 #define MOE_OPT_DECODE_KERNEL 3
+/*   MOE_OPT_PDL: 1 (default) = kernels are launched with programmatic
+ *   dependent launch (each kernel may be scheduled while its predecessor in
+ *   the stream runs and waits on the device, with griddepcontrol.wait, for
+ *   the predecessor's completion before it touches memory); 0 = plain stream
+ *   order.  Same results. */
+#define MOE_OPT_PDL 4
 int moe_set_option(int option, int value);
 
 /* Per-kernel timing hook (process-wide, off by default).  `events` holds

@@ -66,6 +66,7 @@ _SIGS = {
 MOE_OPT_PAIR_TILES = 1
 MOE_OPT_GATHER_A = 2
 MOE_OPT_DECODE_KERNEL = 3
+MOE_OPT_PDL = 4
 
 
 def load_library(path: Optional[str] = None) -> ctypes.CDLL:

@@ -272,6 +272,8 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                         const __grid_constant__ CUtensorMap tmap_a_lo,
                         const __grid_constant__ CUtensorMap tmap_b, const KParams p) {
+  pdl_wait();
+  pdl_launch_dependents();
   using Cfg = StageCfg<SPLIT, FP8, PAIR>;
   // fp8 weights: fp16 operands; everything else: bf16 operands
   constexpr bool F16 = FP8;
@@ -793,6 +795,8 @@ __global__ void __launch_bounds__(DecCfg<SPLIT, FP8>::kThreads, 1)
     grouped_gemm_decode_kernel(const __grid_constant__ CUtensorMap tmap_rows,
                                const __grid_constant__ CUtensorMap tmap_rows_lo,
                                const __grid_constant__ CUtensorMap tmap_w, const KParams p) {
+  pdl_wait();
+  pdl_launch_dependents();
   using Cfg = DecCfg<SPLIT, FP8>;
   constexpr int STAGES = Cfg::kStages;
   constexpr int STAGE_BYTES = Cfg::kStageBytes;
@@ -1146,21 +1150,22 @@ cudaError_t launch_epi(const CUtensorMap& ta, const CUtensorMap& ta_lo, const CU
   if (!PAIR) {
     const int grid =
         static_cast<int>(std::max<long long>(1, std::min<long long>(device_sm_count(), max_tiles)));
-    kern<<<grid, threads, smem, s>>>(ta, ta_lo, tb, kp);
-    return cudaGetLastError();
+    return launch_kernel(kern, dim3(grid), dim3(threads), smem, s, ta, ta_lo, tb, kp);
   }
   // one persistent 2-CTA cluster per SM pair that can hold one
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = g_pdl ? 1 : 0;
   cfg.blockDim = dim3(threads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 1;  // cluster shape only for the occupancy query
   static int max_clusters[64] = {0};
   if (dev < 0 || dev >= 64 || max_clusters[dev] == 0) {
     cfg.gridDim = dim3(2 * (device_sm_count() / 2), 1, 1);
@@ -1173,6 +1178,7 @@ cudaError_t launch_epi(const CUtensorMap& ta, const CUtensorMap& ta_lo, const CU
   const int nclu = static_cast<int>(std::max<long long>(
       1, std::min<long long>(max_clusters[(dev >= 0 && dev < 64) ? dev : 0], max_tiles)));
   cfg.gridDim = dim3(2 * nclu, 1, 1);
+  cfg.numAttrs = 2;
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, ta_lo, tb, kp);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
@@ -1182,6 +1188,7 @@ cudaError_t launch_epi(const CUtensorMap& ta, const CUtensorMap& ta_lo, const CU
 
 int g_pair_tiles = 0;      // set through moe_set_option(MOE_OPT_PAIR_TILES, .)
 int g_decode_kernel = 1;   // set through moe_set_option(MOE_OPT_DECODE_KERNEL, .)
+int g_pdl = 1;             // set through moe_set_option(MOE_OPT_PDL, .)
 bool pair_tiles_requested() { return g_pair_tiles != 0; }
 
 namespace {
@@ -1203,8 +1210,7 @@ cudaError_t launch_dec(const CUtensorMap& tr, const CUtensorMap& tr_lo, const CU
   }
   const int grid =
       static_cast<int>(std::max<long long>(1, std::min<long long>(device_sm_count(), max_tiles)));
-  kern<<<grid, threads, smem, s>>>(tr, tr_lo, tw, kp);
-  return cudaGetLastError();
+  return launch_kernel(kern, dim3(grid), dim3(threads), smem, s, tr, tr_lo, tw, kp);
 }
 
 // Swap-AB launch for decode-size groups: nt rows per tile.

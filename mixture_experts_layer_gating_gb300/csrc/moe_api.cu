@@ -511,6 +511,11 @@ int moe_set_option(int option, int value) {
       g_gather_a = value ? 1 : 0;
       return old;
     }
+    case MOE_OPT_PDL: {
+      const int old = g_pdl;
+      g_pdl = value ? 1 : 0;
+      return old;
+    }
     default: return MOE_ERR_INVALID_ARG;
   }
 }

@@ -18,6 +18,41 @@ struct ControlBlock {
 };
 static_assert(sizeof(ControlBlock) == 256, "control block is 256 bytes");
 
+// ------------------------------------------------- programmatic dependent launch
+// Every kernel of the library starts with pdl_wait() (griddepcontrol.wait:
+// returns once the grids this one depends on have completed and their memory
+// is visible; a no-op when the launch carries no programmatic dependency)
+// before it reads or writes global memory, and then calls
+// pdl_launch_dependents(), which lets the next kernel of the stream be
+// scheduled while this one runs.  Because every kernel waits unconditionally,
+// the completion of kernel n implies that of every earlier kernel, so a
+// kernel may read results from any earlier launch.
+#ifdef __CUDACC__
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+#endif
+
+extern int g_pdl;  // moe_set_option(MOE_OPT_PDL, .)
+
+// Launch with the programmatic-stream-serialization attribute when g_pdl is set.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = g_pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 inline size_t act_bytes(int dt) { return dt == MOE_F32 ? 4 : 2; }
 inline size_t w_bytes(int dt) { return dt == MOE_F32 ? 4 : (dt == MOE_BF16 ? 2 : 1); }
 

@@ -31,6 +31,8 @@ __global__ void topk_softmax_kernel(const float* __restrict__ partials, int nspl
                                     const float* __restrict__ bias, float* logits, int T, int E,
                                     int k, int renorm, int32_t* __restrict__ ids,
                                     float* __restrict__ w, int32_t* err) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int warps_per_block = blockDim.x >> 5;
   const int lane = threadIdx.x & 31;
   const long long t = static_cast<long long>(blockIdx.x) * warps_per_block + (threadIdx.x >> 5);
@@ -142,6 +144,8 @@ __global__ void topk_softmax_kernel(const float* __restrict__ partials, int nspl
 //     __match_any_sync.  Rows with an id outside [0, E) are skipped (dest -1).
 __global__ void route_hist_kernel(const int32_t* __restrict__ ids, int R, int E, int seg,
                                   int32_t* __restrict__ seg_hist, int32_t* err) {
+  pdl_wait();
+  pdl_launch_dependents();
   extern __shared__ int32_t cnt[];
   for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
   __syncthreads();
@@ -164,6 +168,8 @@ __global__ void __launch_bounds__(kScatterWarps * 32)
                          const int32_t* __restrict__ seg_hist, int32_t* __restrict__ counts,
                          int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_rows,
                          int32_t* __restrict__ dest) {
+  pdl_wait();
+  pdl_launch_dependents();
   extern __shared__ int32_t sm[];
   int32_t* base = sm;                    // [E] first position of this segment's rows of e
   int32_t* wcnt = sm + E;                // [kScatterWarps][E] per-warp counts, then starts
@@ -290,6 +296,8 @@ __global__ void __launch_bounds__(kSmallRouteThreads, 1)
                                const uint4* __restrict__ x, int vec_per_row,
                                uint4* __restrict__ x_perm, const float* __restrict__ tok_scale,
                                float* __restrict__ row_scale, int32_t* err) {
+  pdl_wait();
+  pdl_launch_dependents();
   extern __shared__ int32_t sm[];
   int32_t* ids_s = sm;               // [R] expert of each row (-1: invalid)
   int32_t* sorted_s = sm + R;        // [R] row at each permuted position
@@ -416,6 +424,8 @@ __global__ void permute_gather_kernel(const uint4* __restrict__ x,
                                       int vec_per_row, uint4* __restrict__ x_perm,
                                       const float* __restrict__ tok_scale,
                                       float* __restrict__ row_scale, int32_t* err) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
   const long long wstride = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
   for (long long p = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -478,6 +488,8 @@ __device__ __forceinline__ void load8f(const float* row, int v, float (&f)[8]) {
 template <typename Tin>
 __global__ void rows_to_fp16_kernel(const Tin* __restrict__ x, int rows, int D,
                                     __half* __restrict__ x16, float* __restrict__ inv_scale) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
   const long long wstride = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
   const int nvec = D / 8;
@@ -553,6 +565,8 @@ template <typename Tt, int KMAX>
 __global__ void finalize_kernel(const float* __restrict__ y_perm, const int32_t* __restrict__ dest,
                                 const float* __restrict__ w, const float* __restrict__ s_rows,
                                 Tt* __restrict__ out, int T, int k, int D, int R, int32_t* err) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
   const long long wstride = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
   const int nchunk = D / 8;              // 8 output elements per lane and chunk
@@ -629,6 +643,14 @@ int blocks_for(long long work_items, int per_block, int cap) {
   return static_cast<int>(b);
 }
 
+// Launch through launch_kernel (programmatic dependent launch when enabled);
+// a failed launch returns its error from the enclosing launcher.
+#define MOE_LAUNCH(kern, grid, block, smem, stream, ...)                                  \
+  do {                                                                                    \
+    const cudaError_t le_ = launch_kernel(kern, dim3(grid), dim3(block), smem, stream, __VA_ARGS__); \
+    if (le_ != cudaSuccess) return le_;                                                   \
+  } while (0)
+
 }  // namespace
 
 cudaError_t launch_topk_softmax(const float* partials, int nsplit, const float* bias, float* logits,
@@ -639,14 +661,14 @@ cudaError_t launch_topk_softmax(const float* partials, int nsplit, const float* 
   const int blocks = (T + wpb - 1) / wpb;
   const int epl = (E + 31) / 32;
   if (epl <= 4)
-    topk_softmax_kernel<4><<<blocks, threads, 0, s>>>(partials, nsplit, bias, logits, T, E, k,
-                                                      renorm, ids, w, err);
+    MOE_LAUNCH(topk_softmax_kernel<4>, blocks, threads, 0, s, partials, nsplit, bias, logits, T,
+               E, k, renorm, ids, w, err);
   else if (epl <= 8)
-    topk_softmax_kernel<8><<<blocks, threads, 0, s>>>(partials, nsplit, bias, logits, T, E, k,
-                                                      renorm, ids, w, err);
+    MOE_LAUNCH(topk_softmax_kernel<8>, blocks, threads, 0, s, partials, nsplit, bias, logits, T,
+               E, k, renorm, ids, w, err);
   else
-    topk_softmax_kernel<16><<<blocks, threads, 0, s>>>(partials, nsplit, bias, logits, T, E, k,
-                                                       renorm, ids, w, err);
+    MOE_LAUNCH(topk_softmax_kernel<16>, blocks, threads, 0, s, partials, nsplit, bias, logits, T,
+               E, k, renorm, ids, w, err);
   return cudaGetLastError();
 }
 
@@ -661,11 +683,11 @@ cudaError_t launch_init_routing(const int32_t* ids, int R, int E, int32_t* count
   const int seg = route_segment_rows(R);
   const int nseg = (R + seg - 1) / seg;
   if (mark) mark(s);
-  route_hist_kernel<<<nseg, 256, E * sizeof(int32_t), s>>>(ids, R, E, seg, seg_scratch, err);
+  MOE_LAUNCH(route_hist_kernel, nseg, 256, E * sizeof(int32_t), s, ids, R, E, seg, seg_scratch, err);
   if (mark) mark(s);
   const size_t smem = (1 + kScatterWarps) * E * sizeof(int32_t);
-  route_scatter_kernel<<<nseg, kScatterWarps * 32, smem, s>>>(ids, R, E, seg, nseg, seg_scratch,
-                                                               counts, offsets, sorted_rows, dest);
+  MOE_LAUNCH(route_scatter_kernel, nseg, kScatterWarps * 32, smem, s, ids, R, E, seg, nseg,
+             seg_scratch, counts, offsets, sorted_rows, dest);
   return cudaGetLastError();
 }
 
@@ -688,9 +710,10 @@ cudaError_t launch_route_permute_small(const int32_t* ids, int R, int E, int k, 
     if (dev >= 0 && dev < 64) attr_done[dev] = true;
   }
   const int blocks = x ? blocks_for(R, 32, device_sm_count()) : 1;
-  route_permute_small_kernel<<<blocks, kSmallRouteThreads, smem, s>>>(
-      ids, R, E, k, T, counts, offsets, sorted_rows, dest, static_cast<const uint4*>(x),
-      static_cast<int>(row_bytes / 16), static_cast<uint4*>(x_perm), tok_scale, row_scale, err);
+  MOE_LAUNCH(route_permute_small_kernel, blocks, kSmallRouteThreads, smem, s, ids, R, E, k, T,
+             counts, offsets, sorted_rows, dest, static_cast<const uint4*>(x),
+             static_cast<int>(row_bytes / 16), static_cast<uint4*>(x_perm), tok_scale, row_scale,
+             err);
   return cudaGetLastError();
 }
 
@@ -701,9 +724,8 @@ cudaError_t launch_permute_gather(const void* x, const int32_t* sorted_rows, int
   const int vec = static_cast<int>(row_bytes / 16);
   const int threads = 256;
   const int blocks = blocks_for(R, threads / 32, device_sm_count() * 16);
-  permute_gather_kernel<<<blocks, threads, 0, s>>>(static_cast<const uint4*>(x), sorted_rows, R, k,
-                                                   T, vec, static_cast<uint4*>(x_perm), tok_scale,
-                                                   row_scale, err);
+  MOE_LAUNCH(permute_gather_kernel, blocks, threads, 0, s, static_cast<const uint4*>(x),
+             sorted_rows, R, k, T, vec, static_cast<uint4*>(x_perm), tok_scale, row_scale, err);
   return cudaGetLastError();
 }
 
@@ -713,11 +735,11 @@ cudaError_t launch_rows_to_fp16(const void* x, int rows, int D, void* x16, float
   const int threads = 256;
   const int blocks = blocks_for(rows, threads / 32, device_sm_count() * 16);
   if (src_f32)
-    rows_to_fp16_kernel<float><<<blocks, threads, 0, s>>>(static_cast<const float*>(x), rows, D,
-                                                          static_cast<__half*>(x16), inv_scale);
+    MOE_LAUNCH(rows_to_fp16_kernel<float>, blocks, threads, 0, s, static_cast<const float*>(x),
+               rows, D, static_cast<__half*>(x16), inv_scale);
   else
-    rows_to_fp16_kernel<__nv_bfloat16><<<blocks, threads, 0, s>>>(
-        static_cast<const __nv_bfloat16*>(x), rows, D, static_cast<__half*>(x16), inv_scale);
+    MOE_LAUNCH(rows_to_fp16_kernel<__nv_bfloat16>, blocks, threads, 0, s,
+               static_cast<const __nv_bfloat16*>(x), rows, D, static_cast<__half*>(x16), inv_scale);
   return cudaGetLastError();
 }
 
@@ -730,14 +752,17 @@ cudaError_t launch_finalize(int act_dtype, const void* y_perm, const int32_t* de
   const int blocks = blocks_for(items, threads / 32, device_sm_count() * 16);
   const float* y = static_cast<const float*>(y_perm);
   const float* sr = static_cast<const float*>(s_rows);
-#define MOE_FIN(KM)                                                                           \
-  do {                                                                                        \
-    if (act_dtype == MOE_BF16)                                                                \
-      finalize_kernel<__nv_bfloat16, KM><<<blocks, threads, 0, s>>>(                          \
-          y, dest, w, sr, static_cast<__nv_bfloat16*>(out), T, k, D, R, err);                 \
-    else                                                                                      \
-      finalize_kernel<float, KM><<<blocks, threads, 0, s>>>(y, dest, w, sr,                   \
-                                                            static_cast<float*>(out), T, k, D, R, err); \
+#define MOE_FIN(KM)                                                               \
+  do {                                                                            \
+    if (act_dtype == MOE_BF16) {                                                  \
+      auto kern = finalize_kernel<__nv_bfloat16, KM>;                             \
+      MOE_LAUNCH(kern, blocks, threads, 0, s, y, dest, w, sr,                     \
+                 static_cast<__nv_bfloat16*>(out), T, k, D, R, err);              \
+    } else {                                                                      \
+      auto kern = finalize_kernel<float, KM>;                                     \
+      MOE_LAUNCH(kern, blocks, threads, 0, s, y, dest, w, sr,                     \
+                 static_cast<float*>(out), T, k, D, R, err);                      \
+    }                                                                             \
   } while (0)
   if (k <= 2) MOE_FIN(2);
   else if (k <= 4) MOE_FIN(4);

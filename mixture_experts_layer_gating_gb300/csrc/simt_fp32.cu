@@ -36,6 +36,8 @@ __global__ void simt_group_gemm(const float* __restrict__ A, const int32_t* __re
                                 int G, int M, int K, const float* __restrict__ W, int N,
                                 const float* __restrict__ bias, int act, float* __restrict__ out,
                                 int32_t* err) {
+  pdl_wait();
+  pdl_launch_dependents();
   __shared__ float As[TR][TK + 1];
   const int row0 = blockIdx.y * TR;
   const int col0 = blockIdx.x * TC;
@@ -103,8 +105,8 @@ cudaError_t launch_simt_router(const float* x, const float* Wg, const float* bia
                                int T, int D, int E, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
   dim3 grid((E + TC - 1) / TC, (T + TR - 1) / TR);
-  simt_group_gemm<1><<<grid, 256, 0, s>>>(x, nullptr, 1, T, D, Wg, E, bias, 0, logits, nullptr);
-  return cudaGetLastError();
+  return launch_kernel(simt_group_gemm<1>, grid, dim3(256), 0, s, x, nullptr, 1, T, D, Wg, E, bias,
+                       0, logits, nullptr);
 }
 
 cudaError_t launch_simt_gate_up(const float* A, const int32_t* offsets, int G, int M, int K,
@@ -112,16 +114,16 @@ cudaError_t launch_simt_gate_up(const float* A, const int32_t* offsets, int G, i
                                 cudaStream_t s) {
   if (M <= 0) return cudaSuccess;
   dim3 grid((I + TC - 1) / TC, (M + TR - 1) / TR);
-  simt_group_gemm<0><<<grid, 256, 0, s>>>(A, offsets, G, M, K, W13, I, nullptr, act, h, err);
-  return cudaGetLastError();
+  return launch_kernel(simt_group_gemm<0>, grid, dim3(256), 0, s, A, offsets, G, M, K, W13, I,
+                       nullptr, act, h, err);
 }
 
 cudaError_t launch_simt_down(const float* h, const int32_t* offsets, int G, int M, int I,
                              const float* W2, int N, float* y, int32_t* err, cudaStream_t s) {
   if (M <= 0) return cudaSuccess;
   dim3 grid((N + TC - 1) / TC, (M + TR - 1) / TR);
-  simt_group_gemm<1><<<grid, 256, 0, s>>>(h, offsets, G, M, I, W2, N, nullptr, 0, y, err);
-  return cudaGetLastError();
+  return launch_kernel(simt_group_gemm<1>, grid, dim3(256), 0, s, h, offsets, G, M, I, W2, N,
+                       nullptr, 0, y, err);
 }
 
 }  // namespace moe

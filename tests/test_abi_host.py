@@ -128,6 +128,8 @@ def test_set_option_values():
         (moe.MOE_OPT_GATHER_A, 1, 1),
         (moe.MOE_OPT_DECODE_KERNEL, 7, 2),
         (moe.MOE_OPT_DECODE_KERNEL, -3, 0),
+        (moe.MOE_OPT_PDL, 0, 0),
+        (moe.MOE_OPT_PDL, 3, 1),
     ]
     for opt, value, stored in cases:
         old = moe.moe_set_option(opt, value)

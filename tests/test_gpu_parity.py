@@ -148,6 +148,25 @@ def test_layer_parity_full_qwen3_prefill(tile_mode):
     check_layer(C["qwen3_prefill"])
 
 
+@pytest.mark.parametrize("pair", [0, 1])
+@pytest.mark.parametrize("case", ["qwen3_T512", "qwen3_T64_decode", "fp8_small_T300", "gemma4_T256",
+                                  "toy"])
+def test_layer_same_result_without_pdl(case, pair):
+    """Programmatic dependent launch changes only when kernels are scheduled:
+    the layer output is bit-identical with MOE_OPT_PDL on and off."""
+    shape = LAYER_CASES[case]
+    inp = workloads.make_inputs(shape, seed=3, device="cuda")
+    old_pair = moe.moe_set_option(moe.MOE_OPT_PAIR_TILES, pair)
+    old = moe.moe_set_option(moe.MOE_OPT_PDL, 1)
+    try:
+        with_pdl = run_layer(shape, inp)["out"].clone()
+        moe.moe_set_option(moe.MOE_OPT_PDL, 0)
+        assert torch.equal(run_layer(shape, inp)["out"], with_pdl)
+    finally:
+        moe.moe_set_option(moe.MOE_OPT_PDL, old)
+        moe.moe_set_option(moe.MOE_OPT_PAIR_TILES, old_pair)
+
+
 @pytest.mark.parametrize("case", ["qwen3_T512", "fp8_small_T300", "gemma4_T256"])
 def test_layer_parity_gemm_gathers_rows(case):
     """MOE_OPT_GATHER_A: the routed gate/up GEMM reads x rows with TMA gather4."""
