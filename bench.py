@@ -438,8 +438,8 @@ def main():
     ap.add_argument("--ref-step-s", type=float, default=2.0)
     ap.add_argument("--pair-tiles", action="store_true",
                     help="grouped GEMMs on 2-CTA clusters (moe_set_option MOE_OPT_PAIR_TILES)")
-    ap.add_argument("--decode-kernel", type=int, default=None, choices=[0, 1, 2],
-                    help="moe_set_option MOE_OPT_DECODE_KERNEL (0 off, 1 auto, 2 always)")
+    ap.add_argument("--decode-kernel", type=int, default=None, choices=[0, 1, 2, 3],
+                    help="moe_set_option MOE_OPT_DECODE_KERNEL (0 off, 1 auto, 2/3 always with 64/16-row tiles)")
     ap.add_argument("--gather-a", action="store_true",
                     help="routed gate/up GEMM gathers x rows itself (moe_set_option MOE_OPT_GATHER_A)")
     ap.add_argument("--no-pdl", action="store_true",

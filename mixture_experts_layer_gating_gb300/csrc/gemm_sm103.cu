@@ -134,6 +134,7 @@ struct KParams {
   int act;
   int ksplit;  // K split into ksplit parts, each writing its own fp32 output plane
   int kbs;     // k-blocks per split
+  int b_wide;  // bf16 B map viewed as [64-column blocks][K][64]: one load per stage
   int32_t* err;
 };
 
@@ -273,7 +274,6 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
                         const __grid_constant__ CUtensorMap tmap_a_lo,
                         const __grid_constant__ CUtensorMap tmap_b, const KParams p) {
   pdl_wait();
-  pdl_launch_dependents();
   using Cfg = StageCfg<SPLIT, FP8, PAIR>;
   // fp8 weights: fp16 operands; everything else: bf16 operands
   constexpr bool F16 = FP8;
@@ -426,6 +426,23 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
               for (int j = 0; j < nraw; ++j)
                 tma_load_3d(r_dst + j * RAW_BOX_BYTES, &tmap_b, &ctrl->raw_full[stage],
                             c0 + 128 * j, kb * BK, ti.g, pol_b);
+            }
+          } else if (p.b_wide) {
+            // one load brings this CTA's whole B share: 64-column blocks
+            // n0/64 .. (gate then up in the gate/up pass; rank r its half in a pair)
+            if (EPI == kEpiGateUpAct) {
+              if (PAIR)
+                tma_load_5d_pair(b_dst, &tmap_b, fbar, 0, kb * BK, ti.n0 / 64, static_cast<int>(rank),
+                                 ti.g, pol_b);
+              else
+                tma_load_5d(b_dst, &tmap_b, &ctrl->full[stage], 0, kb * BK, ti.n0 / 64, 0, ti.g,
+                            pol_b);
+            } else {
+              if (PAIR)
+                tma_load_4d_pair(b_dst, &tmap_b, fbar, 0, kb * BK,
+                                 ti.n0 / 64 + static_cast<int>(rank) * nbox_cta, ti.g, pol_b);
+              else
+                tma_load_4d(b_dst, &tmap_b, &ctrl->full[stage], 0, kb * BK, ti.n0 / 64, ti.g, pol_b);
             }
           } else if (EPI == kEpiGateUpAct) {
             if (PAIR) {  // rank 0: gate columns n0..n0+127, rank 1: up columns
@@ -733,6 +750,9 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
   }
 
   // ---------------------------------------------------------------- teardown
+  // the next kernel may be scheduled once every CTA got here (not earlier:
+  // its waiting CTAs would sit beside this persistent kernel's for its whole run)
+  pdl_launch_dependents();
   tc_fence_before_sync();
   __syncthreads();
   // a pair finishes together: the leader's MMAs read the peer's shared memory
@@ -796,7 +816,6 @@ __global__ void __launch_bounds__(DecCfg<SPLIT, FP8>::kThreads, 1)
                                const __grid_constant__ CUtensorMap tmap_rows_lo,
                                const __grid_constant__ CUtensorMap tmap_w, const KParams p) {
   pdl_wait();
-  pdl_launch_dependents();
   using Cfg = DecCfg<SPLIT, FP8>;
   constexpr int STAGES = Cfg::kStages;
   constexpr int STAGE_BYTES = Cfg::kStageBytes;
@@ -1086,6 +1105,7 @@ __global__ void __launch_bounds__(DecCfg<SPLIT, FP8>::kThreads, 1)
     __syncwarp();
   }
 
+  pdl_launch_dependents();  // at the end, as in the 128-row kernel
   tc_fence_before_sync();
   __syncthreads();
   if (warp == 1) {
@@ -1306,6 +1326,7 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
   const long long Mg = a.M, Gg = a.G;
   int nt = 0;
   if (g_decode_kernel == 2) nt = DEC_NT_MAX;
+  else if (g_decode_kernel == 3) nt = 16;
   else if (Mg <= Gg) nt = 16;
   else if (Gg == 1 && Mg <= 64) nt = DEC_NT_MAX;
   else if (a.b_fp8 && Mg <= 16 * Gg) nt = DEC_NT_MAX;
@@ -1369,17 +1390,9 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
       a.b_fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const uint32_t box_n = a.b_fp8 ? 128 : 64;  // 128 bytes of columns either way
   if (a.epilogue == kEpiGateUpAct) {
-    const uint64_t dims[4] = {N, 2, K, static_cast<uint64_t>(a.G)};
-    const uint64_t strides[3] = {N * eb, 2 * N * eb, K * 2 * N * eb};
-    const uint32_t box[4] = {box_n, 1, BK, 1};
-    if (!encode_tmap(&tb, a.B, 4, dims, strides, box, bdt)) return cudaErrorInvalidValue;
     kp.bn = 256;
     kp.cols_per_tile = 128;
   } else {
-    const uint64_t dims[3] = {N, K, static_cast<uint64_t>(a.G)};
-    const uint64_t strides[2] = {N * eb, K * N * eb};
-    const uint32_t box[3] = {box_n, BK, 1};
-    if (!encode_tmap(&tb, a.B, 3, dims, strides, box, bdt)) return cudaErrorInvalidValue;
     const uint64_t gran = a.b_fp8 ? 128 : 64;
     kp.bn = static_cast<int>(std::min<uint64_t>(BN_MAX, (N + gran - 1) / gran * gran));
     kp.cols_per_tile = kp.bn;
@@ -1391,6 +1404,34 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
   // leave more rows empty).
   const bool pair = a.pair_ok && !a.a_gather && kp.bn == 256 && kp.ksplit == 1 &&
                     pair_tiles_requested();
+  // bf16 weights with N a multiple of 64: view each expert's [K, N] (gate/up:
+  // [K, 2, N]) matrix as 64-column blocks, [block][K][64], so that one TMA load
+  // brings all the blocks of a stage in the layout the MMA reads (box 0 at
+  // offset 0, box j at j * 8 KB).  Otherwise one load per 64-column box.
+  kp.b_wide = (!a.b_fp8 && N % 64 == 0) ? 1 : 0;
+  const uint64_t G64 = static_cast<uint64_t>(a.G);
+  if (kp.b_wide && a.epilogue == kEpiGateUpAct) {
+    const uint64_t dims[5] = {64, K, N / 64, 2, G64};
+    const uint64_t strides[4] = {2 * N * eb, 64 * eb, N * eb, K * 2 * N * eb};
+    const uint32_t box[5] = {64, BK, 2, pair ? 1u : 2u, 1};
+    if (!encode_tmap(&tb, a.B, 5, dims, strides, box, bdt)) return cudaErrorInvalidValue;
+  } else if (kp.b_wide) {
+    const uint64_t dims[4] = {64, K, N / 64, G64};
+    const uint64_t strides[3] = {N * eb, 64 * eb, K * N * eb};
+    const uint32_t nb = static_cast<uint32_t>(kp.bn / 64) / (pair ? 2u : 1u);
+    const uint32_t box[4] = {64, BK, nb, 1};
+    if (!encode_tmap(&tb, a.B, 4, dims, strides, box, bdt)) return cudaErrorInvalidValue;
+  } else if (a.epilogue == kEpiGateUpAct) {
+    const uint64_t dims[4] = {N, 2, K, G64};
+    const uint64_t strides[3] = {N * eb, 2 * N * eb, K * 2 * N * eb};
+    const uint32_t box[4] = {box_n, 1, BK, 1};
+    if (!encode_tmap(&tb, a.B, 4, dims, strides, box, bdt)) return cudaErrorInvalidValue;
+  } else {
+    const uint64_t dims[3] = {N, K, G64};
+    const uint64_t strides[2] = {N * eb, K * N * eb};
+    const uint32_t box[3] = {box_n, BK, 1};
+    if (!encode_tmap(&tb, a.B, 3, dims, strides, box, bdt)) return cudaErrorInvalidValue;
+  }
   const int tile_m = pair ? 2 * BM : BM;
   const long long max_tiles = (static_cast<long long>((a.M + tile_m - 1) / tile_m) + a.G) *
                               static_cast<long long>(kp.n_tiles) * kp.ksplit;

@@ -503,7 +503,7 @@ int moe_set_option(int option, int value) {
     }
     case MOE_OPT_DECODE_KERNEL: {
       const int old = g_decode_kernel;
-      g_decode_kernel = value < 0 ? 0 : (value > 2 ? 2 : value);
+      g_decode_kernel = value < 0 ? 0 : (value > 3 ? 3 : value);
       return old;
     }
     case MOE_OPT_GATHER_A: {

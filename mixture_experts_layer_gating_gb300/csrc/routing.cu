@@ -425,7 +425,6 @@ __global__ void permute_gather_kernel(const uint4* __restrict__ x,
                                       const float* __restrict__ tok_scale,
                                       float* __restrict__ row_scale, int32_t* err) {
   pdl_wait();
-  pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
   const long long wstride = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
   for (long long p = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -453,6 +452,7 @@ __global__ void permute_gather_kernel(const uint4* __restrict__ x,
     }
     for (; v < vec_per_row; v += 32) dst[v] = src[v];
   }
+  pdl_launch_dependents();  // after the copy: long kernel, see finalize_kernel
 }
 
 // ------------------------------------------------------------------------
@@ -566,7 +566,6 @@ __global__ void finalize_kernel(const float* __restrict__ y_perm, const int32_t*
                                 const float* __restrict__ w, const float* __restrict__ s_rows,
                                 Tt* __restrict__ out, int T, int k, int D, int R, int32_t* err) {
   pdl_wait();
-  pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
   const long long wstride = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
   const int nchunk = D / 8;              // 8 output elements per lane and chunk
@@ -634,6 +633,10 @@ __global__ void finalize_kernel(const float* __restrict__ y_perm, const int32_t*
       store8(out + t * D + c * 8, acc);
     }
   }
+  // The next kernel is scheduled once every CTA got here: an earlier trigger
+  // lets its CTAs wait beside this (at prefill, long) kernel's, which measured
+  // slower; the short routing kernels trigger at their start.
+  pdl_launch_dependents();
 }
 
 int blocks_for(long long work_items, int per_block, int cap) {

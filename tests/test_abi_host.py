@@ -126,7 +126,7 @@ def test_set_option_values():
     cases = [
         (moe.MOE_OPT_PAIR_TILES, 5, 1),
         (moe.MOE_OPT_GATHER_A, 1, 1),
-        (moe.MOE_OPT_DECODE_KERNEL, 7, 2),
+        (moe.MOE_OPT_DECODE_KERNEL, 7, 3),
         (moe.MOE_OPT_DECODE_KERNEL, -3, 0),
         (moe.MOE_OPT_PDL, 0, 0),
         (moe.MOE_OPT_PDL, 3, 1),

@@ -287,12 +287,13 @@ def _grouped_case(E, counts, D, I, act, seed, fp8=False):
     return xp, offsets, W13.to(torch.bfloat16), W2.to(torch.bfloat16)
 
 
-@pytest.fixture(params=["cta1", "pair", "decode"])
+@pytest.fixture(params=["cta1", "pair", "decode", "decode16"])
 def tile_mode(request):
     """Run a grouped-GEMM test on 128-row 1-CTA tiles, on 2-CTA (256-row)
-    tiles, and on the swap-AB decode kernel."""
+    tiles, and on the swap-AB decode kernel with 64- and 16-row tiles."""
     pair = moe.moe_set_option(moe.MOE_OPT_PAIR_TILES, 1 if request.param == "pair" else 0)
-    dec = moe.moe_set_option(moe.MOE_OPT_DECODE_KERNEL, 2 if request.param == "decode" else 0)
+    dec_mode = {"decode": 2, "decode16": 3}.get(request.param, 0)
+    dec = moe.moe_set_option(moe.MOE_OPT_DECODE_KERNEL, dec_mode)
     yield request.param
     moe.moe_set_option(moe.MOE_OPT_PAIR_TILES, pair)
     moe.moe_set_option(moe.MOE_OPT_DECODE_KERNEL, dec)
