@@ -274,6 +274,8 @@ def run_ours(args, world, rank, local):
         moe.moe_set_option(moe.MOE_OPT_DECODE_KERNEL, args.decode_kernel)
     if args.no_pdl:
         moe.moe_set_option(moe.MOE_OPT_PDL, 0)
+    if args.serial_shared:
+        moe.moe_set_option(moe.MOE_OPT_SHARED_STREAM, 0)
     shape = workload_shape(args)
     dev = torch.device("cuda", local)
     inp = workloads.make_inputs(shape, seed=rank, device=dev, weights_seed=0)
@@ -318,10 +320,8 @@ def run_ours(args, world, rank, local):
 
     # ---- per-kernel durations (instrumented pass, same work, after the timed region)
     L = moe.moe_layer_launch_count(cfg)
-    names = ["router_gemm", "topk_softmax"]
-    if shape.w_dtype == "fp8_e4m3":
-        names += ["x_to_fp16"]
     fp8 = shape.w_dtype == "fp8_e4m3"
+    names = (["x_to_fp16"] if fp8 else []) + ["router_gemm", "topk_softmax"]
     if shape.R <= 8192:  # small batches: init_routing + gather in one kernel
         names += ["route_permute"]
     else:
@@ -444,6 +444,8 @@ def main():
                     help="routed gate/up GEMM gathers x rows itself (moe_set_option MOE_OPT_GATHER_A)")
     ap.add_argument("--no-pdl", action="store_true",
                     help="plain stream order instead of programmatic dependent launch (MOE_OPT_PDL 0)")
+    ap.add_argument("--serial-shared", action="store_true",
+                    help="shared expert on the caller's stream (MOE_OPT_SHARED_STREAM 0)")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override T of the workload (smaller cases for profiling)")
     ap.add_argument("--experts", type=int, default=None,

@@ -263,6 +263,15 @@ int moe_layer_launch_count(const moe_config_t* cfg);
  *   the predecessor's completion before it touches memory); 0 = plain stream
  *   order.  Same results. */
 #define MOE_OPT_PDL 4
+/*   MOE_OPT_SHARED_STREAM: 1 (default) = moe_layer runs the shared expert
+ *   on a second stream owned by the library (one per device, created on the
+ *   first call that needs it) that forks from the caller's stream once x is
+ *   ready and joins it before the finalize kernel, so that the shared GEMMs
+ *   overlap routing and the routed GEMMs; 0 = everything on the caller's
+ *   stream.  Same results.  Fork and join are event record / wait pairs made
+ *   under a lock, so calls from several host threads stay correct (their
+ *   shared experts then serialise on the one side stream). */
+#define MOE_OPT_SHARED_STREAM 5
 int moe_set_option(int option, int value);
 
 /* Per-kernel timing hook (process-wide, off by default).  `events` holds

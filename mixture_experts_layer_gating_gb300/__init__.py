@@ -67,6 +67,7 @@ MOE_OPT_PAIR_TILES = 1
 MOE_OPT_GATHER_A = 2
 MOE_OPT_DECODE_KERNEL = 3
 MOE_OPT_PDL = 4
+MOE_OPT_SHARED_STREAM = 5
 
 
 def load_library(path: Optional[str] = None) -> ctypes.CDLL:

@@ -4,6 +4,7 @@
 
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "moe_internal.h"
 
@@ -13,7 +14,54 @@ namespace {
 
 constexpr size_t kAlign = 256;
 
-int g_gather_a = 0;  // moe_set_option(MOE_OPT_GATHER_A, .)
+int g_gather_a = 0;       // moe_set_option(MOE_OPT_GATHER_A, .)
+int g_shared_stream = 1;  // moe_set_option(MOE_OPT_SHARED_STREAM, .)
+
+// The shared expert depends on x alone, so moe_layer runs it on a second
+// stream of the library's own (one per device, created on first use) that
+// forks from the caller's stream after x is ready and joins it before the
+// finalize kernel: its GEMMs then overlap the routing kernels and the routed
+// GEMMs instead of following them.  Fork and join are event record + wait
+// pairs, which stream capture turns into graph edges.
+struct SideStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+constexpr int kMaxDevices = 64;
+SideStream g_side[kMaxDevices];
+std::mutex g_side_mu;
+
+// Fork: work enqueued on the returned stream starts after everything already
+// on s.  nullptr when the stream cannot be had (the caller then stays serial).
+cudaStream_t side_fork(cudaStream_t s) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_side_mu);
+  SideStream& d = g_side[dev];
+  if (!d.stream) {
+    if (cudaStreamCreateWithFlags(&d.stream, cudaStreamNonBlocking) != cudaSuccess) {
+      d.stream = nullptr;
+      return nullptr;
+    }
+    if (cudaEventCreateWithFlags(&d.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&d.join, cudaEventDisableTiming) != cudaSuccess)
+      return nullptr;
+  }
+  if (cudaEventRecord(d.fork, s) != cudaSuccess) return nullptr;
+  if (cudaStreamWaitEvent(d.stream, d.fork, 0) != cudaSuccess) return nullptr;
+  return d.stream;
+}
+
+// Join: work enqueued on s after this starts after everything on `side`.
+bool side_join(cudaStream_t side, cudaStream_t s) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  std::lock_guard<std::mutex> lock(g_side_mu);
+  SideStream& d = g_side[dev];
+  if (d.stream != side) return false;
+  return cudaEventRecord(d.join, side) == cudaSuccess &&
+         cudaStreamWaitEvent(s, d.join, 0) == cudaSuccess;
+}
 
 // Optional per-kernel trace events (moe_set_trace_events).
 void* const* g_trace_events = nullptr;
@@ -431,9 +479,6 @@ int moe_layer(const moe_config_t* cfg, const void* x, const void* Wg, const floa
 
   const bool traced = g_trace_events && g_trace_n >= moe_layer_launch_count(cfg) + 1;
   g_trace_next = traced ? 0 : -1;
-  float* partials = L.router_partials ? reinterpret_cast<float*>(ws_at(ws, L.router_partials)) : nullptr;
-  st = do_route(cfg, x, Wg, logit_bias, logits, ids, w, partials, err, s);
-  if (st != MOE_OK) return (g_trace_next = -1, st);
   const bool fp8 = cfg->w_dtype == MOE_FP8_E4M3;
   const void* x_rows = x;  // what the gather and the shared expert read
   float* tok_inv = nullptr;
@@ -449,6 +494,30 @@ int moe_layer(const moe_config_t* cfg, const void* x, const void* Wg, const floa
       return (g_trace_next = -1, MOE_ERR_CUDA);
     x_rows = x16;
   }
+  // The shared expert on the side stream (not while tracing: the trace
+  // events time kernels one after another on the caller's stream).
+  cudaStream_t side = nullptr;
+  if (shared && g_shared_stream && !traced) {
+    side = side_fork(s);
+    if (side) {
+      st = do_ffn(cfg, x_rows, tok_inv, cfg->T, nullptr, 1, W13s, s13s, W2s, s2s, cfg->I_shared, h_s,
+                  s_out, fp8 ? ws_at(ws, L.hs16) : nullptr,
+                  fp8 ? reinterpret_cast<float*>(ws_at(ws, L.hs_inv)) : nullptr, err, side);
+      if (st != MOE_OK) {
+        side_join(side, s);
+        return (g_trace_next = -1, st);
+      }
+    }
+  }
+  // after the fork every early return first joins the side stream back
+  auto fail = [&](int code) {
+    if (side) side_join(side, s);
+    g_trace_next = -1;
+    return code;
+  };
+  float* partials = L.router_partials ? reinterpret_cast<float*>(ws_at(ws, L.router_partials)) : nullptr;
+  st = do_route(cfg, x, Wg, logit_bias, logits, ids, w, partials, err, s);
+  if (st != MOE_OK) return fail(st);
   // Default: a permuted copy of x (the gather kernel streams at HBM speed).
   // With MOE_OPT_GATHER_A the routed gate/up pass instead gathers its rows from
   // x (or its fp16 copy) with TMA tile::gather4 loads (slower on GB300: 32
@@ -456,11 +525,12 @@ int moe_layer(const moe_config_t* cfg, const void* x, const void* Wg, const floa
   const bool gather = g_gather_a && cfg->act_dtype != MOE_F32;
   st = do_permute(cfg, ids, gather ? nullptr : x_rows, counts, offsets, sorted_rows, dest,
                   gather ? nullptr : x_perm, seg, err, s, tok_inv, row_inv);
-  if (st != MOE_OK) return (g_trace_next = -1, st);
+  if (st != MOE_OK) return fail(st);
   st = do_grouped_ffn(cfg, gather ? x_rows : x_perm, gather ? tok_inv : row_inv, offsets, W13, s13,
-                      W2, s2, h, y_perm, shared ? x_rows : nullptr, tok_inv, W13s, s13s, W2s, s2s,
-                      h_s, s_out, ws, err, s, gather ? sorted_rows : nullptr);
-  if (st != MOE_OK) return (g_trace_next = -1, st);
+                      W2, s2, h, y_perm, (shared && !side) ? x_rows : nullptr, tok_inv, W13s, s13s,
+                      W2s, s2s, h_s, s_out, ws, err, s, gather ? sorted_rows : nullptr);
+  if (st != MOE_OK) return fail(st);
+  if (side && !side_join(side, s)) return (g_trace_next = -1, MOE_ERR_CUDA);
   trace_mark(s);
   st = cuda_status(launch_finalize(cfg->act_dtype, y_perm, dest, w, shared ? s_out : nullptr, out,
                                    cfg->T, cfg->k, cfg->D, cfg->T * cfg->k, err, s));
@@ -509,6 +579,11 @@ int moe_set_option(int option, int value) {
     case MOE_OPT_GATHER_A: {
       const int old = g_gather_a;
       g_gather_a = value ? 1 : 0;
+      return old;
+    }
+    case MOE_OPT_SHARED_STREAM: {
+      const int old = g_shared_stream;
+      g_shared_stream = value ? 1 : 0;
       return old;
     }
     case MOE_OPT_PDL: {

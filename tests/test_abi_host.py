@@ -130,6 +130,8 @@ def test_set_option_values():
         (moe.MOE_OPT_DECODE_KERNEL, -3, 0),
         (moe.MOE_OPT_PDL, 0, 0),
         (moe.MOE_OPT_PDL, 3, 1),
+        (moe.MOE_OPT_SHARED_STREAM, 0, 0),
+        (moe.MOE_OPT_SHARED_STREAM, 2, 1),
     ]
     for opt, value, stored in cases:
         old = moe.moe_set_option(opt, value)

@@ -167,6 +167,23 @@ def test_layer_same_result_without_pdl(case, pair):
         moe.moe_set_option(moe.MOE_OPT_PAIR_TILES, old_pair)
 
 
+@pytest.mark.parametrize("case", ["gemma4_T256", "gemma4_T8_decode", "fp8_small_T300",
+                                  "fp8_small_geglu_T77", "qwen35_T64"])
+def test_layer_same_result_with_shared_expert_stream(case):
+    """The shared expert on the library's side stream (default) and on the
+    caller's stream give bit-identical outputs, over repeated calls."""
+    shape = LAYER_CASES[case]
+    inp = workloads.make_inputs(shape, seed=7, device="cuda")
+    old = moe.moe_set_option(moe.MOE_OPT_SHARED_STREAM, 0)
+    try:
+        serial = run_layer(shape, inp)["out"].clone()
+        moe.moe_set_option(moe.MOE_OPT_SHARED_STREAM, 1)
+        for _ in range(3):
+            assert torch.equal(run_layer(shape, inp)["out"], serial)
+    finally:
+        moe.moe_set_option(moe.MOE_OPT_SHARED_STREAM, old)
+
+
 @pytest.mark.parametrize("case", ["qwen3_T512", "fp8_small_T300", "gemma4_T256"])
 def test_layer_parity_gemm_gathers_rows(case):
     """MOE_OPT_GATHER_A: the routed gate/up GEMM reads x rows with TMA gather4."""
