@@ -29,7 +29,7 @@
 //                 two accumulator buffers (2 x 256 columns).
 //   warps 2..5  : epilogue -- tcgen05.ld 32 lanes x 32 columns, activation /
 //                 scale, masked stores; one row per thread.
-//   warps 6..9  : (fp8 weights only) converters -- TMA brings the raw e4m3
+//   warps 6..13 : (fp8 weights only) converters -- TMA brings the raw e4m3
 //                 weight boxes; these warps expand them exactly to 16-bit
 //                 floats in the swizzled N-major layout the MMA reads, then
 //                 arrive on the stage's full barrier (W8A16).  Both passes run
@@ -83,7 +83,11 @@ struct StageCfg {
   static constexpr int kStageBytes = kABytes + kBBytes + kRawBytes;
   static constexpr int kStages =
       STAGE_BUDGET / kStageBytes > MAX_STAGES ? MAX_STAGES : STAGE_BUDGET / kStageBytes;
-  static constexpr int kThreads = FP8 ? 320 : 192;
+  // fp8: e4m3 -> fp16 converter warps (6 ..): the expansion limits the fp8
+  // passes; 8 warps measured 11 % faster than 4 on the Ling prefill layer, 10
+  // no better
+  static constexpr int kConvWarps = 8;
+  static constexpr int kThreads = FP8 ? (6 + kConvWarps) * 32 : 192;
   static constexpr int kTileM = PAIR ? 2 * BM : BM;  // rows per scheduled tile
 };
 
@@ -304,11 +308,11 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
   // ---------------------------------------------------------------- set-up
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      // fp8: the stage is full once the A bytes landed and all 128 converter
-      // threads stored their part of the bf16 B tile
+      // fp8: the stage is full once the A bytes landed and all converter
+      // threads stored their part of the 16-bit B tile
       // (one arrival per converter warp; in a pair both CTAs' converters and
       // A loads report to the leader's barrier)
-      mbar_init(&ctrl->full[s], FP8 ? 1 + 4 * (PAIR ? 2 : 1) : 1);
+      mbar_init(&ctrl->full[s], FP8 ? 1 + Cfg::kConvWarps * (PAIR ? 2 : 1) : 1);
       mbar_init(&ctrl->empty[s], 1);
       mbar_init(&ctrl->raw_full[s], 1);
     }
@@ -546,7 +550,8 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
   } else if (warp >= 6) {
     // ------------------------------------------------------------ fp8 converters
     if (FP8) {
-      const int tid = threadIdx.x - 6 * 32;  // 0..127
+      constexpr int NCONV = Cfg::kConvWarps * 32;
+      const int tid = threadIdx.x - 6 * 32;  // 0 .. NCONV - 1
       const int nraw = PAIR ? 1 : (p.bn + 127) / 128;
       uint32_t stage = 0, phase = 0;
       bool ok = true;
@@ -563,7 +568,7 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
           // raw box b: 64 rows x 128 bytes (128 e4m3 columns), 128-byte swizzled;
           // each thread expands 16-byte raw chunks into two 16-byte bf16 chunks of
           // the N-major bf16 boxes (64 columns each) the MMA descriptor reads.
-          for (int q = tid; q < nraw * 512; q += 128) {
+          for (int q = tid; q < nraw * 512; q += NCONV) {
             const int b = q >> 9, r = (q >> 3) & 63, cc = q & 7;
             const uint4 v = *reinterpret_cast<const uint4*>(raw + b * RAW_BOX_BYTES + r * 128 +
                                                             ((cc ^ (r & 7)) << 4));
@@ -794,7 +799,10 @@ struct DecCfg {
   static constexpr int kStageBytes = DEC_W_BYTES + kTokBytes + kRawBytes;
   static constexpr int kStages =
       STAGE_BUDGET / kStageBytes > MAX_STAGES ? MAX_STAGES : STAGE_BUDGET / kStageBytes;
-  static constexpr int kThreads = FP8 ? 320 : 192;
+  // fp8: e4m3 -> fp16 converter warps (6 ..); 8 measured slower here (each
+  // stage expands only 8 KB of weights)
+  static constexpr int kConvWarps = 4;
+  static constexpr int kThreads = FP8 ? (6 + kConvWarps) * 32 : 192;
 };
 
 template <bool SPLIT, bool FP8>
@@ -836,7 +844,7 @@ __global__ void __launch_bounds__(DecCfg<SPLIT, FP8>::kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&ctrl->full[s], FP8 ? 1 + 4 : 1);
+      mbar_init(&ctrl->full[s], FP8 ? 1 + Cfg::kConvWarps : 1);
       mbar_init(&ctrl->empty[s], 1);
       mbar_init(&ctrl->raw_full[s], 1);
     }
@@ -982,9 +990,11 @@ __global__ void __launch_bounds__(DecCfg<SPLIT, FP8>::kThreads, 1)
           // raw box b: 64 rows (K) x 64 bytes (64 e4m3 features), unswizzled;
           // each 16-byte chunk becomes two 16-byte fp16 chunks of the 128B-swizzled
           // 64-feature box b of the weight tile
+          constexpr int NCONV = Cfg::kConvWarps * 32;
+          static_assert(512 % NCONV == 0, "converter threads divide the stage's 512 chunks");
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int q = tid + 128 * i;
+          for (int i = 0; i < 512 / NCONV; ++i) {
+            const int q = tid + NCONV * i;
             const int b = q >> 8, r = (q >> 2) & 63, c = q & 3;
             const uint4 v = *reinterpret_cast<const uint4*>(raw + b * DEC_RAW_BOX_BYTES + r * 64 + c * 16);
             const uint2 o0 = e4m3x4_to_f16x4(v.x), o1 = e4m3x4_to_f16x4(v.y);

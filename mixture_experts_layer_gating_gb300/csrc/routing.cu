@@ -6,6 +6,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <algorithm>
 #include <cfloat>
 #include <climits>
 
@@ -530,8 +531,9 @@ __global__ void rows_to_fp16_kernel(const Tin* __restrict__ x, int rows, int D,
 // finalize_routing ("CANN/cann-recipes-infer：Qwen3-MoE优化", section
 // "GMM使能和Routing优化") fused with the shared-expert add ("千问 3.5 MoE 在
 // TPU 上的系统优化实战": y = Router(x) + SharedExpert(x)).  One warp per
-// (token, 256-column slice), so that small batches still spread over every
-// SM; fp32 expert rows and shared row, fp32 accumulation with j ascending,
+// (token, m 256-column slices): m is chosen so that small batches still
+// spread over every SM while large ones keep whole rows per warp; fp32
+// expert rows and shared row, fp32 accumulation with j ascending,
 // shared row last, one rounding to the output type.
 __device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&f)[8]) {
   const uint4 u = *reinterpret_cast<const uint4*>(p);
@@ -564,17 +566,19 @@ __device__ __forceinline__ void store8(float* p, const float (&f)[8]) {
 template <typename Tt, int KMAX>
 __global__ void finalize_kernel(const float* __restrict__ y_perm, const int32_t* __restrict__ dest,
                                 const float* __restrict__ w, const float* __restrict__ s_rows,
-                                Tt* __restrict__ out, int T, int k, int D, int R, int32_t* err) {
+                                Tt* __restrict__ out, int T, int k, int D, int R, int m,
+                                int32_t* err) {
   pdl_wait();
   const int lane = threadIdx.x & 31;
   const long long wstride = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
   const int nchunk = D / 8;              // 8 output elements per lane and chunk
-  const int nslice = (nchunk + 31) / 32;  // one warp item: a token x 256 columns
-  const long long items = static_cast<long long>(T) * nslice;
+  const int nslice = (nchunk + 31) / 32;  // 256-column slices of a row
+  const int nper = (nslice + m - 1) / m;  // warp items per token: m slices each
+  const long long items = static_cast<long long>(T) * nper;
   for (long long it = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
        it < items; it += wstride) {
-    const long long t = it / nslice;
-    const int c = static_cast<int>(it - t * nslice) * 32 + lane;
+    const long long t = it / nper;
+    const int s0 = static_cast<int>(it - t * nper) * m;
     // lanes < k fetch one (position, weight) pair each; a bad position is
     // flagged and replaced by row 0 with weight 0 so every load stays in bounds
     int my_p = 0;
@@ -595,7 +599,7 @@ __global__ void finalize_kernel(const float* __restrict__ y_perm, const int32_t*
       pj[j] = __shfl_sync(FULL, my_p, j);
       wj[j] = __shfl_sync(FULL, my_w, j);
     }
-    if (c < nchunk) {
+    for (int c = s0 * 32 + lane; c < min(nslice, s0 + m) * 32 && c < nchunk; c += 32) {
       // issue all k row loads before any arithmetic so they are in flight together
       float4 a[KMAX], b[KMAX];
 #pragma unroll
@@ -751,7 +755,14 @@ cudaError_t launch_finalize(int act_dtype, const void* y_perm, const int32_t* de
                             int32_t* err, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
   const int threads = 256;
-  const long long items = static_cast<long long>(T) * ((D / 8 + 31) / 32);
+  // warp items of m 256-column slices: whole rows (measured fastest) when
+  // there are enough tokens for ~16 warps per SM, else rows halved until
+  // there are (single slices for decode batches)
+  const int nslice = (D / 8 + 31) / 32;
+  const long long target = static_cast<long long>(device_sm_count()) * 16;
+  int m = nslice;
+  while (m > 1 && static_cast<long long>(T) * ((nslice + m - 1) / m) < target) m = (m + 1) / 2;
+  const long long items = static_cast<long long>(T) * ((nslice + m - 1) / m);
   const int blocks = blocks_for(items, threads / 32, device_sm_count() * 16);
   const float* y = static_cast<const float*>(y_perm);
   const float* sr = static_cast<const float*>(s_rows);
@@ -760,11 +771,11 @@ cudaError_t launch_finalize(int act_dtype, const void* y_perm, const int32_t* de
     if (act_dtype == MOE_BF16) {                                                  \
       auto kern = finalize_kernel<__nv_bfloat16, KM>;                             \
       MOE_LAUNCH(kern, blocks, threads, 0, s, y, dest, w, sr,                     \
-                 static_cast<__nv_bfloat16*>(out), T, k, D, R, err);              \
+                 static_cast<__nv_bfloat16*>(out), T, k, D, R, m, err);           \
     } else {                                                                      \
       auto kern = finalize_kernel<float, KM>;                                     \
       MOE_LAUNCH(kern, blocks, threads, 0, s, y, dest, w, sr,                     \
-                 static_cast<float*>(out), T, k, D, R, err);                      \
+                 static_cast<float*>(out), T, k, D, R, m, err);                   \
     }                                                                             \
   } while (0)
   if (k <= 2) MOE_FIN(2);
