@@ -241,35 +241,16 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Four e4m3 values (bytes of w, low byte first) to four bf16, exactly.
-// Each byte's sign goes to the bf16 sign bit and its 4-bit exponent and 3-bit
-// mantissa to the low exponent bits and top mantissa bits: that bf16 equals
-// the e4m3 value times 2^-120 (an e4m3 subnormal becomes a bf16 subnormal).
-// One bf16x2 multiplication by 2^120 -- exact, bf16 arithmetic keeps
-// subnormal inputs -- gives the value.  The NaN encoding (S.1111.111) is not
-// produced by the saturating quantisation and is not handled.
-__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t u /* [0, b1, 0, b0] */) {
-  const uint32_t bits = ((u << 8) & 0x80008000u) | ((u & 0x007F007Fu) << 4);
-  __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&bits);
-  const __nv_bfloat162 k = __floats2bfloat162_rn(0x1p120f, 0x1p120f);
-  v = __hmul2(v, k);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-__device__ __forceinline__ uint2 e4m3x4_to_bf16x4(uint32_t w) {
-  return make_uint2(e4m3x2_to_bf16x2(__byte_perm(w, 0u, 0x4140)),
-                    e4m3x2_to_bf16x2(__byte_perm(w, 0u, 0x4342)));
-}
-
-// Four e4m3 values to four fp16 (exact: every e4m3 value is an fp16 value),
-// one hardware conversion per pair; element order is kept (low byte first).
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
-  uint32_t r;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
-  return r;
-}
+// Four e4m3 values (bytes of w, low byte first) to four fp16, exactly (every
+// e4m3 value is an fp16 value): one hardware conversion per pair, element
+// order kept.
 __device__ __forceinline__ uint2 e4m3x4_to_f16x4(uint32_t w) {
-  return make_uint2(e4m3x2_to_f16x2(static_cast<uint16_t>(w & 0xFFFFu)),
-                    e4m3x2_to_f16x2(static_cast<uint16_t>(w >> 16)));
+  uint2 r;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, lo;\n\tcvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
+      : "=r"(r.x), "=r"(r.y)
+      : "r"(w));
+  return r;
 }
 
 template <int EPI, bool SPLIT, bool FP8, bool PAIR>
@@ -553,6 +534,22 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
       constexpr int NCONV = Cfg::kConvWarps * 32;
       const int tid = threadIdx.x - 6 * 32;  // 0 .. NCONV - 1
       const int nraw = PAIR ? 1 : (p.bn + 127) / 128;
+      // 16-byte chunk q = tid + NCONV * i of the stage's raw boxes (512 per box):
+      // its offset in the raw boxes and those of its two fp16 chunks
+      constexpr int kConvIters = 2 * 512 / NCONV;
+      static_assert(2 * 512 % NCONV == 0, "converter threads divide the raw chunks");
+      const int conv_iters = nraw * 512 / NCONV;
+      uint32_t conv_src[kConvIters], conv_dst0[kConvIters], conv_dst1[kConvIters];
+#pragma unroll
+      for (int i = 0; i < kConvIters; ++i) {
+        const int q = tid + NCONV * i;
+        const int b = q >> 9, r = (q >> 3) & 63, cc = q & 7;
+        conv_src[i] = b * RAW_BOX_BYTES + r * 128 + ((cc ^ (r & 7)) << 4);
+        const int j = 2 * b + (cc >> 2);  // 64-column fp16 box
+        const int lc = 2 * (cc & 3);      // first logical 16-byte chunk in the row
+        conv_dst0[i] = j * B_BOX_BYTES + r * 128 + ((lc ^ (r & 7)) << 4);
+        conv_dst1[i] = j * B_BOX_BYTES + r * 128 + (((lc + 1) ^ (r & 7)) << 4);
+      }
       uint32_t stage = 0, phase = 0;
       bool ok = true;
       for (int t = work0; t < total_tiles && ok; t += work_stride) {
@@ -566,30 +563,18 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
           const uint8_t* raw = stage_raw(stage);
           uint8_t* dst = stage_b(stage);
           // raw box b: 64 rows x 128 bytes (128 e4m3 columns), 128-byte swizzled;
-          // each thread expands 16-byte raw chunks into two 16-byte bf16 chunks of
-          // the N-major bf16 boxes (64 columns each) the MMA descriptor reads.
-          for (int q = tid; q < nraw * 512; q += NCONV) {
-            const int b = q >> 9, r = (q >> 3) & 63, cc = q & 7;
-            const uint4 v = *reinterpret_cast<const uint4*>(raw + b * RAW_BOX_BYTES + r * 128 +
-                                                            ((cc ^ (r & 7)) << 4));
-            uint2 o0, o1, o2, o3;
-            if (F16) {
-              o0 = e4m3x4_to_f16x4(v.x);
-              o1 = e4m3x4_to_f16x4(v.y);
-              o2 = e4m3x4_to_f16x4(v.z);
-              o3 = e4m3x4_to_f16x4(v.w);
-            } else {
-              o0 = e4m3x4_to_bf16x4(v.x);
-              o1 = e4m3x4_to_bf16x4(v.y);
-              o2 = e4m3x4_to_bf16x4(v.z);
-              o3 = e4m3x4_to_bf16x4(v.w);
+          // each thread expands 16-byte raw chunks into two 16-byte fp16 chunks of
+          // the N-major fp16 boxes (64 columns each) the MMA descriptor reads.
+          // The chunk offsets depend only on the thread (computed once, above).
+#pragma unroll
+          for (int i = 0; i < kConvIters; ++i) {
+            if (i < conv_iters) {
+              const uint4 v = *reinterpret_cast<const uint4*>(raw + conv_src[i]);
+              const uint2 o0 = e4m3x4_to_f16x4(v.x), o1 = e4m3x4_to_f16x4(v.y);
+              const uint2 o2 = e4m3x4_to_f16x4(v.z), o3 = e4m3x4_to_f16x4(v.w);
+              *reinterpret_cast<uint4*>(dst + conv_dst0[i]) = make_uint4(o0.x, o0.y, o1.x, o1.y);
+              *reinterpret_cast<uint4*>(dst + conv_dst1[i]) = make_uint4(o2.x, o2.y, o3.x, o3.y);
             }
-            const int j = 2 * b + (cc >> 2);  // bf16 box
-            const int lc = 2 * (cc & 3);      // first logical 16-byte chunk in the row
-            uint8_t* row = dst + j * B_BOX_BYTES + r * 128;
-            *reinterpret_cast<uint4*>(row + ((lc ^ (r & 7)) << 4)) = make_uint4(o0.x, o0.y, o1.x, o1.y);
-            *reinterpret_cast<uint4*>(row + (((lc + 1) ^ (r & 7)) << 4)) =
-                make_uint4(o2.x, o2.y, o3.x, o3.y);
           }
           fence_proxy_async_smem();  // generic-proxy stores -> tensor core reads
           __syncwarp();
