@@ -239,10 +239,11 @@ int moe_layer_launch_count(const moe_config_t* cfg);
 /* Kernel-variant options (process-wide; set them from the thread that
  * launches, between calls).  Returns the previous value, or
  * MOE_ERR_INVALID_ARG for an unknown option.
- *   MOE_OPT_PAIR_TILES: 1 = grouped GEMMs with a full 256-column B tile use
- *   2-CTA clusters (tcgen05 cta_group::2, M = 256 rows per tile, each CTA
- *   loading half of B); 0 (default) = one CTA per 128-row tile.  Results are
- *   the same up to fp32 summation order. */
+ *   MOE_OPT_PAIR_TILES: 1 = bf16 grouped GEMMs with a full 256-column B tile
+ *   use 2-CTA clusters (tcgen05 cta_group::2, M = 256 rows per tile, each CTA
+ *   loading half of B); fp8-weight GEMMs keep one CTA per tile; 0 (default) =
+ *   one CTA per 128-row tile.  Results are the same up to fp32 summation
+ *   order. */
 #define MOE_OPT_PAIR_TILES 1
 /*   MOE_OPT_GATHER_A: 1 = moe_layer does not materialise the permuted rows;
  *   the routed gate/up GEMM gathers its A rows from x with TMA tile::gather4

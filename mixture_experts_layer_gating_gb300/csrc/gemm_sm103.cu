@@ -1396,8 +1396,10 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
   // 2-CTA tiles need a full 256-column B tile and no split-K.  They are used
   // only when requested with moe_set_option(MOE_OPT_PAIR_TILES, 1) (measured
   // slower than 1-CTA tiles on the configured workloads, where 256-row tiles
-  // leave more rows empty).
-  const bool pair = a.pair_ok && !a.a_gather && kp.bn == 256 && kp.ksplit == 1 &&
+  // leave more rows empty), and never for fp8 weights: there they measured
+  // 40 % slower, and a 2-CTA fp8 run at full Ling size with eight converter
+  // warps per CTA ended in a GPU fault whose cause was not found.
+  const bool pair = a.pair_ok && !a.a_gather && !a.b_fp8 && kp.bn == 256 && kp.ksplit == 1 &&
                     pair_tiles_requested();
   // bf16 weights with N a multiple of 64: view each expert's [K, N] (gate/up:
   // [K, 2, N]) matrix as 64-column blocks, [block][K][64], so that one TMA load

@@ -218,6 +218,45 @@ def test_route_from_logits_bit_exact(E, k, renorm):
     assert np.array_equal(ids[5].cpu().numpy(), np.arange(k))
 
 
+@pytest.mark.parametrize("T,E,k,renorm,bias", [
+    (2048, 64, 4, 1, False), (2048, 256, 16, 0, True), (3000, 128, 8, 1, True),  # fused top-k
+    (2047, 64, 4, 1, False), (512, 256, 8, 0, True),                           # split-K + top-k kernel
+])
+def test_route_projection_then_topk_bit_exact(T, E, k, renorm, bias):
+    """moe_route from x and W_g: routing bit-exact against the oracle's top-k of
+    the GPU's own logits, logits against the fp64 projection.  Duplicate
+    columns of W_g make exact ties that the lowest expert index must win; at
+    >= 2048 tokens and <= 256 experts the top-k runs in the projection's epilogue."""
+    D = 256
+    gen = torch.Generator(device="cuda").manual_seed(T + E + k)
+    x = torch.randn((T, D), generator=gen, device="cuda").to(torch.bfloat16)
+    Wg = (0.05 * torch.randn((D, E), generator=gen, device="cuda")).to(torch.bfloat16)
+    Wg[:, 5] = Wg[:, 3]
+    Wg[:, 11] = Wg[:, 10]
+    Wg[:, 12] = Wg[:, 10]
+    x[7] = 0  # a token whose logits are all equal (zero, plus the bias)
+    b = (0.01 * torch.randn((E,), generator=gen, device="cuda")) if bias else None
+    if bias:
+        b[5] = b[3]
+        b[11] = b[10]
+        b[12] = b[10]
+    cfg = moe.make_config(T, D, E, k, 64, renormalize=renorm)
+    ws = _ws_for(cfg)
+    L = torch.empty((T, E), dtype=torch.float32, device="cuda")
+    ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    moe.moe_route(cfg, x, Wg, b, L, ids, w, ws)
+    assert moe.moe_read_device_status(ws) == 0
+    L_gpu = L.cpu().double().numpy()
+    ids_o, w_o = oracle.topk_softmax(L_gpu, k, renorm)
+    assert np.array_equal(ids.cpu().numpy(), ids_o)
+    assert np.max(np.abs(w.cpu().double().numpy() - w_o)) <= 1e-6
+    L_ref = oracle.router_logits(x.cpu(), Wg.cpu(), b.cpu() if bias else None)
+    assert np.max(np.abs(L_gpu - L_ref)) <= 1e-3 * max(1.0, rms(L_ref))
+    if not bias:
+        assert np.array_equal(ids[7].cpu().numpy(), np.arange(k))
+
+
 @pytest.mark.parametrize("T,E,k,pattern", [
     (1000, 128, 8, "uniform"), (3000, 512, 10, "uniform"), (129, 8, 2, "one_hot"),
     (4096, 256, 8, "skew"), (1, 4, 1, "uniform"), (2500, 64, 6, "empty_half"),
