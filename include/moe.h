@@ -252,10 +252,12 @@ int moe_layer_launch_count(const moe_config_t* cfg);
 #define MOE_OPT_GATHER_A 2
 /*   MOE_OPT_DECODE_KERNEL: 1 (default) = the swap-AB decode kernel (weights
  *   as the 128-row MMA operand, 16 or 64 rows per tile, each active expert's
- *   weights streamed once) for decode-size passes where it is faster: at most
- *   one row per group on average, a single group (shared expert) of at most
- *   64 rows, or fp8 weights at up to 16 rows per group; 0 = always the 128-row-tile kernel; 2 / 3 = the decode kernel
- *   with 64 / 16 rows per tile for every routed or shared FFN pass (testing).  Same results up to fp32
+ *   weights streamed once) for decode-size passes where it measured faster: a
+ *   single group (shared expert) of at most 64 rows, at most one row per group
+ *   on average, up to 4 rows per group with at most 256 groups (bf16), or fp8
+ *   weights at up to 16 rows per group; 0 = always the 128-row-tile kernel;
+ *   2 / 3 = the decode kernel with 64 / 16 rows per tile for every routed or
+ *   shared FFN pass (testing).  Same results up to fp32
  *   summation order. */
 #define MOE_OPT_DECODE_KERNEL 3
 /*   MOE_OPT_PDL: 1 (default) = kernels are launched with programmatic

@@ -771,8 +771,10 @@ constexpr int DEC_NT_MAX = 64;                           // MMA N: rows per tile
 constexpr int DEC_W_BYTES = DEC_M * BK * 2;              // 16-bit weight tile, two 64-feature boxes
 constexpr int DEC_TOK_BYTES = DEC_NT_MAX * BK * 2;       // row tile (one plane)
 constexpr int DEC_RAW_BOX_BYTES = 64 * BK;               // 64 e4m3 features x 64 K, unswizzled
-constexpr uint32_t DEC_TMEM_COLS = 128;                  // two accumulators of <= 64 columns
-constexpr int DEC_ACC_STRIDE = 64;
+// two accumulators of <= 128 columns (the split down pass stacks the h_hi
+// and h_lo rows along N: 2 * rows columns)
+constexpr uint32_t DEC_TMEM_COLS = 256;
+constexpr int DEC_ACC_STRIDE = 128;
 constexpr int DEC_UP_FLOATS = DEC_NT_MAX * 64;           // up values of a gate/up tile
 
 template <bool SPLIT, bool FP8>
@@ -879,7 +881,7 @@ __global__ void __launch_bounds__(DecCfg<SPLIT, FP8>::kThreads, 1)
           mbar_arrive_expect_tx(&ctrl->full[stage], tx);
           tma_load_2d(stage_rows(stage), &tmap_rows, &ctrl->full[stage], kb * BK, ti.row0, pol_rows);
           if (SPLIT)
-            tma_load_2d(stage_rows(stage) + DEC_TOK_BYTES, &tmap_rows_lo, &ctrl->full[stage],
+            tma_load_2d(stage_rows(stage) + NT * 128, &tmap_rows_lo, &ctrl->full[stage],
                         kb * BK, ti.row0, pol_rows);
           uint8_t* wdst = FP8 ? stage_raw(stage) : stage_w(stage);
           uint64_t* wbar = FP8 ? &ctrl->raw_full[stage] : &ctrl->full[stage];
@@ -907,8 +909,13 @@ __global__ void __launch_bounds__(DecCfg<SPLIT, FP8>::kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = FP8 ? make_idesc_f16_f32(DEC_M, NT, 1, 0)
-                                 : make_idesc_bf16_f32(DEC_M, NT, 1, 0);
+      // split down pass: the h_lo rows follow the h_hi rows in the stage, so one
+      // MMA with N = 2 * NT covers both (accumulator columns NT.. hold the lo
+      // products; the epilogue adds them): half the MMA instructions, which
+      // at these N are what bounds the pass
+      const int mma_n = SPLIT ? 2 * NT : NT;
+      const uint32_t idesc = FP8 ? make_idesc_f16_f32(DEC_M, mma_n, 1, 0)
+                                 : make_idesc_bf16_f32(DEC_M, mma_n, 1, 0);
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
@@ -933,11 +940,6 @@ __global__ void __launch_bounds__(DecCfg<SPLIT, FP8>::kThreads, 1)
             // B = rows, K-major: 128-byte rows, K step of 16 = 32 bytes
             const uint64_t bdesc = make_smem_desc_sw128(r_addr + kk * 32, 16, 1024);
             tc_mma_f16(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0);
-            if (SPLIT) {
-              const uint64_t bdesc_lo =
-                  make_smem_desc_sw128(r_addr + DEC_TOK_BYTES + kk * 32, 16, 1024);
-              tc_mma_f16(d_tmem, adesc, bdesc_lo, idesc, 1);
-            }
           }
           tc_commit(&ctrl->empty[stage]);
           if (++stage == STAGES) {
@@ -1026,6 +1028,26 @@ __global__ void __launch_bounds__(DecCfg<SPLIT, FP8>::kThreads, 1)
       tmem_ld_32x32b_x32(taddr, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
       if (NT > 32) tmem_ld_32x32b_x32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
       tc_wait_ld();
+      if (SPLIT) {
+        // h = h_hi + h_lo: row j's lo products are in column NT + j
+        if (NT <= 16) {  // already loaded: columns 16..31
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            v[j] = __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(v[16 + j]));
+        } else {
+#pragma unroll
+          for (int q = 0; q < DEC_NT_MAX / 32; ++q) {
+            if (32 * q < NT) {
+              uint32_t lo[32];
+              tmem_ld_32x32b_x32(taddr + NT + 32 * q, lo);
+              tc_wait_ld();
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                v[32 * q + j] = __float_as_uint(__uint_as_float(v[32 * q + j]) + __uint_as_float(lo[j]));
+            }
+          }
+        }
+      }
       const int rows = ti.rows;
       bool ok = true;
       if (EPI == kEpiGateUpAct) {
@@ -1313,17 +1335,19 @@ int device_sm_count() {
 cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
   if (a.M <= 0) return cudaSuccess;
   // Swap-AB kernel (weights as the 128-row operand) where it measured faster
-  // than 128-row tiles on GB300: groups of at most one row on average (16
-  // rows per tile), a single group of at most 64 rows (the shared expert at
-  // decode), and fp8 weights at up to 16 rows per group on average (64 rows
-  // per tile).  Elsewhere 128-row tiles already stream the weights at close to
-  // HBM peak (87 % of DRAM peak on the Qwen3.5-style T=512 decode layer).
+  // than 128-row tiles on GB300, with 16 rows per tile: a single group of at
+  // most 64 rows (the shared expert at decode: more, smaller tiles), at most
+  // one row per group on average, and up to 4 rows per group when there are
+  // at most 256 groups (Qwen3-MoE decode: 223 -> 213 us); 64 rows per tile for
+  // fp8 weights at up to 16 rows per group.  Elsewhere 128-row tiles already
+  // stream the weights at close to HBM peak (Qwen3.5-style decode: 92-100 %).
   const long long Mg = a.M, Gg = a.G;
   int nt = 0;
   if (g_decode_kernel == 2) nt = DEC_NT_MAX;
   else if (g_decode_kernel == 3) nt = 16;
+  else if (Gg == 1 && Mg <= 64) nt = 16;
   else if (Mg <= Gg) nt = 16;
-  else if (Gg == 1 && Mg <= 64) nt = DEC_NT_MAX;
+  else if (!a.b_fp8 && Gg <= 256 && Mg <= 4 * Gg) nt = 16;
   else if (a.b_fp8 && Mg <= 16 * Gg) nt = DEC_NT_MAX;
   if (g_decode_kernel && nt && a.decode_ok && !a.a_gather && a.ksplit <= 1 && a.G <= MAX_G &&
       (a.epilogue == kEpiGateUpAct || a.epilogue == kEpiStoreF32)) {
