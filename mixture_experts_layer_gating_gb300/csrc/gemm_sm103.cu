@@ -490,19 +490,18 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
             break;
           }
           tc_fence_after_sync();
-          const uint32_t a_addr = smem_u32(stage_a(stage));
-          const uint32_t b_addr = smem_u32(stage_b(stage));
+          // A: K-major, 128-byte rows; a K step of 16 bf16 is 32 bytes.
+          // B: N-major, 64-column boxes 8 KB apart; a K step of 16 rows is 2 KB.
+          const uint64_t adesc0 = make_smem_desc_sw128(smem_u32(stage_a(stage)), 16, 1024);
+          const uint64_t bdesc0 = make_smem_desc_sw128(smem_u32(stage_b(stage)), B_BOX_BYTES, 1024);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
-            // A: K-major, 128-byte rows; a K step of 16 bf16 is 32 bytes.
-            const uint64_t adesc = make_smem_desc_sw128(a_addr + kk * 32, 16, 1024);
-            // B: N-major, 64-column boxes 8 KB apart; a K step of 16 rows is 2 KB.
-            const uint64_t bdesc = make_smem_desc_sw128(b_addr + kk * 2048, B_BOX_BYTES, 1024);
+            const uint64_t adesc = smem_desc_advance(adesc0, kk * 32);
+            const uint64_t bdesc = smem_desc_advance(bdesc0, kk * 2048);
             if (PAIR) tc_mma_f16_pair(d_tmem, adesc, bdesc, idesc, ((kb - kb0) | kk) != 0);
             else tc_mma_f16(d_tmem, adesc, bdesc, idesc, ((kb - kb0) | kk) != 0);
             if (SPLIT) {
-              const uint64_t adesc_lo =
-                  make_smem_desc_sw128(a_addr + A_TILE_BYTES + kk * 32, 16, 1024);
+              const uint64_t adesc_lo = smem_desc_advance(adesc0, A_TILE_BYTES + kk * 32);
               if (PAIR) tc_mma_f16_pair(d_tmem, adesc_lo, bdesc, idesc, 1);
               else tc_mma_f16(d_tmem, adesc_lo, bdesc, idesc, 1);
             }
@@ -931,14 +930,14 @@ __global__ void __launch_bounds__(DecCfg<SPLIT, FP8>::kThreads, 1)
             break;
           }
           tc_fence_after_sync();
-          const uint32_t w_addr = smem_u32(stage_w(stage));
-          const uint32_t r_addr = smem_u32(stage_rows(stage));
+          // A = weights, N-major: 64-feature groups 8 KB apart, K step of 16 rows = 2 KB
+          // B = rows, K-major: 128-byte rows, K step of 16 = 32 bytes
+          const uint64_t adesc0 = make_smem_desc_sw128(smem_u32(stage_w(stage)), DEC_W_BYTES / 2, 1024);
+          const uint64_t bdesc0 = make_smem_desc_sw128(smem_u32(stage_rows(stage)), 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
-            // A = weights, N-major: 64-feature groups 8 KB apart, K step of 16 rows = 2 KB
-            const uint64_t adesc = make_smem_desc_sw128(w_addr + kk * 2048, DEC_W_BYTES / 2, 1024);
-            // B = rows, K-major: 128-byte rows, K step of 16 = 32 bytes
-            const uint64_t bdesc = make_smem_desc_sw128(r_addr + kk * 32, 16, 1024);
+            const uint64_t adesc = smem_desc_advance(adesc0, kk * 2048);
+            const uint64_t bdesc = smem_desc_advance(bdesc0, kk * 32);
             tc_mma_f16(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0);
           }
           tc_commit(&ctrl->empty[stage]);

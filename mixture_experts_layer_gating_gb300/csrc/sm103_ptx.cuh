@@ -344,6 +344,13 @@ __device__ __forceinline__ uint64_t make_smem_desc_sw128(uint32_t saddr, uint32_
   return d;
 }
 
+// The descriptor of the same layout `bytes` further on (16-byte units in the
+// start-address field; shared-memory addresses stay below 2^18, so the field
+// does not overflow for the offsets used inside one stage).
+__device__ __forceinline__ uint64_t smem_desc_advance(uint64_t desc, uint32_t bytes) {
+  return desc + static_cast<uint64_t>(bytes >> 4);
+}
+
 // Instruction descriptor, kind::f16 with fp16 A/B and fp32 D.
 __host__ __device__ constexpr uint32_t make_idesc_f16_f32(uint32_t M, uint32_t N,
                                                           uint32_t a_mn_major,
