@@ -267,7 +267,7 @@ def run_ours(args, world, rank, local):
     barrier(world)
     moe.load_library()
     if args.pair_tiles:
-        moe.moe_set_option(moe.MOE_OPT_PAIR_TILES, 1)
+        moe.moe_set_option(moe.MOE_OPT_PAIR_TILES, args.pair_tiles)
     if args.gather_a:
         moe.moe_set_option(moe.MOE_OPT_GATHER_A, 1)
     if args.decode_kernel is not None:
@@ -465,8 +465,9 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=0,
                     help="reference arm: tokens per step (0: grown until one step takes ~--ref-step-s)")
     ap.add_argument("--ref-step-s", type=float, default=2.0)
-    ap.add_argument("--pair-tiles", action="store_true",
-                    help="grouped GEMMs on 2-CTA clusters (moe_set_option MOE_OPT_PAIR_TILES)")
+    ap.add_argument("--pair-tiles", type=int, nargs="?", const=1, default=0,
+                    help="grouped GEMMs on 2-CTA clusters (moe_set_option MOE_OPT_PAIR_TILES: "
+                         "1 with swapped tails, 2 without)")
     ap.add_argument("--decode-kernel", type=int, default=None, choices=[0, 1, 2, 3],
                     help="moe_set_option MOE_OPT_DECODE_KERNEL (0 off, 1 auto, 2/3 always with 64/16-row tiles)")
     ap.add_argument("--gather-a", action="store_true",

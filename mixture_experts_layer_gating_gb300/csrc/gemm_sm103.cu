@@ -36,6 +36,12 @@
 //                 on the fp16 kind: e4m3 -> fp16 is one hardware convert per
 //                 pair, and the A rows (x, or h) arrive as fp16 rows carrying
 //                 an exact power-of-two row scale that the epilogue removes.
+// 2-CTA mode runs a group's last tile "swapped" when it has few rows (at most
+// 64 in the gate/up pass, 128 in the down pass): the weights become the
+// M = 256 operand (128 features per CTA: gate and matching up features in the
+// gate/up pass) and the rows the N operand (N = rows rounded up to 16; the
+// down pass stacks h_hi and h_lo rows, N = 2 x that), so a short tail costs a
+// short MMA instead of a full 256-row tile.
 // Tiles are ordered (group, column tile, row tile) so that the row tiles that
 // share a weight slice run at the same time and reuse it from L2.  The tile
 // schedule is built on the device from the group offsets, so no host
@@ -139,6 +145,9 @@ struct KParams {
   int ksplit;  // K split into ksplit parts, each writing its own fp32 output plane
   int kbs;     // k-blocks per split
   int b_wide;  // bf16 B map viewed as [64-column blocks][K][64]: one load per stage
+  // 2-CTA tiles: a group's last tile with at most swap_tail rows runs "swapped":
+  // weights as the M = 256 operand (128 features per CTA), its rows as N
+  int swap_tail;
   int32_t* err;
 };
 
@@ -257,7 +266,8 @@ template <int EPI, bool SPLIT, bool FP8, bool PAIR>
 __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                         const __grid_constant__ CUtensorMap tmap_a_lo,
-                        const __grid_constant__ CUtensorMap tmap_b, const KParams p) {
+                        const __grid_constant__ CUtensorMap tmap_b,
+                        const __grid_constant__ CUtensorMap tmap_b_tail, const KParams p) {
   pdl_wait();
   using Cfg = StageCfg<SPLIT, FP8, PAIR>;
   // fp8 weights: fp16 operands; everything else: bf16 operands
@@ -301,6 +311,8 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
       mbar_init(&ctrl->tfull[a], 1);
       mbar_init(&ctrl->tempty[a], 128 * (PAIR ? 2 : 1));
     }
+    mbar_init(&ctrl->xch_full, 64);   // swapped gate/up tail: the 64 up-feature threads
+    mbar_init(&ctrl->xch_empty, 64);  // ... and the 64 gate-feature threads
     ctrl->abort = 0;
     fence_mbarrier_init();
   }
@@ -308,6 +320,7 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
     tma_prefetch_desc(&tmap_a);
     if (SPLIT) tma_prefetch_desc(&tmap_a_lo);
     tma_prefetch_desc(&tmap_b);
+    if (PAIR && EPI == kEpiGateUpAct) tma_prefetch_desc(&tmap_b_tail);
   }
   if (warp == 1) {
     if (PAIR) {  // collective over one warp of each CTA of the pair
@@ -336,6 +349,13 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
   const int nbox_cta = PAIR ? nbox / 2 : nbox;  // bf16 B boxes this CTA loads
   // barrier addresses in the leader CTA (cluster window) for the pair protocol
   auto leader_bar = [&](uint64_t* bar) { return PAIR ? mapa_shared(bar, 0) : smem_u32(bar); };
+  // swapped tail tile (2-CTA mode): its rows padded so that the MMA N (rows,
+  // or 2 x rows in the down pass) is a multiple of 32 and each CTA's half of
+  // the rows a multiple of 8
+  auto is_swap = [&](const TileInfo& ti) { return PAIR && p.swap_tail > 0 && ti.rows <= p.swap_tail; };
+  auto swap_rows = [&](const TileInfo& ti) {
+    return EPI == kEpiGateUpAct ? (ti.rows + 31) & ~31 : (ti.rows + 15) & ~15;
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -368,15 +388,53 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
         }
         int kb0, kb1;
         kb_range(t, kb0, kb1);
+        const bool swap = is_swap(ti);
+        // swapped tail: each CTA loads one 128-row box of rows (the gate/up pass:
+        // rows r * R/2 .. of the tile; the down pass: CTA 0 the h_hi rows, CTA 1
+        // the h_lo rows) and its 128 weight features
+        const uint32_t tile_tx = swap ? 2u * (A_TILE_BYTES + 2 * B_BOX_BYTES) : tx;
+        const int swap_row0 =
+            ti.row0 + (EPI == kEpiGateUpAct ? static_cast<int>(rank) * (swap_rows(ti) / 2) : 0);
         for (int kb = kb0; kb < kb1; ++kb) {
           if (lane == 0) ok = mbar_wait(&ctrl->empty[stage], phase ^ 1u, abort_flag);
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) break;
-          if (lane == 0 && leader) mbar_arrive_expect_tx(&ctrl->full[stage], tx);
+          if (lane == 0 && leader) mbar_arrive_expect_tx(&ctrl->full[stage], tile_tx);
           __syncwarp();
           const uint32_t fbar = leader_bar(&ctrl->full[stage]);
           uint8_t* a_dst = stage_a(stage);
           uint8_t* b_dst = stage_b(stage);
+          if (PAIR && swap) {
+            if (lane == 0) {
+              const CUtensorMap* am = (SPLIT && rank == 1) ? &tmap_a_lo : &tmap_a;
+              tma_load_2d_pair(a_dst, am, fbar, kb * BK, swap_row0, pol_a);
+              if (EPI == kEpiGateUpAct) {
+                // gate and up features n0 + 64 r .. + 63: one box each
+                if (p.b_wide) {
+                  tma_load_5d_pair(b_dst, &tmap_b_tail, fbar, 0, kb * BK, ti.n0 / 64 + static_cast<int>(rank),
+                                   0, ti.g, pol_b);
+                } else {
+                  tma_load_4d_pair(b_dst, &tmap_b_tail, fbar, ti.n0 + 64 * static_cast<int>(rank), 0,
+                                   kb * BK, ti.g, pol_b);
+                  tma_load_4d_pair(b_dst + B_BOX_BYTES, &tmap_b_tail, fbar,
+                                   ti.n0 + 64 * static_cast<int>(rank), 1, kb * BK, ti.g, pol_b);
+                }
+              } else if (p.b_wide) {
+                tma_load_4d_pair(b_dst, &tmap_b, fbar, 0, kb * BK,
+                                 ti.n0 / 64 + static_cast<int>(rank) * nbox_cta, ti.g, pol_b);
+              } else {
+                const int c0 = ti.n0 + static_cast<int>(rank) * 64 * nbox_cta;
+                for (int j = 0; j < nbox_cta; ++j)
+                  tma_load_3d_pair(b_dst + j * B_BOX_BYTES, &tmap_b, fbar, c0 + 64 * j, kb * BK,
+                                   ti.g, pol_b);
+              }
+            }
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            continue;
+          }
           if (gather)
             tma_gather4_2d(a_dst + lane * 4 * 128, &tmap_a, &ctrl->full[stage], kb * BK, tr[0],
                            tr[1], tr[2], tr[3], pol_a);
@@ -484,12 +542,33 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
         const uint32_t d_tmem = tmem_base + acc * ACC_STRIDE;
         int kb0, kb1;
         kb_range(t, kb0, kb1);
+        const TileInfo ti = decode_tile<TILE_M>(ctrl, G, t / p.ksplit, p.n_tiles, p.cols_per_tile);
+        const bool swap = is_swap(ti);
+        // swapped tail: A = weights (N-major boxes: MN-major operand), B = rows
+        // (K-major), N = rows (gate/up) or 2 x rows (down: h_hi | h_lo)
+        const uint32_t idesc_swap =
+            make_idesc_bf16_f32(TILE_M, (EPI == kEpiGateUpAct ? 1 : 2) * swap_rows(ti), 1, 0);
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&ctrl->full[stage], phase, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after_sync();
+          if (PAIR && swap) {
+            const uint64_t wdesc0 = make_smem_desc_sw128(smem_u32(stage_b(stage)), B_BOX_BYTES, 1024);
+            const uint64_t rdesc0 = make_smem_desc_sw128(smem_u32(stage_a(stage)), 16, 1024);
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk)
+              tc_mma_f16_pair(d_tmem, smem_desc_advance(wdesc0, kk * 2048),
+                              smem_desc_advance(rdesc0, kk * 32), idesc_swap,
+                              ((kb - kb0) | kk) != 0);
+            tc_commit_pair_multicast(&ctrl->empty[stage], 0x3);
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            continue;
+          }
           // A: K-major, 128-byte rows; a K step of 16 bf16 is 32 bytes.
           // B: N-major, 64-column boxes 8 KB apart; a K step of 16 rows is 2 KB.
           const uint64_t adesc0 = make_smem_desc_sw128(smem_u32(stage_a(stage)), 16, 1024);
@@ -597,7 +676,7 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;  // TMEM lanes [32*quarter, 32*quarter + 32)
     const int row_in_tile = quarter * 32 + lane;
-    uint32_t acc = 0, acc_phase = 0;
+    uint32_t acc = 0, acc_phase = 0, xch_phase = 0;
     for (int t = work0; t < total_tiles; t += work_stride) {
       TileInfo ti = decode_tile<TILE_M>(ctrl, G, t / p.ksplit, p.n_tiles, p.cols_per_tile);
       ti.row0 += static_cast<int>(rank) * BM;  // this CTA's 128 rows of the tile
@@ -613,6 +692,103 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
       __syncwarp();
       tc_fence_after_sync();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * ACC_STRIDE;
+      if (PAIR) {
+        // ti was shifted to this CTA's half above; the swapped test uses the
+        // whole tile's rows
+        TileInfo tw = ti;
+        tw.row0 -= static_cast<int>(rank) * BM;
+        tw.rows += static_cast<int>(rank) * BM;
+        if (is_swap(tw)) {
+          const int R = swap_rows(tw);  // accumulator columns per plane
+          bool ok = true;
+          if (EPI == kEpiGateUpAct) {
+            // lanes 0..63: gate features, 64..127: the matching up features of
+            // output columns n0 + 64 r + (0..63); up values pass through shared memory
+            float* up = epi_stage;  // [R <= 64][64]
+            const int fl = quarter * 32 + lane;
+            const bool is_up = quarter >= 2;
+            const int f = ti.n0 + 64 * static_cast<int>(rank) + (fl & 63);
+            if (is_up) {
+              ok = mbar_wait(&ctrl->xch_empty, xch_phase ^ 1u, abort_flag);
+              if (ok) {
+#pragma unroll 1
+                for (int c = 0; c < R; c += 32) {
+                  uint32_t v[32];
+                  tmem_ld_32x32b_x32(taddr + c, v);
+                  tc_wait_ld();
+#pragma unroll
+                  for (int j = 0; j < 32; ++j)
+                    if (c + j < R) up[(c + j) * 64 + (fl - 64)] = __uint_as_float(v[j]);
+                }
+              }
+              mbar_arrive(&ctrl->xch_full);
+            } else {
+              ok = mbar_wait(&ctrl->xch_full, xch_phase, abort_flag);
+              __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
+              __nv_bfloat16* out_lo = reinterpret_cast<__nv_bfloat16*>(p.out_lo);
+#pragma unroll 1
+              for (int c = 0; c < R && ok; c += 32) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(taddr + c, v);
+                tc_wait_ld();
+                if (f < p.N) {
+#pragma unroll 4
+                  for (int j = 0; j < 32; ++j) {
+                    if (c + j >= tw.rows) break;
+                    const size_t row = static_cast<size_t>(tw.row0 + c + j);
+                    const float g = __uint_as_float(v[j]);
+                    const float u = up[(c + j) * 64 + fl];
+                    const float hf = ((p.act == MOE_ACT_SWIGLU) ? silu_f(g) : gelu_tanh_f(g)) * u;
+                    if (p.h_fp32) {
+                      reinterpret_cast<float*>(p.out)[row * p.N + f] = hf;
+                    } else {
+                      const __nv_bfloat16 hi = __float2bfloat16_rn(hf);
+                      out[row * p.N + f] = hi;
+                      if (out_lo) out_lo[row * p.N + f] = __float2bfloat16_rn(hf - __bfloat162float(hi));
+                    }
+                  }
+                }
+              }
+              mbar_arrive(&ctrl->xch_empty);  // the up values may be rewritten
+            }
+            xch_phase ^= 1u;
+          } else {
+            // lanes = output features n0 + 128 r + (0..127); columns j (h_hi rows)
+            // and R + j (h_lo rows) add up to row j's result
+            const int f = ti.n0 + 128 * static_cast<int>(rank) + quarter * 32 + lane;
+            float* out = reinterpret_cast<float*>(p.out) + plane;
+#pragma unroll 1
+            for (int c = 0; c < R; c += 32) {
+              uint32_t hi[32], lo[32];
+              tmem_ld_32x32b_x32(taddr + c, hi);
+              tmem_ld_32x32b_x32(taddr + R + c, lo);
+              tc_wait_ld();
+              if (f < p.N) {
+#pragma unroll 4
+                for (int j = 0; j < 32; ++j) {
+                  if (c + j >= tw.rows) break;
+                  out[static_cast<size_t>(tw.row0 + c + j) * p.N + f] =
+                      __uint_as_float(hi[j]) + __uint_as_float(lo[j]);
+                }
+              }
+            }
+          }
+          tc_fence_before_sync();
+          mbar_arrive_cluster(leader_bar(&ctrl->tempty[acc]));
+          if (!ok) {
+            if (lane == 0) {
+              ctrl->abort = 1;
+              atomicOr(p.err, MOE_DEV_WAIT_TIMEOUT);
+            }
+            break;
+          }
+          if (++acc == 2) {
+            acc = 0;
+            acc_phase ^= 1u;
+          }
+          continue;
+        }
+      }
       const bool valid = row_in_tile < ti.rows;
       const size_t out_row = static_cast<size_t>(ti.row0 + row_in_tile);
 
@@ -1169,7 +1345,8 @@ bool encode_tmap(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims
 
 template <int EPI, bool SPLIT, bool FP8, bool PAIR>
 cudaError_t launch_epi(const CUtensorMap& ta, const CUtensorMap& ta_lo, const CUtensorMap& tb,
-                       const KParams& kp, long long max_tiles, cudaStream_t s) {
+                       const CUtensorMap& tb_tail, const KParams& kp, long long max_tiles,
+                       cudaStream_t s) {
   constexpr size_t smem = smem_bytes<SPLIT, FP8, PAIR>();
   constexpr int threads = StageCfg<SPLIT, FP8, PAIR>::kThreads;
   auto kern = grouped_gemm_kernel<EPI, SPLIT, FP8, PAIR>;
@@ -1186,7 +1363,7 @@ cudaError_t launch_epi(const CUtensorMap& ta, const CUtensorMap& ta_lo, const CU
   if (!PAIR) {
     const int grid =
         static_cast<int>(std::max<long long>(1, std::min<long long>(device_sm_count(), max_tiles)));
-    return launch_kernel(kern, dim3(grid), dim3(threads), smem, s, ta, ta_lo, tb, kp);
+    return launch_kernel(kern, dim3(grid), dim3(threads), smem, s, ta, ta_lo, tb, tb_tail, kp);
   }
   // one persistent 2-CTA cluster per SM pair that can hold one
   cudaLaunchConfig_t cfg = {};
@@ -1215,7 +1392,7 @@ cudaError_t launch_epi(const CUtensorMap& ta, const CUtensorMap& ta_lo, const CU
       1, std::min<long long>(max_clusters[(dev >= 0 && dev < 64) ? dev : 0], max_tiles)));
   cfg.gridDim = dim3(2 * nclu, 1, 1);
   cfg.numAttrs = 2;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, ta_lo, tb, kp);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, ta_lo, tb, tb_tail, kp);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -1452,12 +1629,22 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
     const uint32_t box[3] = {box_n, BK, 1};
     if (!encode_tmap(&tb, a.B, 3, dims, strides, box, bdt)) return cudaErrorInvalidValue;
   }
+  // 2-CTA tiles: a group's last tile with few rows runs swapped (rows as the
+  // MMA N); the gate/up pass then loads one gate and one up block per CTA
+  kp.swap_tail = (pair && g_pair_tiles == 1) ? (a.epilogue == kEpiGateUpAct ? 64 : 128) : 0;
+  CUtensorMap tb_tail = tb;
+  if (kp.swap_tail && kp.b_wide && a.epilogue == kEpiGateUpAct) {
+    const uint64_t dims[5] = {64, K, N / 64, 2, G64};
+    const uint64_t strides[4] = {2 * N * eb, 64 * eb, N * eb, K * 2 * N * eb};
+    const uint32_t box[5] = {64, BK, 1, 2, 1};
+    if (!encode_tmap(&tb_tail, a.B, 5, dims, strides, box, bdt)) return cudaErrorInvalidValue;
+  }
   const int tile_m = pair ? 2 * BM : BM;
   const long long max_tiles = (static_cast<long long>((a.M + tile_m - 1) / tile_m) + a.G) *
                               static_cast<long long>(kp.n_tiles) * kp.ksplit;
 #define MOE_LAUNCH(E_, S_, F_)                                                          \
-  (pair ? launch_epi<E_, S_, F_, true>(ta, ta_lo, tb, kp, max_tiles, s)                  \
-        : launch_epi<E_, S_, F_, false>(ta, ta_lo, tb, kp, max_tiles, s))
+  (pair ? launch_epi<E_, S_, F_, true>(ta, ta_lo, tb, tb_tail, kp, max_tiles, s)         \
+        : launch_epi<E_, S_, F_, false>(ta, ta_lo, tb, tb_tail, kp, max_tiles, s))
   if (a.epilogue == kEpiGateUpAct) {
     if (a.A_lo) return cudaErrorInvalidValue;
     return a.b_fp8 ? MOE_LAUNCH(kEpiGateUpAct, false, true) : MOE_LAUNCH(kEpiGateUpAct, false, false);

@@ -343,11 +343,12 @@ def _grouped_case(E, counts, D, I, act, seed, fp8=False):
     return xp, offsets, W13.to(torch.bfloat16), W2.to(torch.bfloat16)
 
 
-@pytest.fixture(params=["cta1", "pair", "decode", "decode16"])
+@pytest.fixture(params=["cta1", "pair", "pair_noswap", "decode", "decode16"])
 def tile_mode(request):
     """Run a grouped-GEMM test on 128-row 1-CTA tiles, on 2-CTA (256-row)
-    tiles, and on the swap-AB decode kernel with 64- and 16-row tiles."""
-    pair = moe.moe_set_option(moe.MOE_OPT_PAIR_TILES, 1 if request.param == "pair" else 0)
+    tiles with and without swapped tails, and on the swap-AB decode kernel
+    with 64- and 16-row tiles."""
+    pair = moe.moe_set_option(moe.MOE_OPT_PAIR_TILES, {"pair": 1, "pair_noswap": 2}.get(request.param, 0))
     dec_mode = {"decode": 2, "decode16": 3}.get(request.param, 0)
     dec = moe.moe_set_option(moe.MOE_OPT_DECODE_KERNEL, dec_mode)
     yield request.param
@@ -384,6 +385,34 @@ def test_grouped_ffn_parity(E, counts, D, I, act, tile_mode):
     check_close("h_hi+h_lo", (hc[0] + hc[1]).numpy(), h_o, 2.0 ** -15, 1e-4)
     # y is fp32: only fp32 accumulation differs from the exact value
     check_close("y", y.cpu().double().numpy(), y_o, 1e-4, 1e-4)
+
+
+@pytest.mark.parametrize("act", ["swiglu", "geglu_tanh"])
+@pytest.mark.parametrize("pair_mode", [1, 2])
+def test_grouped_ffn_pair_tail_sizes(act, pair_mode):
+    """2-CTA tiles, every kind of last tile: swapped tails of 1..64 (gate/up)
+    and 1..128 (down) rows, full-height tails above that, exact multiples of
+    256; mode 2 runs the same groups without swapped tails."""
+    counts = [1, 16, 17, 31, 32, 33, 63, 64, 65, 100, 127, 128, 129, 255, 256, 257, 300, 320,
+              383, 384, 385, 512]
+    E, D, I = len(counts), 256, 128
+    old = moe.moe_set_option(moe.MOE_OPT_PAIR_TILES, pair_mode)
+    try:
+        xp, offsets, W13, W2 = _grouped_case(E, counts, D, I, act, seed=pair_mode + len(act))
+        R = xp.shape[0]
+        cfg = moe.make_config(R, D, E, 1, I, act=act)
+        ws = _ws_for(cfg)
+        h = torch.empty((2, R, I), dtype=torch.bfloat16, device="cuda")
+        y = torch.empty((R, D), dtype=torch.float32, device="cuda")
+        moe.moe_grouped_ffn(cfg, xp, torch.from_numpy(offsets).cuda(), W13, None, W2, None, h, y, ws=ws)
+        assert moe.moe_read_device_status(ws) == 0
+        h_o, y_o = oracle.grouped_ffn(oracle.to_f64(xp.cpu()), offsets, W13.cpu(), W2.cpu(), act)
+        hc = h.cpu().double()
+        check_close("h_hi", hc[0].numpy(), h_o, 2.0 ** -8, 1e-4)
+        check_close("h_hi+h_lo", (hc[0] + hc[1]).numpy(), h_o, 2.0 ** -15, 1e-4)
+        check_close("y", y.cpu().double().numpy(), y_o, 1e-4, 1e-4)
+    finally:
+        moe.moe_set_option(moe.MOE_OPT_PAIR_TILES, old)
 
 
 @pytest.mark.parametrize("E,counts,D,I,act", [
