@@ -266,7 +266,7 @@ def run_ours(args, world, rank, local):
         _build.build()
     barrier(world)
     moe.load_library()
-    if args.pair_tiles:
+    if args.pair_tiles is not None:
         moe.moe_set_option(moe.MOE_OPT_PAIR_TILES, args.pair_tiles)
     if args.gather_a:
         moe.moe_set_option(moe.MOE_OPT_GATHER_A, 1)
@@ -465,9 +465,9 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=0,
                     help="reference arm: tokens per step (0: grown until one step takes ~--ref-step-s)")
     ap.add_argument("--ref-step-s", type=float, default=2.0)
-    ap.add_argument("--pair-tiles", type=int, nargs="?", const=1, default=0,
-                    help="grouped GEMMs on 2-CTA clusters (moe_set_option MOE_OPT_PAIR_TILES: "
-                         "1 with swapped tails, 2 without)")
+    ap.add_argument("--pair-tiles", type=int, nargs="?", const=1, default=None,
+                    help="moe_set_option MOE_OPT_PAIR_TILES: 0 never 2-CTA tiles, 1 always (swapped "
+                         "tails), 2 always without swapped tails, 3 (default) by rows per group")
     ap.add_argument("--decode-kernel", type=int, default=None, choices=[0, 1, 2, 3],
                     help="moe_set_option MOE_OPT_DECODE_KERNEL (0 off, 1 auto, 2/3 always with 64/16-row tiles)")
     ap.add_argument("--gather-a", action="store_true",

@@ -239,13 +239,14 @@ int moe_layer_launch_count(const moe_config_t* cfg);
 /* Kernel-variant options (process-wide; set them from the thread that
  * launches, between calls).  Returns the previous value, or
  * MOE_ERR_INVALID_ARG for an unknown option.
- *   MOE_OPT_PAIR_TILES: 1 = bf16 grouped GEMMs with a full 256-column B tile
+ *   MOE_OPT_PAIR_TILES: how bf16 grouped GEMMs with a full 256-column B tile
  *   use 2-CTA clusters (tcgen05 cta_group::2, M = 256 rows per tile, each CTA
- *   loading half of B), and a group's last tile with at most 64 (gate/up) or
- *   128 (down) rows runs swapped, with the weights as the M = 256 operand and
- *   the rows as N; 2 = 2-CTA tiles without swapped tails; fp8-weight GEMMs
- *   keep one CTA per tile; 0 (default) = one CTA per 128-row tile.  Results
- *   are the same up to fp32 summation order. */
+ *   loading half of B; a group's last tile with at most 64 (gate/up) or 128
+ *   (down) rows runs swapped, with the weights as the M = 256 operand and the
+ *   rows as N): 3 (default) = when there are at least 150 rows per group on
+ *   average; 1 = always; 2 = always, without swapped tails; 0 = never (one
+ *   CTA per 128-row tile).  fp8-weight GEMMs always use one CTA per tile.
+ *   Results are the same up to fp32 summation order. */
 #define MOE_OPT_PAIR_TILES 1
 /*   MOE_OPT_GATHER_A: 1 = moe_layer does not materialise the permuted rows;
  *   the routed gate/up GEMM gathers its A rows from x with TMA tile::gather4

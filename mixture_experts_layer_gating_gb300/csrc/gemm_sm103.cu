@@ -1399,10 +1399,9 @@ cudaError_t launch_epi(const CUtensorMap& ta, const CUtensorMap& ta_lo, const CU
 
 }  // namespace
 
-int g_pair_tiles = 0;      // set through moe_set_option(MOE_OPT_PAIR_TILES, .)
+int g_pair_tiles = 3;      // set through moe_set_option(MOE_OPT_PAIR_TILES, .)
 int g_decode_kernel = 1;   // set through moe_set_option(MOE_OPT_DECODE_KERNEL, .)
 int g_pdl = 1;             // set through moe_set_option(MOE_OPT_PDL, .)
-bool pair_tiles_requested() { return g_pair_tiles != 0; }
 
 namespace {
 
@@ -1593,14 +1592,19 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
     kp.cols_per_tile = kp.bn;
   }
   kp.n_tiles = (a.N + kp.cols_per_tile - 1) / kp.cols_per_tile;
-  // 2-CTA tiles need a full 256-column B tile and no split-K.  They are used
-  // only when requested with moe_set_option(MOE_OPT_PAIR_TILES, 1) (measured
-  // slower than 1-CTA tiles on the configured workloads, where 256-row tiles
-  // leave more rows empty), and never for fp8 weights: there they measured
-  // 40 % slower, and a 2-CTA fp8 run at full Ling size with eight converter
-  // warps per CTA ended in a GPU fault whose cause was not found.
+  // 2-CTA tiles need a full 256-column B tile and no split-K.  Policy
+  // (moe_set_option(MOE_OPT_PAIR_TILES, .)): 3 (default) = with swapped tails
+  // when there are at least 150 rows per group on average (measured faster on
+  // the Qwen3.5 and Qwen3 prefill layers and the shared experts, slower at
+  // ~128 rows per group, where 256-row tiles are half empty); 1 = always, 2 =
+  // always without swapped tails, 0 = never.  Never for fp8 weights: there
+  // they measured 40 % slower, and a 2-CTA fp8 run at full Ling size with
+  // eight converter warps per CTA ended in a GPU fault whose cause was not found.
+  const bool pair_policy =
+      g_pair_tiles == 1 || g_pair_tiles == 2 ||
+      (g_pair_tiles == 3 && static_cast<long long>(a.M) >= 150ll * a.G);
   const bool pair = a.pair_ok && !a.a_gather && !a.b_fp8 && kp.bn == 256 && kp.ksplit == 1 &&
-                    pair_tiles_requested();
+                    pair_policy;
   // bf16 weights with N a multiple of 64: view each expert's [K, N] (gate/up:
   // [K, 2, N]) matrix as 64-column blocks, [block][K][64], so that one TMA load
   // brings all the blocks of a stage in the layout the MMA reads (box 0 at
@@ -1631,7 +1635,7 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
   }
   // 2-CTA tiles: a group's last tile with few rows runs swapped (rows as the
   // MMA N); the gate/up pass then loads one gate and one up block per CTA
-  kp.swap_tail = (pair && g_pair_tiles == 1) ? (a.epilogue == kEpiGateUpAct ? 64 : 128) : 0;
+  kp.swap_tail = (pair && g_pair_tiles != 2) ? (a.epilogue == kEpiGateUpAct ? 64 : 128) : 0;
   CUtensorMap tb_tail = tb;
   if (kp.swap_tail && kp.b_wide && a.epilogue == kEpiGateUpAct) {
     const uint64_t dims[5] = {64, K, N / 64, 2, G64};

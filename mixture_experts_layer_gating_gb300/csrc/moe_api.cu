@@ -568,7 +568,7 @@ int moe_set_option(int option, int value) {
   switch (option) {
     case MOE_OPT_PAIR_TILES: {
       const int old = g_pair_tiles;
-      g_pair_tiles = value < 0 ? 0 : (value > 2 ? 2 : value);
+      g_pair_tiles = value < 0 ? 0 : (value > 3 ? 3 : value);
       return old;
     }
     case MOE_OPT_DECODE_KERNEL: {

@@ -124,7 +124,7 @@ def test_set_option_values():
     with pytest.raises(moe.MoEError):
         moe.moe_set_option(99, 1)
     cases = [
-        (moe.MOE_OPT_PAIR_TILES, 5, 2),
+        (moe.MOE_OPT_PAIR_TILES, 5, 3),
         (moe.MOE_OPT_PAIR_TILES, 1, 1),
         (moe.MOE_OPT_GATHER_A, 1, 1),
         (moe.MOE_OPT_DECODE_KERNEL, 7, 3),
