@@ -267,7 +267,9 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                         const __grid_constant__ CUtensorMap tmap_a_lo,
                         const __grid_constant__ CUtensorMap tmap_b,
-                        const __grid_constant__ CUtensorMap tmap_b_tail, const KParams p) {
+                        const __grid_constant__ CUtensorMap tmap_b_tail,
+                        const __grid_constant__ CUtensorMap tmap_a_tail,
+                        const __grid_constant__ CUtensorMap tmap_a_lo_tail, const KParams p) {
   pdl_wait();
   using Cfg = StageCfg<SPLIT, FP8, PAIR>;
   // fp8 weights: fp16 operands; everything else: bf16 operands
@@ -321,6 +323,8 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
     if (SPLIT) tma_prefetch_desc(&tmap_a_lo);
     tma_prefetch_desc(&tmap_b);
     if (PAIR && EPI == kEpiGateUpAct) tma_prefetch_desc(&tmap_b_tail);
+    if (PAIR) tma_prefetch_desc(&tmap_a_tail);
+    if (PAIR && SPLIT) tma_prefetch_desc(&tmap_a_lo_tail);
   }
   if (warp == 1) {
     if (PAIR) {  // collective over one warp of each CTA of the pair
@@ -389,10 +393,13 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
         int kb0, kb1;
         kb_range(t, kb0, kb1);
         const bool swap = is_swap(ti);
-        // swapped tail: each CTA loads one 128-row box of rows (the gate/up pass:
-        // rows r * R/2 .. of the tile; the down pass: CTA 0 the h_hi rows, CTA 1
-        // the h_lo rows) and its 128 weight features
-        const uint32_t tile_tx = swap ? 2u * (A_TILE_BYTES + 2 * B_BOX_BYTES) : tx;
+        // swapped tail: each CTA loads its rows in 32-row boxes (the gate/up
+        // pass: rows r * R/2 .. of the tile; the down pass: CTA 0 the h_hi rows,
+        // CTA 1 the h_lo rows) and its 128 weight features
+        const int swap_boxes =
+            swap ? ((EPI == kEpiGateUpAct ? swap_rows(ti) / 2 : swap_rows(ti)) + 31) / 32 : 0;
+        const uint32_t tile_tx =
+            swap ? 2u * (static_cast<uint32_t>(swap_boxes) * 32u * 128u + 2u * B_BOX_BYTES) : tx;
         const int swap_row0 =
             ti.row0 + (EPI == kEpiGateUpAct ? static_cast<int>(rank) * (swap_rows(ti) / 2) : 0);
         for (int kb = kb0; kb < kb1; ++kb) {
@@ -406,8 +413,9 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
           uint8_t* b_dst = stage_b(stage);
           if (PAIR && swap) {
             if (lane == 0) {
-              const CUtensorMap* am = (SPLIT && rank == 1) ? &tmap_a_lo : &tmap_a;
-              tma_load_2d_pair(a_dst, am, fbar, kb * BK, swap_row0, pol_a);
+              const CUtensorMap* am = (SPLIT && rank == 1) ? &tmap_a_lo_tail : &tmap_a_tail;
+              for (int i = 0; i < swap_boxes; ++i)
+                tma_load_2d_pair(a_dst + i * 32 * 128, am, fbar, kb * BK, swap_row0 + 32 * i, pol_a);
               if (EPI == kEpiGateUpAct) {
                 // gate and up features n0 + 64 r .. + 63: one box each
                 if (p.b_wide) {
@@ -1345,7 +1353,8 @@ bool encode_tmap(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims
 
 template <int EPI, bool SPLIT, bool FP8, bool PAIR>
 cudaError_t launch_epi(const CUtensorMap& ta, const CUtensorMap& ta_lo, const CUtensorMap& tb,
-                       const CUtensorMap& tb_tail, const KParams& kp, long long max_tiles,
+                       const CUtensorMap& tb_tail, const CUtensorMap& ta_tail,
+                       const CUtensorMap& ta_lo_tail, const KParams& kp, long long max_tiles,
                        cudaStream_t s) {
   constexpr size_t smem = smem_bytes<SPLIT, FP8, PAIR>();
   constexpr int threads = StageCfg<SPLIT, FP8, PAIR>::kThreads;
@@ -1363,7 +1372,8 @@ cudaError_t launch_epi(const CUtensorMap& ta, const CUtensorMap& ta_lo, const CU
   if (!PAIR) {
     const int grid =
         static_cast<int>(std::max<long long>(1, std::min<long long>(device_sm_count(), max_tiles)));
-    return launch_kernel(kern, dim3(grid), dim3(threads), smem, s, ta, ta_lo, tb, tb_tail, kp);
+    return launch_kernel(kern, dim3(grid), dim3(threads), smem, s, ta, ta_lo, tb, tb_tail, ta_tail,
+                         ta_lo_tail, kp);
   }
   // one persistent 2-CTA cluster per SM pair that can hold one
   cudaLaunchConfig_t cfg = {};
@@ -1392,7 +1402,7 @@ cudaError_t launch_epi(const CUtensorMap& ta, const CUtensorMap& ta_lo, const CU
       1, std::min<long long>(max_clusters[(dev >= 0 && dev < 64) ? dev : 0], max_tiles)));
   cfg.gridDim = dim3(2 * nclu, 1, 1);
   cfg.numAttrs = 2;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, ta_lo, tb, tb_tail, kp);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, ta_lo, tb, tb_tail, ta_tail, ta_lo_tail, kp);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -1636,7 +1646,15 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
   // 2-CTA tiles: a group's last tile with few rows runs swapped (rows as the
   // MMA N); the gate/up pass then loads one gate and one up block per CTA
   kp.swap_tail = (pair && g_pair_tiles != 2) ? (a.epilogue == kEpiGateUpAct ? 64 : 128) : 0;
-  CUtensorMap tb_tail = tb;
+  CUtensorMap tb_tail = tb, ta_tail = ta, ta_lo_tail = ta_lo;
+  if (kp.swap_tail) {  // swapped tails load their rows in 32-row boxes
+    const uint64_t dims[2] = {static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.M)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(a.K) * 2};
+    const uint32_t box[2] = {BK, 32};
+    if (!encode_tmap(&ta_tail, a.A, 2, dims, strides, box)) return cudaErrorInvalidValue;
+    if (a.A_lo && !encode_tmap(&ta_lo_tail, a.A_lo, 2, dims, strides, box))
+      return cudaErrorInvalidValue;
+  }
   if (kp.swap_tail && kp.b_wide && a.epilogue == kEpiGateUpAct) {
     const uint64_t dims[5] = {64, K, N / 64, 2, G64};
     const uint64_t strides[4] = {2 * N * eb, 64 * eb, N * eb, K * 2 * N * eb};
@@ -1646,9 +1664,11 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
   const int tile_m = pair ? 2 * BM : BM;
   const long long max_tiles = (static_cast<long long>((a.M + tile_m - 1) / tile_m) + a.G) *
                               static_cast<long long>(kp.n_tiles) * kp.ksplit;
-#define MOE_LAUNCH(E_, S_, F_)                                                          \
-  (pair ? launch_epi<E_, S_, F_, true>(ta, ta_lo, tb, tb_tail, kp, max_tiles, s)         \
-        : launch_epi<E_, S_, F_, false>(ta, ta_lo, tb, tb_tail, kp, max_tiles, s))
+#define MOE_LAUNCH(E_, S_, F_)                                                               \
+  (pair ? launch_epi<E_, S_, F_, true>(ta, ta_lo, tb, tb_tail, ta_tail, ta_lo_tail, kp,       \
+                                       max_tiles, s)                                          \
+        : launch_epi<E_, S_, F_, false>(ta, ta_lo, tb, tb_tail, ta_tail, ta_lo_tail, kp,      \
+                                        max_tiles, s))
   if (a.epilogue == kEpiGateUpAct) {
     if (a.A_lo) return cudaErrorInvalidValue;
     return a.b_fp8 ? MOE_LAUNCH(kEpiGateUpAct, false, true) : MOE_LAUNCH(kEpiGateUpAct, false, false);
