@@ -28,7 +28,8 @@
  *   bytes, which makes D, I and I_shared multiples of 8 (16 for fp8 weights).
  * - Dtypes: act_dtype applies to x, W_g, the permuted rows and out.  w_dtype
  *   applies to W13, W2 and the shared expert's weights.  Supported pairs:
- *   (F32, F32), (BF16, BF16), (BF16, FP8_E4M3).  Router logits, gate weights,
+ *   (F32, F32), (BF16, BF16), (BF16, FP8_E4M3), (BF16, FP8_E4M3_NK).
+ *   Router logits, gate weights,
  *   the expert outputs y_perm and the shared-expert output are always fp32.
  *   The intermediate h takes 4 bytes per element: fp32 for fp32 layers and
  *   for fp8 weights; for bf16 weights two bf16 planes [M, I] -- h_hi =
@@ -39,6 +40,17 @@
  *   times exact powers of two, so the result equals the bf16-activation
  *   product up to fp32 summation order (x exactly; h rounded once to 11
  *   significant bits relative to its row).
+ * - FP8_E4M3_NK: the same e4m3 values and per-column scales, with each
+ *   expert's matrix stored transposed (W13 [E, 2I, D], W2 [E, D, I], W13s
+ *   [2 I_shared, D], W2s [D, I_shared]: the reduction dimension contiguous),
+ *   as moe_pack_weights_nk writes it once from the [.., K, N] layout.  These
+ *   layers run on the 8-bit tensor-core kind (kind::f8f6f4) with no weight
+ *   expansion: every A row (x, then h) is scaled by an exact power of two so
+ *   that its largest element lies in [128, 256) and carried as two e4m3
+ *   terms, hi = e4m3(v) and lo = e4m3(v - hi), multiplied by the weights in
+ *   two products into one fp32 accumulator.  A bf16 x is represented exactly
+ *   except for elements below 2^-9 of their row's largest, which keep an
+ *   absolute error under 2^-17 of it; h keeps 8 significant bits.
  */
 #ifndef MOE_GB300_H
 #define MOE_GB300_H
@@ -50,7 +62,12 @@
 extern "C" {
 #endif
 
-typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_FP8_E4M3 = 2 } moe_dtype_t;
+typedef enum {
+  MOE_F32 = 0,
+  MOE_BF16 = 1,
+  MOE_FP8_E4M3 = 2,   /* weights [.., K, N] as the pages write them */
+  MOE_FP8_E4M3_NK = 3 /* the same weights transposed per matrix (moe_pack_weights_nk) */
+} moe_dtype_t;
 
 /* SwiGLU: SiLU(gate) * up.  GEGLU: tanh-approximated GELU(gate) * up. */
 typedef enum { MOE_ACT_SWIGLU = 0, MOE_ACT_GEGLU_TANH = 1 } moe_act_t;
@@ -162,15 +179,18 @@ int moe_permute_noalloc(const moe_config_t* cfg, const int32_t* topk_ids, const 
  * applied after the K reduction).
  *   x_perm  [T*k, D] act_dtype: expert-ordered rows.
  *   offsets [E+1] int32: segment bounds (from moe_permute).
- *   W13     [E, D, 2I] w_dtype: columns [0, I) gate, [I, 2I) up.
+ *   W13     [E, D, 2I] w_dtype: columns [0, I) gate, [I, 2I) up
+ *           (FP8_E4M3_NK: [E, 2I, D], rows [0, I) gate, [I, 2I) up).
  *   s13     [E, 2I] fp32 per-column scales (fp8 only, else NULL).
- *   W2      [E, I, D] w_dtype;   s2 [E, D] fp32 (fp8 only, else NULL).
+ *   W2      [E, I, D] w_dtype (FP8_E4M3_NK: [E, D, I]);
+ *   s2      [E, D] fp32 (fp8 only, else NULL).
  *   h       out: act(gate) * up, [T*k, I] fp32 (fp32 layers and fp8 weights)
  *           or the bf16 pair [2, T*k, I] (hi plane, then lo plane) for bf16
  *           weights.
  *   y_perm  [T*k, D] fp32 out: h W2 per segment (times s2 for fp8).
  *   x, W13s [D, 2*I_shared], s13s [2*I_shared], W2s [I_shared, D], s2s [D]:
- *           the shared expert; x NULL (or I_shared == 0) skips it.
+ *           the shared expert (FP8_E4M3_NK: W13s [2*I_shared, D], W2s
+ *           [D, I_shared]); x NULL (or I_shared == 0) skips it.
  *   h_s     shared intermediate, same layout as h with T rows.
  *   s_out   [T, D] fp32 out: shared expert output. */
 int moe_grouped_ffn(const moe_config_t* cfg, const void* x_perm, const int32_t* offsets,
@@ -217,9 +237,11 @@ int moe_layer(const moe_config_t* cfg, const void* x, const void* Wg, const floa
 #define MOE_WS_Y_PERM 9
 #define MOE_WS_H_SHARED 10
 #define MOE_WS_S 11
-/* fp8-weight layers only (the fp16 tensor-core path): x as fp16 rows times
- * exact powers of two [T, D], their inverse scales per token [T] and per
- * permuted row [T*k] (fp32); for these layers MOE_WS_X_PERM holds fp16 rows. */
+/* fp8-weight layers only: x times exact powers of two [T, D] -- as fp16
+ * rows (FP8_E4M3) or as two-term e4m3 rows [T, 2D], hi in bytes [0, D) and
+ * lo in [D, 2D) (FP8_E4M3_NK) -- their inverse scales per token [T] and per
+ * permuted row [T*k] (fp32); for these layers MOE_WS_X_PERM holds rows of
+ * the same form. */
 #define MOE_WS_X16 12
 #define MOE_WS_TOK_INV 13
 #define MOE_WS_ROW_INV 14
@@ -230,6 +252,24 @@ size_t moe_workspace_offset(const moe_config_t* cfg, int which);
  * NULL) or MOE_ERR_CUDA. */
 int moe_read_device_status(void* ws, void* stream, int32_t* flags);
 
+/* Transposes one-byte (e4m3) weight matrices into the layout of
+ * MOE_FP8_E4M3_NK layers; run once when the weights are loaded.
+ * Pages: "用SGLang-JAX在TPU上优化Ling-2.6-1T" §5 "逐通道 direct_scaled_dot"
+ * (fp8 tokens and fp8 weights fed straight to the matrix unit, f32 partial
+ * sums, per-token and per-channel scales after the reduction).  The pages
+ * write each projection input dimension first; this library's 8-bit
+ * tensor-core path reads both operands with the reduction dimension
+ * contiguous, hence this one-time copy.
+ *   W     [G, K, N] device, one byte per element (the pages' layout: W13 with
+ *         G = E, K = D, N = 2I; W2 with K = I, N = D; G = 1 for the shared
+ *         expert's matrices).
+ *   W_nk  [G, N, K] device out: W_nk[g][n][c] = W[g][c][n].  Must not
+ *         overlap W.
+ *   G >= 1; K and N positive multiples of 16; both pointers 16-byte
+ *   aligned, else MOE_ERR_INVALID_ARG before anything is enqueued.
+ *   Asynchronous on `stream`; needs no workspace. */
+int moe_pack_weights_nk(const void* W, int64_t G, int32_t K, int32_t N, void* W_nk, void* stream);
+
 /* Human-readable text of a moe_status_t. */
 const char* moe_status_string(int status);
 
@@ -239,14 +279,16 @@ int moe_layer_launch_count(const moe_config_t* cfg);
 /* Kernel-variant options (process-wide; set them from the thread that
  * launches, between calls).  Returns the previous value, or
  * MOE_ERR_INVALID_ARG for an unknown option.
- *   MOE_OPT_PAIR_TILES: how bf16 grouped GEMMs with a full 256-column B tile
+ *   MOE_OPT_PAIR_TILES: how grouped GEMMs with a full 256-column B tile
  *   use 2-CTA clusters (tcgen05 cta_group::2, M = 256 rows per tile, each CTA
  *   loading half of B; a group's last tile with at most 64 (gate/up) or 128
  *   (down) rows runs swapped, with the weights as the M = 256 operand and the
  *   rows as N): 3 (default) = when there are at least 150 rows per group on
  *   average; 1 = always; 2 = always, without swapped tails; 0 = never (one
- *   CTA per 128-row tile).  fp8-weight GEMMs always use one CTA per tile.
- *   Results are the same up to fp32 summation order. */
+ *   CTA per 128-row tile).  FP8_E4M3 GEMMs always use one CTA per tile;
+ *   FP8_E4M3_NK GEMMs use 2-CTA tiles without swapped tails, under policy 3
+ *   only with at least 1024 rows per group on average.  Results are the
+ *   same up to fp32 summation order. */
 #define MOE_OPT_PAIR_TILES 1
 /*   MOE_OPT_GATHER_A: 1 = moe_layer does not materialise the permuted rows;
  *   the routed gate/up GEMM gathers its A rows from x with TMA tile::gather4

@@ -17,7 +17,7 @@ _PKG_DIR = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG_DIR, "libmoe_gb300.so")
 HEADER_PATH = os.path.join(os.path.dirname(_PKG_DIR), "include", "moe.h")
 
-MOE_F32, MOE_BF16, MOE_FP8_E4M3 = 0, 1, 2
+MOE_F32, MOE_BF16, MOE_FP8_E4M3, MOE_FP8_E4M3_NK = 0, 1, 2, 3
 MOE_ACT_SWIGLU, MOE_ACT_GEGLU_TANH = 0, 1
 MOE_OK = 0
 MOE_DEV_BAD_EXPERT_ID = 0x1
@@ -28,7 +28,8 @@ MOE_DEV_WAIT_TIMEOUT = 0x10
 WS_SLOTS = ["logits", "topk_ids", "topk_w", "counts", "offsets", "sorted_rows", "dest",
             "x_perm", "h", "y_perm", "h_shared", "s", "x16", "tok_inv", "row_inv"]
 
-_DTYPES = {"f32": MOE_F32, "bf16": MOE_BF16, "fp8_e4m3": MOE_FP8_E4M3}
+_DTYPES = {"f32": MOE_F32, "bf16": MOE_BF16, "fp8_e4m3": MOE_FP8_E4M3,
+           "fp8_e4m3_nk": MOE_FP8_E4M3_NK}
 _ACTS = {"swiglu": MOE_ACT_SWIGLU, "geglu_tanh": MOE_ACT_GEGLU_TANH}
 
 
@@ -62,6 +63,7 @@ _SIGS = {
     "moe_set_trace_events": (ctypes.c_int, [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]),
     "moe_permute_noalloc": (ctypes.c_int, [ctypes.POINTER(MoEConfig)] + [_P] * 7 + [_P]),
     "moe_set_option": (ctypes.c_int, [ctypes.c_int, ctypes.c_int]),
+    "moe_pack_weights_nk": (ctypes.c_int, [_P, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, _P, _P]),
 }
 MOE_OPT_PAIR_TILES = 1
 MOE_OPT_GATHER_A = 2
@@ -101,10 +103,16 @@ def make_config(T: int, D: int, E: int, k: int, I: int, I_shared: int = 0, act: 
                      1 if renormalize else 0)
 
 
-def config_from_shape(shape) -> MoEConfig:
-    """MoEConfig from a workloads.MoEShape-like object."""
+def config_from_shape(shape, fp8_layout: str = "kn") -> MoEConfig:
+    """MoEConfig from a workloads.MoEShape-like object.  For fp8 weights,
+    fp8_layout "nk" selects MOE_FP8_E4M3_NK (weights packed by pack_weights_nk)."""
+    if fp8_layout not in ("kn", "nk"):
+        raise ValueError("fp8_layout is 'kn' or 'nk'")
+    w = shape.w_dtype
+    if w == "fp8_e4m3" and fp8_layout == "nk":
+        w = "fp8_e4m3_nk"
     return make_config(shape.T, shape.D, shape.E, shape.k, shape.I, shape.I_shared, shape.act,
-                       shape.act_dtype, shape.w_dtype, shape.renormalize)
+                       shape.act_dtype, w, shape.renormalize)
 
 
 def _ptr(t) -> Optional[int]:
@@ -223,6 +231,27 @@ def moe_layer(cfg, x, Wg, logit_bias, W13, s13, W2, s2, W13s, s13s, W2s, s2s, ou
         ctypes.byref(cfg), _ptr(x), _ptr(Wg), _ptr(logit_bias), _ptr(W13), _ptr(s13), _ptr(W2),
         _ptr(s2), _ptr(W13s), _ptr(s13s), _ptr(W2s), _ptr(s2s), _ptr(out), wp, wb,
         _stream(stream)))
+
+
+def moe_pack_weights_nk(W, G: int, K: int, N: int, W_nk, stream=None) -> None:
+    _check("moe_pack_weights_nk", load_library().moe_pack_weights_nk(
+        _ptr(W), G, K, N, _ptr(W_nk), _stream(stream)))
+
+
+def pack_weights_nk(W, stream=None):
+    """A new [G, N, K] (or [N, K]) copy of the one-byte [G, K, N] (or [K, N])
+    weight tensor W, written by moe_pack_weights_nk on W's device."""
+    import torch
+
+    if W.element_size() != 1:
+        raise ValueError("pack_weights_nk takes one-byte (e4m3) weights")
+    if W.dim() not in (2, 3):
+        raise ValueError("pack_weights_nk takes [K, N] or [G, K, N] weights")
+    Wg = W if W.dim() == 3 else W.unsqueeze(0)
+    G, K, N = Wg.shape
+    out = torch.empty((G, N, K), dtype=W.dtype, device=W.device)
+    moe_pack_weights_nk(Wg, G, K, N, out, stream)
+    return out if W.dim() == 3 else out[0]
 
 
 def moe_read_device_status(ws, stream=None) -> int:

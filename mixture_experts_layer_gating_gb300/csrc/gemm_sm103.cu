@@ -262,7 +262,10 @@ __device__ __forceinline__ uint2 e4m3x4_to_f16x4(uint32_t w) {
   return r;
 }
 
-template <int EPI, bool SPLIT, bool FP8, bool PAIR>
+// Q8: A rows are two-term e4m3 (hi and lo tiles of the stage, as in SPLIT)
+// and B is e4m3 stored K-contiguous ([G, N, K]): the 8-bit kind::f8f6f4 with
+// 128 K elements (128 bytes) per stage and no weight expansion.
+template <int EPI, bool SPLIT, bool FP8, bool PAIR, bool Q8>
 __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                         const __grid_constant__ CUtensorMap tmap_a_lo,
@@ -271,9 +274,11 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
                         const __grid_constant__ CUtensorMap tmap_a_tail,
                         const __grid_constant__ CUtensorMap tmap_a_lo_tail, const KParams p) {
   pdl_wait();
+  static_assert(!Q8 || (SPLIT && !FP8), "two-term e4m3 rows use the split A stage layout");
   using Cfg = StageCfg<SPLIT, FP8, PAIR>;
   // fp8 weights: fp16 operands; everything else: bf16 operands
   constexpr bool F16 = FP8;
+  constexpr int KE = Q8 ? 128 : BK;  // K elements per stage (128 bytes of every operand row)
   constexpr int STAGES = Cfg::kStages;
   constexpr int STAGE_BYTES = Cfg::kStageBytes;
   constexpr int A_BYTES = Cfg::kABytes;
@@ -343,7 +348,7 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
 
   const uint32_t tmem_base = ctrl->tmem_slot;
   const int total_tiles = ctrl->tile_start[G] * p.n_tiles * p.ksplit;
-  const int KB = (p.K + BK - 1) / BK;
+  const int KB = (p.K + KE - 1) / KE;
   // work item t = (output tile t / ksplit, K split t % ksplit)
   auto kb_range = [&](int t, int& kb0, int& kb1) {
     kb0 = (t % p.ksplit) * p.kbs;
@@ -356,7 +361,9 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
   // swapped tail tile (2-CTA mode): its rows padded so that the MMA N (rows,
   // or 2 x rows in the down pass) is a multiple of 32 and each CTA's half of
   // the rows a multiple of 8
-  auto is_swap = [&](const TileInfo& ti) { return PAIR && p.swap_tail > 0 && ti.rows <= p.swap_tail; };
+  auto is_swap = [&](const TileInfo& ti) {
+    return PAIR && !Q8 && p.swap_tail > 0 && ti.rows <= p.swap_tail;
+  };
   auto swap_rows = [&](const TileInfo& ti) {
     return EPI == kEpiGateUpAct ? (ti.rows + 31) & ~31 : (ti.rows + 15) & ~15;
   };
@@ -449,17 +456,35 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
           if (lane == 0) {
           if (!gather) {
             if (PAIR) {
-              tma_load_2d_pair(a_dst, &tmap_a, fbar, kb * BK, my_row0, pol_a);
+              tma_load_2d_pair(a_dst, &tmap_a, fbar, kb * KE, my_row0, pol_a);
               if (SPLIT)
-                tma_load_2d_pair(a_dst + A_TILE_BYTES, &tmap_a_lo, fbar, kb * BK, my_row0, pol_a);
+                tma_load_2d_pair(a_dst + A_TILE_BYTES, &tmap_a_lo, fbar, kb * KE, my_row0, pol_a);
             } else {
-              tma_load_2d(a_dst, &tmap_a, &ctrl->full[stage], kb * BK, my_row0, pol_a);
+              tma_load_2d(a_dst, &tmap_a, &ctrl->full[stage], kb * KE, my_row0, pol_a);
               if (SPLIT)
-                tma_load_2d(a_dst + A_TILE_BYTES, &tmap_a_lo, &ctrl->full[stage], kb * BK,
+                tma_load_2d(a_dst + A_TILE_BYTES, &tmap_a_lo, &ctrl->full[stage], kb * KE,
                             my_row0, pol_a);
             }
           }
-          if (FP8) {
+          if (Q8) {
+            // e4m3 weights, K contiguous: 128-byte rows of the B tile (the gate/up
+            // pass: 128 gate rows then the 128 matching up rows; rank r of a pair
+            // its half: the gate rows (0) or the up rows (1), or output rows
+            // n0 + r * bn / 2 ..)
+            if (EPI == kEpiGateUpAct) {
+              if (PAIR)
+                tma_load_4d_pair(b_dst, &tmap_b, fbar, kb * KE, ti.n0, static_cast<int>(rank), ti.g,
+                                 pol_b);
+              else
+                tma_load_4d(b_dst, &tmap_b, &ctrl->full[stage], kb * KE, ti.n0, 0, ti.g, pol_b);
+            } else {
+              if (PAIR)
+                tma_load_3d_pair(b_dst, &tmap_b, fbar, kb * KE,
+                                 ti.n0 + static_cast<int>(rank) * (p.bn / 2), ti.g, pol_b);
+              else
+                tma_load_3d(b_dst, &tmap_b, &ctrl->full[stage], kb * KE, ti.n0, ti.g, pol_b);
+            }
+          } else if (FP8) {
             // raw e4m3 boxes land on this CTA's own barrier for its converters
             uint8_t* r_dst = stage_raw(stage);
             mbar_arrive_expect_tx(&ctrl->raw_full[stage], nraw * RAW_BOX_BYTES);
@@ -556,6 +581,7 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
         // (K-major), N = rows (gate/up) or 2 x rows (down: h_hi | h_lo)
         const uint32_t idesc_swap =
             make_idesc_bf16_f32(TILE_M, (EPI == kEpiGateUpAct ? 1 : 2) * swap_rows(ti), 1, 0);
+        const uint32_t idesc_q8 = make_idesc_e4m3_f32(TILE_M, p.bn);
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&ctrl->full[stage], phase, abort_flag)) {
             ok = false;
@@ -571,6 +597,32 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
                               smem_desc_advance(rdesc0, kk * 32), idesc_swap,
                               ((kb - kb0) | kk) != 0);
             tc_commit_pair_multicast(&ctrl->empty[stage], 0x3);
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            continue;
+          }
+          if (Q8) {
+            // A hi / lo and B all K-major with 128-byte rows; a K step of 32
+            // e4m3 is 32 bytes.  acc += hi * B, then += lo * B.
+            const uint64_t adesc0 = make_smem_desc_sw128(smem_u32(stage_a(stage)), 16, 1024);
+            const uint64_t bdesc0 = make_smem_desc_sw128(smem_u32(stage_b(stage)), 16, 1024);
+#pragma unroll
+            for (int kk = 0; kk < KE / 32; ++kk) {
+              const uint64_t bdesc = smem_desc_advance(bdesc0, kk * 32);
+              const uint64_t ahi = smem_desc_advance(adesc0, kk * 32);
+              const uint64_t alo = smem_desc_advance(adesc0, A_TILE_BYTES + kk * 32);
+              if (PAIR) {
+                tc_mma_f8_pair(d_tmem, ahi, bdesc, idesc_q8, ((kb - kb0) | kk) != 0);
+                tc_mma_f8_pair(d_tmem, alo, bdesc, idesc_q8, 1);
+              } else {
+                tc_mma_f8(d_tmem, ahi, bdesc, idesc_q8, ((kb - kb0) | kk) != 0);
+                tc_mma_f8(d_tmem, alo, bdesc, idesc_q8, 1);
+              }
+            }
+            if (PAIR) tc_commit_pair_multicast(&ctrl->empty[stage], 0x3);
+            else tc_commit(&ctrl->empty[stage]);
             if (++stage == STAGES) {
               stage = 0;
               phase ^= 1u;
@@ -988,12 +1040,17 @@ static_assert(dec_smem_bytes<false, true>() <= 227 * 1024, "shared memory budget
 // group_offsets, K reduction, N output features, bn = rows per tile (MMA N),
 // cols_per_tile = output features per tile (64 gate/up, 128 down),
 // a_row_scale per row.
-template <int EPI, bool SPLIT, bool FP8>
+// Q8: two-term e4m3 rows (the hi rows, then the lo rows, stacked along N as in
+// SPLIT) and e4m3 weights stored K-contiguous ([G, N, K]), K-major as the
+// M = 128 operand: kind::f8f6f4, 128 K elements per stage, no expansion.
+template <int EPI, bool SPLIT, bool FP8, bool Q8>
 __global__ void __launch_bounds__(DecCfg<SPLIT, FP8>::kThreads, 1)
     grouped_gemm_decode_kernel(const __grid_constant__ CUtensorMap tmap_rows,
                                const __grid_constant__ CUtensorMap tmap_rows_lo,
                                const __grid_constant__ CUtensorMap tmap_w, const KParams p) {
   pdl_wait();
+  static_assert(!Q8 || (SPLIT && !FP8), "two-term e4m3 rows use the split row layout");
+  constexpr int KE = Q8 ? 128 : BK;  // K elements per stage (128 bytes of every operand row)
   using Cfg = DecCfg<SPLIT, FP8>;
   constexpr int STAGES = Cfg::kStages;
   constexpr int STAGE_BYTES = Cfg::kStageBytes;
@@ -1043,7 +1100,7 @@ __global__ void __launch_bounds__(DecCfg<SPLIT, FP8>::kThreads, 1)
 
   const uint32_t tmem_base = ctrl->tmem_slot;
   const int total_tiles = ctrl->tile_start[G] * p.n_tiles;
-  const int KB = (p.K + BK - 1) / BK;
+  const int KB = (p.K + KE - 1) / KE;
   const uint32_t rows_bytes = static_cast<uint32_t>(NT) * BK * 2;
 
   if (warp == 0) {
@@ -1062,10 +1119,24 @@ __global__ void __launch_bounds__(DecCfg<SPLIT, FP8>::kThreads, 1)
             break;
           }
           mbar_arrive_expect_tx(&ctrl->full[stage], tx);
-          tma_load_2d(stage_rows(stage), &tmap_rows, &ctrl->full[stage], kb * BK, ti.row0, pol_rows);
+          tma_load_2d(stage_rows(stage), &tmap_rows, &ctrl->full[stage], kb * KE, ti.row0, pol_rows);
           if (SPLIT)
             tma_load_2d(stage_rows(stage) + NT * 128, &tmap_rows_lo, &ctrl->full[stage],
-                        kb * BK, ti.row0, pol_rows);
+                        kb * KE, ti.row0, pol_rows);
+          if (Q8) {
+            // 128 weight rows of 128 bytes (64 gate rows, then the 64 matching up
+            // rows; or 128 consecutive output features)
+            if (EPI == kEpiGateUpAct)
+              tma_load_4d(stage_w(stage), &tmap_w, &ctrl->full[stage], kb * KE, ti.n0, 0, ti.g,
+                          pol_w);
+            else
+              tma_load_3d(stage_w(stage), &tmap_w, &ctrl->full[stage], kb * KE, ti.n0, ti.g, pol_w);
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            continue;
+          }
           uint8_t* wdst = FP8 ? stage_raw(stage) : stage_w(stage);
           uint64_t* wbar = FP8 ? &ctrl->raw_full[stage] : &ctrl->full[stage];
           const int wbox = FP8 ? DEC_RAW_BOX_BYTES : DEC_W_BYTES / 2;
@@ -1097,8 +1168,9 @@ __global__ void __launch_bounds__(DecCfg<SPLIT, FP8>::kThreads, 1)
       // products; the epilogue adds them): half the MMA instructions, which
       // at these N are what bounds the pass
       const int mma_n = SPLIT ? 2 * NT : NT;
-      const uint32_t idesc = FP8 ? make_idesc_f16_f32(DEC_M, mma_n, 1, 0)
-                                 : make_idesc_bf16_f32(DEC_M, mma_n, 1, 0);
+      const uint32_t idesc = Q8    ? make_idesc_e4m3_f32(DEC_M, mma_n)
+                             : FP8 ? make_idesc_f16_f32(DEC_M, mma_n, 1, 0)
+                                   : make_idesc_bf16_f32(DEC_M, mma_n, 1, 0);
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
@@ -1114,15 +1186,23 @@ __global__ void __launch_bounds__(DecCfg<SPLIT, FP8>::kThreads, 1)
             break;
           }
           tc_fence_after_sync();
-          // A = weights, N-major: 64-feature groups 8 KB apart, K step of 16 rows = 2 KB
-          // B = rows, K-major: 128-byte rows, K step of 16 = 32 bytes
-          const uint64_t adesc0 = make_smem_desc_sw128(smem_u32(stage_w(stage)), DEC_W_BYTES / 2, 1024);
           const uint64_t bdesc0 = make_smem_desc_sw128(smem_u32(stage_rows(stage)), 16, 1024);
+          if (Q8) {
+            // A = weights and B = rows, both K-major 128-byte rows; K step of 32 e4m3 = 32 bytes
+            const uint64_t adesc0 = make_smem_desc_sw128(smem_u32(stage_w(stage)), 16, 1024);
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t adesc = smem_desc_advance(adesc0, kk * 2048);
-            const uint64_t bdesc = smem_desc_advance(bdesc0, kk * 32);
-            tc_mma_f16(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0);
+            for (int kk = 0; kk < KE / 32; ++kk)
+              tc_mma_f8(d_tmem, smem_desc_advance(adesc0, kk * 32), smem_desc_advance(bdesc0, kk * 32),
+                        idesc, (kb | kk) != 0);
+          } else {
+            // A = weights, N-major: 64-feature groups 8 KB apart, K step of 16 rows = 2 KB
+            // B = rows, K-major: 128-byte rows, K step of 16 = 32 bytes
+            const uint64_t adesc0 =
+                make_smem_desc_sw128(smem_u32(stage_w(stage)), DEC_W_BYTES / 2, 1024);
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk)
+              tc_mma_f16(d_tmem, smem_desc_advance(adesc0, kk * 2048),
+                         smem_desc_advance(bdesc0, kk * 32), idesc, (kb | kk) != 0);
           }
           tc_commit(&ctrl->empty[stage]);
           if (++stage == STAGES) {
@@ -1351,14 +1431,14 @@ bool encode_tmap(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims
   return r == CUDA_SUCCESS;
 }
 
-template <int EPI, bool SPLIT, bool FP8, bool PAIR>
+template <int EPI, bool SPLIT, bool FP8, bool PAIR, bool Q8 = false>
 cudaError_t launch_epi(const CUtensorMap& ta, const CUtensorMap& ta_lo, const CUtensorMap& tb,
                        const CUtensorMap& tb_tail, const CUtensorMap& ta_tail,
                        const CUtensorMap& ta_lo_tail, const KParams& kp, long long max_tiles,
                        cudaStream_t s) {
   constexpr size_t smem = smem_bytes<SPLIT, FP8, PAIR>();
   constexpr int threads = StageCfg<SPLIT, FP8, PAIR>::kThreads;
-  auto kern = grouped_gemm_kernel<EPI, SPLIT, FP8, PAIR>;
+  auto kern = grouped_gemm_kernel<EPI, SPLIT, FP8, PAIR, Q8>;
   // the attribute is per device: set it once for each device this process uses
   static bool done[64] = {false};
   int dev = 0;
@@ -1415,12 +1495,12 @@ int g_pdl = 1;             // set through moe_set_option(MOE_OPT_PDL, .)
 
 namespace {
 
-template <int EPI, bool SPLIT, bool FP8>
+template <int EPI, bool SPLIT, bool FP8, bool Q8 = false>
 cudaError_t launch_dec(const CUtensorMap& tr, const CUtensorMap& tr_lo, const CUtensorMap& tw,
                        const KParams& kp, long long max_tiles, cudaStream_t s) {
   constexpr size_t smem = dec_smem_bytes<SPLIT, FP8>();
   constexpr int threads = DecCfg<SPLIT, FP8>::kThreads;
-  auto kern = grouped_gemm_decode_kernel<EPI, SPLIT, FP8>;
+  auto kern = grouped_gemm_decode_kernel<EPI, SPLIT, FP8, Q8>;
   static bool done[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -1435,8 +1515,60 @@ cudaError_t launch_dec(const CUtensorMap& tr, const CUtensorMap& tr_lo, const CU
   return launch_kernel(kern, dim3(grid), dim3(threads), smem, s, tr, tr_lo, tw, kp);
 }
 
+// Swap-AB launch for decode-size groups, two-term e4m3 rows and K-contiguous
+// e4m3 weights: nt rows per tile (2 nt MMA columns: hi rows, then lo rows).
+cudaError_t launch_grouped_gemm_decode_q8(const GroupedGemmArgs& a, int nt, cudaStream_t s) {
+  CUtensorMap tr, tr_lo, tw;
+  const uint64_t K = static_cast<uint64_t>(a.K), N = static_cast<uint64_t>(a.N);
+  const uint64_t M = static_cast<uint64_t>(a.M), G = static_cast<uint64_t>(a.G);
+  const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  {
+    const uint64_t dims[2] = {K, M};
+    const uint64_t strides[1] = {2 * K};
+    const uint32_t box[2] = {128, static_cast<uint32_t>(nt)};
+    if (!encode_tmap(&tr, a.A, 2, dims, strides, box, u8)) return cudaErrorInvalidValue;
+    if (!encode_tmap(&tr_lo, static_cast<const uint8_t*>(a.A) + K, 2, dims, strides, box, u8))
+      return cudaErrorInvalidValue;
+  }
+  KParams kp{};
+  kp.group_offsets = a.group_offsets;
+  kp.G = a.G;
+  kp.M = a.M;
+  kp.K = a.K;
+  kp.N = a.N;
+  kp.out = a.out;
+  kp.b_scale = a.b_scale;
+  kp.a_row_scale = a.a_row_scale;
+  kp.h_fp32 = a.h_fp32;
+  kp.act = a.act;
+  kp.err = a.err;
+  kp.bn = nt;
+  kp.ksplit = 1;
+  kp.kbs = (a.K + 127) / 128;
+  if (a.epilogue == kEpiGateUpAct) {  // [G][2][N][K]: 64 gate rows, then the 64 up rows
+    const uint64_t dims[4] = {K, N, 2, G};
+    const uint64_t strides[3] = {K, N * K, 2 * N * K};
+    const uint32_t box[4] = {128, 64, 2, 1};
+    if (!encode_tmap(&tw, a.B, 4, dims, strides, box, u8)) return cudaErrorInvalidValue;
+    kp.cols_per_tile = 64;
+  } else {  // [G][N][K]: 128 output features
+    const uint64_t dims[3] = {K, N, G};
+    const uint64_t strides[2] = {K, N * K};
+    const uint32_t box[3] = {128, 128, 1};
+    if (!encode_tmap(&tw, a.B, 3, dims, strides, box, u8)) return cudaErrorInvalidValue;
+    kp.cols_per_tile = 128;
+  }
+  kp.n_tiles = (a.N + kp.cols_per_tile - 1) / kp.cols_per_tile;
+  const long long max_tiles =
+      (static_cast<long long>((a.M + nt - 1) / nt) + a.G) * static_cast<long long>(kp.n_tiles);
+  if (a.epilogue == kEpiGateUpAct)
+    return launch_dec<kEpiGateUpAct, true, false, true>(tr, tr_lo, tw, kp, max_tiles, s);
+  return launch_dec<kEpiStoreF32, true, false, true>(tr, tr_lo, tw, kp, max_tiles, s);
+}
+
 // Swap-AB launch for decode-size groups: nt rows per tile.
 cudaError_t launch_grouped_gemm_decode(const GroupedGemmArgs& a, int nt, cudaStream_t s) {
+  if (a.a_e4m3x2) return launch_grouped_gemm_decode_q8(a, nt, s);
   CUtensorMap tr, tr_lo, tw;
   const CUtensorMapDataType adt =
       a.a_fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -1494,6 +1626,81 @@ cudaError_t launch_grouped_gemm_decode(const GroupedGemmArgs& a, int nt, cudaStr
                 : launch_dec<kEpiStoreF32, false, false>(tr, tr_lo, tw, kp, max_tiles, s);
 }
 
+// 128-row (or 2-CTA 256-row) tiles for two-term e4m3 rows and K-contiguous
+// e4m3 weights: kind::f8f6f4, hi and lo products into one accumulator.
+cudaError_t launch_grouped_gemm_q8(const GroupedGemmArgs& a, cudaStream_t s) {
+  if (!a.b_fp8 || a.a_gather || a.A_lo || a.ksplit > 1 || a.bias) return cudaErrorInvalidValue;
+  if (a.G < 1 || a.G > MAX_G) return cudaErrorInvalidValue;
+  const uint64_t K = static_cast<uint64_t>(a.K), N = static_cast<uint64_t>(a.N);
+  const uint64_t M = static_cast<uint64_t>(a.M), G = static_cast<uint64_t>(a.G);
+  const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  KParams kp{};
+  kp.group_offsets = a.group_offsets;
+  kp.G = a.G;
+  kp.M = a.M;
+  kp.K = a.K;
+  kp.N = a.N;
+  kp.out = a.out;
+  kp.b_scale = a.b_scale;
+  kp.a_row_scale = a.a_row_scale;
+  kp.h_fp32 = a.h_fp32;
+  kp.act = a.act;
+  kp.err = a.err;
+  kp.ksplit = 1;
+  kp.kbs = (a.K + 127) / 128;
+  if (a.epilogue == kEpiGateUpAct) {
+    kp.bn = 256;
+    kp.cols_per_tile = 128;
+  } else {
+    kp.bn = static_cast<int>(std::min<uint64_t>(BN_MAX, (N + 63) / 64 * 64));
+    kp.cols_per_tile = kp.bn;
+  }
+  kp.n_tiles = (a.N + kp.cols_per_tile - 1) / kp.cols_per_tile;
+  // 2-CTA tiles here have no swapped tails, so a group's last 256-row tile is
+  // often mostly empty: by default (policy 3) they run only with >= 1024 rows
+  // per group on average (the shared expert at prefill: 5-9 % faster), where
+  // that waste is small; Ling-style routed passes (~512 rows per group)
+  // measured 7 % slower on them than on 128-row tiles.
+  const bool pair_policy =
+      g_pair_tiles == 1 || g_pair_tiles == 2 ||
+      (g_pair_tiles == 3 && static_cast<long long>(a.M) >= 1024ll * a.G);
+  const bool pair = a.pair_ok && kp.bn == 256 && pair_policy;
+  CUtensorMap ta, ta_lo, tb;
+  {
+    const uint64_t dims[2] = {K, M};
+    const uint64_t strides[1] = {2 * K};
+    const uint32_t box[2] = {128, BM};
+    if (!encode_tmap(&ta, a.A, 2, dims, strides, box, u8)) return cudaErrorInvalidValue;
+    if (!encode_tmap(&ta_lo, static_cast<const uint8_t*>(a.A) + K, 2, dims, strides, box, u8))
+      return cudaErrorInvalidValue;
+  }
+  if (a.epilogue == kEpiGateUpAct) {  // [G][2][N][K]: gate rows, then up rows
+    const uint64_t dims[4] = {K, N, 2, G};
+    const uint64_t strides[3] = {K, N * K, 2 * N * K};
+    const uint32_t box[4] = {128, 128, pair ? 1u : 2u, 1};
+    if (!encode_tmap(&tb, a.B, 4, dims, strides, box, u8)) return cudaErrorInvalidValue;
+  } else {  // [G][N][K]
+    const uint64_t dims[3] = {K, N, G};
+    const uint64_t strides[2] = {K, N * K};
+    const uint32_t box[3] = {128, static_cast<uint32_t>(pair ? kp.bn / 2 : kp.bn), 1};
+    if (!encode_tmap(&tb, a.B, 3, dims, strides, box, u8)) return cudaErrorInvalidValue;
+  }
+  const int tile_m = pair ? 2 * BM : BM;
+  const long long max_tiles = (static_cast<long long>((a.M + tile_m - 1) / tile_m) + a.G) *
+                              static_cast<long long>(kp.n_tiles);
+  if (a.epilogue == kEpiGateUpAct)
+    return pair ? launch_epi<kEpiGateUpAct, true, false, true, true>(ta, ta_lo, tb, tb, ta, ta_lo, kp,
+                                                                     max_tiles, s)
+                : launch_epi<kEpiGateUpAct, true, false, false, true>(ta, ta_lo, tb, tb, ta, ta_lo,
+                                                                      kp, max_tiles, s);
+  if (a.epilogue == kEpiStoreF32)
+    return pair ? launch_epi<kEpiStoreF32, true, false, true, true>(ta, ta_lo, tb, tb, ta, ta_lo, kp,
+                                                                    max_tiles, s)
+                : launch_epi<kEpiStoreF32, true, false, false, true>(ta, ta_lo, tb, tb, ta, ta_lo, kp,
+                                                                     max_tiles, s);
+  return cudaErrorInvalidValue;
+}
+
 }  // namespace
 
 int router_k_split(int T, int E, int D) {
@@ -1526,7 +1733,12 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
   // at most 256 groups (Qwen3-MoE decode: 223 -> 213 us); 64 rows per tile for
   // fp8 weights at up to 16 rows per group.  Elsewhere 128-row tiles already
   // stream the weights at close to HBM peak (Qwen3.5-style decode: 92-100 %).
+  // fp8 weights (expanded on chip, or read as e4m3 by the 8-bit kind) take
+  // 64-row decode tiles up to 16 rows per group: Ling-style decode (16 rows
+  // per group) measured 2201 us per layer on them against 2380 us on 128-row
+  // tiles and 2606 us on 16-row decode tiles with e4m3 rows.
   const long long Mg = a.M, Gg = a.G;
+  if (a.a_e4m3x2 && (!a.b_fp8 || a.a_fp16)) return cudaErrorInvalidValue;
   int nt = 0;
   if (g_decode_kernel == 2) nt = DEC_NT_MAX;
   else if (g_decode_kernel == 3) nt = 16;
@@ -1536,10 +1748,11 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
   else if (a.b_fp8 && Mg <= 16 * Gg) nt = DEC_NT_MAX;
   if (g_decode_kernel && nt && a.decode_ok && !a.a_gather && a.ksplit <= 1 && a.G <= MAX_G &&
       (a.epilogue == kEpiGateUpAct || a.epilogue == kEpiStoreF32)) {
-    if ((a.a_fp16 != 0) != (a.b_fp8 != 0)) return cudaErrorInvalidValue;
+    if (!a.a_e4m3x2 && (a.a_fp16 != 0) != (a.b_fp8 != 0)) return cudaErrorInvalidValue;
     if (a.b_fp8 && a.A_lo) return cudaErrorNotSupported;
     return launch_grouped_gemm_decode(a, nt, s);
   }
+  if (a.a_e4m3x2) return launch_grouped_gemm_q8(a, s);
   if (a.b_fp8 && a.A_lo) return cudaErrorNotSupported;
   // fp16 A rows exactly when the weights are fp8
   if ((a.a_fp16 != 0) != (a.b_fp8 != 0)) return cudaErrorInvalidValue;

@@ -96,8 +96,12 @@ bool cfg_valid(const moe_config_t* c) {
   if (c->D % 8 || c->I % 8 || c->I_shared % 8) return false;
   if (c->act != MOE_ACT_SWIGLU && c->act != MOE_ACT_GEGLU_TANH) return false;
   if (c->act_dtype != MOE_F32 && c->act_dtype != MOE_BF16) return false;
-  if (c->w_dtype != MOE_F32 && c->w_dtype != MOE_BF16 && c->w_dtype != MOE_FP8_E4M3) return false;
-  if (c->w_dtype == MOE_FP8_E4M3 && (c->D % 16 || c->I % 16 || c->I_shared % 16)) return false;
+  if (c->w_dtype != MOE_F32 && c->w_dtype != MOE_BF16 && c->w_dtype != MOE_FP8_E4M3 &&
+      c->w_dtype != MOE_FP8_E4M3_NK)
+    return false;
+  if ((c->w_dtype == MOE_FP8_E4M3 || c->w_dtype == MOE_FP8_E4M3_NK) &&
+      (c->D % 16 || c->I % 16 || c->I_shared % 16))
+    return false;
   const long long R = static_cast<long long>(c->T) * c->k;
   if (R > (1ll << 30)) return false;
   return true;
@@ -105,7 +109,23 @@ bool cfg_valid(const moe_config_t* c) {
 
 bool combo_supported(const moe_config_t* c) {
   if (c->act_dtype == MOE_F32) return c->w_dtype == MOE_F32;
-  return c->w_dtype == MOE_BF16 || c->w_dtype == MOE_FP8_E4M3;
+  return c->w_dtype == MOE_BF16 || c->w_dtype == MOE_FP8_E4M3 || c->w_dtype == MOE_FP8_E4M3_NK;
+}
+
+// fp8 weights of either layout (per-column scales, rows with power-of-two scales)
+inline bool is_fp8(const moe_config_t* c) {
+  return c->w_dtype == MOE_FP8_E4M3 || c->w_dtype == MOE_FP8_E4M3_NK;
+}
+// fp8 weights stored K-contiguous: the 8-bit kind with two-term e4m3 rows
+inline bool is_nk(const moe_config_t* c) { return c->w_dtype == MOE_FP8_E4M3_NK; }
+
+// bf16 / fp32 rows -> the A-row form of an fp8 layer: fp16 rows (expanded
+// weights) or two-term e4m3 rows (K-contiguous weights), both D * 2 bytes per
+// row, with inverse power-of-two scales.
+cudaError_t rows_to_fp8_layer_form(const moe_config_t* c, const void* x, int rows, int D, void* q,
+                                   float* inv_scale, cudaStream_t s, bool src_f32 = false) {
+  return is_nk(c) ? launch_rows_to_e4m3x2(x, rows, D, q, inv_scale, s, src_f32)
+                  : launch_rows_to_fp16(x, rows, D, q, inv_scale, s, src_f32);
 }
 
 Layout make_layout(const moe_config_t* c) {
@@ -136,7 +156,7 @@ Layout make_layout(const moe_config_t* c) {
   L.off[MOE_WS_Y_PERM] = take(R * D * 4);    // fp32
   L.off[MOE_WS_H_SHARED] = take(T * Is * 4);
   L.off[MOE_WS_S] = take(T * D * 4);
-  if (c->w_dtype == MOE_FP8_E4M3) {
+  if (is_fp8(c)) {
     L.x16 = take(T * D * 2);
     L.tok_inv = take(T * 4);
     L.row_inv = take(R * 4);
@@ -257,8 +277,10 @@ int do_ffn(const moe_config_t* c, const void* A, const float* a_row_scale, int M
     return cuda_status(e);
   }
   // bf16 weights: h is two bf16 planes [M, I], h_hi then h_lo (h ~= h_hi + h_lo),
-  // and the down pass multiplies both.  fp8 weights: h in fp32, then fp16 rows.
-  const bool fp8 = c->w_dtype == MOE_FP8_E4M3;
+  // and the down pass multiplies both.  fp8 weights: h in fp32, then fp16 rows
+  // (or two-term e4m3 rows for K-contiguous weights).
+  const bool fp8 = is_fp8(c);
+  const bool nk = is_nk(c);
   void* h_lo = fp8 ? nullptr : static_cast<uint8_t*>(h) + static_cast<size_t>(M) * I * 2;
   GroupedGemmArgs a{};
   a.epilogue = kEpiGateUpAct;
@@ -269,7 +291,8 @@ int do_ffn(const moe_config_t* c, const void* A, const float* a_row_scale, int M
   a.G = G;
   a.B = W13;
   a.b_fp8 = fp8;
-  a.a_fp16 = fp8;
+  a.a_fp16 = fp8 && !nk;
+  a.a_e4m3x2 = nk;
   a.a_row_scale = a_row_scale;
   a.a_gather = a_gather;
   a.gather_k = c->k;
@@ -287,7 +310,7 @@ int do_ffn(const moe_config_t* c, const void* A, const float* a_row_scale, int M
   if (e != cudaSuccess) return e == cudaErrorNotSupported ? MOE_ERR_UNSUPPORTED : MOE_ERR_CUDA;
   if (fp8) {
     trace_mark(s);
-    if (launch_rows_to_fp16(h, M, I, h16, h_inv, s, /*src_f32=*/true) != cudaSuccess)
+    if (rows_to_fp8_layer_form(c, h, M, I, h16, h_inv, s, /*src_f32=*/true) != cudaSuccess)
       return MOE_ERR_CUDA;
   }
   GroupedGemmArgs b = a;
@@ -298,7 +321,7 @@ int do_ffn(const moe_config_t* c, const void* A, const float* a_row_scale, int M
   b.B = W2;
   b.N = c->D;
   b.b_scale = s2;
-  b.a_fp16 = fp8;
+  b.a_fp16 = fp8 && !nk;
   b.a_row_scale = fp8 ? h_inv : nullptr;
   b.a_gather = nullptr;
   b.h_fp32 = 0;
@@ -322,7 +345,7 @@ int do_grouped_ffn(const moe_config_t* c, const void* x_perm, const float* xp_sc
                    const int32_t* gather = nullptr) {
   const int R = c->T * c->k;
   const Layout L = make_layout(c);
-  const bool fp8 = c->w_dtype == MOE_FP8_E4M3;
+  const bool fp8 = is_fp8(c);
   int st = do_ffn(c, x_perm, xp_scale, R, offsets, c->E, W13, s13, W2, s2, c->I, h, y_perm,
                   fp8 ? ws_at(ws, L.h16) : nullptr,
                   fp8 ? reinterpret_cast<float*>(ws_at(ws, L.h_inv)) : nullptr, err, s, gather,
@@ -336,7 +359,7 @@ int do_grouped_ffn(const moe_config_t* c, const void* x_perm, const float* xp_sc
 }
 
 bool fp8_scales_ok(const moe_config_t* c, const float* s13, const float* s2) {
-  const bool fp8 = c->w_dtype == MOE_FP8_E4M3;
+  const bool fp8 = is_fp8(c);
   return fp8 ? (s13 && s2) : (!s13 && !s2);
 }
 
@@ -353,7 +376,7 @@ size_t moe_workspace_offset(const moe_config_t* cfg, int which) {
   if (!cfg_valid(cfg) || which < 0 || which > MOE_WS_ROW_INV) return static_cast<size_t>(-1);
   const Layout L = make_layout(cfg);
   if (which <= MOE_WS_S) return L.off[which];
-  if (cfg->w_dtype != MOE_FP8_E4M3) return static_cast<size_t>(-1);
+  if (!is_fp8(cfg)) return static_cast<size_t>(-1);
   return which == MOE_WS_X16 ? L.x16 : which == MOE_WS_TOK_INV ? L.tok_inv : L.row_inv;
 }
 
@@ -406,21 +429,21 @@ int moe_grouped_ffn(const moe_config_t* cfg, const void* x_perm, const int32_t* 
   }
   if (cfg->T == 0) return MOE_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cfg->w_dtype == MOE_FP8_E4M3) {
-    // fp8 weights run on the fp16 tensor-core kind: convert the bf16 rows to
-    // fp16 rows with exact power-of-two scales in the workspace first
+  if (is_fp8(cfg)) {
+    // fp8 weights: convert the bf16 rows to fp16 rows (or two-term e4m3 rows)
+    // with exact power-of-two scales in the workspace first
     const Layout L = make_layout(cfg);
     const int R = cfg->T * cfg->k;
     void* xp16 = ws_at(ws, L.off[MOE_WS_X_PERM]);
     float* row_inv = reinterpret_cast<float*>(ws_at(ws, L.row_inv));
-    if (launch_rows_to_fp16(x_perm, R, cfg->D, xp16, row_inv, s) != cudaSuccess)
+    if (rows_to_fp8_layer_form(cfg, x_perm, R, cfg->D, xp16, row_inv, s) != cudaSuccess)
       return MOE_ERR_CUDA;
     void* x16 = nullptr;
     float* tok_inv = nullptr;
     if (shared) {
       x16 = ws_at(ws, L.x16);
       tok_inv = reinterpret_cast<float*>(ws_at(ws, L.tok_inv));
-      if (launch_rows_to_fp16(x, cfg->T, cfg->D, x16, tok_inv, s) != cudaSuccess)
+      if (rows_to_fp8_layer_form(cfg, x, cfg->T, cfg->D, x16, tok_inv, s) != cudaSuccess)
         return MOE_ERR_CUDA;
     }
     return do_grouped_ffn(cfg, xp16, row_inv, offsets, W13, s13, W2, s2, h, y_perm, x16, tok_inv,
@@ -479,18 +502,18 @@ int moe_layer(const moe_config_t* cfg, const void* x, const void* Wg, const floa
 
   const bool traced = g_trace_events && g_trace_n >= moe_layer_launch_count(cfg) + 1;
   g_trace_next = traced ? 0 : -1;
-  const bool fp8 = cfg->w_dtype == MOE_FP8_E4M3;
+  const bool fp8 = is_fp8(cfg);
   const void* x_rows = x;  // what the gather and the shared expert read
   float* tok_inv = nullptr;
   float* row_inv = nullptr;
   if (fp8) {
-    // fp16 tensor-core kind for fp8 weights: x once to fp16 rows with exact
+    // fp8 weights: x once to fp16 rows (or two-term e4m3 rows) with exact
     // power-of-two scales; the gather carries the inverse scale per row
     void* x16 = ws_at(ws, L.x16);
     tok_inv = reinterpret_cast<float*>(ws_at(ws, L.tok_inv));
     row_inv = reinterpret_cast<float*>(ws_at(ws, L.row_inv));
     trace_mark(s);
-    if (launch_rows_to_fp16(x, cfg->T, cfg->D, x16, tok_inv, s) != cudaSuccess)
+    if (rows_to_fp8_layer_form(cfg, x, cfg->T, cfg->D, x16, tok_inv, s) != cudaSuccess)
       return (g_trace_next = -1, MOE_ERR_CUDA);
     x_rows = x16;
   }
@@ -522,7 +545,7 @@ int moe_layer(const moe_config_t* cfg, const void* x, const void* Wg, const floa
   // With MOE_OPT_GATHER_A the routed gate/up pass instead gathers its rows from
   // x (or its fp16 copy) with TMA tile::gather4 loads (slower on GB300: 32
   // four-row requests per 16 KB A tile).
-  const bool gather = g_gather_a && cfg->act_dtype != MOE_F32;
+  const bool gather = g_gather_a && cfg->act_dtype != MOE_F32 && !is_nk(cfg);
   st = do_permute(cfg, ids, gather ? nullptr : x_rows, counts, offsets, sorted_rows, dest,
                   gather ? nullptr : x_perm, seg, err, s, tok_inv, row_inv);
   if (st != MOE_OK) return fail(st);
@@ -537,6 +560,15 @@ int moe_layer(const moe_config_t* cfg, const void* x, const void* Wg, const floa
   trace_mark(s);
   g_trace_next = -1;
   return st;
+}
+
+int moe_pack_weights_nk(const void* W, int64_t G, int32_t K, int32_t N, void* W_nk, void* stream) {
+  if (!W || !W_nk || !aligned16(W) || !aligned16(W_nk)) return MOE_ERR_INVALID_ARG;
+  if (G < 1 || G > (1ll << 16) - 1 || K < 16 || N < 16 || K % 16 || N % 16) return MOE_ERR_INVALID_ARG;
+  const uintptr_t a = reinterpret_cast<uintptr_t>(W), b = reinterpret_cast<uintptr_t>(W_nk);
+  const uintptr_t bytes = static_cast<uintptr_t>(G) * static_cast<uintptr_t>(K) * static_cast<uintptr_t>(N);
+  if (a < b + bytes && b < a + bytes) return MOE_ERR_INVALID_ARG;  // overlap
+  return cuda_status(launch_transpose_bytes(W, G, K, N, W_nk, static_cast<cudaStream_t>(stream)));
 }
 
 int moe_read_device_status(void* ws, void* stream, int32_t* flags) {
@@ -606,15 +638,15 @@ int moe_layer_launch_count(const moe_config_t* cfg) {
   int n = 0;
   n += 1;  // router projection
   n += 1;  // top-k softmax
-  if (cfg->w_dtype == MOE_FP8_E4M3) {
-    n += 1;                          // x to fp16 rows (fp16 tensor-core path)
-    n += cfg->I_shared > 0 ? 2 : 1;  // h to fp16 rows, routed (and shared)
+  if (is_fp8(cfg)) {
+    n += 1;                          // x to fp16 (or two-term e4m3) rows
+    n += cfg->I_shared > 0 ? 2 : 1;  // h to fp16 (or two-term e4m3) rows, routed (and shared)
   }
   if (small_route(static_cast<long long>(cfg->T) * cfg->k, cfg->E)) {
     n += 1;  // init_routing + permutation gather in one kernel
   } else {
     n += 2;  // histogram, scan + stable scatter
-    if (cfg->act_dtype == MOE_F32 || !g_gather_a) n += 1;  // permutation gather
+    if (cfg->act_dtype == MOE_F32 || !g_gather_a || is_nk(cfg)) n += 1;  // permutation gather
   }
   n += 2;  // routed gate/up, down
   if (cfg->I_shared > 0) n += 2;  // shared gate/up, down

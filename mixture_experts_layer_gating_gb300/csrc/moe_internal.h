@@ -102,6 +102,14 @@ cudaError_t launch_permute_gather(const void* x, const int32_t* sorted_rows, int
 // (max |row| < 2^14); inv_scale[r] = the inverse power of two.
 cudaError_t launch_rows_to_fp16(const void* x, int rows, int D, void* x16, float* inv_scale,
                                 cudaStream_t s, bool src_f32 = false);
+// bf16 (or fp32 when src_f32) rows -> two-term e4m3 rows [rows, 2D] (hi
+// bytes, then lo bytes) times an exact power of two putting the row's largest
+// |element| in [128, 256); inv_scale[r] = the inverse power of two.
+cudaError_t launch_rows_to_e4m3x2(const void* x, int rows, int D, void* q, float* inv_scale,
+                                  cudaStream_t s, bool src_f32 = false);
+// W_nk[g][n][c] = W[g][c][n], one-byte elements (K, N multiples of 16).
+cudaError_t launch_transpose_bytes(const void* W, long long G, int K, int N, void* W_nk,
+                                   cudaStream_t s);
 // y_perm and s_rows are fp32; out is act_dtype.
 cudaError_t launch_finalize(int act_dtype, const void* y_perm, const int32_t* dest, const float* w,
                             const void* s_rows, void* out, int T, int k, int D, int R,
@@ -143,6 +151,9 @@ struct GroupedGemmArgs {
   int gather_k;
   int a_rows;                    // rows of A when gathering
   int a_fp16;                    // 1: A is fp16 (fp8 layers), B e4m3 expanded to fp16
+  int a_e4m3x2;                  // 1: A rows are two-term e4m3 [M, 2K] (hi | lo) and B is
+                                 //    e4m3 stored [G, N, K] (gate/up: [G, 2N, K]):
+                                 //    the 8-bit tensor-core kind, no expansion
   int h_fp32;                    // gate/up pass: store h as fp32 (no lo plane)
   int ksplit;                    // >1: K split into planes out[s] = partial sums (fp32 store only)
   int pair_ok;                   // 1: 2-CTA (M=256) tiles may be used

@@ -527,6 +527,108 @@ __global__ void rows_to_fp16_kernel(const Tin* __restrict__ x, int rows, int D,
   }
 }
 
+// Two e4m3 values (lo -> low byte) from two floats, round to nearest even,
+// saturating to +-448.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// The two e4m3 values of the low 16 bits of w as floats (exact).
+__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t w) {
+  uint32_t h;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, lo;\n\t}"
+      : "=r"(h)
+      : "r"(w));
+  return __half22float2(*reinterpret_cast<const __half2*>(&h));
+}
+
+// Rows as two e4m3 terms for the 8-bit tensor-core path: per row a power of
+// two 2^e puts the largest |element| in [128, 256); v = x * 2^e, hi =
+// e4m3(v), lo = e4m3(v - hi) (v - hi is exact in fp32), so hi + lo = v for
+// every bf16 element of magnitude at least 2^-9 of the row's largest, and
+// within 2^-10 (scaled units) below that; fp32 sources keep 8 significant
+// bits.  Output row r: bytes [0, D) hi, [D, 2D) lo; inv_scale[r] = 2^-e.
+template <typename Tin>
+__global__ void rows_to_e4m3x2_kernel(const Tin* __restrict__ x, int rows, int D,
+                                      uint8_t* __restrict__ q, float* __restrict__ inv_scale) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int lane = threadIdx.x & 31;
+  const long long wstride = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+  const int nvec = D / 8;
+  for (long long r = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       r < rows; r += wstride) {
+    const Tin* src = x + r * D;
+    float m = 0.0f;
+    for (int v = lane; v < nvec; v += 32) {
+      float f[8];
+      load8f(src, v, f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(f[i]));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(FULL, m, off));
+    int e = 0;
+    if (m > 0.0f && isfinite(m)) {
+      int ex;
+      frexpf(m, &ex);  // 2^(ex-1) <= m < 2^ex
+      e = min(100, max(-100, 8 - ex));
+    }
+    const float sc = exp2_int(e);
+    if (lane == 0) inv_scale[r] = exp2_int(-e);
+    uint8_t* hi_row = q + r * 2 * D;
+    uint8_t* lo_row = hi_row + D;
+    for (int v = lane; v < nvec; v += 32) {
+      float f[8];
+      load8f(src, v, f);
+      uint32_t hw[2] = {0u, 0u}, lw[2] = {0u, 0u};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float a = f[2 * i] * sc, b = f[2 * i + 1] * sc;
+        const uint32_t h = f32x2_to_e4m3x2(a, b);
+        const float2 hv = e4m3x2_to_f32x2(h);
+        const uint32_t l = f32x2_to_e4m3x2(a - hv.x, b - hv.y);
+        hw[i >> 1] |= h << (16 * (i & 1));
+        lw[i >> 1] |= l << (16 * (i & 1));
+      }
+      *reinterpret_cast<uint2*>(hi_row + 8 * v) = make_uint2(hw[0], hw[1]);
+      *reinterpret_cast<uint2*>(lo_row + 8 * v) = make_uint2(lw[0], lw[1]);
+    }
+  }
+}
+
+// W_nk[g][n][c] = W[g][c][n] for one-byte elements: 64 x 64 tiles through
+// shared memory, 16-byte loads and stores (K and N multiples of 16).
+__global__ void transpose_bytes_kernel(const uint8_t* __restrict__ W, int K, int N,
+                                       uint8_t* __restrict__ W_nk) {
+  pdl_wait();
+  pdl_launch_dependents();
+  __shared__ uint8_t tile[64][64 + 16];
+  const size_t g = blockIdx.z;
+  const int c0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
+  const int t = threadIdx.x;  // 256 threads: 64 rows x 4 chunks of 16 bytes
+  const int r = t >> 2, ch = (t & 3) * 16;
+  const uint8_t* src = W + g * K * static_cast<size_t>(N);
+  if (c0 + r < K && n0 + ch < N)
+    *reinterpret_cast<uint4*>(&tile[r][ch]) =
+        *reinterpret_cast<const uint4*>(src + static_cast<size_t>(c0 + r) * N + n0 + ch);
+  __syncthreads();
+  uint8_t* dst = W_nk + g * K * static_cast<size_t>(N);
+  if (n0 + r < N && c0 + ch < K) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      w[i] = static_cast<uint32_t>(tile[ch + 4 * i][r]) |
+             (static_cast<uint32_t>(tile[ch + 4 * i + 1][r]) << 8) |
+             (static_cast<uint32_t>(tile[ch + 4 * i + 2][r]) << 16) |
+             (static_cast<uint32_t>(tile[ch + 4 * i + 3][r]) << 24);
+    *reinterpret_cast<uint4*>(dst + static_cast<size_t>(n0 + r) * K + c0 + ch) =
+        make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
 // ------------------------------------------------------------------------
 // finalize_routing ("CANN/cann-recipes-infer：Qwen3-MoE优化", section
 // "GMM使能和Routing优化") fused with the shared-expert add ("千问 3.5 MoE 在
@@ -747,6 +849,29 @@ cudaError_t launch_rows_to_fp16(const void* x, int rows, int D, void* x16, float
   else
     MOE_LAUNCH(rows_to_fp16_kernel<__nv_bfloat16>, blocks, threads, 0, s,
                static_cast<const __nv_bfloat16*>(x), rows, D, static_cast<__half*>(x16), inv_scale);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rows_to_e4m3x2(const void* x, int rows, int D, void* q, float* inv_scale,
+                                  cudaStream_t s, bool src_f32) {
+  if (rows <= 0) return cudaSuccess;
+  const int threads = 256;
+  const int blocks = blocks_for(rows, threads / 32, device_sm_count() * 16);
+  if (src_f32)
+    MOE_LAUNCH(rows_to_e4m3x2_kernel<float>, blocks, threads, 0, s, static_cast<const float*>(x),
+               rows, D, static_cast<uint8_t*>(q), inv_scale);
+  else
+    MOE_LAUNCH(rows_to_e4m3x2_kernel<__nv_bfloat16>, blocks, threads, 0, s,
+               static_cast<const __nv_bfloat16*>(x), rows, D, static_cast<uint8_t*>(q), inv_scale);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_transpose_bytes(const void* W, long long G, int K, int N, void* W_nk,
+                                   cudaStream_t s) {
+  if (G <= 0) return cudaSuccess;
+  const dim3 grid((N + 63) / 64, (K + 63) / 64, static_cast<unsigned>(G));
+  MOE_LAUNCH(transpose_bytes_kernel, grid, 256, 0, s, static_cast<const uint8_t*>(W), K, N,
+             static_cast<uint8_t*>(W_nk));
   return cudaGetLastError();
 }
 

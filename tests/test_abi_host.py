@@ -137,3 +137,32 @@ def test_set_option_values():
     for opt, value, stored in cases:
         old = moe.moe_set_option(opt, value)
         assert moe.moe_set_option(opt, old) == stored
+
+
+def test_fp8_nk_layout_host_logic(lib):
+    """MOE_FP8_E4M3_NK: accepted with bf16 activations, the same workspace and
+    launch count as the [.., K, N] fp8 layout (two-term e4m3 rows take the
+    fp16 rows' bytes), rejected with fp32 activations or widths not a
+    multiple of 16; moe_pack_weights_nk validates before enqueueing anything."""
+    for name in ("ling_prefill", "ling_decode"):
+        shape = workloads.CONFIGS[name]
+        kn, nk = moe.config_from_shape(shape), moe.config_from_shape(shape, "nk")
+        assert nk.w_dtype == moe.MOE_FP8_E4M3_NK
+        assert moe.moe_workspace_size(nk) == moe.moe_workspace_size(kn) > 0
+        assert moe.moe_layer_launch_count(nk) == moe.moe_layer_launch_count(kn)
+        for i in range(len(moe.WS_SLOTS)):
+            assert moe.moe_workspace_offset(nk, i) == moe.moe_workspace_offset(kn, i)
+    assert moe.moe_workspace_size(moe.make_config(64, 264, 8, 2, 128, w_dtype="fp8_e4m3_nk")) == 0
+    good = 1 << 20
+    cfg32 = moe.make_config(64, 256, 8, 2, 128, act_dtype="f32", w_dtype="fp8_e4m3_nk")
+    ptrs = [good] * 12
+    assert _call_layer(lib, cfg32, ptrs, good, moe.moe_workspace_size(cfg32)) == -2
+    with pytest.raises(ValueError):
+        moe.config_from_shape(workloads.CONFIGS["ling_decode"], "mn")
+    P = lib.moe_pack_weights_nk
+    assert P(good, 1, 40, 64, good * 8, None) == -1          # K not a multiple of 16
+    assert P(good, 1, 64, 24, good * 8, None) == -1          # N not a multiple of 16
+    assert P(good, 0, 64, 64, good * 8, None) == -1          # no matrices
+    assert P(good + 8, 1, 64, 64, good * 8, None) == -1      # misaligned source
+    assert P(None, 1, 64, 64, good * 8, None) == -1          # null source
+    assert P(good, 2, 64, 64, good + 4096, None) == -1       # overlapping buffers

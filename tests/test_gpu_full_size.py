@@ -1,5 +1,6 @@
 """Every configured workload at its full size, in the configuration bench.py
-times (default kernel options), through the C ABI.
+times (default kernel options; fp8 workloads in both weight layouts),
+through the C ABI.
 
 The oracle cannot run a whole full-size layer in test time, so each case
 checks (1) what holds at any size for every token -- top-k ids bit-exact
@@ -27,6 +28,9 @@ pytestmark = pytest.mark.gpu
 # copies of the weights are large (Ling: 268 MB per expert for W13)
 SAMPLE = {"ling_prefill": 6, "ling_decode": 6, "qwen35_prefill": 16}
 WORKLOADS = sorted(n for n in workloads.CONFIGS if n not in ("toy", "qwen3_prefill"))
+# fp8 workloads run in both weight layouts (bench.py times the K-contiguous one)
+CASES = [(n, "kn") for n in WORKLOADS] + [(n, "nk") for n in WORKLOADS
+                                          if workloads.CONFIGS[n].w_dtype == "fp8_e4m3"]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -35,16 +39,20 @@ def lib():
     return ensure_library()
 
 
-@pytest.mark.parametrize("name", WORKLOADS)
-def test_full_size_workload(name):
+@pytest.mark.parametrize("name,layout", CASES)
+def test_full_size_workload(name, layout):
     shape = workloads.CONFIGS[name]
     T, E, k, R = shape.T, shape.E, shape.k, shape.R
     inp = workloads.make_inputs(shape, seed=11, device="cuda")
-    cfg = moe.config_from_shape(shape)
+    cfg = moe.config_from_shape(shape, layout)
     ws = moe.alloc_workspace(cfg)
     out = torch.empty((T, shape.D), dtype=workloads.torch_dtype(shape.act_dtype), device="cuda")
-    moe.moe_layer(cfg, inp["x"], inp["Wg"], inp["logit_bias"], inp["W13"], inp["s13"], inp["W2"],
-                  inp["s2"], inp["W13s"], inp["s13s"], inp["W2s"], inp["s2s"], out, ws)
+    W = {n: inp[n] for n in ("W13", "W2", "W13s", "W2s")}
+    if layout == "nk":
+        W = {n: (None if v is None else moe.pack_weights_nk(v)) for n, v in W.items()}
+    moe.moe_layer(cfg, inp["x"], inp["Wg"], inp["logit_bias"], W["W13"], inp["s13"], W["W2"],
+                  inp["s2"], W["W13s"], inp["s13s"], W["W2s"], inp["s2s"], out, ws)
+    del W
     assert moe.moe_read_device_status(ws) == 0
 
     view = lambda slot, shp, dt: moe.workspace_view(ws, cfg, slot, shp, dt).cpu()  # noqa: E731

@@ -31,12 +31,22 @@ def _cpu(d):
     return {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
 
 
-def run_layer(shape, inp):
-    cfg = moe.config_from_shape(shape)
+def packed_weights(inp, layout):
+    """The layer's weight tensors in the layout the configuration names: as
+    drawn ("kn"), or fp8 weights transposed once by moe_pack_weights_nk ("nk")."""
+    names = ("W13", "W2", "W13s", "W2s")
+    if layout == "kn":
+        return {n: inp[n] for n in names}
+    return {n: (None if inp[n] is None else moe.pack_weights_nk(inp[n])) for n in names}
+
+
+def run_layer(shape, inp, layout="kn"):
+    cfg = moe.config_from_shape(shape, layout)
     ws = moe.alloc_workspace(cfg)
     out = torch.empty((shape.T, shape.D), dtype=workloads.torch_dtype(shape.act_dtype), device="cuda")
-    moe.moe_layer(cfg, inp["x"], inp["Wg"], inp["logit_bias"], inp["W13"], inp["s13"], inp["W2"],
-                  inp["s2"], inp["W13s"], inp["s13s"], inp["W2s"], inp["s2s"], out, ws)
+    W = packed_weights(inp, layout)
+    moe.moe_layer(cfg, inp["x"], inp["Wg"], inp["logit_bias"], W["W13"], inp["s13"], W["W2"],
+                  inp["s2"], W["W13s"], inp["s13s"], W["W2s"], inp["s2s"], out, ws)
     flags = moe.moe_read_device_status(ws)
     assert flags == 0, f"device error flags {flags:#x}"
     R = shape.R
@@ -54,14 +64,34 @@ def run_layer(shape, inp):
         "x_perm": view("x_perm", (R, shape.D), adt),
     }
     if shape.w_dtype == "fp8_e4m3":
-        res["x16"] = view("x16", (shape.T, shape.D), torch.float16)
+        # fp16 rows, or two-term e4m3 rows (hi bytes, then lo bytes)
+        res["x16"] = (view("x16", (shape.T, shape.D), torch.float16) if layout == "kn"
+                      else view("x16", (shape.T, 2 * shape.D), torch.uint8))
         res["tok_inv"] = view("tok_inv", (shape.T,), torch.float32)
     return res
 
 
-def check_layer(shape, seed=0):
+def check_two_term_rows(q, inv, x):
+    """Two-term e4m3 rows [n, 2D] (hi bytes, then lo) with inverse power-of-two
+    scales reproduce x exactly where |x| >= 2^-9 of the row's largest |x|, and
+    within 2^-17 of it elsewhere; the scaled largest lies in [128, 256)."""
+    D = x.shape[1]
+    hi = q[:, :D].contiguous().view(torch.float8_e4m3fn).double()
+    lo = q[:, D:].contiguous().view(torch.float8_e4m3fn).double()
+    inv = inv.double()[:, None]
+    xd = x.double()
+    amax = xd.abs().amax(dim=1, keepdim=True)
+    live = amax[:, 0] > 0
+    assert torch.all((amax / inv)[live] >= 128) and torch.all((amax / inv)[live] < 256)
+    rec = (hi + lo) * inv
+    big = xd.abs() >= amax * 2.0 ** -9
+    assert torch.equal(rec[big], xd[big]), "two-term e4m3 rows must carry x exactly"
+    assert torch.all((rec - xd).abs() <= amax * 2.0 ** -17)
+
+
+def check_layer(shape, seed=0, layout="kn"):
     inp = workloads.make_inputs(shape, seed=seed, device="cuda")
-    g = run_layer(shape, inp)
+    g = run_layer(shape, inp, layout)
     cinp = _cpu(inp)
     k, E = shape.k, shape.E
 
@@ -82,10 +112,12 @@ def check_layer(shape, seed=0):
         xs = cinp["x"][torch.from_numpy(r["sorted_rows"] // k)]
         if shape.w_dtype == "fp8_e4m3":
             xs = g["x16"][torch.from_numpy(r["sorted_rows"] // k)]
-            assert torch.equal(g["x_perm"].view(torch.float16), xs)
+            assert torch.equal(g["x_perm"].view(xs.dtype).reshape(xs.shape), xs)
         else:
             assert torch.equal(g["x_perm"], xs), "permutation gather must copy rows bit-exactly"
-    if shape.w_dtype == "fp8_e4m3":
+    if shape.w_dtype == "fp8_e4m3" and layout == "nk":
+        check_two_term_rows(g["x16"], g["tok_inv"], cinp["x"])
+    elif shape.w_dtype == "fp8_e4m3":
         # fp16 rows times exact powers of two: scaling back gives x bit-exactly
         x16 = g["x16"].float()
         inv = g["tok_inv"].float()[:, None]
