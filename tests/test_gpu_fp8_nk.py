@@ -90,6 +90,42 @@ def test_grouped_ffn_nk_parity(E, counts, D, I, act, tile_mode):
     check_close("y vs oracle", y.cpu().double().numpy(), y_o, 2.0 ** -7, 2e-2)
 
 
+@pytest.mark.parametrize("act", ["swiglu", "geglu_tanh"])
+@pytest.mark.parametrize("pair_mode", [0, 1])
+def test_grouped_ffn_nk_tail_sizes(act, pair_mode):
+    """Every kind of last tile of a group on 128-row tiles (mode 0) and on
+    2-CTA 256-row tiles (mode 1): 1 row, multiples of 16 and their
+    neighbours, exact multiples of the tile height.  The down pass has 320
+    output columns: a full 256-row weight tile and one with 64 rows of
+    weights (the rest of the box zero-filled)."""
+    counts = [1, 15, 16, 17, 31, 32, 33, 63, 64, 65, 80, 95, 96, 97, 112, 127, 128, 129, 200, 224,
+              225, 256, 300]
+    E, D, I = len(counts), 320, 256
+    old = moe.moe_set_option(moe.MOE_OPT_PAIR_TILES, pair_mode)
+    try:
+        xp, offsets, W13, W2, s13, s2 = _grouped_case(E, counts, D, I, act, seed=pair_mode + 3 * len(act), fp8=True)
+        R = xp.shape[0]
+        cfg = moe.make_config(R, D, E, 1, I, act=act, w_dtype="fp8_e4m3_nk")
+        ws = moe.alloc_workspace(cfg)
+        h = torch.empty((R, I), dtype=torch.float32, device="cuda")
+        y = torch.empty((R, D), dtype=torch.float32, device="cuda")
+        moe.moe_grouped_ffn(cfg, xp, torch.from_numpy(offsets).cuda(), moe.pack_weights_nk(W13), s13,
+                            moe.pack_weights_nk(W2), s2, h, y, ws=ws)
+        assert moe.moe_read_device_status(ws) == 0
+        h_o, _ = oracle.grouped_ffn(oracle.to_f64(xp.cpu()), offsets, W13.cpu(), W2.cpu(), act,
+                                    s13.cpu(), s2.cpu())
+        check_close("h", h.cpu().double().numpy(), h_o, 1e-4, 1e-4)
+        hq = two_term_rows(h.cpu()).numpy()
+        y_ref = np.zeros((R, D))
+        for e in range(E):
+            a, b = offsets[e], offsets[e + 1]
+            y_ref[a:b] = oracle.scaled_projection(hq[a:b], oracle.to_f64(W2[e].cpu()),
+                                                  oracle.to_f64(s2[e].cpu()))
+        check_close("y", y.cpu().double().numpy(), y_ref, 1e-5, 1e-5)
+    finally:
+        moe.moe_set_option(moe.MOE_OPT_PAIR_TILES, old)
+
+
 def test_nk_weights_with_subnormal_codes(tile_mode):
     """Weight codes mostly from the e4m3 subnormal range go to the tensor core
     unchanged: y against the GPU's h (two-term rounding emulated) times the
