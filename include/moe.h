@@ -286,9 +286,9 @@ int moe_layer_launch_count(const moe_config_t* cfg);
  *   rows as N): 3 (default) = when there are at least 150 rows per group on
  *   average; 1 = always; 2 = always, without swapped tails; 0 = never (one
  *   CTA per 128-row tile).  FP8_E4M3 GEMMs always use one CTA per tile;
- *   FP8_E4M3_NK GEMMs use 2-CTA tiles without swapped tails, under policy 3
- *   only with at least 1024 rows per group on average.  Results are the
- *   same up to fp32 summation order. */
+ *   FP8_E4M3_NK GEMMs follow the same policy (their swapped tails stack the
+ *   hi and lo e4m3 rows along N).  Results are the same up to fp32
+ *   summation order. */
 #define MOE_OPT_PAIR_TILES 1
 /*   MOE_OPT_GATHER_A: 1 = moe_layer does not materialise the permuted rows;
  *   the routed gate/up GEMM gathers its A rows from x with TMA tile::gather4

@@ -361,12 +361,16 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
   // swapped tail tile (2-CTA mode): its rows padded so that the MMA N (rows,
   // or 2 x rows in the down pass) is a multiple of 32 and each CTA's half of
   // the rows a multiple of 8
+  // Two-term e4m3 rows stack their hi rows (CTA 0) and lo rows (CTA 1) along
+  // N in both passes, N = 2 x rows rounded up to 16.
   auto is_swap = [&](const TileInfo& ti) {
-    return PAIR && !Q8 && p.swap_tail > 0 && ti.rows <= p.swap_tail;
+    return PAIR && p.swap_tail > 0 && ti.rows <= p.swap_tail;
   };
   auto swap_rows = [&](const TileInfo& ti) {
-    return EPI == kEpiGateUpAct ? (ti.rows + 31) & ~31 : (ti.rows + 15) & ~15;
+    return (EPI == kEpiGateUpAct && !Q8) ? (ti.rows + 31) & ~31 : (ti.rows + 15) & ~15;
   };
+  // rows each CTA of the pair loads for a swapped tail, from row swap_row0 on
+  constexpr bool kSplitRowsAcrossPair = EPI == kEpiGateUpAct && !Q8;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -404,11 +408,11 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
         // pass: rows r * R/2 .. of the tile; the down pass: CTA 0 the h_hi rows,
         // CTA 1 the h_lo rows) and its 128 weight features
         const int swap_boxes =
-            swap ? ((EPI == kEpiGateUpAct ? swap_rows(ti) / 2 : swap_rows(ti)) + 31) / 32 : 0;
+            swap ? ((kSplitRowsAcrossPair ? swap_rows(ti) / 2 : swap_rows(ti)) + 31) / 32 : 0;
         const uint32_t tile_tx =
             swap ? 2u * (static_cast<uint32_t>(swap_boxes) * 32u * 128u + 2u * B_BOX_BYTES) : tx;
         const int swap_row0 =
-            ti.row0 + (EPI == kEpiGateUpAct ? static_cast<int>(rank) * (swap_rows(ti) / 2) : 0);
+            ti.row0 + (kSplitRowsAcrossPair ? static_cast<int>(rank) * (swap_rows(ti) / 2) : 0);
         for (int kb = kb0; kb < kb1; ++kb) {
           if (lane == 0) ok = mbar_wait(&ctrl->empty[stage], phase ^ 1u, abort_flag);
           ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -422,8 +426,17 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
             if (lane == 0) {
               const CUtensorMap* am = (SPLIT && rank == 1) ? &tmap_a_lo_tail : &tmap_a_tail;
               for (int i = 0; i < swap_boxes; ++i)
-                tma_load_2d_pair(a_dst + i * 32 * 128, am, fbar, kb * BK, swap_row0 + 32 * i, pol_a);
-              if (EPI == kEpiGateUpAct) {
+                tma_load_2d_pair(a_dst + i * 32 * 128, am, fbar, kb * KE, swap_row0 + 32 * i, pol_a);
+              if (Q8) {
+                // K-contiguous e4m3 weights: CTA r its 64 gate rows n0 + 64 r .. and
+                // the matching 64 up rows, or its 128 output rows n0 + 128 r ..
+                if (EPI == kEpiGateUpAct)
+                  tma_load_4d_pair(b_dst, &tmap_b_tail, fbar, kb * KE, ti.n0 + 64 * static_cast<int>(rank), 0,
+                                   ti.g, pol_b);
+                else
+                  tma_load_3d_pair(b_dst, &tmap_b, fbar, kb * KE, ti.n0 + static_cast<int>(rank) * (p.bn / 2),
+                                   ti.g, pol_b);
+              } else if (EPI == kEpiGateUpAct) {
                 // gate and up features n0 + 64 r .. + 63: one box each
                 if (p.b_wide) {
                   tma_load_5d_pair(b_dst, &tmap_b_tail, fbar, 0, kb * BK, ti.n0 / 64 + static_cast<int>(rank),
@@ -580,7 +593,8 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
         // swapped tail: A = weights (N-major boxes: MN-major operand), B = rows
         // (K-major), N = rows (gate/up) or 2 x rows (down: h_hi | h_lo)
         const uint32_t idesc_swap =
-            make_idesc_bf16_f32(TILE_M, (EPI == kEpiGateUpAct ? 1 : 2) * swap_rows(ti), 1, 0);
+            Q8 ? make_idesc_e4m3_f32(TILE_M, 2 * swap_rows(ti))
+               : make_idesc_bf16_f32(TILE_M, (EPI == kEpiGateUpAct ? 1 : 2) * swap_rows(ti), 1, 0);
         const uint32_t idesc_q8 = make_idesc_e4m3_f32(TILE_M, p.bn);
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&ctrl->full[stage], phase, abort_flag)) {
@@ -588,6 +602,22 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
             break;
           }
           tc_fence_after_sync();
+          if (PAIR && swap && Q8) {
+            // weights (K-major, 128 rows per CTA) as the M = 256 operand; the
+            // hi rows (CTA 0) and lo rows (CTA 1) as N
+            const uint64_t wdesc0 = make_smem_desc_sw128(smem_u32(stage_b(stage)), 16, 1024);
+            const uint64_t rdesc0 = make_smem_desc_sw128(smem_u32(stage_a(stage)), 16, 1024);
+#pragma unroll
+            for (int kk = 0; kk < KE / 32; ++kk)
+              tc_mma_f8_pair(d_tmem, smem_desc_advance(wdesc0, kk * 32), smem_desc_advance(rdesc0, kk * 32),
+                             idesc_swap, ((kb - kb0) | kk) != 0);
+            tc_commit_pair_multicast(&ctrl->empty[stage], 0x3);
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            continue;
+          }
           if (PAIR && swap) {
             const uint64_t wdesc0 = make_smem_desc_sw128(smem_u32(stage_b(stage)), B_BOX_BYTES, 1024);
             const uint64_t rdesc0 = make_smem_desc_sw128(smem_u32(stage_a(stage)), 16, 1024);
@@ -761,6 +791,20 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
         if (is_swap(tw)) {
           const int R = swap_rows(tw);  // accumulator columns per plane
           bool ok = true;
+          // two-term e4m3 rows: columns [0, R) hold the hi products of rows
+          // 0..R-1, [R, 2R) their lo products
+          auto load_cols = [&](int c, uint32_t (&v)[32]) {
+            tmem_ld_32x32b_x32(taddr + c, v);
+            if (Q8) {
+              uint32_t lo[32];
+              tmem_ld_32x32b_x32(taddr + R + c, lo);
+              tc_wait_ld();
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(lo[j]));
+            } else {
+              tc_wait_ld();
+            }
+          };
           if (EPI == kEpiGateUpAct) {
             // lanes 0..63: gate features, 64..127: the matching up features of
             // output columns n0 + 64 r + (0..63); up values pass through shared memory
@@ -774,8 +818,7 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
 #pragma unroll 1
                 for (int c = 0; c < R; c += 32) {
                   uint32_t v[32];
-                  tmem_ld_32x32b_x32(taddr + c, v);
-                  tc_wait_ld();
+                  load_cols(c, v);
 #pragma unroll
                   for (int j = 0; j < 32; ++j)
                     if (c + j < R) up[(c + j) * 64 + (fl - 64)] = __uint_as_float(v[j]);
@@ -786,18 +829,21 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
               ok = mbar_wait(&ctrl->xch_full, xch_phase, abort_flag);
               __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
               __nv_bfloat16* out_lo = reinterpret_cast<__nv_bfloat16*>(p.out_lo);
+              const float* sg = p.b_scale ? p.b_scale + static_cast<size_t>(ti.g) * 2 * p.N : nullptr;
+              const float gs = (sg && f < p.N) ? sg[f] : 1.0f;
+              const float us = (sg && f < p.N) ? sg[p.N + f] : 1.0f;
 #pragma unroll 1
               for (int c = 0; c < R && ok; c += 32) {
                 uint32_t v[32];
-                tmem_ld_32x32b_x32(taddr + c, v);
-                tc_wait_ld();
+                load_cols(c, v);
                 if (f < p.N) {
 #pragma unroll 4
                   for (int j = 0; j < 32; ++j) {
                     if (c + j >= tw.rows) break;
                     const size_t row = static_cast<size_t>(tw.row0 + c + j);
-                    const float g = __uint_as_float(v[j]);
-                    const float u = up[(c + j) * 64 + fl];
+                    const float rs = p.a_row_scale ? p.a_row_scale[row] : 1.0f;
+                    const float g = __uint_as_float(v[j]) * rs * gs;
+                    const float u = up[(c + j) * 64 + fl] * rs * us;
                     const float hf = ((p.act == MOE_ACT_SWIGLU) ? silu_f(g) : gelu_tanh_f(g)) * u;
                     if (p.h_fp32) {
                       reinterpret_cast<float*>(p.out)[row * p.N + f] = hf;
@@ -813,10 +859,12 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
             }
             xch_phase ^= 1u;
           } else {
-            // lanes = output features n0 + 128 r + (0..127); columns j (h_hi rows)
-            // and R + j (h_lo rows) add up to row j's result
+            // lanes = output features n0 + 128 r + (0..127); columns j (h_hi rows,
+            // or hi e4m3 terms) and R + j (h_lo rows, lo terms) add up to row j's result
             const int f = ti.n0 + 128 * static_cast<int>(rank) + quarter * 32 + lane;
             float* out = reinterpret_cast<float*>(p.out) + plane;
+            const float cs =
+                (p.b_scale && f < p.N) ? p.b_scale[static_cast<size_t>(ti.g) * p.N + f] : 1.0f;
 #pragma unroll 1
             for (int c = 0; c < R; c += 32) {
               uint32_t hi[32], lo[32];
@@ -827,8 +875,9 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
 #pragma unroll 4
                 for (int j = 0; j < 32; ++j) {
                   if (c + j >= tw.rows) break;
-                  out[static_cast<size_t>(tw.row0 + c + j) * p.N + f] =
-                      __uint_as_float(hi[j]) + __uint_as_float(lo[j]);
+                  const size_t row = static_cast<size_t>(tw.row0 + c + j);
+                  const float rs = p.a_row_scale ? p.a_row_scale[row] : 1.0f;
+                  out[row * p.N + f] = (__uint_as_float(hi[j]) + __uint_as_float(lo[j])) * rs * cs;
                 }
               }
             }
@@ -1656,48 +1705,53 @@ cudaError_t launch_grouped_gemm_q8(const GroupedGemmArgs& a, cudaStream_t s) {
     kp.cols_per_tile = kp.bn;
   }
   kp.n_tiles = (a.N + kp.cols_per_tile - 1) / kp.cols_per_tile;
-  // 2-CTA tiles here have no swapped tails, so a group's last 256-row tile is
-  // often mostly empty: by default (policy 3) they run only with >= 1024 rows
-  // per group on average (the shared expert at prefill: 5-9 % faster), where
-  // that waste is small; Ling-style routed passes (~512 rows per group)
-  // measured 7 % slower on them than on 128-row tiles.
+  // Policy as for bf16 (3: 2-CTA tiles with swapped tails from 150 rows per
+  // group on average).  Ling-style prefill (~512 rows per group), layer time:
+  // 12.0-12.1 ms on 2-CTA tiles with swapped tails, 12.4 ms on 128-row tiles,
+  // 12.65 ms on 2-CTA tiles without swapped tails.
   const bool pair_policy =
       g_pair_tiles == 1 || g_pair_tiles == 2 ||
-      (g_pair_tiles == 3 && static_cast<long long>(a.M) >= 1024ll * a.G);
+      (g_pair_tiles == 3 && static_cast<long long>(a.M) >= 150ll * a.G);
   const bool pair = a.pair_ok && kp.bn == 256 && pair_policy;
-  CUtensorMap ta, ta_lo, tb;
+  // 2-CTA tiles: a group's last tile with at most 64 (gate/up) or 128 (down)
+  // rows runs swapped (weights as the M = 256 operand, hi and lo rows as N)
+  kp.swap_tail = (pair && g_pair_tiles != 2) ? (a.epilogue == kEpiGateUpAct ? 64 : 128) : 0;
+  CUtensorMap ta, ta_lo, tb, ta_tail, ta_lo_tail, tb_tail;
   {
     const uint64_t dims[2] = {K, M};
     const uint64_t strides[1] = {2 * K};
     const uint32_t box[2] = {128, BM};
+    const uint8_t* lo = static_cast<const uint8_t*>(a.A) + K;
     if (!encode_tmap(&ta, a.A, 2, dims, strides, box, u8)) return cudaErrorInvalidValue;
-    if (!encode_tmap(&ta_lo, static_cast<const uint8_t*>(a.A) + K, 2, dims, strides, box, u8))
-      return cudaErrorInvalidValue;
+    if (!encode_tmap(&ta_lo, lo, 2, dims, strides, box, u8)) return cudaErrorInvalidValue;
+    const uint32_t tbox[2] = {128, 32};  // swapped tails: 32-row boxes
+    if (!encode_tmap(&ta_tail, a.A, 2, dims, strides, tbox, u8)) return cudaErrorInvalidValue;
+    if (!encode_tmap(&ta_lo_tail, lo, 2, dims, strides, tbox, u8)) return cudaErrorInvalidValue;
   }
   if (a.epilogue == kEpiGateUpAct) {  // [G][2][N][K]: gate rows, then up rows
     const uint64_t dims[4] = {K, N, 2, G};
     const uint64_t strides[3] = {K, N * K, 2 * N * K};
     const uint32_t box[4] = {128, 128, pair ? 1u : 2u, 1};
     if (!encode_tmap(&tb, a.B, 4, dims, strides, box, u8)) return cudaErrorInvalidValue;
+    const uint32_t tbox[4] = {128, 64, 2, 1};  // swapped tails: 64 gate + 64 up rows per CTA
+    if (!encode_tmap(&tb_tail, a.B, 4, dims, strides, tbox, u8)) return cudaErrorInvalidValue;
   } else {  // [G][N][K]
     const uint64_t dims[3] = {K, N, G};
     const uint64_t strides[2] = {K, N * K};
     const uint32_t box[3] = {128, static_cast<uint32_t>(pair ? kp.bn / 2 : kp.bn), 1};
     if (!encode_tmap(&tb, a.B, 3, dims, strides, box, u8)) return cudaErrorInvalidValue;
+    tb_tail = tb;
   }
   const int tile_m = pair ? 2 * BM : BM;
   const long long max_tiles = (static_cast<long long>((a.M + tile_m - 1) / tile_m) + a.G) *
                               static_cast<long long>(kp.n_tiles);
+#define MOE_LAUNCH_Q8(E_, P_) \
+  launch_epi<E_, true, false, P_, true>(ta, ta_lo, tb, tb_tail, ta_tail, ta_lo_tail, kp, max_tiles, s)
   if (a.epilogue == kEpiGateUpAct)
-    return pair ? launch_epi<kEpiGateUpAct, true, false, true, true>(ta, ta_lo, tb, tb, ta, ta_lo, kp,
-                                                                     max_tiles, s)
-                : launch_epi<kEpiGateUpAct, true, false, false, true>(ta, ta_lo, tb, tb, ta, ta_lo,
-                                                                      kp, max_tiles, s);
+    return pair ? MOE_LAUNCH_Q8(kEpiGateUpAct, true) : MOE_LAUNCH_Q8(kEpiGateUpAct, false);
   if (a.epilogue == kEpiStoreF32)
-    return pair ? launch_epi<kEpiStoreF32, true, false, true, true>(ta, ta_lo, tb, tb, ta, ta_lo, kp,
-                                                                    max_tiles, s)
-                : launch_epi<kEpiStoreF32, true, false, false, true>(ta, ta_lo, tb, tb, ta, ta_lo, kp,
-                                                                     max_tiles, s);
+    return pair ? MOE_LAUNCH_Q8(kEpiStoreF32, true) : MOE_LAUNCH_Q8(kEpiStoreF32, false);
+#undef MOE_LAUNCH_Q8
   return cudaErrorInvalidValue;
 }
 
