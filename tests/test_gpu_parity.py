@@ -550,3 +550,47 @@ def test_finalize_parity(T, k, D, shared):
     got = out.cpu().double().numpy()
     # fp32 accumulation then one bf16 rounding: within one bf16 ulp of the exact sum
     assert (np.abs(got - ref) <= np.abs(ref) * 2.0 ** -8 + 1e-5).all()
+
+
+@pytest.mark.parametrize("case,layout", [("gemma4_T256", "kn"), ("qwen35_T64", "kn"), ("fp8_small_T300", "kn"),
+                                         ("fp8_small_T300", "nk"), ("fp8_small_geglu_T77", "nk")])
+def test_stage_calls_match_moe_layer(case, layout):
+    """The four stage calls in a row -- moe_route, moe_permute, moe_grouped_ffn
+    with the shared expert, moe_finalize -- give the same output as moe_layer,
+    bit for bit, and meet the layer bar against the oracle."""
+    shape = LAYER_CASES[case]
+    inp = workloads.make_inputs(shape, seed=5, device="cuda")
+    layer = run_layer(shape, inp, layout)["out"]
+    cfg = moe.config_from_shape(shape, layout)
+    ws = moe.alloc_workspace(cfg)
+    T, E, k, D, I, Is, R = shape.T, shape.E, shape.k, shape.D, shape.I, shape.I_shared, shape.R
+    adt = workloads.torch_dtype(shape.act_dtype)
+    dev = "cuda"
+    logits = torch.empty((T, E), dtype=torch.float32, device=dev)
+    ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+    w = torch.empty((T, k), dtype=torch.float32, device=dev)
+    moe.moe_route(cfg, inp["x"], inp["Wg"], inp["logit_bias"], logits, ids, w, ws)
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    sorted_rows = torch.empty(R, dtype=torch.int32, device=dev)
+    dest = torch.empty(R, dtype=torch.int32, device=dev)
+    x_perm = torch.empty((R, D), dtype=adt, device=dev)
+    moe.moe_permute(cfg, ids, inp["x"], counts, offsets, sorted_rows, dest, x_perm, ws)
+    fp8 = shape.w_dtype == "fp8_e4m3"
+    h = (torch.empty((R, I), dtype=torch.float32, device=dev) if fp8
+         else torch.empty((2, R, I), dtype=torch.bfloat16, device=dev))
+    h_s = (torch.empty((T, Is), dtype=torch.float32, device=dev) if fp8
+           else torch.empty((2, T, Is), dtype=torch.bfloat16, device=dev))
+    y = torch.empty((R, D), dtype=torch.float32, device=dev)
+    s_out = torch.empty((T, D), dtype=torch.float32, device=dev)
+    W = packed_weights(inp, layout)
+    moe.moe_grouped_ffn(cfg, x_perm, offsets, W["W13"], inp["s13"], W["W2"], inp["s2"], h, y,
+                        inp["x"], W["W13s"], inp["s13s"], W["W2s"], inp["s2s"], h_s, s_out, ws)
+    out = torch.empty((T, D), dtype=adt, device=dev)
+    moe.moe_finalize(cfg, y, dest, w, s_out, out, ws)
+    assert moe.moe_read_device_status(ws) == 0
+    assert torch.equal(out.cpu(), layer), "stage calls and moe_layer differ"
+    ref = oracle.moe_layer(_cpu(inp), k, shape.act, shape.renormalize)
+    keep = ~oracle.near_tie_tokens(ref["logits"], k)
+    err = np.abs(out.cpu().double().numpy() - ref["out"])[keep]
+    assert err.max() <= tol_factor(shape) * rms(ref["out"])
