@@ -265,8 +265,9 @@ int moe_read_device_status(void* ws, void* stream, int32_t* flags);
  *         expert's matrices).
  *   W_nk  [G, N, K] device out: W_nk[g][n][c] = W[g][c][n].  Must not
  *         overlap W.
- *   G >= 1; K and N positive multiples of 16; both pointers 16-byte
- *   aligned, else MOE_ERR_INVALID_ARG before anything is enqueued.
+ *   1 <= G <= 65535; K and N positive multiples of 16; both pointers
+ *   16-byte aligned and the two buffers disjoint, else MOE_ERR_INVALID_ARG
+ *   before anything is enqueued.
  *   Asynchronous on `stream`; needs no workspace. */
 int moe_pack_weights_nk(const void* W, int64_t G, int32_t K, int32_t N, void* W_nk, void* stream);
 

@@ -1758,7 +1758,8 @@ cudaError_t launch_grouped_gemm_q8(const GroupedGemmArgs& a, cudaStream_t s) {
 }  // namespace
 
 int router_k_split(int T, int E, int D) {
-  // aim for about 148 work items (the SM count of a GB300) without making a
+  // aim for about 148 work items (one wave on a GB300's 152 SMs; a constant, so
+  // that the workspace size depends on the shape alone) without making a
   // split shorter than 4 k-blocks; at most 8 partial planes
   const int tiles = ((T + BM - 1) / BM) * ((E + BN_MAX - 1) / BN_MAX);
   const int KB = (D + BK - 1) / BK;
