@@ -45,13 +45,25 @@ __global__ void topk_softmax_kernel(const float* __restrict__ partials, int nspl
     const int e = lane + 32 * i;
     v[i] = e < E ? partials[t * E + e] : 0.0f;
   }
-  // planes summed in order; each plane's loads are issued together
-  for (int sp = 1; sp < nsplit; ++sp) {
-    const float* pl = partials + sp * plane + t * E;
+  // planes summed in order; the loads of up to four planes are issued
+  // together (one memory round trip per four planes, not per plane)
+  for (int sp0 = 1; sp0 < nsplit; sp0 += 4) {
+    float pv[4][EPL];
 #pragma unroll
-    for (int i = 0; i < EPL; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E) v[i] += pl[e];
+    for (int q = 0; q < 4; ++q) {
+      const float* pl = partials + min(sp0 + q, nsplit - 1) * plane + t * E;
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) {
+        const int e = lane + 32 * i;
+        pv[q][i] = (sp0 + q < nsplit && e < E) ? pl[e] : 0.0f;
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (sp0 + q < nsplit) {
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) v[i] += pv[q][i];
+      }
     }
   }
   bool nonfinite = false;
