@@ -594,3 +594,26 @@ def test_stage_calls_match_moe_layer(case, layout):
     keep = ~oracle.near_tie_tokens(ref["logits"], k)
     err = np.abs(out.cpu().double().numpy() - ref["out"])[keep]
     assert err.max() <= tol_factor(shape) * rms(ref["out"])
+
+
+def test_layer_parity_max_k():
+    """k = 16 (the largest top-k the interface takes) on 32 experts."""
+    check_layer(workloads.MoEShape("maxk", 100, 256, 32, 16, 128, I_shared=64))
+
+
+def test_layer_parity_one_hot_expert():
+    """A logit bias that sends every token to expert 0 (its group holds all T
+    rows, several full tiles) while the other choices stay spread."""
+    shape = workloads.MoEShape("hot", 700, 512, 64, 4, 256)
+    inp = workloads.make_inputs(shape, seed=9, device="cuda")
+    bias = torch.zeros(shape.E, dtype=torch.float32, device="cuda")
+    bias[0] = 50.0
+    inp["logit_bias"] = bias
+    g = run_layer(shape, inp)
+    assert int(g["counts"][0]) == shape.T
+    cinp = _cpu(inp)
+    ref = oracle.moe_layer(cinp, shape.k, shape.act, shape.renormalize)
+    assert np.array_equal(ref["counts"], g["counts"].numpy()) or oracle.near_tie_tokens(ref["logits"], shape.k).any()
+    keep = ~oracle.near_tie_tokens(ref["logits"], shape.k)
+    err = np.abs(g["out"].double().numpy() - ref["out"])[keep]
+    assert err.max() <= tol_factor(shape) * rms(ref["out"])
