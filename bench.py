@@ -213,6 +213,43 @@ def cpu_baseline(shape, inp_cpu, budget_s: float = 15.0):
                       f"BLAS threads = host cores), {total:.1f} s"}
 
 
+def router_planes(T: int, E: int, D: int) -> int:
+    """Split-K planes of the router projection: the library's rule (a
+    function of the shape only), restated for the byte counts below."""
+    tiles = ((T + 127) // 128) * ((E + 255) // 256)
+    kb = (D + 63) // 64
+    ks = max(1, min(8, 148 // max(1, tiles), kb // 4))
+    kbs = (kb + ks - 1) // ks
+    return (kb + kbs - 1) // kbs
+
+
+def memory_kernel_bytes(shape, name: str, rows_form_bytes: int):
+    """Algorithmic bytes of one launch of a memory-bound kernel of the layer
+    (every tensor it must read or write, once), or None for the GEMMs.
+    rows_form_bytes: bytes per element of the GEMM A rows (2)."""
+    T, D, E, k, I, Is, R = shape.T, shape.D, shape.E, shape.k, shape.I, shape.I_shared, shape.R
+    ab = 4 if shape.act_dtype == "f32" else 2
+    S = router_planes(T, E, D)
+    bias = shape.zipf > 0
+    fp8 = shape.w_dtype == "fp8_e4m3"
+    gathered = rows_form_bytes if fp8 else ab  # bytes per element of the permuted rows
+    nseg_hist = E * 4 * max(1, (R + 1023) // 1024)
+    table = {
+        "topk_softmax": S * T * E * 4 + (E * 4 if bias else 0) + (T * E * 4 if (S > 1 or bias) else 0) + 8 * T * k,
+        "route_hist": 4 * R + nseg_hist,
+        "route_scan_scatter": 4 * R + nseg_hist + 8 * E + 8 * R,
+        "route_permute": 4 * R + T * D * gathered + R * D * gathered + 8 * R + 8 * E,
+        "permute_gather": T * D * gathered + 4 * R + R * D * gathered,
+        "finalize": R * D * 4 + 4 * R + 4 * T * k + (T * D * 4 if Is else 0) + T * D * ab,
+    }
+    for pre in ("x_to_fp16", "x_to_e4m3x2"):
+        table[pre] = T * D * ab + T * D * 2 + 4 * T
+    for pre in ("h_to_fp16", "h_to_e4m3x2"):
+        table[pre] = R * I * 4 + R * I * 2 + 4 * R
+        table["shared_" + pre] = T * Is * 4 + T * Is * 2 + 4 * T
+    return table.get(name)
+
+
 # ------------------------------------------------------------------ arms
 def workload_shape(args):
     import dataclasses
@@ -357,6 +394,15 @@ def run_ours(args, world, rank, local):
         for i in range(L):
             per[i].append(evs[i].elapsed_time(evs[i + 1]))
     kernels_us = {n: 1e3 * statistics.mean(v) for n, v in zip(names, per)}
+    # achieved HBM bandwidth of the memory-bound kernels (routing, gather,
+    # row conversions, combine): algorithmic bytes / event-timed duration
+    pk_hbm = peaks()["hbm_gbs"]
+    memory_kernels = {}
+    for n, t_us in kernels_us.items():
+        nb = memory_kernel_bytes(shape, n, 2)
+        if nb is not None and t_us > 0:
+            gbs = nb / (t_us * 1e3)
+            memory_kernels[n] = {"bytes": nb, "us": t_us, "gbs": gbs, "frac_hbm": gbs / pk_hbm}
 
     # ---- end to end through the public API with host buffers: every step
     # copies its x from pinned host memory and its out back, on copy streams,
@@ -470,6 +516,7 @@ def run_ours(args, world, rank, local):
         "layer_roofline": {"t_roofline_us": t_roof * 1e6, "t_measured_us": ms_step * 1e3,
                            "frac": t_roof / (ms_step / 1e3), "flops": layer_flops, "bytes": layer_bytes},
         "kernels_us": kernels_us,
+        "memory_kernels": memory_kernels,
         "e2e": {"value": shape.T * world / (e2e_ms / 1e3 / args.steps), "unit": "tokens/s",
                 "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
                 "d2h_bytes_per_step": out_host[0].numel() * out_host[0].element_size(),
