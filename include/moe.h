@@ -292,9 +292,11 @@ int moe_layer_launch_count(const moe_config_t* cfg);
  *   summation order. */
 #define MOE_OPT_PAIR_TILES 1
 /*   MOE_OPT_GATHER_A: 1 = moe_layer does not materialise the permuted rows;
- *   the routed gate/up GEMM gathers its A rows from x with TMA tile::gather4
- *   loads (measured slower on GB300 than the streaming gather kernel); 0
- *   (default) = gather kernel, then tiled loads.  Same results. */
+ *   the routed gate/up GEMM gathers its A rows from x (or, for fp8 weights,
+ *   from x's fp16 or two-term e4m3 rows) with TMA tile::gather4 loads, on
+ *   one-CTA tiles (measured 2.5-2.8x slower on GB300 than the streaming
+ *   gather kernel plus tiled loads); 0 (default) = gather kernel, then tiled
+ *   loads.  Same results. */
 #define MOE_OPT_GATHER_A 2
 /*   MOE_OPT_DECODE_KERNEL: 1 (default) = the swap-AB decode kernel (weights
  *   as the 128-row MMA operand, 16 or 64 rows per tile, each active expert's

@@ -463,9 +463,13 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
             }
             continue;
           }
-          if (gather)
-            tma_gather4_2d(a_dst + lane * 4 * 128, &tmap_a, &ctrl->full[stage], kb * BK, tr[0],
+          if (gather) {
+            tma_gather4_2d(a_dst + lane * 4 * 128, &tmap_a, &ctrl->full[stage], kb * KE, tr[0],
                            tr[1], tr[2], tr[3], pol_a);
+            if (Q8)  // the lo terms of the same rows
+              tma_gather4_2d(a_dst + A_TILE_BYTES + lane * 4 * 128, &tmap_a_lo, &ctrl->full[stage],
+                             kb * KE, tr[0], tr[1], tr[2], tr[3], pol_a);
+          }
           if (lane == 0) {
           if (!gather) {
             if (PAIR) {
@@ -1678,7 +1682,8 @@ cudaError_t launch_grouped_gemm_decode(const GroupedGemmArgs& a, int nt, cudaStr
 // 128-row (or 2-CTA 256-row) tiles for two-term e4m3 rows and K-contiguous
 // e4m3 weights: kind::f8f6f4, hi and lo products into one accumulator.
 cudaError_t launch_grouped_gemm_q8(const GroupedGemmArgs& a, cudaStream_t s) {
-  if (!a.b_fp8 || a.a_gather || a.A_lo || a.ksplit > 1 || a.bias) return cudaErrorInvalidValue;
+  if (!a.b_fp8 || a.A_lo || a.ksplit > 1 || a.bias) return cudaErrorInvalidValue;
+  if (a.a_gather && (a.a_rows < 1 || a.gather_k < 1)) return cudaErrorInvalidValue;
   if (a.G < 1 || a.G > MAX_G) return cudaErrorInvalidValue;
   const uint64_t K = static_cast<uint64_t>(a.K), N = static_cast<uint64_t>(a.N);
   const uint64_t M = static_cast<uint64_t>(a.M), G = static_cast<uint64_t>(a.G);
@@ -1692,6 +1697,9 @@ cudaError_t launch_grouped_gemm_q8(const GroupedGemmArgs& a, cudaStream_t s) {
   kp.out = a.out;
   kp.b_scale = a.b_scale;
   kp.a_row_scale = a.a_row_scale;
+  kp.a_gather = a.a_gather;
+  kp.gather_k = a.gather_k;
+  kp.a_rows = a.a_rows;
   kp.h_fp32 = a.h_fp32;
   kp.act = a.act;
   kp.err = a.err;
@@ -1712,7 +1720,7 @@ cudaError_t launch_grouped_gemm_q8(const GroupedGemmArgs& a, cudaStream_t s) {
   const bool pair_policy =
       g_pair_tiles == 1 || g_pair_tiles == 2 ||
       (g_pair_tiles == 3 && static_cast<long long>(a.M) >= 150ll * a.G);
-  const bool pair = a.pair_ok && kp.bn == 256 && pair_policy;
+  const bool pair = a.pair_ok && !a.a_gather && kp.bn == 256 && pair_policy;
   // 2-CTA tiles: a group's last tile with at most 64 (gate/up) or 128 (down)
   // rows runs swapped (weights as the M = 256 operand, hi and lo rows as N)
   kp.swap_tail = (pair && g_pair_tiles != 2) ? (a.epilogue == kEpiGateUpAct ? 64 : 128) : 0;
@@ -1722,8 +1730,16 @@ cudaError_t launch_grouped_gemm_q8(const GroupedGemmArgs& a, cudaStream_t s) {
     const uint64_t strides[1] = {2 * K};
     const uint32_t box[2] = {128, BM};
     const uint8_t* lo = static_cast<const uint8_t*>(a.A) + K;
-    if (!encode_tmap(&ta, a.A, 2, dims, strides, box, u8)) return cudaErrorInvalidValue;
-    if (!encode_tmap(&ta_lo, lo, 2, dims, strides, box, u8)) return cudaErrorInvalidValue;
+    if (a.a_gather) {
+      // row gather from the [a_rows, 2K] two-term rows: one-row boxes, 4 rows per load
+      const uint64_t gdims[2] = {K, static_cast<uint64_t>(a.a_rows)};
+      const uint32_t gbox[2] = {128, 1};
+      if (!encode_tmap(&ta, a.A, 2, gdims, strides, gbox, u8)) return cudaErrorInvalidValue;
+      if (!encode_tmap(&ta_lo, lo, 2, gdims, strides, gbox, u8)) return cudaErrorInvalidValue;
+    } else {
+      if (!encode_tmap(&ta, a.A, 2, dims, strides, box, u8)) return cudaErrorInvalidValue;
+      if (!encode_tmap(&ta_lo, lo, 2, dims, strides, box, u8)) return cudaErrorInvalidValue;
+    }
     const uint32_t tbox[2] = {128, 32};  // swapped tails: 32-row boxes
     if (!encode_tmap(&ta_tail, a.A, 2, dims, strides, tbox, u8)) return cudaErrorInvalidValue;
     if (!encode_tmap(&ta_lo_tail, lo, 2, dims, strides, tbox, u8)) return cudaErrorInvalidValue;

@@ -545,7 +545,7 @@ int moe_layer(const moe_config_t* cfg, const void* x, const void* Wg, const floa
   // With MOE_OPT_GATHER_A the routed gate/up pass instead gathers its rows from
   // x (or its fp16 copy) with TMA tile::gather4 loads (slower on GB300: 32
   // four-row requests per 16 KB A tile).
-  const bool gather = g_gather_a && cfg->act_dtype != MOE_F32 && !is_nk(cfg);
+  const bool gather = g_gather_a && cfg->act_dtype != MOE_F32;
   st = do_permute(cfg, ids, gather ? nullptr : x_rows, counts, offsets, sorted_rows, dest,
                   gather ? nullptr : x_perm, seg, err, s, tok_inv, row_inv);
   if (st != MOE_OK) return fail(st);
@@ -646,7 +646,7 @@ int moe_layer_launch_count(const moe_config_t* cfg) {
     n += 1;  // init_routing + permutation gather in one kernel
   } else {
     n += 2;  // histogram, scan + stable scatter
-    if (cfg->act_dtype == MOE_F32 || !g_gather_a || is_nk(cfg)) n += 1;  // permutation gather
+    if (cfg->act_dtype == MOE_F32 || !g_gather_a) n += 1;  // permutation gather
   }
   n += 2;  // routed gate/up, down
   if (cfg->I_shared > 0) n += 2;  // shared gate/up, down

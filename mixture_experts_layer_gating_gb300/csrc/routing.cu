@@ -509,12 +509,23 @@ __global__ void rows_to_fp16_kernel(const Tin* __restrict__ x, int rows, int D,
   for (long long r = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
        r < rows; r += wstride) {
     const Tin* src = x + r * D;
+    // row maximum: four 8-element loads in flight per lane
     float m = 0.0f;
-    for (int v = lane; v < nvec; v += 32) {
-      float f[8];
-      load8f(src, v, f);
+    for (int v0 = lane; v0 < nvec; v0 += 128) {
+      float f[4][8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(f[i]));
+      for (int u = 0; u < 4; ++u) {
+        if (v0 + 32 * u < nvec) {
+          load8f(src, v0 + 32 * u, f[u]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) f[u][i] = 0.0f;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(f[u][i]));
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(FULL, m, off));
@@ -527,6 +538,7 @@ __global__ void rows_to_fp16_kernel(const Tin* __restrict__ x, int rows, int D,
     const float sc = exp2_int(e);
     if (lane == 0) inv_scale[r] = exp2_int(-e);
     uint4* dst = reinterpret_cast<uint4*>(x16 + r * D);
+#pragma unroll 4
     for (int v = lane; v < nvec; v += 32) {
       float f[8];
       load8f(src, v, f);
@@ -573,12 +585,23 @@ __global__ void rows_to_e4m3x2_kernel(const Tin* __restrict__ x, int rows, int D
   for (long long r = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
        r < rows; r += wstride) {
     const Tin* src = x + r * D;
+    // row maximum: four 8-element loads in flight per lane
     float m = 0.0f;
-    for (int v = lane; v < nvec; v += 32) {
-      float f[8];
-      load8f(src, v, f);
+    for (int v0 = lane; v0 < nvec; v0 += 128) {
+      float f[4][8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(f[i]));
+      for (int u = 0; u < 4; ++u) {
+        if (v0 + 32 * u < nvec) {
+          load8f(src, v0 + 32 * u, f[u]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) f[u][i] = 0.0f;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(f[u][i]));
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(FULL, m, off));
@@ -592,6 +615,7 @@ __global__ void rows_to_e4m3x2_kernel(const Tin* __restrict__ x, int rows, int D
     if (lane == 0) inv_scale[r] = exp2_int(-e);
     uint8_t* hi_row = q + r * 2 * D;
     uint8_t* lo_row = hi_row + D;
+#pragma unroll 4
     for (int v = lane; v < nvec; v += 32) {
       float f[8];
       load8f(src, v, f);

@@ -208,3 +208,14 @@ def test_nk_layer_matches_kn_layer_routing():
         assert torch.equal(a[key], b[key]), key
     ref = a["out"].double().numpy()
     assert np.abs(b["out"].double().numpy() - ref).max() <= 6e-2 * rms(ref)
+
+
+@pytest.mark.parametrize("case", ["fp8_small_T300", "fp8_T2048", "ling_T64"])
+def test_layer_parity_nk_gemm_gathers_rows(case):
+    """MOE_OPT_GATHER_A with e4m3 rows: the routed gate/up GEMM gathers the
+    hi and lo terms of its rows from x's two-term rows with TMA gather4."""
+    old = moe.moe_set_option(moe.MOE_OPT_GATHER_A, 1)
+    try:
+        check_layer(NK_LAYERS[case], layout="nk")
+    finally:
+        moe.moe_set_option(moe.MOE_OPT_GATHER_A, old)
