@@ -84,35 +84,37 @@ __global__ void topk_softmax_kernel(const float* __restrict__ partials, int nspl
   }
   if (__any_sync(FULL, nonfinite) && lane == 0) atomicOr(err, MOE_DEV_NONFINITE_LOGIT);
 
+  // Selection on order-preserving integer keys: key(a) > key(b) exactly when
+  // a > b as floats (-0 is first made +0, so equal values get equal keys);
+  // experts past E get key 0, below every finite or -inf logit.  Each round
+  // takes the largest key with one warp max-reduction and, among the lanes
+  // holding it, the lowest expert index with one min-reduction: the same
+  // order as (value descending, index ascending).
+  uint32_t key[EPL];
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const uint32_t u = __float_as_uint(v[i] + 0.0f);
+    key[i] = (lane + 32 * i < E) ? ((u & 0x80000000u) ? ~u : (u | 0x80000000u)) : 0u;
+  }
   uint32_t taken = 0;
   float my_v = -INFINITY;
   int my_e = 0;
   for (int j = 0; j < k; ++j) {
-    float bv = -INFINITY;
-    int be = INT_MAX;
+    uint32_t bk = 0;  // this lane's best remaining key (the lower index among equal keys)
+    int bi = 0;
 #pragma unroll
     for (int i = 0; i < EPL; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E && !((taken >> i) & 1u)) {
-        if (v[i] > bv || (v[i] == bv && e < be)) {
-          bv = v[i];
-          be = e;
-        }
+      if (!((taken >> i) & 1u) && key[i] > bk) {
+        bk = key[i];
+        bi = i;
       }
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ov = __shfl_xor_sync(FULL, bv, off);
-      const int oe = __shfl_xor_sync(FULL, be, off);
-      if (ov > bv || (ov == bv && oe < be)) {
-        bv = ov;
-        be = oe;
-      }
-    }
-    if ((be & 31) == lane) taken |= 1u << (be >> 5);
+    const uint32_t wmax = __reduce_max_sync(FULL, bk);
+    const uint32_t be = __reduce_min_sync(FULL, bk == wmax ? static_cast<uint32_t>(lane + 32 * bi) : 0xFFFFFFFFu);
+    if (static_cast<int>(be & 31u) == lane) taken |= 1u << (be >> 5);
     if (lane == j) {
-      my_v = bv;
-      my_e = be;
+      my_v = __uint_as_float((wmax & 0x80000000u) ? (wmax & 0x7FFFFFFFu) : ~wmax);
+      my_e = static_cast<int>(be);
     }
   }
   const float m = __shfl_sync(FULL, my_v, 0);
