@@ -18,6 +18,10 @@
  *   holds the device error word.
  * - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call is
  *   asynchronous on that stream and returns after enqueueing its kernels.
+ *   The compute calls enqueue only kernels and event records / waits (no
+ *   host synchronisation, no allocation), so they can be captured into a
+ *   CUDA graph; the first call on a device does one-time set-up (kernel
+ *   attributes, moe_layer's side stream), so make it before capturing.
  * - Return value: MOE_OK or a negative moe_status_t.  Argument errors are
  *   detected on the host before anything is enqueued.  Data errors found on
  *   the device (an expert id outside [0, E), non-monotone offsets, a permuted

@@ -617,3 +617,33 @@ def test_layer_parity_one_hot_expert():
     keep = ~oracle.near_tie_tokens(ref["logits"], shape.k)
     err = np.abs(g["out"].double().numpy() - ref["out"])[keep]
     assert err.max() <= tol_factor(shape) * rms(ref["out"])
+
+
+@pytest.mark.parametrize("case,layout", [("gemma4_T8_decode", "kn"), ("qwen3_T512", "kn"),
+                                         ("fp8_small_T300", "nk")])
+def test_moe_layer_captures_into_a_cuda_graph(case, layout):
+    """moe_layer enqueues only kernels, event records and waits (no host
+    synchronisation, no allocation), so a stream capture of it replays to the
+    eager call's output bit for bit, shared-expert side stream included."""
+    shape = LAYER_CASES[case]
+    inp = workloads.make_inputs(shape, seed=13, device="cuda")
+    cfg = moe.config_from_shape(shape, layout)
+    W = packed_weights(inp, layout)
+    ws = moe.alloc_workspace(cfg)
+    out = torch.empty((shape.T, shape.D), dtype=workloads.torch_dtype(shape.act_dtype), device="cuda")
+    s = torch.cuda.Stream()
+    args = (cfg, inp["x"], inp["Wg"], inp["logit_bias"], W["W13"], inp["s13"], W["W2"], inp["s2"],
+            W["W13s"], inp["s13s"], W["W2s"], inp["s2s"], out, ws)
+    with torch.cuda.stream(s):
+        moe.moe_layer(*args, stream=s)  # first call: per-device one-time set-up outside the capture
+    torch.cuda.synchronize()
+    eager = out.clone()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        moe.moe_layer(*args, stream=s)
+    for _ in range(3):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, eager)
+    assert moe.moe_read_device_status(ws) == 0
