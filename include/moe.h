@@ -33,8 +33,9 @@
  * - Dtypes: act_dtype applies to x, W_g, the permuted rows and out.  w_dtype
  *   applies to W13, W2 and the shared expert's weights.  Supported pairs:
  *   (F32, F32), (BF16, BF16), (BF16, FP8_E4M3), (BF16, FP8_E4M3_NK).
- *   Router logits, gate weights,
- *   the expert outputs y_perm and the shared-expert output are always fp32.
+ *   Router logits and gate weights are always fp32; the expert outputs
+ *   y_perm and the shared-expert output are fp32, or bf16 for fp8-weight
+ *   layers (one rounding each, inside the 6e-2 RMS bar of those layers).
  *   The intermediate h takes 4 bytes per element: fp32 for fp32 layers and
  *   for fp8 weights; for bf16 weights two bf16 planes [M, I] -- h_hi =
  *   bf16(h) followed by h_lo = bf16(h - h_hi) -- which the down projection
@@ -191,12 +192,14 @@ int moe_permute_noalloc(const moe_config_t* cfg, const int32_t* topk_ids, const 
  *   h       out: act(gate) * up, [T*k, I] fp32 (fp32 layers and fp8 weights)
  *           or the bf16 pair [2, T*k, I] (hi plane, then lo plane) for bf16
  *           weights.
- *   y_perm  [T*k, D] fp32 out: h W2 per segment (times s2 for fp8).
+ *   y_perm  [T*k, D] out: h W2 per segment (times s2 for fp8); fp32, or
+ *           bf16 for fp8-weight layers (their 6e-2 bar leaves room, and the
+ *           combine then reads half the bytes).
  *   x, W13s [D, 2*I_shared], s13s [2*I_shared], W2s [I_shared, D], s2s [D]:
  *           the shared expert (FP8_E4M3_NK: W13s [2*I_shared, D], W2s
  *           [D, I_shared]); x NULL (or I_shared == 0) skips it.
  *   h_s     shared intermediate, same layout as h with T rows.
- *   s_out   [T, D] fp32 out: shared expert output. */
+ *   s_out   [T, D] out: shared expert output, fp32 (bf16 for fp8 weights). */
 int moe_grouped_ffn(const moe_config_t* cfg, const void* x_perm, const int32_t* offsets,
                     const void* W13, const float* s13, const void* W2, const float* s2, void* h,
                     void* y_perm, const void* x, const void* W13s, const float* s13s,
@@ -210,8 +213,9 @@ int moe_grouped_ffn(const moe_config_t* cfg, const void* x_perm, const int32_t* 
  *   out[t] = round( sum_{j<k} w[t, j] * y_perm[dest[t*k + j]] + s[t] ),
  *   accumulated in fp32 with j ascending, the shared row added last, one
  *   rounding to act_dtype.
- *   y_perm [T*k, D] fp32, dest [T*k] int32, topk_w [T, k] fp32,
- *   s [T, D] fp32 or NULL, out [T, D] act_dtype. */
+ *   y_perm [T*k, D] fp32 (bf16 for fp8-weight layers), dest [T*k] int32,
+ *   topk_w [T, k] fp32, s [T, D] of y_perm's type or NULL, out [T, D]
+ *   act_dtype. */
 int moe_finalize(const moe_config_t* cfg, const void* y_perm, const int32_t* dest,
                  const float* topk_w, const void* s, void* out, void* ws, size_t ws_bytes,
                  void* stream);

@@ -326,6 +326,7 @@ int do_ffn(const moe_config_t* c, const void* A, const float* a_row_scale, int M
   b.a_gather = nullptr;
   b.h_fp32 = 0;
   b.out = y;
+  b.out_bf16 = fp8;  // fp8-weight layers: expert (and shared) rows in bf16
   b.out_lo = nullptr;
   trace_mark(s);
   e = launch_grouped_gemm(b, s);
@@ -463,7 +464,7 @@ int moe_finalize(const moe_config_t* cfg, const void* y_perm, const int32_t* des
   if (cfg->T == 0) return MOE_OK;
   return cuda_status(launch_finalize(cfg->act_dtype, y_perm, dest, topk_w, s, out, cfg->T, cfg->k,
                                      cfg->D, cfg->T * cfg->k, err_word(ws),
-                                     static_cast<cudaStream_t>(stream)));
+                                     static_cast<cudaStream_t>(stream), is_fp8(cfg)));
 }
 
 int moe_layer(const moe_config_t* cfg, const void* x, const void* Wg, const float* logit_bias,
@@ -556,7 +557,7 @@ int moe_layer(const moe_config_t* cfg, const void* x, const void* Wg, const floa
   if (side && !side_join(side, s)) return (g_trace_next = -1, MOE_ERR_CUDA);
   trace_mark(s);
   st = cuda_status(launch_finalize(cfg->act_dtype, y_perm, dest, w, shared ? s_out : nullptr, out,
-                                   cfg->T, cfg->k, cfg->D, cfg->T * cfg->k, err, s));
+                                   cfg->T, cfg->k, cfg->D, cfg->T * cfg->k, err, s, fp8));
   trace_mark(s);
   g_trace_next = -1;
   return st;

@@ -110,10 +110,10 @@ cudaError_t launch_rows_to_e4m3x2(const void* x, int rows, int D, void* q, float
 // W_nk[g][n][c] = W[g][c][n], one-byte elements (K, N multiples of 16).
 cudaError_t launch_transpose_bytes(const void* W, long long G, int K, int N, void* W_nk,
                                    cudaStream_t s);
-// y_perm and s_rows are fp32; out is act_dtype.
+// y_perm and s_rows are fp32 (bf16 when y_bf16); out is act_dtype.
 cudaError_t launch_finalize(int act_dtype, const void* y_perm, const int32_t* dest, const float* w,
                             const void* s_rows, void* out, int T, int k, int D, int R,
-                            int32_t* err, cudaStream_t s);
+                            int32_t* err, cudaStream_t s, bool y_bf16 = false);
 
 // ---------------------------------------------------------------- simt_fp32.cu
 // fp32 path (exact-fp32 configurations): plain CUDA-core kernels.
@@ -158,7 +158,8 @@ struct GroupedGemmArgs {
   int ksplit;                    // >1: K split into planes out[s] = partial sums (fp32 store only)
   int pair_ok;                   // 1: 2-CTA (M=256) tiles may be used
   int decode_ok;                 // 1: the swap-AB decode kernel may be used
-  void* out;                     // [M, N] fp32, or bf16 h_hi (gate/up pass)
+  void* out;                     // [M, N] fp32 (bf16 when out_bf16), or bf16 h_hi (gate/up pass)
+  int out_bf16;                  // store pass: bf16 output rows
   void* out_lo;                  // [M, N] bf16 h_lo (gate/up pass)
   int act;                       // moe_act_t (gate/up epilogue)
   int32_t* err;

@@ -703,9 +703,28 @@ __device__ __forceinline__ void store8(float* p, const float (&f)[8]) {
   *reinterpret_cast<float4*>(p + 4) = make_float4(f[4], f[5], f[6], f[7]);
 }
 
-template <typename Tt, int KMAX>
-__global__ void finalize_kernel(const float* __restrict__ y_perm, const int32_t* __restrict__ dest,
-                                const float* __restrict__ w, const float* __restrict__ s_rows,
+// Ty: the type of the expert rows and the shared row (fp32, or bf16 for
+// fp8-weight layers).
+// 8 elements from their raw 16-byte words: two words of fp32, or one of bf16
+__device__ __forceinline__ void unpack8(const uint4 (&u)[2], float (&f)[8]) {
+  f[0] = __uint_as_float(u[0].x); f[1] = __uint_as_float(u[0].y);
+  f[2] = __uint_as_float(u[0].z); f[3] = __uint_as_float(u[0].w);
+  f[4] = __uint_as_float(u[1].x); f[5] = __uint_as_float(u[1].y);
+  f[6] = __uint_as_float(u[1].z); f[7] = __uint_as_float(u[1].w);
+}
+__device__ __forceinline__ void unpack8(const uint4 (&u)[1], float (&f)[8]) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u[0]);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 v = __bfloat1622float2(h[i]);
+    f[2 * i] = v.x;
+    f[2 * i + 1] = v.y;
+  }
+}
+
+template <typename Tt, int KMAX, typename Ty>
+__global__ void finalize_kernel(const Ty* __restrict__ y_perm, const int32_t* __restrict__ dest,
+                                const float* __restrict__ w, const Ty* __restrict__ s_rows,
                                 Tt* __restrict__ out, int T, int k, int D, int R, int m,
                                 int32_t* err) {
   pdl_wait();
@@ -741,20 +760,24 @@ __global__ void finalize_kernel(const float* __restrict__ y_perm, const int32_t*
     }
     for (int c = s0 * 32 + lane; c < min(nslice, s0 + m) * 32 && c < nchunk; c += 32) {
       // issue all k row loads before any arithmetic so they are in flight together
-      float4 a[KMAX], b[KMAX];
+      // (8 elements per row: 32 bytes of fp32, or 16 bytes of bf16)
+      constexpr int kVec = sizeof(Ty) == 4 ? 2 : 1;
+      uint4 rv[KMAX][kVec];
 #pragma unroll
       for (int j = 0; j < KMAX; ++j) {
         if (j < k) {
-          const float4* src = reinterpret_cast<const float4*>(y_perm + static_cast<long long>(pj[j]) * D) + 2 * c;
-          a[j] = __ldcs(src);
-          b[j] = __ldcs(src + 1);
+          const uint4* src = reinterpret_cast<const uint4*>(y_perm + static_cast<long long>(pj[j]) * D) + kVec * c;
+#pragma unroll
+          for (int q = 0; q < kVec; ++q) rv[j][q] = __ldcs(src + q);
         }
       }
-      float4 sa = make_float4(0.f, 0.f, 0.f, 0.f), sb = sa;
+      uint4 sv[kVec];
+#pragma unroll
+      for (int q = 0; q < kVec; ++q) sv[q] = make_uint4(0u, 0u, 0u, 0u);
       if (s_rows) {
-        const float4* src = reinterpret_cast<const float4*>(s_rows + t * D) + 2 * c;
-        sa = __ldcs(src);
-        sb = __ldcs(src + 1);
+        const uint4* src = reinterpret_cast<const uint4*>(s_rows + t * D) + kVec * c;
+#pragma unroll
+        for (int q = 0; q < kVec; ++q) sv[q] = __ldcs(src + q);
       }
       float acc[8];
 #pragma unroll
@@ -762,18 +785,18 @@ __global__ void finalize_kernel(const float* __restrict__ y_perm, const int32_t*
 #pragma unroll
       for (int j = 0; j < KMAX; ++j) {
         if (j < k) {
-          acc[0] = fmaf(wj[j], a[j].x, acc[0]);
-          acc[1] = fmaf(wj[j], a[j].y, acc[1]);
-          acc[2] = fmaf(wj[j], a[j].z, acc[2]);
-          acc[3] = fmaf(wj[j], a[j].w, acc[3]);
-          acc[4] = fmaf(wj[j], b[j].x, acc[4]);
-          acc[5] = fmaf(wj[j], b[j].y, acc[5]);
-          acc[6] = fmaf(wj[j], b[j].z, acc[6]);
-          acc[7] = fmaf(wj[j], b[j].w, acc[7]);
+          float f[8];
+          unpack8(rv[j], f);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj[j], f[i], acc[i]);
         }
       }
-      acc[0] += sa.x; acc[1] += sa.y; acc[2] += sa.z; acc[3] += sa.w;
-      acc[4] += sb.x; acc[5] += sb.y; acc[6] += sb.z; acc[7] += sb.w;
+      {
+        float f[8];
+        unpack8(sv, f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] += f[i];
+      }
       store8(out + t * D + c * 8, acc);
     }
   }
@@ -915,7 +938,7 @@ cudaError_t launch_transpose_bytes(const void* W, long long G, int K, int N, voi
 
 cudaError_t launch_finalize(int act_dtype, const void* y_perm, const int32_t* dest, const float* w,
                             const void* s_rows, void* out, int T, int k, int D, int R,
-                            int32_t* err, cudaStream_t s) {
+                            int32_t* err, cudaStream_t s, bool y_bf16) {
   if (T <= 0) return cudaSuccess;
   const int threads = 256;
   // warp items of m 256-column slices: whole rows (measured fastest) when
@@ -929,14 +952,20 @@ cudaError_t launch_finalize(int act_dtype, const void* y_perm, const int32_t* de
   const int blocks = blocks_for(items, threads / 32, device_sm_count() * 16);
   const float* y = static_cast<const float*>(y_perm);
   const float* sr = static_cast<const float*>(s_rows);
+  const __nv_bfloat16* yb = static_cast<const __nv_bfloat16*>(y_perm);
+  const __nv_bfloat16* srb = static_cast<const __nv_bfloat16*>(s_rows);
 #define MOE_FIN(KM)                                                               \
   do {                                                                            \
-    if (act_dtype == MOE_BF16) {                                                  \
-      auto kern = finalize_kernel<__nv_bfloat16, KM>;                             \
+    if (act_dtype == MOE_BF16 && y_bf16) {                                        \
+      auto kern = finalize_kernel<__nv_bfloat16, KM, __nv_bfloat16>;              \
+      MOE_LAUNCH(kern, blocks, threads, 0, s, yb, dest, w, srb,                   \
+                 static_cast<__nv_bfloat16*>(out), T, k, D, R, m, err);           \
+    } else if (act_dtype == MOE_BF16) {                                           \
+      auto kern = finalize_kernel<__nv_bfloat16, KM, float>;                      \
       MOE_LAUNCH(kern, blocks, threads, 0, s, y, dest, w, sr,                     \
                  static_cast<__nv_bfloat16*>(out), T, k, D, R, m, err);           \
     } else {                                                                      \
-      auto kern = finalize_kernel<float, KM>;                                     \
+      auto kern = finalize_kernel<float, KM, float>;                              \
       MOE_LAUNCH(kern, blocks, threads, 0, s, y, dest, w, sr,                     \
                  static_cast<float*>(out), T, k, D, R, m, err);                   \
     }                                                                             \

@@ -461,15 +461,15 @@ def test_grouped_ffn_fp8_parity(E, counts, D, I, act, tile_mode):
     cfg = moe.make_config(R, D, E, 1, I, act=act, w_dtype="fp8_e4m3")
     ws = _ws_for(cfg)
     h = torch.empty((R, I), dtype=torch.float32, device="cuda")
-    y = torch.empty((R, D), dtype=torch.float32, device="cuda")
+    y = torch.empty((R, D), dtype=torch.bfloat16, device="cuda")  # fp8 layers: bf16 expert rows
     moe.moe_grouped_ffn(cfg, xp, torch.from_numpy(offsets).cuda(), W13, s13, W2, s2, h, y, ws=ws)
     assert moe.moe_read_device_status(ws) == 0
     h_o, y_o = oracle.grouped_ffn(oracle.to_f64(xp.cpu()), offsets, W13.cpu(), W2.cpu(), act,
                                   s13.cpu(), s2.cpu())
     # h is fp32 (exact fp16 x rows, fp32 accumulation)
     check_close("h", h.cpu().double().numpy(), h_o, 1e-4, 1e-4)
-    # y from h rounded once to fp16 (11 bits) relative to its row maximum
-    check_close("y", y.cpu().double().numpy(), y_o, 2.0 ** -9, 2e-3)
+    # y from h rounded once to fp16 (11 bits) relative to its row maximum, then to bf16
+    check_close("y", y.cpu().double().numpy(), y_o, 2.0 ** -8, 2e-3)
 
 
 def test_fp8_weight_expansion_is_exact_including_subnormals(tile_mode):
@@ -498,7 +498,7 @@ def test_fp8_weight_expansion_is_exact_including_subnormals(tile_mode):
     cfg = moe.make_config(R, D, E, 1, I, w_dtype="fp8_e4m3")
     ws = _ws_for(cfg)
     h = torch.empty((R, I), dtype=torch.float32, device="cuda")
-    y = torch.empty((R, D), dtype=torch.float32, device="cuda")
+    y = torch.empty((R, D), dtype=torch.bfloat16, device="cuda")
     moe.moe_grouped_ffn(cfg, xp, torch.from_numpy(offsets).cuda(), W13, s13, W2, s2, h, y, ws=ws)
     assert moe.moe_read_device_status(ws) == 0
     h_o, _ = oracle.grouped_ffn(oracle.to_f64(xp.cpu()), offsets, W13.cpu(), W2.cpu(), "swiglu",
@@ -515,7 +515,8 @@ def test_fp8_weight_expansion_is_exact_including_subnormals(tile_mode):
     for e in range(E):
         a, b = offsets[e], offsets[e + 1]
         y_ref[a:b] = oracle.scaled_projection(hg[a:b], oracle.to_f64(W2[e].cpu()), oracle.to_f64(s2[e].cpu()))
-    check_close("y", y.cpu().double().numpy(), y_ref, 1e-5, 1e-5)
+    # fp32 accumulation, then one bf16 rounding
+    check_close("y", y.cpu().double().numpy(), y_ref, 2.0 ** -8, 1e-5)
     assert rms(y_ref) > 0
 
 
@@ -581,8 +582,9 @@ def test_stage_calls_match_moe_layer(case, layout):
          else torch.empty((2, R, I), dtype=torch.bfloat16, device=dev))
     h_s = (torch.empty((T, Is), dtype=torch.float32, device=dev) if fp8
            else torch.empty((2, T, Is), dtype=torch.bfloat16, device=dev))
-    y = torch.empty((R, D), dtype=torch.float32, device=dev)
-    s_out = torch.empty((T, D), dtype=torch.float32, device=dev)
+    ydt = torch.bfloat16 if fp8 else torch.float32  # fp8 layers: bf16 expert and shared rows
+    y = torch.empty((R, D), dtype=ydt, device=dev)
+    s_out = torch.empty((T, D), dtype=ydt, device=dev)
     W = packed_weights(inp, layout)
     moe.moe_grouped_ffn(cfg, x_perm, offsets, W["W13"], inp["s13"], W["W2"], inp["s2"], h, y,
                         inp["x"], W["W13s"], inp["s13s"], W["W2s"], inp["s2s"], h_s, s_out, ws)
@@ -647,3 +649,24 @@ def test_moe_layer_captures_into_a_cuda_graph(case, layout):
         torch.cuda.synchronize()
         assert torch.equal(out, eager)
     assert moe.moe_read_device_status(ws) == 0
+
+
+@pytest.mark.parametrize("T,k,D,shared", [(513, 8, 2048, True), (3, 1, 272, False)])
+def test_finalize_parity_bf16_rows(T, k, D, shared):
+    """fp8-weight layers hand finalize bf16 expert and shared rows."""
+    gen = torch.Generator(device="cuda").manual_seed(T + 3 * k)
+    R = T * k
+    y = torch.randn((R, D), generator=gen, device="cuda").to(torch.bfloat16)
+    perm = torch.randperm(R, generator=gen, device="cuda").to(torch.int32)
+    w = torch.rand((T, k), generator=gen, device="cuda")
+    w = w / w.sum(1, keepdim=True)
+    s = torch.randn((T, D), generator=gen, device="cuda").to(torch.bfloat16) if shared else None
+    out = torch.empty((T, D), dtype=torch.bfloat16, device="cuda")
+    cfg = moe.make_config(T, D, 16, k, 64, w_dtype="fp8_e4m3_nk")
+    ws = _ws_for(cfg)
+    moe.moe_finalize(cfg, y, perm, w, s, out, ws)
+    assert moe.moe_read_device_status(ws) == 0
+    ref = oracle.finalize(oracle.to_f64(y.cpu()), perm.cpu().numpy(), w.cpu().double().numpy(),
+                          None if s is None else oracle.to_f64(s.cpu()))
+    got = out.cpu().double().numpy()
+    assert (np.abs(got - ref) <= np.abs(ref) * 2.0 ** -8 + 1e-5).all()
