@@ -51,6 +51,7 @@
 
 #include <algorithm>
 #include <mutex>
+#include <type_traits>
 
 #include "moe_internal.h"
 #include "sm103_ptx.cuh"
@@ -148,14 +149,16 @@ struct KParams {
   // 2-CTA tiles: a group's last tile with at most swap_tail rows runs "swapped":
   // weights as the M = 256 operand (128 features per CTA), its rows as N
   int swap_tail;
-  int out_bf16;  // store pass: write the output rows in bf16 instead of fp32
   int32_t* err;
 };
 
-// One element of a store-pass output row: fp32, or bf16 when p.out_bf16.
-__device__ __forceinline__ void store_out(void* out, size_t i, float v, int out_bf16) {
-  if (out_bf16) reinterpret_cast<__nv_bfloat16*>(out)[i] = __float2bfloat16_rn(v);
-  else reinterpret_cast<float*>(out)[i] = v;
+// Element type of the store pass's output rows: bf16 for fp8-weight layers
+// (expanded on chip or read as e4m3), fp32 otherwise.
+template <bool FP8W>
+using StoreT = typename std::conditional<FP8W, __nv_bfloat16, float>::type;
+__device__ __forceinline__ void store_elem(float* out, size_t i, float v) { out[i] = v; }
+__device__ __forceinline__ void store_elem(__nv_bfloat16* out, size_t i, float v) {
+  out[i] = __float2bfloat16_rn(v);
 }
 
 struct TileInfo {
@@ -887,8 +890,8 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
                   if (c + j >= tw.rows) break;
                   const size_t row = static_cast<size_t>(tw.row0 + c + j);
                   const float rs = p.a_row_scale ? p.a_row_scale[row] : 1.0f;
-                  store_out(p.out, plane + row * p.N + f,
-                            (__uint_as_float(hi[j]) + __uint_as_float(lo[j])) * rs * cs, p.out_bf16);
+                  store_elem(reinterpret_cast<StoreT<FP8 || Q8>*>(p.out), plane + row * p.N + f,
+                             (__uint_as_float(hi[j]) + __uint_as_float(lo[j])) * rs * cs);
                 }
               }
             }
@@ -976,9 +979,9 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
           }
         }
       } else {  // kEpiStoreF32: (acc * row scale * scale[col]) + bias[col]
-        // this split's output plane (fp32, or bf16 when p.out_bf16)
-        void* out_base = p.out_bf16 ? static_cast<void*>(reinterpret_cast<__nv_bfloat16*>(p.out) + plane)
-                                    : static_cast<void*>(reinterpret_cast<float*>(p.out) + plane);
+        // this split's output plane (bf16 rows for fp8-weight layers)
+        using OutT = StoreT<FP8 || Q8>;
+        OutT* out = reinterpret_cast<OutT*>(p.out) + plane;
         const float* sc = p.b_scale ? p.b_scale + static_cast<size_t>(ti.g) * p.N : nullptr;
         const float rs = (p.a_row_scale && valid) ? p.a_row_scale[out_row] : 1.0f;
         // after the transpose lane l owns 4 columns (4 * (l % 8) ..) of rows
@@ -1011,21 +1014,19 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
 #pragma unroll 2
           for (int rr = sub; rr < wrows; rr += 4) {
             const float4 v = *reinterpret_cast<const float4*>(stg + rr * EPI_STAGE_LD + c4);
-            const size_t orow = static_cast<size_t>(wrow0 + rr) * p.N;
+            OutT* orow = out + static_cast<size_t>(wrow0 + rr) * p.N;
             const float o0 = v.x * cs[0] + cb[0], o1 = v.y * cs[1] + cb[1];
             const float o2 = v.z * cs[2] + cb[2], o3 = v.w * cs[3] + cb[3];
             if (vec && cl + 4 <= p.N) {
-              if (p.out_bf16)
-                *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(out_base) + orow + cl) =
-                    make_uint2(pack_bf16x2(o0, o1), pack_bf16x2(o2, o3));
+              if (FP8 || Q8)
+                *reinterpret_cast<uint2*>(orow + cl) = make_uint2(pack_bf16x2(o0, o1), pack_bf16x2(o2, o3));
               else
-                *reinterpret_cast<float4*>(reinterpret_cast<float*>(out_base) + orow + cl) =
-                    make_float4(o0, o1, o2, o3);
+                *reinterpret_cast<float4*>(orow + cl) = make_float4(o0, o1, o2, o3);
             } else {
-              if (cl < p.N) store_out(out_base, orow + cl, o0, p.out_bf16);
-              if (cl + 1 < p.N) store_out(out_base, orow + cl + 1, o1, p.out_bf16);
-              if (cl + 2 < p.N) store_out(out_base, orow + cl + 2, o2, p.out_bf16);
-              if (cl + 3 < p.N) store_out(out_base, orow + cl + 3, o3, p.out_bf16);
+              if (cl < p.N) store_elem(orow, cl, o0);
+              if (cl + 1 < p.N) store_elem(orow, cl + 1, o1);
+              if (cl + 2 < p.N) store_elem(orow, cl + 2, o2);
+              if (cl + 3 < p.N) store_elem(orow, cl + 3, o3);
             }
           }
         }
@@ -1430,7 +1431,8 @@ __global__ void __launch_bounds__(DecCfg<SPLIT, FP8>::kThreads, 1)
             if (j >= rows) break;
             const size_t row = static_cast<size_t>(ti.row0 + j);
             const float rs = p.a_row_scale ? p.a_row_scale[row] : 1.0f;
-            store_out(p.out, row * p.N + f, __uint_as_float(v[j]) * rs * cs, p.out_bf16);
+            store_elem(reinterpret_cast<StoreT<FP8 || Q8>*>(p.out), row * p.N + f,
+                       __uint_as_float(v[j]) * rs * cs);
           }
         }
       }
@@ -1607,7 +1609,6 @@ cudaError_t launch_grouped_gemm_decode_q8(const GroupedGemmArgs& a, int nt, cuda
   kp.a_row_scale = a.a_row_scale;
   kp.h_fp32 = a.h_fp32;
   kp.act = a.act;
-  kp.out_bf16 = a.out_bf16;
   kp.err = a.err;
   kp.bn = nt;
   kp.ksplit = 1;
@@ -1665,7 +1666,6 @@ cudaError_t launch_grouped_gemm_decode(const GroupedGemmArgs& a, int nt, cudaStr
   kp.a_row_scale = a.a_row_scale;
   kp.h_fp32 = a.h_fp32;
   kp.act = a.act;
-  kp.out_bf16 = a.out_bf16;
   kp.err = a.err;
   kp.bn = nt;
   kp.ksplit = 1;
@@ -1717,7 +1717,6 @@ cudaError_t launch_grouped_gemm_q8(const GroupedGemmArgs& a, cudaStream_t s) {
   kp.a_rows = a.a_rows;
   kp.h_fp32 = a.h_fp32;
   kp.act = a.act;
-  kp.out_bf16 = a.out_bf16;
   kp.err = a.err;
   kp.ksplit = 1;
   kp.kbs = (a.K + 127) / 128;
@@ -1879,7 +1878,6 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
   kp.a_rows = a.a_rows;
   kp.h_fp32 = a.h_fp32;
   kp.act = a.act;
-  kp.out_bf16 = a.out_bf16;
   kp.err = a.err;
   {
     const int KB = (a.K + BK - 1) / BK;

@@ -98,6 +98,12 @@ cudaError_t launch_init_routing(const int32_t* ids, int R, int E, int32_t* count
 cudaError_t launch_permute_gather(const void* x, const int32_t* sorted_rows, int R, int k, int T,
                                   size_t row_bytes, void* x_perm, int32_t* err, cudaStream_t s,
                                   const float* tok_scale = nullptr, float* row_scale = nullptr);
+// The same permutation from the token side (x read once): x_perm[dest[t*k+j]]
+// = x[t]; rows at positions >= *nvalid (only after invalid ids) are zeroed.
+cudaError_t launch_permute_scatter(const void* x, const int32_t* dest, const int32_t* nvalid,
+                                   int R, int k, int T, size_t row_bytes, void* x_perm,
+                                   int32_t* err, cudaStream_t s, const float* tok_scale = nullptr,
+                                   float* row_scale = nullptr);
 // bf16 (or fp32 when src_f32) rows -> fp16 rows times an exact power of two
 // (max |row| < 2^14); inv_scale[r] = the inverse power of two.
 cudaError_t launch_rows_to_fp16(const void* x, int rows, int D, void* x16, float* inv_scale,
@@ -158,8 +164,8 @@ struct GroupedGemmArgs {
   int ksplit;                    // >1: K split into planes out[s] = partial sums (fp32 store only)
   int pair_ok;                   // 1: 2-CTA (M=256) tiles may be used
   int decode_ok;                 // 1: the swap-AB decode kernel may be used
-  void* out;                     // [M, N] fp32 (bf16 when out_bf16), or bf16 h_hi (gate/up pass)
-  int out_bf16;                  // store pass: bf16 output rows
+  void* out;                     // [M, N] fp32 (bf16 when the weights are fp8), or bf16 h_hi
+                                 // (gate/up pass)
   void* out_lo;                  // [M, N] bf16 h_lo (gate/up pass)
   int act;                       // moe_act_t (gate/up epilogue)
   int32_t* err;

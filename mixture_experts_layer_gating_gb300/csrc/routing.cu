@@ -470,6 +470,70 @@ __global__ void permute_gather_kernel(const uint4* __restrict__ x,
   pdl_launch_dependents();  // after the copy: long kernel, see finalize_kernel
 }
 
+// The same permutation driven from the token side: each warp item is one
+// token's slice of 256 16-byte chunks, read once and written to the token's k
+// permuted rows (dest[t*k + j]); positions past the last valid row (only
+// when ids were invalid) are zero-filled.  Reads x once instead of k times,
+// which matters when x is larger than L2 (every row would come from HBM k
+// times).
+constexpr int kScatterSlice = 256;
+
+__global__ void permute_scatter_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ dest,
+                                       const int32_t* __restrict__ nvalid_ptr, int R, int k, int T,
+                                       int vec_per_row, uint4* __restrict__ x_perm,
+                                       const float* __restrict__ tok_scale,
+                                       float* __restrict__ row_scale, int32_t* err) {
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const long long wid = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const long long wstride = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+  const int nsl = (vec_per_row + kScatterSlice - 1) / kScatterSlice;
+  const long long items = static_cast<long long>(T) * nsl;
+  for (long long it = wid; it < items; it += wstride) {
+    const long long t = it / nsl;
+    const int sl = static_cast<int>(it - t * nsl);
+    int my_p = -1;
+    if (lane < k) {
+      const int p = dest[t * k + lane];
+      if (p >= R) atomicOr(err, MOE_DEV_BAD_DEST);
+      my_p = (p >= 0 && p < R) ? p : -1;  // -1: a row whose id was invalid
+      if (sl == 0 && row_scale && my_p >= 0) row_scale[my_p] = tok_scale[t];
+    }
+    int pj[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) pj[j] = __shfl_sync(FULL, my_p, j);
+    const uint4* src = x + t * vec_per_row;
+    const int v1 = min(vec_per_row, (sl + 1) * kScatterSlice);
+    int v = sl * kScatterSlice + lane;
+    for (; v + 96 < v1; v += 128) {
+      const uint4 a = src[v], b = src[v + 32], c = src[v + 64], d = src[v + 96];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        if (j < k && pj[j] >= 0) {
+          uint4* dst = x_perm + static_cast<long long>(pj[j]) * vec_per_row;
+          dst[v] = a;
+          dst[v + 32] = b;
+          dst[v + 64] = c;
+          dst[v + 96] = d;
+        }
+      }
+    }
+    for (; v < v1; v += 32) {
+      const uint4 a = src[v];
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        if (j < k && pj[j] >= 0) x_perm[static_cast<long long>(pj[j]) * vec_per_row + v] = a;
+    }
+  }
+  // rows past the last valid one (ids that were out of range)
+  const int nvalid = max(0, min(R, *nvalid_ptr));
+  for (long long p = nvalid + wid; p < R; p += wstride) {
+    if (row_scale && lane == 0) row_scale[p] = 0.0f;
+    for (int v = lane; v < vec_per_row; v += 32) x_perm[p * vec_per_row + v] = make_uint4(0, 0, 0, 0);
+  }
+  pdl_launch_dependents();  // after the copy: long kernel, see finalize_kernel
+}
+
 // ------------------------------------------------------------------------
 // bf16 rows to fp16 rows with an exact power-of-two row scale, for the fp16
 // tensor-core path of fp8-weight layers: row t is multiplied by 2^e_t with
@@ -896,6 +960,21 @@ cudaError_t launch_permute_gather(const void* x, const int32_t* sorted_rows, int
   const int blocks = blocks_for(R, threads / 32, device_sm_count() * 16);
   MOE_LAUNCH(permute_gather_kernel, blocks, threads, 0, s, static_cast<const uint4*>(x),
              sorted_rows, R, k, T, vec, static_cast<uint4*>(x_perm), tok_scale, row_scale, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_permute_scatter(const void* x, const int32_t* dest, const int32_t* nvalid,
+                                   int R, int k, int T, size_t row_bytes, void* x_perm,
+                                   int32_t* err, cudaStream_t s, const float* tok_scale,
+                                   float* row_scale) {
+  if (R <= 0) return cudaSuccess;
+  if (k > 16) return cudaErrorInvalidValue;
+  const int vec = static_cast<int>(row_bytes / 16);
+  const int threads = 256;
+  const long long items = static_cast<long long>(T) * ((vec + kScatterSlice - 1) / kScatterSlice);
+  const int blocks = blocks_for(items, threads / 32, device_sm_count() * 16);
+  MOE_LAUNCH(permute_scatter_kernel, blocks, threads, 0, s, static_cast<const uint4*>(x), dest,
+             nvalid, R, k, T, vec, static_cast<uint4*>(x_perm), tok_scale, row_scale, err);
   return cudaGetLastError();
 }
 

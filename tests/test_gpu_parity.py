@@ -289,13 +289,15 @@ def test_route_projection_then_topk_bit_exact(T, E, k, renorm, bias):
         assert np.array_equal(ids[7].cpu().numpy(), np.arange(k))
 
 
-@pytest.mark.parametrize("T,E,k,pattern", [
-    (1000, 128, 8, "uniform"), (3000, 512, 10, "uniform"), (129, 8, 2, "one_hot"),
-    (4096, 256, 8, "skew"), (1, 4, 1, "uniform"), (2500, 64, 6, "empty_half"),
+@pytest.mark.parametrize("T,E,k,pattern,D", [
+    (1000, 128, 8, "uniform", 136), (3000, 512, 10, "uniform", 136), (129, 8, 2, "one_hot", 136),
+    (4096, 256, 8, "skew", 136), (1, 4, 1, "uniform", 136), (2500, 64, 6, "empty_half", 136),
     # either side of the one-launch small-batch path (at most 8192 expanded rows)
-    (1024, 512, 8, "uniform"), (8193, 16, 1, "skew"), (64, 128, 8, "skew"),
+    (1024, 512, 8, "uniform", 136), (8193, 16, 1, "skew", 136), (64, 128, 8, "skew", 136),
+    # x above 32 MB: each token row read once and written to its k positions
+    (4200, 64, 4, "skew", 4096), (5000, 32, 16, "uniform", 4104),
 ])
-def test_permute_bit_exact(T, E, k, pattern):
+def test_permute_bit_exact(T, E, k, pattern, D):
     gen = np.random.default_rng(T + E + k)
     if pattern == "one_hot":  # expert 3 and 5 take every token
         ids = np.tile(np.array([3, 5]), (T, 1))
@@ -306,7 +308,6 @@ def test_permute_bit_exact(T, E, k, pattern):
         ids = np.stack([gen.permutation(E // 2)[:k] * 2 for _ in range(T)])
     else:
         ids = np.stack([gen.permutation(E)[:k] for _ in range(T)])
-    D = 136
     cfg = moe.make_config(T, D, E, k, 64)
     ws = _ws_for(cfg)
     tids = torch.from_numpy(ids.astype(np.int32)).cuda()
@@ -329,9 +330,9 @@ def test_permute_bit_exact(T, E, k, pattern):
     assert torch.equal(xp[dest.long()].view(T, k, D)[:, 0], x)
 
 
-@pytest.mark.parametrize("T", [300, 5000])  # small-batch and segmented routing
-def test_permute_flags_bad_ids_without_fault(T):
-    E, k, D = 16, 2, 64
+@pytest.mark.parametrize("T,D", [(300, 64), (5000, 64), (5000, 4096)])  # small-batch, segmented, x > 32 MB
+def test_permute_flags_bad_ids_without_fault(T, D):
+    E, k = 16, 2
     ids = torch.randint(0, E, (T, k), dtype=torch.int32, device="cuda")
     ids[7, 1] = E
     ids[100, 0] = -3
@@ -350,6 +351,11 @@ def test_permute_flags_bad_ids_without_fault(T):
     assert int(offsets[E]) == R - 2
     d = dest.cpu().numpy()
     assert d[7 * k + 1] == -1 and d[100 * k] == -1
+    # valid rows copied, the positions past them zero-filled
+    nvalid = int(offsets[E])
+    xc, xpc = x.cpu(), xp.cpu()
+    assert torch.equal(xpc[:nvalid], xc[torch.from_numpy(sr.cpu().numpy()[:nvalid] // k)])
+    assert int(torch.count_nonzero(xpc[nvalid:])) == 0
     assert moe.moe_read_device_status(ws) == 0  # reading clears the word
 
 
