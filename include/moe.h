@@ -40,11 +40,12 @@
  *   for fp8 weights; for bf16 weights two bf16 planes [M, I] -- h_hi =
  *   bf16(h) followed by h_lo = bf16(h - h_hi) -- which the down projection
  *   consumes as two bf16 tensor-core products, so that h keeps about 16
- *   significant bits.  fp8 weights (W8A16) run on the fp16 tensor-core kind:
- *   e4m3 expands exactly to fp16, and the A rows (x, then h) are fp16 rows
- *   times exact powers of two, so the result equals the bf16-activation
- *   product up to fp32 summation order (x exactly; h rounded once to 11
- *   significant bits relative to its row).
+ *   significant bits.  FP8_E4M3 weights (W8A16, in the pages' [.., K, N]
+ *   layout) run on the fp16 tensor-core kind: e4m3 expands exactly to fp16,
+ *   and the A rows (x, then h) are fp16 rows times exact powers of two, so
+ *   each product equals the bf16-activation product up to fp32 summation
+ *   order (x exactly; h rounded once to 11 significant bits relative to its
+ *   row).
  * - FP8_E4M3_NK: the same e4m3 values and per-column scales, with each
  *   expert's matrix stored transposed (W13 [E, 2I, D], W2 [E, D, I], W13s
  *   [2 I_shared, D], W2s [D, I_shared]: the reduction dimension contiguous),
