@@ -223,16 +223,19 @@ def router_planes(T: int, E: int, D: int) -> int:
     return (kb + kbs - 1) // kbs
 
 
-def memory_kernel_bytes(shape, name: str, rows_form_bytes: int):
+def memory_kernel_bytes(shape, name: str, rows_form_bytes: int, nk: bool = False):
     """Algorithmic bytes of one launch of a memory-bound kernel of the layer
     (every tensor it must read or write, once), or None for the GEMMs.
-    rows_form_bytes: bytes per element of the GEMM A rows (2)."""
+    rows_form_bytes: bytes per element of the GEMM A rows (2); nk: fp8
+    weights stored K-contiguous (h in bf16 rather than fp32)."""
     T, D, E, k, I, Is, R = shape.T, shape.D, shape.E, shape.k, shape.I, shape.I_shared, shape.R
     ab = 4 if shape.act_dtype == "f32" else 2
     S = router_planes(T, E, D)
     bias = shape.zipf > 0
     fp8 = shape.w_dtype == "fp8_e4m3"
     gathered = rows_form_bytes if fp8 else ab  # bytes per element of the permuted rows
+    yb = 2 if fp8 else 4  # expert and shared-expert rows: bf16 for fp8 layers, else fp32
+    hb = 2 if (fp8 and nk) else 4  # h as the gate/up pass writes it
     nseg_hist = E * 4 * max(1, (R + 1023) // 1024)
     table = {
         "topk_softmax": S * T * E * 4 + (E * 4 if bias else 0) + (T * E * 4 if (S > 1 or bias) else 0) + 8 * T * k,
@@ -240,13 +243,13 @@ def memory_kernel_bytes(shape, name: str, rows_form_bytes: int):
         "route_scan_scatter": 4 * R + nseg_hist + 8 * E + 8 * R,
         "route_permute": 4 * R + T * D * gathered + R * D * gathered + 8 * R + 8 * E,
         "permute_gather": T * D * gathered + 4 * R + R * D * gathered,
-        "finalize": R * D * 4 + 4 * R + 4 * T * k + (T * D * 4 if Is else 0) + T * D * ab,
+        "finalize": R * D * yb + 4 * R + 4 * T * k + (T * D * yb if Is else 0) + T * D * ab,
     }
     for pre in ("x_to_fp16", "x_to_e4m3x2"):
         table[pre] = T * D * ab + T * D * 2 + 4 * T
     for pre in ("h_to_fp16", "h_to_e4m3x2"):
-        table[pre] = R * I * 4 + R * I * 2 + 4 * R
-        table["shared_" + pre] = T * Is * 4 + T * Is * 2 + 4 * T
+        table[pre] = R * I * hb + R * I * 2 + 4 * R
+        table["shared_" + pre] = T * Is * hb + T * Is * 2 + 4 * T
     return table.get(name)
 
 
@@ -399,7 +402,7 @@ def run_ours(args, world, rank, local):
     pk_hbm = peaks()["hbm_gbs"]
     memory_kernels = {}
     for n, t_us in kernels_us.items():
-        nb = memory_kernel_bytes(shape, n, 2)
+        nb = memory_kernel_bytes(shape, n, 2, nk)
         if nb is not None and t_us > 0:
             gbs = nb / (t_us * 1e3)
             memory_kernels[n] = {"bytes": nb, "us": t_us, "gbs": gbs, "frac_hbm": gbs / pk_hbm}

@@ -37,7 +37,7 @@
  *   y_perm and the shared-expert output are fp32, or bf16 for fp8-weight
  *   layers (one rounding each, inside the 6e-2 RMS bar of those layers).
  *   The intermediate h takes 4 bytes per element: fp32 for fp32 layers and
- *   for fp8 weights; for bf16 weights two bf16 planes [M, I] -- h_hi =
+ *   for FP8_E4M3 weights; for bf16 weights two bf16 planes [M, I] -- h_hi =
  *   bf16(h) followed by h_lo = bf16(h - h_hi) -- which the down projection
  *   consumes as two bf16 tensor-core products, so that h keeps about 16
  *   significant bits.  FP8_E4M3 weights (W8A16, in the pages' [.., K, N]
@@ -56,7 +56,10 @@
  *   terms, hi = e4m3(v) and lo = e4m3(v - hi), multiplied by the weights in
  *   two products into one fp32 accumulator.  A bf16 x is represented exactly
  *   except for elements below 2^-9 of their row's largest, which keep an
- *   absolute error under 2^-17 of it; h keeps 8 significant bits.
+ *   absolute error under 2^-17 of it.  h is stored in bf16 (2 bytes per
+ *   element; 8 significant bits) and reaches the down projection the same
+ *   way, so both products see exactly the bf16 rows but for those small
+ *   elements.
  */
 #ifndef MOE_GB300_H
 #define MOE_GB300_H
@@ -190,9 +193,9 @@ int moe_permute_noalloc(const moe_config_t* cfg, const int32_t* topk_ids, const 
  *   s13     [E, 2I] fp32 per-column scales (fp8 only, else NULL).
  *   W2      [E, I, D] w_dtype (FP8_E4M3_NK: [E, D, I]);
  *   s2      [E, D] fp32 (fp8 only, else NULL).
- *   h       out: act(gate) * up, [T*k, I] fp32 (fp32 layers and fp8 weights)
- *           or the bf16 pair [2, T*k, I] (hi plane, then lo plane) for bf16
- *           weights.
+ *   h       out: act(gate) * up, [T*k, I] fp32 (fp32 layers and FP8_E4M3
+ *           weights), [T*k, I] bf16 (FP8_E4M3_NK weights), or the bf16 pair
+ *           [2, T*k, I] (hi plane, then lo plane) for bf16 weights.
  *   y_perm  [T*k, D] out: h W2 per segment (times s2 for fp8); fp32, or
  *           bf16 for fp8-weight layers (their 6e-2 bar leaves room, and the
  *           combine then reads half the bytes).

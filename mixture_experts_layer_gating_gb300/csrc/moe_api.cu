@@ -152,8 +152,8 @@ Layout make_layout(const moe_config_t* c) {
   L.off[MOE_WS_DEST] = take(R * 4);
   L.seg_scratch = take(E * static_cast<size_t>(route_segments(static_cast<long long>(R))) * 4 + 4);
   L.off[MOE_WS_X_PERM] = take(R * D * ab);
-  L.off[MOE_WS_H] = take(R * I * 4);         // fp32, or bf16 (hi, lo) planes
-  L.off[MOE_WS_Y_PERM] = take(R * D * 4);    // fp32
+  L.off[MOE_WS_H] = take(R * I * 4);         // fp32, bf16 (hi, lo) planes, or bf16
+  L.off[MOE_WS_Y_PERM] = take(R * D * 4);    // fp32 (bf16 rows for fp8 layers)
   L.off[MOE_WS_H_SHARED] = take(T * Is * 4);
   L.off[MOE_WS_S] = take(T * D * 4);
   if (is_fp8(c)) {
@@ -264,8 +264,9 @@ int do_permute(const moe_config_t* c, const int32_t* ids, const void* x, int32_t
 }
 
 // One gated FFN (gate/up + act, then down) over grouped rows.  For fp8
-// weights A holds fp16 rows and a_row_scale their inverse power-of-two scales;
-// h is written in fp32 and converted to fp16 rows (h16, h_inv) for the down pass.
+// weights A holds fp16 (or two-term e4m3) rows and a_row_scale their inverse
+// power-of-two scales; h is written in fp32 (bf16 for K-contiguous weights)
+// and converted to the same row form (h16, h_inv) for the down pass.
 // When a_gather is given, the gate/up pass reads A row a_gather[r] / k of an
 // [a_rows, D] A for output row r (a_row_scale then indexed by that A row).
 int do_ffn(const moe_config_t* c, const void* A, const float* a_row_scale, int M,
@@ -286,8 +287,9 @@ int do_ffn(const moe_config_t* c, const void* A, const float* a_row_scale, int M
     return cuda_status(e);
   }
   // bf16 weights: h is two bf16 planes [M, I], h_hi then h_lo (h ~= h_hi + h_lo),
-  // and the down pass multiplies both.  fp8 weights: h in fp32, then fp16 rows
-  // (or two-term e4m3 rows for K-contiguous weights).
+  // and the down pass multiplies both.  fp8 weights: h in fp32, then fp16 rows;
+  // K-contiguous fp8 weights: h in bf16, then two-term e4m3 rows (exact for a
+  // bf16 row but for its elements below 2^-9 of the row's largest).
   const bool fp8 = is_fp8(c);
   const bool nk = is_nk(c);
   void* h_lo = fp8 ? nullptr : static_cast<uint8_t*>(h) + static_cast<size_t>(M) * I * 2;
@@ -310,7 +312,7 @@ int do_ffn(const moe_config_t* c, const void* A, const float* a_row_scale, int M
   a.b_scale = s13;
   a.out = h;
   a.out_lo = h_lo;
-  a.h_fp32 = fp8;
+  a.h_fp32 = fp8 && !nk;
   a.act = c->act;
   a.pair_ok = 1;
   a.decode_ok = 1;
@@ -319,7 +321,7 @@ int do_ffn(const moe_config_t* c, const void* A, const float* a_row_scale, int M
   if (e != cudaSuccess) return e == cudaErrorNotSupported ? MOE_ERR_UNSUPPORTED : MOE_ERR_CUDA;
   if (fp8) {
     trace_mark(s);
-    if (rows_to_fp8_layer_form(c, h, M, I, h16, h_inv, s, /*src_f32=*/true) != cudaSuccess)
+    if (rows_to_fp8_layer_form(c, h, M, I, h16, h_inv, s, /*src_f32=*/!nk) != cudaSuccess)
       return MOE_ERR_CUDA;
   }
   GroupedGemmArgs b = a;

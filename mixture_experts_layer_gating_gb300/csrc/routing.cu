@@ -562,6 +562,23 @@ __device__ __forceinline__ void load8f(const float* row, int v, float (&f)[8]) {
   f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
 }
 
+// 8 elements from their raw 16-byte words: two words of fp32, or one of bf16
+__device__ __forceinline__ void unpack8(const uint4 (&u)[2], float (&f)[8]) {
+  f[0] = __uint_as_float(u[0].x); f[1] = __uint_as_float(u[0].y);
+  f[2] = __uint_as_float(u[0].z); f[3] = __uint_as_float(u[0].w);
+  f[4] = __uint_as_float(u[1].x); f[5] = __uint_as_float(u[1].y);
+  f[6] = __uint_as_float(u[1].z); f[7] = __uint_as_float(u[1].w);
+}
+__device__ __forceinline__ void unpack8(const uint4 (&u)[1], float (&f)[8]) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u[0]);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 v = __bfloat1622float2(h[i]);
+    f[2 * i] = v.x;
+    f[2 * i + 1] = v.y;
+  }
+}
+
 // Source rows bf16 (exact conversion) or fp32 (rounded once to fp16's 11
 // significant bits, relative to the row maximum's scale).
 template <typename Tin>
@@ -640,6 +657,36 @@ __device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t w) {
 // every bf16 element of magnitude at least 2^-9 of the row's largest, and
 // within 2^-10 (scaled units) below that; fp32 sources keep 8 significant
 // bits.  Output row r: bytes [0, D) hi, [D, 2D) lo; inv_scale[r] = 2^-e.
+
+// the exponent e of a row whose largest magnitude is m (0 for an all-zero row)
+__device__ __forceinline__ int e4m3x2_row_exp(float m) {
+  int e = 0;
+  if (m > 0.0f && isfinite(m)) {
+    int ex;
+    frexpf(m, &ex);  // 2^(ex-1) <= m < 2^ex
+    e = min(100, max(-100, 8 - ex));
+  }
+  return e;
+}
+
+// hi and lo terms of 8 consecutive elements scaled by sc (8 bytes each)
+__device__ __forceinline__ void e4m3x2_terms8(const float (&f)[8], float sc, uint2& hi, uint2& lo) {
+  uint32_t hw[2] = {0u, 0u}, lw[2] = {0u, 0u};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float a = f[2 * i] * sc, b = f[2 * i + 1] * sc;
+    const uint32_t h = f32x2_to_e4m3x2(a, b);
+    const float2 hv = e4m3x2_to_f32x2(h);
+    const uint32_t l = f32x2_to_e4m3x2(a - hv.x, b - hv.y);
+    hw[i >> 1] |= h << (16 * (i & 1));
+    lw[i >> 1] |= l << (16 * (i & 1));
+  }
+  hi = make_uint2(hw[0], hw[1]);
+  lo = make_uint2(lw[0], lw[1]);
+}
+
+// One warp per row; the row is read twice (maximum, then conversion), the
+// second time mostly from cache.  For rows outside the register kernel's range.
 template <typename Tin>
 __global__ void rows_to_e4m3x2_kernel(const Tin* __restrict__ x, int rows, int D,
                                       uint8_t* __restrict__ q, float* __restrict__ inv_scale) {
@@ -671,12 +718,7 @@ __global__ void rows_to_e4m3x2_kernel(const Tin* __restrict__ x, int rows, int D
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(FULL, m, off));
-    int e = 0;
-    if (m > 0.0f && isfinite(m)) {
-      int ex;
-      frexpf(m, &ex);  // 2^(ex-1) <= m < 2^ex
-      e = min(100, max(-100, 8 - ex));
-    }
+    const int e = e4m3x2_row_exp(m);
     const float sc = exp2_int(e);
     if (lane == 0) inv_scale[r] = exp2_int(-e);
     uint8_t* hi_row = q + r * 2 * D;
@@ -685,18 +727,85 @@ __global__ void rows_to_e4m3x2_kernel(const Tin* __restrict__ x, int rows, int D
     for (int v = lane; v < nvec; v += 32) {
       float f[8];
       load8f(src, v, f);
-      uint32_t hw[2] = {0u, 0u}, lw[2] = {0u, 0u};
+      uint2 hw, lw;
+      e4m3x2_terms8(f, sc, hw, lw);
+      *reinterpret_cast<uint2*>(hi_row + 8 * v) = hw;
+      *reinterpret_cast<uint2*>(lo_row + 8 * v) = lw;
+    }
+  }
+}
+
+// The same rows, each held in registers from its maximum to its conversion,
+// so that it is read from memory once: a group of 2^tpr_log2 threads (32 ..
+// 256) per row, up to kRegRowVecs 8-element vectors per thread, 256 >>
+// tpr_log2 rows per block.  Rows of 1024 .. 8192 elements: with a warp per
+// row, the rows in flight on the whole GPU at that length outgrow the L2, and
+// the second pass reads them from HBM again.
+constexpr int kRegRowVecs = 4;
+constexpr int kRegRowBlocksPerSm = 5;  // resident blocks at <= 48 registers, no spills
+template <typename Tin>
+__global__ void __launch_bounds__(256, kRegRowBlocksPerSm) rows_to_e4m3x2_reg_kernel(
+    const Tin* __restrict__ x, int rows, int D, int tpr_log2, uint8_t* __restrict__ q,
+    float* __restrict__ inv_scale) {
+  pdl_wait();
+  pdl_launch_dependents();
+  __shared__ float red[2][8];  // per-warp maxima, two buffers (one barrier per row)
+  const int tpr = 1 << tpr_log2;
+  const int rpb = 256 >> tpr_log2;
+  const int g = threadIdx.x >> tpr_log2, li = threadIdx.x & (tpr - 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int wpr = tpr >> 5;  // warps per row
+  const int nvec = D / 8;
+  int buf = 0;
+  // every thread of the block runs the same iterations (the barrier below)
+  for (long long base = static_cast<long long>(blockIdx.x) * rpb; base < rows;
+       base += static_cast<long long>(gridDim.x) * rpb) {
+    const long long r = base + g;
+    const bool valid = r < rows;
+    const Tin* src = x + (valid ? r : 0) * D;
+    // the row's 8-element vectors as loaded (one or two 16-byte words each)
+    constexpr int kWords = sizeof(Tin) == 4 ? 2 : 1;
+    uint4 raw[kRegRowVecs][kWords];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float a = f[2 * i] * sc, b = f[2 * i + 1] * sc;
-        const uint32_t h = f32x2_to_e4m3x2(a, b);
-        const float2 hv = e4m3x2_to_f32x2(h);
-        const uint32_t l = f32x2_to_e4m3x2(a - hv.x, b - hv.y);
-        hw[i >> 1] |= h << (16 * (i & 1));
-        lw[i >> 1] |= l << (16 * (i & 1));
+    for (int j = 0; j < kRegRowVecs; ++j) {
+      const int v = li + tpr * j;
+#pragma unroll
+      for (int w = 0; w < kWords; ++w)
+        raw[j][w] = (valid && v < nvec) ? __ldcs(reinterpret_cast<const uint4*>(src) + kWords * v + w)
+                                        : make_uint4(0u, 0u, 0u, 0u);
+    }
+    float m = 0.0f;
+#pragma unroll
+    for (int j = 0; j < kRegRowVecs; ++j) {
+      float f[8];
+      unpack8(raw[j], f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(f[i]));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(FULL, m, off));
+    if (lane == 0) red[buf][warp] = m;
+    __syncthreads();
+    m = red[buf][g * wpr];
+    for (int w = 1; w < wpr; ++w) m = fmaxf(m, red[buf][g * wpr + w]);
+    buf ^= 1;
+    if (!valid) continue;
+    const int e = e4m3x2_row_exp(m);
+    const float sc = exp2_int(e);
+    if (li == 0) inv_scale[r] = exp2_int(-e);
+    uint8_t* hi_row = q + r * 2 * D;
+    uint8_t* lo_row = hi_row + D;
+#pragma unroll
+    for (int j = 0; j < kRegRowVecs; ++j) {
+      const int v = li + tpr * j;
+      if (v < nvec) {
+        float f[8];
+        unpack8(raw[j], f);
+        uint2 hw, lw;
+        e4m3x2_terms8(f, sc, hw, lw);
+        *reinterpret_cast<uint2*>(hi_row + 8 * v) = hw;
+        *reinterpret_cast<uint2*>(lo_row + 8 * v) = lw;
       }
-      *reinterpret_cast<uint2*>(hi_row + 8 * v) = make_uint2(hw[0], hw[1]);
-      *reinterpret_cast<uint2*>(lo_row + 8 * v) = make_uint2(lw[0], lw[1]);
     }
   }
 }
@@ -769,23 +878,6 @@ __device__ __forceinline__ void store8(float* p, const float (&f)[8]) {
 
 // Ty: the type of the expert rows and the shared row (fp32, or bf16 for
 // fp8-weight layers).
-// 8 elements from their raw 16-byte words: two words of fp32, or one of bf16
-__device__ __forceinline__ void unpack8(const uint4 (&u)[2], float (&f)[8]) {
-  f[0] = __uint_as_float(u[0].x); f[1] = __uint_as_float(u[0].y);
-  f[2] = __uint_as_float(u[0].z); f[3] = __uint_as_float(u[0].w);
-  f[4] = __uint_as_float(u[1].x); f[5] = __uint_as_float(u[1].y);
-  f[6] = __uint_as_float(u[1].z); f[7] = __uint_as_float(u[1].w);
-}
-__device__ __forceinline__ void unpack8(const uint4 (&u)[1], float (&f)[8]) {
-  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u[0]);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 v = __bfloat1622float2(h[i]);
-    f[2 * i] = v.x;
-    f[2 * i + 1] = v.y;
-  }
-}
-
 template <typename Tt, int KMAX, typename Ty>
 __global__ void finalize_kernel(const Ty* __restrict__ y_perm, const int32_t* __restrict__ dest,
                                 const float* __restrict__ w, const Ty* __restrict__ s_rows,
@@ -996,6 +1088,22 @@ cudaError_t launch_rows_to_e4m3x2(const void* x, int rows, int D, void* q, float
                                   cudaStream_t s, bool src_f32) {
   if (rows <= 0) return cudaSuccess;
   const int threads = 256;
+  const int nvec = D / 8;
+  if (nvec >= 128 && nvec <= 256 * kRegRowVecs) {
+    int tpr_log2 = 5;  // the smallest group that holds the row: 32 .. 256 threads
+    while ((1 << tpr_log2) * kRegRowVecs < nvec) ++tpr_log2;
+    const int blocks =
+        blocks_for(rows, threads >> tpr_log2, device_sm_count() * kRegRowBlocksPerSm);
+    if (src_f32)
+      MOE_LAUNCH(rows_to_e4m3x2_reg_kernel<float>, blocks, threads, 0, s,
+                 static_cast<const float*>(x), rows, D, tpr_log2, static_cast<uint8_t*>(q),
+                 inv_scale);
+    else
+      MOE_LAUNCH(rows_to_e4m3x2_reg_kernel<__nv_bfloat16>, blocks, threads, 0, s,
+                 static_cast<const __nv_bfloat16*>(x), rows, D, tpr_log2,
+                 static_cast<uint8_t*>(q), inv_scale);
+    return cudaGetLastError();
+  }
   const int blocks = blocks_for(rows, threads / 32, device_sm_count() * 16);
   if (src_f32)
     MOE_LAUNCH(rows_to_e4m3x2_kernel<float>, blocks, threads, 0, s, static_cast<const float*>(x),

@@ -91,3 +91,29 @@ def test_max_over_ranks_two_gloo_ranks():
         out = m.dict()
         mp.spawn(_rank_main, args=(2, _free_port(), out), nprocs=2, join=True)
         assert dict(out) == {0: 2.5, 1: 2.5}
+
+
+def test_memory_kernel_bytes_follow_the_row_types():
+    """The algorithmic bytes bench.py divides by the event-timed duration:
+    finalize reads fp32 expert and shared rows for bf16 weights and bf16 rows
+    for fp8 weights; the h conversion reads fp32 h, or bf16 h for fp8 weights
+    stored K-contiguous."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import workloads
+
+    q = workloads.CONFIGS["qwen3_prefill"]
+    T, D, k, R = q.T, q.D, q.k, q.R
+    assert bench.memory_kernel_bytes(q, "finalize", 2) == R * D * 4 + 4 * R + 4 * T * k + T * D * 2
+    assert bench.memory_kernel_bytes(q, "w13_gate_up", 2) is None
+    ling = workloads.CONFIGS["ling_prefill"]
+    T, D, k, R, I, Is = ling.T, ling.D, ling.k, ling.R, ling.I, ling.I_shared
+    for nk in (False, True):
+        assert bench.memory_kernel_bytes(ling, "finalize", 2, nk) == \
+            R * D * 2 + 4 * R + 4 * T * k + T * D * 2 + T * D * 2
+        assert bench.memory_kernel_bytes(ling, "x_to_e4m3x2", 2, nk) == T * D * 2 + T * D * 2 + 4 * T
+    hb = {False: 4, True: 2}
+    for nk in (False, True):
+        assert bench.memory_kernel_bytes(ling, "h_to_e4m3x2", 2, nk) == R * I * hb[nk] + R * I * 2 + 4 * R
+        assert bench.memory_kernel_bytes(ling, "shared_h_to_e4m3x2", 2, nk) == \
+            T * Is * hb[nk] + T * Is * 2 + 4 * T

@@ -40,9 +40,9 @@ def test_pack_weights_nk_rejects_bad_shapes():
 
 
 def two_term_rows(h):
-    """Emulates the library's fp32 rows -> two-term e4m3 rows: a power of two
-    2^e with the row's largest |h| * 2^e in [128, 256), hi = e4m3(v), lo =
-    e4m3(v - hi), round to nearest even; returns (hi + lo) / 2^e in fp64."""
+    """Emulates the library's bf16 / fp32 rows -> two-term e4m3 rows: a power
+    of two 2^e with the row's largest |h| * 2^e in [128, 256), hi = e4m3(v),
+    lo = e4m3(v - hi), round to nearest even; returns (hi + lo) / 2^e in fp64."""
     h = h.float()
     m = h.abs().amax(dim=1, keepdim=True)
     e = torch.where(m > 0, 8 - torch.frexp(m).exponent, torch.zeros_like(m, dtype=torch.int32))
@@ -65,21 +65,21 @@ GROUPED_CASES = [
 
 @pytest.mark.parametrize("E,counts,D,I,act", GROUPED_CASES)
 def test_grouped_ffn_nk_parity(E, counts, D, I, act, tile_mode):
-    """h (fp32) against the oracle from x carried exactly by its two-term rows;
-    y (bf16) against the GPU's own h, rounded as the library rounds it to
-    two-term rows, times the dequantised W2 (one bf16 rounding)."""
+    """h (bf16: one rounding) against the oracle from x carried exactly by its
+    two-term rows; y (bf16) against the GPU's own h, rounded as the library
+    rounds it to two-term rows, times the dequantised W2 (one bf16 rounding)."""
     xp, offsets, W13, W2, s13, s2 = _grouped_case(E, counts, D, I, act, seed=E + D + I + 5, fp8=True)
     R = xp.shape[0]
     cfg = moe.make_config(R, D, E, 1, I, act=act, w_dtype="fp8_e4m3_nk")
     ws = moe.alloc_workspace(cfg)
-    h = torch.empty((R, I), dtype=torch.float32, device="cuda")
+    h = torch.empty((R, I), dtype=torch.bfloat16, device="cuda")  # K-contiguous fp8: bf16 h
     y = torch.empty((R, D), dtype=torch.bfloat16, device="cuda")  # fp8 layers: bf16 expert rows
     moe.moe_grouped_ffn(cfg, xp, torch.from_numpy(offsets).cuda(), moe.pack_weights_nk(W13), s13,
                         moe.pack_weights_nk(W2), s2, h, y, ws=ws)
     assert moe.moe_read_device_status(ws) == 0
     h_o, y_o = oracle.grouped_ffn(oracle.to_f64(xp.cpu()), offsets, W13.cpu(), W2.cpu(), act,
                                   s13.cpu(), s2.cpu())
-    check_close("h", h.cpu().double().numpy(), h_o, 1e-4, 1e-4)
+    check_close("h", h.cpu().double().numpy(), h_o, 2.0 ** -8, 1e-4)
     hq = two_term_rows(h.cpu()).numpy()
     y_ref = np.zeros((R, D))
     for e in range(E):
@@ -107,14 +107,14 @@ def test_grouped_ffn_nk_tail_sizes(act, pair_mode):
         R = xp.shape[0]
         cfg = moe.make_config(R, D, E, 1, I, act=act, w_dtype="fp8_e4m3_nk")
         ws = moe.alloc_workspace(cfg)
-        h = torch.empty((R, I), dtype=torch.float32, device="cuda")
+        h = torch.empty((R, I), dtype=torch.bfloat16, device="cuda")  # K-contiguous fp8: bf16 h
         y = torch.empty((R, D), dtype=torch.bfloat16, device="cuda")  # fp8 layers: bf16 expert rows
         moe.moe_grouped_ffn(cfg, xp, torch.from_numpy(offsets).cuda(), moe.pack_weights_nk(W13), s13,
                             moe.pack_weights_nk(W2), s2, h, y, ws=ws)
         assert moe.moe_read_device_status(ws) == 0
         h_o, _ = oracle.grouped_ffn(oracle.to_f64(xp.cpu()), offsets, W13.cpu(), W2.cpu(), act,
                                     s13.cpu(), s2.cpu())
-        check_close("h", h.cpu().double().numpy(), h_o, 1e-4, 1e-4)
+        check_close("h", h.cpu().double().numpy(), h_o, 2.0 ** -8, 1e-4)
         hq = two_term_rows(h.cpu()).numpy()
         y_ref = np.zeros((R, D))
         for e in range(E):
@@ -150,14 +150,14 @@ def test_nk_weights_with_subnormal_codes(tile_mode):
     offsets = np.array([0, counts[0], R], dtype=np.int32)
     cfg = moe.make_config(R, D, E, 1, I, w_dtype="fp8_e4m3_nk")
     ws = moe.alloc_workspace(cfg)
-    h = torch.empty((R, I), dtype=torch.float32, device="cuda")
+    h = torch.empty((R, I), dtype=torch.bfloat16, device="cuda")  # K-contiguous fp8: bf16 h
     y = torch.empty((R, D), dtype=torch.bfloat16, device="cuda")  # fp8 layers: bf16 expert rows
     moe.moe_grouped_ffn(cfg, xp, torch.from_numpy(offsets).cuda(), moe.pack_weights_nk(W13), s13,
                         moe.pack_weights_nk(W2), s2, h, y, ws=ws)
     assert moe.moe_read_device_status(ws) == 0
     h_o, _ = oracle.grouped_ffn(oracle.to_f64(xp.cpu()), offsets, W13.cpu(), W2.cpu(), "swiglu",
                                 s13.cpu(), s2.cpu())
-    check_close("h", h.cpu().double().numpy(), h_o, 1e-4, 1e-4)
+    check_close("h", h.cpu().double().numpy(), h_o, 2.0 ** -8, 1e-4)
     hq = two_term_rows(h.cpu()).numpy()
     y_ref = np.zeros((R, D))
     for e in range(E):
@@ -174,6 +174,10 @@ NK_LAYERS = {
     # 512 rows per group: 2-CTA tiles by default
     "fp8_T2048": workloads.MoEShape("fp8_T2048", 2048, 512, 16, 4, 256, I_shared=256, w_dtype="fp8_e4m3"),
     "ling_T1": LAYER_CASES["ling_T64"].with_tokens(1),
+    # rows of 1040 and 1296 elements: thread groups of 64 whose last vectors
+    # run past the row (the register-resident row conversion), ragged N tiles
+    "fp8_rows_1040_1296": workloads.MoEShape("fp8_rows", 300, 1040, 8, 2, 1296, I_shared=1040,
+                                             w_dtype="fp8_e4m3"),
 }
 
 

@@ -584,9 +584,10 @@ def test_stage_calls_match_moe_layer(case, layout):
     x_perm = torch.empty((R, D), dtype=adt, device=dev)
     moe.moe_permute(cfg, ids, inp["x"], counts, offsets, sorted_rows, dest, x_perm, ws)
     fp8 = shape.w_dtype == "fp8_e4m3"
-    h = (torch.empty((R, I), dtype=torch.float32, device=dev) if fp8
+    hdt = torch.bfloat16 if layout == "nk" else torch.float32  # fp8 layers' h
+    h = (torch.empty((R, I), dtype=hdt, device=dev) if fp8
          else torch.empty((2, R, I), dtype=torch.bfloat16, device=dev))
-    h_s = (torch.empty((T, Is), dtype=torch.float32, device=dev) if fp8
+    h_s = (torch.empty((T, Is), dtype=hdt, device=dev) if fp8
            else torch.empty((2, T, Is), dtype=torch.bfloat16, device=dev))
     ydt = torch.bfloat16 if fp8 else torch.float32  # fp8 layers: bf16 expert and shared rows
     y = torch.empty((R, D), dtype=ydt, device=dev)
