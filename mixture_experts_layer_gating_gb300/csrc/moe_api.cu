@@ -203,21 +203,28 @@ int do_route(const moe_config_t* c, const void* x, const void* Wg, const float* 
       bias = nullptr;  // added by the projection
     } else {
       nsplit = partials ? router_k_split(c->T, c->E, c->D) : 1;
-      GroupedGemmArgs a{};
-      a.epilogue = kEpiStoreF32;
-      a.A = x;
-      a.M = c->T;
-      a.K = c->D;
-      a.group_offsets = nullptr;
-      a.G = 1;
-      a.B = Wg;
-      a.N = c->E;
-      a.bias = nullptr;  // added, after the split planes, by the top-k kernel
-      a.ksplit = nsplit;
-      a.out = nsplit > 1 ? partials : logits;
-      a.err = err;
-      e = launch_grouped_gemm(a, s);
-      src = nsplit > 1 ? partials : logits;
+      float* dst = nsplit > 1 ? partials : logits;
+      if (router_small_ok(c->T, c->E, c->D, nsplit)) {
+        // a few tokens: a matrix-vector product per token on the CUDA cores,
+        // into the same split planes
+        e = launch_router_small(x, Wg, c->T, c->D, c->E, nsplit, dst, s);
+      } else {
+        GroupedGemmArgs a{};
+        a.epilogue = kEpiStoreF32;
+        a.A = x;
+        a.M = c->T;
+        a.K = c->D;
+        a.group_offsets = nullptr;
+        a.G = 1;
+        a.B = Wg;
+        a.N = c->E;
+        a.bias = nullptr;  // added, after the split planes, by the top-k kernel
+        a.ksplit = nsplit;
+        a.out = dst;
+        a.err = err;
+        e = launch_grouped_gemm(a, s);
+      }
+      src = dst;
     }
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   } else {

@@ -89,6 +89,12 @@ cudaError_t launch_topk_softmax(const float* partials, int nsplit, const float* 
 // Split-K factor of the router projection (a pure function of the shape, so
 // the workspace size does not depend on the device).
 int router_k_split(int T, int E, int D);
+// Small batches (decode): the router projection on the CUDA cores, written as
+// nsplit fp32 planes [nsplit, T, E] over consecutive slices of D (bf16 x and
+// W_g, E even).  router_small_ok says whether a shape takes this path.
+bool router_small_ok(int T, int E, int D, int nsplit);
+cudaError_t launch_router_small(const void* x, const void* Wg, int T, int D, int E, int nsplit,
+                                float* planes, cudaStream_t s);
 // `mark`, when not null, is called on the stream right before each of the
 // three launches (trace hook of moe_layer).
 cudaError_t launch_init_routing(const int32_t* ids, int R, int E, int32_t* counts, int32_t* offsets,

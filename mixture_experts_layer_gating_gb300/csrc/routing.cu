@@ -144,6 +144,91 @@ __global__ void topk_softmax_kernel(const float* __restrict__ partials, int nspl
 }
 
 // ------------------------------------------------------------------------
+// Router projection for small batches ("CANN/cann-recipes-infer：Qwen3-MoE优化",
+// the gate GEMM in fp32; "千问 3.5 MoE 在 TPU 上的系统优化实战": decode is bound by
+// reading weights).  At a few tokens the projection is a matrix-vector product
+// per token bounded by reading W_g, and a 128-row tensor-core tile would be
+// almost empty, so it runs on the CUDA cores:
+//   planes[s][t][e] = sum over d in slice s of x[t][d] * W_g[d][e]
+// with slice s = [s*dc, min(D, (s+1)*dc)).  A block takes 64 experts (two per
+// lane), one slice and kRouterTok tokens; its kRouterWarps warps split the
+// slice into contiguous pieces (fp32 FMA in ascending d inside a piece), and
+// the pieces are added in warp order.  The top-k kernel sums the planes in
+// plane order and adds the bias.
+constexpr int kRouterTok = 4;
+constexpr int kRouterWarps = 8;
+constexpr int kRouterMaxSlice = 1024;  // d per plane staged in shared memory
+constexpr int kRouterUnroll = 16;      // W_g loads in flight per lane
+
+__global__ void __launch_bounds__(kRouterWarps * 32)
+    router_small_kernel(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ Wg,
+                        int T, int D, int E, int dc, float* __restrict__ planes) {
+  pdl_wait();
+  pdl_launch_dependents();
+  __shared__ float4 xs[kRouterMaxSlice];                   // x[t0 + j][d0 + i], j = 0..3
+  __shared__ float2 part[kRouterWarps][kRouterTok][32];  // per-warp sums, two experts a lane
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int s = blockIdx.y;
+  const int t0 = blockIdx.z * kRouterTok;
+  const int d0 = s * dc;
+  const int n = max(0, min(D, d0 + dc) - d0);
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    float v[kRouterTok];
+#pragma unroll
+    for (int j = 0; j < kRouterTok; ++j)
+      v[j] = t0 + j < T ? __bfloat162float(x[static_cast<size_t>(t0 + j) * D + d0 + i]) : 0.0f;
+    xs[i] = make_float4(v[0], v[1], v[2], v[3]);
+  }
+  __syncthreads();
+  const int e = blockIdx.x * 64 + 2 * lane;  // this lane's experts e, e + 1
+  const int per = (n + kRouterWarps - 1) / kRouterWarps;
+  const int i0 = min(n, wid * per), i1 = min(n, i0 + per);
+  float a0[kRouterTok] = {0.0f, 0.0f, 0.0f, 0.0f}, a1[kRouterTok] = {0.0f, 0.0f, 0.0f, 0.0f};
+  if (e < E) {
+    const __nv_bfloat162* wp = reinterpret_cast<const __nv_bfloat162*>(Wg + static_cast<size_t>(d0) * E + e);
+    const size_t stride = static_cast<size_t>(E) / 2;  // one W_g row in bf16 pairs
+    for (int i = i0; i < i1; i += kRouterUnroll) {
+      __nv_bfloat162 w[kRouterUnroll];
+#pragma unroll
+      for (int u = 0; u < kRouterUnroll; ++u)
+        w[u] = i + u < i1 ? wp[static_cast<size_t>(i + u) * stride] : __floats2bfloat162_rn(0.0f, 0.0f);
+#pragma unroll
+      for (int u = 0; u < kRouterUnroll; ++u) {
+        if (i + u < i1) {
+          const float2 wf = __bfloat1622float2(w[u]);
+          const float4 xv = xs[i + u];
+          a0[0] = fmaf(xv.x, wf.x, a0[0]);
+          a0[1] = fmaf(xv.y, wf.x, a0[1]);
+          a0[2] = fmaf(xv.z, wf.x, a0[2]);
+          a0[3] = fmaf(xv.w, wf.x, a0[3]);
+          a1[0] = fmaf(xv.x, wf.y, a1[0]);
+          a1[1] = fmaf(xv.y, wf.y, a1[1]);
+          a1[2] = fmaf(xv.z, wf.y, a1[2]);
+          a1[3] = fmaf(xv.w, wf.y, a1[3]);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < kRouterTok; ++j) part[wid][j][lane] = make_float2(a0[j], a1[j]);
+  __syncthreads();
+  if (wid < kRouterTok) {  // warp j writes token t0 + j
+    const int t = t0 + wid;
+    if (t < T && e < E) {
+      float2 sum = part[0][wid][lane];
+#pragma unroll
+      for (int w = 1; w < kRouterWarps; ++w) {
+        sum.x += part[w][wid][lane].x;
+        sum.y += part[w][wid][lane].y;
+      }
+      float* o = planes + (static_cast<size_t>(s) * T + t) * E + e;
+      o[0] = sum.x;
+      o[1] = sum.y;
+    }
+  }
+}
+
+// ------------------------------------------------------------------------
 // init_routing ("CANN/cann-recipes-infer：Qwen3-MoE优化", section
 // "GMM使能和Routing优化": npu_moe_init_routing + npu_moe_compute_expert_tokens).
 // A stable counting sort of the expanded rows r = t*k + j by expert id, in two
@@ -995,6 +1080,25 @@ cudaError_t launch_topk_softmax(const float* partials, int nsplit, const float* 
   else
     MOE_LAUNCH(topk_softmax_kernel<16>, blocks, threads, 0, s, partials, nsplit, bias, logits, T,
                E, k, renorm, ids, w, err);
+  return cudaGetLastError();
+}
+
+// Up to 64 tokens and 2^25 multiply-adds (x W_g of Qwen3- and Gemma-4-style
+// decode batches), with every slice staged in shared memory.
+bool router_small_ok(int T, int E, int D, int nsplit) {
+  if (T <= 0 || T > 64 || E <= 0 || (E & 1) || nsplit < 1) return false;
+  if (static_cast<long long>(T) * D * E > (1ll << 25)) return false;
+  return (D + nsplit - 1) / nsplit <= kRouterMaxSlice;
+}
+
+cudaError_t launch_router_small(const void* x, const void* Wg, int T, int D, int E, int nsplit,
+                                float* planes, cudaStream_t s) {
+  if (!router_small_ok(T, E, D, nsplit)) return cudaErrorInvalidValue;
+  const int dc = (D + nsplit - 1) / nsplit;
+  const dim3 grid((E + 63) / 64, nsplit, (T + kRouterTok - 1) / kRouterTok);
+  MOE_LAUNCH(router_small_kernel, grid, kRouterWarps * 32, 0, s,
+             static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(Wg), T, D, E,
+             dc, planes);
   return cudaGetLastError();
 }
 

@@ -250,23 +250,27 @@ def test_route_from_logits_bit_exact(E, k, renorm):
     assert np.array_equal(ids[5].cpu().numpy(), np.arange(k))
 
 
-@pytest.mark.parametrize("T,E,k,renorm,bias", [
-    (2048, 64, 4, 1, False), (2048, 256, 16, 0, True), (3000, 128, 8, 1, True),  # fused top-k
-    (2047, 64, 4, 1, False), (512, 256, 8, 0, True),                           # split-K + top-k kernel
+@pytest.mark.parametrize("T,E,k,renorm,bias,D", [
+    (2048, 64, 4, 1, False, 256), (2048, 256, 16, 0, True, 256), (3000, 128, 8, 1, True, 256),
+    (2047, 64, 4, 1, False, 256), (512, 256, 8, 0, True, 256), (512, 128, 8, 1, True, 2048),
+    # up to 64 tokens: the CUDA-core projection (one plane at D = 256, else 4-8
+    # planes over slices of D, the last slices shorter or empty)
+    (64, 128, 8, 1, False, 2048), (8, 128, 8, 1, True, 2816), (1, 128, 8, 1, False, 2048),
+    (3, 512, 10, 0, True, 4096), (33, 64, 4, 1, True, 256), (64, 512, 16, 1, False, 1024),
+    (65, 128, 8, 1, False, 2048),  # one token past it: the tensor-core projection
 ])
-def test_route_projection_then_topk_bit_exact(T, E, k, renorm, bias):
+def test_route_projection_then_topk_bit_exact(T, E, k, renorm, bias, D):
     """moe_route from x and W_g: routing bit-exact against the oracle's top-k of
     the GPU's own logits, logits against the fp64 projection.  Duplicate
-    columns of W_g make exact ties that the lowest expert index must win; at
-    >= 2048 tokens and <= 256 experts the top-k runs in the projection's epilogue."""
-    D = 256
-    gen = torch.Generator(device="cuda").manual_seed(T + E + k)
+    columns of W_g make exact ties that the lowest expert index must win."""
+    gen = torch.Generator(device="cuda").manual_seed(T + E + k + D)
     x = torch.randn((T, D), generator=gen, device="cuda").to(torch.bfloat16)
     Wg = (0.05 * torch.randn((D, E), generator=gen, device="cuda")).to(torch.bfloat16)
     Wg[:, 5] = Wg[:, 3]
     Wg[:, 11] = Wg[:, 10]
     Wg[:, 12] = Wg[:, 10]
-    x[7] = 0  # a token whose logits are all equal (zero, plus the bias)
+    tz = min(7, T - 1)
+    x[tz] = 0  # a token whose logits are all equal (zero, plus the bias)
     b = (0.01 * torch.randn((E,), generator=gen, device="cuda")) if bias else None
     if bias:
         b[5] = b[3]
@@ -286,7 +290,7 @@ def test_route_projection_then_topk_bit_exact(T, E, k, renorm, bias):
     L_ref = oracle.router_logits(x.cpu(), Wg.cpu(), b.cpu() if bias else None)
     assert np.max(np.abs(L_gpu - L_ref)) <= 1e-3 * max(1.0, rms(L_ref))
     if not bias:
-        assert np.array_equal(ids[7].cpu().numpy(), np.arange(k))
+        assert np.array_equal(ids[tz].cpu().numpy(), np.arange(k))
 
 
 @pytest.mark.parametrize("T,E,k,pattern,D", [
