@@ -16,7 +16,6 @@ namespace moe {
 namespace {
 
 constexpr unsigned FULL = 0xffffffffu;
-constexpr int kMaxTopK = 16;
 
 // ------------------------------------------------------------------------
 // gating_top_k_softmax ("CANN/cann-recipes-infer：Qwen3-MoE优化", section
@@ -930,25 +929,10 @@ __global__ void transpose_bytes_kernel(const uint8_t* __restrict__ W, int K, int
 // "GMM使能和Routing优化") fused with the shared-expert add ("千问 3.5 MoE 在
 // TPU 上的系统优化实战": y = Router(x) + SharedExpert(x)).  One warp per
 // (token, m 256-column slices): m is chosen so that small batches still
-// spread over every SM while large ones keep whole rows per warp; fp32
-// expert rows and shared row, fp32 accumulation with j ascending,
-// shared row last, one rounding to the output type.
-__device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&f)[8]) {
-  const uint4 u = *reinterpret_cast<const uint4*>(p);
-  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 v = __bfloat1622float2(h[i]);
-    f[2 * i] = v.x;
-    f[2 * i + 1] = v.y;
-  }
-}
-__device__ __forceinline__ void load8(const float* p, float (&f)[8]) {
-  const float4 a = *reinterpret_cast<const float4*>(p);
-  const float4 b = *reinterpret_cast<const float4*>(p + 4);
-  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
-  f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
-}
+// spread over every SM while large ones keep whole rows per warp; expert
+// rows and shared row in fp32 (bf16 for fp8-weight layers), fp32
+// accumulation with j ascending, shared row last, one rounding to the output
+// type.
 __device__ __forceinline__ void store8(__nv_bfloat16* p, const float (&f)[8]) {
   uint4 u;
   __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
