@@ -1,8 +1,12 @@
-// Routing-side kernels of the MoE layer: gating top-k softmax, init_routing
-// (histogram, exclusive scan, stable scatter), the permutation gather and the
-// finalize (weighted un-permute + shared-expert add).  All are memory-bound;
-// they move 16-byte vectors and keep every index bounds-checked so that bad
-// input data is reported through the error word instead of faulting.
+// Routing-side kernels of the MoE layer: the router projection of small
+// batches (CUDA cores), gating top-k softmax, init_routing (histogram,
+// exclusive scan, stable scatter), the permutation (gather or token-side
+// scatter), the fp8 layers' row forms (fp16 or two-term e4m3 rows with
+// power-of-two scales), the one-time fp8 weight transpose and the finalize
+// (weighted un-permute + shared-expert add).  All are memory- or
+// latency-bound; they move 16-byte vectors and keep every index
+// bounds-checked so that bad input data is reported through the error word
+// instead of faulting.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
