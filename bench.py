@@ -3,8 +3,11 @@
 A step is one whole moe_layer call (router projection, top-k softmax,
 init_routing, permutation gather, grouped gate/up + activation, grouped down
 projection, shared expert when present, finalize) over one batch of T tokens
-already resident in HBM.  Default workload: the Qwen3-MoE-style prefill layer
-(T=4096, D=2048, E=128, top-8, I=768, bf16).
+already resident in HBM.  Default workload: the largest configured layer that
+fits one GPU, the Ling-2.6-1T-style prefill layer (T=16384, D=8192, E=256,
+top-8, I=2048, one shared expert of 2048, e4m3 weights with per-column scales,
+bf16 activations); the Qwen3-MoE-style prefill layer (T=4096, D=2048, E=128,
+top-8, I=768, bf16) is timed in the same run as a secondary line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                   [--impl ours|reference] [--no-cpu-baseline]
@@ -196,7 +199,7 @@ def cpu_baseline(shape, inp_cpu, budget_s: float = 15.0):
     """Time the oracle, as it stands, on a bounded sample of about budget_s:
     the first n tokens of the batch (n grown until one call takes the budget),
     or the whole batch repeated when one pass is shorter than the budget."""
-    n = min(shape.T, 128)
+    n = min(shape.T, 16)
     while True:
         dt = time_oracle(shape, inp_cpu, n)
         if dt >= budget_s or n == shape.T:
@@ -273,15 +276,18 @@ def run_reference(args, world, rank):
         {k: (v.cpu() if isinstance(v, torch.Tensor) else v)
          for k, v in workloads.make_inputs(shape, seed=0, device="cuda").items()}
     # each step: the oracle on a bounded sample so the whole run stays within
-    # minutes -- the first n tokens, n grown from 64 (one call is also the first
-    # warm-up) while a call stays under --ref-step-s and n < T
+    # minutes -- the first n tokens, n doubled from 1 (one call is also the
+    # first warm-up) while a call stays under half the per-step target and
+    # n < T; the target is --ref-step-s, lowered so that all warm-up and timed
+    # steps take about --ref-total-s
+    step_s = min(args.ref_step_s, args.ref_total_s / max(1, args.steps + args.warmup))
     if args.ref_tokens:
         n = min(shape.T, args.ref_tokens)
         done = 0
     else:
-        n = min(shape.T, 64)
+        n = 1
         dt = time_oracle(shape, inp, n)
-        while n < shape.T and dt < 0.5 * args.ref_step_s:
+        while n < shape.T and dt < 0.5 * step_s:
             n = min(shape.T, 2 * n)
             dt = time_oracle(shape, inp, n)
         done = 1
@@ -303,14 +309,7 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
-def run_ours(args, world, rank, local):
-    import mixture_experts_layer_gating_gb300 as moe
-    from mixture_experts_layer_gating_gb300 import _build
-
-    if rank == 0 or not os.path.exists(moe.LIB_PATH):
-        _build.build()
-    barrier(world)
-    moe.load_library()
+def set_options(moe, args):
     if args.pair_tiles is not None:
         moe.moe_set_option(moe.MOE_OPT_PAIR_TILES, args.pair_tiles)
     if args.gather_a:
@@ -321,7 +320,42 @@ def run_ours(args, world, rank, local):
         moe.moe_set_option(moe.MOE_OPT_PDL, 0)
     if args.serial_shared:
         moe.moe_set_option(moe.MOE_OPT_SHARED_STREAM, 0)
-    shape = workload_shape(args)
+
+
+def pct(v, q):
+    """q-th percentile (linear interpolation) of a list."""
+    v = sorted(v)
+    if not v:
+        return None
+    pos = (len(v) - 1) * q / 100.0
+    lo = int(pos)
+    hi = min(lo + 1, len(v) - 1)
+    return v[lo] + (v[hi] - v[lo]) * (pos - lo)
+
+
+def kernel_names(shape, nk, gather_a):
+    """Names of the kernels one moe_layer call launches, in launch order."""
+    fp8 = shape.w_dtype == "fp8_e4m3"
+    rows = "e4m3x2" if nk else "fp16"  # the A-row form of fp8 layers
+    names = ([f"x_to_{rows}"] if fp8 else []) + ["router_gemm", "topk_softmax"]
+    if shape.R <= 8192:  # small batches: init_routing + gather in one kernel
+        names += ["route_permute"]
+    else:
+        names += ["route_hist", "route_scan_scatter"]
+        names += ["permute_gather"] if (shape.act_dtype == "f32" or not gather_a) else []
+    names += ["w13_gate_up"]
+    names += [f"h_to_{rows}"] if fp8 else []
+    names += ["w2_down"]
+    if shape.I_shared:
+        names += ["shared_w13"] + ([f"shared_h_to_{rows}"] if fp8 else []) + ["shared_w2"]
+    names += ["finalize"]
+    return names
+
+
+def measure(args, world, rank, local, shape, primary: bool):
+    """Time moe_layer on one workload; returns the fields of a bench line."""
+    import mixture_experts_layer_gating_gb300 as moe
+
     dev = torch.device("cuda", local)
     inp = workloads.make_inputs(shape, seed=rank, device=dev, weights_seed=0)
     fp8 = shape.w_dtype == "fp8_e4m3"
@@ -354,38 +388,39 @@ def run_ours(args, world, rank, local):
     if flags:
         raise RuntimeError(f"device error flags {flags:#x}")
 
-    # ---- device-resident timed region
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize()
+    # ---- device-resident timed region: exactly K steps, an event before each
+    # (per-step durations for the percentiles), barrier + synchronize around
+    def timed_loop(n):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+        barrier(world)
+        torch.cuda.synchronize()
+        for i in range(n):
+            evs[i].record(stream)
+            step()
+        evs[n].record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        return evs[0].elapsed_time(evs[n]), [evs[i].elapsed_time(evs[i + 1]) for i in range(n)]
+
     sampler.mark("start")
-    ev0.record(stream)
-    for _ in range(args.steps):
-        step()
-    ev1.record(stream)
-    torch.cuda.synchronize()
+    t_ms, per_step = timed_loop(args.steps)
+    # percentiles over at least --min-window-ms of steps: the K timed steps,
+    # extended by further loops of K steps when they are shorter
+    window_ms, window = t_ms, list(per_step)
+    while window_ms < args.min_window_ms:
+        dt, more = timed_loop(args.steps)
+        window_ms += dt
+        window += more
     sampler.mark("end")
-    barrier(world)
-    t_ms = ev0.elapsed_time(ev1)
     t_ms = max_over_ranks(t_ms, world)
     ms_step = t_ms / args.steps
     value = shape.T * world / (t_ms / 1e3 / args.steps)
+    step_stats = {"median_ms": pct(window, 50), "p10_ms": pct(window, 10), "p90_ms": pct(window, 90),
+                  "mean_ms": sum(window) / len(window), "steps": len(window), "window_ms": window_ms}
 
     # ---- per-kernel durations (instrumented pass, same work, after the timed region)
     L = moe.moe_layer_launch_count(cfg)
-    rows = "e4m3x2" if nk else "fp16"  # the A-row form of fp8 layers
-    names = ([f"x_to_{rows}"] if fp8 else []) + ["router_gemm", "topk_softmax"]
-    if shape.R <= 8192:  # small batches: init_routing + gather in one kernel
-        names += ["route_permute"]
-    else:
-        names += ["route_hist", "route_scan_scatter"]
-        names += ["permute_gather"] if (shape.act_dtype == "f32" or not args.gather_a) else []
-    names += ["w13_gate_up"]
-    names += [f"h_to_{rows}"] if fp8 else []
-    names += ["w2_down"]
-    if shape.I_shared:
-        names += ["shared_w13"] + ([f"shared_h_to_{rows}"] if fp8 else []) + ["shared_w2"]
-    names += ["finalize"]
+    names = kernel_names(shape, nk, args.gather_a)
     assert len(names) == L
     per = [[] for _ in range(L)]
     for _ in range(args.steps):
@@ -477,37 +512,37 @@ def run_ours(args, world, rank, local):
     # region, as it does for long tensor-bound steps
     capped = "sw_power_cap" in clocks.get("reasons", [])
     bf16_peak = pk["bf16_tflops_sustained"] if capped else pk["bf16_tflops"]
-    t_tensor = flops / (bf16_peak * 1e12)
+    # fp8 weights stored K-contiguous run on the e4m3 kind, whose dense peak
+    # is twice the 16-bit one (the nominal 4.5 / 2.25 PFLOP/s ratio times the
+    # measured bf16 figure); everything else on the 16-bit kinds
+    kind_peak = 2 * bf16_peak if nk else bf16_peak
+    t_tensor = flops / (kind_peak * 1e12)
     t_hbm = nbytes / (pk["hbm_gbs"] * 1e9)
-    if t_tensor >= t_hbm and nk:
-        # the e4m3 kind runs two products (hi and lo rows) per multiply-add, at
-        # twice the dense bf16 rate (the nominal 4.5 / 2.25 PFLOP/s ratio times
-        # the measured bf16 peak): the same fraction as useful FLOPs vs bf16
-        roof = {"bound": "tensor", "achieved": 2 * flops / t_s / 1e12, "peak": 2 * bf16_peak,
-                "unit": "TFLOP/s", "operand_dtype": "e4m3 (x and h as two e4m3 terms: two products "
-                "per multiply-add); peak = 2 x the measured bf16 figure (nominal 4.5 / 2.25 PFLOP/s)"}
-    elif t_tensor >= t_hbm:
-        roof = {"bound": "tensor", "achieved": flops / t_s / 1e12, "peak": bf16_peak, "unit": "TFLOP/s"}
+    if t_tensor >= t_hbm:
+        roof = {"bound": "tensor", "achieved": flops / t_s / 1e12, "peak": kind_peak, "unit": "TFLOP/s"}
+        if nk:
+            roof["peak_kind"] = ("kind::f8f6f4 (e4m3): 2 x the measured bf16 figure; achieved counts "
+                                 "the method's multiply-adds once (2 R D 2I for W13), although x and h "
+                                 "ride as two e4m3 terms, i.e. two tensor-core products per multiply-add")
+            roof["bf16_equivalent_frac"] = (flops / t_s / 1e12) / bf16_peak
     else:
         roof = {"bound": "hbm", "achieved": nbytes / t_s / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    tr = profiled_traffic(dom, args.workload)
+    tr = profiled_traffic(dom, args.workload if primary else shape_key(shape))
     roof.update({"traffic": tr, "kernel": dom, "kernel_us": kernels_us[dom],
                  "algorithmic_flops": flops, "algorithmic_bytes": nbytes,
-                 "tensor_frac": (flops / t_s / 1e12) / bf16_peak,
+                 "tensor_frac": (flops / t_s / 1e12) / kind_peak,
                  "hbm_frac": (nbytes / t_s / 1e9) / pk["hbm_gbs"],
                  "peak_source": "%s (MEASURED_PEAKS.json: HBM copy; bf16 %s)" % (
                      pk["source"], "sustained, sw_power_cap seen" if capped else "burst")})
     layer_flops = workloads.layer_flops(shape)
     layer_bytes = workloads.layer_bytes(shape, active_experts=active)
-    t_roof = max(layer_flops / (bf16_peak * 1e12), layer_bytes / (pk["hbm_gbs"] * 1e9))
+    t_roof = max(layer_flops / (kind_peak * 1e12), layer_bytes / (pk["hbm_gbs"] * 1e9))
+    sm_mhz = clocks.get("sm_mhz")
 
-    line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None,
+    res = {
+        "value": value, "ms_per_step": ms_step, "step_ms": step_stats,
         "dtype": ("f32" if shape.act_dtype == "f32" else "e4m3" if nk else "fp16" if fp8 else "bf16"),
-        "data": "synthetic (seeded Gaussian x ~ N(0,1), weights ~ N(0,0.02), random init)",
         "config": dict(workloads.config_summary(shape), parallelism=f"replicas x{world}",
                        l2="inputs larger than L2: %.2f GB of expert weights per step" %
                           (shape.E * workloads.expert_weight_bytes(shape.D, shape.I, shape.w_dtype) / 1e9),
@@ -517,7 +552,10 @@ def run_ours(args, world, rank, local):
                            if nk else "kn: weights as drawn; expanded to fp16 on chip"} if fp8 else {})),
         "roofline": roof,
         "layer_roofline": {"t_roofline_us": t_roof * 1e6, "t_measured_us": ms_step * 1e3,
-                           "frac": t_roof / (ms_step / 1e3), "flops": layer_flops, "bytes": layer_bytes},
+                           "frac": t_roof / (ms_step / 1e3), "flops": layer_flops, "bytes": layer_bytes,
+                           "tensor_peak_tflops": kind_peak},
+        # time x median SM clock: the step's length in SM cycles, comparable across clocks
+        "mcycles_per_step": (ms_step * 1e-3 * sm_mhz) if sm_mhz else None,
         "kernels_us": kernels_us,
         "memory_kernels": memory_kernels,
         "e2e": {"value": shape.T * world / (e2e_ms / 1e3 / args.steps), "unit": "tokens/s",
@@ -527,9 +565,55 @@ def run_ours(args, world, rank, local):
         "gpu_launches": L * args.steps,
         "clocks": clocks,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    cpu_inp = None
+    if primary and rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu_inp = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
-        line["cpu_baseline"] = cpu_baseline(shape, cpu_inp, budget_s=args.cpu_budget)
+    del inp, W, args_layer, ws, out, x_dev, out_dev
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    if cpu_inp is not None:
+        res["cpu_baseline"] = cpu_baseline(shape, cpu_inp, budget_s=args.cpu_budget)
+    return res
+
+
+def shape_key(shape):
+    for k, v in workloads.CONFIGS.items():
+        if v == shape:
+            return k
+    return shape.name
+
+
+def run_ours(args, world, rank, local):
+    import mixture_experts_layer_gating_gb300 as moe
+    from mixture_experts_layer_gating_gb300 import _build
+
+    if rank == 0 or not os.path.exists(moe.LIB_PATH):
+        _build.build()
+    barrier(world)
+    moe.load_library()
+    set_options(moe, args)
+    shape = workload_shape(args)
+    res = measure(args, world, rank, local, shape, primary=True)
+    line = {
+        "metric": METRIC, "value": res.pop("value"), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": res.pop("ms_per_step"),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": res.pop("dtype"),
+        "data": "synthetic (seeded Gaussian x ~ N(0,1), weights ~ N(0,0.02), random init)",
+    }
+    line.update(res)
+    # secondary workloads of the same run (their own timed regions, after the
+    # primary one): by default the Qwen3-MoE-style prefill layer
+    sec = {}
+    for name in (args.secondary.split(",") if args.secondary else []):
+        if not name or name == args.workload:
+            continue
+        r = measure(args, world, rank, local, workloads.CONFIGS[name], primary=False)
+        sec[name] = {k: r[k] for k in ("value", "ms_per_step", "step_ms", "dtype", "roofline",
+                                        "layer_roofline", "kernels_us", "e2e", "clocks")}
+        sec[name]["workload"] = r["config"]["workload"]
+    if sec:
+        line["secondary"] = sec
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -539,13 +623,21 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="qwen3_prefill", choices=sorted(workloads.CONFIGS))
+    ap.add_argument("--workload", default="ling_prefill", choices=sorted(workloads.CONFIGS))
+    ap.add_argument("--secondary", default="qwen3_prefill",
+                    help="comma-separated workloads also timed in the same run (their own lines "
+                         "under 'secondary'); empty for none")
+    ap.add_argument("--min-window-ms", type=float, default=200.0,
+                    help="per-step percentiles cover at least this much device time (the K timed "
+                         "steps, repeated when shorter)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--ref-tokens", type=int, default=0,
                     help="reference arm: tokens per step (0: grown until one step takes ~--ref-step-s)")
     ap.add_argument("--ref-step-s", type=float, default=2.0)
+    ap.add_argument("--ref-total-s", type=float, default=150.0,
+                    help="reference arm: about this many seconds for all warm-up and timed steps")
     ap.add_argument("--pair-tiles", type=int, nargs="?", const=1, default=None,
                     help="moe_set_option MOE_OPT_PAIR_TILES: 0 never 2-CTA tiles, 1 always (swapped "
                          "tails), 2 always without swapped tails, 3 (default) by rows per group")

@@ -159,7 +159,8 @@ int moe_permute(const moe_config_t* cfg, const int32_t* topk_ids, const void* x,
  * while a request runs (a serving runtime that plans all device memory at
  * start-up, a plugin interface without a workspace argument), so they cannot
  * provide the workspace moe_permute takes.
- *   Same arguments and results as moe_permute, without ws / ws_bytes.  Its
+ *   Same arguments, argument checks and results as moe_permute, without
+ *   ws / ws_bytes (the configuration is validated exactly as there).  Its
  *   scratch (one expert histogram per routing segment: E <= 512 experts times
  *   at most 128 segments) is a fixed 256 KiB array in the library's device
  *   memory, held on every GPU that loads the library until the process exits.

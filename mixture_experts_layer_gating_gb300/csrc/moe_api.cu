@@ -88,6 +88,10 @@ struct Layout {
   size_t total;
 };
 
+}  // namespace
+
+namespace moe {
+
 bool cfg_valid(const moe_config_t* c) {
   if (!c) return false;
   if (c->T < 0 || c->D < 8 || c->E < 1 || c->E > 512 || c->k < 1 || c->k > 16 || c->k > c->E ||
@@ -111,6 +115,10 @@ bool combo_supported(const moe_config_t* c) {
   if (c->act_dtype == MOE_F32) return c->w_dtype == MOE_F32;
   return c->w_dtype == MOE_BF16 || c->w_dtype == MOE_FP8_E4M3 || c->w_dtype == MOE_FP8_E4M3_NK;
 }
+
+}  // namespace moe
+
+namespace {
 
 // fp8 weights of either layout (per-column scales, rows with power-of-two scales)
 inline bool is_fp8(const moe_config_t* c) {

@@ -53,6 +53,12 @@ cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t 
   return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
 }
 
+// Host-side validation shared by every entry point (moe_api.cu): the
+// configuration's shape and dtype limits, and whether its (act_dtype,
+// w_dtype, act) combination is built.
+bool cfg_valid(const moe_config_t* c);
+bool combo_supported(const moe_config_t* c);
+
 inline size_t act_bytes(int dt) { return dt == MOE_F32 ? 4 : 2; }
 inline size_t w_bytes(int dt) { return dt == MOE_F32 ? 4 : (dt == MOE_BF16 ? 2 : 1); }
 

@@ -52,16 +52,14 @@ extern "C" int moe_permute_noalloc(const moe_config_t* cfg, const int32_t* topk_
                                    const void* x, int32_t* counts, int32_t* offsets,
                                    int32_t* sorted_rows, int32_t* dest, void* x_perm,
                                    void* stream) {
-  if (!cfg || cfg->T < 0 || cfg->E < 1 || cfg->E > 512 || cfg->k < 1 || cfg->k > 16 ||
-      cfg->k > cfg->E || cfg->D < 8 || cfg->D % 8)
-    return MOE_ERR_INVALID_ARG;
-  if (cfg->act_dtype != MOE_F32 && cfg->act_dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+  // the same configuration checks as moe_permute, then the scratch-size guard
+  if (!moe::cfg_valid(cfg)) return MOE_ERR_INVALID_ARG;
+  if (!moe::combo_supported(cfg)) return MOE_ERR_UNSUPPORTED;
   if (!topk_ids || !counts || !offsets || !sorted_rows || !dest) return MOE_ERR_INVALID_ARG;
   if (x && (!x_perm || (reinterpret_cast<uintptr_t>(x) & 15u) ||
             (reinterpret_cast<uintptr_t>(x_perm) & 15u)))
     return MOE_ERR_INVALID_ARG;
-  const long long R = static_cast<long long>(cfg->T) * cfg->k;
-  if (R > (1ll << 30)) return MOE_ERR_INVALID_ARG;
+  const long long R = static_cast<long long>(cfg->T) * cfg->k;  // <= 2^30 (cfg_valid)
   // the histogram needs E * route_segments(R) entries (never more than the
   // array holds while R <= 2^30); the check stays as a guard
   if (static_cast<long long>(cfg->E) * moe::route_segments(R) > kMaxScratchInts)

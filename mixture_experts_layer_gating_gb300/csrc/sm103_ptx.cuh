@@ -70,6 +70,22 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   }
 }
 
+// After an abort: waits at most kDrainLimitNs for a phase whose copies may
+// still be in flight (ignores the abort flag; gives up silently).
+constexpr uint64_t kDrainLimitNs = 10000000ull;  // 10 ms
+__device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = smem_u32(bar);
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(a, parity))
+    if (globaltimer_ns() - t0 > kDrainLimitNs) return;
+}
+// A further 200 us after an abort, so that copies whose barrier could not be
+// observed (one whose other arrivals never came) land before the CTA exits.
+__device__ __forceinline__ void drain_grace() {
+  const uint64_t t0 = globaltimer_ns();
+  while (globaltimer_ns() - t0 < 200000ull) __nanosleep(1000);
+}
+
 // ------------------------------------------------------------------ TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");

@@ -27,3 +27,12 @@ def tol_factor(shape) -> float:
 
 def to_device(inp, device="cuda"):
     return {k: (v.to(device) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+
+
+def max_near_ties(T: int) -> int:
+    """Most tokens a parity check may leave out for a near tie: 1 % of the
+    batch (at least one token).  With logits of spread ~1 the gap between the
+    k-th and (k+1)-th largest is about 0.05 on these workloads, so a gap below
+    1e-4 hits ~0.2 % of the tokens; far more would mean the comparison is
+    being weakened."""
+    return max(1, T // 100)

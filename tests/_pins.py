@@ -87,6 +87,56 @@ def check_topk_weight_invariants(o):
         assert (np.diff(sel, axis=1) <= 0).all(), "ids must be ordered by descending logit"
 
 
+def _brute_near_ties(L, k, eps):
+    """Per token: sort its logits with Python's sorted(), descending, and
+    compare the k-th and (k+1)-th values; no (k+1)-th value (k = E) means no
+    near tie."""
+    T, E = L.shape
+    out = []
+    for t in range(T):
+        v = sorted((float(a) for a in L[t]), reverse=True)
+        out.append(k < E and (v[k - 1] - v[k]) < eps)
+    return np.array(out, dtype=bool)
+
+
+def check_near_ties(o):
+    """Which tokens the parity tests leave out: those whose k-th and (k+1)-th
+    largest logits differ by less than 1e-4 (strictly), checked on hand-built
+    gaps at the boundary and against a brute-force sort on random rows."""
+    eps = 1e-4
+    below, above = np.nextafter(eps, 0.0), np.nextafter(eps, 1.0)
+    # k = 3 of E = 6; the third and fourth logits are `gap` and 0.0, so the
+    # gap is exactly the double `gap`; the others are far away
+    def row(gap, perm=None):
+        r = np.array([5.0, 4.0, gap, 0.0, -3.0, -4.0])
+        return r if perm is None else r[perm]
+    perm = np.array([3, 5, 0, 2, 4, 1])  # the same values in another order
+    L = np.stack([row(eps), row(below), row(above), row(0.0), row(eps, perm), row(below, perm),
+                  row(2e-4), row(0.5e-4)])
+    want = np.array([False, True, False, True, False, True, False, True])
+    got = np.asarray(o.near_tie_tokens(L, 3), dtype=bool)
+    assert got.shape == (len(L),)
+    assert np.array_equal(got, want), f"near-tie boundary cases: {got} != {want}"
+    # ties inside the top k, or below the (k+1)-th, are not near ties
+    L2 = np.array([[5.0, 5.0, 3.0, 1.0, 1.0], [2.0, 9.0, 9.0, 9.0, -1.0], [7.0, 1.0, 3.0, 5.0, 1.0]])
+    assert np.array_equal(np.asarray(o.near_tie_tokens(L2, 2), dtype=bool), [False, True, False])
+    # k = E: there is no (k+1)-th logit, so no token is left out
+    assert not np.asarray(o.near_tie_tokens(np.zeros((4, 5)), 5), dtype=bool).any()
+    # k = 1: the gap between the largest and the second largest
+    L3 = np.array([[1.0, 1.0 - 0.5e-4, 0.0], [1.0, 0.0, 0.5], [0.25, 0.25, 0.25]])
+    assert np.array_equal(np.asarray(o.near_tie_tokens(L3, 1), dtype=bool), [True, False, True])
+    # random rows, some with values on a grid of eps / 2 so that gaps land on,
+    # below and above eps, against the brute-force sort
+    rng = _rng(13)
+    for E, k in [(8, 2), (16, 5), (7, 6), (9, 1), (12, 12)]:
+        R1 = rng.standard_normal((300, E))
+        R2 = rng.integers(-6, 7, size=(300, E)) * (eps / 2)
+        R3 = rng.integers(-3, 4, size=(300, E)) * eps
+        for R in (R1, R2, R3):
+            got = np.asarray(o.near_tie_tokens(R, k), dtype=bool)
+            assert np.array_equal(got, _brute_near_ties(R, k, eps)), f"near ties differ (E={E}, k={k})"
+
+
 def check_routing_brute_force(o):
     rng = _rng(4)
     for T, E, k in [(50, 6, 2), (17, 33, 4), (1, 4, 1), (64, 8, 8)]:
@@ -277,4 +327,5 @@ ALL_CHECKS = [
     check_routing_brute_force, check_permute_round_trip, check_swiglu_golden, check_activations_library,
     check_single_expert_is_dense_mlp, check_layer_vs_dense_then_mask, check_identical_experts,
     check_shared_only, check_fp8_scale_identity, check_subset_matches_full, check_counts_sum,
+    check_near_ties,
 ]

@@ -117,3 +117,30 @@ def test_memory_kernel_bytes_follow_the_row_types():
         assert bench.memory_kernel_bytes(ling, "h_to_e4m3x2", 2, nk) == R * I * hb[nk] + R * I * 2 + 4 * R
         assert bench.memory_kernel_bytes(ling, "shared_h_to_e4m3x2", 2, nk) == \
             T * Is * hb[nk] + T * Is * 2 + 4 * T
+
+
+@pytest.mark.parametrize("name", sorted(__import__("workloads").CONFIGS))
+@pytest.mark.parametrize("layout", ["kn", "nk"])
+def test_bench_kernel_names_match_launch_count(name, layout):
+    """bench.py names each kernel moe_layer launches (per-kernel timings):
+    one name per launch the library reports, for every workload."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import mixture_experts_layer_gating_gb300 as moe
+    import workloads
+    from tests._lib import ensure_library
+
+    ensure_library()
+    shape = workloads.CONFIGS[name]
+    nk = layout == "nk" and shape.w_dtype == "fp8_e4m3"
+    cfg = moe.config_from_shape(shape, "nk" if nk else "kn")
+    assert len(bench.kernel_names(shape, nk, False)) == moe.moe_layer_launch_count(cfg)
+
+
+def test_bench_percentiles():
+    sys.path.insert(0, ROOT)
+    import bench
+
+    v = [5.0, 1.0, 3.0, 2.0, 4.0]
+    assert bench.pct(v, 50) == 3.0 and bench.pct(v, 0) == 1.0 and bench.pct(v, 100) == 5.0
+    assert bench.pct(v, 10) == pytest.approx(1.4) and bench.pct(v, 90) == pytest.approx(4.6)

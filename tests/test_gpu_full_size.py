@@ -20,13 +20,15 @@ import torch
 import mixture_experts_layer_gating_gb300 as moe
 import oracle
 import workloads
-from tests._lib import ensure_library, rms, tol_factor
+from tests._lib import ensure_library, max_near_ties, rms, tol_factor
 
 pytestmark = pytest.mark.gpu
 
-# sampled tokens per workload: fewer where the oracle's per-expert fp64
-# copies of the weights are large (Ling: 268 MB per expert for W13)
-SAMPLE = {"ling_prefill": 6, "ling_decode": 6, "qwen35_prefill": 16}
+# sampled tokens per workload (the first and last token are always added).
+# The oracle's cost is dominated by its fp64 copy of each expert a sampled
+# token reaches (Ling: 268 MB per expert for W13), so once most experts are
+# hit more tokens cost little: the prefill layers take a few hundred.
+SAMPLE = {"ling_prefill": 256, "qwen35_prefill": 256, "gemma4_prefill": 128, "ling_decode": 64}
 WORKLOADS = sorted(n for n in workloads.CONFIGS if n not in ("toy", "qwen3_prefill"))
 # fp8 workloads run in both weight layouts (bench.py times the K-contiguous one)
 CASES = [(n, "kn") for n in WORKLOADS] + [(n, "nk") for n in WORKLOADS
@@ -76,13 +78,19 @@ def test_full_size_workload(name, layout):
 
     # (2) sampled tokens against the oracle
     gen = np.random.default_rng(T + E)
-    n = min(T, SAMPLE.get(name, 32))
+    n = min(T, SAMPLE.get(name, 64))
     tokens = np.unique(np.concatenate([[0, T - 1], gen.choice(T, n, replace=False)]))[: n + 2]
     sub = dict(inp)
     sub["x"] = inp["x"].cpu()[torch.from_numpy(tokens)]
     ref = oracle.moe_layer(sub, k, shape.act, shape.renormalize)
     ties = oracle.near_tie_tokens(ref["logits"], k)
+    assert ties.sum() <= max_near_ties(len(tokens))
     keep = ~ties
+    # every token of the batch: how many have a near tie in the GPU's logits
+    # (the oracle's logits exist for the sample only); at most 1 %
+    all_ties = oracle.near_tie_tokens(logits, k)
+    print(f"{name}/{layout}: {int(all_ties.sum())} of {T} tokens with a near tie")
+    assert all_ties.sum() <= max_near_ties(T)
     got = out[torch.from_numpy(tokens).cuda()].double().cpu().numpy()
     assert (np.array_equal(ids[tokens][keep], ref["ids"][keep]))
     assert keep.any()

@@ -8,7 +8,7 @@ from tests import _pins
 
 _orig = {name: getattr(o, name) for name in
          ("topk_softmax", "init_routing", "expert_ffn", "finalize", "activation",
-          "scaled_projection", "router_logits", "permute")}
+          "scaled_projection", "router_logits", "permute", "near_tie_tokens")}
 
 
 def _swap_gate_up(rows, W13_e, W2_e, act, s13_e=None, s2_e=None):
@@ -75,6 +75,41 @@ def _permute_off_by_one(x, sorted_rows, k):
     return xx[(np.asarray(sorted_rows) + 1) % (xx.shape[0] * k) // k]
 
 
+def _ties_next_pair(L, k, eps=1e-4):
+    """Compares the (k+1)-th and (k+2)-th logits instead of the k-th and (k+1)-th."""
+    L = np.asarray(L, np.float64)
+    if k + 1 >= L.shape[1]:
+        return np.zeros(L.shape[0], dtype=bool)
+    s = -np.sort(-L, axis=1)
+    return (s[:, k] - s[:, k + 1]) < eps
+
+
+def _ties_inclusive(L, k, eps=1e-4):
+    """<= in place of <: a gap of exactly eps counts as a near tie."""
+    L = np.asarray(L, np.float64)
+    if k >= L.shape[1]:
+        return np.zeros(L.shape[0], dtype=bool)
+    s = -np.sort(-L, axis=1)
+    return (s[:, k - 1] - s[:, k]) <= eps
+
+
+def _ties_all_when_k_is_e(L, k, eps=1e-4):
+    """k = E treated as if every token had a near tie."""
+    L = np.asarray(L, np.float64)
+    if k >= L.shape[1]:
+        return np.ones(L.shape[0], dtype=bool)
+    return _orig["near_tie_tokens"](L, k, eps)
+
+
+def _ties_ascending(L, k, eps=1e-4):
+    """The k-th and (k+1)-th smallest instead of largest logits."""
+    L = np.asarray(L, np.float64)
+    if k >= L.shape[1]:
+        return np.zeros(L.shape[0], dtype=bool)
+    s = np.sort(L, axis=1)
+    return (s[:, k] - s[:, k - 1]) < eps
+
+
 MUTATIONS = {
     "gate_up_swapped": ("expert_ffn", _swap_gate_up),
     "ties_to_high_index": ("topk_softmax", _ties_to_high_index),
@@ -87,6 +122,10 @@ MUTATIONS = {
     "erf_instead_of_tanh_gelu": ("activation", _erf_gelu),
     "router_bias_dropped": ("router_logits", _bias_dropped),
     "permute_off_by_one": ("permute", _permute_off_by_one),
+    "near_ties_next_pair": ("near_tie_tokens", _ties_next_pair),
+    "near_ties_inclusive": ("near_tie_tokens", _ties_inclusive),
+    "near_ties_all_when_k_is_e": ("near_tie_tokens", _ties_all_when_k_is_e),
+    "near_ties_ascending": ("near_tie_tokens", _ties_ascending),
 }
 
 
