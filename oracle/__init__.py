@@ -5,7 +5,13 @@ import this package; the product path never does.
 """
 from .moe_oracle import (  # noqa: F401
     ACT_GEGLU_TANH,
+    ACT_QUANT_E4M3_ROW,
     ACT_SWIGLU,
+    E4M3_MAX,
+    bf16_round,
+    dequantize_rows,
+    e4m3_round,
+    quantize_rows_e4m3,
     activation,
     expert_ffn,
     finalize,

@@ -44,6 +44,9 @@ Steps and the passages they follow
 8. Shared expert / dense MLP -- Qwen3.5 page: y = Router(x) + SharedExpert(x);
    Ling page §1 (the shared expert is a local dense path on every token);
    Gemma-4 page §2 (dense MLP and MoE run in parallel and are added).
+9. W8A8 (optional) -- Ling page §5 "激活量化" and "逐通道 direct_scaled_dot":
+   activations quantised to fp8 per token with a dynamic scale, fp8 x fp8
+   products, per-token and per-channel scales after the reduction.
 
 Every function here is pinned by the CPU tests to something other than itself
 (brute force, textbook / library routines, invariants, printed values).
@@ -57,6 +60,7 @@ import numpy as np
 
 ACT_SWIGLU = "swiglu"
 ACT_GEGLU_TANH = "geglu_tanh"
+ACT_QUANT_E4M3_ROW = "e4m3_row"  # W8A8: activations quantised per row to e4m3
 
 
 def to_f64(a) -> Optional[np.ndarray]:
@@ -122,6 +126,62 @@ def near_tie_tokens(L, k: int, eps: float = 1e-4) -> np.ndarray:
     return (s[:, k - 1] - s[:, k]) < eps
 
 
+# ---------------------------------------------------------------- W8A8 forms
+# "用SGLang-JAX在TPU上优化Ling-2.6-1T" §5, "激活量化": the fused kernel
+# quantises the routed tokens' activations from bf16 to fp8 with a dynamic
+# per-token scale (before the scatter), and "逐通道 direct_scaled_dot" feeds
+# fp8 tokens and fp8 weights to the matrix unit, applying the per-token and
+# per-channel scales after the f32 reduction.  Readings (the pages give no
+# formula): the scale of a row is its largest |value| over 448, the largest
+# e4m3 value; codes are the nearest e4m3 value of value / scale with ties to
+# the even code; both divisions are fp32 operations on the bf16 values; the
+# intermediate h is carried in bf16 between the two projections (as the bf16
+# activations are) and quantised per row the same way before the down
+# projection.
+E4M3_MAX = 448.0
+
+
+def _round_binary(v, mant_bits: int, emin: int, vmax: float) -> np.ndarray:
+    """Nearest value of a binary floating-point format with `mant_bits`
+    fraction bits, smallest normal exponent `emin` (subnormals below it) and
+    largest finite value `vmax`; ties to the even significand; magnitudes
+    beyond vmax saturate to vmax."""
+    v = np.asarray(v, dtype=np.float64)
+    a = np.abs(v)
+    _, ex = np.frexp(np.maximum(a, 2.0 ** emin))  # a = m 2^ex, m in [0.5, 1)
+    quantum = np.ldexp(1.0, ex - 1 - mant_bits)  # spacing of the format at a
+    r = np.round(a / quantum) * quantum  # a / quantum is exact; np.round: half to even
+    r = np.minimum(r, vmax)
+    return np.copysign(r, v)
+
+
+def e4m3_round(v) -> np.ndarray:
+    """Nearest e4m3 (fn: 4 exponent bits, bias 7, 3 fraction bits, largest
+    finite 448) value of each element, ties to the even code, saturating."""
+    return _round_binary(v, 3, -6, E4M3_MAX)
+
+
+def bf16_round(v) -> np.ndarray:
+    """Nearest bf16 value of each element (ties to even)."""
+    return _round_binary(v, 7, -126, float(np.finfo(np.float32).max))
+
+
+def quantize_rows_e4m3(a):
+    """Dynamic per-row e4m3 quantisation: returns (q, s) with q [rows, n] the
+    e4m3 codes' values and s [rows] the fp32 scales, so that q * s[:, None]
+    approximates a.  s = amax / 448 and q = e4m3(a / s), divisions in fp32; a
+    row of zeros gets s = 1."""
+    a32 = np.asarray(a, dtype=np.float64).astype(np.float32)
+    amax = np.abs(a32).max(axis=1) if a32.shape[1] else np.zeros(a32.shape[0], np.float32)
+    s = np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
+    q = e4m3_round((a32 / s[:, None]).astype(np.float32))
+    return q, s.astype(np.float64)
+
+
+def dequantize_rows(q, s) -> np.ndarray:
+    return np.asarray(q, np.float64) * np.asarray(s, np.float64)[:, None]
+
+
 # ---------------------------------------------------------------- step 3
 def init_routing(ids, E: int) -> Dict[str, np.ndarray]:
     """Expert histogram, exclusive scan and stable sort of expanded rows.
@@ -169,23 +229,34 @@ def scaled_projection(A: np.ndarray, W: np.ndarray, scale: Optional[np.ndarray])
     return out
 
 
-def expert_ffn(rows: np.ndarray, W13_e, W2_e, act: str, s13_e=None, s2_e=None):
+def expert_ffn(rows: np.ndarray, W13_e, W2_e, act: str, s13_e=None, s2_e=None,
+               act_quant: Optional[str] = None):
     """One expert on a block of rows: h = act(gate) * up; y = h W2.
 
     W13_e is [D, 2I] with the gate projection in the first I columns and the
-    up projection in the last I columns.  Returns (h, y).
+    up projection in the last I columns.  Returns (h, y).  With act_quant =
+    "e4m3_row" (W8A8) the rows arrive already quantised (q * s) and h is
+    rounded to bf16, then quantised per row, before the down projection; the
+    returned h is the bf16 h.
     """
     W13_e, W2_e = to_f64(W13_e), to_f64(W2_e)
     I = W2_e.shape[0]
     gu = scaled_projection(rows, W13_e, to_f64(s13_e))
     gate, up = gu[:, :I], gu[:, I:]
     h = activation(gate, act) * up
-    y = scaled_projection(h, W2_e, to_f64(s2_e))
+    h_in = h
+    if act_quant == ACT_QUANT_E4M3_ROW:
+        h = bf16_round(h)
+        h_in = dequantize_rows(*quantize_rows_e4m3(h))
+    elif act_quant is not None:
+        raise ValueError(f"unknown activation quantisation {act_quant!r}")
+    y = scaled_projection(h_in, W2_e, to_f64(s2_e))
     return h, y
 
 
 # ---------------------------------------------------------------- step 6
-def grouped_ffn(x_perm: np.ndarray, offsets, W13, W2, act: str, s13=None, s2=None):
+def grouped_ffn(x_perm: np.ndarray, offsets, W13, W2, act: str, s13=None, s2=None,
+                act_quant: Optional[str] = None):
     """Per-expert loop over the contiguous expert segments of x_perm."""
     offsets = np.asarray(offsets)
     E = len(offsets) - 1
@@ -199,14 +270,16 @@ def grouped_ffn(x_perm: np.ndarray, offsets, W13, W2, act: str, s13=None, s2=Non
             continue
         h[a:b], y[a:b] = expert_ffn(
             x_perm[a:b], W13[e], W2[e], act,
-            None if s13 is None else s13[e], None if s2 is None else s2[e])
+            None if s13 is None else s13[e], None if s2 is None else s2[e], act_quant)
     return h, y
 
 
 # ---------------------------------------------------------------- step 8
-def shared_expert(x, W13s, W2s, act: str, s13s=None, s2s=None) -> np.ndarray:
-    """The always-on expert (or dense MLP) applied to every token."""
-    _, y = expert_ffn(to_f64(x), W13s, W2s, act, s13s, s2s)
+def shared_expert(x, W13s, W2s, act: str, s13s=None, s2s=None,
+                  act_quant: Optional[str] = None) -> np.ndarray:
+    """The always-on expert (or dense MLP) applied to every token (x already
+    quantised when act_quant is set)."""
+    _, y = expert_ffn(to_f64(x), W13s, W2s, act, s13s, s2s, act_quant)
     return y
 
 
@@ -226,25 +299,35 @@ def finalize(y_perm: np.ndarray, dest, w, s: Optional[np.ndarray] = None) -> np.
 
 # ---------------------------------------------------------------- layer
 def moe_layer(inp: Dict, k: int, act: str, renormalize: bool = True,
-              logits: Optional[np.ndarray] = None) -> Dict[str, np.ndarray]:
+              logits: Optional[np.ndarray] = None,
+              act_quant: Optional[str] = None) -> Dict[str, np.ndarray]:
     """The whole layer: route, permute, grouped FFN, shared expert, finalize.
 
     ``inp`` holds x, Wg, logit_bias, W13, W2, s13, s2, W13s, W2s, s13s, s2s
     (torch tensors or arrays; absent / None entries are skipped).  When
     ``logits`` is given it replaces step 1 (used to compare routing against
-    an implementation's own fp32 logits).  Returns every intermediate.
+    an implementation's own fp32 logits).  ``act_quant`` = "e4m3_row" is the
+    W8A8 form: the router still projects the bf16 x, while the expert and
+    shared-expert FFNs take x quantised per token (before the permutation)
+    and h quantised per row.  Returns every intermediate.
     """
     x = to_f64(inp["x"])
     E = inp["W13"].shape[0]
     L = router_logits(x, inp["Wg"], inp.get("logit_bias")) if logits is None else np.asarray(logits, np.float64)
     ids, w = topk_softmax(L, k, renormalize)
     r = init_routing(ids, E)
-    x_perm = permute(x, r["sorted_rows"], k)
+    x_ffn = x
+    if act_quant == ACT_QUANT_E4M3_ROW:
+        x_ffn = dequantize_rows(*quantize_rows_e4m3(x))
+    elif act_quant is not None:
+        raise ValueError(f"unknown activation quantisation {act_quant!r}")
+    x_perm = permute(x_ffn, r["sorted_rows"], k)
     h, y_perm = grouped_ffn(x_perm, r["offsets"], inp["W13"], inp["W2"], act,
-                            inp.get("s13"), inp.get("s2"))
+                            inp.get("s13"), inp.get("s2"), act_quant)
     s = None
     if inp.get("W13s") is not None:
-        s = shared_expert(x, inp["W13s"], inp["W2s"], act, inp.get("s13s"), inp.get("s2s"))
+        s = shared_expert(x_ffn, inp["W13s"], inp["W2s"], act, inp.get("s13s"), inp.get("s2s"),
+                          act_quant)
     out = finalize(y_perm, r["dest"], w, s)
     res = {"logits": L, "ids": ids, "w": w, "x_perm": x_perm, "h": h, "y_perm": y_perm,
            "shared": s, "out": out}
@@ -252,7 +335,8 @@ def moe_layer(inp: Dict, k: int, act: str, renormalize: bool = True,
     return res
 
 
-def moe_layer_tokens(inp: Dict, tokens, k: int, act: str, renormalize: bool = True) -> np.ndarray:
+def moe_layer_tokens(inp: Dict, tokens, k: int, act: str, renormalize: bool = True,
+                     act_quant: Optional[str] = None) -> np.ndarray:
     """Layer output for a subset of tokens only.
 
     Routing, expert FFNs and the combine act on each token independently, so
@@ -262,4 +346,4 @@ def moe_layer_tokens(inp: Dict, tokens, k: int, act: str, renormalize: bool = Tr
     sub = dict(inp)
     x = inp["x"]
     sub["x"] = x[tokens] if not hasattr(x, "detach") else x.detach().cpu()[tokens]
-    return moe_layer(sub, k, act, renormalize)["out"]
+    return moe_layer(sub, k, act, renormalize, act_quant=act_quant)["out"]

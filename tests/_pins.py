@@ -322,10 +322,157 @@ def check_counts_sum(o):
     assert res["counts"].sum() == 33 * 4, "per-expert counts must sum to T*k"
 
 
+# ---------------------------------------------------------------- W8A8 forms
+def _e4m3_table():
+    """Every finite e4m3 (fn) value with its code, decoded from the bit
+    fields: sign, 4 exponent bits (bias 7), 3 fraction bits; exponent field 0
+    is subnormal (f / 8 * 2^-6); code 0x7f / 0xff is NaN."""
+    vals = []
+    for c in range(256):
+        if c & 0x7F == 0x7F:
+            continue
+        sgn = -1.0 if c & 0x80 else 1.0
+        e, f = (c >> 3) & 0xF, c & 7
+        mag = (f / 8.0) * 2.0 ** -6 if e == 0 else (1 + f / 8.0) * 2.0 ** (e - 7)
+        vals.append((sgn * mag, c))
+    return vals
+
+
+def _brute_e4m3(v):
+    """Nearest table value by exhaustive search; a tie goes to the even code
+    (fraction LSB 0); beyond 448 saturates."""
+    table = _e4m3_table()
+    out = np.empty(len(v))
+    for i, x in enumerate(v):
+        if abs(x) >= 448.0:
+            out[i] = math.copysign(448.0, x)
+            continue
+        best = min(table, key=lambda vc: (abs(vc[0] - x), vc[1] & 1, -abs(vc[0])))
+        out[i] = best[0]
+        if best[0] == 0.0:
+            out[i] = math.copysign(0.0, x)
+    return out
+
+
+def _e4m3_probe_values(rng, n):
+    """Random magnitudes over every binade (subnormals included), the exact
+    midpoints between neighbouring e4m3 values (ties), the values themselves."""
+    mags = sorted({abs(v) for v, _ in _e4m3_table()})
+    mids = [(a + b) / 2 for a, b in zip(mags[:-1], mags[1:])]
+    r = np.exp(rng.uniform(np.log(2.0 ** -11), np.log(448.0), n))
+    v = np.concatenate([r, mids, mags, [0.0, 448.0]])
+    sgn = rng.choice([-1.0, 1.0], v.size)
+    return (v * sgn).astype(np.float32).astype(np.float64)
+
+
+def check_e4m3_round(o):
+    rng = _rng(14)
+    v = _e4m3_probe_values(rng, 3000)
+    got = o.e4m3_round(v)
+    lib = torch.from_numpy(v).float().to(torch.float8_e4m3fn).double().numpy()
+    assert np.array_equal(got, lib), "e4m3 rounding differs from torch's float8_e4m3fn cast"
+    idx = rng.choice(v.size, 600, replace=False)
+    assert np.array_equal(got[idx], _brute_e4m3(v[idx])), "e4m3 rounding differs from the code table"
+    # beyond the largest finite value: saturation
+    assert np.array_equal(o.e4m3_round(np.array([448.5, -460.0, 1e6])), [448.0, -448.0, 448.0])
+
+
+def check_bf16_round(o):
+    rng = _rng(15)
+    v = (rng.standard_normal(20000) * np.exp(rng.uniform(-30, 30, 20000))).astype(np.float32)
+    # exact ties: bf16 values with the next bit set and nothing below
+    t = (torch.from_numpy(v).to(torch.bfloat16).float().numpy().view(np.uint32) | np.uint32(0x8000))
+    v = np.concatenate([v, t.view(np.float32)]).astype(np.float64)
+    lib = torch.from_numpy(v).float().to(torch.bfloat16).double().numpy()
+    assert np.array_equal(o.bf16_round(v), lib), "bf16 rounding differs from torch's bf16 cast"
+
+
+def check_quantize_rows(o):
+    rng = _rng(16)
+    a = rng.standard_normal((50, 40)) * np.exp(rng.uniform(-6, 6, (50, 1)))
+    a = torch.from_numpy(a).to(torch.bfloat16).double().numpy()  # bf16 activations
+    a[3] = 0.0
+    q, sc = o.quantize_rows_e4m3(a)
+    assert q.shape == a.shape and sc.shape == (50,)
+    amax = np.abs(a).max(axis=1).astype(np.float32)
+    want_s = np.where(amax > 0, amax / np.float32(448.0), np.float32(1.0)).astype(np.float64)
+    assert np.array_equal(sc, want_s), "row scale = amax / 448 in fp32"
+    assert sc[3] == 1.0 and not q[3].any()
+    live = np.arange(50) != 3
+    arg = np.abs(a).argmax(axis=1)
+    assert np.array_equal(np.abs(q[np.arange(50), arg])[live], np.full(49, 448.0)), \
+        "the largest element of a row maps to +-448"
+    assert np.array_equal(q, _brute_e4m3((a.astype(np.float32) / sc.astype(np.float32)[:, None])
+                                         .astype(np.float64).ravel()).reshape(a.shape))
+    deq = o.dequantize_rows(q, sc)
+    rel = np.abs(a) / sc[:, None]
+    normal = rel >= 2.0 ** -6
+    assert (np.abs(deq - a)[normal] <= 2.0 ** -4 * np.abs(a)[normal] * (1 + 1e-6)).all()
+    assert (np.abs(deq - a)[~normal] <= 2.0 ** -10 * np.broadcast_to(sc[:, None], a.shape)[~normal]
+            * (1 + 1e-6)).all()
+
+
+def _brute_w8a8_dense_layer(inp, k, act):
+    """Dense-then-mask W8A8: x and h quantised per row through the code table,
+    every expert on every token, masked by the brute-force gates."""
+    x = np.asarray(inp["x"], np.float64)
+    E = inp["W13"].shape[0]
+    L = x @ inp["Wg"] + inp.get("logit_bias", 0.0)
+    ids, w = _brute_topk(L, k)
+
+    def quant(a):
+        out = np.empty_like(a)
+        for r in range(a.shape[0]):
+            amax = np.float32(np.max(np.abs(a[r])))
+            sc = amax / np.float32(448.0) if amax > 0 else np.float32(1.0)
+            qv = _brute_e4m3((a[r].astype(np.float32) / sc).astype(np.float64))
+            out[r] = qv * np.float64(sc)
+        return out
+
+    def ffn(xq, W13, W2, s13, s2):
+        W13 = W13 if s13 is None else W13 * np.asarray(s13)[None, :]
+        W2 = W2 if s2 is None else W2 * np.asarray(s2)[None, :]
+        gu = torch.from_numpy(xq) @ torch.from_numpy(W13)
+        gate, up = torch.chunk(gu, 2, dim=-1)
+        a = F.silu(gate) if act == "swiglu" else F.gelu(gate, approximate="tanh")
+        h = (a * up).to(torch.bfloat16).double().numpy()
+        return quant(h) @ W2
+
+    xq = quant(x)
+    out = np.zeros_like(x)
+    for t in range(x.shape[0]):
+        for j in range(k):
+            e = ids[t, j]
+            out[t] += w[t, j] * ffn(xq[t:t + 1], inp["W13"][e], inp["W2"][e],
+                                    None if inp.get("s13") is None else inp["s13"][e],
+                                    None if inp.get("s2") is None else inp["s2"][e])[0]
+    if inp.get("W13s") is not None:
+        out += ffn(xq, inp["W13s"], inp["W2s"], inp.get("s13s"), inp.get("s2s"))
+    return out
+
+
+def check_w8a8_layer(o):
+    """The W8A8 layer against a dense-then-mask brute force with the
+    activations quantised through the e4m3 code table; the router sees the
+    unquantised x; the quantisation error is present and of e4m3 size."""
+    rng = _rng(17)
+    for act in (o.ACT_SWIGLU, o.ACT_GEGLU_TANH):
+        for (E, k, Is) in [(6, 3, 4), (5, 2, 0)]:
+            inp = _tiny_layer(rng, T=11, E=E, k=k, Is=Is, fp8=True)
+            inp["x"] = torch.from_numpy(inp["x"]).to(torch.bfloat16).double().numpy()
+            res = o.moe_layer(inp, k, act, act_quant=o.ACT_QUANT_E4M3_ROW)
+            ref = _brute_w8a8_dense_layer(inp, k, act)
+            assert np.allclose(res["out"], ref, rtol=1e-11, atol=1e-12), f"W8A8 layer (act={act}, E={E})"
+            plain = o.moe_layer(inp, k, act)
+            assert np.array_equal(res["ids"], plain["ids"]), "the router projects the unquantised x"
+            d = np.abs(res["out"] - plain["out"]).max() / np.sqrt(np.mean(plain["out"] ** 2))
+            assert 1e-4 < d < 0.5, f"W8A8 error {d} not of e4m3 size"
+
+
 ALL_CHECKS = [
     check_topk_brute_force, check_topk_all_equal, check_topk_full_softmax, check_topk_weight_invariants,
     check_routing_brute_force, check_permute_round_trip, check_swiglu_golden, check_activations_library,
     check_single_expert_is_dense_mlp, check_layer_vs_dense_then_mask, check_identical_experts,
     check_shared_only, check_fp8_scale_identity, check_subset_matches_full, check_counts_sum,
-    check_near_ties,
+    check_near_ties, check_e4m3_round, check_bf16_round, check_quantize_rows, check_w8a8_layer,
 ]

@@ -8,15 +8,24 @@ from tests import _pins
 
 _orig = {name: getattr(o, name) for name in
          ("topk_softmax", "init_routing", "expert_ffn", "finalize", "activation",
-          "scaled_projection", "router_logits", "permute", "near_tie_tokens")}
+          "scaled_projection", "router_logits", "permute", "near_tie_tokens", "quantize_rows_e4m3",
+         "e4m3_round", "bf16_round", "dequantize_rows")}
 
 
-def _swap_gate_up(rows, W13_e, W2_e, act, s13_e=None, s2_e=None):
+def _swap_gate_up(rows, W13_e, W2_e, act, s13_e=None, s2_e=None, act_quant=None):
     W13_e, W2_e = o.to_f64(W13_e), o.to_f64(W2_e)
     I = W2_e.shape[0]
     gu = o.scaled_projection(rows, W13_e, o.to_f64(s13_e))
     h = o.activation(gu[:, I:], act) * gu[:, :I]
-    return h, o.scaled_projection(h, W2_e, o.to_f64(s2_e))
+    h_in = h
+    if act_quant:
+        h = o.bf16_round(h)
+        h_in = o.dequantize_rows(*o.quantize_rows_e4m3(h))
+    return h, o.scaled_projection(h_in, W2_e, o.to_f64(s2_e))
+
+
+def _h_not_quantised(rows, W13_e, W2_e, act, s13_e=None, s2_e=None, act_quant=None):
+    return _orig["expert_ffn"](rows, W13_e, W2_e, act, s13_e, s2_e, None)
 
 
 def _ties_to_high_index(L, k, renormalize=True):
@@ -110,6 +119,37 @@ def _ties_ascending(L, k, eps=1e-4):
     return (s[:, k] - s[:, k - 1]) < eps
 
 
+def _quant_per_column(a):
+    q, sc = _orig["quantize_rows_e4m3"](np.asarray(a, np.float64).T)
+    # a per-column scale, broadcast back as if it were per row (first rows)
+    return q.T, np.resize(sc, np.asarray(a).shape[0])
+
+
+def _quant_max_127(a):
+    a32 = np.asarray(a, np.float64).astype(np.float32)
+    amax = np.abs(a32).max(axis=1)
+    sc = np.where(amax > 0, amax / np.float32(127.0), np.float32(1.0)).astype(np.float32)
+    return o.e4m3_round((a32 / sc[:, None]).astype(np.float32)), sc.astype(np.float64)
+
+
+def _quant_ties_away(v):
+    v = np.asarray(v, np.float64)
+    a = np.abs(v)
+    _, ex = np.frexp(np.maximum(a, 2.0 ** -6))
+    qn = np.ldexp(1.0, ex - 4)
+    r = np.minimum(np.floor(a / qn + 0.5) * qn, 448.0)
+    return np.copysign(r, v)
+
+
+def _bf16_truncate(v):
+    v = np.asarray(v, np.float64).astype(np.float32)
+    return (v.view(np.uint32) & np.uint32(0xFFFF0000)).view(np.float32).astype(np.float64)
+
+
+def _dequant_without_scale(q, sc):
+    return np.asarray(q, np.float64)
+
+
 MUTATIONS = {
     "gate_up_swapped": ("expert_ffn", _swap_gate_up),
     "ties_to_high_index": ("topk_softmax", _ties_to_high_index),
@@ -126,6 +166,12 @@ MUTATIONS = {
     "near_ties_inclusive": ("near_tie_tokens", _ties_inclusive),
     "near_ties_all_when_k_is_e": ("near_tie_tokens", _ties_all_when_k_is_e),
     "near_ties_ascending": ("near_tie_tokens", _ties_ascending),
+    "w8a8_quantised_per_column": ("quantize_rows_e4m3", _quant_per_column),
+    "w8a8_scale_to_127": ("quantize_rows_e4m3", _quant_max_127),
+    "e4m3_ties_away_from_zero": ("e4m3_round", _quant_ties_away),
+    "bf16_truncated": ("bf16_round", _bf16_truncate),
+    "w8a8_scale_not_applied": ("dequantize_rows", _dequant_without_scale),
+    "w8a8_h_not_quantised": ("expert_ffn", _h_not_quantised),
 }
 
 
