@@ -248,11 +248,12 @@ def memory_kernel_bytes(shape, name: str, rows_form_bytes: int, nk: bool = False
         "permute_gather": T * D * gathered + 4 * R + R * D * gathered,
         "finalize": R * D * yb + 4 * R + 4 * T * k + (T * D * yb if Is else 0) + T * D * ab,
     }
-    for pre in ("x_to_fp16", "x_to_e4m3x2"):
-        table[pre] = T * D * ab + T * D * 2 + 4 * T
-    for pre in ("h_to_fp16", "h_to_e4m3x2"):
-        table[pre] = R * I * hb + R * I * 2 + 4 * R
-        table["shared_" + pre] = T * Is * hb + T * Is * 2 + 4 * T
+    rf = rows_form_bytes
+    for pre in ("x_to_fp16", "x_to_e4m3x2", "x_to_e4m3"):
+        table[pre] = T * D * ab + T * D * rf + 4 * T
+    for pre in ("h_to_fp16", "h_to_e4m3x2", "h_to_e4m3"):
+        table[pre] = R * I * hb + R * I * rf + 4 * R
+        table["shared_" + pre] = T * Is * hb + T * Is * rf + 4 * T
     return table.get(name)
 
 
@@ -333,10 +334,10 @@ def pct(v, q):
     return v[lo] + (v[hi] - v[lo]) * (pos - lo)
 
 
-def kernel_names(shape, nk, gather_a):
+def kernel_names(shape, nk, gather_a, a8=False):
     """Names of the kernels one moe_layer call launches, in launch order."""
     fp8 = shape.w_dtype == "fp8_e4m3"
-    rows = "e4m3x2" if nk else "fp16"  # the A-row form of fp8 layers
+    rows = "e4m3" if a8 else "e4m3x2" if nk else "fp16"  # the A-row form of fp8 layers
     names = ([f"x_to_{rows}"] if fp8 else []) + ["router_gemm", "topk_softmax"]
     if shape.R <= 8192:  # small batches: init_routing + gather in one kernel
         names += ["route_permute"]
@@ -352,15 +353,17 @@ def kernel_names(shape, nk, gather_a):
     return names
 
 
-def measure(args, world, rank, local, shape, primary: bool):
-    """Time moe_layer on one workload; returns the fields of a bench line."""
+def measure(args, world, rank, local, shape, primary: bool, layout: str):
+    """Time moe_layer on one workload; returns the fields of a bench line.
+    layout: the fp8 weight layout ("kn", "nk", or "nk_a8" for W8A8)."""
     import mixture_experts_layer_gating_gb300 as moe
 
     dev = torch.device("cuda", local)
     inp = workloads.make_inputs(shape, seed=rank, device=dev, weights_seed=0)
     fp8 = shape.w_dtype == "fp8_e4m3"
-    nk = fp8 and args.fp8_layout == "nk"
-    cfg = moe.config_from_shape(shape, "nk" if nk else "kn")
+    nk = fp8 and layout in ("nk", "nk_a8")
+    a8 = fp8 and layout == "nk_a8"
+    cfg = moe.config_from_shape(shape, layout if fp8 else "kn")
     ws = moe.alloc_workspace(cfg, device=dev)
     out = torch.empty((shape.T, shape.D), dtype=workloads.torch_dtype(shape.act_dtype), device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -420,7 +423,7 @@ def measure(args, world, rank, local, shape, primary: bool):
 
     # ---- per-kernel durations (instrumented pass, same work, after the timed region)
     L = moe.moe_layer_launch_count(cfg)
-    names = kernel_names(shape, nk, args.gather_a)
+    names = kernel_names(shape, nk, args.gather_a, a8)
     assert len(names) == L
     per = [[] for _ in range(L)]
     for _ in range(args.steps):
@@ -437,7 +440,7 @@ def measure(args, world, rank, local, shape, primary: bool):
     pk_hbm = peaks()["hbm_gbs"]
     memory_kernels = {}
     for n, t_us in kernels_us.items():
-        nb = memory_kernel_bytes(shape, n, 2, nk)
+        nb = memory_kernel_bytes(shape, n, 1 if a8 else 2, nk)
         if nb is not None and t_us > 0:
             gbs = nb / (t_us * 1e3)
             memory_kernels[n] = {"bytes": nb, "us": t_us, "gbs": gbs, "frac_hbm": gbs / pk_hbm}
@@ -516,15 +519,20 @@ def measure(args, world, rank, local, shape, primary: bool):
     # is twice the 16-bit one (the nominal 4.5 / 2.25 PFLOP/s ratio times the
     # measured bf16 figure); everything else on the 16-bit kinds
     kind_peak = 2 * bf16_peak if nk else bf16_peak
+    if a8:  # one-term rows: the rows carry 1 byte per element
+        nbytes -= (R * D + R * I) * (ab - 1) if dom == "w13_gate_up" else R * I * (ab - 1)
     t_tensor = flops / (kind_peak * 1e12)
     t_hbm = nbytes / (pk["hbm_gbs"] * 1e9)
     if t_tensor >= t_hbm:
         roof = {"bound": "tensor", "achieved": flops / t_s / 1e12, "peak": kind_peak, "unit": "TFLOP/s"}
-        if nk:
+        if nk and not a8:
             roof["peak_kind"] = ("kind::f8f6f4 (e4m3): 2 x the measured bf16 figure; achieved counts "
                                  "the method's multiply-adds once (2 R D 2I for W13), although x and h "
                                  "ride as two e4m3 terms, i.e. two tensor-core products per multiply-add")
             roof["bf16_equivalent_frac"] = (flops / t_s / 1e12) / bf16_peak
+        elif a8:
+            roof["peak_kind"] = ("kind::f8f6f4 (e4m3): 2 x the measured bf16 figure; W8A8, one "
+                                 "tensor-core product per multiply-add")
     else:
         roof = {"bound": "hbm", "achieved": nbytes / t_s / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
@@ -543,13 +551,18 @@ def measure(args, world, rank, local, shape, primary: bool):
     res = {
         "value": value, "ms_per_step": ms_step, "step_ms": step_stats,
         "dtype": ("f32" if shape.act_dtype == "f32" else "e4m3" if nk else "fp16" if fp8 else "bf16"),
+        "layout": layout if fp8 else None,
         "config": dict(workloads.config_summary(shape), parallelism=f"replicas x{world}",
                        l2="inputs larger than L2: %.2f GB of expert weights per step" %
                           (shape.E * workloads.expert_weight_bytes(shape.D, shape.I, shape.w_dtype) / 1e9),
                        active_experts=active,
-                       **({"fp8_layout": ("nk: weights transposed once by moe_pack_weights_nk before "
-                                          "timing; e4m3 tensor-core kind, x and h as two e4m3 terms")
-                           if nk else "kn: weights as drawn; expanded to fp16 on chip"} if fp8 else {})),
+                       **({"fp8_layout": {
+                           "nk": "nk: weights transposed once by moe_pack_weights_nk before timing; "
+                                 "e4m3 tensor-core kind, x and h as two e4m3 terms (bf16 activations)",
+                           "nk_a8": "nk_a8: W8A8 -- weights as for nk; x and h quantised per row to "
+                                    "one e4m3 term with a dynamic scale (changes the result)",
+                           "kn": "kn: weights as drawn; expanded to fp16 on chip"}[layout]}
+                          if fp8 else {})),
         "roofline": roof,
         "layer_roofline": {"t_roofline_us": t_roof * 1e6, "t_measured_us": ms_step * 1e3,
                            "frac": t_roof / (ms_step / 1e3), "flops": layer_flops, "bytes": layer_bytes,
@@ -593,7 +606,7 @@ def run_ours(args, world, rank, local):
     moe.load_library()
     set_options(moe, args)
     shape = workload_shape(args)
-    res = measure(args, world, rank, local, shape, primary=True)
+    res = measure(args, world, rank, local, shape, primary=True, layout=args.fp8_layout)
     line = {
         "metric": METRIC, "value": res.pop("value"), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": res.pop("ms_per_step"),
@@ -601,17 +614,21 @@ def run_ours(args, world, rank, local):
         "dtype": res.pop("dtype"),
         "data": "synthetic (seeded Gaussian x ~ N(0,1), weights ~ N(0,0.02), random init)",
     }
+    line.pop("layout", None)
     line.update(res)
+    line.pop("layout", None)
     # secondary workloads of the same run (their own timed regions, after the
-    # primary one): by default the Qwen3-MoE-style prefill layer
+    # primary one): NAME or NAME:LAYOUT (fp8 weight layout kn / nk / nk_a8)
     sec = {}
-    for name in (args.secondary.split(",") if args.secondary else []):
-        if not name or name == args.workload:
+    for item in (args.secondary.split(",") if args.secondary else []):
+        name, _, layout = item.partition(":")
+        layout = layout or args.fp8_layout
+        if not name or (name == args.workload and layout == args.fp8_layout):
             continue
-        r = measure(args, world, rank, local, workloads.CONFIGS[name], primary=False)
-        sec[name] = {k: r[k] for k in ("value", "ms_per_step", "step_ms", "dtype", "roofline",
+        r = measure(args, world, rank, local, workloads.CONFIGS[name], primary=False, layout=layout)
+        sec[item] = {k: r[k] for k in ("value", "ms_per_step", "step_ms", "dtype", "layout", "roofline",
                                         "layer_roofline", "kernels_us", "e2e", "clocks")}
-        sec[name]["workload"] = r["config"]["workload"]
+        sec[item]["workload"] = r["config"]["workload"]
     if sec:
         line["secondary"] = sec
     if rank == 0:
@@ -624,9 +641,9 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="ling_prefill", choices=sorted(workloads.CONFIGS))
-    ap.add_argument("--secondary", default="qwen3_prefill",
-                    help="comma-separated workloads also timed in the same run (their own lines "
-                         "under 'secondary'); empty for none")
+    ap.add_argument("--secondary", default="qwen3_prefill,ling_prefill:nk_a8",
+                    help="comma-separated workloads (NAME or NAME:FP8_LAYOUT) also timed in the same "
+                         "run, each under 'secondary'; empty for none")
     ap.add_argument("--min-window-ms", type=float, default=200.0,
                     help="per-step percentiles cover at least this much device time (the K timed "
                          "steps, repeated when shorter)")
@@ -645,9 +662,10 @@ def main():
                     help="moe_set_option MOE_OPT_DECODE_KERNEL (0 off, 1 auto, 2/3 always with 64/16-row tiles)")
     ap.add_argument("--gather-a", action="store_true",
                     help="routed gate/up GEMM gathers x rows itself (moe_set_option MOE_OPT_GATHER_A)")
-    ap.add_argument("--fp8-layout", default="nk", choices=["kn", "nk"],
+    ap.add_argument("--fp8-layout", default="nk", choices=["kn", "nk", "nk_a8"],
                     help="fp8 workloads: weights transposed once to [.., N, K] and run on the e4m3 "
-                         "tensor-core kind (nk, default), or as drawn and expanded to fp16 on chip (kn)")
+                         "tensor-core kind (nk, default), or as drawn and expanded to fp16 on chip (kn); "
+                         "nk_a8: nk weights with W8A8 activations (opt-in, changes the result)")
     ap.add_argument("--no-pdl", action="store_true",
                     help="plain stream order instead of programmatic dependent launch (MOE_OPT_PDL 0)")
     ap.add_argument("--serial-shared", action="store_true",

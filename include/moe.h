@@ -32,7 +32,8 @@
  *   bytes, which makes D, I and I_shared multiples of 8 (16 for fp8 weights).
  * - Dtypes: act_dtype applies to x, W_g, the permuted rows and out.  w_dtype
  *   applies to W13, W2 and the shared expert's weights.  Supported pairs:
- *   (F32, F32), (BF16, BF16), (BF16, FP8_E4M3), (BF16, FP8_E4M3_NK).
+ *   (F32, F32), (BF16, BF16), (BF16, FP8_E4M3), (BF16, FP8_E4M3_NK),
+ *   (BF16, FP8_E4M3_NK_A8).
  *   Router logits and gate weights are always fp32; the expert outputs
  *   y_perm and the shared-expert output are fp32, or bf16 for fp8-weight
  *   layers (one rounding each, inside the 6e-2 RMS bar of those layers).
@@ -60,6 +61,16 @@
  *   element; 8 significant bits) and reaches the down projection the same
  *   way, so both products see exactly the bf16 rows but for those small
  *   elements.
+ * - FP8_E4M3_NK_A8 (W8A8, opt-in): the weights of FP8_E4M3_NK, and the
+ *   activations quantised per row to one e4m3 term with a dynamic scale, as
+ *   "用SGLang-JAX在TPU上优化Ling-2.6-1T" §5 ("激活量化", "逐通道
+ *   direct_scaled_dot") describes: s = max|row| / 448 and q = e4m3(v / s)
+ *   (fp32 divisions, nearest even, saturating); x per token before the
+ *   permutation, h per row after it is stored in bf16; one 8-bit product per
+ *   multiply-add, (sum q_a q_w) * s_a * s_w[n] after the reduction.  The
+ *   router still projects the bf16 x.  This changes the result (e4m3 keeps
+ *   4 significant bits of each activation); the bf16-activation layouts
+ *   above are the configured arithmetic.
  */
 #ifndef MOE_GB300_H
 #define MOE_GB300_H
@@ -75,7 +86,8 @@ typedef enum {
   MOE_F32 = 0,
   MOE_BF16 = 1,
   MOE_FP8_E4M3 = 2,   /* weights [.., K, N] as the pages write them */
-  MOE_FP8_E4M3_NK = 3 /* the same weights transposed per matrix (moe_pack_weights_nk) */
+  MOE_FP8_E4M3_NK = 3, /* the same weights transposed per matrix (moe_pack_weights_nk) */
+  MOE_FP8_E4M3_NK_A8 = 4 /* FP8_E4M3_NK weights, activations quantised per row (W8A8) */
 } moe_dtype_t;
 
 /* SwiGLU: SiLU(gate) * up.  GEGLU: tanh-approximated GELU(gate) * up. */

@@ -17,7 +17,7 @@ _PKG_DIR = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG_DIR, "libmoe_gb300.so")
 HEADER_PATH = os.path.join(os.path.dirname(_PKG_DIR), "include", "moe.h")
 
-MOE_F32, MOE_BF16, MOE_FP8_E4M3, MOE_FP8_E4M3_NK = 0, 1, 2, 3
+MOE_F32, MOE_BF16, MOE_FP8_E4M3, MOE_FP8_E4M3_NK, MOE_FP8_E4M3_NK_A8 = 0, 1, 2, 3, 4
 MOE_ACT_SWIGLU, MOE_ACT_GEGLU_TANH = 0, 1
 MOE_OK = 0
 MOE_DEV_BAD_EXPERT_ID = 0x1
@@ -29,7 +29,7 @@ WS_SLOTS = ["logits", "topk_ids", "topk_w", "counts", "offsets", "sorted_rows", 
             "x_perm", "h", "y_perm", "h_shared", "s", "x16", "tok_inv", "row_inv"]
 
 _DTYPES = {"f32": MOE_F32, "bf16": MOE_BF16, "fp8_e4m3": MOE_FP8_E4M3,
-           "fp8_e4m3_nk": MOE_FP8_E4M3_NK}
+           "fp8_e4m3_nk": MOE_FP8_E4M3_NK, "fp8_e4m3_nk_a8": MOE_FP8_E4M3_NK_A8}
 _ACTS = {"swiglu": MOE_ACT_SWIGLU, "geglu_tanh": MOE_ACT_GEGLU_TANH}
 
 
@@ -105,12 +105,15 @@ def make_config(T: int, D: int, E: int, k: int, I: int, I_shared: int = 0, act: 
 
 def config_from_shape(shape, fp8_layout: str = "kn") -> MoEConfig:
     """MoEConfig from a workloads.MoEShape-like object.  For fp8 weights,
-    fp8_layout "nk" selects MOE_FP8_E4M3_NK (weights packed by pack_weights_nk)."""
-    if fp8_layout not in ("kn", "nk"):
-        raise ValueError("fp8_layout is 'kn' or 'nk'")
+    fp8_layout "nk" selects MOE_FP8_E4M3_NK (weights packed by pack_weights_nk)
+    and "nk_a8" MOE_FP8_E4M3_NK_A8 (the same weights, W8A8 activations)."""
+    if fp8_layout not in ("kn", "nk", "nk_a8"):
+        raise ValueError("fp8_layout is 'kn', 'nk' or 'nk_a8'")
     w = shape.w_dtype
     if w == "fp8_e4m3" and fp8_layout == "nk":
         w = "fp8_e4m3_nk"
+    if w == "fp8_e4m3" and fp8_layout == "nk_a8":
+        w = "fp8_e4m3_nk_a8"
     return make_config(shape.T, shape.D, shape.E, shape.k, shape.I, shape.I_shared, shape.act,
                        shape.act_dtype, w, shape.renormalize)
 

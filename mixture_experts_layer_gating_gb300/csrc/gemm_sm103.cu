@@ -276,9 +276,10 @@ __device__ __forceinline__ uint2 e4m3x4_to_f16x4(uint32_t w) {
   return r;
 }
 
-// Q8: A rows are two-term e4m3 (hi and lo tiles of the stage, as in SPLIT)
-// and B is e4m3 stored K-contiguous ([G, N, K]): the 8-bit kind::f8f6f4 with
-// 128 K elements (128 bytes) per stage and no weight expansion.
+// Q8: B is e4m3 stored K-contiguous ([G, N, K]): the 8-bit kind::f8f6f4 with
+// 128 K elements (128 bytes) per stage and no weight expansion; the A rows are
+// two-term e4m3 (hi and lo tiles of the stage, as in SPLIT: W8A16) or, with
+// SPLIT off, one e4m3 term with a per-row scale (W8A8).
 template <int EPI, bool SPLIT, bool FP8, bool PAIR, bool Q8>
 __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
@@ -288,7 +289,7 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
                         const __grid_constant__ CUtensorMap tmap_a_tail,
                         const __grid_constant__ CUtensorMap tmap_a_lo_tail, const KParams p) {
   pdl_wait();
-  static_assert(!Q8 || (SPLIT && !FP8), "two-term e4m3 rows use the split A stage layout");
+  static_assert(!Q8 || !FP8, "e4m3 rows meet K-contiguous e4m3 weights, not expanded ones");
   using Cfg = StageCfg<SPLIT, FP8, PAIR>;
   // fp8 weights: fp16 operands; everything else: bf16 operands
   constexpr bool F16 = FP8;
@@ -372,19 +373,20 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
   const int nbox_cta = PAIR ? nbox / 2 : nbox;  // bf16 B boxes this CTA loads
   // barrier addresses in the leader CTA (cluster window) for the pair protocol
   auto leader_bar = [&](uint64_t* bar) { return PAIR ? mapa_shared(bar, 0) : smem_u32(bar); };
-  // swapped tail tile (2-CTA mode): its rows padded so that the MMA N (rows,
-  // or 2 x rows in the down pass) is a multiple of 32 and each CTA's half of
-  // the rows a multiple of 8
-  // Two-term e4m3 rows stack their hi rows (CTA 0) and lo rows (CTA 1) along
-  // N in both passes, N = 2 x rows rounded up to 16.
+  // swapped tail tile (2-CTA mode): the rows are the MMA N operand.  With a
+  // split A (bf16 h_hi / h_lo, or two-term e4m3 rows) CTA 0 loads the first
+  // plane of the rows and CTA 1 the second, stacked along N (N = 2 x rows
+  // rounded up to 16); with one plane (bf16 x, one-term e4m3 rows) each CTA
+  // loads half of the rows (N = rows rounded up to 32, a multiple of 16 per
+  // CTA).
   auto is_swap = [&](const TileInfo& ti) {
     return PAIR && p.swap_tail > 0 && ti.rows <= p.swap_tail;
   };
   auto swap_rows = [&](const TileInfo& ti) {
-    return (EPI == kEpiGateUpAct && !Q8) ? (ti.rows + 31) & ~31 : (ti.rows + 15) & ~15;
+    return SPLIT ? (ti.rows + 15) & ~15 : (ti.rows + 31) & ~31;
   };
   // rows each CTA of the pair loads for a swapped tail, from row swap_row0 on
-  constexpr bool kSplitRowsAcrossPair = EPI == kEpiGateUpAct && !Q8;
+  constexpr bool kSplitRowsAcrossPair = !SPLIT;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -485,7 +487,7 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
           if (gather) {
             tma_gather4_2d(a_dst + lane * 4 * 128, &tmap_a, &ctrl->full[stage], kb * KE, tr[0],
                            tr[1], tr[2], tr[3], pol_a);
-            if (Q8)  // the lo terms of the same rows
+            if (Q8 && SPLIT)  // the lo terms of the same rows
               tma_gather4_2d(a_dst + A_TILE_BYTES + lane * 4 * 128, &tmap_a_lo, &ctrl->full[stage],
                              kb * KE, tr[0], tr[1], tr[2], tr[3], pol_a);
           }
@@ -628,8 +630,8 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
         // swapped tail: A = weights (N-major boxes: MN-major operand), B = rows
         // (K-major), N = rows (gate/up) or 2 x rows (down: h_hi | h_lo)
         const uint32_t idesc_swap =
-            Q8 ? make_idesc_e4m3_f32(TILE_M, 2 * swap_rows(ti))
-               : make_idesc_bf16_f32(TILE_M, (EPI == kEpiGateUpAct ? 1 : 2) * swap_rows(ti), 1, 0);
+            Q8 ? make_idesc_e4m3_f32(TILE_M, (SPLIT ? 2 : 1) * swap_rows(ti))
+               : make_idesc_bf16_f32(TILE_M, (SPLIT ? 2 : 1) * swap_rows(ti), 1, 0);
         const uint32_t idesc_q8 = make_idesc_e4m3_f32(TILE_M, p.bn);
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&ctrl->full[stage], phase, abort_flag)) {
@@ -639,7 +641,8 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
           tc_fence_after_sync();
           if (PAIR && swap && Q8) {
             // weights (K-major, 128 rows per CTA) as the M = 256 operand; the
-            // hi rows (CTA 0) and lo rows (CTA 1) as N
+            // hi rows (CTA 0) and lo rows (CTA 1), or each CTA's half of the
+            // one-term rows, as N
             const uint64_t wdesc0 = make_smem_desc_sw128(smem_u32(stage_b(stage)), 16, 1024);
             const uint64_t rdesc0 = make_smem_desc_sw128(smem_u32(stage_a(stage)), 16, 1024);
 #pragma unroll
@@ -670,7 +673,8 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
           }
           if (Q8) {
             // A hi / lo and B all K-major with 128-byte rows; a K step of 32
-            // e4m3 is 32 bytes.  acc += hi * B, then += lo * B.
+            // e4m3 is 32 bytes.  acc += hi * B, then += lo * B (one-term rows:
+            // the hi product only).
             const uint64_t adesc0 = make_smem_desc_sw128(smem_u32(stage_a(stage)), 16, 1024);
             const uint64_t bdesc0 = make_smem_desc_sw128(smem_u32(stage_b(stage)), 16, 1024);
 #pragma unroll
@@ -680,10 +684,10 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
               const uint64_t alo = smem_desc_advance(adesc0, A_TILE_BYTES + kk * 32);
               if (PAIR) {
                 tc_mma_f8_pair(d_tmem, ahi, bdesc, idesc_q8, ((kb - kb0) | kk) != 0);
-                tc_mma_f8_pair(d_tmem, alo, bdesc, idesc_q8, 1);
+                if (SPLIT) tc_mma_f8_pair(d_tmem, alo, bdesc, idesc_q8, 1);
               } else {
                 tc_mma_f8(d_tmem, ahi, bdesc, idesc_q8, ((kb - kb0) | kk) != 0);
-                tc_mma_f8(d_tmem, alo, bdesc, idesc_q8, 1);
+                if (SPLIT) tc_mma_f8(d_tmem, alo, bdesc, idesc_q8, 1);
               }
             }
             if (PAIR) tc_commit_pair_multicast(&ctrl->empty[stage], 0x3);
@@ -826,11 +830,11 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
         if (is_swap(tw)) {
           const int R = swap_rows(tw);  // accumulator columns per plane
           bool ok = true;
-          // two-term e4m3 rows: columns [0, R) hold the hi products of rows
-          // 0..R-1, [R, 2R) their lo products
+          // split rows (two-term e4m3): columns [0, R) hold the hi products
+          // of rows 0..R-1, [R, 2R) their lo products
           auto load_cols = [&](int c, uint32_t (&v)[32]) {
             tmem_ld_32x32b_x32(taddr + c, v);
-            if (Q8) {
+            if (SPLIT) {
               uint32_t lo[32];
               tmem_ld_32x32b_x32(taddr + R + c, lo);
               tc_wait_ld();
@@ -895,7 +899,8 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
             xch_phase ^= 1u;
           } else {
             // lanes = output features n0 + 128 r + (0..127); columns j (h_hi rows,
-            // or hi e4m3 terms) and R + j (h_lo rows, lo terms) add up to row j's result
+            // or hi e4m3 terms) and R + j (h_lo rows, lo terms) add up to row j's
+            // result (one plane: column j alone)
             const int f = ti.n0 + 128 * static_cast<int>(rank) + quarter * 32 + lane;
             const float cs =
                 (p.b_scale && f < p.N) ? p.b_scale[static_cast<size_t>(ti.g) * p.N + f] : 1.0f;
@@ -903,7 +908,12 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
             for (int c = 0; c < R; c += 32) {
               uint32_t hi[32], lo[32];
               tmem_ld_32x32b_x32(taddr + c, hi);
-              tmem_ld_32x32b_x32(taddr + R + c, lo);
+              if (SPLIT) {
+                tmem_ld_32x32b_x32(taddr + R + c, lo);
+              } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) lo[j] = 0u;  // +0.0f
+              }
               tc_wait_ld();
               if (f < p.N) {
 #pragma unroll 4
@@ -1138,7 +1148,7 @@ __global__ void __launch_bounds__(DecCfg<SPLIT, FP8>::kThreads, 1)
                                const __grid_constant__ CUtensorMap tmap_rows_lo,
                                const __grid_constant__ CUtensorMap tmap_w, const KParams p) {
   pdl_wait();
-  static_assert(!Q8 || (SPLIT && !FP8), "two-term e4m3 rows use the split row layout");
+  static_assert(!Q8 || !FP8, "e4m3 rows meet K-contiguous e4m3 weights, not expanded ones");
   constexpr int KE = Q8 ? 128 : BK;  // K elements per stage (128 bytes of every operand row)
   using Cfg = DecCfg<SPLIT, FP8>;
   constexpr int STAGES = Cfg::kStages;
@@ -1616,19 +1626,22 @@ cudaError_t launch_dec(const CUtensorMap& tr, const CUtensorMap& tr_lo, const CU
   return launch_kernel(kern, dim3(grid), dim3(threads), smem, s, tr, tr_lo, tw, kp);
 }
 
-// Swap-AB launch for decode-size groups, two-term e4m3 rows and K-contiguous
-// e4m3 weights: nt rows per tile (2 nt MMA columns: hi rows, then lo rows).
+// Swap-AB launch for decode-size groups, e4m3 rows and K-contiguous e4m3
+// weights: nt rows per tile (two-term rows: 2 nt MMA columns, hi rows then lo
+// rows; one-term rows: nt).
 cudaError_t launch_grouped_gemm_decode_q8(const GroupedGemmArgs& a, int nt, cudaStream_t s) {
   CUtensorMap tr, tr_lo, tw;
   const uint64_t K = static_cast<uint64_t>(a.K), N = static_cast<uint64_t>(a.N);
   const uint64_t M = static_cast<uint64_t>(a.M), G = static_cast<uint64_t>(a.G);
   const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const bool one = a.a_e4m3 != 0;  // one-term rows [M, K]; else two-term [M, 2K]
   {
     const uint64_t dims[2] = {K, M};
-    const uint64_t strides[1] = {2 * K};
+    const uint64_t strides[1] = {one ? K : 2 * K};
     const uint32_t box[2] = {128, static_cast<uint32_t>(nt)};
     if (!encode_tmap(&tr, a.A, 2, dims, strides, box, u8)) return cudaErrorInvalidValue;
-    if (!encode_tmap(&tr_lo, static_cast<const uint8_t*>(a.A) + K, 2, dims, strides, box, u8))
+    if (one) tr_lo = tr;
+    else if (!encode_tmap(&tr_lo, static_cast<const uint8_t*>(a.A) + K, 2, dims, strides, box, u8))
       return cudaErrorInvalidValue;
   }
   KParams kp{};
@@ -1662,6 +1675,10 @@ cudaError_t launch_grouped_gemm_decode_q8(const GroupedGemmArgs& a, int nt, cuda
   kp.n_tiles = (a.N + kp.cols_per_tile - 1) / kp.cols_per_tile;
   const long long max_tiles =
       (static_cast<long long>((a.M + nt - 1) / nt) + a.G) * static_cast<long long>(kp.n_tiles);
+  if (one)
+    return a.epilogue == kEpiGateUpAct
+               ? launch_dec<kEpiGateUpAct, false, false, true>(tr, tr_lo, tw, kp, max_tiles, s)
+               : launch_dec<kEpiStoreF32, false, false, true>(tr, tr_lo, tw, kp, max_tiles, s);
   if (a.epilogue == kEpiGateUpAct)
     return launch_dec<kEpiGateUpAct, true, false, true>(tr, tr_lo, tw, kp, max_tiles, s);
   return launch_dec<kEpiStoreF32, true, false, true>(tr, tr_lo, tw, kp, max_tiles, s);
@@ -1669,7 +1686,7 @@ cudaError_t launch_grouped_gemm_decode_q8(const GroupedGemmArgs& a, int nt, cuda
 
 // Swap-AB launch for decode-size groups: nt rows per tile.
 cudaError_t launch_grouped_gemm_decode(const GroupedGemmArgs& a, int nt, cudaStream_t s) {
-  if (a.a_e4m3x2) return launch_grouped_gemm_decode_q8(a, nt, s);
+  if (a.a_e4m3x2 || a.a_e4m3) return launch_grouped_gemm_decode_q8(a, nt, s);
   CUtensorMap tr, tr_lo, tw;
   const CUtensorMapDataType adt =
       a.a_fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -1727,8 +1744,9 @@ cudaError_t launch_grouped_gemm_decode(const GroupedGemmArgs& a, int nt, cudaStr
                 : launch_dec<kEpiStoreF32, false, false>(tr, tr_lo, tw, kp, max_tiles, s);
 }
 
-// 128-row (or 2-CTA 256-row) tiles for two-term e4m3 rows and K-contiguous
-// e4m3 weights: kind::f8f6f4, hi and lo products into one accumulator.
+// 128-row (or 2-CTA 256-row) tiles for e4m3 rows and K-contiguous e4m3
+// weights: kind::f8f6f4; two-term rows put the hi and lo products into one
+// accumulator, one-term rows (W8A8) one product.
 cudaError_t launch_grouped_gemm_q8(const GroupedGemmArgs& a, cudaStream_t s) {
   if (!a.b_fp8 || a.A_lo || a.ksplit > 1 || a.bias) return cudaErrorInvalidValue;
   if (a.a_gather && (a.a_rows < 1 || a.gather_k < 1)) return cudaErrorInvalidValue;
@@ -1773,24 +1791,28 @@ cudaError_t launch_grouped_gemm_q8(const GroupedGemmArgs& a, cudaStream_t s) {
   // rows runs swapped (weights as the M = 256 operand, hi and lo rows as N)
   kp.swap_tail = (pair && g_pair_tiles != 2) ? (a.epilogue == kEpiGateUpAct ? 64 : 128) : 0;
   CUtensorMap ta, ta_lo, tb, ta_tail, ta_lo_tail, tb_tail;
+  const bool one = a.a_e4m3 != 0;  // one-term rows [M, K]; else two-term [M, 2K] (hi | lo)
   {
     const uint64_t dims[2] = {K, M};
-    const uint64_t strides[1] = {2 * K};
+    const uint64_t strides[1] = {one ? K : 2 * K};
     const uint32_t box[2] = {128, BM};
     const uint8_t* lo = static_cast<const uint8_t*>(a.A) + K;
     if (a.a_gather) {
-      // row gather from the [a_rows, 2K] two-term rows: one-row boxes, 4 rows per load
+      // row gather from the [a_rows, .] rows: one-row boxes, 4 rows per load
       const uint64_t gdims[2] = {K, static_cast<uint64_t>(a.a_rows)};
       const uint32_t gbox[2] = {128, 1};
       if (!encode_tmap(&ta, a.A, 2, gdims, strides, gbox, u8)) return cudaErrorInvalidValue;
-      if (!encode_tmap(&ta_lo, lo, 2, gdims, strides, gbox, u8)) return cudaErrorInvalidValue;
+      if (one) ta_lo = ta;
+      else if (!encode_tmap(&ta_lo, lo, 2, gdims, strides, gbox, u8)) return cudaErrorInvalidValue;
     } else {
       if (!encode_tmap(&ta, a.A, 2, dims, strides, box, u8)) return cudaErrorInvalidValue;
-      if (!encode_tmap(&ta_lo, lo, 2, dims, strides, box, u8)) return cudaErrorInvalidValue;
+      if (one) ta_lo = ta;
+      else if (!encode_tmap(&ta_lo, lo, 2, dims, strides, box, u8)) return cudaErrorInvalidValue;
     }
     const uint32_t tbox[2] = {128, 32};  // swapped tails: 32-row boxes
     if (!encode_tmap(&ta_tail, a.A, 2, dims, strides, tbox, u8)) return cudaErrorInvalidValue;
-    if (!encode_tmap(&ta_lo_tail, lo, 2, dims, strides, tbox, u8)) return cudaErrorInvalidValue;
+    if (one) ta_lo_tail = ta_tail;
+    else if (!encode_tmap(&ta_lo_tail, lo, 2, dims, strides, tbox, u8)) return cudaErrorInvalidValue;
   }
   if (a.epilogue == kEpiGateUpAct) {  // [G][2][N][K]: gate rows, then up rows
     const uint64_t dims[4] = {K, N, 2, G};
@@ -1809,12 +1831,19 @@ cudaError_t launch_grouped_gemm_q8(const GroupedGemmArgs& a, cudaStream_t s) {
   const int tile_m = pair ? 2 * BM : BM;
   const long long max_tiles = (static_cast<long long>((a.M + tile_m - 1) / tile_m) + a.G) *
                               static_cast<long long>(kp.n_tiles);
-#define MOE_LAUNCH_Q8(E_, P_) \
-  launch_epi<E_, true, false, P_, true>(ta, ta_lo, tb, tb_tail, ta_tail, ta_lo_tail, kp, max_tiles, s)
+#define MOE_LAUNCH_Q8(E_, S_, P_) \
+  launch_epi<E_, S_, false, P_, true>(ta, ta_lo, tb, tb_tail, ta_tail, ta_lo_tail, kp, max_tiles, s)
+  if (one) {
+    if (a.epilogue == kEpiGateUpAct)
+      return pair ? MOE_LAUNCH_Q8(kEpiGateUpAct, false, true) : MOE_LAUNCH_Q8(kEpiGateUpAct, false, false);
+    if (a.epilogue == kEpiStoreF32)
+      return pair ? MOE_LAUNCH_Q8(kEpiStoreF32, false, true) : MOE_LAUNCH_Q8(kEpiStoreF32, false, false);
+    return cudaErrorInvalidValue;
+  }
   if (a.epilogue == kEpiGateUpAct)
-    return pair ? MOE_LAUNCH_Q8(kEpiGateUpAct, true) : MOE_LAUNCH_Q8(kEpiGateUpAct, false);
+    return pair ? MOE_LAUNCH_Q8(kEpiGateUpAct, true, true) : MOE_LAUNCH_Q8(kEpiGateUpAct, true, false);
   if (a.epilogue == kEpiStoreF32)
-    return pair ? MOE_LAUNCH_Q8(kEpiStoreF32, true) : MOE_LAUNCH_Q8(kEpiStoreF32, false);
+    return pair ? MOE_LAUNCH_Q8(kEpiStoreF32, true, true) : MOE_LAUNCH_Q8(kEpiStoreF32, true, false);
 #undef MOE_LAUNCH_Q8
   return cudaErrorInvalidValue;
 }
@@ -1857,7 +1886,8 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
   // per group) measured 2201 us per layer on them against 2380 us on 128-row
   // tiles and 2606 us on 16-row decode tiles with e4m3 rows.
   const long long Mg = a.M, Gg = a.G;
-  if (a.a_e4m3x2 && (!a.b_fp8 || a.a_fp16)) return cudaErrorInvalidValue;
+  if ((a.a_e4m3x2 || a.a_e4m3) && (!a.b_fp8 || a.a_fp16 || (a.a_e4m3x2 && a.a_e4m3)))
+    return cudaErrorInvalidValue;
   int nt = 0;
   if (g_decode_kernel == 2) nt = DEC_NT_MAX;
   else if (g_decode_kernel == 3) nt = 16;
@@ -1867,11 +1897,11 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
   else if (a.b_fp8 && Mg <= 16 * Gg) nt = DEC_NT_MAX;
   if (g_decode_kernel && nt && a.decode_ok && !a.a_gather && a.ksplit <= 1 && a.G <= MAX_G &&
       (a.epilogue == kEpiGateUpAct || a.epilogue == kEpiStoreF32)) {
-    if (!a.a_e4m3x2 && (a.a_fp16 != 0) != (a.b_fp8 != 0)) return cudaErrorInvalidValue;
+    if (!a.a_e4m3x2 && !a.a_e4m3 && (a.a_fp16 != 0) != (a.b_fp8 != 0)) return cudaErrorInvalidValue;
     if (a.b_fp8 && a.A_lo) return cudaErrorNotSupported;
     return launch_grouped_gemm_decode(a, nt, s);
   }
-  if (a.a_e4m3x2) return launch_grouped_gemm_q8(a, s);
+  if (a.a_e4m3x2 || a.a_e4m3) return launch_grouped_gemm_q8(a, s);
   if (a.b_fp8 && a.A_lo) return cudaErrorNotSupported;
   // fp16 A rows exactly when the weights are fp8
   if ((a.a_fp16 != 0) != (a.b_fp8 != 0)) return cudaErrorInvalidValue;

@@ -101,9 +101,10 @@ bool cfg_valid(const moe_config_t* c) {
   if (c->act != MOE_ACT_SWIGLU && c->act != MOE_ACT_GEGLU_TANH) return false;
   if (c->act_dtype != MOE_F32 && c->act_dtype != MOE_BF16) return false;
   if (c->w_dtype != MOE_F32 && c->w_dtype != MOE_BF16 && c->w_dtype != MOE_FP8_E4M3 &&
-      c->w_dtype != MOE_FP8_E4M3_NK)
+      c->w_dtype != MOE_FP8_E4M3_NK && c->w_dtype != MOE_FP8_E4M3_NK_A8)
     return false;
-  if ((c->w_dtype == MOE_FP8_E4M3 || c->w_dtype == MOE_FP8_E4M3_NK) &&
+  if ((c->w_dtype == MOE_FP8_E4M3 || c->w_dtype == MOE_FP8_E4M3_NK ||
+       c->w_dtype == MOE_FP8_E4M3_NK_A8) &&
       (c->D % 16 || c->I % 16 || c->I_shared % 16))
     return false;
   const long long R = static_cast<long long>(c->T) * c->k;
@@ -113,27 +114,42 @@ bool cfg_valid(const moe_config_t* c) {
 
 bool combo_supported(const moe_config_t* c) {
   if (c->act_dtype == MOE_F32) return c->w_dtype == MOE_F32;
-  return c->w_dtype == MOE_BF16 || c->w_dtype == MOE_FP8_E4M3 || c->w_dtype == MOE_FP8_E4M3_NK;
+  return c->w_dtype == MOE_BF16 || c->w_dtype == MOE_FP8_E4M3 || c->w_dtype == MOE_FP8_E4M3_NK ||
+         c->w_dtype == MOE_FP8_E4M3_NK_A8;
 }
 
 }  // namespace moe
 
 namespace {
 
-// fp8 weights of either layout (per-column scales, rows with power-of-two scales)
+// fp8 weights of any layout (per-column scales; A rows in an fp8 layer form
+// with per-row scales)
 inline bool is_fp8(const moe_config_t* c) {
-  return c->w_dtype == MOE_FP8_E4M3 || c->w_dtype == MOE_FP8_E4M3_NK;
+  return c->w_dtype == MOE_FP8_E4M3 || c->w_dtype == MOE_FP8_E4M3_NK ||
+         c->w_dtype == MOE_FP8_E4M3_NK_A8;
 }
-// fp8 weights stored K-contiguous: the 8-bit kind with two-term e4m3 rows
-inline bool is_nk(const moe_config_t* c) { return c->w_dtype == MOE_FP8_E4M3_NK; }
+// fp8 weights stored K-contiguous: the 8-bit kind (two-term e4m3 rows, or
+// one-term rows for W8A8)
+inline bool is_nk(const moe_config_t* c) {
+  return c->w_dtype == MOE_FP8_E4M3_NK || c->w_dtype == MOE_FP8_E4M3_NK_A8;
+}
+// W8A8: activations quantised per row to one e4m3 term with a dynamic scale
+inline bool is_a8(const moe_config_t* c) { return c->w_dtype == MOE_FP8_E4M3_NK_A8; }
 
 // bf16 / fp32 rows -> the A-row form of an fp8 layer: fp16 rows (expanded
 // weights) or two-term e4m3 rows (K-contiguous weights), both D * 2 bytes per
-// row, with inverse power-of-two scales.
+// row, with inverse power-of-two scales; or, for W8A8, one-term e4m3 rows of
+// D bytes with their dynamic scales.
 cudaError_t rows_to_fp8_layer_form(const moe_config_t* c, const void* x, int rows, int D, void* q,
                                    float* inv_scale, cudaStream_t s, bool src_f32 = false) {
+  if (is_a8(c)) return launch_rows_to_e4m3(x, rows, D, q, inv_scale, s, src_f32);
   return is_nk(c) ? launch_rows_to_e4m3x2(x, rows, D, q, inv_scale, s, src_f32)
                   : launch_rows_to_fp16(x, rows, D, q, inv_scale, s, src_f32);
+}
+// Bytes per row of D elements in the form moe_layer permutes: x itself, or
+// for fp8 layers their A-row form (2 bytes per element, 1 for W8A8).
+inline size_t layer_row_bytes(const moe_config_t* c) {
+  return static_cast<size_t>(c->D) * (is_a8(c) ? 1 : act_bytes(c->act_dtype));
 }
 
 Layout make_layout(const moe_config_t* c) {
@@ -243,9 +259,10 @@ int do_route(const moe_config_t* c, const void* x, const void* Wg, const float* 
                                          c->renormalize, ids, w, err, s));
 }
 
+// row_bytes: bytes of one row of x (act_dtype rows, or moe_layer's fp8 row form)
 int do_permute(const moe_config_t* c, const int32_t* ids, const void* x, int32_t* counts,
                int32_t* offsets, int32_t* sorted_rows, int32_t* dest, void* x_perm,
-               int32_t* seg_scratch, int32_t* err, cudaStream_t s,
+               int32_t* seg_scratch, int32_t* err, cudaStream_t s, size_t row_bytes,
                const float* tok_scale = nullptr, float* row_scale = nullptr) {
   const int R = c->T * c->k;
   if (small_route(R, c->E)) {  // one launch: sort + gather
@@ -253,7 +270,7 @@ int do_permute(const moe_config_t* c, const int32_t* ids, const void* x, int32_t
     const bool gather = x && x_perm;
     return cuda_status(launch_route_permute_small(
         ids, R, c->E, c->k, c->T, counts, offsets, sorted_rows, dest, gather ? x : nullptr,
-        static_cast<size_t>(c->D) * act_bytes(c->act_dtype), gather ? x_perm : nullptr, tok_scale,
+        row_bytes, gather ? x_perm : nullptr, tok_scale,
         row_scale, err, s));
   }
   cudaError_t e = launch_init_routing(ids, R, c->E, counts, offsets, sorted_rows, dest, seg_scratch,
@@ -266,7 +283,6 @@ int do_permute(const moe_config_t* c, const int32_t* ids, const void* x, int32_t
     // once and write its k copies (Qwen3.5-style prefill, 67 MB of x: 162 ->
     // 117 us; Ling-style, 268 MB: 600 -> 388 us; Qwen3-style, 17 MB: 27.5 vs
     // 28.8 us in favour of the gather)
-    const size_t row_bytes = static_cast<size_t>(c->D) * act_bytes(c->act_dtype);
     if (static_cast<size_t>(c->T) * row_bytes > (size_t{32} << 20))
       e = launch_permute_scatter(x, dest, offsets + c->E, R, c->k, c->T, row_bytes, x_perm, err, s,
                                  tok_scale, row_scale);
@@ -318,7 +334,8 @@ int do_ffn(const moe_config_t* c, const void* A, const float* a_row_scale, int M
   a.B = W13;
   a.b_fp8 = fp8;
   a.a_fp16 = fp8 && !nk;
-  a.a_e4m3x2 = nk;
+  a.a_e4m3x2 = nk && !is_a8(c);
+  a.a_e4m3 = is_a8(c);
   a.a_row_scale = a_row_scale;
   a.a_gather = a_gather;
   a.gather_k = c->k;
@@ -432,7 +449,8 @@ int moe_permute(const moe_config_t* cfg, const int32_t* topk_ids, const void* x,
   const Layout L = make_layout(cfg);
   return do_permute(cfg, topk_ids, x, counts, offsets, sorted_rows, dest, x_perm,
                     reinterpret_cast<int32_t*>(ws_at(ws, L.seg_scratch)), err_word(ws),
-                    static_cast<cudaStream_t>(stream));
+                    static_cast<cudaStream_t>(stream),
+                    static_cast<size_t>(cfg->D) * act_bytes(cfg->act_dtype));
 }
 
 int moe_grouped_ffn(const moe_config_t* cfg, const void* x_perm, const int32_t* offsets,
@@ -573,7 +591,7 @@ int moe_layer(const moe_config_t* cfg, const void* x, const void* Wg, const floa
   // four-row requests per 16 KB A tile).
   const bool gather = g_gather_a && cfg->act_dtype != MOE_F32;
   st = do_permute(cfg, ids, gather ? nullptr : x_rows, counts, offsets, sorted_rows, dest,
-                  gather ? nullptr : x_perm, seg, err, s, tok_inv, row_inv);
+                  gather ? nullptr : x_perm, seg, err, s, layer_row_bytes(cfg), tok_inv, row_inv);
   if (st != MOE_OK) return fail(st);
   st = do_grouped_ffn(cfg, gather ? x_rows : x_perm, gather ? tok_inv : row_inv, offsets, W13, s13,
                       W2, s2, h, y_perm, (shared && !side) ? x_rows : nullptr, tok_inv, W13s, s13s,

@@ -125,6 +125,10 @@ cudaError_t launch_rows_to_fp16(const void* x, int rows, int D, void* x16, float
 // |element| in [128, 256); inv_scale[r] = the inverse power of two.
 cudaError_t launch_rows_to_e4m3x2(const void* x, int rows, int D, void* q, float* inv_scale,
                                   cudaStream_t s, bool src_f32 = false);
+// bf16 (or fp32) rows -> one-term e4m3 rows [rows, D] with a dynamic per-row
+// scale (W8A8): scale[r] = max|row| / 448, q = e4m3(x / scale[r]).
+cudaError_t launch_rows_to_e4m3(const void* x, int rows, int D, void* q, float* scale,
+                                cudaStream_t s, bool src_f32 = false);
 // W_nk[g][n][c] = W[g][c][n], one-byte elements (K, N multiples of 16).
 cudaError_t launch_transpose_bytes(const void* W, long long G, int K, int N, void* W_nk,
                                    cudaStream_t s);
@@ -172,6 +176,8 @@ struct GroupedGemmArgs {
   int a_e4m3x2;                  // 1: A rows are two-term e4m3 [M, 2K] (hi | lo) and B is
                                  //    e4m3 stored [G, N, K] (gate/up: [G, 2N, K]):
                                  //    the 8-bit tensor-core kind, no expansion
+  int a_e4m3;                    // 1: A rows are one-term e4m3 [M, K] with a per-row scale
+                                 //    in a_row_scale (W8A8), B as for a_e4m3x2
   int h_fp32;                    // gate/up pass: store h as fp32 (no lo plane)
   int ksplit;                    // >1: K split into planes out[s] = partial sums (fp32 store only)
   int pair_ok;                   // 1: 2-CTA (M=256) tiles may be used

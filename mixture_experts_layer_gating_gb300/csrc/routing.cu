@@ -773,9 +773,28 @@ __device__ __forceinline__ void e4m3x2_terms8(const float (&f)[8], float sc, uin
   lo = make_uint2(lw[0], lw[1]);
 }
 
+// W8A8 rows (one e4m3 term, dynamic per-row scale): the "用SGLang-JAX在TPU上
+// 优化Ling-2.6-1T" §5 activation quantisation.  s = m / 448 for a row whose
+// largest |element| is m (1 for an all-zero row), code = e4m3(v / s), both
+// divisions correctly rounded in fp32, round to nearest even, saturating.
+__device__ __forceinline__ float e4m3_row_scale(float m) {
+  return (m > 0.0f && isfinite(m)) ? __fdiv_rn(m, 448.0f) : 1.0f;
+}
+// the codes of 8 consecutive elements under the row scale s (8 bytes)
+__device__ __forceinline__ uint2 e4m3_codes8(const float (&f)[8], float s) {
+  uint32_t w[2] = {0u, 0u};
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    w[i >> 1] |= f32x2_to_e4m3x2(__fdiv_rn(f[2 * i], s), __fdiv_rn(f[2 * i + 1], s)) << (16 * (i & 1));
+  return make_uint2(w[0], w[1]);
+}
+
 // One warp per row; the row is read twice (maximum, then conversion), the
 // second time mostly from cache.  For rows outside the register kernel's range.
-template <typename Tin>
+// A8: one e4m3 term with the dynamic scale (output rows of D bytes,
+// inv_scale[r] = s), else two terms with a power-of-two scale (rows of 2D
+// bytes, inv_scale[r] = 2^-e).
+template <typename Tin, bool A8>
 __global__ void rows_to_e4m3x2_kernel(const Tin* __restrict__ x, int rows, int D,
                                       uint8_t* __restrict__ q, float* __restrict__ inv_scale) {
   pdl_wait();
@@ -806,6 +825,18 @@ __global__ void rows_to_e4m3x2_kernel(const Tin* __restrict__ x, int rows, int D
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(FULL, m, off));
+    if (A8) {
+      const float sr = e4m3_row_scale(m);
+      if (lane == 0) inv_scale[r] = sr;
+      uint8_t* row = q + r * D;
+#pragma unroll 4
+      for (int v = lane; v < nvec; v += 32) {
+        float f[8];
+        load8f(src, v, f);
+        *reinterpret_cast<uint2*>(row + 8 * v) = e4m3_codes8(f, sr);
+      }
+      continue;
+    }
     const int e = e4m3x2_row_exp(m);
     const float sc = exp2_int(e);
     if (lane == 0) inv_scale[r] = exp2_int(-e);
@@ -831,7 +862,7 @@ __global__ void rows_to_e4m3x2_kernel(const Tin* __restrict__ x, int rows, int D
 // the second pass reads them from HBM again.
 constexpr int kRegRowVecs = 4;
 constexpr int kRegRowBlocksPerSm = 5;  // resident blocks at <= 48 registers, no spills
-template <typename Tin>
+template <typename Tin, bool A8>
 __global__ void __launch_bounds__(256, kRegRowBlocksPerSm) rows_to_e4m3x2_reg_kernel(
     const Tin* __restrict__ x, int rows, int D, int tpr_log2, uint8_t* __restrict__ q,
     float* __restrict__ inv_scale) {
@@ -878,6 +909,21 @@ __global__ void __launch_bounds__(256, kRegRowBlocksPerSm) rows_to_e4m3x2_reg_ke
     for (int w = 1; w < wpr; ++w) m = fmaxf(m, red[buf][g * wpr + w]);
     buf ^= 1;
     if (!valid) continue;
+    if (A8) {
+      const float sr = e4m3_row_scale(m);
+      if (li == 0) inv_scale[r] = sr;
+      uint8_t* row = q + r * D;
+#pragma unroll
+      for (int j = 0; j < kRegRowVecs; ++j) {
+        const int v = li + tpr * j;
+        if (v < nvec) {
+          float f[8];
+          unpack8(raw[j], f);
+          *reinterpret_cast<uint2*>(row + 8 * v) = e4m3_codes8(f, sr);
+        }
+      }
+      continue;
+    }
     const int e = e4m3x2_row_exp(m);
     const float sc = exp2_int(e);
     if (li == 0) inv_scale[r] = exp2_int(-e);
@@ -1176,8 +1222,10 @@ cudaError_t launch_rows_to_fp16(const void* x, int rows, int D, void* x16, float
   return cudaGetLastError();
 }
 
-cudaError_t launch_rows_to_e4m3x2(const void* x, int rows, int D, void* q, float* inv_scale,
-                                  cudaStream_t s, bool src_f32) {
+namespace {
+template <bool A8>
+cudaError_t launch_rows_e4m3(const void* x, int rows, int D, void* q, float* inv_scale,
+                             cudaStream_t s, bool src_f32) {
   if (rows <= 0) return cudaSuccess;
   const int threads = 256;
   const int nvec = D / 8;
@@ -1187,23 +1235,34 @@ cudaError_t launch_rows_to_e4m3x2(const void* x, int rows, int D, void* q, float
     const int blocks =
         blocks_for(rows, threads >> tpr_log2, device_sm_count() * kRegRowBlocksPerSm);
     if (src_f32)
-      MOE_LAUNCH(rows_to_e4m3x2_reg_kernel<float>, blocks, threads, 0, s,
+      MOE_LAUNCH((rows_to_e4m3x2_reg_kernel<float, A8>), blocks, threads, 0, s,
                  static_cast<const float*>(x), rows, D, tpr_log2, static_cast<uint8_t*>(q),
                  inv_scale);
     else
-      MOE_LAUNCH(rows_to_e4m3x2_reg_kernel<__nv_bfloat16>, blocks, threads, 0, s,
+      MOE_LAUNCH((rows_to_e4m3x2_reg_kernel<__nv_bfloat16, A8>), blocks, threads, 0, s,
                  static_cast<const __nv_bfloat16*>(x), rows, D, tpr_log2,
                  static_cast<uint8_t*>(q), inv_scale);
     return cudaGetLastError();
   }
   const int blocks = blocks_for(rows, threads / 32, device_sm_count() * 16);
   if (src_f32)
-    MOE_LAUNCH(rows_to_e4m3x2_kernel<float>, blocks, threads, 0, s, static_cast<const float*>(x),
-               rows, D, static_cast<uint8_t*>(q), inv_scale);
+    MOE_LAUNCH((rows_to_e4m3x2_kernel<float, A8>), blocks, threads, 0, s,
+               static_cast<const float*>(x), rows, D, static_cast<uint8_t*>(q), inv_scale);
   else
-    MOE_LAUNCH(rows_to_e4m3x2_kernel<__nv_bfloat16>, blocks, threads, 0, s,
+    MOE_LAUNCH((rows_to_e4m3x2_kernel<__nv_bfloat16, A8>), blocks, threads, 0, s,
                static_cast<const __nv_bfloat16*>(x), rows, D, static_cast<uint8_t*>(q), inv_scale);
   return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_rows_to_e4m3x2(const void* x, int rows, int D, void* q, float* inv_scale,
+                                  cudaStream_t s, bool src_f32) {
+  return launch_rows_e4m3<false>(x, rows, D, q, inv_scale, s, src_f32);
+}
+
+cudaError_t launch_rows_to_e4m3(const void* x, int rows, int D, void* q, float* scale,
+                                cudaStream_t s, bool src_f32) {
+  return launch_rows_e4m3<true>(x, rows, D, q, scale, s, src_f32);
 }
 
 cudaError_t launch_transpose_bytes(const void* W, long long G, int K, int N, void* W_nk,
