@@ -128,7 +128,7 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"]}
         inside = [l for (t, l) in self.lines if self.t_start and self.t_end and self.t_start <= t <= self.t_end + 0.15]
         used = inside if inside else [l for (_, l) in self.lines]
-        sm, smax, reasons = [], [], set()
+        sm, smax, pw, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for l in used:
             parts = [p.strip() for p in l.split(",")]
@@ -139,12 +139,17 @@ class ClockSampler:
                 smax.append(float(parts[3]))
             except ValueError:
                 continue
+            try:
+                pw.append(float(parts[4]))
+            except ValueError:
+                pass
             for n, v in zip(names, parts[6:10]):
                 if v.lower() == "active":
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
                 "reasons": sorted(reasons),
+                "power_w": statistics.median(pw) if pw else None,
                 "samples": len(sm),
                 "window": "timed region" if inside else "whole run (timed region shorter than the sampling period)"}
 
@@ -247,6 +252,7 @@ def memory_kernel_bytes(shape, name: str, rows_form_bytes: int, nk: bool = False
         "route_permute": 4 * R + T * D * gathered + R * D * gathered + 8 * R + 8 * E,
         "permute_gather": T * D * gathered + 4 * R + R * D * gathered,
         "finalize": R * D * yb + 4 * R + 4 * T * k + (T * D * yb if Is else 0) + T * D * ab,
+        "combine_round": T * D * 4 + (T * D * yb if Is else 0) + T * D * ab,
     }
     rf = rows_form_bytes
     for pre in ("x_to_fp16", "x_to_e4m3x2", "x_to_e4m3"):
@@ -321,6 +327,8 @@ def set_options(moe, args):
         moe.moe_set_option(moe.MOE_OPT_PDL, 0)
     if args.serial_shared:
         moe.moe_set_option(moe.MOE_OPT_SHARED_STREAM, 0)
+    if args.fused_combine:
+        moe.moe_set_option(moe.MOE_OPT_FUSED_COMBINE, 1)
 
 
 def pct(v, q):
@@ -334,7 +342,7 @@ def pct(v, q):
     return v[lo] + (v[hi] - v[lo]) * (pos - lo)
 
 
-def kernel_names(shape, nk, gather_a, a8=False):
+def kernel_names(shape, nk, gather_a, a8=False, fused=False):
     """Names of the kernels one moe_layer call launches, in launch order."""
     fp8 = shape.w_dtype == "fp8_e4m3"
     rows = "e4m3" if a8 else "e4m3x2" if nk else "fp16"  # the A-row form of fp8 layers
@@ -349,7 +357,7 @@ def kernel_names(shape, nk, gather_a, a8=False):
     names += ["w2_down"]
     if shape.I_shared:
         names += ["shared_w13"] + ([f"shared_h_to_{rows}"] if fp8 else []) + ["shared_w2"]
-    names += ["finalize"]
+    names += ["combine_round" if fused else "finalize"]
     return names
 
 
@@ -423,7 +431,8 @@ def measure(args, world, rank, local, shape, primary: bool, layout: str):
 
     # ---- per-kernel durations (instrumented pass, same work, after the timed region)
     L = moe.moe_layer_launch_count(cfg)
-    names = kernel_names(shape, nk, args.gather_a, a8)
+    fused = args.fused_combine and shape.act_dtype == "bf16" and (nk or not fp8)
+    names = kernel_names(shape, nk, args.gather_a, a8, fused)
     assert len(names) == L
     per = [[] for _ in range(L)]
     for _ in range(args.steps):
@@ -668,6 +677,9 @@ def main():
                          "nk_a8: nk weights with W8A8 activations (opt-in, changes the result)")
     ap.add_argument("--no-pdl", action="store_true",
                     help="plain stream order instead of programmatic dependent launch (MOE_OPT_PDL 0)")
+    ap.add_argument("--fused-combine", action="store_true",
+                    help="routed down pass adds weighted rows into [T, D] fp32 sums "
+                         "(MOE_OPT_FUSED_COMBINE 1; the combine's summation order then varies)")
     ap.add_argument("--serial-shared", action="store_true",
                     help="shared expert on the caller's stream (MOE_OPT_SHARED_STREAM 0)")
     ap.add_argument("--tokens", type=int, default=None,

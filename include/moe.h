@@ -348,6 +348,18 @@ int moe_layer_launch_count(const moe_config_t* cfg);
  *   under a lock, so calls from several host threads stay correct (their
  *   shared experts then serialise on the one side stream). */
 #define MOE_OPT_SHARED_STREAM 5
+/*   MOE_OPT_FUSED_COMBINE: 1 = moe_layer fuses the combine into the routed
+ *   down projection (NEXT-1's second half: "千问 3.5 MoE 在 TPU 上的系统优化实战",
+ *   SparseCore paragraph -- un-permute and reduce without the intermediate
+ *   expert rows): the down pass multiplies each row by its routing weight and
+ *   adds it, with fp32 atomics, into [T, D] fp32 sums (the y_perm region of the
+ *   workspace, zeroed first), and the last kernel adds the shared row and
+ *   rounds once; no y_perm rows are written or read.  The k rows of a token
+ *   are then summed in whatever order they arrive, so the output may differ
+ *   from the default's fixed j-ascending order in the last bit (run to run as
+ *   well).  Layers with bf16 weights or K-contiguous e4m3 weights; others
+ *   (and 0, the default) keep finalize's fixed order. */
+#define MOE_OPT_FUSED_COMBINE 6
 int moe_set_option(int option, int value);
 
 /* Per-kernel timing hook (process-wide, off by default).  `events` holds

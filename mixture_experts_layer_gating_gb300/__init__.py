@@ -70,6 +70,7 @@ MOE_OPT_GATHER_A = 2
 MOE_OPT_DECODE_KERNEL = 3
 MOE_OPT_PDL = 4
 MOE_OPT_SHARED_STREAM = 5
+MOE_OPT_FUSED_COMBINE = 6
 
 
 def load_library(path: Optional[str] = None) -> ctypes.CDLL:

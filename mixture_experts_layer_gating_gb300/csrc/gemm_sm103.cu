@@ -154,7 +154,19 @@ struct KParams {
   // weights as the M = 256 operand (128 features per CTA), its rows as N
   int swap_tail;
   int32_t* err;
+  // kEpiCombineF32 (fused combine): expanded row of each output row, routing
+  // weights, k; out is the [T, N] fp32 accumulator
+  const int32_t* comb_rows;
+  const float* comb_w;
+  int comb_k;
 };
+
+// Fused combine: the token and routing weight of permuted output row `row`.
+__device__ __forceinline__ void comb_token(const KParams& p, size_t row, int& t, float& w) {
+  const int q = p.comb_rows[row];
+  t = q / p.comb_k;
+  w = p.comb_w[q];
+}
 
 // Element type of the store pass's output rows: bf16 for fp8-weight layers
 // (expanded on chip or read as e4m3), fp32 otherwise.
@@ -921,8 +933,15 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
                   if (c + j >= tw.rows) break;
                   const size_t row = static_cast<size_t>(tw.row0 + c + j);
                   const float rs = p.a_row_scale ? p.a_row_scale[row] : 1.0f;
-                  store_elem(reinterpret_cast<StoreT<FP8 || Q8>*>(p.out), plane + row * p.N + f,
-                             (__uint_as_float(hi[j]) + __uint_as_float(lo[j])) * rs * cs);
+                  const float v = (__uint_as_float(hi[j]) + __uint_as_float(lo[j])) * rs * cs;
+                  if (EPI == kEpiCombineF32) {
+                    int t;
+                    float w;
+                    comb_token(p, row, t, w);
+                    atomicAdd(reinterpret_cast<float*>(p.out) + static_cast<size_t>(t) * p.N + f, v * w);
+                  } else {
+                    store_elem(reinterpret_cast<StoreT<FP8 || Q8>*>(p.out), plane + row * p.N + f, v);
+                  }
                 }
               }
             }
@@ -1019,6 +1038,56 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
         // l / 8, l / 8 + 4, ...: one warp store writes 4 rows x 128 bytes
         const int sub = lane >> 3, c4 = (lane & 7) * 4;
         const bool vec = (p.N % 4) == 0;
+        if (EPI == kEpiCombineF32) {
+          // fused combine: the token and weight of the 8 rows this lane adds
+          int ct[8];
+          float cw[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            ct[i] = 0;
+            cw[i] = 0.0f;
+            if (sub + 4 * i < wrows) comb_token(p, static_cast<size_t>(wrow0 + sub + 4 * i), ct[i], cw[i]);
+          }
+          float* acc = reinterpret_cast<float*>(p.out);
+#pragma unroll 1
+          for (int c = 0; c < p.bn; c += 32) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(taddr + c, r);
+            tc_wait_ld();
+            const int col = ti.n0 + c;
+            if (col >= p.N) continue;  // warp-uniform
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              *reinterpret_cast<float4*>(stg + lane * EPI_STAGE_LD + 4 * j) =
+                  make_float4(__uint_as_float(r[4 * j]) * rs, __uint_as_float(r[4 * j + 1]) * rs,
+                              __uint_as_float(r[4 * j + 2]) * rs, __uint_as_float(r[4 * j + 3]) * rs);
+            __syncwarp();
+            const int cl = col + c4;
+            float cs[4] = {1.f, 1.f, 1.f, 1.f};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              if (sc && cl + i < p.N) cs[i] = sc[cl + i];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int rr = sub + 4 * i;
+              if (rr < wrows) {
+                const float4 v = *reinterpret_cast<const float4*>(stg + rr * EPI_STAGE_LD + c4);
+                float* arow = acc + static_cast<size_t>(ct[i]) * p.N;
+                const float w = cw[i];
+                if (vec && cl + 4 <= p.N) {
+                  atomicAdd(reinterpret_cast<float4*>(arow + cl),
+                            make_float4(v.x * cs[0] * w, v.y * cs[1] * w, v.z * cs[2] * w, v.w * cs[3] * w));
+                } else {
+                  if (cl < p.N) atomicAdd(arow + cl, v.x * cs[0] * w);
+                  if (cl + 1 < p.N) atomicAdd(arow + cl + 1, v.y * cs[1] * w);
+                  if (cl + 2 < p.N) atomicAdd(arow + cl + 2, v.z * cs[2] * w);
+                  if (cl + 3 < p.N) atomicAdd(arow + cl + 3, v.w * cs[3] * w);
+                }
+              }
+            }
+          }
+        } else {
 #pragma unroll 1
         for (int c = 0; c < p.bn; c += 32) {
           uint32_t r[32];
@@ -1061,6 +1130,7 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
             }
           }
         }
+        }  // not the fused combine
       }
       tc_fence_before_sync();
       if (PAIR) mbar_arrive_cluster(leader_bar(&ctrl->tempty[acc]));
@@ -1474,8 +1544,16 @@ __global__ void __launch_bounds__(DecCfg<SPLIT, FP8>::kThreads, 1)
             if (j >= rows) break;
             const size_t row = static_cast<size_t>(ti.row0 + j);
             const float rs = p.a_row_scale ? p.a_row_scale[row] : 1.0f;
-            store_elem(reinterpret_cast<StoreT<FP8 || Q8>*>(p.out), row * p.N + f,
-                       __uint_as_float(v[j]) * rs * cs);
+            if (EPI == kEpiCombineF32) {
+              int t;
+              float w;
+              comb_token(p, row, t, w);
+              atomicAdd(reinterpret_cast<float*>(p.out) + static_cast<size_t>(t) * p.N + f,
+                        __uint_as_float(v[j]) * rs * cs * w);
+            } else {
+              store_elem(reinterpret_cast<StoreT<FP8 || Q8>*>(p.out), row * p.N + f,
+                         __uint_as_float(v[j]) * rs * cs);
+            }
           }
         }
       }
@@ -1656,6 +1734,9 @@ cudaError_t launch_grouped_gemm_decode_q8(const GroupedGemmArgs& a, int nt, cuda
   kp.h_fp32 = a.h_fp32;
   kp.act = a.act;
   kp.err = a.err;
+  kp.comb_rows = a.comb_rows;
+  kp.comb_w = a.comb_w;
+  kp.comb_k = a.comb_k;
   kp.bn = nt;
   kp.ksplit = 1;
   kp.kbs = (a.K + 127) / 128;
@@ -1675,6 +1756,9 @@ cudaError_t launch_grouped_gemm_decode_q8(const GroupedGemmArgs& a, int nt, cuda
   kp.n_tiles = (a.N + kp.cols_per_tile - 1) / kp.cols_per_tile;
   const long long max_tiles =
       (static_cast<long long>((a.M + nt - 1) / nt) + a.G) * static_cast<long long>(kp.n_tiles);
+  if (a.epilogue == kEpiCombineF32)
+    return one ? launch_dec<kEpiCombineF32, false, false, true>(tr, tr_lo, tw, kp, max_tiles, s)
+               : launch_dec<kEpiCombineF32, true, false, true>(tr, tr_lo, tw, kp, max_tiles, s);
   if (one)
     return a.epilogue == kEpiGateUpAct
                ? launch_dec<kEpiGateUpAct, false, false, true>(tr, tr_lo, tw, kp, max_tiles, s)
@@ -1717,6 +1801,9 @@ cudaError_t launch_grouped_gemm_decode(const GroupedGemmArgs& a, int nt, cudaStr
   kp.h_fp32 = a.h_fp32;
   kp.act = a.act;
   kp.err = a.err;
+  kp.comb_rows = a.comb_rows;
+  kp.comb_w = a.comb_w;
+  kp.comb_k = a.comb_k;
   kp.bn = nt;
   kp.ksplit = 1;
   kp.kbs = (a.K + BK - 1) / BK;
@@ -1739,6 +1826,10 @@ cudaError_t launch_grouped_gemm_decode(const GroupedGemmArgs& a, int nt, cudaStr
   if (a.epilogue == kEpiGateUpAct)
     return a.b_fp8 ? launch_dec<kEpiGateUpAct, false, true>(tr, tr_lo, tw, kp, max_tiles, s)
                    : launch_dec<kEpiGateUpAct, false, false>(tr, tr_lo, tw, kp, max_tiles, s);
+  if (a.epilogue == kEpiCombineF32) {  // bf16 h pairs only
+    if (a.b_fp8 || !a.A_lo) return cudaErrorNotSupported;
+    return launch_dec<kEpiCombineF32, true, false>(tr, tr_lo, tw, kp, max_tiles, s);
+  }
   if (a.b_fp8) return launch_dec<kEpiStoreF32, false, true>(tr, tr_lo, tw, kp, max_tiles, s);
   return a.A_lo ? launch_dec<kEpiStoreF32, true, false>(tr, tr_lo, tw, kp, max_tiles, s)
                 : launch_dec<kEpiStoreF32, false, false>(tr, tr_lo, tw, kp, max_tiles, s);
@@ -1749,6 +1840,8 @@ cudaError_t launch_grouped_gemm_decode(const GroupedGemmArgs& a, int nt, cudaStr
 // accumulator, one-term rows (W8A8) one product.
 cudaError_t launch_grouped_gemm_q8(const GroupedGemmArgs& a, cudaStream_t s) {
   if (!a.b_fp8 || a.A_lo || a.ksplit > 1 || a.bias) return cudaErrorInvalidValue;
+  if (a.epilogue == kEpiCombineF32 && (!a.comb_rows || !a.comb_w || a.comb_k < 1))
+    return cudaErrorInvalidValue;
   if (a.a_gather && (a.a_rows < 1 || a.gather_k < 1)) return cudaErrorInvalidValue;
   if (a.G < 1 || a.G > MAX_G) return cudaErrorInvalidValue;
   const uint64_t K = static_cast<uint64_t>(a.K), N = static_cast<uint64_t>(a.N);
@@ -1769,6 +1862,9 @@ cudaError_t launch_grouped_gemm_q8(const GroupedGemmArgs& a, cudaStream_t s) {
   kp.h_fp32 = a.h_fp32;
   kp.act = a.act;
   kp.err = a.err;
+  kp.comb_rows = a.comb_rows;
+  kp.comb_w = a.comb_w;
+  kp.comb_k = a.comb_k;
   kp.ksplit = 1;
   kp.kbs = (a.K + 127) / 128;
   if (a.epilogue == kEpiGateUpAct) {
@@ -1838,8 +1934,12 @@ cudaError_t launch_grouped_gemm_q8(const GroupedGemmArgs& a, cudaStream_t s) {
       return pair ? MOE_LAUNCH_Q8(kEpiGateUpAct, false, true) : MOE_LAUNCH_Q8(kEpiGateUpAct, false, false);
     if (a.epilogue == kEpiStoreF32)
       return pair ? MOE_LAUNCH_Q8(kEpiStoreF32, false, true) : MOE_LAUNCH_Q8(kEpiStoreF32, false, false);
+    if (a.epilogue == kEpiCombineF32)
+      return pair ? MOE_LAUNCH_Q8(kEpiCombineF32, false, true) : MOE_LAUNCH_Q8(kEpiCombineF32, false, false);
     return cudaErrorInvalidValue;
   }
+  if (a.epilogue == kEpiCombineF32)
+    return pair ? MOE_LAUNCH_Q8(kEpiCombineF32, true, true) : MOE_LAUNCH_Q8(kEpiCombineF32, true, false);
   if (a.epilogue == kEpiGateUpAct)
     return pair ? MOE_LAUNCH_Q8(kEpiGateUpAct, true, true) : MOE_LAUNCH_Q8(kEpiGateUpAct, true, false);
   if (a.epilogue == kEpiStoreF32)
@@ -1874,6 +1974,8 @@ int device_sm_count() {
 
 cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
   if (a.M <= 0) return cudaSuccess;
+  if (a.epilogue == kEpiCombineF32 && (!a.comb_rows || !a.comb_w || a.comb_k < 1 || a.ksplit > 1))
+    return cudaErrorInvalidValue;
   // Swap-AB kernel (weights as the 128-row operand) where it measured faster
   // than 128-row tiles on GB300, with 16 rows per tile: a single group of at
   // most 64 rows (the shared expert at decode: more, smaller tiles), at most
@@ -1896,7 +1998,7 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
   else if (!a.b_fp8 && Gg <= 256 && Mg <= 4 * Gg) nt = 16;
   else if (a.b_fp8 && Mg <= 16 * Gg) nt = DEC_NT_MAX;
   if (g_decode_kernel && nt && a.decode_ok && !a.a_gather && a.ksplit <= 1 && a.G <= MAX_G &&
-      (a.epilogue == kEpiGateUpAct || a.epilogue == kEpiStoreF32)) {
+      (a.epilogue == kEpiGateUpAct || a.epilogue == kEpiStoreF32 || a.epilogue == kEpiCombineF32)) {
     if (!a.a_e4m3x2 && !a.a_e4m3 && (a.a_fp16 != 0) != (a.b_fp8 != 0)) return cudaErrorInvalidValue;
     if (a.b_fp8 && a.A_lo) return cudaErrorNotSupported;
     return launch_grouped_gemm_decode(a, nt, s);
@@ -1942,6 +2044,9 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
   kp.h_fp32 = a.h_fp32;
   kp.act = a.act;
   kp.err = a.err;
+  kp.comb_rows = a.comb_rows;
+  kp.comb_w = a.comb_w;
+  kp.comb_k = a.comb_k;
   {
     const int KB = (a.K + BK - 1) / BK;
     int ks = std::max(1, std::min(a.ksplit, KB));
@@ -2039,6 +2144,10 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
   if (a.epilogue == kEpiStoreF32) {
     if (a.b_fp8) return MOE_LAUNCH(kEpiStoreF32, false, true);
     return a.A_lo ? MOE_LAUNCH(kEpiStoreF32, true, false) : MOE_LAUNCH(kEpiStoreF32, false, false);
+  }
+  if (a.epilogue == kEpiCombineF32) {  // bf16 h pairs only
+    if (a.b_fp8 || !a.A_lo) return cudaErrorNotSupported;
+    return MOE_LAUNCH(kEpiCombineF32, true, false);
   }
 #undef MOE_LAUNCH
   return cudaErrorInvalidValue;

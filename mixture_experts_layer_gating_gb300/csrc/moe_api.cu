@@ -16,6 +16,7 @@ constexpr size_t kAlign = 256;
 
 int g_gather_a = 0;       // moe_set_option(MOE_OPT_GATHER_A, .)
 int g_shared_stream = 1;  // moe_set_option(MOE_OPT_SHARED_STREAM, .)
+int g_fused_combine = 0;  // moe_set_option(MOE_OPT_FUSED_COMBINE, .)
 
 // The shared expert depends on x alone, so moe_layer runs it on a second
 // stream of the library's own (one per device, created on first use) that
@@ -204,6 +205,14 @@ inline uint8_t* ws_at(void* ws, size_t off) { return static_cast<uint8_t*>(ws) +
 
 inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
+// moe_layer runs the fused combine: the option is on and the layer's down
+// pass has the kernel for it (bf16 weights, or e4m3 weights stored
+// K-contiguous; bf16 activations; D a multiple of 4)
+inline bool fused_combine_on(const moe_config_t* c) {
+  return g_fused_combine && c->act_dtype == MOE_BF16 && (c->w_dtype == MOE_BF16 || is_nk(c)) &&
+         c->D % 4 == 0;
+}
+
 int common_checks(const moe_config_t* cfg, void* ws, size_t ws_bytes) {
   if (!cfg_valid(cfg)) return MOE_ERR_INVALID_ARG;
   if (!combo_supported(cfg)) return MOE_ERR_UNSUPPORTED;
@@ -300,10 +309,13 @@ int do_permute(const moe_config_t* c, const int32_t* ids, const void* x, int32_t
 // and converted to the same row form (h16, h_inv) for the down pass.
 // When a_gather is given, the gate/up pass reads A row a_gather[r] / k of an
 // [a_rows, D] A for output row r (a_row_scale then indexed by that A row).
+// comb_rows / comb_w (fused combine, routed pass only): y is then the [T, D]
+// fp32 accumulator the down pass adds each row times its routing weight into.
 int do_ffn(const moe_config_t* c, const void* A, const float* a_row_scale, int M,
            const int32_t* offsets, int G, const void* W13, const float* s13, const void* W2,
            const float* s2, int I, void* h, void* y, void* h16, float* h_inv, int32_t* err,
-           cudaStream_t s, const int32_t* a_gather = nullptr, int a_rows = 0) {
+           cudaStream_t s, const int32_t* a_gather = nullptr, int a_rows = 0,
+           const int32_t* comb_rows = nullptr, const float* comb_w = nullptr) {
   if (M <= 0) return MOE_OK;
   cudaError_t e;
   trace_mark(s);
@@ -370,6 +382,12 @@ int do_ffn(const moe_config_t* c, const void* A, const float* a_row_scale, int M
   b.h_fp32 = 0;
   b.out = y;  // fp8-weight layers: the store pass writes bf16 rows
   b.out_lo = nullptr;
+  if (comb_rows) {
+    b.epilogue = kEpiCombineF32;
+    b.comb_rows = comb_rows;
+    b.comb_w = comb_w;
+    b.comb_k = c->k;
+  }
   trace_mark(s);
   e = launch_grouped_gemm(b, s);
   if (e != cudaSuccess) return e == cudaErrorNotSupported ? MOE_ERR_UNSUPPORTED : MOE_ERR_CUDA;
@@ -385,14 +403,15 @@ int do_grouped_ffn(const moe_config_t* c, const void* x_perm, const float* xp_sc
                    const float* s2, void* h, void* y_perm, const void* x, const float* x_scale,
                    const void* W13s, const float* s13s, const void* W2s, const float* s2s,
                    void* h_s, void* s_out, void* ws, int32_t* err, cudaStream_t s,
-                   const int32_t* gather = nullptr) {
+                   const int32_t* gather = nullptr, const int32_t* comb_rows = nullptr,
+                   const float* comb_w = nullptr) {
   const int R = c->T * c->k;
   const Layout L = make_layout(c);
   const bool fp8 = is_fp8(c);
   int st = do_ffn(c, x_perm, xp_scale, R, offsets, c->E, W13, s13, W2, s2, c->I, h, y_perm,
                   fp8 ? ws_at(ws, L.h16) : nullptr,
                   fp8 ? reinterpret_cast<float*>(ws_at(ws, L.h_inv)) : nullptr, err, s, gather,
-                  gather ? c->T : 0);
+                  gather ? c->T : 0, comb_rows, comb_w);
   if (st != MOE_OK) return st;
   if (x && c->I_shared > 0)
     st = do_ffn(c, x, x_scale, c->T, nullptr, 1, W13s, s13s, W2s, s2s, c->I_shared, h_s, s_out,
@@ -547,6 +566,12 @@ int moe_layer(const moe_config_t* cfg, const void* x, const void* Wg, const floa
   const bool traced = g_trace_events && g_trace_n >= moe_layer_launch_count(cfg) + 1;
   g_trace_next = traced ? 0 : -1;
   const bool fp8 = is_fp8(cfg);
+  // Fused combine (MOE_OPT_FUSED_COMBINE): the routed down pass adds each row
+  // times its routing weight into [T, D] fp32 sums (the y_perm region), zeroed
+  // here first, and the last kernel rounds sums + shared row; no y_perm rows.
+  const bool fused = fused_combine_on(cfg);
+  if (fused && cudaMemsetAsync(y_perm, 0, static_cast<size_t>(cfg->T) * cfg->D * 4, s) != cudaSuccess)
+    return (g_trace_next = -1, MOE_ERR_CUDA);
   const void* x_rows = x;  // what the gather and the shared expert read
   float* tok_inv = nullptr;
   float* row_inv = nullptr;
@@ -595,12 +620,17 @@ int moe_layer(const moe_config_t* cfg, const void* x, const void* Wg, const floa
   if (st != MOE_OK) return fail(st);
   st = do_grouped_ffn(cfg, gather ? x_rows : x_perm, gather ? tok_inv : row_inv, offsets, W13, s13,
                       W2, s2, h, y_perm, (shared && !side) ? x_rows : nullptr, tok_inv, W13s, s13s,
-                      W2s, s2s, h_s, s_out, ws, err, s, gather ? sorted_rows : nullptr);
+                      W2s, s2s, h_s, s_out, ws, err, s, gather ? sorted_rows : nullptr,
+                      fused ? sorted_rows : nullptr, fused ? w : nullptr);
   if (st != MOE_OK) return fail(st);
   if (side && !side_join(side, s)) return (g_trace_next = -1, MOE_ERR_CUDA);
   trace_mark(s);
-  st = cuda_status(launch_finalize(cfg->act_dtype, y_perm, dest, w, shared ? s_out : nullptr, out,
-                                   cfg->T, cfg->k, cfg->D, cfg->T * cfg->k, err, s, fp8));
+  if (fused)
+    st = cuda_status(launch_combine_round(static_cast<const float*>(y_perm), shared ? s_out : nullptr,
+                                          fp8, cfg->T, cfg->D, out, s));
+  else
+    st = cuda_status(launch_finalize(cfg->act_dtype, y_perm, dest, w, shared ? s_out : nullptr, out,
+                                     cfg->T, cfg->k, cfg->D, cfg->T * cfg->k, err, s, fp8));
   trace_mark(s);
   g_trace_next = -1;
   return st;
@@ -665,6 +695,11 @@ int moe_set_option(int option, int value) {
     case MOE_OPT_PDL: {
       const int old = g_pdl;
       g_pdl = value ? 1 : 0;
+      return old;
+    }
+    case MOE_OPT_FUSED_COMBINE: {
+      const int old = g_fused_combine;
+      g_fused_combine = value ? 1 : 0;
       return old;
     }
     default: return MOE_ERR_INVALID_ARG;

@@ -132,6 +132,10 @@ cudaError_t launch_rows_to_e4m3(const void* x, int rows, int D, void* q, float* 
 // W_nk[g][n][c] = W[g][c][n], one-byte elements (K, N multiples of 16).
 cudaError_t launch_transpose_bytes(const void* W, long long G, int K, int N, void* W_nk,
                                    cudaStream_t s);
+// Fused combine: out[t] = bf16(acc[t] + s[t]) for the [T, D] fp32 sums acc; s
+// fp32, bf16 (s_bf16) or null; D a multiple of 4.
+cudaError_t launch_combine_round(const float* acc, const void* s_rows, bool s_bf16, int T, int D,
+                                 void* out, cudaStream_t s);
 // y_perm and s_rows are fp32 (bf16 when y_bf16); out is act_dtype.
 cudaError_t launch_finalize(int act_dtype, const void* y_perm, const int32_t* dest, const float* w,
                             const void* s_rows, void* out, int T, int k, int D, int R,
@@ -152,6 +156,11 @@ cudaError_t launch_simt_down(const float* h, const int32_t* offsets, int G, int 
 enum GemmEpilogue : int {
   kEpiGateUpAct = 0,  // W13 pass: acc = [gate | up] -> act(gate) * up as a bf16 (hi, lo) pair
   kEpiStoreF32 = 2,   // down pass / router: acc (* scale) (+ bias) -> fp32
+  // down pass with the combine fused in: row r's result (times its scales)
+  // times its routing weight comb_w[q] (q = comb_rows[r], the expanded row
+  // t * comb_k + j) is added with fp32 atomics into out[t] ([T, N] fp32,
+  // zeroed beforehand); no per-row output
+  kEpiCombineF32 = 3,
 };
 
 struct GroupedGemmArgs {
@@ -187,6 +196,11 @@ struct GroupedGemmArgs {
   void* out_lo;                  // [M, N] bf16 h_lo (gate/up pass)
   int act;                       // moe_act_t (gate/up epilogue)
   int32_t* err;
+  // kEpiCombineF32: the expanded row of each output row (sorted_rows), the
+  // routing weights [T * comb_k], and k
+  const int32_t* comb_rows;
+  const float* comb_w;
+  int comb_k;
 };
 
 cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s);

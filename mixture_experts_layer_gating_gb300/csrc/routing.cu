@@ -944,6 +944,35 @@ __global__ void __launch_bounds__(256, kRegRowBlocksPerSm) rows_to_e4m3x2_reg_ke
   }
 }
 
+// The end of the fused combine: out[t] = round(acc[t] + s[t]) (s fp32, bf16
+// or absent), acc the [T, D] fp32 sums the down pass added its weighted rows
+// into.  16-byte vectors of 4 elements; one rounding to bf16.
+template <typename Ts>
+__global__ void combine_round_kernel(const float4* __restrict__ acc, const Ts* __restrict__ s,
+                                     long long n4, uint2* __restrict__ out) {
+  pdl_wait();
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += stride) {
+    float4 a = acc[i];
+    if (s) {
+      float f[4];
+      if constexpr (sizeof(Ts) == 4) {
+        const float4 v = reinterpret_cast<const float4*>(s)[i];
+        f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
+      } else {
+        const uint2 u = reinterpret_cast<const uint2*>(s)[i];
+        const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+        const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+        f[0] = lo.x; f[1] = lo.y; f[2] = hi.x; f[3] = hi.y;
+      }
+      a.x += f[0]; a.y += f[1]; a.z += f[2]; a.w += f[3];
+    }
+    __nv_bfloat162 o0 = __floats2bfloat162_rn(a.x, a.y), o1 = __floats2bfloat162_rn(a.z, a.w);
+    out[i] = make_uint2(*reinterpret_cast<uint32_t*>(&o0), *reinterpret_cast<uint32_t*>(&o1));
+  }
+  pdl_launch_dependents();
+}
+
 // W_nk[g][n][c] = W[g][c][n] for one-byte elements: 64 x 64 tiles through
 // shared memory, 16-byte loads and stores (K and N multiples of 16).
 __global__ void transpose_bytes_kernel(const uint8_t* __restrict__ W, int K, int N,
@@ -1263,6 +1292,24 @@ cudaError_t launch_rows_to_e4m3x2(const void* x, int rows, int D, void* q, float
 cudaError_t launch_rows_to_e4m3(const void* x, int rows, int D, void* q, float* scale,
                                 cudaStream_t s, bool src_f32) {
   return launch_rows_e4m3<true>(x, rows, D, q, scale, s, src_f32);
+}
+
+cudaError_t launch_combine_round(const float* acc, const void* s_rows, bool s_bf16, int T, int D,
+                                 void* out, cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
+  if (D % 4) return cudaErrorInvalidValue;
+  const long long n4 = static_cast<long long>(T) * D / 4;
+  const int threads = 256;
+  const int blocks = static_cast<int>(std::min<long long>((n4 + threads - 1) / threads,
+                                                          static_cast<long long>(device_sm_count()) * 8));
+  if (s_bf16)
+    MOE_LAUNCH(combine_round_kernel<__nv_bfloat16>, blocks, threads, 0, s,
+               reinterpret_cast<const float4*>(acc), static_cast<const __nv_bfloat16*>(s_rows), n4,
+               static_cast<uint2*>(out));
+  else
+    MOE_LAUNCH(combine_round_kernel<float>, blocks, threads, 0, s, reinterpret_cast<const float4*>(acc),
+               static_cast<const float*>(s_rows), n4, static_cast<uint2*>(out));
+  return cudaGetLastError();
 }
 
 cudaError_t launch_transpose_bytes(const void* W, long long G, int K, int N, void* W_nk,
