@@ -329,6 +329,8 @@ def set_options(moe, args):
         moe.moe_set_option(moe.MOE_OPT_SHARED_STREAM, 0)
     if args.fused_combine:
         moe.moe_set_option(moe.MOE_OPT_FUSED_COMBINE, 1)
+    if args.lpt:
+        moe.moe_set_option(moe.MOE_OPT_TILE_ORDER, 1)
 
 
 def pct(v, q):
@@ -680,6 +682,8 @@ def main():
     ap.add_argument("--fused-combine", action="store_true",
                     help="routed down pass adds weighted rows into [T, D] fp32 sums "
                          "(MOE_OPT_FUSED_COMBINE 1; the combine's summation order then varies)")
+    ap.add_argument("--lpt", action="store_true",
+                    help="grouped GEMMs run the experts heaviest first (MOE_OPT_TILE_ORDER 1)")
     ap.add_argument("--serial-shared", action="store_true",
                     help="shared expert on the caller's stream (MOE_OPT_SHARED_STREAM 0)")
     ap.add_argument("--tokens", type=int, default=None,

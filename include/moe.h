@@ -360,6 +360,14 @@ int moe_layer_launch_count(const moe_config_t* cfg);
  *   well).  Layers with bf16 weights or K-contiguous e4m3 weights; others
  *   (and 0, the default) keep finalize's fixed order. */
 #define MOE_OPT_FUSED_COMBINE 6
+/*   MOE_OPT_TILE_ORDER: 1 = the grouped GEMMs schedule the experts heaviest
+ *   first (most rows; the lower index first among equal counts), the
+ *   longest-processing-time order of "企业官网建设流程全解析" §4 (sort the
+ *   experts' work heaviest first so that the largest ones do not trail);
+ *   every CTA sorts the expert counts itself (a bitonic sort in one warp)
+ *   while it builds its tile schedule; 0 (default) = expert order.  Same
+ *   results. */
+#define MOE_OPT_TILE_ORDER 7
 int moe_set_option(int option, int value);
 
 /* Per-kernel timing hook (process-wide, off by default).  `events` holds

@@ -112,6 +112,9 @@ struct Ctrl {
   uint64_t xch_full, xch_empty;  // decode gate/up epilogue: up values staged / consumed
   uint32_t tmem_slot;
   int abort;
+  // the schedule's groups in the order their tiles run: position i holds
+  // group grp_id[i] (i itself in expert order; heaviest first under LPT)
+  int grp_id[MAX_G];
   int grp_start[MAX_G];
   int grp_cnt[MAX_G];
   int tile_start[MAX_G + 1];
@@ -159,6 +162,7 @@ struct KParams {
   const int32_t* comb_rows;
   const float* comb_w;
   int comb_k;
+  int lpt;  // 1: groups scheduled heaviest first (most rows; lower index on ties)
 };
 
 // Fused combine: the token and routing weight of permuted output row `row`.
@@ -191,7 +195,7 @@ __device__ __forceinline__ TileInfo decode_tile(const Ctrl* c, int G, int t, int
     if (c->tile_start[mid] <= q) lo = mid; else hi = mid - 1;
   }
   TileInfo ti;
-  ti.g = lo;
+  ti.g = c->grp_id[lo];
   const int mt_g = c->tile_start[lo + 1] - c->tile_start[lo];
   const int local = t - c->tile_start[lo] * n_tiles;
   const int nt = local / mt_g;
@@ -202,12 +206,119 @@ __device__ __forceinline__ TileInfo decode_tile(const Ctrl* c, int G, int t, int
   return ti;
 }
 
+// Rows [a, b) of group g, validated (a bad group gets none and sets `bad`).
+__device__ __forceinline__ void group_rows(const int32_t* offsets, int g, int M, int& a, int& b,
+                                           bool& bad) {
+  a = 0;
+  b = M;
+  if (offsets) {
+    a = offsets[g];
+    b = offsets[g + 1];
+  }
+  if (a < 0 || b < a || b > M) {
+    bad = true;
+    a = 0;
+    b = 0;
+  }
+}
+
+// Heaviest-first (LPT) schedule: the groups sorted by row count, descending,
+// the lower index first among equal counts, by a bitonic sort of 512 32-bit
+// keys (min(count, 2^23 - 1) << 9 | 511 - g; counts beyond 2^23 rows keep
+// index order among themselves) held 16 per lane in one warp: position
+// i = lane * 16 + r.  Then grp_id / grp_start / grp_cnt / tile_start by
+// position.  G <= 512 (a key of 0 is padding: real keys are >= 512 - G).
+template <int J>  // one bitonic stage whose partner is r ^ J in this lane
+__device__ __forceinline__ void lpt_stage_in_lane(uint32_t (&key)[16], int lane, int k) {
+#pragma unroll
+  for (int r = 0; r < 16; ++r) {
+    if ((r ^ J) > r) {
+      const int i = lane * 16 + r;
+      const uint32_t a = key[r], b = key[r ^ J];
+      const bool swap = ((i & k) == 0) ? (a < b) : (a > b);  // descending blocks first
+      key[r] = swap ? b : a;
+      key[r ^ J] = swap ? a : b;
+    }
+  }
+}
+
+__device__ __noinline__ void build_schedule_lpt(Ctrl* ctrl, const int32_t* offsets, int G, int M,
+                                                int tile_h, int32_t* err, int lane) {
+  uint32_t key[16];
+  bool bad = false;
+#pragma unroll
+  for (int r = 0; r < 16; ++r) {
+    const int g = lane * 16 + r;
+    key[r] = 0;  // padding sorts last
+    if (g < G) {
+      int a, b;
+      group_rows(offsets, g, M, a, b, bad);
+      key[r] = (static_cast<uint32_t>(min(b - a, (1 << 23) - 1)) << 9) | static_cast<uint32_t>(511 - g);
+    }
+  }
+#pragma unroll 1
+  for (int k = 2; k <= 512; k <<= 1) {
+#pragma unroll 1
+    for (int j = k >> 1; j >= 16; j >>= 1) {  // partner in lane ^ (j / 16), same register
+#pragma unroll
+      for (int r = 0; r < 16; ++r) {
+        const uint32_t other = __shfl_xor_sync(0xffffffffu, key[r], j >> 4);
+        const int i = lane * 16 + r;
+        const bool keep_max = (((i & j) == 0) == ((i & k) == 0));
+        key[r] = keep_max ? max(key[r], other) : min(key[r], other);
+      }
+    }
+    if (k >= 16) lpt_stage_in_lane<8>(key, lane, k);
+    if (k >= 8) lpt_stage_in_lane<4>(key, lane, k);
+    if (k >= 4) lpt_stage_in_lane<2>(key, lane, k);
+    lpt_stage_in_lane<1>(key, lane, k);
+  }
+  int local = 0;
+#pragma unroll
+  for (int r = 0; r < 16; ++r) {
+    const int i = lane * 16 + r;
+    if (i < G) {
+      const int g = 511 - static_cast<int>(key[r] & 511u);
+      int a, b;
+      bool bad2 = false;
+      group_rows(offsets, g, M, a, b, bad2);
+      ctrl->grp_id[i] = g;
+      ctrl->grp_start[i] = a;
+      ctrl->grp_cnt[i] = b - a;
+      local += (b - a + tile_h - 1) / tile_h;
+    }
+  }
+  int incl = local;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += v;
+  }
+  int run = incl - local;
+#pragma unroll
+  for (int r = 0; r < 16; ++r) {
+    const int i = lane * 16 + r;
+    if (i < G) {
+      ctrl->tile_start[i] = run;
+      run += (ctrl->grp_cnt[i] + tile_h - 1) / tile_h;
+    }
+  }
+  const int total = __shfl_sync(0xffffffffu, incl, 31);
+  if (lane == 0) ctrl->tile_start[G] = total;
+  if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(err, MOE_DEV_BAD_OFFSETS);
+}
+
 // One warp builds the row-tile schedule of the groups in shared memory:
 // grp_start / grp_cnt per group (offsets validated: a bad group gets no rows and
-// MOE_DEV_BAD_OFFSETS is flagged) and tile_start[g] = sum_{g' < g} ceil(cnt_g' / tile_h).
+// MOE_DEV_BAD_OFFSETS is flagged) and tile_start[g] = sum_{g' < g} ceil(cnt_g' / tile_h),
+// in expert order (grp_id[g] = g), or heaviest first when lpt is set.
 // offsets == nullptr: one group of M rows.
 __device__ void build_schedule(Ctrl* ctrl, const int32_t* offsets, int G, int M, int tile_h,
-                               int32_t* err, int lane) {
+                               int32_t* err, int lane, int lpt = 0) {
+  if (lpt && G > 1) {
+    build_schedule_lpt(ctrl, offsets, G, M, tile_h, err, lane);
+    return;
+  }
   const int per = (G + 31) / 32;
   const int g0 = min(G, lane * per), g1 = min(G, g0 + per);
   int local = 0;
@@ -223,6 +334,7 @@ __device__ void build_schedule(Ctrl* ctrl, const int32_t* offsets, int G, int M,
       a = 0;
       b = 0;
     }
+    ctrl->grp_id[g] = g;
     ctrl->grp_start[g] = a;
     ctrl->grp_cnt[g] = b - a;
     local += (b - a + tile_h - 1) / tile_h;
@@ -254,7 +366,7 @@ __device__ __forceinline__ TileInfo decode_tile_h(const Ctrl* c, int G, int t, i
     if (c->tile_start[mid] <= q) lo = mid; else hi = mid - 1;
   }
   TileInfo ti;
-  ti.g = lo;
+  ti.g = c->grp_id[lo];
   const int mt_g = c->tile_start[lo + 1] - c->tile_start[lo];
   const int local = t - c->tile_start[lo] * n_tiles;
   const int nt = local / mt_g;
@@ -367,7 +479,7 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
       tmem_relinquish();
     }
   }
-  if (warp == 2) build_schedule(ctrl, p.group_offsets, G, p.M, TILE_M, p.err, lane);
+  if (warp == 2) build_schedule(ctrl, p.group_offsets, G, p.M, TILE_M, p.err, lane, p.lpt);
   tc_fence_before_sync();
   __syncthreads();
   if (PAIR) cluster_sync();  // the peer's barriers exist before anyone signals them
@@ -1262,7 +1374,7 @@ __global__ void __launch_bounds__(DecCfg<SPLIT, FP8>::kThreads, 1)
     tmem_alloc(&ctrl->tmem_slot, DEC_TMEM_COLS);
     tmem_relinquish();
   }
-  if (warp == 2) build_schedule(ctrl, p.group_offsets, G, p.M, NT, p.err, lane);
+  if (warp == 2) build_schedule(ctrl, p.group_offsets, G, p.M, NT, p.err, lane, p.lpt);
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
@@ -1681,6 +1793,7 @@ cudaError_t launch_epi(const CUtensorMap& ta, const CUtensorMap& ta_lo, const CU
 int g_pair_tiles = 3;      // set through moe_set_option(MOE_OPT_PAIR_TILES, .)
 int g_decode_kernel = 1;   // set through moe_set_option(MOE_OPT_DECODE_KERNEL, .)
 int g_pdl = 1;             // set through moe_set_option(MOE_OPT_PDL, .)
+int g_tile_order = 0;      // set through moe_set_option(MOE_OPT_TILE_ORDER, .)
 
 namespace {
 
@@ -1737,6 +1850,7 @@ cudaError_t launch_grouped_gemm_decode_q8(const GroupedGemmArgs& a, int nt, cuda
   kp.comb_rows = a.comb_rows;
   kp.comb_w = a.comb_w;
   kp.comb_k = a.comb_k;
+  kp.lpt = g_tile_order == 1 && a.group_offsets != nullptr && a.G > 1;
   kp.bn = nt;
   kp.ksplit = 1;
   kp.kbs = (a.K + 127) / 128;
@@ -1804,6 +1918,7 @@ cudaError_t launch_grouped_gemm_decode(const GroupedGemmArgs& a, int nt, cudaStr
   kp.comb_rows = a.comb_rows;
   kp.comb_w = a.comb_w;
   kp.comb_k = a.comb_k;
+  kp.lpt = g_tile_order == 1 && a.group_offsets != nullptr && a.G > 1;
   kp.bn = nt;
   kp.ksplit = 1;
   kp.kbs = (a.K + BK - 1) / BK;
@@ -1865,6 +1980,7 @@ cudaError_t launch_grouped_gemm_q8(const GroupedGemmArgs& a, cudaStream_t s) {
   kp.comb_rows = a.comb_rows;
   kp.comb_w = a.comb_w;
   kp.comb_k = a.comb_k;
+  kp.lpt = g_tile_order == 1 && a.group_offsets != nullptr && a.G > 1;
   kp.ksplit = 1;
   kp.kbs = (a.K + 127) / 128;
   if (a.epilogue == kEpiGateUpAct) {
@@ -2047,6 +2163,7 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
   kp.comb_rows = a.comb_rows;
   kp.comb_w = a.comb_w;
   kp.comb_k = a.comb_k;
+  kp.lpt = g_tile_order == 1 && a.group_offsets != nullptr && a.G > 1;
   {
     const int KB = (a.K + BK - 1) / BK;
     int ks = std::max(1, std::min(a.ksplit, KB));

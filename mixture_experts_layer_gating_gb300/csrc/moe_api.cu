@@ -697,6 +697,11 @@ int moe_set_option(int option, int value) {
       g_pdl = value ? 1 : 0;
       return old;
     }
+    case MOE_OPT_TILE_ORDER: {
+      const int old = g_tile_order;
+      g_tile_order = value ? 1 : 0;
+      return old;
+    }
     case MOE_OPT_FUSED_COMBINE: {
       const int old = g_fused_combine;
       g_fused_combine = value ? 1 : 0;

@@ -208,6 +208,7 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s);
 // Kernel-variant options (moe_set_option).
 extern int g_pair_tiles;
 extern int g_decode_kernel;
+extern int g_tile_order;
 
 // Shared helper: SM count of the current device (cached).
 int device_sm_count();

@@ -135,6 +135,8 @@ def test_set_option_values():
         (moe.MOE_OPT_SHARED_STREAM, 2, 1),
         (moe.MOE_OPT_FUSED_COMBINE, 5, 1),
         (moe.MOE_OPT_FUSED_COMBINE, 0, 0),
+        (moe.MOE_OPT_TILE_ORDER, 3, 1),
+        (moe.MOE_OPT_TILE_ORDER, 0, 0),
     ]
     for opt, value, stored in cases:
         old = moe.moe_set_option(opt, value)
