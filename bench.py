@@ -331,6 +331,8 @@ def set_options(moe, args):
         moe.moe_set_option(moe.MOE_OPT_FUSED_COMBINE, 1)
     if args.lpt:
         moe.moe_set_option(moe.MOE_OPT_TILE_ORDER, 1)
+    if args.shared_in_gemm:
+        moe.moe_set_option(moe.MOE_OPT_SHARED_IN_GEMM, 1)
 
 
 def pct(v, q):
@@ -344,7 +346,7 @@ def pct(v, q):
     return v[lo] + (v[hi] - v[lo]) * (pos - lo)
 
 
-def kernel_names(shape, nk, gather_a, a8=False, fused=False):
+def kernel_names(shape, nk, gather_a, a8=False, fused=False, shared_in_gemm=False):
     """Names of the kernels one moe_layer call launches, in launch order."""
     fp8 = shape.w_dtype == "fp8_e4m3"
     rows = "e4m3" if a8 else "e4m3x2" if nk else "fp16"  # the A-row form of fp8 layers
@@ -357,7 +359,7 @@ def kernel_names(shape, nk, gather_a, a8=False, fused=False):
     names += ["w13_gate_up"]
     names += [f"h_to_{rows}"] if fp8 else []
     names += ["w2_down"]
-    if shape.I_shared:
+    if shape.I_shared and not shared_in_gemm:
         names += ["shared_w13"] + ([f"shared_h_to_{rows}"] if fp8 else []) + ["shared_w2"]
     names += ["combine_round" if fused else "finalize"]
     return names
@@ -434,7 +436,9 @@ def measure(args, world, rank, local, shape, primary: bool, layout: str):
     # ---- per-kernel durations (instrumented pass, same work, after the timed region)
     L = moe.moe_layer_launch_count(cfg)
     fused = args.fused_combine and shape.act_dtype == "bf16" and (nk or not fp8)
-    names = kernel_names(shape, nk, args.gather_a, a8, fused)
+    in_gemm = (args.shared_in_gemm and shape.I_shared == shape.I and shape.I_shared > 0 and
+               shape.act_dtype == "bf16" and (nk or not fp8) and not args.gather_a)
+    names = kernel_names(shape, nk, args.gather_a, a8, fused, in_gemm)
     assert len(names) == L
     per = [[] for _ in range(L)]
     for _ in range(args.steps):
@@ -682,6 +686,9 @@ def main():
     ap.add_argument("--fused-combine", action="store_true",
                     help="routed down pass adds weighted rows into [T, D] fp32 sums "
                          "(MOE_OPT_FUSED_COMBINE 1; the combine's summation order then varies)")
+    ap.add_argument("--shared-in-gemm", action="store_true",
+                    help="shared expert as the last group of the routed GEMMs (MOE_OPT_SHARED_IN_GEMM 1; "
+                         "layers whose I_shared equals I)")
     ap.add_argument("--lpt", action="store_true",
                     help="grouped GEMMs run the experts heaviest first (MOE_OPT_TILE_ORDER 1)")
     ap.add_argument("--serial-shared", action="store_true",

@@ -368,6 +368,17 @@ int moe_layer_launch_count(const moe_config_t* cfg);
  *   while it builds its tile schedule; 0 (default) = expert order.  Same
  *   results. */
 #define MOE_OPT_TILE_ORDER 7
+/*   MOE_OPT_SHARED_IN_GEMM: 1 = moe_layer runs the shared expert as one more
+ *   group of the routed grouped GEMMs (NEXT-3: "用SGLang-JAX在TPU上优化
+ *   Ling-2.6-1T" §5 "核内共享专家", the shared expert moved into the routed
+ *   kernel): its token rows are appended to the permuted rows (rows R .. R+T-1
+ *   of x_perm, h and y_perm), its tiles follow the routed tiles in the same
+ *   persistent launches, and the layer makes no launches of its own for it.
+ *   Layers whose I_shared equals I with bf16 or K-contiguous e4m3 weights
+ *   (the workspace of such a layer always holds those T extra rows); other
+ *   layers, and 0 (default), run the shared expert in its own launches (on
+ *   the side stream, MOE_OPT_SHARED_STREAM).  Same results. */
+#define MOE_OPT_SHARED_IN_GEMM 9
 int moe_set_option(int option, int value);
 
 /* Per-kernel timing hook (process-wide, off by default).  `events` holds

@@ -72,7 +72,9 @@ constexpr int STAGE_BUDGET = 192 * 1024;
 constexpr int EPI_STAGE_LD = 36;  // padded row (144 bytes: 16-byte aligned rows)
 constexpr int EPI_STAGE_FLOATS = 32 * EPI_STAGE_LD;
 constexpr int EPI_STAGE_BYTES = 4 * EPI_STAGE_FLOATS * 4;
-constexpr int MAX_G = 512;
+// groups of one launch: 512 experts, plus the shared expert as one more
+// group when it runs inside the routed GEMMs
+constexpr int MAX_G = 513;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_STRIDE = 256;  // TMEM columns per accumulator buffer
 
@@ -163,10 +165,20 @@ struct KParams {
   const float* comb_w;
   int comb_k;
   int lpt;  // 1: groups scheduled heaviest first (most rows; lower index on ties)
+  // > 0: the last group (G - 1) is the shared expert: its rows are the last
+  // sh_rows rows of A [M - sh_rows, M) and its weights the second weight map
+  // (tmap_b2) with per-column scales sh_b_scale
+  int sh_rows;
+  const float* sh_b_scale;
 };
 
 // Fused combine: the token and routing weight of permuted output row `row`.
 __device__ __forceinline__ void comb_token(const KParams& p, size_t row, int& t, float& w) {
+  if (p.sh_rows > 0 && row >= static_cast<size_t>(p.M - p.sh_rows)) {  // shared expert: weight 1
+    t = static_cast<int>(row - static_cast<size_t>(p.M - p.sh_rows));
+    w = 1.0f;
+    return;
+  }
   const int q = p.comb_rows[row];
   t = q / p.comb_k;
   w = p.comb_w[q];
@@ -206,9 +218,16 @@ __device__ __forceinline__ TileInfo decode_tile(const Ctrl* c, int G, int t, int
   return ti;
 }
 
-// Rows [a, b) of group g, validated (a bad group gets none and sets `bad`).
+// Rows [a, b) of group g, validated (a bad group gets none and sets `bad`);
+// with sh_rows > 0 the last group g = G - 1 is the shared expert's rows
+// [M - sh_rows, M).
 __device__ __forceinline__ void group_rows(const int32_t* offsets, int g, int M, int& a, int& b,
-                                           bool& bad) {
+                                           bool& bad, int G = 0, int sh_rows = 0) {
+  if (sh_rows > 0 && g == G - 1) {
+    a = M - sh_rows;
+    b = M;
+    return;
+  }
   a = 0;
   b = M;
   if (offsets) {
@@ -243,7 +262,7 @@ __device__ __forceinline__ void lpt_stage_in_lane(uint32_t (&key)[16], int lane,
 }
 
 __device__ __noinline__ void build_schedule_lpt(Ctrl* ctrl, const int32_t* offsets, int G, int M,
-                                                int tile_h, int32_t* err, int lane) {
+                                                int tile_h, int32_t* err, int lane, int sh_rows) {
   uint32_t key[16];
   bool bad = false;
 #pragma unroll
@@ -252,7 +271,7 @@ __device__ __noinline__ void build_schedule_lpt(Ctrl* ctrl, const int32_t* offse
     key[r] = 0;  // padding sorts last
     if (g < G) {
       int a, b;
-      group_rows(offsets, g, M, a, b, bad);
+      group_rows(offsets, g, M, a, b, bad, G, sh_rows);
       key[r] = (static_cast<uint32_t>(min(b - a, (1 << 23) - 1)) << 9) | static_cast<uint32_t>(511 - g);
     }
   }
@@ -281,7 +300,7 @@ __device__ __noinline__ void build_schedule_lpt(Ctrl* ctrl, const int32_t* offse
       const int g = 511 - static_cast<int>(key[r] & 511u);
       int a, b;
       bool bad2 = false;
-      group_rows(offsets, g, M, a, b, bad2);
+      group_rows(offsets, g, M, a, b, bad2, G, sh_rows);
       ctrl->grp_id[i] = g;
       ctrl->grp_start[i] = a;
       ctrl->grp_cnt[i] = b - a;
@@ -314,9 +333,9 @@ __device__ __noinline__ void build_schedule_lpt(Ctrl* ctrl, const int32_t* offse
 // in expert order (grp_id[g] = g), or heaviest first when lpt is set.
 // offsets == nullptr: one group of M rows.
 __device__ void build_schedule(Ctrl* ctrl, const int32_t* offsets, int G, int M, int tile_h,
-                               int32_t* err, int lane, int lpt = 0) {
-  if (lpt && G > 1) {
-    build_schedule_lpt(ctrl, offsets, G, M, tile_h, err, lane);
+                               int32_t* err, int lane, int lpt = 0, int sh_rows = 0) {
+  if (lpt && G > 1 && G <= 512) {
+    build_schedule_lpt(ctrl, offsets, G, M, tile_h, err, lane, sh_rows);
     return;
   }
   const int per = (G + 31) / 32;
@@ -324,16 +343,8 @@ __device__ void build_schedule(Ctrl* ctrl, const int32_t* offsets, int G, int M,
   int local = 0;
   bool bad = false;
   for (int g = g0; g < g1; ++g) {
-    int a = 0, b = M;
-    if (offsets) {
-      a = offsets[g];
-      b = offsets[g + 1];
-    }
-    if (a < 0 || b < a || b > M) {
-      bad = true;
-      a = 0;
-      b = 0;
-    }
+    int a, b;
+    group_rows(offsets, g, M, a, b, bad, G, sh_rows);
     ctrl->grp_id[g] = g;
     ctrl->grp_start[g] = a;
     ctrl->grp_cnt[g] = b - a;
@@ -411,7 +422,9 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
                         const __grid_constant__ CUtensorMap tmap_b,
                         const __grid_constant__ CUtensorMap tmap_b_tail,
                         const __grid_constant__ CUtensorMap tmap_a_tail,
-                        const __grid_constant__ CUtensorMap tmap_a_lo_tail, const KParams p) {
+                        const __grid_constant__ CUtensorMap tmap_a_lo_tail,
+                        const __grid_constant__ CUtensorMap tmap_b2,
+                        const __grid_constant__ CUtensorMap tmap_b2_tail, const KParams p) {
   pdl_wait();
   static_assert(!Q8 || !FP8, "e4m3 rows meet K-contiguous e4m3 weights, not expanded ones");
   using Cfg = StageCfg<SPLIT, FP8, PAIR>;
@@ -469,6 +482,10 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
     if (PAIR && EPI == kEpiGateUpAct) tma_prefetch_desc(&tmap_b_tail);
     if (PAIR) tma_prefetch_desc(&tmap_a_tail);
     if (PAIR && SPLIT) tma_prefetch_desc(&tmap_a_lo_tail);
+    if (p.sh_rows > 0) {
+      tma_prefetch_desc(&tmap_b2);
+      if (PAIR) tma_prefetch_desc(&tmap_b2_tail);
+    }
   }
   if (warp == 1) {
     if (PAIR) {  // collective over one warp of each CTA of the pair
@@ -479,7 +496,7 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
       tmem_relinquish();
     }
   }
-  if (warp == 2) build_schedule(ctrl, p.group_offsets, G, p.M, TILE_M, p.err, lane, p.lpt);
+  if (warp == 2) build_schedule(ctrl, p.group_offsets, G, p.M, TILE_M, p.err, lane, p.lpt, p.sh_rows);
   tc_fence_before_sync();
   __syncthreads();
   if (PAIR) cluster_sync();  // the peer's barriers exist before anyone signals them
@@ -511,6 +528,13 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
   };
   // rows each CTA of the pair loads for a swapped tail, from row swap_row0 on
   constexpr bool kSplitRowsAcrossPair = !SPLIT;
+  // the shared expert's group (sh_rows > 0): its own weight maps and scales
+  auto is_shared_group = [&](int g) { return p.sh_rows > 0 && g == G - 1; };
+  // per-column scales of group g (per = 2 for [gate | up], 1 otherwise)
+  auto bscale_base = [&](int g, int per) -> const float* {
+    if (is_shared_group(g)) return p.sh_b_scale;
+    return p.b_scale ? p.b_scale + static_cast<size_t>(g) * per * p.N : nullptr;
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -533,6 +557,12 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
       for (int t = work0; t < total_tiles && ok; t += work_stride) {
         const TileInfo ti = decode_tile<TILE_M>(ctrl, G, t / p.ksplit, p.n_tiles, p.cols_per_tile);
         const int my_row0 = ti.row0 + static_cast<int>(rank) * BM;
+        // the group's weights: the routed tensor at coordinate g, or the shared
+        // expert's own tensor (one matrix, coordinate 0)
+        const bool shg = is_shared_group(ti.g);
+        const CUtensorMap* bmap = shg ? &tmap_b2 : &tmap_b;
+        const CUtensorMap* bmap_tail = shg ? &tmap_b2_tail : &tmap_b_tail;
+        const int gb = shg ? 0 : ti.g;
         // gather mode: the source rows of this lane's 4 tile rows (rows past the
         // group repeat the tile's first row; their results are never stored)
         int tr[4] = {0, 0, 0, 0};
@@ -574,30 +604,30 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
                 // K-contiguous e4m3 weights: CTA r its 64 gate rows n0 + 64 r .. and
                 // the matching 64 up rows, or its 128 output rows n0 + 128 r ..
                 if (EPI == kEpiGateUpAct)
-                  tma_load_4d_pair(b_dst, &tmap_b_tail, fbar, kb * KE, ti.n0 + 64 * static_cast<int>(rank), 0,
-                                   ti.g, pol_b);
+                  tma_load_4d_pair(b_dst, bmap_tail, fbar, kb * KE, ti.n0 + 64 * static_cast<int>(rank), 0,
+                                   gb, pol_b);
                 else
-                  tma_load_3d_pair(b_dst, &tmap_b, fbar, kb * KE, ti.n0 + static_cast<int>(rank) * (p.bn / 2),
-                                   ti.g, pol_b);
+                  tma_load_3d_pair(b_dst, bmap, fbar, kb * KE, ti.n0 + static_cast<int>(rank) * (p.bn / 2),
+                                   gb, pol_b);
               } else if (EPI == kEpiGateUpAct) {
                 // gate and up features n0 + 64 r .. + 63: one box each
                 if (p.b_wide) {
-                  tma_load_5d_pair(b_dst, &tmap_b_tail, fbar, 0, kb * BK, ti.n0 / 64 + static_cast<int>(rank),
-                                   0, ti.g, pol_b);
+                  tma_load_5d_pair(b_dst, bmap_tail, fbar, 0, kb * BK, ti.n0 / 64 + static_cast<int>(rank),
+                                   0, gb, pol_b);
                 } else {
-                  tma_load_4d_pair(b_dst, &tmap_b_tail, fbar, ti.n0 + 64 * static_cast<int>(rank), 0,
-                                   kb * BK, ti.g, pol_b);
-                  tma_load_4d_pair(b_dst + B_BOX_BYTES, &tmap_b_tail, fbar,
-                                   ti.n0 + 64 * static_cast<int>(rank), 1, kb * BK, ti.g, pol_b);
+                  tma_load_4d_pair(b_dst, bmap_tail, fbar, ti.n0 + 64 * static_cast<int>(rank), 0,
+                                   kb * BK, gb, pol_b);
+                  tma_load_4d_pair(b_dst + B_BOX_BYTES, bmap_tail, fbar,
+                                   ti.n0 + 64 * static_cast<int>(rank), 1, kb * BK, gb, pol_b);
                 }
               } else if (p.b_wide) {
-                tma_load_4d_pair(b_dst, &tmap_b, fbar, 0, kb * BK,
-                                 ti.n0 / 64 + static_cast<int>(rank) * nbox_cta, ti.g, pol_b);
+                tma_load_4d_pair(b_dst, bmap, fbar, 0, kb * BK,
+                                 ti.n0 / 64 + static_cast<int>(rank) * nbox_cta, gb, pol_b);
               } else {
                 const int c0 = ti.n0 + static_cast<int>(rank) * 64 * nbox_cta;
                 for (int j = 0; j < nbox_cta; ++j)
-                  tma_load_3d_pair(b_dst + j * B_BOX_BYTES, &tmap_b, fbar, c0 + 64 * j, kb * BK,
-                                   ti.g, pol_b);
+                  tma_load_3d_pair(b_dst + j * B_BOX_BYTES, bmap, fbar, c0 + 64 * j, kb * BK,
+                                   gb, pol_b);
               }
             }
             fill_mask |= 1u << stage;
@@ -635,16 +665,16 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
             // n0 + r * bn / 2 ..)
             if (EPI == kEpiGateUpAct) {
               if (PAIR)
-                tma_load_4d_pair(b_dst, &tmap_b, fbar, kb * KE, ti.n0, static_cast<int>(rank), ti.g,
+                tma_load_4d_pair(b_dst, bmap, fbar, kb * KE, ti.n0, static_cast<int>(rank), gb,
                                  pol_b);
               else
-                tma_load_4d(b_dst, &tmap_b, &ctrl->full[stage], kb * KE, ti.n0, 0, ti.g, pol_b);
+                tma_load_4d(b_dst, bmap, &ctrl->full[stage], kb * KE, ti.n0, 0, gb, pol_b);
             } else {
               if (PAIR)
-                tma_load_3d_pair(b_dst, &tmap_b, fbar, kb * KE,
-                                 ti.n0 + static_cast<int>(rank) * (p.bn / 2), ti.g, pol_b);
+                tma_load_3d_pair(b_dst, bmap, fbar, kb * KE,
+                                 ti.n0 + static_cast<int>(rank) * (p.bn / 2), gb, pol_b);
               else
-                tma_load_3d(b_dst, &tmap_b, &ctrl->full[stage], kb * KE, ti.n0, ti.g, pol_b);
+                tma_load_3d(b_dst, bmap, &ctrl->full[stage], kb * KE, ti.n0, gb, pol_b);
             }
           } else if (FP8) {
             // raw e4m3 boxes land on this CTA's own barrier for its converters
@@ -652,60 +682,60 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
             mbar_arrive_expect_tx(&ctrl->raw_full[stage], nraw * RAW_BOX_BYTES);
             if (EPI == kEpiGateUpAct) {
               if (PAIR) {  // rank 0: gate half, rank 1: up half
-                tma_load_4d(r_dst, &tmap_b, &ctrl->raw_full[stage], ti.n0, static_cast<int>(rank),
-                            kb * BK, ti.g, pol_b);
+                tma_load_4d(r_dst, bmap, &ctrl->raw_full[stage], ti.n0, static_cast<int>(rank),
+                            kb * BK, gb, pol_b);
               } else {
-                tma_load_4d(r_dst, &tmap_b, &ctrl->raw_full[stage], ti.n0, 0, kb * BK, ti.g, pol_b);
-                tma_load_4d(r_dst + RAW_BOX_BYTES, &tmap_b, &ctrl->raw_full[stage], ti.n0, 1,
-                            kb * BK, ti.g, pol_b);
+                tma_load_4d(r_dst, bmap, &ctrl->raw_full[stage], ti.n0, 0, kb * BK, gb, pol_b);
+                tma_load_4d(r_dst + RAW_BOX_BYTES, bmap, &ctrl->raw_full[stage], ti.n0, 1,
+                            kb * BK, gb, pol_b);
               }
             } else {
               const int c0 = ti.n0 + (PAIR ? 128 * static_cast<int>(rank) : 0);
               for (int j = 0; j < nraw; ++j)
-                tma_load_3d(r_dst + j * RAW_BOX_BYTES, &tmap_b, &ctrl->raw_full[stage],
-                            c0 + 128 * j, kb * BK, ti.g, pol_b);
+                tma_load_3d(r_dst + j * RAW_BOX_BYTES, bmap, &ctrl->raw_full[stage],
+                            c0 + 128 * j, kb * BK, gb, pol_b);
             }
           } else if (p.b_wide) {
             // one load brings this CTA's whole B share: 64-column blocks
             // n0/64 .. (gate then up in the gate/up pass; rank r its half in a pair)
             if (EPI == kEpiGateUpAct) {
               if (PAIR)
-                tma_load_5d_pair(b_dst, &tmap_b, fbar, 0, kb * BK, ti.n0 / 64, static_cast<int>(rank),
-                                 ti.g, pol_b);
+                tma_load_5d_pair(b_dst, bmap, fbar, 0, kb * BK, ti.n0 / 64, static_cast<int>(rank),
+                                 gb, pol_b);
               else
-                tma_load_5d(b_dst, &tmap_b, &ctrl->full[stage], 0, kb * BK, ti.n0 / 64, 0, ti.g,
+                tma_load_5d(b_dst, bmap, &ctrl->full[stage], 0, kb * BK, ti.n0 / 64, 0, gb,
                             pol_b);
             } else {
               if (PAIR)
-                tma_load_4d_pair(b_dst, &tmap_b, fbar, 0, kb * BK,
-                                 ti.n0 / 64 + static_cast<int>(rank) * nbox_cta, ti.g, pol_b);
+                tma_load_4d_pair(b_dst, bmap, fbar, 0, kb * BK,
+                                 ti.n0 / 64 + static_cast<int>(rank) * nbox_cta, gb, pol_b);
               else
-                tma_load_4d(b_dst, &tmap_b, &ctrl->full[stage], 0, kb * BK, ti.n0 / 64, ti.g, pol_b);
+                tma_load_4d(b_dst, bmap, &ctrl->full[stage], 0, kb * BK, ti.n0 / 64, gb, pol_b);
             }
           } else if (EPI == kEpiGateUpAct) {
             if (PAIR) {  // rank 0: gate columns n0..n0+127, rank 1: up columns
               for (int j = 0; j < 2; ++j)
-                tma_load_4d_pair(b_dst + j * B_BOX_BYTES, &tmap_b, fbar, ti.n0 + 64 * j,
-                                 static_cast<int>(rank), kb * BK, ti.g, pol_b);
+                tma_load_4d_pair(b_dst + j * B_BOX_BYTES, bmap, fbar, ti.n0 + 64 * j,
+                                 static_cast<int>(rank), kb * BK, gb, pol_b);
             } else {
               // gate columns n0..n0+127 into boxes 0,1; up columns into boxes 2,3
               for (int j = 0; j < 2; ++j) {
-                tma_load_4d(b_dst + j * B_BOX_BYTES, &tmap_b, &ctrl->full[stage], ti.n0 + 64 * j,
-                            0, kb * BK, ti.g, pol_b);
-                tma_load_4d(b_dst + (2 + j) * B_BOX_BYTES, &tmap_b, &ctrl->full[stage],
-                            ti.n0 + 64 * j, 1, kb * BK, ti.g, pol_b);
+                tma_load_4d(b_dst + j * B_BOX_BYTES, bmap, &ctrl->full[stage], ti.n0 + 64 * j,
+                            0, kb * BK, gb, pol_b);
+                tma_load_4d(b_dst + (2 + j) * B_BOX_BYTES, bmap, &ctrl->full[stage],
+                            ti.n0 + 64 * j, 1, kb * BK, gb, pol_b);
               }
             }
           } else {
             if (PAIR) {  // rank r: columns n0 + r*bn/2 ...
               const int c0 = ti.n0 + static_cast<int>(rank) * 64 * nbox_cta;
               for (int j = 0; j < nbox_cta; ++j)
-                tma_load_3d_pair(b_dst + j * B_BOX_BYTES, &tmap_b, fbar, c0 + 64 * j, kb * BK,
-                                 ti.g, pol_b);
+                tma_load_3d_pair(b_dst + j * B_BOX_BYTES, bmap, fbar, c0 + 64 * j, kb * BK,
+                                 gb, pol_b);
             } else {
               for (int j = 0; j < nbox; ++j)
-                tma_load_3d(b_dst + j * B_BOX_BYTES, &tmap_b, &ctrl->full[stage], ti.n0 + 64 * j,
-                            kb * BK, ti.g, pol_b);
+                tma_load_3d(b_dst + j * B_BOX_BYTES, bmap, &ctrl->full[stage], ti.n0 + 64 * j,
+                            kb * BK, gb, pol_b);
             }
           }
           }  // lane 0
@@ -992,7 +1022,7 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
               ok = mbar_wait(&ctrl->xch_full, xch_phase, abort_flag);
               __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
               __nv_bfloat16* out_lo = reinterpret_cast<__nv_bfloat16*>(p.out_lo);
-              const float* sg = p.b_scale ? p.b_scale + static_cast<size_t>(ti.g) * 2 * p.N : nullptr;
+              const float* sg = bscale_base(ti.g, 2);
               const float gs = (sg && f < p.N) ? sg[f] : 1.0f;
               const float us = (sg && f < p.N) ? sg[p.N + f] : 1.0f;
 #pragma unroll 1
@@ -1026,8 +1056,8 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
             // or hi e4m3 terms) and R + j (h_lo rows, lo terms) add up to row j's
             // result (one plane: column j alone)
             const int f = ti.n0 + 128 * static_cast<int>(rank) + quarter * 32 + lane;
-            const float cs =
-                (p.b_scale && f < p.N) ? p.b_scale[static_cast<size_t>(ti.g) * p.N + f] : 1.0f;
+            const float* sb = bscale_base(ti.g, 1);
+            const float cs = (sb && f < p.N) ? sb[f] : 1.0f;
 #pragma unroll 1
             for (int c = 0; c < R; c += 32) {
               uint32_t hi[32], lo[32];
@@ -1084,7 +1114,7 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
       if (EPI == kEpiGateUpAct) {
         __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
         __nv_bfloat16* out_lo = reinterpret_cast<__nv_bfloat16*>(p.out_lo);
-        const float* sg = p.b_scale ? p.b_scale + static_cast<size_t>(ti.g) * 2 * p.N : nullptr;
+        const float* sg = bscale_base(ti.g, 2);
         const float rs =
             (p.a_row_scale && valid)
                 ? p.a_row_scale[p.a_gather ? p.a_gather[out_row] / p.gather_k : out_row]
@@ -1144,7 +1174,7 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
         // this split's output plane (bf16 rows for fp8-weight layers)
         using OutT = StoreT<FP8 || Q8>;
         OutT* out = reinterpret_cast<OutT*>(p.out) + plane;
-        const float* sc = p.b_scale ? p.b_scale + static_cast<size_t>(ti.g) * p.N : nullptr;
+        const float* sc = bscale_base(ti.g, 1);
         const float rs = (p.a_row_scale && valid) ? p.a_row_scale[out_row] : 1.0f;
         // after the transpose lane l owns 4 columns (4 * (l % 8) ..) of rows
         // l / 8, l / 8 + 4, ...: one warp store writes 4 rows x 128 bytes
@@ -1374,7 +1404,7 @@ __global__ void __launch_bounds__(DecCfg<SPLIT, FP8>::kThreads, 1)
     tmem_alloc(&ctrl->tmem_slot, DEC_TMEM_COLS);
     tmem_relinquish();
   }
-  if (warp == 2) build_schedule(ctrl, p.group_offsets, G, p.M, NT, p.err, lane, p.lpt);
+  if (warp == 2) build_schedule(ctrl, p.group_offsets, G, p.M, NT, p.err, lane, p.lpt, p.sh_rows);
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
@@ -1735,7 +1765,8 @@ bool encode_tmap(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims
 template <int EPI, bool SPLIT, bool FP8, bool PAIR, bool Q8 = false>
 cudaError_t launch_epi(const CUtensorMap& ta, const CUtensorMap& ta_lo, const CUtensorMap& tb,
                        const CUtensorMap& tb_tail, const CUtensorMap& ta_tail,
-                       const CUtensorMap& ta_lo_tail, const KParams& kp, long long max_tiles,
+                       const CUtensorMap& ta_lo_tail, const CUtensorMap& tb2,
+                       const CUtensorMap& tb2_tail, const KParams& kp, long long max_tiles,
                        cudaStream_t s) {
   constexpr size_t smem = smem_bytes<SPLIT, FP8, PAIR>();
   constexpr int threads = StageCfg<SPLIT, FP8, PAIR>::kThreads;
@@ -1754,7 +1785,7 @@ cudaError_t launch_epi(const CUtensorMap& ta, const CUtensorMap& ta_lo, const CU
     const int grid =
         static_cast<int>(std::max<long long>(1, std::min<long long>(device_sm_count(), max_tiles)));
     return launch_kernel(kern, dim3(grid), dim3(threads), smem, s, ta, ta_lo, tb, tb_tail, ta_tail,
-                         ta_lo_tail, kp);
+                         ta_lo_tail, tb2, tb2_tail, kp);
   }
   // one persistent 2-CTA cluster per SM pair that can hold one
   cudaLaunchConfig_t cfg = {};
@@ -1783,7 +1814,8 @@ cudaError_t launch_epi(const CUtensorMap& ta, const CUtensorMap& ta_lo, const CU
       1, std::min<long long>(max_clusters[(dev >= 0 && dev < 64) ? dev : 0], max_tiles)));
   cfg.gridDim = dim3(2 * nclu, 1, 1);
   cfg.numAttrs = 2;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, ta_lo, tb, tb_tail, ta_tail, ta_lo_tail, kp);
+  cudaError_t e =
+      cudaLaunchKernelEx(&cfg, kern, ta, ta_lo, tb, tb_tail, ta_tail, ta_lo_tail, tb2, tb2_tail, kp);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -1851,6 +1883,8 @@ cudaError_t launch_grouped_gemm_decode_q8(const GroupedGemmArgs& a, int nt, cuda
   kp.comb_w = a.comb_w;
   kp.comb_k = a.comb_k;
   kp.lpt = g_tile_order == 1 && a.group_offsets != nullptr && a.G > 1;
+  kp.sh_rows = a.sh_rows;
+  kp.sh_b_scale = a.sh_b_scale;
   kp.bn = nt;
   kp.ksplit = 1;
   kp.kbs = (a.K + 127) / 128;
@@ -1919,6 +1953,8 @@ cudaError_t launch_grouped_gemm_decode(const GroupedGemmArgs& a, int nt, cudaStr
   kp.comb_w = a.comb_w;
   kp.comb_k = a.comb_k;
   kp.lpt = g_tile_order == 1 && a.group_offsets != nullptr && a.G > 1;
+  kp.sh_rows = a.sh_rows;
+  kp.sh_b_scale = a.sh_b_scale;
   kp.bn = nt;
   kp.ksplit = 1;
   kp.kbs = (a.K + BK - 1) / BK;
@@ -1981,6 +2017,8 @@ cudaError_t launch_grouped_gemm_q8(const GroupedGemmArgs& a, cudaStream_t s) {
   kp.comb_w = a.comb_w;
   kp.comb_k = a.comb_k;
   kp.lpt = g_tile_order == 1 && a.group_offsets != nullptr && a.G > 1;
+  kp.sh_rows = a.sh_rows;
+  kp.sh_b_scale = a.sh_b_scale;
   kp.ksplit = 1;
   kp.kbs = (a.K + 127) / 128;
   if (a.epilogue == kEpiGateUpAct) {
@@ -2026,25 +2064,38 @@ cudaError_t launch_grouped_gemm_q8(const GroupedGemmArgs& a, cudaStream_t s) {
     if (one) ta_lo_tail = ta_tail;
     else if (!encode_tmap(&ta_lo_tail, lo, 2, dims, strides, tbox, u8)) return cudaErrorInvalidValue;
   }
-  if (a.epilogue == kEpiGateUpAct) {  // [G][2][N][K]: gate rows, then up rows
-    const uint64_t dims[4] = {K, N, 2, G};
-    const uint64_t strides[3] = {K, N * K, 2 * N * K};
-    const uint32_t box[4] = {128, 128, pair ? 1u : 2u, 1};
-    if (!encode_tmap(&tb, a.B, 4, dims, strides, box, u8)) return cudaErrorInvalidValue;
-    const uint32_t tbox[4] = {128, 64, 2, 1};  // swapped tails: 64 gate + 64 up rows per CTA
-    if (!encode_tmap(&tb_tail, a.B, 4, dims, strides, tbox, u8)) return cudaErrorInvalidValue;
-  } else {  // [G][N][K]
-    const uint64_t dims[3] = {K, N, G};
+  // the weight maps of a tensor of ng matrices: the routed experts, or the
+  // shared expert's one matrix (the last group when sh_rows > 0)
+  auto make_b = [&](const void* Bp, uint64_t ng, CUtensorMap& mb, CUtensorMap& mb_tail) {
+    if (a.epilogue == kEpiGateUpAct) {  // [G][2][N][K]: gate rows, then up rows
+      const uint64_t dims[4] = {K, N, 2, ng};
+      const uint64_t strides[3] = {K, N * K, 2 * N * K};
+      const uint32_t box[4] = {128, 128, pair ? 1u : 2u, 1};
+      const uint32_t tbox[4] = {128, 64, 2, 1};  // swapped tails: 64 gate + 64 up rows per CTA
+      return encode_tmap(&mb, Bp, 4, dims, strides, box, u8) &&
+             encode_tmap(&mb_tail, Bp, 4, dims, strides, tbox, u8);
+    }
+    const uint64_t dims[3] = {K, N, ng};  // [G][N][K]
     const uint64_t strides[2] = {K, N * K};
     const uint32_t box[3] = {128, static_cast<uint32_t>(pair ? kp.bn / 2 : kp.bn), 1};
-    if (!encode_tmap(&tb, a.B, 3, dims, strides, box, u8)) return cudaErrorInvalidValue;
-    tb_tail = tb;
+    if (!encode_tmap(&mb, Bp, 3, dims, strides, box, u8)) return false;
+    mb_tail = mb;
+    return true;
+  };
+  CUtensorMap tb2, tb2_tail;
+  if (!make_b(a.B, G - (a.sh_rows > 0 ? 1 : 0), tb, tb_tail)) return cudaErrorInvalidValue;
+  if (a.sh_rows > 0) {
+    if (!make_b(a.sh_B, 1, tb2, tb2_tail)) return cudaErrorInvalidValue;
+  } else {
+    tb2 = tb;
+    tb2_tail = tb_tail;
   }
   const int tile_m = pair ? 2 * BM : BM;
   const long long max_tiles = (static_cast<long long>((a.M + tile_m - 1) / tile_m) + a.G) *
                               static_cast<long long>(kp.n_tiles);
 #define MOE_LAUNCH_Q8(E_, S_, P_) \
-  launch_epi<E_, S_, false, P_, true>(ta, ta_lo, tb, tb_tail, ta_tail, ta_lo_tail, kp, max_tiles, s)
+  launch_epi<E_, S_, false, P_, true>(ta, ta_lo, tb, tb_tail, ta_tail, ta_lo_tail, tb2, tb2_tail, kp, \
+                                      max_tiles, s)
   if (one) {
     if (a.epilogue == kEpiGateUpAct)
       return pair ? MOE_LAUNCH_Q8(kEpiGateUpAct, false, true) : MOE_LAUNCH_Q8(kEpiGateUpAct, false, false);
@@ -2092,6 +2143,11 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
   if (a.M <= 0) return cudaSuccess;
   if (a.epilogue == kEpiCombineF32 && (!a.comb_rows || !a.comb_w || a.comb_k < 1 || a.ksplit > 1))
     return cudaErrorInvalidValue;
+  // the shared expert as the last group: 128-row / 2-CTA tiles only, its own
+  // weight tensor, no row gather or split-K; weights expanded on chip excluded
+  if (a.sh_rows > 0 && (!a.sh_B || a.a_gather || a.ksplit > 1 || a.sh_rows > a.M || a.G < 2 ||
+                        (a.b_fp8 && !a.a_e4m3x2 && !a.a_e4m3)))
+    return cudaErrorInvalidValue;
   // Swap-AB kernel (weights as the 128-row operand) where it measured faster
   // than 128-row tiles on GB300, with 16 rows per tile: a single group of at
   // most 64 rows (the shared expert at decode: more, smaller tiles), at most
@@ -2114,6 +2170,7 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
   else if (!a.b_fp8 && Gg <= 256 && Mg <= 4 * Gg) nt = 16;
   else if (a.b_fp8 && Mg <= 16 * Gg) nt = DEC_NT_MAX;
   if (g_decode_kernel && nt && a.decode_ok && !a.a_gather && a.ksplit <= 1 && a.G <= MAX_G &&
+      a.sh_rows == 0 &&
       (a.epilogue == kEpiGateUpAct || a.epilogue == kEpiStoreF32 || a.epilogue == kEpiCombineF32)) {
     if (!a.a_e4m3x2 && !a.a_e4m3 && (a.a_fp16 != 0) != (a.b_fp8 != 0)) return cudaErrorInvalidValue;
     if (a.b_fp8 && a.A_lo) return cudaErrorNotSupported;
@@ -2164,6 +2221,8 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
   kp.comb_w = a.comb_w;
   kp.comb_k = a.comb_k;
   kp.lpt = g_tile_order == 1 && a.group_offsets != nullptr && a.G > 1;
+  kp.sh_rows = a.sh_rows;
+  kp.sh_b_scale = a.sh_b_scale;
   {
     const int KB = (a.K + BK - 1) / BK;
     int ks = std::max(1, std::min(a.ksplit, KB));
@@ -2204,33 +2263,54 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
   // brings all the blocks of a stage in the layout the MMA reads (box 0 at
   // offset 0, box j at j * 8 KB).  Otherwise one load per 64-column box.
   kp.b_wide = (!a.b_fp8 && N % 64 == 0) ? 1 : 0;
-  const uint64_t G64 = static_cast<uint64_t>(a.G);
-  if (kp.b_wide && a.epilogue == kEpiGateUpAct) {
-    const uint64_t dims[5] = {64, K, N / 64, 2, G64};
-    const uint64_t strides[4] = {2 * N * eb, 64 * eb, N * eb, K * 2 * N * eb};
-    const uint32_t box[5] = {64, BK, 2, pair ? 1u : 2u, 1};
-    if (!encode_tmap(&tb, a.B, 5, dims, strides, box, bdt)) return cudaErrorInvalidValue;
-  } else if (kp.b_wide) {
-    const uint64_t dims[4] = {64, K, N / 64, G64};
-    const uint64_t strides[3] = {N * eb, 64 * eb, K * N * eb};
-    const uint32_t nb = static_cast<uint32_t>(kp.bn / 64) / (pair ? 2u : 1u);
-    const uint32_t box[4] = {64, BK, nb, 1};
-    if (!encode_tmap(&tb, a.B, 4, dims, strides, box, bdt)) return cudaErrorInvalidValue;
-  } else if (a.epilogue == kEpiGateUpAct) {
-    const uint64_t dims[4] = {N, 2, K, G64};
-    const uint64_t strides[3] = {N * eb, 2 * N * eb, K * 2 * N * eb};
-    const uint32_t box[4] = {box_n, 1, BK, 1};
-    if (!encode_tmap(&tb, a.B, 4, dims, strides, box, bdt)) return cudaErrorInvalidValue;
-  } else {
-    const uint64_t dims[3] = {N, K, G64};
-    const uint64_t strides[2] = {N * eb, K * N * eb};
-    const uint32_t box[3] = {box_n, BK, 1};
-    if (!encode_tmap(&tb, a.B, 3, dims, strides, box, bdt)) return cudaErrorInvalidValue;
-  }
   // 2-CTA tiles: a group's last tile with few rows runs swapped (rows as the
   // MMA N); the gate/up pass then loads one gate and one up block per CTA
   kp.swap_tail = (pair && g_pair_tiles != 2) ? (a.epilogue == kEpiGateUpAct ? 64 : 128) : 0;
-  CUtensorMap tb_tail = tb, ta_tail = ta, ta_lo_tail = ta_lo;
+  // the weight maps of a tensor of ng matrices: the routed experts, or the
+  // shared expert's one matrix (the last group when sh_rows > 0)
+  auto make_b = [&](const void* Bp, uint64_t G64, CUtensorMap& mb, CUtensorMap& mb_tail) {
+    bool ok;
+    if (kp.b_wide && a.epilogue == kEpiGateUpAct) {
+      const uint64_t dims[5] = {64, K, N / 64, 2, G64};
+      const uint64_t strides[4] = {2 * N * eb, 64 * eb, N * eb, K * 2 * N * eb};
+      const uint32_t box[5] = {64, BK, 2, pair ? 1u : 2u, 1};
+      ok = encode_tmap(&mb, Bp, 5, dims, strides, box, bdt);
+    } else if (kp.b_wide) {
+      const uint64_t dims[4] = {64, K, N / 64, G64};
+      const uint64_t strides[3] = {N * eb, 64 * eb, K * N * eb};
+      const uint32_t nb = static_cast<uint32_t>(kp.bn / 64) / (pair ? 2u : 1u);
+      const uint32_t box[4] = {64, BK, nb, 1};
+      ok = encode_tmap(&mb, Bp, 4, dims, strides, box, bdt);
+    } else if (a.epilogue == kEpiGateUpAct) {
+      const uint64_t dims[4] = {N, 2, K, G64};
+      const uint64_t strides[3] = {N * eb, 2 * N * eb, K * 2 * N * eb};
+      const uint32_t box[4] = {box_n, 1, BK, 1};
+      ok = encode_tmap(&mb, Bp, 4, dims, strides, box, bdt);
+    } else {
+      const uint64_t dims[3] = {N, K, G64};
+      const uint64_t strides[2] = {N * eb, K * N * eb};
+      const uint32_t box[3] = {box_n, BK, 1};
+      ok = encode_tmap(&mb, Bp, 3, dims, strides, box, bdt);
+    }
+    mb_tail = mb;
+    if (ok && kp.swap_tail && kp.b_wide && a.epilogue == kEpiGateUpAct) {
+      const uint64_t dims[5] = {64, K, N / 64, 2, G64};
+      const uint64_t strides[4] = {2 * N * eb, 64 * eb, N * eb, K * 2 * N * eb};
+      const uint32_t box[5] = {64, BK, 1, 2, 1};
+      ok = encode_tmap(&mb_tail, Bp, 5, dims, strides, box, bdt);
+    }
+    return ok;
+  };
+  CUtensorMap tb_tail, tb2, tb2_tail;
+  if (!make_b(a.B, static_cast<uint64_t>(a.G - (a.sh_rows > 0 ? 1 : 0)), tb, tb_tail))
+    return cudaErrorInvalidValue;
+  if (a.sh_rows > 0) {
+    if (!make_b(a.sh_B, 1, tb2, tb2_tail)) return cudaErrorInvalidValue;
+  } else {
+    tb2 = tb;
+    tb2_tail = tb_tail;
+  }
+  CUtensorMap ta_tail = ta, ta_lo_tail = ta_lo;
   if (kp.swap_tail) {  // swapped tails load their rows in 32-row boxes
     const uint64_t dims[2] = {static_cast<uint64_t>(a.K), static_cast<uint64_t>(a.M)};
     const uint64_t strides[1] = {static_cast<uint64_t>(a.K) * 2};
@@ -2239,21 +2319,15 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
     if (a.A_lo && !encode_tmap(&ta_lo_tail, a.A_lo, 2, dims, strides, box))
       return cudaErrorInvalidValue;
   }
-  if (kp.swap_tail && kp.b_wide && a.epilogue == kEpiGateUpAct) {
-    const uint64_t dims[5] = {64, K, N / 64, 2, G64};
-    const uint64_t strides[4] = {2 * N * eb, 64 * eb, N * eb, K * 2 * N * eb};
-    const uint32_t box[5] = {64, BK, 1, 2, 1};
-    if (!encode_tmap(&tb_tail, a.B, 5, dims, strides, box, bdt)) return cudaErrorInvalidValue;
-  }
   const int tile_m = pair ? 2 * BM : BM;
   const long long max_tiles = (static_cast<long long>((a.M + tile_m - 1) / tile_m) + a.G) *
                               static_cast<long long>(kp.n_tiles) * kp.ksplit;
   // (pair is never set for fp8 weights: their kernels exist on 1-CTA tiles only)
 #define MOE_LAUNCH(E_, S_, F_)                                                               \
   ((pair && !(F_)) ? launch_epi<E_, S_, F_, !(F_)>(ta, ta_lo, tb, tb_tail, ta_tail, ta_lo_tail, \
-                                                  kp, max_tiles, s)                           \
+                                                  tb2, tb2_tail, kp, max_tiles, s)            \
                    : launch_epi<E_, S_, F_, false>(ta, ta_lo, tb, tb_tail, ta_tail, ta_lo_tail, \
-                                                   kp, max_tiles, s))
+                                                   tb2, tb2_tail, kp, max_tiles, s))
   if (a.epilogue == kEpiGateUpAct) {
     if (a.A_lo) return cudaErrorInvalidValue;
     return a.b_fp8 ? MOE_LAUNCH(kEpiGateUpAct, false, true) : MOE_LAUNCH(kEpiGateUpAct, false, false);

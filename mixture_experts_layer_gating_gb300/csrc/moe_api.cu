@@ -17,6 +17,7 @@ constexpr size_t kAlign = 256;
 int g_gather_a = 0;       // moe_set_option(MOE_OPT_GATHER_A, .)
 int g_shared_stream = 1;  // moe_set_option(MOE_OPT_SHARED_STREAM, .)
 int g_fused_combine = 0;  // moe_set_option(MOE_OPT_FUSED_COMBINE, .)
+int g_shared_in_gemm = 0;  // moe_set_option(MOE_OPT_SHARED_IN_GEMM, .)
 
 // The shared expert depends on x alone, so moe_layer runs it on a second
 // stream of the library's own (one per device, created on first use) that
@@ -147,6 +148,19 @@ cudaError_t rows_to_fp8_layer_form(const moe_config_t* c, const void* x, int row
   return is_nk(c) ? launch_rows_to_e4m3x2(x, rows, D, q, inv_scale, s, src_f32)
                   : launch_rows_to_fp16(x, rows, D, q, inv_scale, s, src_f32);
 }
+// The shared expert can run as one more group of the routed GEMMs (it then
+// has rows R .. R+T-1 of the permuted rows, h and the expert outputs): its
+// intermediate size equals the experts', and the weights are bf16 or
+// K-contiguous e4m3 (the 128-row / 2-CTA tile kernels).  The workspace of
+// such a layer always has room for those T extra rows.
+inline bool shared_group_capable(const moe_config_t* c) {
+  return c->I_shared > 0 && c->I_shared == c->I && c->act_dtype == MOE_BF16 &&
+         (c->w_dtype == MOE_BF16 || is_nk(c));
+}
+inline bool shared_in_gemm_on(const moe_config_t* c) {
+  return g_shared_in_gemm && shared_group_capable(c) && !g_gather_a;
+}
+
 // Bytes per row of D elements in the form moe_layer permutes: x itself, or
 // for fp8 layers their A-row form (2 bytes per element, 1 for W8A8).
 inline size_t layer_row_bytes(const moe_config_t* c) {
@@ -158,6 +172,9 @@ Layout make_layout(const moe_config_t* c) {
   const size_t T = c->T, E = c->E, R = static_cast<size_t>(c->T) * c->k, D = c->D, I = c->I,
                Is = c->I_shared;
   const size_t ab = act_bytes(c->act_dtype);
+  // rows of the permuted rows, h and the expert outputs: R, plus T when the
+  // shared expert may run as the last group of the routed GEMMs
+  const size_t Rx = R + (shared_group_capable(c) ? T : 0);
   size_t cur = sizeof(ControlBlock);
   auto take = [&](size_t bytes) {
     const size_t o = cur;
@@ -176,17 +193,17 @@ Layout make_layout(const moe_config_t* c) {
   L.off[MOE_WS_SORTED_ROWS] = take(R * 4);
   L.off[MOE_WS_DEST] = take(R * 4);
   L.seg_scratch = take(E * static_cast<size_t>(route_segments(static_cast<long long>(R))) * 4 + 4);
-  L.off[MOE_WS_X_PERM] = take(R * D * ab);
-  L.off[MOE_WS_H] = take(R * I * 4);         // fp32, bf16 (hi, lo) planes, or bf16
-  L.off[MOE_WS_Y_PERM] = take(R * D * 4);    // fp32 (bf16 rows for fp8 layers)
+  L.off[MOE_WS_X_PERM] = take(Rx * D * ab);
+  L.off[MOE_WS_H] = take(Rx * I * 4);        // fp32, bf16 (hi, lo) planes, or bf16
+  L.off[MOE_WS_Y_PERM] = take(Rx * D * 4);   // fp32 (bf16 rows for fp8 layers)
   L.off[MOE_WS_H_SHARED] = take(T * Is * 4);
   L.off[MOE_WS_S] = take(T * D * 4);
   if (is_fp8(c)) {
     L.x16 = take(T * D * 2);
     L.tok_inv = take(T * 4);
-    L.row_inv = take(R * 4);
-    L.h16 = take(R * I * 2);
-    L.h_inv = take(R * 4);
+    L.row_inv = take(Rx * 4);
+    L.h16 = take(Rx * I * 2);
+    L.h_inv = take(Rx * 4);
     L.hs16 = take(T * Is * 2);
     L.hs_inv = take(T * 4);
   }
@@ -269,10 +286,12 @@ int do_route(const moe_config_t* c, const void* x, const void* Wg, const float* 
 }
 
 // row_bytes: bytes of one row of x (act_dtype rows, or moe_layer's fp8 row form)
+// extra_rows = T: x_perm rows R .. R+T-1 become copies of the tokens (the
+// shared expert's rows as the last group of the routed GEMMs).
 int do_permute(const moe_config_t* c, const int32_t* ids, const void* x, int32_t* counts,
                int32_t* offsets, int32_t* sorted_rows, int32_t* dest, void* x_perm,
                int32_t* seg_scratch, int32_t* err, cudaStream_t s, size_t row_bytes,
-               const float* tok_scale = nullptr, float* row_scale = nullptr) {
+               const float* tok_scale = nullptr, float* row_scale = nullptr, int extra_rows = 0) {
   const int R = c->T * c->k;
   if (small_route(R, c->E)) {  // one launch: sort + gather
     trace_mark(s);
@@ -280,7 +299,7 @@ int do_permute(const moe_config_t* c, const int32_t* ids, const void* x, int32_t
     return cuda_status(launch_route_permute_small(
         ids, R, c->E, c->k, c->T, counts, offsets, sorted_rows, dest, gather ? x : nullptr,
         row_bytes, gather ? x_perm : nullptr, tok_scale,
-        row_scale, err, s));
+        row_scale, err, s, extra_rows));
   }
   cudaError_t e = launch_init_routing(ids, R, c->E, counts, offsets, sorted_rows, dest, seg_scratch,
                                       err, s, g_trace_next >= 0 ? trace_mark : nullptr);
@@ -294,10 +313,10 @@ int do_permute(const moe_config_t* c, const int32_t* ids, const void* x, int32_t
     // 28.8 us in favour of the gather)
     if (static_cast<size_t>(c->T) * row_bytes > (size_t{32} << 20))
       e = launch_permute_scatter(x, dest, offsets + c->E, R, c->k, c->T, row_bytes, x_perm, err, s,
-                                 tok_scale, row_scale);
+                                 tok_scale, row_scale, extra_rows);
     else
       e = launch_permute_gather(x, sorted_rows, R, c->k, c->T, row_bytes, x_perm, err, s, tok_scale,
-                                row_scale);
+                                row_scale, extra_rows);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   }
   return MOE_OK;
@@ -315,7 +334,9 @@ int do_ffn(const moe_config_t* c, const void* A, const float* a_row_scale, int M
            const int32_t* offsets, int G, const void* W13, const float* s13, const void* W2,
            const float* s2, int I, void* h, void* y, void* h16, float* h_inv, int32_t* err,
            cudaStream_t s, const int32_t* a_gather = nullptr, int a_rows = 0,
-           const int32_t* comb_rows = nullptr, const float* comb_w = nullptr) {
+           const int32_t* comb_rows = nullptr, const float* comb_w = nullptr, int sh_rows = 0,
+           const void* W13s = nullptr, const float* s13s = nullptr, const void* W2s = nullptr,
+           const float* s2s = nullptr) {
   if (M <= 0) return MOE_OK;
   cudaError_t e;
   trace_mark(s);
@@ -361,6 +382,9 @@ int do_ffn(const moe_config_t* c, const void* A, const float* a_row_scale, int M
   a.pair_ok = 1;
   a.decode_ok = 1;
   a.err = err;
+  a.sh_rows = sh_rows;  // > 0: the last group is the shared expert (its own weights)
+  a.sh_B = W13s;
+  a.sh_b_scale = s13s;
   e = launch_grouped_gemm(a, s);
   if (e != cudaSuccess) return e == cudaErrorNotSupported ? MOE_ERR_UNSUPPORTED : MOE_ERR_CUDA;
   if (fp8) {
@@ -382,6 +406,8 @@ int do_ffn(const moe_config_t* c, const void* A, const float* a_row_scale, int M
   b.h_fp32 = 0;
   b.out = y;  // fp8-weight layers: the store pass writes bf16 rows
   b.out_lo = nullptr;
+  b.sh_B = W2s;
+  b.sh_b_scale = s2s;
   if (comb_rows) {
     b.epilogue = kEpiCombineF32;
     b.comb_rows = comb_rows;
@@ -404,10 +430,18 @@ int do_grouped_ffn(const moe_config_t* c, const void* x_perm, const float* xp_sc
                    const void* W13s, const float* s13s, const void* W2s, const float* s2s,
                    void* h_s, void* s_out, void* ws, int32_t* err, cudaStream_t s,
                    const int32_t* gather = nullptr, const int32_t* comb_rows = nullptr,
-                   const float* comb_w = nullptr) {
+                   const float* comb_w = nullptr, bool shared_in_gemm = false) {
   const int R = c->T * c->k;
   const Layout L = make_layout(c);
   const bool fp8 = is_fp8(c);
+  if (shared_in_gemm) {
+    // the shared expert as group E of the routed GEMMs: rows R .. R+T-1 of
+    // x_perm (written by the permutation), h and y_perm
+    return do_ffn(c, x_perm, xp_scale, R + c->T, offsets, c->E + 1, W13, s13, W2, s2, c->I, h, y_perm,
+                  fp8 ? ws_at(ws, L.h16) : nullptr,
+                  fp8 ? reinterpret_cast<float*>(ws_at(ws, L.h_inv)) : nullptr, err, s, nullptr, 0,
+                  comb_rows, comb_w, c->T, W13s, s13s, W2s, s2s);
+  }
   int st = do_ffn(c, x_perm, xp_scale, R, offsets, c->E, W13, s13, W2, s2, c->I, h, y_perm,
                   fp8 ? ws_at(ws, L.h16) : nullptr,
                   fp8 ? reinterpret_cast<float*>(ws_at(ws, L.h_inv)) : nullptr, err, s, gather,
@@ -586,10 +620,12 @@ int moe_layer(const moe_config_t* cfg, const void* x, const void* Wg, const floa
       return (g_trace_next = -1, MOE_ERR_CUDA);
     x_rows = x16;
   }
-  // The shared expert on the side stream (not while tracing: the trace
-  // events time kernels one after another on the caller's stream).
+  // The shared expert as the last group of the routed GEMMs
+  // (MOE_OPT_SHARED_IN_GEMM), or on the side stream (not while tracing: the
+  // trace events time kernels one after another on the caller's stream).
+  const bool in_gemm = shared && shared_in_gemm_on(cfg);
   cudaStream_t side = nullptr;
-  if (shared && g_shared_stream && !traced) {
+  if (shared && g_shared_stream && !traced && !in_gemm) {
     side = side_fork(s);
     if (side) {
       st = do_ffn(cfg, x_rows, tok_inv, cfg->T, nullptr, 1, W13s, s13s, W2s, s2s, cfg->I_shared, h_s,
@@ -616,21 +652,30 @@ int moe_layer(const moe_config_t* cfg, const void* x, const void* Wg, const floa
   // four-row requests per 16 KB A tile).
   const bool gather = g_gather_a && cfg->act_dtype != MOE_F32;
   st = do_permute(cfg, ids, gather ? nullptr : x_rows, counts, offsets, sorted_rows, dest,
-                  gather ? nullptr : x_perm, seg, err, s, layer_row_bytes(cfg), tok_inv, row_inv);
+                  gather ? nullptr : x_perm, seg, err, s, layer_row_bytes(cfg), tok_inv, row_inv,
+                  in_gemm ? cfg->T : 0);
   if (st != MOE_OK) return fail(st);
   st = do_grouped_ffn(cfg, gather ? x_rows : x_perm, gather ? tok_inv : row_inv, offsets, W13, s13,
                       W2, s2, h, y_perm, (shared && !side) ? x_rows : nullptr, tok_inv, W13s, s13s,
                       W2s, s2s, h_s, s_out, ws, err, s, gather ? sorted_rows : nullptr,
-                      fused ? sorted_rows : nullptr, fused ? w : nullptr);
+                      fused ? sorted_rows : nullptr, fused ? w : nullptr, in_gemm);
   if (st != MOE_OK) return fail(st);
   if (side && !side_join(side, s)) return (g_trace_next = -1, MOE_ERR_CUDA);
   trace_mark(s);
+  // the shared expert's output rows: s_out, or rows R .. R+T-1 of y_perm when it
+  // ran inside the routed GEMMs (the fused combine has added those already)
+  const void* s_rows =
+      !shared ? nullptr
+              : in_gemm ? static_cast<const void*>(static_cast<const uint8_t*>(y_perm) +
+                                                   static_cast<size_t>(cfg->T) * cfg->k * cfg->D *
+                                                       (fp8 ? 2 : 4))
+                        : s_out;
   if (fused)
-    st = cuda_status(launch_combine_round(static_cast<const float*>(y_perm), shared ? s_out : nullptr,
+    st = cuda_status(launch_combine_round(static_cast<const float*>(y_perm), in_gemm ? nullptr : s_rows,
                                           fp8, cfg->T, cfg->D, out, s));
   else
-    st = cuda_status(launch_finalize(cfg->act_dtype, y_perm, dest, w, shared ? s_out : nullptr, out,
-                                     cfg->T, cfg->k, cfg->D, cfg->T * cfg->k, err, s, fp8));
+    st = cuda_status(launch_finalize(cfg->act_dtype, y_perm, dest, w, s_rows, out, cfg->T, cfg->k,
+                                     cfg->D, cfg->T * cfg->k, err, s, fp8));
   trace_mark(s);
   g_trace_next = -1;
   return st;
@@ -697,6 +742,11 @@ int moe_set_option(int option, int value) {
       g_pdl = value ? 1 : 0;
       return old;
     }
+    case MOE_OPT_SHARED_IN_GEMM: {
+      const int old = g_shared_in_gemm;
+      g_shared_in_gemm = value ? 1 : 0;
+      return old;
+    }
     case MOE_OPT_TILE_ORDER: {
       const int old = g_tile_order;
       g_tile_order = value ? 1 : 0;
@@ -722,9 +772,11 @@ int moe_layer_launch_count(const moe_config_t* cfg) {
   int n = 0;
   n += 1;  // router projection
   n += 1;  // top-k softmax
+  // the shared expert inside the routed GEMMs: no launches of its own
+  const bool sep_shared = cfg->I_shared > 0 && !shared_in_gemm_on(cfg);
   if (is_fp8(cfg)) {
-    n += 1;                          // x to fp16 (or two-term e4m3) rows
-    n += cfg->I_shared > 0 ? 2 : 1;  // h to fp16 (or two-term e4m3) rows, routed (and shared)
+    n += 1;                     // x to fp16 (or e4m3) rows
+    n += sep_shared ? 2 : 1;    // h to fp16 (or e4m3) rows, routed (and shared)
   }
   if (small_route(static_cast<long long>(cfg->T) * cfg->k, cfg->E)) {
     n += 1;  // init_routing + permutation gather in one kernel
@@ -733,7 +785,7 @@ int moe_layer_launch_count(const moe_config_t* cfg) {
     if (cfg->act_dtype == MOE_F32 || !g_gather_a) n += 1;  // permutation gather
   }
   n += 2;  // routed gate/up, down
-  if (cfg->I_shared > 0) n += 2;  // shared gate/up, down
+  if (sep_shared) n += 2;  // shared gate/up, down
   n += 1;  // finalize
   return n;
 }

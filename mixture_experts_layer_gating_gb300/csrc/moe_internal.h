@@ -84,7 +84,7 @@ cudaError_t launch_route_permute_small(const int32_t* ids, int R, int E, int k, 
                                        int32_t* counts, int32_t* offsets, int32_t* sorted_rows,
                                        int32_t* dest, const void* x, size_t row_bytes,
                                        void* x_perm, const float* tok_scale, float* row_scale,
-                                       int32_t* err, cudaStream_t s);
+                                       int32_t* err, cudaStream_t s, int extra_rows = 0);
 
 // Router logits = sum of nsplit fp32 partial planes [nsplit, T, E] (+ bias),
 // written to `logits` when nsplit > 1 or bias != nullptr; then top-k softmax.
@@ -107,15 +107,19 @@ cudaError_t launch_init_routing(const int32_t* ids, int R, int E, int32_t* count
                                 int32_t* sorted_rows, int32_t* dest, int32_t* seg_scratch,
                                 int32_t* err, cudaStream_t s, void (*mark)(cudaStream_t) = nullptr);
 // tok_scale / row_scale (optional): row_scale[p] = tok_scale[sorted_rows[p] / k].
+// extra_rows = T (all three permutation launchers): x_perm rows R + t are
+// also written, copies of token t (the shared expert's rows as the last group
+// of the routed GEMMs); x_perm then holds R + T rows.
 cudaError_t launch_permute_gather(const void* x, const int32_t* sorted_rows, int R, int k, int T,
                                   size_t row_bytes, void* x_perm, int32_t* err, cudaStream_t s,
-                                  const float* tok_scale = nullptr, float* row_scale = nullptr);
+                                  const float* tok_scale = nullptr, float* row_scale = nullptr,
+                                  int extra_rows = 0);
 // The same permutation from the token side (x read once): x_perm[dest[t*k+j]]
 // = x[t]; rows at positions >= *nvalid (only after invalid ids) are zeroed.
 cudaError_t launch_permute_scatter(const void* x, const int32_t* dest, const int32_t* nvalid,
                                    int R, int k, int T, size_t row_bytes, void* x_perm,
                                    int32_t* err, cudaStream_t s, const float* tok_scale = nullptr,
-                                   float* row_scale = nullptr);
+                                   float* row_scale = nullptr, int extra_rows = 0);
 // bf16 (or fp32 when src_f32) rows -> fp16 rows times an exact power of two
 // (max |row| < 2^14); inv_scale[r] = the inverse power of two.
 cudaError_t launch_rows_to_fp16(const void* x, int rows, int D, void* x16, float* inv_scale,
@@ -201,6 +205,12 @@ struct GroupedGemmArgs {
   const int32_t* comb_rows;
   const float* comb_w;
   int comb_k;
+  // > 0: the last group (G - 1) is the shared expert, rows [M - sh_rows, M) of
+  // A (and of the output), weights sh_B (one matrix, laid out as B's) with
+  // per-column scales sh_b_scale (fp8)
+  int sh_rows;
+  const void* sh_B;
+  const float* sh_b_scale;
 };
 
 cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s);

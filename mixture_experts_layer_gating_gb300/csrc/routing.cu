@@ -398,7 +398,7 @@ __global__ void __launch_bounds__(kSmallRouteThreads, 1)
                                int32_t* __restrict__ sorted_rows, int32_t* __restrict__ dest,
                                const uint4* __restrict__ x, int vec_per_row,
                                uint4* __restrict__ x_perm, const float* __restrict__ tok_scale,
-                               float* __restrict__ row_scale, int32_t* err) {
+                               float* __restrict__ row_scale, int32_t* err, int extra) {
   pdl_wait();
   pdl_launch_dependents();
   extern __shared__ int32_t sm[];
@@ -492,18 +492,20 @@ __global__ void __launch_bounds__(kSmallRouteThreads, 1)
   }
   __syncthreads();
   if (!x) return;
-  // (e) gather: one warp per permuted row, grid-strided over all CTAs
+  // (e) gather: one warp per permuted row, grid-strided over all CTAs; with
+  // extra = T, rows R + t are copies of the tokens in order (the shared
+  // expert's rows when it runs as the last group of the routed GEMMs)
   const int nvalid = off_s[E];
   const long long wstride = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
-  for (long long p = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + wid; p < R;
+  for (long long p = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + wid; p < R + extra;
        p += wstride) {
     uint4* dst = x_perm + p * vec_per_row;
-    if (p >= nvalid) {
+    if (p < R && p >= nvalid) {
       if (row_scale && lane == 0) row_scale[p] = 0.0f;
       for (int v = lane; v < vec_per_row; v += 32) dst[v] = make_uint4(0, 0, 0, 0);
       continue;
     }
-    const int t = sorted_s[p] / k;  // a valid row: t < T
+    const int t = p < R ? sorted_s[p] / k : static_cast<int>(p - R);  // a valid row: t < T
     if (row_scale && lane == 0) row_scale[p] = tok_scale[t];
     const uint4* src = x + static_cast<long long>(t) * vec_per_row;
     int v = lane;
@@ -522,17 +524,19 @@ __global__ void __launch_bounds__(kSmallRouteThreads, 1)
 // Permutation gather (the "千问 3.5 MoE 在 TPU 上的系统优化实战" SparseCore
 // paragraph: rows gathered by routing index into one contiguous buffer).
 // One warp per permuted row, 16-byte vectors.
+// extra = T: rows R + t of x_perm are copies of the tokens in order (the
+// shared expert's rows when it runs as the last group of the routed GEMMs).
 __global__ void permute_gather_kernel(const uint4* __restrict__ x,
                                       const int32_t* __restrict__ sorted_rows, int R, int k, int T,
                                       int vec_per_row, uint4* __restrict__ x_perm,
                                       const float* __restrict__ tok_scale,
-                                      float* __restrict__ row_scale, int32_t* err) {
+                                      float* __restrict__ row_scale, int32_t* err, int extra) {
   pdl_wait();
   const int lane = threadIdx.x & 31;
   const long long wstride = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
   for (long long p = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
-       p < R; p += wstride) {
-    const int r = sorted_rows[p];
+       p < R + extra; p += wstride) {
+    const int r = p < R ? sorted_rows[p] : static_cast<int>((p - R) * k);
     const int t = r / k;
     uint4* dst = x_perm + p * vec_per_row;
     if (r < 0 || t >= T) {
@@ -566,11 +570,13 @@ __global__ void permute_gather_kernel(const uint4* __restrict__ x,
 // times).
 constexpr int kScatterSlice = 256;
 
+// extra = T: each token's row is also written to R + t (the shared expert's
+// rows when it runs as the last group of the routed GEMMs).
 __global__ void permute_scatter_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ dest,
                                        const int32_t* __restrict__ nvalid_ptr, int R, int k, int T,
                                        int vec_per_row, uint4* __restrict__ x_perm,
                                        const float* __restrict__ tok_scale,
-                                       float* __restrict__ row_scale, int32_t* err) {
+                                       float* __restrict__ row_scale, int32_t* err, int extra) {
   pdl_wait();
   const int lane = threadIdx.x & 31;
   const long long wid = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -585,19 +591,22 @@ __global__ void permute_scatter_kernel(const uint4* __restrict__ x, const int32_
       const int p = dest[t * k + lane];
       if (p >= R) atomicOr(err, MOE_DEV_BAD_DEST);
       my_p = (p >= 0 && p < R) ? p : -1;  // -1: a row whose id was invalid
-      if (sl == 0 && row_scale && my_p >= 0) row_scale[my_p] = tok_scale[t];
+    } else if (lane == k && extra > 0) {
+      my_p = static_cast<int>(R + t);  // the shared expert's copy
     }
-    int pj[16];
+    if (sl == 0 && row_scale && my_p >= 0) row_scale[my_p] = tok_scale[t];
+    const int kk = k + (extra > 0 ? 1 : 0);  // destinations of this token
+    int pj[17];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) pj[j] = __shfl_sync(FULL, my_p, j);
+    for (int j = 0; j < 17; ++j) pj[j] = __shfl_sync(FULL, my_p, j);
     const uint4* src = x + t * vec_per_row;
     const int v1 = min(vec_per_row, (sl + 1) * kScatterSlice);
     int v = sl * kScatterSlice + lane;
     for (; v + 96 < v1; v += 128) {
       const uint4 a = src[v], b = src[v + 32], c = src[v + 64], d = src[v + 96];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        if (j < k && pj[j] >= 0) {
+      for (int j = 0; j < 17; ++j) {
+        if (j < kk && pj[j] >= 0) {
           uint4* dst = x_perm + static_cast<long long>(pj[j]) * vec_per_row;
           dst[v] = a;
           dst[v + 32] = b;
@@ -609,8 +618,8 @@ __global__ void permute_scatter_kernel(const uint4* __restrict__ x, const int32_
     for (; v < v1; v += 32) {
       const uint4 a = src[v];
 #pragma unroll
-      for (int j = 0; j < 16; ++j)
-        if (j < k && pj[j] >= 0) x_perm[static_cast<long long>(pj[j]) * vec_per_row + v] = a;
+      for (int j = 0; j < 17; ++j)
+        if (j < kk && pj[j] >= 0) x_perm[static_cast<long long>(pj[j]) * vec_per_row + v] = a;
     }
   }
   // rows past the last valid one (ids that were out of range)
@@ -1188,7 +1197,7 @@ cudaError_t launch_route_permute_small(const int32_t* ids, int R, int E, int k, 
                                        int32_t* counts, int32_t* offsets, int32_t* sorted_rows,
                                        int32_t* dest, const void* x, size_t row_bytes,
                                        void* x_perm, const float* tok_scale, float* row_scale,
-                                       int32_t* err, cudaStream_t s) {
+                                       int32_t* err, cudaStream_t s, int extra_rows) {
   if (R <= 0 || !small_route(R, E)) return cudaErrorInvalidValue;
   const size_t smem = (2 * static_cast<size_t>(R) + 33 * static_cast<size_t>(E) + 1) * sizeof(int32_t);
   static bool attr_done[64] = {false};
@@ -1202,30 +1211,31 @@ cudaError_t launch_route_permute_small(const int32_t* ids, int R, int E, int k, 
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_done[dev] = true;
   }
-  const int blocks = x ? blocks_for(R, 32, device_sm_count()) : 1;
+  const int blocks = x ? blocks_for(R + (x ? extra_rows : 0), 32, device_sm_count()) : 1;
   MOE_LAUNCH(route_permute_small_kernel, blocks, kSmallRouteThreads, smem, s, ids, R, E, k, T,
              counts, offsets, sorted_rows, dest, static_cast<const uint4*>(x),
              static_cast<int>(row_bytes / 16), static_cast<uint4*>(x_perm), tok_scale, row_scale,
-             err);
+             err, x ? extra_rows : 0);
   return cudaGetLastError();
 }
 
 cudaError_t launch_permute_gather(const void* x, const int32_t* sorted_rows, int R, int k, int T,
                                   size_t row_bytes, void* x_perm, int32_t* err, cudaStream_t s,
-                                  const float* tok_scale, float* row_scale) {
+                                  const float* tok_scale, float* row_scale, int extra_rows) {
   if (R <= 0) return cudaSuccess;
   const int vec = static_cast<int>(row_bytes / 16);
   const int threads = 256;
-  const int blocks = blocks_for(R, threads / 32, device_sm_count() * 16);
+  const int blocks = blocks_for(R + extra_rows, threads / 32, device_sm_count() * 16);
   MOE_LAUNCH(permute_gather_kernel, blocks, threads, 0, s, static_cast<const uint4*>(x),
-             sorted_rows, R, k, T, vec, static_cast<uint4*>(x_perm), tok_scale, row_scale, err);
+             sorted_rows, R, k, T, vec, static_cast<uint4*>(x_perm), tok_scale, row_scale, err,
+             extra_rows);
   return cudaGetLastError();
 }
 
 cudaError_t launch_permute_scatter(const void* x, const int32_t* dest, const int32_t* nvalid,
                                    int R, int k, int T, size_t row_bytes, void* x_perm,
                                    int32_t* err, cudaStream_t s, const float* tok_scale,
-                                   float* row_scale) {
+                                   float* row_scale, int extra_rows) {
   if (R <= 0) return cudaSuccess;
   if (k > 16) return cudaErrorInvalidValue;
   const int vec = static_cast<int>(row_bytes / 16);
@@ -1233,7 +1243,8 @@ cudaError_t launch_permute_scatter(const void* x, const int32_t* dest, const int
   const long long items = static_cast<long long>(T) * ((vec + kScatterSlice - 1) / kScatterSlice);
   const int blocks = blocks_for(items, threads / 32, device_sm_count() * 16);
   MOE_LAUNCH(permute_scatter_kernel, blocks, threads, 0, s, static_cast<const uint4*>(x), dest,
-             nvalid, R, k, T, vec, static_cast<uint4*>(x_perm), tok_scale, row_scale, err);
+             nvalid, R, k, T, vec, static_cast<uint4*>(x_perm), tok_scale, row_scale, err,
+             extra_rows);
   return cudaGetLastError();
 }
 

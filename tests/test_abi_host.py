@@ -137,6 +137,8 @@ def test_set_option_values():
         (moe.MOE_OPT_FUSED_COMBINE, 0, 0),
         (moe.MOE_OPT_TILE_ORDER, 3, 1),
         (moe.MOE_OPT_TILE_ORDER, 0, 0),
+        (moe.MOE_OPT_SHARED_IN_GEMM, 4, 1),
+        (moe.MOE_OPT_SHARED_IN_GEMM, 0, 0),
     ]
     for opt, value, stored in cases:
         old = moe.moe_set_option(opt, value)
@@ -144,17 +146,21 @@ def test_set_option_values():
 
 
 def test_fp8_nk_layout_host_logic(lib):
-    """MOE_FP8_E4M3_NK: accepted with bf16 activations, the same workspace and
-    launch count as the [.., K, N] fp8 layout (two-term e4m3 rows take the
-    fp16 rows' bytes), rejected with fp32 activations or widths not a
-    multiple of 16; moe_pack_weights_nk validates before enqueueing anything."""
+    """MOE_FP8_E4M3_NK: accepted with bf16 activations, the same launch count
+    as the [.., K, N] fp8 layout, and the same workspace but for the T extra
+    rows its shared expert may take as the last group of the routed GEMMs
+    (two-term e4m3 rows take the fp16 rows' bytes); rejected with fp32
+    activations or widths not a multiple of 16; moe_pack_weights_nk
+    validates before enqueueing anything."""
     for name in ("ling_prefill", "ling_decode"):
         shape = workloads.CONFIGS[name]
         kn, nk = moe.config_from_shape(shape), moe.config_from_shape(shape, "nk")
         assert nk.w_dtype == moe.MOE_FP8_E4M3_NK
-        assert moe.moe_workspace_size(nk) == moe.moe_workspace_size(kn) > 0
+        T, D, I = shape.T, shape.D, shape.I
+        extra = T * D * 2 + T * I * 4 + T * D * 4 + T * 4 + T * I * 2 + T * 4  # x_perm, h, y, scales, h rows
+        assert 0 < moe.moe_workspace_size(nk) - moe.moe_workspace_size(kn) <= extra + 8 * 256
         assert moe.moe_layer_launch_count(nk) == moe.moe_layer_launch_count(kn)
-        for i in range(len(moe.WS_SLOTS)):
+        for i in range(8):  # the regions before the permuted rows sit at the same offsets
             assert moe.moe_workspace_offset(nk, i) == moe.moe_workspace_offset(kn, i)
     assert moe.moe_workspace_size(moe.make_config(64, 264, 8, 2, 128, w_dtype="fp8_e4m3_nk")) == 0
     good = 1 << 20

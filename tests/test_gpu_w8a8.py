@@ -169,7 +169,14 @@ def check_layer_a8(shape, seed=0):
     flips = np.zeros(T, dtype=bool)
     flips[sorted_rows[flip_rows] // k] = True
     if shape.I_shared:
-        hs_gpu = view("h_shared", (T, shape.I_shared), torch.bfloat16)
+        # the shared expert's h: its own region, or rows R .. R+T-1 of h when it
+        # ran as the last group of the routed GEMMs
+        in_gemm = moe.moe_set_option(moe.MOE_OPT_SHARED_IN_GEMM, 0)
+        moe.moe_set_option(moe.MOE_OPT_SHARED_IN_GEMM, in_gemm)
+        if in_gemm and shape.I_shared == shape.I:
+            hs_gpu = view("h", (R + T, shape.I), torch.bfloat16)[R:]
+        else:
+            hs_gpu = view("h_shared", (T, shape.I_shared), torch.bfloat16)
         xs = oracle.dequantize_rows(q_o, s_o)
         gu = oracle.scaled_projection(xs, oracle.to_f64(cinp["W13s"]), oracle.to_f64(cinp["s13s"]))
         Is = shape.I_shared
@@ -264,7 +271,11 @@ def test_full_size_w8a8(name):
     rows_gpu = dest[(tokens[:, None] * k + np.arange(k)[None, :]).ravel()]
     rows_ref = ref["dest"][np.arange(len(tokens) * k)]
     flips = amax_flips(h_gpu[torch.from_numpy(rows_gpu)], ref["h"][rows_ref]).reshape(-1, k).any(axis=1)
-    hs_gpu = view("h_shared", (T, shape.I_shared), torch.bfloat16)[torch.from_numpy(tokens)]
+    in_gemm = moe.moe_set_option(moe.MOE_OPT_SHARED_IN_GEMM, 0)
+    moe.moe_set_option(moe.MOE_OPT_SHARED_IN_GEMM, in_gemm)
+    hs_all = (view("h", (R + T, shape.I), torch.bfloat16)[R:] if in_gemm and shape.I_shared == shape.I
+              else view("h_shared", (T, shape.I_shared), torch.bfloat16))
+    hs_gpu = hs_all[torch.from_numpy(tokens)]
     xs = oracle.dequantize_rows(*oracle.quantize_rows_e4m3(oracle.to_f64(sub["x"])))
     gu = oracle.scaled_projection(xs, oracle.to_f64(sub["W13s"]), oracle.to_f64(sub["s13s"]))
     Is = shape.I_shared
