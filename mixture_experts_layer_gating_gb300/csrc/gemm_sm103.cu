@@ -127,6 +127,7 @@ constexpr size_t smem_bytes() {
   return 1024 + StageCfg<SPLIT, FP8, PAIR>::kStages * StageCfg<SPLIT, FP8, PAIR>::kStageBytes +
          sizeof(Ctrl) + EPI_STAGE_BYTES;
 }
+static_assert(EPI_STAGE_BYTES >= 4 * 4096 + 1023, "TMA store staging fits the epilogue staging area");
 static_assert(smem_bytes<false, false, false>() <= 227 * 1024, "shared memory budget");
 static_assert(smem_bytes<true, false, false>() <= 227 * 1024, "shared memory budget");
 static_assert(smem_bytes<false, true, false>() <= 227 * 1024, "shared memory budget");
@@ -170,6 +171,9 @@ struct KParams {
   // (tmap_b2) with per-column scales sh_b_scale
   int sh_rows;
   const float* sh_b_scale;
+  // store pass (one plane, no bias): full 32-row warp chunks leave through
+  // TMA bulk-tensor stores (tmap_out: the [M, N] output, 128-byte rows per box)
+  int tma_out;
 };
 
 // Fused combine: the token and routing weight of permuted output row `row`.
@@ -424,7 +428,8 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
                         const __grid_constant__ CUtensorMap tmap_a_tail,
                         const __grid_constant__ CUtensorMap tmap_a_lo_tail,
                         const __grid_constant__ CUtensorMap tmap_b2,
-                        const __grid_constant__ CUtensorMap tmap_b2_tail, const KParams p) {
+                        const __grid_constant__ CUtensorMap tmap_b2_tail,
+                        const __grid_constant__ CUtensorMap tmap_out, const KParams p) {
   pdl_wait();
   static_assert(!Q8 || !FP8, "e4m3 rows meet K-contiguous e4m3 weights, not expanded ones");
   using Cfg = StageCfg<SPLIT, FP8, PAIR>;
@@ -444,6 +449,10 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
   auto stage_raw = [&](int st) { return base + st * STAGE_BYTES + A_BYTES + Cfg::kBBytes; };
   Ctrl* ctrl = reinterpret_cast<Ctrl*>(base + STAGES * STAGE_BYTES);
   float* epi_stage = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ctrl) + sizeof(Ctrl));
+  // the same bytes as 1024-byte-aligned 4 KB staging tiles of the TMA stores,
+  // one per epilogue warp (16 KB + alignment within EPI_STAGE_BYTES)
+  uint8_t* tma_stage = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(epi_stage) + 1023) & ~static_cast<uintptr_t>(1023));
   volatile int* abort_flag = &ctrl->abort;
 
   const int warp = threadIdx.x >> 5;
@@ -486,6 +495,7 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
       tma_prefetch_desc(&tmap_b2);
       if (PAIR) tma_prefetch_desc(&tmap_b2_tail);
     }
+    if (p.tma_out) tma_prefetch_desc(&tmap_out);
   }
   if (warp == 1) {
     if (PAIR) {  // collective over one warp of each CTA of the pair
@@ -1230,19 +1240,80 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
             }
           }
         } else {
+        // TMA stores (p.tma_out): a warp holding 32 valid rows writes its chunk
+        // of 128-byte rows (32 fp32 or 64 bf16 columns) into its 4 KB staging
+        // tile with the 128-byte swizzle (16-byte piece q of row r at q ^ (r & 7):
+        // conflict-free) and one lane stores the box; a warp with fewer rows (a
+        // group's last tile) takes the masked row stores below
+        constexpr int CW = (FP8 || Q8) ? 64 : 32;  // output columns per box
+        const bool full_warp = p.tma_out && wrows == 32;
+        uint8_t* tst = tma_stage + (warp - 2) * 4096;
 #pragma unroll 1
-        for (int c = 0; c < p.bn; c += 32) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(taddr + c, r);
+        for (int c0 = 0; c0 < p.bn; c0 += CW) {
+          if (c0 + CW > p.bn) break;  // bn is a multiple of 64
+          uint32_t rv[CW];
+          tmem_ld_32x32b_x32(taddr + c0, *reinterpret_cast<uint32_t(*)[32]>(&rv[0]));
+          if (CW == 64) tmem_ld_32x32b_x32(taddr + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&rv[CW - 32]));
           tc_wait_ld();
+          if (ti.n0 + c0 >= p.N) continue;  // warp-uniform
+          if (p.tma_out) {
+            if (lane == 0) bulk_wait_read0();  // the last store has read the staging tile
+            __syncwarp();
+          }
+          if (full_warp) {
+            // lane l: the column scales of columns n0 + c0 + l (+ 32)
+            float csl[CW / 32];
+#pragma unroll
+            for (int h = 0; h < CW / 32; ++h) {
+              const int cc = ti.n0 + c0 + 32 * h + lane;
+              csl[h] = (sc && cc < p.N) ? sc[cc] : 1.0f;
+            }
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {  // 16-byte piece q of this lane's row
+              uint4 w;
+              uint32_t* wv = reinterpret_cast<uint32_t*>(&w);
+              if (CW == 32) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  const int j = 4 * q + i;
+                  wv[i] = __float_as_uint(__uint_as_float(rv[j]) * rs * __shfl_sync(0xffffffffu, csl[0], j));
+                }
+              } else {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  const int j = 8 * q + 2 * i;
+                  const float a = __uint_as_float(rv[j]) * rs *
+                                  __shfl_sync(0xffffffffu, csl[j >> 5], j & 31);
+                  const float b = __uint_as_float(rv[j + 1]) * rs *
+                                  __shfl_sync(0xffffffffu, csl[(j + 1) >> 5], (j + 1) & 31);
+                  wv[i] = pack_bf16x2(a, b);
+                }
+              }
+              *reinterpret_cast<uint4*>(tst + lane * 128 + ((q ^ (lane & 7)) << 4)) = w;
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmap_out, tst, ti.n0 + c0, wrow0);
+              bulk_commit();
+            }
+            continue;
+          }
+        // masked row stores: each 32-column piece staged (fp32) in this warp's
+        // own 4 KB tile with the same swizzle, then written out as 4 rows x 128
+        // bytes per warp store (the tile is this warp's alone, so no other
+        // warp's bulk store can be reading it)
+#pragma unroll
+        for (int c1 = 0; c1 < CW; c1 += 32) {
+          const int c = c0 + c1;
           const int col = ti.n0 + c;
           if (col >= p.N) continue;  // warp-uniform
           __syncwarp();
 #pragma unroll
           for (int j = 0; j < 8; ++j)
-            *reinterpret_cast<float4*>(stg + lane * EPI_STAGE_LD + 4 * j) =
-                make_float4(__uint_as_float(r[4 * j]) * rs, __uint_as_float(r[4 * j + 1]) * rs,
-                            __uint_as_float(r[4 * j + 2]) * rs, __uint_as_float(r[4 * j + 3]) * rs);
+            *reinterpret_cast<float4*>(tst + lane * 128 + ((j ^ (lane & 7)) << 4)) = make_float4(
+                __uint_as_float(rv[c1 + 4 * j]) * rs, __uint_as_float(rv[c1 + 4 * j + 1]) * rs,
+                __uint_as_float(rv[c1 + 4 * j + 2]) * rs, __uint_as_float(rv[c1 + 4 * j + 3]) * rs);
           __syncwarp();
           const int cl = col + c4;
           float cs[4] = {1.f, 1.f, 1.f, 1.f}, cb[4] = {0.f, 0.f, 0.f, 0.f};
@@ -1255,7 +1326,7 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
           }
 #pragma unroll 2
           for (int rr = sub; rr < wrows; rr += 4) {
-            const float4 v = *reinterpret_cast<const float4*>(stg + rr * EPI_STAGE_LD + c4);
+            const float4 v = *reinterpret_cast<const float4*>(tst + rr * 128 + (((lane & 7) ^ (rr & 7)) << 4));
             OutT* orow = out + static_cast<size_t>(wrow0 + rr) * p.N;
             const float o0 = v.x * cs[0] + cb[0], o1 = v.y * cs[1] + cb[1];
             const float o2 = v.z * cs[2] + cb[2], o3 = v.w * cs[3] + cb[3];
@@ -1272,6 +1343,7 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
             }
           }
         }
+        }
         }  // not the fused combine
       }
       tc_fence_before_sync();
@@ -1282,6 +1354,7 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
         acc_phase ^= 1u;
       }
     }
+    if (p.tma_out && lane == 0) bulk_wait0();  // this lane's output stores are done
     __syncwarp();
   }
 
@@ -1762,11 +1835,32 @@ bool encode_tmap(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims
   return r == CUDA_SUCCESS;
 }
 
+// The store pass's output as a TMA store target: [M, N] rows of fp32 (or
+// bf16 when out_bf16), 32 rows x 128 bytes per box, 128-byte swizzle.  Only
+// for one-plane outputs without bias (kp.tma_out); otherwise kp.tma_out stays
+// 0 and the map is unused.
+constexpr bool kTmaStoreEpilogue = true;
+void make_out_map(const GroupedGemmArgs& a, KParams& kp, bool out_bf16, CUtensorMap& tout) {
+  kp.tma_out = 0;
+  if (!kTmaStoreEpilogue || a.epilogue != kEpiStoreF32 || kp.ksplit != 1 || a.bias || !a.out ||
+      (reinterpret_cast<uintptr_t>(a.out) & 15u))
+    return;
+  const uint64_t eb = out_bf16 ? 2 : 4;
+  const uint64_t dims[2] = {static_cast<uint64_t>(a.N), static_cast<uint64_t>(a.M)};
+  const uint64_t strides[1] = {static_cast<uint64_t>(a.N) * eb};
+  if (strides[0] % 16) return;
+  const uint32_t box[2] = {out_bf16 ? 64u : 32u, 32u};
+  if (encode_tmap(&tout, a.out, 2, dims, strides, box,
+                  out_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32))
+    kp.tma_out = 1;
+}
+
 template <int EPI, bool SPLIT, bool FP8, bool PAIR, bool Q8 = false>
 cudaError_t launch_epi(const CUtensorMap& ta, const CUtensorMap& ta_lo, const CUtensorMap& tb,
                        const CUtensorMap& tb_tail, const CUtensorMap& ta_tail,
                        const CUtensorMap& ta_lo_tail, const CUtensorMap& tb2,
-                       const CUtensorMap& tb2_tail, const KParams& kp, long long max_tiles,
+                       const CUtensorMap& tb2_tail, const CUtensorMap& tout, const KParams& kp,
+                       long long max_tiles,
                        cudaStream_t s) {
   constexpr size_t smem = smem_bytes<SPLIT, FP8, PAIR>();
   constexpr int threads = StageCfg<SPLIT, FP8, PAIR>::kThreads;
@@ -1785,7 +1879,7 @@ cudaError_t launch_epi(const CUtensorMap& ta, const CUtensorMap& ta_lo, const CU
     const int grid =
         static_cast<int>(std::max<long long>(1, std::min<long long>(device_sm_count(), max_tiles)));
     return launch_kernel(kern, dim3(grid), dim3(threads), smem, s, ta, ta_lo, tb, tb_tail, ta_tail,
-                         ta_lo_tail, tb2, tb2_tail, kp);
+                         ta_lo_tail, tb2, tb2_tail, tout, kp);
   }
   // one persistent 2-CTA cluster per SM pair that can hold one
   cudaLaunchConfig_t cfg = {};
@@ -1815,7 +1909,7 @@ cudaError_t launch_epi(const CUtensorMap& ta, const CUtensorMap& ta_lo, const CU
   cfg.gridDim = dim3(2 * nclu, 1, 1);
   cfg.numAttrs = 2;
   cudaError_t e =
-      cudaLaunchKernelEx(&cfg, kern, ta, ta_lo, tb, tb_tail, ta_tail, ta_lo_tail, tb2, tb2_tail, kp);
+      cudaLaunchKernelEx(&cfg, kern, ta, ta_lo, tb, tb_tail, ta_tail, ta_lo_tail, tb2, tb2_tail, tout, kp);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -2093,9 +2187,11 @@ cudaError_t launch_grouped_gemm_q8(const GroupedGemmArgs& a, cudaStream_t s) {
   const int tile_m = pair ? 2 * BM : BM;
   const long long max_tiles = (static_cast<long long>((a.M + tile_m - 1) / tile_m) + a.G) *
                               static_cast<long long>(kp.n_tiles);
+  CUtensorMap tout = ta;
+  make_out_map(a, kp, /*out_bf16=*/true, tout);
 #define MOE_LAUNCH_Q8(E_, S_, P_) \
-  launch_epi<E_, S_, false, P_, true>(ta, ta_lo, tb, tb_tail, ta_tail, ta_lo_tail, tb2, tb2_tail, kp, \
-                                      max_tiles, s)
+  launch_epi<E_, S_, false, P_, true>(ta, ta_lo, tb, tb_tail, ta_tail, ta_lo_tail, tb2, tb2_tail, tout, \
+                                      kp, max_tiles, s)
   if (one) {
     if (a.epilogue == kEpiGateUpAct)
       return pair ? MOE_LAUNCH_Q8(kEpiGateUpAct, false, true) : MOE_LAUNCH_Q8(kEpiGateUpAct, false, false);
@@ -2322,12 +2418,14 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
   const int tile_m = pair ? 2 * BM : BM;
   const long long max_tiles = (static_cast<long long>((a.M + tile_m - 1) / tile_m) + a.G) *
                               static_cast<long long>(kp.n_tiles) * kp.ksplit;
+  CUtensorMap tout = ta;
+  make_out_map(a, kp, /*out_bf16=*/a.b_fp8 != 0, tout);
   // (pair is never set for fp8 weights: their kernels exist on 1-CTA tiles only)
 #define MOE_LAUNCH(E_, S_, F_)                                                               \
   ((pair && !(F_)) ? launch_epi<E_, S_, F_, !(F_)>(ta, ta_lo, tb, tb_tail, ta_tail, ta_lo_tail, \
-                                                  tb2, tb2_tail, kp, max_tiles, s)            \
+                                                  tb2, tb2_tail, tout, kp, max_tiles, s)      \
                    : launch_epi<E_, S_, F_, false>(ta, ta_lo, tb, tb_tail, ta_tail, ta_lo_tail, \
-                                                   tb2, tb2_tail, kp, max_tiles, s))
+                                                   tb2, tb2_tail, tout, kp, max_tiles, s))
   if (a.epilogue == kEpiGateUpAct) {
     if (a.A_lo) return cudaErrorInvalidValue;
     return a.b_fp8 ? MOE_LAUNCH(kEpiGateUpAct, false, true) : MOE_LAUNCH(kEpiGateUpAct, false, false);
