@@ -551,7 +551,8 @@ def measure(args, world, rank, local, shape, primary: bool, layout: str):
     else:
         roof = {"bound": "hbm", "achieved": nbytes / t_s / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    tr = profiled_traffic(dom, args.workload if primary else shape_key(shape))
+    # the committed ncu summary of this kernel on this workload (W8A8: its own)
+    tr = profiled_traffic(dom, (args.workload if primary else shape_key(shape)) + ("_w8a8" if a8 else ""))
     roof.update({"traffic": tr, "kernel": dom, "kernel_us": kernels_us[dom],
                  "algorithmic_flops": flops, "algorithmic_bytes": nbytes,
                  "tensor_frac": (flops / t_s / 1e12) / kind_peak,
