@@ -231,6 +231,19 @@ def router_planes(T: int, E: int, D: int) -> int:
     return (kb + kbs - 1) // kbs
 
 
+def fused_router(T: int, E: int, D: int, k: int, act_dtype: str) -> bool:
+    """Whether moe_layer runs the router projection and the top-k softmax as
+    one kernel: the library's rule (MOE_OPT_FUSED_ROUTING on, its default),
+    restated -- bf16 activations, 64 <= E <= 512, E and D multiples of 8,
+    k <= 32, and not a batch the CUDA-core projection takes (at most 64
+    tokens and 2^25 multiply-adds, slices of D of at most 1024)."""
+    if act_dtype != "bf16" or not 64 <= E <= 512 or E % 8 or D % 8 or k > 32:
+        return False
+    S = router_planes(T, E, D)
+    small = T <= 64 and E % 2 == 0 and T * D * E <= 2 ** 25 and (D + S - 1) // S <= 1024
+    return not small
+
+
 def memory_kernel_bytes(shape, name: str, rows_form_bytes: int, nk: bool = False):
     """Algorithmic bytes of one launch of a memory-bound kernel of the layer
     (every tensor it must read or write, once), or None for the GEMMs.
@@ -247,8 +260,12 @@ def memory_kernel_bytes(shape, name: str, rows_form_bytes: int, nk: bool = False
     nseg_hist = E * 4 * max(1, (R + 1023) // 1024)
     table = {
         "topk_softmax": S * T * E * 4 + (E * 4 if bias else 0) + (T * E * 4 if (S > 1 or bias) else 0) + 8 * T * k,
+        # x and W_g read once, logits written, ids and weights written
+        "router_topk": T * D * ab + D * E * ab + (E * 4 if bias else 0) + T * E * 4 + 8 * T * k,
         "route_hist": 4 * R + nseg_hist,
         "route_scan_scatter": 4 * R + nseg_hist + 8 * E + 8 * R,
+        # ids read twice (histogram, scatter), sorted_rows and dest written
+        "route_sort": 8 * R + 8 * R + 8 * E,
         "route_permute": 4 * R + T * D * gathered + R * D * gathered + 8 * R + 8 * E,
         "permute_gather": T * D * gathered + 4 * R + R * D * gathered,
         "finalize": R * D * yb + 4 * R + 4 * T * k + (T * D * yb if Is else 0) + T * D * ab,
@@ -329,6 +346,8 @@ def set_options(moe, args):
         moe.moe_set_option(moe.MOE_OPT_SHARED_STREAM, 0)
     if args.fused_combine:
         moe.moe_set_option(moe.MOE_OPT_FUSED_COMBINE, 1)
+    if getattr(args, "split_routing", False):
+        moe.moe_set_option(moe.MOE_OPT_FUSED_ROUTING, 0)
     if args.lpt:
         moe.moe_set_option(moe.MOE_OPT_TILE_ORDER, 1)
     if args.shared_in_gemm:
@@ -346,15 +365,18 @@ def pct(v, q):
     return v[lo] + (v[hi] - v[lo]) * (pos - lo)
 
 
-def kernel_names(shape, nk, gather_a, a8=False, fused=False, shared_in_gemm=False):
+def kernel_names(shape, nk, gather_a, a8=False, fused=False, shared_in_gemm=False, fused_routing=True):
     """Names of the kernels one moe_layer call launches, in launch order."""
     fp8 = shape.w_dtype == "fp8_e4m3"
     rows = "e4m3" if a8 else "e4m3x2" if nk else "fp16"  # the A-row form of fp8 layers
-    names = ([f"x_to_{rows}"] if fp8 else []) + ["router_gemm", "topk_softmax"]
+    router = ["router_topk"] if fused_routing and fused_router(shape.T, shape.E, shape.D, shape.k,
+                                                                shape.act_dtype) \
+        else ["router_gemm", "topk_softmax"]
+    names = ([f"x_to_{rows}"] if fp8 else []) + router
     if shape.R <= 8192:  # small batches: init_routing + gather in one kernel
         names += ["route_permute"]
     else:
-        names += ["route_hist", "route_scan_scatter"]
+        names += ["route_sort"] if fused_routing else ["route_hist", "route_scan_scatter"]
         names += ["permute_gather"] if (shape.act_dtype == "f32" or not gather_a) else []
     names += ["w13_gate_up"]
     names += [f"h_to_{rows}"] if fp8 else []
@@ -438,7 +460,7 @@ def measure(args, world, rank, local, shape, primary: bool, layout: str):
     fused = args.fused_combine and shape.act_dtype == "bf16" and (nk or not fp8)
     in_gemm = (args.shared_in_gemm and shape.I_shared == shape.I and shape.I_shared > 0 and
                shape.act_dtype == "bf16" and (nk or not fp8) and not args.gather_a)
-    names = kernel_names(shape, nk, args.gather_a, a8, fused, in_gemm)
+    names = kernel_names(shape, nk, args.gather_a, a8, fused, in_gemm, not args.split_routing)
     assert len(names) == L
     per = [[] for _ in range(L)]
     for _ in range(args.steps):
@@ -684,6 +706,9 @@ def main():
                          "nk_a8: nk weights with W8A8 activations (opt-in, changes the result)")
     ap.add_argument("--no-pdl", action="store_true",
                     help="plain stream order instead of programmatic dependent launch (MOE_OPT_PDL 0)")
+    ap.add_argument("--split-routing", action="store_true",
+                    help="router projection and top-k, histogram and scatter as separate launches "
+                         "(MOE_OPT_FUSED_ROUTING 0)")
     ap.add_argument("--fused-combine", action="store_true",
                     help="routed down pass adds weighted rows into [T, D] fp32 sums "
                          "(MOE_OPT_FUSED_COMBINE 1; the combine's summation order then varies)")

@@ -379,6 +379,23 @@ int moe_layer_launch_count(const moe_config_t* cfg);
  *   layers, and 0 (default), run the shared expert in its own launches (on
  *   the side stream, MOE_OPT_SHARED_STREAM).  Same results. */
 #define MOE_OPT_SHARED_IN_GEMM 9
+/*   MOE_OPT_FUSED_ROUTING: 1 (default) = the routing chain in fewer
+ *   launches ("CANN/cann-recipes-infer：Qwen3-MoE优化", section "GMM使能和
+ *   Routing优化": fused gate + gating_top_k_softmax, fused init_routing):
+ *   (a) for more than 64 tokens of bf16 activations (64 <= E <= 512), the
+ *   router projection and the top-k softmax are one kernel: a cluster of up
+ *   to 8 CTAs per 128 tokens splits the fp32 sum over D into consecutive
+ *   slices on the tensor core and hands the partial rows through distributed
+ *   shared memory to the CTA that adds them in slice order and takes the
+ *   top-k; (b) for more than 8192 expanded rows, the histogram, scan and
+ *   stable scatter of init_routing are one cluster of 8 CTAs that exchange
+ *   their expert histograms through distributed shared memory.
+ *   0 = a grouped-GEMM launch writing split-K planes, then the top-k kernel;
+ *   a histogram kernel, then a scan + scatter kernel.  The logits may differ
+ *   in the last bits between the two (another split of the fp32 sum over D);
+ *   ids and weights follow from each one's own logits by the same rule, and
+ *   the permutation is the same. */
+#define MOE_OPT_FUSED_ROUTING 10
 int moe_set_option(int option, int value);
 
 /* Per-kernel timing hook (process-wide, off by default).  `events` holds

@@ -73,6 +73,7 @@ MOE_OPT_SHARED_STREAM = 5
 MOE_OPT_FUSED_COMBINE = 6
 MOE_OPT_TILE_ORDER = 7
 MOE_OPT_SHARED_IN_GEMM = 9
+MOE_OPT_FUSED_ROUTING = 10
 
 
 def load_library(path: Optional[str] = None) -> ctypes.CDLL:

@@ -1798,7 +1798,10 @@ __global__ void __launch_bounds__(DecCfg<SPLIT, FP8>::kThreads, 1)
   }
 }
 
+}  // namespace
+
 // ------------------------------------------------------------------ host side
+namespace {
 PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -1812,11 +1815,11 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
   });
   return fn;
 }
+}  // namespace
 
 bool encode_tmap(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims,
-                 const uint64_t* strides_bytes, const uint32_t* box,
-                 CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                 CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
+                 const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapDataType dt,
+                 CUtensorMapSwizzle swz) {
   auto fn = get_encode_fn();
   if (!fn) return false;
   cuuint64_t gd[5];
@@ -1834,6 +1837,8 @@ bool encode_tmap(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
+
+namespace {
 
 // The store pass's output as a TMA store target: [M, N] rows of fp32 (or
 // bf16 when out_bf16), 32 rows x 128 bytes per box, 128-byte swizzle.  Only

@@ -18,6 +18,7 @@ int g_gather_a = 0;       // moe_set_option(MOE_OPT_GATHER_A, .)
 int g_shared_stream = 1;  // moe_set_option(MOE_OPT_SHARED_STREAM, .)
 int g_fused_combine = 0;  // moe_set_option(MOE_OPT_FUSED_COMBINE, .)
 int g_shared_in_gemm = 0;  // moe_set_option(MOE_OPT_SHARED_IN_GEMM, .)
+int g_fused_routing = 1;  // moe_set_option(MOE_OPT_FUSED_ROUTING, .)
 
 // The shared expert depends on x alone, so moe_layer runs it on a second
 // stream of the library's own (one per device, created on first use) that
@@ -236,6 +237,13 @@ int common_checks(const moe_config_t* cfg, void* ws, size_t ws_bytes) {
   return check_ws(cfg, ws, ws_bytes);
 }
 
+// The router projection and top-k as one kernel (MOE_OPT_FUSED_ROUTING): bf16
+// activations, batches the CUDA-core projection does not take.
+bool fused_router_on(const moe_config_t* c, int nsplit) {
+  return g_fused_routing && c->act_dtype == MOE_BF16 && !router_small_ok(c->T, c->E, c->D, nsplit) &&
+         router_topk_ok(c->T, c->E, c->D, c->k);
+}
+
 // ------------------------------------------------------------------ stages
 // `partials`: workspace room for the router's split-K planes (may be null when
 // the configuration does not split).
@@ -254,6 +262,11 @@ int do_route(const moe_config_t* c, const void* x, const void* Wg, const float* 
     } else {
       nsplit = partials ? router_k_split(c->T, c->E, c->D) : 1;
       float* dst = nsplit > 1 ? partials : logits;
+      if (fused_router_on(c, nsplit)) {
+        // projection and top-k in one launch
+        return cuda_status(launch_router_topk(x, Wg, bias, c->T, c->D, c->E, c->k, c->renormalize,
+                                              logits, ids, w, err, s));
+      }
       if (router_small_ok(c->T, c->E, c->D, nsplit)) {
         // a few tokens: a matrix-vector product per token on the CUDA cores,
         // into the same split planes
@@ -301,8 +314,14 @@ int do_permute(const moe_config_t* c, const int32_t* ids, const void* x, int32_t
         row_bytes, gather ? x_perm : nullptr, tok_scale,
         row_scale, err, s, extra_rows));
   }
-  cudaError_t e = launch_init_routing(ids, R, c->E, counts, offsets, sorted_rows, dest, seg_scratch,
-                                      err, s, g_trace_next >= 0 ? trace_mark : nullptr);
+  cudaError_t e;
+  if (g_fused_routing && R > 0 && c->E <= 512) {  // histogram, scan, scatter: one cluster launch
+    trace_mark(s);
+    e = launch_route_sort_cluster(ids, R, c->E, counts, offsets, sorted_rows, dest, err, s);
+  } else {
+    e = launch_init_routing(ids, R, c->E, counts, offsets, sorted_rows, dest, seg_scratch, err, s,
+                            g_trace_next >= 0 ? trace_mark : nullptr);
+  }
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   if (x && x_perm) {
     trace_mark(s);
@@ -752,6 +771,11 @@ int moe_set_option(int option, int value) {
       g_tile_order = value ? 1 : 0;
       return old;
     }
+    case MOE_OPT_FUSED_ROUTING: {
+      const int old = g_fused_routing;
+      g_fused_routing = value ? 1 : 0;
+      return old;
+    }
     case MOE_OPT_FUSED_COMBINE: {
       const int old = g_fused_combine;
       g_fused_combine = value ? 1 : 0;
@@ -770,8 +794,9 @@ int moe_set_trace_events(void* const* events, int n_events) {
 int moe_layer_launch_count(const moe_config_t* cfg) {
   if (!cfg_valid(cfg) || cfg->T == 0) return 0;
   int n = 0;
-  n += 1;  // router projection
-  n += 1;  // top-k softmax
+  // router projection and top-k softmax (one launch when fused)
+  const int nsplit = router_k_split(cfg->T, cfg->E, cfg->D);
+  n += fused_router_on(cfg, nsplit) ? 1 : 2;
   // the shared expert inside the routed GEMMs: no launches of its own
   const bool sep_shared = cfg->I_shared > 0 && !shared_in_gemm_on(cfg);
   if (is_fp8(cfg)) {
@@ -781,7 +806,7 @@ int moe_layer_launch_count(const moe_config_t* cfg) {
   if (small_route(static_cast<long long>(cfg->T) * cfg->k, cfg->E)) {
     n += 1;  // init_routing + permutation gather in one kernel
   } else {
-    n += 2;  // histogram, scan + stable scatter
+    n += g_fused_routing ? 1 : 2;  // histogram, scan + stable scatter (one cluster launch when fused)
     if (cfg->act_dtype == MOE_F32 || !g_gather_a) n += 1;  // permutation gather
   }
   n += 2;  // routed gate/up, down

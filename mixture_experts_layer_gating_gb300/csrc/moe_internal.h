@@ -53,6 +53,15 @@ cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t 
   return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
 }
 
+// TMA tensor map (gemm_sm103.cu) of a tensor with `rank` dimensions, innermost
+// first: dims, rank - 1 byte strides of the outer dimensions (multiples of 16),
+// box sizes; 128-byte swizzle by default.  Returns false when the driver's
+// encoder is unavailable or refuses the shape.
+bool encode_tmap(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims,
+                 const uint64_t* strides_bytes, const uint32_t* box,
+                 CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                 CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B);
+
 // Host-side validation shared by every entry point (moe_api.cu): the
 // configuration's shape and dtype limits, and whether its (act_dtype,
 // w_dtype, act) combination is built.
@@ -92,6 +101,17 @@ cudaError_t launch_topk_softmax(const float* partials, int nsplit, const float* 
                                 int T, int E, int k, int renorm, int32_t* ids, float* w,
                                 int32_t* err, cudaStream_t s);
 
+// Router projection fused with the top-k softmax (router_sm103.cu), bf16 x
+// and W_g: logits (+ bias) written, then ids / w.  router_topk_ok says which
+// shapes it takes (64 <= E <= 512, E and D multiples of 8, k <= 32);
+// router_topk_split gives its cluster shape: ck slices of D times nh expert
+// halves (a function of the shape alone).
+bool router_topk_ok(int T, int E, int D, int k);
+void router_topk_split(int T, int E, int D, int& ck, int& nh);
+cudaError_t launch_router_topk(const void* x, const void* Wg, const float* bias, int T, int D,
+                               int E, int k, int renorm, float* logits, int32_t* ids, float* w,
+                               int32_t* err, cudaStream_t s);
+
 // Split-K factor of the router projection (a pure function of the shape, so
 // the workspace size does not depend on the device).
 int router_k_split(int T, int E, int D);
@@ -106,6 +126,12 @@ cudaError_t launch_router_small(const void* x, const void* Wg, int T, int D, int
 cudaError_t launch_init_routing(const int32_t* ids, int R, int E, int32_t* counts, int32_t* offsets,
                                 int32_t* sorted_rows, int32_t* dest, int32_t* seg_scratch,
                                 int32_t* err, cudaStream_t s, void (*mark)(cudaStream_t) = nullptr);
+// The same stable counting sort as launch_init_routing in one launch: a
+// cluster of 8 CTAs that exchange their expert histograms through distributed
+// shared memory (no scratch).  E <= 512.
+cudaError_t launch_route_sort_cluster(const int32_t* ids, int R, int E, int32_t* counts,
+                                      int32_t* offsets, int32_t* sorted_rows, int32_t* dest,
+                                      int32_t* err, cudaStream_t s);
 // tok_scale / row_scale (optional): row_scale[p] = tok_scale[sorted_rows[p] / k].
 // extra_rows = T (all three permutation launchers): x_perm rows R + t are
 // also written, copies of token t (the shared expert's rows as the last group

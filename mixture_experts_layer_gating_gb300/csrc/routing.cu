@@ -1,6 +1,8 @@
 // Routing-side kernels of the MoE layer: the router projection of small
 // batches (CUDA cores), gating top-k softmax, init_routing (histogram,
-// exclusive scan, stable scatter), the permutation (gather or token-side
+// exclusive scan, stable scatter: two kernels, or one 8-CTA cluster that
+// exchanges its histograms through distributed shared memory, or one
+// launch with the gather for small batches), the permutation (gather or token-side
 // scatter), the fp8 layers' row forms (fp16 or two-term e4m3 rows with
 // power-of-two scales), the one-time fp8 weight transpose and the finalize
 // (weighted un-permute + shared-expert add).  All are memory- or
@@ -15,6 +17,8 @@
 #include <climits>
 
 #include "moe_internal.h"
+#include "sm103_ptx.cuh"
+#include "topk_warp.cuh"
 
 namespace moe {
 namespace {
@@ -69,81 +73,8 @@ __global__ void topk_softmax_kernel(const float* __restrict__ partials, int nspl
       }
     }
   }
-  bool nonfinite = false;
-#pragma unroll
-  for (int i = 0; i < EPL; ++i) {
-    const int e = lane + 32 * i;
-    float x = -INFINITY;
-    if (e < E) {
-      x = v[i];
-      if (bias) x += bias[e];
-      if (nsplit > 1 || bias) logits[t * E + e] = x;
-      if (!isfinite(x)) {
-        nonfinite = true;
-        x = -INFINITY;
-      }
-    }
-    v[i] = x;
-  }
-  if (__any_sync(FULL, nonfinite) && lane == 0) atomicOr(err, MOE_DEV_NONFINITE_LOGIT);
-
-  // Selection on order-preserving integer keys: key(a) > key(b) exactly when
-  // a > b as floats (-0 is first made +0, so equal values get equal keys);
-  // experts past E get key 0, below every finite or -inf logit.  Each round
-  // takes the largest key with one warp max-reduction and, among the lanes
-  // holding it, the lowest expert index with one min-reduction: the same
-  // order as (value descending, index ascending).
-  uint32_t key[EPL];
-#pragma unroll
-  for (int i = 0; i < EPL; ++i) {
-    const uint32_t u = __float_as_uint(v[i] + 0.0f);
-    key[i] = (lane + 32 * i < E) ? ((u & 0x80000000u) ? ~u : (u | 0x80000000u)) : 0u;
-  }
-  uint32_t taken = 0;
-  float my_v = -INFINITY;
-  int my_e = 0;
-  for (int j = 0; j < k; ++j) {
-    uint32_t bk = 0;  // this lane's best remaining key (the lower index among equal keys)
-    int bi = 0;
-#pragma unroll
-    for (int i = 0; i < EPL; ++i) {
-      if (!((taken >> i) & 1u) && key[i] > bk) {
-        bk = key[i];
-        bi = i;
-      }
-    }
-    const uint32_t wmax = __reduce_max_sync(FULL, bk);
-    const uint32_t be = __reduce_min_sync(FULL, bk == wmax ? static_cast<uint32_t>(lane + 32 * bi) : 0xFFFFFFFFu);
-    if (static_cast<int>(be & 31u) == lane) taken |= 1u << (be >> 5);
-    if (lane == j) {
-      my_v = __uint_as_float((wmax & 0x80000000u) ? (wmax & 0x7FFFFFFFu) : ~wmax);
-      my_e = static_cast<int>(be);
-    }
-  }
-  const float m = __shfl_sync(FULL, my_v, 0);
-  float z = 0.0f;
-  float denom;
-  if (m == -INFINITY) {  // every logit non-finite: uniform weights
-    z = lane < k ? 1.0f : 0.0f;
-    denom = static_cast<float>(k);
-  } else if (renorm) {
-    z = lane < k ? expf(my_v - m) : 0.0f;
-    denom = z;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) denom += __shfl_xor_sync(FULL, denom, off);
-  } else {
-    z = lane < k ? expf(my_v - m) : 0.0f;
-    float s = 0.0f;
-#pragma unroll
-    for (int i = 0; i < EPL; ++i) s += (lane + 32 * i < E) ? expf(v[i] - m) : 0.0f;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(FULL, s, off);
-    denom = s;
-  }
-  if (lane < k) {
-    ids[t * k + lane] = my_e;
-    w[t * k + lane] = z / denom;
-  }
+  warp_topk_softmax<EPL>(v, lane, E, k, renorm, bias, (nsplit > 1 || bias) ? logits + t * E : nullptr,
+                         ids + t * k, w + t * k, err);
 }
 
 // ------------------------------------------------------------------------
@@ -376,6 +307,156 @@ __global__ void __launch_bounds__(kScatterWarps * 32)
     if (valid && (peers & lt) == 0) my[e] += __popc(peers);
     __syncwarp();
   }
+}
+
+// ------------------------------------------------------------------------
+// init_routing in one launch for larger batches: one cluster of kSortCtas
+// CTAs.  CTA c takes the expanded rows [c R / n, (c + 1) R / n), each of its
+// warps a contiguous piece of them, and counts them per warp and expert in
+// shared memory; after a cluster barrier every CTA reads the others' expert
+// histograms through distributed shared memory and adds those of the CTAs
+// before it (its base position per expert) and of all of them (counts),
+// scans the counts over experts (offsets; CTA 0 publishes both) and scatters
+// its rows in order as route_scatter_kernel does.  The same stable counting
+// sort as route_hist_kernel + route_scatter_kernel, without their global
+// histogram round trip.  A CTA leaves only after every CTA has finished
+// reading the others' histograms (split cluster barrier).
+constexpr int kSortCtas = 8;
+constexpr int kSortWarps = 32;
+constexpr int kSortBatch = 8;  // ids per lane held in registers: 256 rows of a warp's piece
+
+__global__ void __launch_bounds__(kSortWarps * 32, 1)
+    route_sort_cluster_kernel(const int32_t* __restrict__ ids, int R, int E,
+                              int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                              int32_t* __restrict__ sorted_rows, int32_t* __restrict__ dest,
+                              int32_t* err) {
+  pdl_wait();
+  pdl_launch_dependents();
+  extern __shared__ int32_t sm[];
+  int32_t* wcnt = sm;                      // [kSortWarps][E]: per-warp counts, then starts
+  int32_t* cta_tot = sm + kSortWarps * E;  // [E]: this CTA's histogram (read by the others)
+  __shared__ int32_t warp_sum[kSortWarps];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int nthr = blockDim.x;
+  const int c = static_cast<int>(cluster_ctarank());
+  const int r0 = static_cast<int>(static_cast<long long>(c) * R / kSortCtas);
+  const int r1 = static_cast<int>(static_cast<long long>(c + 1) * R / kSortCtas);
+
+  // (a) per-warp counts of each warp's contiguous piece, then the CTA's
+  // histogram.  A warp reads its ids in batches of 32 x kSortBatch rows, all
+  // loads of a batch in flight together; a piece of at most one batch keeps
+  // its ids in registers for the scatter.
+  for (int i = threadIdx.x; i < kSortWarps * E; i += nthr) wcnt[i] = 0;
+  const int piece = (r1 - r0 + kSortWarps - 1) / kSortWarps;
+  const int w0 = min(r1, r0 + wid * piece), w1 = min(r1, w0 + piece);
+  int idv[kSortBatch];
+  auto load_batch = [&](int rb) {
+#pragma unroll
+    for (int j = 0; j < kSortBatch; ++j) {
+      const int r = rb + 32 * j + lane;
+      idv[j] = r < w1 ? __ldg(ids + r) : -1;
+    }
+  };
+  __syncthreads();
+  bool bad = false;
+  for (int rb = w0; rb < w1; rb += 32 * kSortBatch) {
+    load_batch(rb);
+#pragma unroll
+    for (int j = 0; j < kSortBatch; ++j) {
+      const int r = rb + 32 * j + lane;
+      if (r < w1) {
+        const int e = idv[j];
+        if (e >= 0 && e < E) atomicAdd(&wcnt[wid * E + e], 1);
+        else bad = true;
+      }
+    }
+  }
+  if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(err, MOE_DEV_BAD_EXPERT_ID);
+  for (int e = threadIdx.x; e < E; e += nthr) {
+    int sum = 0;
+#pragma unroll 8
+    for (int w = 0; w < kSortWarps; ++w) sum += wcnt[w * E + e];
+    cta_tot[e] = sum;
+  }
+  cluster_sync();  // every CTA's histogram is complete
+
+  // (b) per expert e = thread (E <= 512 < threads): rows in earlier CTAs and
+  // in all of them; the loads from the other CTAs are issued together
+  const int e = threadIdx.x;
+  int pre = 0, tot = 0;
+  if (e < E) {
+    int v[kSortCtas];
+#pragma unroll
+    for (int q = 0; q < kSortCtas; ++q)
+      v[q] = ld_cluster_s32(mapa_shared(&cta_tot[e], static_cast<uint32_t>(q)));
+#pragma unroll
+    for (int q = 0; q < kSortCtas; ++q) {
+      if (q < c) pre += v[q];
+      tot += v[q];
+    }
+  }
+  cluster_arrive_release();  // this thread is done with the other CTAs' memory
+  // exclusive scan of tot over experts
+  int incl = tot;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int y = __shfl_up_sync(FULL, incl, d);
+    if (lane >= d) incl += y;
+  }
+  if (lane == 31) warp_sum[wid] = incl;
+  __syncthreads();
+  int wbase = 0, all = 0;
+  for (int w = 0; w < nthr / 32; ++w) {
+    const int t = warp_sum[w];
+    if (w < wid) wbase += t;
+    all += t;
+  }
+  const int excl = wbase + incl - tot;
+  // (c) start position of every warp's rows of each expert
+  if (e < E) {
+    if (c == 0) {
+      counts[e] = tot;
+      offsets[e] = excl;
+    }
+    int run = excl + pre;
+#pragma unroll 8
+    for (int w = 0; w < kSortWarps; ++w) {
+      const int cnt = wcnt[w * E + e];
+      wcnt[w * E + e] = run;
+      run += cnt;
+    }
+  }
+  if (c == 0 && threadIdx.x == 0) offsets[E] = all;
+  __syncthreads();
+
+  // (d) ordered scatter of each warp's piece, 32 consecutive rows per step;
+  // inside a step, equal ids are ranked by lane with __match_any_sync
+  int32_t* my = wcnt + wid * E;
+  const unsigned lt = (1u << lane) - 1u;
+  const bool one_batch = w1 - w0 <= 32 * kSortBatch;
+  for (int rb = w0; rb < w1; rb += 32 * kSortBatch) {
+    if (!one_batch) load_batch(rb);
+#pragma unroll
+    for (int j = 0; j < kSortBatch; ++j) {
+      if (rb + 32 * j >= w1) break;  // warp-uniform
+      const int r = rb + 32 * j + lane;
+      const bool in = r < w1;
+      const int id = idv[j];
+      const bool valid = in && id >= 0 && id < E;
+      if (in && !valid) dest[r] = -1;
+      const int key = valid ? id : -1 - lane;  // invalid rows never match anything
+      const unsigned peers = __match_any_sync(FULL, key);
+      if (valid) {
+        const int pos = my[id] + __popc(peers & lt);
+        sorted_rows[pos] = r;
+        dest[r] = pos;
+      }
+      __syncwarp();
+      if (valid && (peers & lt) == 0) my[id] += __popc(peers);
+      __syncwarp();
+    }
+  }
+  cluster_wait_acquire();  // no CTA leaves while another may read its histogram
 }
 
 // ------------------------------------------------------------------------
@@ -1190,6 +1271,41 @@ cudaError_t launch_init_routing(const int32_t* ids, int R, int E, int32_t* count
   const size_t smem = (1 + kScatterWarps) * E * sizeof(int32_t);
   MOE_LAUNCH(route_scatter_kernel, nseg, kScatterWarps * 32, smem, s, ids, R, E, seg, nseg,
              seg_scratch, counts, offsets, sorted_rows, dest);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route_sort_cluster(const int32_t* ids, int R, int E, int32_t* counts,
+                                      int32_t* offsets, int32_t* sorted_rows, int32_t* dest,
+                                      int32_t* err, cudaStream_t s) {
+  if (R <= 0 || E < 1 || E > 512) return cudaErrorInvalidValue;
+  const size_t smem = static_cast<size_t>(kSortWarps + 1) * E * sizeof(int32_t);
+  static bool attr_done[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+  if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(route_sort_cluster_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>((kSortWarps + 1) * 512 * sizeof(int32_t)));
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_done[dev] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kSortCtas;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = g_pdl ? 1 : 0;
+  cfg.gridDim = dim3(kSortCtas, 1, 1);
+  cfg.blockDim = dim3(kSortWarps * 32, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, route_sort_cluster_kernel, ids, R, E, counts, offsets,
+                                     sorted_rows, dest, err);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -42,8 +42,13 @@ def test_workspace_size_covers_intermediates(lib, name):
     if shape.T * shape.k <= 8192:
         routing = 1  # small batches: init_routing and the gather in one kernel
     else:
-        routing = 3  # histogram, scan + scatter, gather (default MOE_OPT_GATHER_A = 0)
-    base = 7 if shape.I_shared else 5  # router, top-k, 2 (+2 shared) GEMMs, finalize
+        routing = 2  # one cluster launch (histogram, scan, scatter), gather (MOE_OPT_GATHER_A = 0)
+    # router projection and top-k as one kernel: bf16 activations, 64 <= E, and
+    # more than the CUDA-core projection takes (64 tokens, 2^25 multiply-adds)
+    fused = shape.act_dtype == "bf16" and shape.E >= 64 and not (
+        shape.T <= 64 and shape.T * shape.D * shape.E <= 2 ** 25)
+    # router (+ top-k), 2 (+2 shared) GEMMs, finalize
+    base = (6 if fused else 7) if shape.I_shared else (4 if fused else 5)
     assert moe.moe_layer_launch_count(cfg) == base + fp8_extra + routing
 
 
@@ -139,10 +144,41 @@ def test_set_option_values():
         (moe.MOE_OPT_TILE_ORDER, 0, 0),
         (moe.MOE_OPT_SHARED_IN_GEMM, 4, 1),
         (moe.MOE_OPT_SHARED_IN_GEMM, 0, 0),
+        (moe.MOE_OPT_FUSED_ROUTING, 0, 0),
+        (moe.MOE_OPT_FUSED_ROUTING, 2, 1),
     ]
     for opt, value, stored in cases:
         old = moe.moe_set_option(opt, value)
         assert moe.moe_set_option(opt, old) == stored
+
+
+@pytest.mark.parametrize("T,E,D,k,fused", [
+    (4096, 128, 2048, 8, True),    # Qwen3-MoE prefill
+    (16384, 256, 8192, 8, True),   # Ling-style prefill
+    (8192, 512, 4096, 10, True),   # two expert halves
+    (64, 128, 2048, 8, False),     # decode: the CUDA-core projection
+    (4096, 32, 2048, 4, False),    # fewer than 64 experts
+    (4096, 128, 2050, 8, False),   # D not a multiple of 8 (row pitch)
+])
+def test_fused_router_launch_count(T, E, D, k, fused):
+    """moe_layer makes one launch fewer where the router projection and the
+    top-k run as one kernel (MOE_OPT_FUSED_ROUTING), none fewer for them where
+    that kernel does not apply, and one more fewer where init_routing's
+    histogram and scatter run as one cluster launch (more than 8192 expanded
+    rows)."""
+    ensure_library()
+    cfg = moe.make_config(T, D, E, k, 768)
+    old = moe.moe_set_option(moe.MOE_OPT_FUSED_ROUTING, 1)
+    try:
+        n_on = moe.moe_layer_launch_count(cfg)
+        moe.moe_set_option(moe.MOE_OPT_FUSED_ROUTING, 0)
+        n_off = moe.moe_layer_launch_count(cfg)
+    finally:
+        moe.moe_set_option(moe.MOE_OPT_FUSED_ROUTING, old)
+    if D % 8:
+        assert n_on == n_off == 0  # invalid configuration
+    else:
+        assert n_on == n_off - (1 if fused else 0) - (1 if T * k > 8192 else 0)
 
 
 def test_fp8_nk_layout_host_logic(lib):
