@@ -336,8 +336,8 @@ def run_reference(args, world, rank):
 def set_options(moe, args):
     if args.pair_tiles is not None:
         moe.moe_set_option(moe.MOE_OPT_PAIR_TILES, args.pair_tiles)
-    if args.gather_a:
-        moe.moe_set_option(moe.MOE_OPT_GATHER_A, 1)
+    if args.gather_a is not None:
+        moe.moe_set_option(moe.MOE_OPT_GATHER_A, args.gather_a)
     if args.decode_kernel is not None:
         moe.moe_set_option(moe.MOE_OPT_DECODE_KERNEL, args.decode_kernel)
     if args.no_pdl:
@@ -365,7 +365,25 @@ def pct(v, q):
     return v[lo] + (v[hi] - v[lo]) * (pos - lo)
 
 
-def kernel_names(shape, nk, gather_a, a8=False, fused=False, shared_in_gemm=False, fused_routing=True):
+def gather_mode(shape, opt: int, shared_in_gemm: bool) -> int:
+    """Where moe_layer's routed gate/up pass takes its rows for MOE_OPT_GATHER_A
+    = opt (the library's rule, restated): 0 = the gather kernel's permuted copy,
+    1 = TMA gather4, 2 = cp.async gather warps (bf16 layers); the default (3)
+    takes 2 for bf16 layers with at least 32 routed rows per expert, else 0,
+    and 0 when the shared expert runs inside the routed GEMMs."""
+    if shape.act_dtype == "f32" or opt == 0:
+        return 0
+    bf16 = shape.w_dtype == "bf16"
+    if opt == 1:
+        return 1
+    if opt == 2:
+        return 2 if bf16 else 1
+    if shared_in_gemm:
+        return 0
+    return 2 if (bf16 and shape.R >= 32 * shape.E) else 0
+
+
+def kernel_names(shape, nk, gather_a=3, a8=False, fused=False, shared_in_gemm=False, fused_routing=True):
     """Names of the kernels one moe_layer call launches, in launch order."""
     fp8 = shape.w_dtype == "fp8_e4m3"
     rows = "e4m3" if a8 else "e4m3x2" if nk else "fp16"  # the A-row form of fp8 layers
@@ -377,7 +395,7 @@ def kernel_names(shape, nk, gather_a, a8=False, fused=False, shared_in_gemm=Fals
         names += ["route_permute"]
     else:
         names += ["route_sort"] if fused_routing else ["route_hist", "route_scan_scatter"]
-        names += ["permute_gather"] if (shape.act_dtype == "f32" or not gather_a) else []
+        names += ["permute_gather"] if gather_mode(shape, gather_a, shared_in_gemm) == 0 else []
     names += ["w13_gate_up"]
     names += [f"h_to_{rows}"] if fp8 else []
     names += ["w2_down"]
@@ -458,9 +476,10 @@ def measure(args, world, rank, local, shape, primary: bool, layout: str):
     # ---- per-kernel durations (instrumented pass, same work, after the timed region)
     L = moe.moe_layer_launch_count(cfg)
     fused = args.fused_combine and shape.act_dtype == "bf16" and (nk or not fp8)
+    gather_opt = 3 if args.gather_a is None else args.gather_a
     in_gemm = (args.shared_in_gemm and shape.I_shared == shape.I and shape.I_shared > 0 and
-               shape.act_dtype == "bf16" and (nk or not fp8) and not args.gather_a)
-    names = kernel_names(shape, nk, args.gather_a, a8, fused, in_gemm, not args.split_routing)
+               shape.act_dtype == "bf16" and (nk or not fp8) and gather_opt in (0, 3))
+    names = kernel_names(shape, nk, gather_opt, a8, fused, in_gemm, not args.split_routing)
     assert len(names) == L
     per = [[] for _ in range(L)]
     for _ in range(args.steps):
@@ -698,8 +717,10 @@ def main():
                          "tails), 2 always without swapped tails, 3 (default) by rows per group")
     ap.add_argument("--decode-kernel", type=int, default=None, choices=[0, 1, 2, 3],
                     help="moe_set_option MOE_OPT_DECODE_KERNEL (0 off, 1 auto, 2/3 always with 64/16-row tiles)")
-    ap.add_argument("--gather-a", action="store_true",
-                    help="routed gate/up GEMM gathers x rows itself (moe_set_option MOE_OPT_GATHER_A)")
+    ap.add_argument("--gather-a", type=int, nargs="?", const=1, default=None, choices=[0, 1, 2, 3],
+                    help="where the routed gate/up GEMM takes its rows (moe_set_option MOE_OPT_GATHER_A: "
+                         "0 = permuted copy, 1 = TMA gather4, 2 = cp.async gather warps for bf16 "
+                         "layers, 3 = the library's default rule)")
     ap.add_argument("--fp8-layout", default="nk", choices=["kn", "nk", "nk_a8"],
                     help="fp8 workloads: weights transposed once to [.., N, K] and run on the e4m3 "
                          "tensor-core kind (nk, default), or as drawn and expanded to fp16 on chip (kn); "

@@ -316,12 +316,18 @@ int moe_layer_launch_count(const moe_config_t* cfg);
  *   hi and lo e4m3 rows along N).  Results are the same up to fp32
  *   summation order. */
 #define MOE_OPT_PAIR_TILES 1
-/*   MOE_OPT_GATHER_A: 1 = moe_layer does not materialise the permuted rows;
- *   the routed gate/up GEMM gathers its A rows from x (or, for fp8 weights,
- *   from x's fp16 or two-term e4m3 rows) with TMA tile::gather4 loads, on
- *   one-CTA tiles (measured 2.5-2.8x slower on GB300 than the streaming
- *   gather kernel plus tiled loads); 0 (default) = gather kernel, then tiled
- *   loads.  Same results. */
+/*   MOE_OPT_GATHER_A: where moe_layer's routed gate/up GEMM takes its A
+ *   rows.  0 = a permuted copy of x written by the gather kernel, read by
+ *   tiled TMA loads; 1 = no copy: the GEMM reads the rows of x (for fp8
+ *   weights, x's fp16 or two-term e4m3 rows) with TMA tile::gather4 loads, on
+ *   one-CTA tiles (measured 2.5-2.8x slower on GB300); 2 = no copy, for bf16
+ *   layers: four extra warps of the GEMM copy each tile row's 128 bytes per
+ *   k-block from x by 16-byte cp.async, eight lanes per row (fp8 layers take
+ *   1); 3 (default) = 2 for bf16 layers with at least 32 routed rows per
+ *   expert on average (prefill: Qwen3-MoE-style layer 526 -> 490 us,
+ *   Gemma-4-style 491 -> 469 us on GB300), 0 otherwise and when
+ *   MOE_OPT_SHARED_IN_GEMM is set for a layer that can take it.  Same
+ *   results. */
 #define MOE_OPT_GATHER_A 2
 /*   MOE_OPT_DECODE_KERNEL: 1 (default) = the swap-AB decode kernel (weights
  *   as the 128-row MMA operand, 16 or 64 rows per tile, each active expert's
@@ -384,7 +390,7 @@ int moe_layer_launch_count(const moe_config_t* cfg);
  *   Routing优化": fused gate + gating_top_k_softmax, fused init_routing):
  *   (a) for more than 64 tokens of bf16 activations (64 <= E <= 512), the
  *   router projection and the top-k softmax are one kernel: a cluster of up
- *   to 8 CTAs per 128 tokens splits the fp32 sum over D into consecutive
+ *   to 4 CTAs per 128 tokens splits the fp32 sum over D into consecutive
  *   slices on the tensor core and hands the partial rows through distributed
  *   shared memory to the CTA that adds them in slice order and takes the
  *   top-k; (b) for more than 8192 expanded rows, the histogram, scan and

@@ -149,6 +149,7 @@ struct KParams {
   const float* bias;
   const float* a_row_scale;  // per-row factor on the accumulator (fp16 A rows), or nullptr
   const int32_t* a_gather;   // gather mode: A row of output row r is a_gather[r] / gather_k
+  const void* a_src;         // cp.async gather mode: the [a_rows, K] bf16 A rows
   int gather_k;
   int a_rows;                // rows of the A tensor (gather mode)
   int h_fp32;                // gate/up pass: store h as fp32
@@ -419,8 +420,10 @@ __device__ __forceinline__ uint2 e4m3x4_to_f16x4(uint32_t w) {
 // 128 K elements (128 bytes) per stage and no weight expansion; the A rows are
 // two-term e4m3 (hi and lo tiles of the stage, as in SPLIT: W8A16) or, with
 // SPLIT off, one e4m3 term with a per-row scale (W8A8).
-template <int EPI, bool SPLIT, bool FP8, bool PAIR, bool Q8>
-__global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
+// CPG: the A rows are gathered by four extra warps (6..9) with 16-byte
+// cp.async copies from the unpermuted rows (bf16, one-CTA tiles, gate/up pass).
+template <int EPI, bool SPLIT, bool FP8, bool PAIR, bool Q8, bool CPG = false>
+__global__ void __launch_bounds__(CPG ? 320 : StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                         const __grid_constant__ CUtensorMap tmap_a_lo,
                         const __grid_constant__ CUtensorMap tmap_b,
@@ -432,6 +435,8 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
                         const __grid_constant__ CUtensorMap tmap_out, const KParams p) {
   pdl_wait();
   static_assert(!Q8 || !FP8, "e4m3 rows meet K-contiguous e4m3 weights, not expanded ones");
+  static_assert(!CPG || (!SPLIT && !FP8 && !PAIR && !Q8 && EPI == kEpiGateUpAct),
+                "cp.async row gather: bf16 gate/up pass on one-CTA tiles");
   using Cfg = StageCfg<SPLIT, FP8, PAIR>;
   // fp8 weights: fp16 operands; everything else: bf16 operands
   constexpr bool F16 = FP8;
@@ -471,7 +476,8 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
       // threads stored their part of the 16-bit B tile
       // (one arrival per converter warp; in a pair both CTAs' converters and
       // A loads report to the leader's barrier)
-      mbar_init(&ctrl->full[s], FP8 ? 1 + Cfg::kConvWarps * (PAIR ? 2 : 1) : 1);
+      // (CPG: the producer's B bytes plus one cp.async arrival per gather thread)
+      mbar_init(&ctrl->full[s], FP8 ? 1 + Cfg::kConvWarps * (PAIR ? 2 : 1) : CPG ? 1 + BM : 1);
       mbar_init(&ctrl->empty[s], 1);
       mbar_init(&ctrl->raw_full[s], 1);
     }
@@ -552,12 +558,13 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
     // except in gather mode, where every lane fetches 4 of the tile's 128 A
     // rows straight from x with one tile::gather4 per k-block).
     {
-      const bool gather = p.a_gather != nullptr;
+      const bool gather = p.a_gather != nullptr && !CPG;  // TMA tile::gather4 rows
       // L2 priorities: A rows (re-read by every column tile) and B weights
       const uint64_t pol_a = l2_policy_evict_normal();
       const uint64_t pol_b = l2_policy_evict_normal();
       // bytes the (leader's) full barrier waits for: A (+ bf16 B) of every CTA
-      const uint32_t tx = (PAIR ? 2u : 1u) * (FP8 ? A_BYTES : A_BYTES + nbox_cta * B_BOX_BYTES);
+      const uint32_t tx = CPG ? static_cast<uint32_t>(nbox_cta * B_BOX_BYTES)
+                              : (PAIR ? 2u : 1u) * (FP8 ? A_BYTES : A_BYTES + nbox_cta * B_BOX_BYTES);
       const int nraw = PAIR ? 1 : (p.bn + 127) / 128;  // raw e4m3 boxes this CTA loads (fp8)
       uint32_t stage = 0, phase = 0;
       // stages filled by this producer and the barrier phase each fill completes
@@ -656,7 +663,7 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
                              kb * KE, tr[0], tr[1], tr[2], tr[3], pol_a);
           }
           if (lane == 0) {
-          if (!gather) {
+          if (!gather && !CPG) {
             if (PAIR) {
               tma_load_2d_pair(a_dst, &tmap_a, fbar, kb * KE, my_row0, pol_a);
               if (SPLIT)
@@ -803,6 +810,9 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
             break;
           }
           tc_fence_after_sync();
+          // A rows written by the gather warps' cp.async (generic proxy), read
+          // by the tensor core (async proxy)
+          if (CPG) fence_proxy_async_smem();
           if (PAIR && swap && Q8) {
             // weights (K-major, 128 rows per CTA) as the M = 256 operand; the
             // hi rows (CTA 0) and lo rows (CTA 1), or each CTA's half of the
@@ -900,6 +910,65 @@ __global__ void __launch_bounds__(StageCfg<SPLIT, FP8, PAIR>::kThreads, 1)
     }
     __syncwarp();
   } else if (warp >= 6) {
+    // ------------------------------------------------------------ row gather
+    // Warps 6..9 fill the A tiles: warp w the rows 32 w .. 32 w + 31, eight
+    // lanes per row, so that one copy instruction reads four whole 128-byte
+    // row segments (k-block kb of source row x[a_gather[row] / k]) and lane
+    // l copies piece l % 8 of row 32 w + 4 j + l / 8 (j = 0..7) into the
+    // 128-byte-swizzled K-major layout the MMA reads (piece c of row r at
+    // c ^ (r & 7)).  Columns past K are zeros; rows past the group are not
+    // loaded (their results are never stored).  Each thread then arrives on
+    // the stage's full barrier once its copies have landed.
+    if (CPG) {
+      const int gw = warp - 6;
+      const int piece = lane & 7;
+      const __nv_bfloat16* src_base = static_cast<const __nv_bfloat16*>(p.a_src);
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      for (int t = work0; t < total_tiles && ok; t += work_stride) {
+        const TileInfo ti = decode_tile<TILE_M>(ctrl, G, t / p.ksplit, p.n_tiles, p.cols_per_tile);
+        const __nv_bfloat16* src_row[8];
+        uint32_t live = 0;  // bit j: row 32 gw + 4 j + lane / 8 is inside the group
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          const int r = 32 * gw + 4 * jj + (lane >> 3);
+          src_row[jj] = src_base;
+          if (r < ti.rows) {
+            const int src = p.a_gather[ti.row0 + r] / p.gather_k;
+            src_row[jj] = src_base + static_cast<size_t>(min(max(src, 0), p.a_rows - 1)) * p.K;
+            live |= 1u << jj;
+          }
+        }
+        int kb0, kb1;
+        kb_range(t, kb0, kb1);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (lane == 0) ok = mbar_wait(&ctrl->empty[stage], phase ^ 1u, abort_flag);
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+          const int kc = kb * BK + 8 * piece;  // K is a multiple of 8: a piece is all in or all out
+          const uint32_t nbytes = kc < p.K ? 16u : 0u;
+          const int koff = kc < p.K ? kc : 0;
+          const uint32_t a0 = smem_u32(stage_a(stage));
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) {
+            const uint32_t r = static_cast<uint32_t>(32 * gw + 4 * jj + (lane >> 3));
+            if ((live >> jj) & 1u)
+              cp_async_16(a0 + r * 128u + ((static_cast<uint32_t>(piece) ^ (r & 7u)) << 4),
+                          src_row[jj] + koff, nbytes);
+          }
+          cp_async_mbar_arrive_noinc(&ctrl->full[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok && lane == 0) {
+        ctrl->abort = 1;
+        atomicOr(p.err, MOE_DEV_WAIT_TIMEOUT);
+      }
+      cp_async_wait_all();  // this thread's copies land before the CTA may leave
+    }
     // ------------------------------------------------------------ fp8 converters
     if (FP8) {
       constexpr int NCONV = Cfg::kConvWarps * 32;
@@ -1860,7 +1929,7 @@ void make_out_map(const GroupedGemmArgs& a, KParams& kp, bool out_bf16, CUtensor
     kp.tma_out = 1;
 }
 
-template <int EPI, bool SPLIT, bool FP8, bool PAIR, bool Q8 = false>
+template <int EPI, bool SPLIT, bool FP8, bool PAIR, bool Q8 = false, bool CPG = false>
 cudaError_t launch_epi(const CUtensorMap& ta, const CUtensorMap& ta_lo, const CUtensorMap& tb,
                        const CUtensorMap& tb_tail, const CUtensorMap& ta_tail,
                        const CUtensorMap& ta_lo_tail, const CUtensorMap& tb2,
@@ -1868,8 +1937,8 @@ cudaError_t launch_epi(const CUtensorMap& ta, const CUtensorMap& ta_lo, const CU
                        long long max_tiles,
                        cudaStream_t s) {
   constexpr size_t smem = smem_bytes<SPLIT, FP8, PAIR>();
-  constexpr int threads = StageCfg<SPLIT, FP8, PAIR>::kThreads;
-  auto kern = grouped_gemm_kernel<EPI, SPLIT, FP8, PAIR, Q8>;
+  constexpr int threads = CPG ? 320 : StageCfg<SPLIT, FP8, PAIR>::kThreads;
+  auto kern = grouped_gemm_kernel<EPI, SPLIT, FP8, PAIR, Q8, CPG>;
   // the attribute is per device: set it once for each device this process uses
   static bool done[64] = {false};
   int dev = 0;
@@ -2107,6 +2176,7 @@ cudaError_t launch_grouped_gemm_q8(const GroupedGemmArgs& a, cudaStream_t s) {
   kp.b_scale = a.b_scale;
   kp.a_row_scale = a.a_row_scale;
   kp.a_gather = a.a_gather;
+  kp.a_src = a.A;
   kp.gather_k = a.gather_k;
   kp.a_rows = a.a_rows;
   kp.h_fp32 = a.h_fp32;
@@ -2313,6 +2383,7 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
   kp.bias = a.bias;
   kp.a_row_scale = a.a_row_scale;
   kp.a_gather = a.a_gather;
+  kp.a_src = a.A;
   kp.gather_k = a.gather_k;
   kp.a_rows = a.a_rows;
   kp.h_fp32 = a.h_fp32;
@@ -2433,6 +2504,9 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
                                                    tb2, tb2_tail, tout, kp, max_tiles, s))
   if (a.epilogue == kEpiGateUpAct) {
     if (a.A_lo) return cudaErrorInvalidValue;
+    if (a.a_gather && a.a_gather_cp && !a.b_fp8 && !a.a_fp16 && a.K % 8 == 0)  // cp.async row gather
+      return launch_epi<kEpiGateUpAct, false, false, false, false, true>(
+          ta, ta_lo, tb, tb_tail, ta_tail, ta_lo_tail, tb2, tb2_tail, tout, kp, max_tiles, s);
     return a.b_fp8 ? MOE_LAUNCH(kEpiGateUpAct, false, true) : MOE_LAUNCH(kEpiGateUpAct, false, false);
   }
   if (a.epilogue == kEpiStoreF32) {

@@ -14,7 +14,7 @@ namespace {
 
 constexpr size_t kAlign = 256;
 
-int g_gather_a = 0;       // moe_set_option(MOE_OPT_GATHER_A, .)
+int g_gather_a = 3;       // moe_set_option(MOE_OPT_GATHER_A, .)
 int g_shared_stream = 1;  // moe_set_option(MOE_OPT_SHARED_STREAM, .)
 int g_fused_combine = 0;  // moe_set_option(MOE_OPT_FUSED_COMBINE, .)
 int g_shared_in_gemm = 0;  // moe_set_option(MOE_OPT_SHARED_IN_GEMM, .)
@@ -158,8 +158,27 @@ inline bool shared_group_capable(const moe_config_t* c) {
   return c->I_shared > 0 && c->I_shared == c->I && c->act_dtype == MOE_BF16 &&
          (c->w_dtype == MOE_BF16 || is_nk(c));
 }
+// Where the routed gate/up pass of moe_layer takes its rows (MOE_OPT_GATHER_A):
+// 0 = the gather kernel's permuted copy, 1 = TMA tile::gather4 from x (or its
+// row form), 2 = the GEMM's cp.async gather warps from x (bf16 layers).  The
+// default (3) takes 2 for bf16 layers whose routed pass has at least 32 rows
+// per expert on average (prefill: measured faster than the gather kernel plus
+// 2-CTA tiles on the Qwen3-MoE and Gemma-4 prefill layers), else 0 -- and 0
+// when the shared expert is asked to run inside the routed GEMMs.
+inline int gather_mode(const moe_config_t* c) {
+  if (c->act_dtype == MOE_F32) return 0;
+  const bool bf16 = c->w_dtype == MOE_BF16;
+  switch (g_gather_a) {
+    case 0: return 0;
+    case 1: return 1;
+    case 2: return bf16 ? 2 : 1;
+    default:
+      if (g_shared_in_gemm && shared_group_capable(c)) return 0;
+      return (bf16 && static_cast<long long>(c->T) * c->k >= 32ll * c->E) ? 2 : 0;
+  }
+}
 inline bool shared_in_gemm_on(const moe_config_t* c) {
-  return g_shared_in_gemm && shared_group_capable(c) && !g_gather_a;
+  return g_shared_in_gemm && shared_group_capable(c) && gather_mode(c) == 0;
 }
 
 // Bytes per row of D elements in the form moe_layer permutes: x itself, or
@@ -392,6 +411,7 @@ int do_ffn(const moe_config_t* c, const void* A, const float* a_row_scale, int M
   a.a_gather = a_gather;
   a.gather_k = c->k;
   a.a_rows = a_rows;
+  a.a_gather_cp = gather_mode(c) == 2;
   a.N = I;
   a.b_scale = s13;
   a.out = h;
@@ -665,11 +685,13 @@ int moe_layer(const moe_config_t* cfg, const void* x, const void* Wg, const floa
   float* partials = L.router_partials ? reinterpret_cast<float*>(ws_at(ws, L.router_partials)) : nullptr;
   st = do_route(cfg, x, Wg, logit_bias, logits, ids, w, partials, err, s);
   if (st != MOE_OK) return fail(st);
-  // Default: a permuted copy of x (the gather kernel streams at HBM speed).
-  // With MOE_OPT_GATHER_A the routed gate/up pass instead gathers its rows from
-  // x (or its fp16 copy) with TMA tile::gather4 loads (slower on GB300: 32
-  // four-row requests per 16 KB A tile).
-  const bool gather = g_gather_a && cfg->act_dtype != MOE_F32;
+  // The routed gate/up pass reads its rows from a permuted copy of x (the
+  // gather kernel streams at HBM speed), or gathers them from x itself
+  // (gather_mode): bf16 prefill layers by default with the GEMM's cp.async
+  // gather warps (x stays in L2; no permuted copy is written or read), on
+  // request with TMA tile::gather4 loads (slower on GB300: 32 four-row
+  // requests per 16 KB A tile).
+  const bool gather = gather_mode(cfg) != 0;
   st = do_permute(cfg, ids, gather ? nullptr : x_rows, counts, offsets, sorted_rows, dest,
                   gather ? nullptr : x_perm, seg, err, s, layer_row_bytes(cfg), tok_inv, row_inv,
                   in_gemm ? cfg->T : 0);
@@ -748,7 +770,7 @@ int moe_set_option(int option, int value) {
     }
     case MOE_OPT_GATHER_A: {
       const int old = g_gather_a;
-      g_gather_a = value ? 1 : 0;
+      g_gather_a = value <= 0 ? 0 : value >= 3 ? 3 : value;
       return old;
     }
     case MOE_OPT_SHARED_STREAM: {
@@ -807,7 +829,7 @@ int moe_layer_launch_count(const moe_config_t* cfg) {
     n += 1;  // init_routing + permutation gather in one kernel
   } else {
     n += g_fused_routing ? 1 : 2;  // histogram, scan + stable scatter (one cluster launch when fused)
-    if (cfg->act_dtype == MOE_F32 || !g_gather_a) n += 1;  // permutation gather
+    if (gather_mode(cfg) == 0) n += 1;  // permutation gather
   }
   n += 2;  // routed gate/up, down
   if (sep_shared) n += 2;  // shared gate/up, down

@@ -211,6 +211,7 @@ struct GroupedGemmArgs {
   const int32_t* a_gather;       // [M] row gather: output row r reads A row a_gather[r] / gather_k
   int gather_k;
   int a_rows;                    // rows of A when gathering
+  int a_gather_cp;               // 1: gather by cp.async warps (bf16 gate/up pass), not TMA gather4
   int a_fp16;                    // 1: A is fp16 (fp8 layers), B e4m3 expanded to fp16
   int a_e4m3x2;                  // 1: A rows are two-term e4m3 [M, 2K] (hi | lo) and B is
                                  //    e4m3 stored [G, N, K] (gate/up: [G, 2N, K]):

@@ -7,7 +7,7 @@
 //   ids[t, :], w[t, :] = top-k of logits[t, :] and its softmax
 //
 // One thread-block cluster per tile of 128 tokens.  Its C = ck x nh CTAs split
-// the reduction over D into ck consecutive slices (ck = 1, 2, 4, 8) and, when
+// the reduction over D into ck consecutive slices (ck = 1, 2, 4) and, when
 // E > 256, the experts into nh = 2 halves of 256.  Each CTA:
 //   warp 0      : TMA producer (one lane) -- x tile 128 tokens x 64 d (K-major)
 //                 and the W_g boxes of its experts, 64 d x 64 experts each
@@ -47,7 +47,10 @@ constexpr int RT_RING_BYTES = 192 * 1024;        // stage ring (later: partial r
 constexpr int RT_MAX_STAGES = 8;
 constexpr int RT_THREADS = 512;  // 16 warps: all of them take tokens in the top-k phase
 constexpr int RT_WARPS = RT_THREADS / 32;
-constexpr int RT_MAX_CLUSTER = 8;
+// Clusters of 8 such CTAs (197 KB of shared memory each) measured slower than
+// 4 (Gemma-4-style prefill router, 16 token tiles: 24.4 us with 8 slices);
+// at most 4 CTAs per cluster.
+constexpr int RT_MAX_CLUSTER = 4;
 
 template <int NB>
 struct RtCfg {
@@ -317,7 +320,7 @@ void router_topk_split(int T, int E, int D, int& ck, int& nh) {
   const int KB = (D + RT_BK - 1) / RT_BK;
   // about one wave of CTAs on a 152-SM GB300 (a constant, so that the choice
   // depends on the shape alone), slices of at least 4 k-blocks, clusters of
-  // at most 8 CTAs
+  // at most RT_MAX_CLUSTER CTAs
   const int want = std::max(1, std::min({RT_MAX_CLUSTER / nh, 148 / std::max(1, tiles * nh), KB / 4}));
   ck = 1;
   while (2 * ck <= want) ck *= 2;

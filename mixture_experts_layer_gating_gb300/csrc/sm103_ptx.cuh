@@ -208,6 +208,22 @@ __device__ __forceinline__ void tma_load_5d_pair(void* dst, const CUtensorMap* m
       : "memory");
 }
 
+// ------------------------------------------------------------------ cp.async
+// 16-byte global -> shared copy; src_bytes < 16 fills the rest with zeros
+// (0: nothing is read).  Generic-proxy writes: a consumer that reads them with
+// the tensor core first waits on the mbarrier below, then fences the proxies.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+// One arrival on `bar` once every cp.async this thread issued before has
+// landed (the arrival counts toward the barrier's expected count).
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // ------------------------------------------------------------------ clusters
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;

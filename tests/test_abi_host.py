@@ -42,7 +42,12 @@ def test_workspace_size_covers_intermediates(lib, name):
     if shape.T * shape.k <= 8192:
         routing = 1  # small batches: init_routing and the gather in one kernel
     else:
-        routing = 2  # one cluster launch (histogram, scan, scatter), gather (MOE_OPT_GATHER_A = 0)
+        # one cluster launch (histogram, scan, scatter), and the gather kernel
+        # unless the routed GEMM gathers its rows itself (bf16 layers with at
+        # least 32 rows per expert, MOE_OPT_GATHER_A's default)
+        gemm_gathers = shape.act_dtype == "bf16" and shape.w_dtype == "bf16" and \
+            shape.T * shape.k >= 32 * shape.E
+        routing = 1 if gemm_gathers else 2
     # router projection and top-k as one kernel: bf16 activations, 64 <= E, and
     # more than the CUDA-core projection takes (64 tokens, 2^25 multiply-adds)
     fused = shape.act_dtype == "bf16" and shape.E >= 64 and not (
@@ -132,6 +137,10 @@ def test_set_option_values():
         (moe.MOE_OPT_PAIR_TILES, 5, 3),
         (moe.MOE_OPT_PAIR_TILES, 1, 1),
         (moe.MOE_OPT_GATHER_A, 1, 1),
+        (moe.MOE_OPT_GATHER_A, 2, 2),
+        (moe.MOE_OPT_GATHER_A, 9, 3),
+        (moe.MOE_OPT_GATHER_A, 3, 3),
+        (moe.MOE_OPT_GATHER_A, -1, 0),
         (moe.MOE_OPT_DECODE_KERNEL, 7, 3),
         (moe.MOE_OPT_DECODE_KERNEL, -3, 0),
         (moe.MOE_OPT_PDL, 0, 0),

@@ -134,18 +134,18 @@ def test_bench_kernel_names_match_launch_count(name, layout):
     shape = workloads.CONFIGS[name]
     nk = layout == "nk" and shape.w_dtype == "fp8_e4m3"
     cfg = moe.config_from_shape(shape, "nk" if nk else "kn")
-    assert len(bench.kernel_names(shape, nk, False)) == moe.moe_layer_launch_count(cfg)
+    assert len(bench.kernel_names(shape, nk)) == moe.moe_layer_launch_count(cfg)
     old = moe.moe_set_option(moe.MOE_OPT_SHARED_IN_GEMM, 1)
     try:
         in_gemm = (shape.I_shared == shape.I and shape.I_shared > 0 and shape.act_dtype == "bf16" and
                    (nk or shape.w_dtype != "fp8_e4m3"))
-        assert len(bench.kernel_names(shape, nk, False, shared_in_gemm=in_gemm)) == \
+        assert len(bench.kernel_names(shape, nk, shared_in_gemm=in_gemm)) == \
             moe.moe_layer_launch_count(cfg)
     finally:
         moe.moe_set_option(moe.MOE_OPT_SHARED_IN_GEMM, old)
     old = moe.moe_set_option(moe.MOE_OPT_FUSED_ROUTING, 0)
     try:
-        assert len(bench.kernel_names(shape, nk, False, fused_routing=False)) == \
+        assert len(bench.kernel_names(shape, nk, fused_routing=False)) == \
             moe.moe_layer_launch_count(cfg)
     finally:
         moe.moe_set_option(moe.MOE_OPT_FUSED_ROUTING, old)

@@ -2,11 +2,11 @@
 
 The router projection fused with the top-k softmax (one cluster launch per
 128 tokens), through moe_route.  The fused kernel splits the fp32 sum over D
-into up to 8 consecutive slices on the CTAs of a cluster and, when E > 256,
+into up to 4 consecutive slices on the CTAs of a cluster and, when E > 256,
 the experts into two halves; the CTA that finishes a token adds the partial
 rows in slice order.  Routing is checked bit-exact against the oracle's top-k
 of the GPU's own logits, the logits against the fp64 projection, with both
-settings of the option.  The shapes cover one to eight slices, two expert
+settings of the option.  The shapes cover one to four slices, two expert
 halves (E = 320 and 512, the second half partly past E), expert counts that
 leave the last 64-expert box partly or wholly past E (96, 160, 200), token
 counts that leave the last 128-token tile short, and D that is not a multiple
@@ -33,9 +33,9 @@ pytestmark = pytest.mark.gpu
 SHAPES = [
     # T, E, k, renorm, bias, D
     (4096, 128, 8, 1, False, 2048),   # Qwen3-MoE prefill shape: 4 slices
-    (2048, 128, 8, 1, False, 2816),   # Gemma-4 prefill shape: 8 slices, D % 64 != 0
+    (2048, 128, 8, 1, False, 2816),   # Gemma-4 prefill shape: 4 slices, D % 64 != 0
     (8192, 512, 10, 1, True, 4096),   # Qwen3.5 prefill shape: two expert halves
-    (65, 128, 8, 1, True, 2048),      # one short tile, 8 slices
+    (65, 128, 8, 1, True, 2048),      # one short tile, 4 slices
     (300, 96, 6, 0, False, 1000),     # last box partly past E; 3 tiles
     (1000, 160, 8, 1, True, 136),     # a box wholly past E; 3 k-blocks, one slice
     (777, 200, 16, 1, False, 520),    # k = 16

@@ -218,10 +218,13 @@ def test_layer_same_result_with_shared_expert_stream(case):
         moe.moe_set_option(moe.MOE_OPT_SHARED_STREAM, old)
 
 
+@pytest.mark.parametrize("mode", [1, 2])
 @pytest.mark.parametrize("case", ["qwen3_T512", "fp8_small_T300", "gemma4_T256"])
-def test_layer_parity_gemm_gathers_rows(case):
-    """MOE_OPT_GATHER_A: the routed gate/up GEMM reads x rows with TMA gather4."""
-    old = moe.moe_set_option(moe.MOE_OPT_GATHER_A, 1)
+def test_layer_parity_gemm_gathers_rows(case, mode):
+    """MOE_OPT_GATHER_A: the routed gate/up GEMM reads x rows itself, with TMA
+    gather4 (1) or, for bf16 layers, with cp.async gather warps (2; fp8 layers
+    keep gather4)."""
+    old = moe.moe_set_option(moe.MOE_OPT_GATHER_A, mode)
     try:
         check_layer(LAYER_CASES[case])
     finally:

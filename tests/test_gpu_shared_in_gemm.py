@@ -89,8 +89,11 @@ def test_shared_in_gemm_bit_identical_to_separate_launches(case, pair):
 
 def test_shared_in_gemm_launch_count():
     """A layer that takes the path makes no launches of its own for the shared
-    expert (two GEMMs fewer; fp8 layers one row conversion fewer)."""
-    for name, layout, fewer in [("qwen35_prefill", "kn", 2), ("ling_prefill", "nk", 3),
+    expert (two GEMMs fewer; fp8 layers one row conversion fewer).  A bf16
+    prefill layer then also takes the permuted copy of x (one gather launch
+    more) instead of the routed GEMM's own row gather, since the shared
+    expert's rows are appended to the permuted rows."""
+    for name, layout, fewer in [("qwen35_prefill", "kn", 1), ("ling_prefill", "nk", 3),
                                 ("gemma4_prefill", "kn", 0)]:
         cfg = moe.config_from_shape(C[name], layout)
         old = moe.moe_set_option(moe.MOE_OPT_SHARED_IN_GEMM, 0)
