@@ -344,8 +344,12 @@ def set_options(moe, args):
         moe.moe_set_option(moe.MOE_OPT_PDL, 0)
     if args.serial_shared:
         moe.moe_set_option(moe.MOE_OPT_SHARED_STREAM, 0)
+    if getattr(args, "shared_fork", None) is not None:
+        moe.moe_set_option(moe.MOE_OPT_SHARED_STREAM, args.shared_fork)
     if args.fused_combine:
         moe.moe_set_option(moe.MOE_OPT_FUSED_COMBINE, 1)
+    if getattr(args, "b_prefetch", None) is not None:
+        moe.moe_set_option(moe.MOE_OPT_B_PREFETCH, args.b_prefetch)
     if getattr(args, "split_routing", False):
         moe.moe_set_option(moe.MOE_OPT_FUSED_ROUTING, 0)
     if args.lpt:
@@ -727,6 +731,8 @@ def main():
                          "nk_a8: nk weights with W8A8 activations (opt-in, changes the result)")
     ap.add_argument("--no-pdl", action="store_true",
                     help="plain stream order instead of programmatic dependent launch (MOE_OPT_PDL 0)")
+    ap.add_argument("--b-prefetch", type=int, default=None,
+                    help="weight boxes prefetched into L2 this many k-blocks ahead (MOE_OPT_B_PREFETCH)")
     ap.add_argument("--split-routing", action="store_true",
                     help="router projection and top-k, histogram and scatter as separate launches "
                          "(MOE_OPT_FUSED_ROUTING 0)")
@@ -740,6 +746,9 @@ def main():
                     help="grouped GEMMs run the experts heaviest first (MOE_OPT_TILE_ORDER 1)")
     ap.add_argument("--serial-shared", action="store_true",
                     help="shared expert on the caller's stream (MOE_OPT_SHARED_STREAM 0)")
+    ap.add_argument("--shared-fork", type=int, default=None, choices=[1, 2],
+                    help="where the shared expert's side stream forks (MOE_OPT_SHARED_STREAM: "
+                         "1 = once x is ready, 2 = after init_routing)")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override T of the workload (smaller cases for profiling)")
     ap.add_argument("--experts", type=int, default=None,

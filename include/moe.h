@@ -349,10 +349,13 @@ int moe_layer_launch_count(const moe_config_t* cfg);
  *   on a second stream owned by the library (one per device, created on the
  *   first call that needs it) that forks from the caller's stream once x is
  *   ready and joins it before the finalize kernel, so that the shared GEMMs
- *   overlap routing and the routed GEMMs; 0 = everything on the caller's
- *   stream.  Same results.  Fork and join are event record / wait pairs made
- *   under a lock, so calls from several host threads stay correct (their
- *   shared experts then serialise on the one side stream). */
+ *   overlap routing and the routed GEMMs; 2 = the same stream, forked after
+ *   init_routing instead (the shared GEMMs then start beside the permutation
+ *   kernel, which needs no shared memory, rather than ahead of the routing
+ *   kernels, which do); 0 = everything on the caller's stream.  Same results.
+ *   Fork and join are event record / wait pairs made under a lock, so calls
+ *   from several host threads stay correct (their shared experts then
+ *   serialise on the one side stream). */
 #define MOE_OPT_SHARED_STREAM 5
 /*   MOE_OPT_FUSED_COMBINE: 1 = moe_layer fuses the combine into the routed
  *   down projection (NEXT-1's second half: "千问 3.5 MoE 在 TPU 上的系统优化实战",
@@ -402,6 +405,13 @@ int moe_layer_launch_count(const moe_config_t* cfg);
  *   ids and weights follow from each one's own logits by the same rule, and
  *   the permutation is the same. */
 #define MOE_OPT_FUSED_ROUTING 10
+/*   MOE_OPT_B_PREFETCH: n > 0 = the grouped GEMMs' TMA producer also
+ *   prefetches its weight box n k-blocks ahead into L2 (near the end of a
+ *   tile, the first k-blocks of its next tile), so that more weight bytes are
+ *   in flight from HBM than the shared-memory ring holds; for the weights
+ *   read in one box per stage (bf16 as 64-column blocks, K-contiguous e4m3).
+ *   0 (default) = off; at most 16.  Same results. */
+#define MOE_OPT_B_PREFETCH 11
 int moe_set_option(int option, int value);
 
 /* Per-kernel timing hook (process-wide, off by default).  `events` holds

@@ -167,6 +167,9 @@ struct KParams {
   const float* comb_w;
   int comb_k;
   int lpt;  // 1: groups scheduled heaviest first (most rows; lower index on ties)
+  // > 0: the producer also prefetches this CTA's weight box b_prefetch
+  // k-blocks ahead into L2 (into the next tile of this CTA near a tile's end)
+  int b_prefetch;
   // > 0: the last group (G - 1) is the shared expert: its rows are the last
   // sh_rows rows of A [M - sh_rows, M) and its weights the second weight map
   // (tmap_b2) with per-column scales sh_b_scale
@@ -594,6 +597,30 @@ __global__ void __launch_bounds__(CPG ? 320 : StageCfg<SPLIT, FP8, PAIR>::kThrea
         int kb0, kb1;
         kb_range(t, kb0, kb1);
         const bool swap = is_swap(ti);
+        // L2 prefetch of this CTA's weight box (k-block kbp of tile tp): the
+        // same coordinates as its load below, for the weight layouts read in
+        // one box per stage (K-contiguous e4m3, or bf16 viewed as 64-column blocks)
+        const int tn = t + work_stride;
+        TileInfo tin{};
+        int kb0n = 0, kb1n = 0;
+        if (p.b_prefetch > 0 && tn < total_tiles) {
+          tin = decode_tile<TILE_M>(ctrl, G, tn / p.ksplit, p.n_tiles, p.cols_per_tile);
+          kb_range(tn, kb0n, kb1n);
+        }
+        auto prefetch_b = [&](const TileInfo& tp, int kbp) {
+          if (PAIR && is_swap(tp)) return;  // swapped tails load other boxes
+          const bool shp = is_shared_group(tp.g);
+          const CUtensorMap* pm = shp ? &tmap_b2 : &tmap_b;
+          const int gp = shp ? 0 : tp.g;
+          const int r = static_cast<int>(rank);
+          if (Q8) {
+            if (EPI == kEpiGateUpAct) tma_prefetch_l2_4d(pm, kbp * KE, tp.n0, PAIR ? r : 0, gp);
+            else tma_prefetch_l2_3d(pm, kbp * KE, tp.n0 + (PAIR ? r * (p.bn / 2) : 0), gp);
+          } else if (!FP8 && p.b_wide) {
+            if (EPI == kEpiGateUpAct) tma_prefetch_l2_5d(pm, 0, kbp * BK, tp.n0 / 64, PAIR ? r : 0, gp);
+            else tma_prefetch_l2_4d(pm, 0, kbp * BK, tp.n0 / 64 + (PAIR ? r * nbox_cta : 0), gp);
+          }
+        };
         // swapped tail: each CTA loads its rows in 32-row boxes (the gate/up
         // pass: rows r * R/2 .. of the tile; the down pass: CTA 0 the h_hi rows,
         // CTA 1 the h_lo rows) and its 128 weight features
@@ -754,6 +781,11 @@ __global__ void __launch_bounds__(CPG ? 320 : StageCfg<SPLIT, FP8, PAIR>::kThrea
                 tma_load_3d(b_dst + j * B_BOX_BYTES, bmap, &ctrl->full[stage], ti.n0 + 64 * j,
                             kb * BK, gb, pol_b);
             }
+          }
+          if (p.b_prefetch > 0) {  // this CTA's weight box b_prefetch k-blocks ahead
+            const int kbp = kb + p.b_prefetch;
+            if (kbp < kb1) prefetch_b(ti, kbp);
+            else if (tn < total_tiles && kb0n + (kbp - kb1) < kb1n) prefetch_b(tin, kb0n + (kbp - kb1));
           }
           }  // lane 0
           fill_mask |= 1u << stage;
@@ -1994,6 +2026,7 @@ int g_pair_tiles = 3;      // set through moe_set_option(MOE_OPT_PAIR_TILES, .)
 int g_decode_kernel = 1;   // set through moe_set_option(MOE_OPT_DECODE_KERNEL, .)
 int g_pdl = 1;             // set through moe_set_option(MOE_OPT_PDL, .)
 int g_tile_order = 0;      // set through moe_set_option(MOE_OPT_TILE_ORDER, .)
+int g_b_prefetch = 0;      // set through moe_set_option(MOE_OPT_B_PREFETCH, .)
 
 namespace {
 
@@ -2051,6 +2084,7 @@ cudaError_t launch_grouped_gemm_decode_q8(const GroupedGemmArgs& a, int nt, cuda
   kp.comb_w = a.comb_w;
   kp.comb_k = a.comb_k;
   kp.lpt = g_tile_order == 1 && a.group_offsets != nullptr && a.G > 1;
+  kp.b_prefetch = g_b_prefetch;
   kp.sh_rows = a.sh_rows;
   kp.sh_b_scale = a.sh_b_scale;
   kp.bn = nt;
@@ -2121,6 +2155,7 @@ cudaError_t launch_grouped_gemm_decode(const GroupedGemmArgs& a, int nt, cudaStr
   kp.comb_w = a.comb_w;
   kp.comb_k = a.comb_k;
   kp.lpt = g_tile_order == 1 && a.group_offsets != nullptr && a.G > 1;
+  kp.b_prefetch = g_b_prefetch;
   kp.sh_rows = a.sh_rows;
   kp.sh_b_scale = a.sh_b_scale;
   kp.bn = nt;
@@ -2186,6 +2221,7 @@ cudaError_t launch_grouped_gemm_q8(const GroupedGemmArgs& a, cudaStream_t s) {
   kp.comb_w = a.comb_w;
   kp.comb_k = a.comb_k;
   kp.lpt = g_tile_order == 1 && a.group_offsets != nullptr && a.G > 1;
+  kp.b_prefetch = g_b_prefetch;
   kp.sh_rows = a.sh_rows;
   kp.sh_b_scale = a.sh_b_scale;
   kp.ksplit = 1;
@@ -2393,6 +2429,7 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
   kp.comb_w = a.comb_w;
   kp.comb_k = a.comb_k;
   kp.lpt = g_tile_order == 1 && a.group_offsets != nullptr && a.G > 1;
+  kp.b_prefetch = g_b_prefetch;
   kp.sh_rows = a.sh_rows;
   kp.sh_b_scale = a.sh_b_scale;
   {

@@ -317,6 +317,29 @@ int do_route(const moe_config_t* c, const void* x, const void* Wg, const float* 
                                          c->renormalize, ids, w, err, s));
 }
 
+// The permutation of the rows of x after init_routing (batches above the
+// one-launch size): x_perm[p] = x[sorted_rows[p] / k].
+int do_permute_rows(const moe_config_t* c, const void* x, const int32_t* sorted_rows,
+                    const int32_t* dest, const int32_t* offsets, void* x_perm, int32_t* err,
+                    cudaStream_t s, size_t row_bytes, const float* tok_scale, float* row_scale,
+                    int extra_rows) {
+  const int R = c->T * c->k;
+  trace_mark(s);
+  // x well inside L2: gather rows in permuted order (each token row re-read
+  // from L2 k times, the writes sequential); larger x: read each token row
+  // once and write its k copies (Qwen3.5-style prefill, 67 MB of x: 162 ->
+  // 117 us; Ling-style, 268 MB: 600 -> 388 us; Qwen3-style, 17 MB: 27.5 vs
+  // 28.8 us in favour of the gather)
+  cudaError_t e;
+  if (static_cast<size_t>(c->T) * row_bytes > (size_t{32} << 20))
+    e = launch_permute_scatter(x, dest, offsets + c->E, R, c->k, c->T, row_bytes, x_perm, err, s,
+                               tok_scale, row_scale, extra_rows);
+  else
+    e = launch_permute_gather(x, sorted_rows, R, c->k, c->T, row_bytes, x_perm, err, s, tok_scale,
+                              row_scale, extra_rows);
+  return cuda_status(e);
+}
+
 // row_bytes: bytes of one row of x (act_dtype rows, or moe_layer's fp8 row form)
 // extra_rows = T: x_perm rows R .. R+T-1 become copies of the tokens (the
 // shared expert's rows as the last group of the routed GEMMs).
@@ -342,21 +365,9 @@ int do_permute(const moe_config_t* c, const int32_t* ids, const void* x, int32_t
                             g_trace_next >= 0 ? trace_mark : nullptr);
   }
   if (e != cudaSuccess) return MOE_ERR_CUDA;
-  if (x && x_perm) {
-    trace_mark(s);
-    // x well inside L2: gather rows in permuted order (each token row re-read
-    // from L2 k times, the writes sequential); larger x: read each token row
-    // once and write its k copies (Qwen3.5-style prefill, 67 MB of x: 162 ->
-    // 117 us; Ling-style, 268 MB: 600 -> 388 us; Qwen3-style, 17 MB: 27.5 vs
-    // 28.8 us in favour of the gather)
-    if (static_cast<size_t>(c->T) * row_bytes > (size_t{32} << 20))
-      e = launch_permute_scatter(x, dest, offsets + c->E, R, c->k, c->T, row_bytes, x_perm, err, s,
-                                 tok_scale, row_scale, extra_rows);
-    else
-      e = launch_permute_gather(x, sorted_rows, R, c->k, c->T, row_bytes, x_perm, err, s, tok_scale,
-                                row_scale, extra_rows);
-    if (e != cudaSuccess) return MOE_ERR_CUDA;
-  }
+  if (x && x_perm)
+    return do_permute_rows(c, x, sorted_rows, dest, offsets, x_perm, err, s, row_bytes, tok_scale,
+                           row_scale, extra_rows);
   return MOE_OK;
 }
 
@@ -664,17 +675,26 @@ int moe_layer(const moe_config_t* cfg, const void* x, const void* Wg, const floa
   // trace events time kernels one after another on the caller's stream).
   const bool in_gemm = shared && shared_in_gemm_on(cfg);
   cudaStream_t side = nullptr;
-  if (shared && g_shared_stream && !traced && !in_gemm) {
+  // MOE_OPT_SHARED_STREAM 1: the side stream forks here, once x is ready;
+  // 2: after init_routing, so that the shared expert's GEMMs (which hold most
+  // of every SM's shared memory) start once the routing kernels (which need
+  // some too) are done, and run beside the permutation kernel (which needs none)
+  const bool want_side = shared && g_shared_stream && !traced && !in_gemm;
+  auto fork_shared = [&]() -> int {
     side = side_fork(s);
-    if (side) {
-      st = do_ffn(cfg, x_rows, tok_inv, cfg->T, nullptr, 1, W13s, s13s, W2s, s2s, cfg->I_shared, h_s,
-                  s_out, fp8 ? ws_at(ws, L.hs16) : nullptr,
-                  fp8 ? reinterpret_cast<float*>(ws_at(ws, L.hs_inv)) : nullptr, err, side);
-      if (st != MOE_OK) {
-        side_join(side, s);
-        return (g_trace_next = -1, st);
-      }
+    if (!side) return MOE_OK;  // no side stream: the shared expert runs on s below
+    const int r = do_ffn(cfg, x_rows, tok_inv, cfg->T, nullptr, 1, W13s, s13s, W2s, s2s,
+                         cfg->I_shared, h_s, s_out, fp8 ? ws_at(ws, L.hs16) : nullptr,
+                         fp8 ? reinterpret_cast<float*>(ws_at(ws, L.hs_inv)) : nullptr, err, side);
+    if (r != MOE_OK) {
+      side_join(side, s);
+      side = nullptr;
     }
+    return r;
+  };
+  if (want_side && g_shared_stream == 1) {
+    st = fork_shared();
+    if (st != MOE_OK) return (g_trace_next = -1, st);
   }
   // after the fork every early return first joins the side stream back
   auto fail = [&](int code) {
@@ -692,9 +712,22 @@ int moe_layer(const moe_config_t* cfg, const void* x, const void* Wg, const floa
   // request with TMA tile::gather4 loads (slower on GB300: 32 four-row
   // requests per 16 KB A tile).
   const bool gather = gather_mode(cfg) != 0;
-  st = do_permute(cfg, ids, gather ? nullptr : x_rows, counts, offsets, sorted_rows, dest,
-                  gather ? nullptr : x_perm, seg, err, s, layer_row_bytes(cfg), tok_inv, row_inv,
-                  in_gemm ? cfg->T : 0);
+  const bool late_fork = want_side && g_shared_stream == 2;
+  if (late_fork && !gather && !small_route(static_cast<long long>(cfg->T) * cfg->k, cfg->E)) {
+    // init_routing, the fork, then the permutation beside the shared GEMMs
+    st = do_permute(cfg, ids, nullptr, counts, offsets, sorted_rows, dest, nullptr, seg, err, s,
+                    layer_row_bytes(cfg));
+    if (st != MOE_OK) return fail(st);
+    st = fork_shared();
+    if (st != MOE_OK) return fail(st);
+    st = do_permute_rows(cfg, x_rows, sorted_rows, dest, offsets, x_perm, err, s, layer_row_bytes(cfg),
+                         tok_inv, row_inv, 0);
+  } else {
+    st = do_permute(cfg, ids, gather ? nullptr : x_rows, counts, offsets, sorted_rows, dest,
+                    gather ? nullptr : x_perm, seg, err, s, layer_row_bytes(cfg), tok_inv, row_inv,
+                    in_gemm ? cfg->T : 0);
+    if (st == MOE_OK && late_fork) st = fork_shared();
+  }
   if (st != MOE_OK) return fail(st);
   st = do_grouped_ffn(cfg, gather ? x_rows : x_perm, gather ? tok_inv : row_inv, offsets, W13, s13,
                       W2, s2, h, y_perm, (shared && !side) ? x_rows : nullptr, tok_inv, W13s, s13s,
@@ -775,7 +808,7 @@ int moe_set_option(int option, int value) {
     }
     case MOE_OPT_SHARED_STREAM: {
       const int old = g_shared_stream;
-      g_shared_stream = value ? 1 : 0;
+      g_shared_stream = value <= 0 ? 0 : value >= 2 ? 2 : 1;
       return old;
     }
     case MOE_OPT_PDL: {
@@ -791,6 +824,11 @@ int moe_set_option(int option, int value) {
     case MOE_OPT_TILE_ORDER: {
       const int old = g_tile_order;
       g_tile_order = value ? 1 : 0;
+      return old;
+    }
+    case MOE_OPT_B_PREFETCH: {
+      const int old = g_b_prefetch;
+      g_b_prefetch = value < 0 ? 0 : value > 16 ? 16 : value;
       return old;
     }
     case MOE_OPT_FUSED_ROUTING: {

@@ -246,6 +246,7 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s);
 extern int g_pair_tiles;
 extern int g_decode_kernel;
 extern int g_tile_order;
+extern int g_b_prefetch;  // moe_set_option(MOE_OPT_B_PREFETCH, .)
 
 // Shared helper: SM count of the current device (cached).
 int device_sm_count();

@@ -146,13 +146,18 @@ def test_set_option_values():
         (moe.MOE_OPT_PDL, 0, 0),
         (moe.MOE_OPT_PDL, 3, 1),
         (moe.MOE_OPT_SHARED_STREAM, 0, 0),
-        (moe.MOE_OPT_SHARED_STREAM, 2, 1),
+        (moe.MOE_OPT_SHARED_STREAM, 2, 2),
+        (moe.MOE_OPT_SHARED_STREAM, 5, 2),
+        (moe.MOE_OPT_SHARED_STREAM, 1, 1),
         (moe.MOE_OPT_FUSED_COMBINE, 5, 1),
         (moe.MOE_OPT_FUSED_COMBINE, 0, 0),
         (moe.MOE_OPT_TILE_ORDER, 3, 1),
         (moe.MOE_OPT_TILE_ORDER, 0, 0),
         (moe.MOE_OPT_SHARED_IN_GEMM, 4, 1),
         (moe.MOE_OPT_SHARED_IN_GEMM, 0, 0),
+        (moe.MOE_OPT_B_PREFETCH, 4, 4),
+        (moe.MOE_OPT_B_PREFETCH, 99, 16),
+        (moe.MOE_OPT_B_PREFETCH, -2, 0),
         (moe.MOE_OPT_FUSED_ROUTING, 0, 0),
         (moe.MOE_OPT_FUSED_ROUTING, 2, 1),
     ]

@@ -201,21 +201,52 @@ def test_layer_same_result_without_pdl(case, pair):
         moe.moe_set_option(moe.MOE_OPT_PAIR_TILES, old_pair)
 
 
-@pytest.mark.parametrize("case", ["gemma4_T256", "gemma4_T8_decode", "fp8_small_T300",
-                                  "fp8_small_geglu_T77", "qwen35_T64"])
-def test_layer_same_result_with_shared_expert_stream(case):
-    """The shared expert on the library's side stream (default) and on the
-    caller's stream give bit-identical outputs, over repeated calls."""
-    shape = LAYER_CASES[case]
+SIDE_CASES = {
+    **{c: (LAYER_CASES[c], "kn") for c in ["gemma4_T256", "gemma4_T8_decode", "fp8_small_T300",
+                                            "fp8_small_geglu_T77", "qwen35_T64"]},
+    # more than 8192 expanded rows and the permutation kernel: the late fork
+    # comes between init_routing and the permutation
+    "qwen35_T1024": (C["qwen35_prefill"].with_tokens(1024), "kn"),
+    "ling_T1100_nk": (C["ling_prefill"].with_tokens(1100), "nk"),
+}
+
+
+@pytest.mark.parametrize("fork", [1, 2])
+@pytest.mark.parametrize("case", sorted(SIDE_CASES))
+def test_layer_same_result_with_shared_expert_stream(case, fork):
+    """The shared expert on the library's side stream, forked once x is ready
+    (1, default) or after init_routing (2), and on the caller's stream give
+    bit-identical outputs, over repeated calls."""
+    shape, layout = SIDE_CASES[case]
     inp = workloads.make_inputs(shape, seed=7, device="cuda")
     old = moe.moe_set_option(moe.MOE_OPT_SHARED_STREAM, 0)
     try:
-        serial = run_layer(shape, inp)["out"].clone()
-        moe.moe_set_option(moe.MOE_OPT_SHARED_STREAM, 1)
+        serial = run_layer(shape, inp, layout)["out"].clone()
+        moe.moe_set_option(moe.MOE_OPT_SHARED_STREAM, fork)
         for _ in range(3):
-            assert torch.equal(run_layer(shape, inp)["out"], serial)
+            assert torch.equal(run_layer(shape, inp, layout)["out"], serial)
     finally:
         moe.moe_set_option(moe.MOE_OPT_SHARED_STREAM, old)
+
+
+@pytest.mark.parametrize("dist", [2, 7])
+@pytest.mark.parametrize("case,layout,pair", [
+    ("qwen3_T512", "kn", 3),       # bf16: the routed gate/up pass gathers its rows; 2-CTA down pass
+    ("qwen3_T512", "kn", 0),       # bf16 on one-CTA tiles
+    ("gemma4_T256", "kn", 1),      # bf16 2-CTA tiles with swapped tails
+    ("fp8_small_T300", "nk", 1),   # K-contiguous e4m3 weights, 2-CTA tiles
+    ("fp8_small_T300", "nk", 0),
+])
+def test_layer_parity_weight_prefetch(case, layout, pair, dist):
+    """MOE_OPT_B_PREFETCH: the producer's L2 prefetch of weight boxes ahead
+    (into the next tile near a tile's end) leaves the results unchanged."""
+    old = moe.moe_set_option(moe.MOE_OPT_B_PREFETCH, dist)
+    old_pair = moe.moe_set_option(moe.MOE_OPT_PAIR_TILES, pair)
+    try:
+        check_layer(LAYER_CASES[case], layout=layout)
+    finally:
+        moe.moe_set_option(moe.MOE_OPT_B_PREFETCH, old)
+        moe.moe_set_option(moe.MOE_OPT_PAIR_TILES, old_pair)
 
 
 @pytest.mark.parametrize("mode", [1, 2])
