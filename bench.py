@@ -350,6 +350,8 @@ def set_options(moe, args):
         moe.moe_set_option(moe.MOE_OPT_FUSED_COMBINE, 1)
     if getattr(args, "b_prefetch", None) is not None:
         moe.moe_set_option(moe.MOE_OPT_B_PREFETCH, args.b_prefetch)
+    if getattr(args, "dynamic_tiles", None) is not None:
+        moe.moe_set_option(moe.MOE_OPT_DYNAMIC_TILES, args.dynamic_tiles)
     if getattr(args, "split_routing", False):
         moe.moe_set_option(moe.MOE_OPT_FUSED_ROUTING, 0)
     if args.lpt:
@@ -733,6 +735,8 @@ def main():
                     help="plain stream order instead of programmatic dependent launch (MOE_OPT_PDL 0)")
     ap.add_argument("--b-prefetch", type=int, default=None,
                     help="weight boxes prefetched into L2 this many k-blocks ahead (MOE_OPT_B_PREFETCH)")
+    ap.add_argument("--dynamic-tiles", type=int, default=None, choices=[0, 1],
+                    help="grouped GEMM tiles handed out by an atomic counter (MOE_OPT_DYNAMIC_TILES)")
     ap.add_argument("--split-routing", action="store_true",
                     help="router projection and top-k, histogram and scatter as separate launches "
                          "(MOE_OPT_FUSED_ROUTING 0)")

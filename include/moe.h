@@ -15,7 +15,8 @@
  *   caller.  The library allocates no device memory; scratch space comes from
  *   the caller's workspace `ws` of at least moe_workspace_size(cfg) bytes
  *   (256-byte aligned).  The first 256 bytes of `ws` are a control block that
- *   holds the device error word.
+ *   holds the device error word (and, with MOE_OPT_DYNAMIC_TILES, the GEMMs'
+ *   tile counters).
  * - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call is
  *   asynchronous on that stream and returns after enqueueing its kernels.
  *   The compute calls enqueue only kernels and event records / waits (no
@@ -412,6 +413,19 @@ int moe_layer_launch_count(const moe_config_t* cfg);
  *   read in one box per stage (bf16 as 64-column blocks, K-contiguous e4m3).
  *   0 (default) = off; at most 16.  Same results. */
 #define MOE_OPT_B_PREFETCH 11
+/*   MOE_OPT_DYNAMIC_TILES: the persistent grouped GEMMs (128-row and 2-CTA
+ *   tiles) can hand out their tiles dynamically: each CTA's producer (the
+ *   leader's, in a pair) takes tiles from a counter in the workspace's
+ *   control block with an atomic add and passes them to the CTA's (pair's)
+ *   other roles through a small queue in shared memory, one tile ahead, so
+ *   that CTAs whose tiles run faster take more of them; the calls that launch
+ *   those GEMMs zero the counters first (one memset).  2 (default) = for the
+ *   gate/up passes whose tiles are at least 64 k-blocks long (D >= 4096 for
+ *   bf16 weights, D >= 8192 for K-contiguous e4m3 weights; Ling-style prefill
+ *   layer 11.35-11.39 -> 11.04-11.07 ms on GB300); 1 = every pass (the short
+ *   down-pass tiles measured 3-8 % slower); 0 = tile t to CTA (pair) t modulo
+ *   the grid.  Same results. */
+#define MOE_OPT_DYNAMIC_TILES 12
 int moe_set_option(int option, int value);
 
 /* Per-kernel timing hook (process-wide, off by default).  `events` holds

@@ -75,6 +75,7 @@ MOE_OPT_TILE_ORDER = 7
 MOE_OPT_SHARED_IN_GEMM = 9
 MOE_OPT_FUSED_ROUTING = 10
 MOE_OPT_B_PREFETCH = 11
+MOE_OPT_DYNAMIC_TILES = 12
 
 
 def load_library(path: Optional[str] = None) -> ctypes.CDLL:

@@ -76,6 +76,7 @@ constexpr int EPI_STAGE_BYTES = 4 * EPI_STAGE_FLOATS * 4;
 // group when it runs inside the routed GEMMs
 constexpr int MAX_G = 513;
 constexpr uint32_t TMEM_COLS = 512;
+constexpr int TQ_DEPTH = 4;  // tile indices in flight between the producer and the other roles
 constexpr uint32_t ACC_STRIDE = 256;  // TMEM columns per accumulator buffer
 
 constexpr int RAW_BOX_BYTES = 128 * BK;        // one 128-column x 64-row e4m3 box, 8 KB
@@ -112,6 +113,10 @@ struct Ctrl {
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t xch_full, xch_empty;  // decode gate/up epilogue: up values staged / consumed
+  // dynamic tile order: the tile indices handed to every role of the CTA (pair)
+  uint64_t tq_full[TQ_DEPTH];
+  uint64_t tq_empty[TQ_DEPTH];
+  int tq[TQ_DEPTH];
   uint32_t tmem_slot;
   int abort;
   // the schedule's groups in the order their tiles run: position i holds
@@ -178,6 +183,10 @@ struct KParams {
   // store pass (one plane, no bias): full 32-row warp chunks leave through
   // TMA bulk-tensor stores (tmap_out: the [M, N] output, 128-byte rows per box)
   int tma_out;
+  // dynamic tile order: a global counter, zero before the launch, from which
+  // the producer of each CTA (the leader of each pair) takes its next tile;
+  // nullptr = static round-robin (tile t to CTA / pair t mod grid)
+  int32_t* tile_counter;
 };
 
 // Fused combine: the token and routing weight of permuted output row `row`.
@@ -490,6 +499,14 @@ __global__ void __launch_bounds__(CPG ? 320 : StageCfg<SPLIT, FP8, PAIR>::kThrea
     }
     mbar_init(&ctrl->xch_full, 64);   // swapped gate/up tail: the 64 up-feature threads
     mbar_init(&ctrl->xch_empty, 64);  // ... and the 64 gate-feature threads
+    // tile queue: filled by the leader's producer; emptied by the MMA thread,
+    // the 4 epilogue warps and the gather / converter warps of a one-CTA tile,
+    // or, in a pair, by the leader's MMA thread and epilogue warps and the
+    // peer's producer warp and epilogue warps (all on the leader's barrier)
+    for (int q = 0; q < TQ_DEPTH; ++q) {
+      mbar_init(&ctrl->tq_full[q], 1);
+      mbar_init(&ctrl->tq_empty[q], PAIR ? 10 : 5 + (CPG ? 4 : FP8 ? Cfg::kConvWarps : 0));
+    }
     ctrl->abort = 0;
     fence_mbarrier_init();
   }
@@ -529,10 +546,97 @@ __global__ void __launch_bounds__(CPG ? 320 : StageCfg<SPLIT, FP8, PAIR>::kThrea
     kb0 = (t % p.ksplit) * p.kbs;
     kb1 = min(KB, kb0 + p.kbs);
   };
-  const int nbox = p.bn / 64;
-  const int nbox_cta = PAIR ? nbox / 2 : nbox;  // bf16 B boxes this CTA loads
   // barrier addresses in the leader CTA (cluster window) for the pair protocol
   auto leader_bar = [&](uint64_t* bar) { return PAIR ? mapa_shared(bar, 0) : smem_u32(bar); };
+  // ---------------------------------------------------------------- tile order
+  // Static: this CTA (pair) takes tiles work0, work0 + work_stride, ...
+  // Dynamic (p.tile_counter): the leader's producer takes each next tile from
+  // the global counter (one tile ahead, so that the atomic's latency stays off
+  // the load path) and hands it to every role of the CTA (pair) through a
+  // ring of TQ_DEPTH slots; an index >= total_tiles ends every role's loop.
+  const bool dyn = p.tile_counter != nullptr;
+  struct Cursor {
+    int t;
+    int ahead;  // publisher: published, runs next
+    int pend;   // publisher: taken from the counter, published at the next tile
+    uint32_t qs, qph;
+    bool started;
+  };
+  auto cursor = [&]() { return Cursor{0, 0, 0, 0u, 0u, false}; };
+  // consumer: a whole warp (every lane waits, lane 0 arrives) or one thread
+  auto next_tile = [&](Cursor& c, bool whole_warp) -> int {
+    if (!dyn) {
+      c.t = c.started ? c.t + work_stride : work0;
+      c.started = true;
+      return c.t;
+    }
+    const bool got = PAIR ? mbar_wait_cluster(&ctrl->tq_full[c.qs], c.qph, abort_flag)
+                          : mbar_wait(&ctrl->tq_full[c.qs], c.qph, abort_flag);
+    int t = -1;
+    if (got) t = *reinterpret_cast<volatile int*>(&ctrl->tq[c.qs]);
+    if (whole_warp) __syncwarp();
+    if (got && (!whole_warp || lane == 0)) {
+      if (PAIR) mbar_arrive_cluster(leader_bar(&ctrl->tq_empty[c.qs]));
+      else mbar_arrive(&ctrl->tq_empty[c.qs]);
+    }
+    if (++c.qs == TQ_DEPTH) {
+      c.qs = 0;
+      c.qph ^= 1u;
+    }
+    return t;  // -1: a wait gave up
+  };
+  // one slot of the queue, in this CTA and (pair) the peer; lane 0 only
+  auto push_tile = [&](Cursor& c, int t) -> bool {
+    const bool ok = PAIR ? mbar_wait_cluster(&ctrl->tq_empty[c.qs], c.qph ^ 1u, abort_flag)
+                         : mbar_wait(&ctrl->tq_empty[c.qs], c.qph ^ 1u, abort_flag);
+    if (ok) {
+      ctrl->tq[c.qs] = t;
+      mbar_arrive(&ctrl->tq_full[c.qs]);
+      if (PAIR) {  // the peer's copy of the slot, then its barrier (release.cluster)
+        st_cluster_s32(mapa_shared(&ctrl->tq[c.qs], 1), t);
+        mbar_arrive_cluster(mapa_shared(&ctrl->tq_full[c.qs], 1));
+      }
+    }
+    if (++c.qs == TQ_DEPTH) {
+      c.qs = 0;
+      c.qph ^= 1u;
+    }
+    return ok;
+  };
+  // publisher (the leader's producer warp; lane 0 takes tiles and publishes):
+  // the queue always holds the tile after the current one, so the other roles
+  // (the peer's above all) never wait for an index at a tile boundary, and the
+  // atomic for the tile after that is in flight while the current tile loads
+  auto publish_tile = [&](Cursor& c) -> int {
+    if (!dyn) return next_tile(c, true);
+    bool ok = true;
+    if (lane == 0) {
+      if (!c.started) {
+        c.started = true;
+        c.t = atomicAdd(p.tile_counter, 1);
+        ok = push_tile(c, c.t);
+        c.ahead = total_tiles;
+        if (ok && c.t < total_tiles) {
+          c.ahead = atomicAdd(p.tile_counter, 1);
+          ok = push_tile(c, c.ahead);
+          if (ok && c.ahead < total_tiles) c.pend = atomicAdd(p.tile_counter, 1);
+        }
+      } else {
+        c.t = c.ahead;
+        if (c.t < total_tiles) {  // the pending tile was taken when this one was published
+          ok = push_tile(c, c.pend);
+          c.ahead = c.pend;
+          if (ok && c.ahead < total_tiles) c.pend = atomicAdd(p.tile_counter, 1);
+        }
+      }
+    }
+    const int t = __shfl_sync(0xffffffffu, c.t, 0);
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    return ok ? t : -1;
+  };
+
+  const int nbox = p.bn / 64;
+  const int nbox_cta = PAIR ? nbox / 2 : nbox;  // bf16 B boxes this CTA loads
   // swapped tail tile (2-CTA mode): the rows are the MMA N operand.  With a
   // split A (bf16 h_hi / h_lo, or two-term e4m3 rows) CTA 0 loads the first
   // plane of the rows and CTA 1 the second, stacked along N (N = 2 x rows
@@ -574,7 +678,16 @@ __global__ void __launch_bounds__(CPG ? 320 : StageCfg<SPLIT, FP8, PAIR>::kThrea
       // (for the drain after an abort)
       uint32_t fill_mask = 0, fill_par = 0;
       bool ok = true;
-      for (int t = work0; t < total_tiles && ok; t += work_stride) {
+      Cursor cur = cursor();
+      auto next_p = [&]() { return leader ? publish_tile(cur) : next_tile(cur, true); };
+      for (;;) {
+        if (!ok) break;
+        const int t = next_p();
+        if (t < 0) {
+          ok = false;
+          break;
+        }
+        if (t >= total_tiles) break;
         const TileInfo ti = decode_tile<TILE_M>(ctrl, G, t / p.ksplit, p.n_tiles, p.cols_per_tile);
         const int my_row0 = ti.row0 + static_cast<int>(rank) * BM;
         // the group's weights: the routed tensor at coordinate g, or the shared
@@ -600,7 +713,7 @@ __global__ void __launch_bounds__(CPG ? 320 : StageCfg<SPLIT, FP8, PAIR>::kThrea
         // L2 prefetch of this CTA's weight box (k-block kbp of tile tp): the
         // same coordinates as its load below, for the weight layouts read in
         // one box per stage (K-contiguous e4m3, or bf16 viewed as 64-column blocks)
-        const int tn = t + work_stride;
+        const int tn = dyn ? total_tiles : t + work_stride;  // the next tile, when known
         TileInfo tin{};
         int kb0n = 0, kb1n = 0;
         if (p.b_prefetch > 0 && tn < total_tiles) {
@@ -819,7 +932,15 @@ __global__ void __launch_bounds__(CPG ? 320 : StageCfg<SPLIT, FP8, PAIR>::kThrea
                                  : make_idesc_bf16_f32(TILE_M, p.bn, 0, 1);
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
-      for (int t = work0; t < total_tiles && ok; t += work_stride) {
+      Cursor cur = cursor();
+      for (;;) {
+        if (!ok) break;
+        const int t = next_tile(cur, false);
+        if (t < 0) {
+          ok = false;
+          break;
+        }
+        if (t >= total_tiles) break;
         if (!mbar_wait(&ctrl->tempty[acc], acc_phase ^ 1u, abort_flag)) {
           ok = false;
           break;
@@ -957,7 +1078,15 @@ __global__ void __launch_bounds__(CPG ? 320 : StageCfg<SPLIT, FP8, PAIR>::kThrea
       const __nv_bfloat16* src_base = static_cast<const __nv_bfloat16*>(p.a_src);
       uint32_t stage = 0, phase = 0;
       bool ok = true;
-      for (int t = work0; t < total_tiles && ok; t += work_stride) {
+      Cursor cur = cursor();
+      for (;;) {
+        if (!ok) break;
+        const int t = next_tile(cur, true);
+        if (t < 0) {
+          ok = false;
+          break;
+        }
+        if (t >= total_tiles) break;
         const TileInfo ti = decode_tile<TILE_M>(ctrl, G, t / p.ksplit, p.n_tiles, p.cols_per_tile);
         const __nv_bfloat16* src_row[8];
         uint32_t live = 0;  // bit j: row 32 gw + 4 j + lane / 8 is inside the group
@@ -1024,7 +1153,15 @@ __global__ void __launch_bounds__(CPG ? 320 : StageCfg<SPLIT, FP8, PAIR>::kThrea
       }
       uint32_t stage = 0, phase = 0;
       bool ok = true;
-      for (int t = work0; t < total_tiles && ok; t += work_stride) {
+      Cursor cur = cursor();
+      for (;;) {
+        if (!ok) break;
+        const int t = next_tile(cur, true);
+        if (t < 0) {
+          ok = false;
+          break;
+        }
+        if (t >= total_tiles) break;
         int kb0, kb1;
         kb_range(t, kb0, kb1);
         for (int kb = kb0; kb < kb1; ++kb) {
@@ -1071,7 +1208,17 @@ __global__ void __launch_bounds__(CPG ? 320 : StageCfg<SPLIT, FP8, PAIR>::kThrea
     const int quarter = warp & 3;  // TMEM lanes [32*quarter, 32*quarter + 32)
     const int row_in_tile = quarter * 32 + lane;
     uint32_t acc = 0, acc_phase = 0, xch_phase = 0;
-    for (int t = work0; t < total_tiles; t += work_stride) {
+    Cursor cur = cursor();
+    for (;;) {
+      const int t = next_tile(cur, true);
+      if (t < 0) {
+        if (lane == 0) {
+          ctrl->abort = 1;
+          atomicOr(p.err, MOE_DEV_WAIT_TIMEOUT);
+        }
+        break;
+      }
+      if (t >= total_tiles) break;
       TileInfo ti = decode_tile<TILE_M>(ctrl, G, t / p.ksplit, p.n_tiles, p.cols_per_tile);
       ti.row0 += static_cast<int>(rank) * BM;  // this CTA's 128 rows of the tile
       ti.rows -= static_cast<int>(rank) * BM;
@@ -2084,6 +2231,7 @@ cudaError_t launch_grouped_gemm_decode_q8(const GroupedGemmArgs& a, int nt, cuda
   kp.comb_w = a.comb_w;
   kp.comb_k = a.comb_k;
   kp.lpt = g_tile_order == 1 && a.group_offsets != nullptr && a.G > 1;
+  kp.tile_counter = a.tile_counter;
   kp.b_prefetch = g_b_prefetch;
   kp.sh_rows = a.sh_rows;
   kp.sh_b_scale = a.sh_b_scale;
@@ -2155,6 +2303,7 @@ cudaError_t launch_grouped_gemm_decode(const GroupedGemmArgs& a, int nt, cudaStr
   kp.comb_w = a.comb_w;
   kp.comb_k = a.comb_k;
   kp.lpt = g_tile_order == 1 && a.group_offsets != nullptr && a.G > 1;
+  kp.tile_counter = a.tile_counter;
   kp.b_prefetch = g_b_prefetch;
   kp.sh_rows = a.sh_rows;
   kp.sh_b_scale = a.sh_b_scale;
@@ -2221,6 +2370,7 @@ cudaError_t launch_grouped_gemm_q8(const GroupedGemmArgs& a, cudaStream_t s) {
   kp.comb_w = a.comb_w;
   kp.comb_k = a.comb_k;
   kp.lpt = g_tile_order == 1 && a.group_offsets != nullptr && a.G > 1;
+  kp.tile_counter = a.tile_counter;
   kp.b_prefetch = g_b_prefetch;
   kp.sh_rows = a.sh_rows;
   kp.sh_b_scale = a.sh_b_scale;
@@ -2429,6 +2579,7 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
   kp.comb_w = a.comb_w;
   kp.comb_k = a.comb_k;
   kp.lpt = g_tile_order == 1 && a.group_offsets != nullptr && a.G > 1;
+  kp.tile_counter = a.tile_counter;
   kp.b_prefetch = g_b_prefetch;
   kp.sh_rows = a.sh_rows;
   kp.sh_b_scale = a.sh_b_scale;

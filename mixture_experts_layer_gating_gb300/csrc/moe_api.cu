@@ -19,6 +19,7 @@ int g_shared_stream = 1;  // moe_set_option(MOE_OPT_SHARED_STREAM, .)
 int g_fused_combine = 0;  // moe_set_option(MOE_OPT_FUSED_COMBINE, .)
 int g_shared_in_gemm = 0;  // moe_set_option(MOE_OPT_SHARED_IN_GEMM, .)
 int g_fused_routing = 1;  // moe_set_option(MOE_OPT_FUSED_ROUTING, .)
+int g_dynamic_tiles = 2;  // moe_set_option(MOE_OPT_DYNAMIC_TILES, .)
 
 // The shared expert depends on x alone, so moe_layer runs it on a second
 // stream of the library's own (one per device, created on first use) that
@@ -238,6 +239,15 @@ int check_ws(const moe_config_t* c, void* ws, size_t ws_bytes) {
 }
 
 inline int32_t* err_word(void* ws) { return &static_cast<ControlBlock*>(ws)->err; }
+// The four tile counters of the control block (dynamic tile order), or null.
+inline int32_t* tile_counters(void* ws) {
+  return g_dynamic_tiles ? static_cast<ControlBlock*>(ws)->reserved + kTileCounterSlot : nullptr;
+}
+// Zeroes them on s before a call's first grouped GEMM (nothing when off).
+inline cudaError_t zero_tile_counters(void* ws, cudaStream_t s) {
+  int32_t* c = tile_counters(ws);
+  return c ? cudaMemsetAsync(c, 0, 4 * sizeof(int32_t), s) : cudaSuccess;
+}
 inline uint8_t* ws_at(void* ws, size_t off) { return static_cast<uint8_t*>(ws) + off; }
 
 inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
@@ -385,7 +395,7 @@ int do_ffn(const moe_config_t* c, const void* A, const float* a_row_scale, int M
            cudaStream_t s, const int32_t* a_gather = nullptr, int a_rows = 0,
            const int32_t* comb_rows = nullptr, const float* comb_w = nullptr, int sh_rows = 0,
            const void* W13s = nullptr, const float* s13s = nullptr, const void* W2s = nullptr,
-           const float* s2s = nullptr) {
+           const float* s2s = nullptr, int32_t* counters = nullptr) {
   if (M <= 0) return MOE_OK;
   cudaError_t e;
   trace_mark(s);
@@ -435,6 +445,12 @@ int do_ffn(const moe_config_t* c, const void* A, const float* a_row_scale, int M
   a.sh_rows = sh_rows;  // > 0: the last group is the shared expert (its own weights)
   a.sh_B = W13s;
   a.sh_b_scale = s13s;
+  // counters[0]: gate/up pass, counters[1]: down pass (MOE_OPT_DYNAMIC_TILES:
+  // 1 = both; 2, the default = the gate/up pass when its tiles are at least 64
+  // k-blocks long -- there the balance pays for the queue, which costs the
+  // short tiles of the down passes more than it saves)
+  const int kblocks = c->D / ((nk || is_a8(c)) ? 128 : 64);
+  a.tile_counter = (counters && (g_dynamic_tiles == 1 || kblocks >= 64)) ? counters : nullptr;
   e = launch_grouped_gemm(a, s);
   if (e != cudaSuccess) return e == cudaErrorNotSupported ? MOE_ERR_UNSUPPORTED : MOE_ERR_CUDA;
   if (fp8) {
@@ -458,6 +474,7 @@ int do_ffn(const moe_config_t* c, const void* A, const float* a_row_scale, int M
   b.out_lo = nullptr;
   b.sh_B = W2s;
   b.sh_b_scale = s2s;
+  b.tile_counter = (counters && g_dynamic_tiles == 1) ? counters + 1 : nullptr;
   if (comb_rows) {
     b.epilogue = kEpiCombineF32;
     b.comb_rows = comb_rows;
@@ -490,17 +507,19 @@ int do_grouped_ffn(const moe_config_t* c, const void* x_perm, const float* xp_sc
     return do_ffn(c, x_perm, xp_scale, R + c->T, offsets, c->E + 1, W13, s13, W2, s2, c->I, h, y_perm,
                   fp8 ? ws_at(ws, L.h16) : nullptr,
                   fp8 ? reinterpret_cast<float*>(ws_at(ws, L.h_inv)) : nullptr, err, s, nullptr, 0,
-                  comb_rows, comb_w, c->T, W13s, s13s, W2s, s2s);
+                  comb_rows, comb_w, c->T, W13s, s13s, W2s, s2s, tile_counters(ws));
   }
+  int32_t* ctr = tile_counters(ws);
   int st = do_ffn(c, x_perm, xp_scale, R, offsets, c->E, W13, s13, W2, s2, c->I, h, y_perm,
                   fp8 ? ws_at(ws, L.h16) : nullptr,
                   fp8 ? reinterpret_cast<float*>(ws_at(ws, L.h_inv)) : nullptr, err, s, gather,
-                  gather ? c->T : 0, comb_rows, comb_w);
+                  gather ? c->T : 0, comb_rows, comb_w, 0, nullptr, nullptr, nullptr, nullptr, ctr);
   if (st != MOE_OK) return st;
   if (x && c->I_shared > 0)
     st = do_ffn(c, x, x_scale, c->T, nullptr, 1, W13s, s13s, W2s, s2s, c->I_shared, h_s, s_out,
                 fp8 ? ws_at(ws, L.hs16) : nullptr,
-                fp8 ? reinterpret_cast<float*>(ws_at(ws, L.hs_inv)) : nullptr, err, s);
+                fp8 ? reinterpret_cast<float*>(ws_at(ws, L.hs_inv)) : nullptr, err, s, nullptr, 0,
+                nullptr, nullptr, 0, nullptr, nullptr, nullptr, nullptr, ctr ? ctr + 2 : nullptr);
   return st;
 }
 
@@ -576,6 +595,7 @@ int moe_grouped_ffn(const moe_config_t* cfg, const void* x_perm, const int32_t* 
   }
   if (cfg->T == 0) return MOE_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (zero_tile_counters(ws, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (is_fp8(cfg)) {
     // fp8 weights: convert the bf16 rows to fp16 rows (or two-term e4m3 rows)
     // with exact power-of-two scales in the workspace first
@@ -656,6 +676,7 @@ int moe_layer(const moe_config_t* cfg, const void* x, const void* Wg, const floa
   const bool fused = fused_combine_on(cfg);
   if (fused && cudaMemsetAsync(y_perm, 0, static_cast<size_t>(cfg->T) * cfg->D * 4, s) != cudaSuccess)
     return (g_trace_next = -1, MOE_ERR_CUDA);
+  if (zero_tile_counters(ws, s) != cudaSuccess) return (g_trace_next = -1, MOE_ERR_CUDA);
   const void* x_rows = x;  // what the gather and the shared expert read
   float* tok_inv = nullptr;
   float* row_inv = nullptr;
@@ -683,9 +704,12 @@ int moe_layer(const moe_config_t* cfg, const void* x, const void* Wg, const floa
   auto fork_shared = [&]() -> int {
     side = side_fork(s);
     if (!side) return MOE_OK;  // no side stream: the shared expert runs on s below
+    int32_t* ctr = tile_counters(ws);
     const int r = do_ffn(cfg, x_rows, tok_inv, cfg->T, nullptr, 1, W13s, s13s, W2s, s2s,
                          cfg->I_shared, h_s, s_out, fp8 ? ws_at(ws, L.hs16) : nullptr,
-                         fp8 ? reinterpret_cast<float*>(ws_at(ws, L.hs_inv)) : nullptr, err, side);
+                         fp8 ? reinterpret_cast<float*>(ws_at(ws, L.hs_inv)) : nullptr, err, side,
+                         nullptr, 0, nullptr, nullptr, 0, nullptr, nullptr, nullptr, nullptr,
+                         ctr ? ctr + 2 : nullptr);
     if (r != MOE_OK) {
       side_join(side, s);
       side = nullptr;
@@ -824,6 +848,11 @@ int moe_set_option(int option, int value) {
     case MOE_OPT_TILE_ORDER: {
       const int old = g_tile_order;
       g_tile_order = value ? 1 : 0;
+      return old;
+    }
+    case MOE_OPT_DYNAMIC_TILES: {
+      const int old = g_dynamic_tiles;
+      g_dynamic_tiles = value <= 0 ? 0 : value >= 2 ? 2 : 1;
       return old;
     }
     case MOE_OPT_B_PREFETCH: {

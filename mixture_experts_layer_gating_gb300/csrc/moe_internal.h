@@ -17,6 +17,10 @@ struct ControlBlock {
   int32_t reserved[63];
 };
 static_assert(sizeof(ControlBlock) == 256, "control block is 256 bytes");
+// reserved[kTileCounterSlot .. + 3]: the tile counters of the routed gate/up
+// and down GEMMs and of the shared expert's two GEMMs (dynamic tile order),
+// zeroed by the call that launches them before its first kernel
+constexpr int kTileCounterSlot = 7;
 
 // ------------------------------------------------- programmatic dependent launch
 // Every kernel of the library starts with pdl_wait() (griddepcontrol.wait:
@@ -238,6 +242,9 @@ struct GroupedGemmArgs {
   int sh_rows;
   const void* sh_B;
   const float* sh_b_scale;
+  // dynamic tile order (moe_set_option(MOE_OPT_DYNAMIC_TILES, 1)): a counter
+  // that is zero when the launch starts; nullptr = static round-robin order
+  int32_t* tile_counter;
 };
 
 cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s);

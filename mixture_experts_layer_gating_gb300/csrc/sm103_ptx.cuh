@@ -70,6 +70,34 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   }
 }
 
+// mbar_wait with cluster-scope acquire: for a barrier that threads of another
+// CTA of the cluster arrive on (release.cluster) after writing data this
+// thread reads next.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar_addr, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar_addr), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity,
+                                                  volatile int* abort_flag) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try_wait_cluster(a, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait_cluster(a, parity)) return true;
+    if ((i & 255u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    }
+  }
+}
+
 // After an abort: waits at most kDrainLimitNs for a phase whose copies may
 // still be in flight (ignores the abort flag; gives up silently).
 constexpr uint64_t kDrainLimitNs = 10000000ull;  // 10 ms
@@ -278,6 +306,11 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_
   asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b),
                "r"(c), "r"(d)
                : "memory");
+}
+// 4-byte store to a shared::cluster address (possibly another CTA's shared
+// memory).
+__device__ __forceinline__ void st_cluster_s32(uint32_t addr, int32_t v) {
+  asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 // 4-byte load from a shared::cluster address (possibly another CTA's shared
 // memory).

@@ -158,6 +158,9 @@ def test_set_option_values():
         (moe.MOE_OPT_B_PREFETCH, 4, 4),
         (moe.MOE_OPT_B_PREFETCH, 99, 16),
         (moe.MOE_OPT_B_PREFETCH, -2, 0),
+        (moe.MOE_OPT_DYNAMIC_TILES, 3, 2),
+        (moe.MOE_OPT_DYNAMIC_TILES, 1, 1),
+        (moe.MOE_OPT_DYNAMIC_TILES, 0, 0),
         (moe.MOE_OPT_FUSED_ROUTING, 0, 0),
         (moe.MOE_OPT_FUSED_ROUTING, 2, 1),
     ]

@@ -229,6 +229,45 @@ def test_layer_same_result_with_shared_expert_stream(case, fork):
         moe.moe_set_option(moe.MOE_OPT_SHARED_STREAM, old)
 
 
+DYN_CASES = [
+    # case, layout, pair-tile policy, gather policy
+    ("qwen3_T512", "kn", 3, 3),         # bf16: cp.async row gather (one-CTA tiles), 2-CTA down pass
+    ("qwen3_T512", "kn", 0, 0),         # bf16 one-CTA tiles, permuted copy
+    ("qwen3_T512", "kn", 1, 0),         # bf16 2-CTA tiles with swapped tails, both passes
+    ("gemma4_T256", "kn", 1, 0),        # GEGLU + dense MLP on 2-CTA tiles
+    ("qwen35_T64", "kn", 0, 0),         # shared expert, 128-row tiles
+    ("fp8_small_T300", "kn", 0, 0),     # fp8 weights expanded on chip (converter warps)
+    ("fp8_small_T300", "nk", 1, 0),     # K-contiguous e4m3 weights, 2-CTA tiles
+    ("fp8_small_T300", "nk", 0, 0),
+    ("fp8_small_geglu_T77", "nk", 1, 0),
+]
+
+
+@pytest.mark.parametrize("case,layout,pair,gather", DYN_CASES)
+def test_layer_dynamic_tiles_same_result(case, layout, pair, gather):
+    """MOE_OPT_DYNAMIC_TILES: tiles handed out by an atomic counter through
+    the shared-memory tile queue give the layer bit for bit (every tile is
+    computed the same way whichever CTA takes it), on every tile kernel, and
+    the result passes the oracle bar."""
+    shape = LAYER_CASES[case]
+    inp = workloads.make_inputs(shape, seed=3, device="cuda")
+    old_pair = moe.moe_set_option(moe.MOE_OPT_PAIR_TILES, pair)
+    old_gather = moe.moe_set_option(moe.MOE_OPT_GATHER_A, gather)
+    old_dec = moe.moe_set_option(moe.MOE_OPT_DECODE_KERNEL, 0)  # the tile kernels, not swap-AB
+    old = moe.moe_set_option(moe.MOE_OPT_DYNAMIC_TILES, 0)
+    try:
+        base = run_layer(shape, inp, layout)["out"].clone()
+        moe.moe_set_option(moe.MOE_OPT_DYNAMIC_TILES, 1)
+        for _ in range(3):
+            assert torch.equal(run_layer(shape, inp, layout)["out"], base)
+        check_layer(shape, layout=layout)
+    finally:
+        moe.moe_set_option(moe.MOE_OPT_DYNAMIC_TILES, old)
+        moe.moe_set_option(moe.MOE_OPT_DECODE_KERNEL, old_dec)
+        moe.moe_set_option(moe.MOE_OPT_GATHER_A, old_gather)
+        moe.moe_set_option(moe.MOE_OPT_PAIR_TILES, old_pair)
+
+
 @pytest.mark.parametrize("dist", [2, 7])
 @pytest.mark.parametrize("case,layout,pair", [
     ("qwen3_T512", "kn", 3),       # bf16: the routed gate/up pass gathers its rows; 2-CTA down pass
