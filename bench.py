@@ -400,7 +400,7 @@ def kernel_names(shape, nk, gather_a=3, a8=False, fused=False, shared_in_gemm=Fa
     if shape.R <= 8192:  # small batches: init_routing + gather in one kernel
         names += ["route_permute"]
     else:
-        names += ["route_sort"] if fused_routing else ["route_hist", "route_scan_scatter"]
+        names += ["route_sort"] if (fused_routing and shape.R <= 65536) else ["route_hist", "route_scan_scatter"]
         names += ["permute_gather"] if gather_mode(shape, gather_a, shared_in_gemm) == 0 else []
     names += ["w13_gate_up"]
     names += [f"h_to_{rows}"] if fp8 else []

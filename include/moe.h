@@ -397,7 +397,7 @@ int moe_layer_launch_count(const moe_config_t* cfg);
  *   to 4 CTAs per 128 tokens splits the fp32 sum over D into consecutive
  *   slices on the tensor core and hands the partial rows through distributed
  *   shared memory to the CTA that adds them in slice order and takes the
- *   top-k; (b) for more than 8192 expanded rows, the histogram, scan and
+ *   top-k; (b) for 8193 to 65536 expanded rows, the histogram, scan and
  *   stable scatter of init_routing are one cluster of 8 CTAs that exchange
  *   their expert histograms through distributed shared memory.
  *   0 = a grouped-GEMM launch writing split-K planes, then the top-k kernel;

@@ -367,7 +367,11 @@ int do_permute(const moe_config_t* c, const int32_t* ids, const void* x, int32_t
         row_scale, err, s, extra_rows));
   }
   cudaError_t e;
-  if (g_fused_routing && R > 0 && c->E <= 512) {  // histogram, scan, scatter: one cluster launch
+  // histogram, scan and scatter as one 8-CTA cluster launch up to 65536
+  // expanded rows; above, the two-kernel sort spreads the scattered writes
+  // over one CTA per segment (Ling-style prefill, 131072 rows: 38 us in the
+  // cluster against 25 us in two kernels)
+  if (g_fused_routing && R > 0 && R <= kClusterSortRows && c->E <= 512) {
     trace_mark(s);
     e = launch_route_sort_cluster(ids, R, c->E, counts, offsets, sorted_rows, dest, err, s);
   } else {
@@ -895,7 +899,9 @@ int moe_layer_launch_count(const moe_config_t* cfg) {
   if (small_route(static_cast<long long>(cfg->T) * cfg->k, cfg->E)) {
     n += 1;  // init_routing + permutation gather in one kernel
   } else {
-    n += g_fused_routing ? 1 : 2;  // histogram, scan + stable scatter (one cluster launch when fused)
+    // histogram, scan + stable scatter (one cluster launch when fused, up to
+    // kClusterSortRows expanded rows)
+    n += (g_fused_routing && static_cast<long long>(cfg->T) * cfg->k <= kClusterSortRows) ? 1 : 2;
     if (gather_mode(cfg) == 0) n += 1;  // permutation gather
   }
   n += 2;  // routed gate/up, down

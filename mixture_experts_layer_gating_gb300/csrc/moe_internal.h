@@ -130,6 +130,8 @@ cudaError_t launch_router_small(const void* x, const void* Wg, int T, int D, int
 cudaError_t launch_init_routing(const int32_t* ids, int R, int E, int32_t* counts, int32_t* offsets,
                                 int32_t* sorted_rows, int32_t* dest, int32_t* seg_scratch,
                                 int32_t* err, cudaStream_t s, void (*mark)(cudaStream_t) = nullptr);
+// Expanded rows up to which moe_permute / moe_layer sort with the cluster kernel.
+constexpr long long kClusterSortRows = 65536;
 // The same stable counting sort as launch_init_routing in one launch: a
 // cluster of 8 CTAs that exchange their expert histograms through distributed
 // shared memory (no scratch).  E <= 512.

@@ -17,8 +17,8 @@ the histograms exchanged through distributed shared memory), through
 moe_permute: counts, offsets, sorted_rows, dest and the permuted rows
 bit-exact against the oracle's counting sort, with both settings of the
 option, on uniform, skewed, one-expert and half-empty routings, E up to 512,
-and a batch with ids out of range (those rows get dest = -1 and stay out of
-the sort).
+up to the 65536 expanded rows the cluster sort takes, and a batch with ids out
+of range (those rows get dest = -1 and stay out of the sort).
 """
 import numpy as np
 import pytest
@@ -96,8 +96,9 @@ SORT_CASES = [
     # T, E, k, pattern
     (1025, 8, 8, "uniform"),       # 8200 expanded rows: just past the one-launch sort
     (4096, 128, 8, "uniform"),     # Qwen3-MoE prefill
-    (8192, 512, 10, "skew"),       # Qwen3.5-style prefill
-    (16384, 256, 8, "uniform"),    # Ling-style prefill
+    (6000, 512, 10, "skew"),       # 60000 rows, 512 experts
+    (8192, 256, 8, "uniform"),     # 65536 rows: the largest batch the cluster sort takes
+    (16384, 256, 8, "uniform"),    # Ling-style prefill: two-kernel sort either way
     (3001, 64, 6, "one_expert"),   # every token's first choice is expert 0
     (2500, 64, 6, "empty_half"),   # experts 32.. never chosen
     (5000, 100, 4, "bad_ids"),     # a few ids out of range
