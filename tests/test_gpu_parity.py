@@ -510,8 +510,8 @@ def test_grouped_ffn_pair_tail_sizes(act, pair_mode):
     """2-CTA tiles, every kind of last tile: swapped tails of 1..64 (gate/up)
     and 1..128 (down) rows, full-height tails above that, exact multiples of
     256; mode 2 runs the same groups without swapped tails."""
-    counts = [1, 16, 17, 31, 32, 33, 63, 64, 65, 100, 127, 128, 129, 255, 256, 257, 300, 320,
-              383, 384, 385, 512]
+    counts = [1, 16, 17, 31, 32, 33, 63, 64, 65, 100, 127, 128, 129, 130, 200, 240, 255, 256, 257,
+              300, 320, 383, 384, 385, 449, 511, 512]
     E, D, I = len(counts), 256, 128
     old = moe.moe_set_option(moe.MOE_OPT_PAIR_TILES, pair_mode)
     try:

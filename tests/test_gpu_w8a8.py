@@ -94,7 +94,7 @@ def test_grouped_ffn_w8a8_tail_sizes(act, pair_mode):
     2-CTA 256-row tiles with swapped tails (mode 1, each CTA loading half of
     a tail's rows)."""
     counts = [1, 15, 16, 17, 31, 32, 33, 63, 64, 65, 80, 95, 96, 97, 112, 127, 128, 129, 200, 224,
-              225, 256, 300]
+              225, 256, 300, 385, 449, 511]
     E, D, I = len(counts), 320, 256
     old = moe.moe_set_option(moe.MOE_OPT_PAIR_TILES, pair_mode)
     try:
