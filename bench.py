@@ -235,13 +235,20 @@ def fused_router(T: int, E: int, D: int, k: int, act_dtype: str) -> bool:
     """Whether moe_layer runs the router projection and the top-k softmax as
     one kernel: the library's rule (MOE_OPT_FUSED_ROUTING on, its default),
     restated -- bf16 activations, 64 <= E <= 512, E and D multiples of 8,
-    k <= 32, and not a batch the CUDA-core projection takes (at most 64
-    tokens and 2^25 multiply-adds, slices of D of at most 1024)."""
+    k <= 32, not a batch the CUDA-core projection takes (at most 64 tokens
+    and 2^25 multiply-adds, slices of D of at most 1024), and a fused grid of
+    at least 64 CTAs."""
     if act_dtype != "bf16" or not 64 <= E <= 512 or E % 8 or D % 8 or k > 32:
         return False
     S = router_planes(T, E, D)
     small = T <= 64 and E % 2 == 0 and T * D * E <= 2 ** 25 and (D + S - 1) // S <= 1024
-    return not small
+    # at least 64 CTAs: token tiles of 128 x slices of D (clusters of <= 4) x expert halves
+    tiles, nh, kb = (T + 127) // 128, (2 if E > 256 else 1), (D + 63) // 64
+    want = max(1, min(4 // nh, 148 // max(1, tiles * nh), kb // 4))
+    ck = 1
+    while 2 * ck <= want:
+        ck *= 2
+    return not small and tiles * ck * nh >= 64
 
 
 def memory_kernel_bytes(shape, name: str, rows_form_bytes: int, nk: bool = False):

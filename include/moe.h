@@ -400,8 +400,10 @@ int moe_layer_launch_count(const moe_config_t* cfg);
  *   top-k; (b) for 8193 to 65536 expanded rows, the histogram, scan and
  *   stable scatter of init_routing are one cluster of 8 CTAs that exchange
  *   their expert histograms through distributed shared memory.
- *   0 = a grouped-GEMM launch writing split-K planes, then the top-k kernel;
- *   a histogram kernel, then a scan + scatter kernel.  The logits may differ
+ *   (a) applies where its grid has at least 64 CTAs (prefill; decode batches
+ *   take the split-K projection); 2 = (a) wherever the shape allows it
+ *   (testing).  0 = a grouped-GEMM launch writing split-K planes, then the
+ *   top-k kernel; a histogram kernel, then a scan + scatter kernel.  The logits may differ
  *   in the last bits between the two (another split of the fp32 sum over D);
  *   ids and weights follow from each one's own logits by the same rule, and
  *   the permutation is the same. */
@@ -420,9 +422,10 @@ int moe_layer_launch_count(const moe_config_t* cfg);
  *   other roles through a small queue in shared memory, one tile ahead, so
  *   that CTAs whose tiles run faster take more of them; the calls that launch
  *   those GEMMs zero the counters first (one memset).  2 (default) = for the
- *   gate/up passes whose tiles are at least 64 k-blocks long (D >= 4096 for
- *   bf16 weights, D >= 8192 for K-contiguous e4m3 weights; Ling-style prefill
- *   layer 11.35-11.39 -> 11.04-11.07 ms on GB300); 1 = every pass (the short
+ *   prefill-sized gate/up passes (at least 1024 rows and 32 per group) whose
+ *   tiles are at least 64 k-blocks long (D >= 4096 for bf16 weights, D >=
+ *   8192 for K-contiguous e4m3 weights; Ling-style prefill layer 11.35-11.39
+ *   -> 11.04-11.07 ms on GB300); 1 = every pass (the short
  *   down-pass tiles measured 3-8 % slower); 0 = tile t to CTA (pair) t modulo
  *   the grid.  Same results. */
 #define MOE_OPT_DYNAMIC_TILES 12

@@ -243,10 +243,24 @@ inline int32_t* err_word(void* ws) { return &static_cast<ControlBlock*>(ws)->err
 inline int32_t* tile_counters(void* ws) {
   return g_dynamic_tiles ? static_cast<ControlBlock*>(ws)->reserved + kTileCounterSlot : nullptr;
 }
-// Zeroes them on s before a call's first grouped GEMM (nothing when off).
-inline cudaError_t zero_tile_counters(void* ws, cudaStream_t s) {
-  int32_t* c = tile_counters(ws);
-  return c ? cudaMemsetAsync(c, 0, 4 * sizeof(int32_t), s) : cudaSuccess;
+// Whether a gate/up pass of M rows in G groups takes the dynamic tile order
+// (MOE_OPT_DYNAMIC_TILES 2: tiles of at least 64 k-blocks in a prefill-sized
+// pass, at least 1024 rows and 32 per group; 1: every pass).
+inline bool dynamic_gate_up(const moe_config_t* c, long long M, int G) {
+  if (g_dynamic_tiles == 1) return true;
+  if (!g_dynamic_tiles) return false;
+  const int kblocks = c->D / ((is_nk(c) || is_a8(c)) ? 128 : 64);
+  return kblocks >= 64 && M >= 1024 && M >= 32ll * G;
+}
+// Zeroes the counters on s before a call's first grouped GEMM when one of
+// its passes takes the dynamic order (nothing otherwise).
+inline cudaError_t zero_tile_counters(void* ws, const moe_config_t* c, cudaStream_t s) {
+  int32_t* ctr = tile_counters(ws);
+  const long long R = static_cast<long long>(c->T) * c->k;
+  const bool any = g_dynamic_tiles == 1 || dynamic_gate_up(c, R, c->E) ||
+                   dynamic_gate_up(c, R + c->T, c->E + 1) ||
+                   (c->I_shared > 0 && dynamic_gate_up(c, c->T, 1));
+  return (ctr && any) ? cudaMemsetAsync(ctr, 0, 4 * sizeof(int32_t), s) : cudaSuccess;
 }
 inline uint8_t* ws_at(void* ws, size_t off) { return static_cast<uint8_t*>(ws) + off; }
 
@@ -268,9 +282,11 @@ int common_checks(const moe_config_t* cfg, void* ws, size_t ws_bytes) {
 
 // The router projection and top-k as one kernel (MOE_OPT_FUSED_ROUTING): bf16
 // activations, batches the CUDA-core projection does not take.
+// MOE_OPT_FUSED_ROUTING 2 takes it wherever the shape allows (testing).
 bool fused_router_on(const moe_config_t* c, int nsplit) {
   return g_fused_routing && c->act_dtype == MOE_BF16 && !router_small_ok(c->T, c->E, c->D, nsplit) &&
-         router_topk_ok(c->T, c->E, c->D, c->k);
+         router_topk_ok(c->T, c->E, c->D, c->k) &&
+         (g_fused_routing == 2 || router_topk_preferred(c->T, c->E, c->D));
 }
 
 // ------------------------------------------------------------------ stages
@@ -450,11 +466,11 @@ int do_ffn(const moe_config_t* c, const void* A, const float* a_row_scale, int M
   a.sh_B = W13s;
   a.sh_b_scale = s13s;
   // counters[0]: gate/up pass, counters[1]: down pass (MOE_OPT_DYNAMIC_TILES:
-  // 1 = both; 2, the default = the gate/up pass when its tiles are at least 64
-  // k-blocks long -- there the balance pays for the queue, which costs the
-  // short tiles of the down passes more than it saves)
-  const int kblocks = c->D / ((nk || is_a8(c)) ? 128 : 64);
-  a.tile_counter = (counters && (g_dynamic_tiles == 1 || kblocks >= 64)) ? counters : nullptr;
+  // 1 = both; 2, the default = a prefill-sized gate/up pass whose tiles are at
+  // least 64 k-blocks long -- there the balance pays for the queue, which
+  // costs the short tiles of the down passes and decode-sized passes more
+  // than it saves)
+  a.tile_counter = (counters && dynamic_gate_up(c, M, G)) ? counters : nullptr;
   e = launch_grouped_gemm(a, s);
   if (e != cudaSuccess) return e == cudaErrorNotSupported ? MOE_ERR_UNSUPPORTED : MOE_ERR_CUDA;
   if (fp8) {
@@ -599,7 +615,7 @@ int moe_grouped_ffn(const moe_config_t* cfg, const void* x_perm, const int32_t* 
   }
   if (cfg->T == 0) return MOE_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (zero_tile_counters(ws, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (zero_tile_counters(ws, cfg, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (is_fp8(cfg)) {
     // fp8 weights: convert the bf16 rows to fp16 rows (or two-term e4m3 rows)
     // with exact power-of-two scales in the workspace first
@@ -680,7 +696,7 @@ int moe_layer(const moe_config_t* cfg, const void* x, const void* Wg, const floa
   const bool fused = fused_combine_on(cfg);
   if (fused && cudaMemsetAsync(y_perm, 0, static_cast<size_t>(cfg->T) * cfg->D * 4, s) != cudaSuccess)
     return (g_trace_next = -1, MOE_ERR_CUDA);
-  if (zero_tile_counters(ws, s) != cudaSuccess) return (g_trace_next = -1, MOE_ERR_CUDA);
+  if (zero_tile_counters(ws, cfg, s) != cudaSuccess) return (g_trace_next = -1, MOE_ERR_CUDA);
   const void* x_rows = x;  // what the gather and the shared expert read
   float* tok_inv = nullptr;
   float* row_inv = nullptr;
@@ -866,7 +882,7 @@ int moe_set_option(int option, int value) {
     }
     case MOE_OPT_FUSED_ROUTING: {
       const int old = g_fused_routing;
-      g_fused_routing = value ? 1 : 0;
+      g_fused_routing = value <= 0 ? 0 : value >= 2 ? 2 : 1;
       return old;
     }
     case MOE_OPT_FUSED_COMBINE: {

@@ -111,6 +111,8 @@ cudaError_t launch_topk_softmax(const float* partials, int nsplit, const float* 
 // router_topk_split gives its cluster shape: ck slices of D times nh expert
 // halves (a function of the shape alone).
 bool router_topk_ok(int T, int E, int D, int k);
+// Whether the fused kernel is the faster choice for the shape (>= 64 CTAs).
+bool router_topk_preferred(int T, int E, int D);
 void router_topk_split(int T, int E, int D, int& ck, int& nh);
 cudaError_t launch_router_topk(const void* x, const void* Wg, const float* bias, int T, int D,
                                int E, int k, int renorm, float* logits, int32_t* ids, float* w,

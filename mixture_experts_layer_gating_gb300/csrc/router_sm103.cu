@@ -332,6 +332,15 @@ bool router_topk_ok(int T, int E, int D, int k) {
          (D % 8) == 0;
 }
 
+bool router_topk_preferred(int T, int E, int D) {
+  // at least 64 CTAs: with fewer token tiles (decode batches up to 512
+  // tokens: 4-16 CTAs) the split-K projection over ~64-148 CTAs plus the
+  // top-k kernel is faster (Qwen3.5-style decode, 512 tokens: 60 us fused)
+  int ck, nh;
+  router_topk_split(T, E, D, ck, nh);
+  return static_cast<long long>((T + RT_BM - 1) / RT_BM) * ck * nh >= 64;
+}
+
 cudaError_t launch_router_topk(const void* x, const void* Wg, const float* bias, int T, int D,
                                int E, int k, int renorm, float* logits, int32_t* ids, float* w,
                                int32_t* err, cudaStream_t s) {

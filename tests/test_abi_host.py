@@ -51,8 +51,9 @@ def test_workspace_size_covers_intermediates(lib, name):
         routing = (1 if shape.T * shape.k <= 65536 else 2) + (0 if gemm_gathers else 1)
     # router projection and top-k as one kernel: bf16 activations, 64 <= E, and
     # more than the CUDA-core projection takes (64 tokens, 2^25 multiply-adds)
+    # (and a grid of at least 64 CTAs: prefill batches; see bench.fused_router)
     fused = shape.act_dtype == "bf16" and shape.E >= 64 and not (
-        shape.T <= 64 and shape.T * shape.D * shape.E <= 2 ** 25)
+        shape.T <= 64 and shape.T * shape.D * shape.E <= 2 ** 25) and shape.T >= 2048
     # router (+ top-k), 2 (+2 shared) GEMMs, finalize
     base = (6 if fused else 7) if shape.I_shared else (4 if fused else 5)
     assert moe.moe_layer_launch_count(cfg) == base + fp8_extra + routing
@@ -163,7 +164,9 @@ def test_set_option_values():
         (moe.MOE_OPT_DYNAMIC_TILES, 1, 1),
         (moe.MOE_OPT_DYNAMIC_TILES, 0, 0),
         (moe.MOE_OPT_FUSED_ROUTING, 0, 0),
-        (moe.MOE_OPT_FUSED_ROUTING, 2, 1),
+        (moe.MOE_OPT_FUSED_ROUTING, 2, 2),
+        (moe.MOE_OPT_FUSED_ROUTING, 7, 2),
+        (moe.MOE_OPT_FUSED_ROUTING, 1, 1),
     ]
     for opt, value, stored in cases:
         old = moe.moe_set_option(opt, value)
@@ -174,6 +177,7 @@ def test_set_option_values():
     (4096, 128, 2048, 8, True),    # Qwen3-MoE prefill
     (16384, 256, 8192, 8, True),   # Ling-style prefill
     (8192, 512, 4096, 10, True),   # two expert halves
+    (512, 256, 8192, 8, False),    # decode batch: 16 CTAs, the split-K projection
     (64, 128, 2048, 8, False),     # decode: the CUDA-core projection
     (4096, 32, 2048, 4, False),    # fewer than 64 experts
     (4096, 128, 2050, 8, False),   # D not a multiple of 8 (row pitch)
