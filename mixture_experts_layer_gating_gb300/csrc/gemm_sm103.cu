@@ -355,17 +355,41 @@ __device__ void build_schedule(Ctrl* ctrl, const int32_t* offsets, int G, int M,
     build_schedule_lpt(ctrl, offsets, G, M, tile_h, err, lane, sh_rows);
     return;
   }
-  const int per = (G + 31) / 32;
+  const int per = (G + 31) / 32;  // <= 17 groups per lane (G <= MAX_G)
   const int g0 = min(G, lane * per), g1 = min(G, g0 + per);
+  // this lane's offsets[g0 .. g1] first, every load in flight at once (one
+  // memory round trip instead of one per group); offsets holds G + 1 entries,
+  // or G when the last group is the shared expert's rows
+  constexpr int kPer = (MAX_G + 31) / 32;
+  static_assert(kPer <= 17, "groups per lane");
+  const int n_ofs = (sh_rows > 0) ? G : G + 1;
+  int ofs[kPer + 1];
+#pragma unroll
+  for (int i = 0; i <= kPer; ++i)
+    ofs[i] = (offsets && i <= g1 - g0 && g0 + i < n_ofs) ? offsets[g0 + i] : 0;
   int local = 0;
   bool bad = false;
-  for (int g = g0; g < g1; ++g) {
-    int a, b;
-    group_rows(offsets, g, M, a, b, bad, G, sh_rows);
-    ctrl->grp_id[g] = g;
-    ctrl->grp_start[g] = a;
-    ctrl->grp_cnt[g] = b - a;
-    local += (b - a + tile_h - 1) / tile_h;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int g = g0 + i;
+    if (g < g1) {
+      int a = 0, b = M;
+      if (sh_rows > 0 && g == G - 1) {
+        a = M - sh_rows;
+      } else if (offsets) {
+        a = ofs[i];
+        b = ofs[i + 1];
+      }
+      if (a < 0 || b < a || b > M) {
+        bad = true;
+        a = 0;
+        b = 0;
+      }
+      ctrl->grp_id[g] = g;
+      ctrl->grp_start[g] = a;
+      ctrl->grp_cnt[g] = b - a;
+      local += (b - a + tile_h - 1) / tile_h;
+    }
   }
   int incl = local;
 #pragma unroll
