@@ -357,6 +357,8 @@ def set_options(moe, args):
         moe.moe_set_option(moe.MOE_OPT_FUSED_COMBINE, 1)
     if getattr(args, "b_prefetch", None) is not None:
         moe.moe_set_option(moe.MOE_OPT_B_PREFETCH, args.b_prefetch)
+    if getattr(args, "shared_ctas", None) is not None:
+        moe.moe_set_option(moe.MOE_OPT_SHARED_CTAS, args.shared_ctas)
     if getattr(args, "dynamic_tiles", None) is not None:
         moe.moe_set_option(moe.MOE_OPT_DYNAMIC_TILES, args.dynamic_tiles)
     if getattr(args, "split_routing", False):
@@ -742,7 +744,9 @@ def main():
                     help="plain stream order instead of programmatic dependent launch (MOE_OPT_PDL 0)")
     ap.add_argument("--b-prefetch", type=int, default=None,
                     help="weight boxes prefetched into L2 this many k-blocks ahead (MOE_OPT_B_PREFETCH)")
-    ap.add_argument("--dynamic-tiles", type=int, default=None, choices=[0, 1],
+    ap.add_argument("--shared-ctas", type=int, default=None,
+                    help="CTAs of the shared expert's side-stream GEMMs (MOE_OPT_SHARED_CTAS; 0 = all)")
+    ap.add_argument("--dynamic-tiles", type=int, default=None, choices=[0, 1, 2],
                     help="grouped GEMM tiles handed out by an atomic counter (MOE_OPT_DYNAMIC_TILES)")
     ap.add_argument("--split-routing", action="store_true",
                     help="router projection and top-k, histogram and scatter as separate launches "

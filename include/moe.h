@@ -429,6 +429,11 @@ int moe_layer_launch_count(const moe_config_t* cfg);
  *   down-pass tiles measured 3-8 % slower); 0 = tile t to CTA (pair) t modulo
  *   the grid.  Same results. */
 #define MOE_OPT_DYNAMIC_TILES 12
+/*   MOE_OPT_SHARED_CTAS: n > 0 = the shared expert's GEMMs on the library's
+ *   side stream use at most n CTAs (their persistent grid), leaving the other
+ *   SMs to the routed path's kernels that run beside them; 0 (default) = one
+ *   CTA per SM.  Same results. */
+#define MOE_OPT_SHARED_CTAS 13
 int moe_set_option(int option, int value);
 
 /* Per-kernel timing hook (process-wide, off by default).  `events` holds

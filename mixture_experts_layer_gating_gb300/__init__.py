@@ -76,6 +76,7 @@ MOE_OPT_SHARED_IN_GEMM = 9
 MOE_OPT_FUSED_ROUTING = 10
 MOE_OPT_B_PREFETCH = 11
 MOE_OPT_DYNAMIC_TILES = 12
+MOE_OPT_SHARED_CTAS = 13
 
 
 def load_library(path: Optional[str] = None) -> ctypes.CDLL:

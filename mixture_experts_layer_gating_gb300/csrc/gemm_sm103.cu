@@ -2201,6 +2201,13 @@ int g_b_prefetch = 0;      // set through moe_set_option(MOE_OPT_B_PREFETCH, .)
 
 namespace {
 
+// The persistent grid: one CTA (cluster) per tile at most, and at most
+// a.max_ctas CTAs when the caller caps it (the shared expert's GEMMs beside the
+// routed path: MOE_OPT_SHARED_CTAS).
+long long cap_grid(long long tiles, const GroupedGemmArgs& a, bool pair) {
+  if (a.max_ctas <= 0) return tiles;
+  return std::min<long long>(tiles, std::max(1, pair ? a.max_ctas / 2 : a.max_ctas));
+}
 template <int EPI, bool SPLIT, bool FP8, bool Q8 = false>
 cudaError_t launch_dec(const CUtensorMap& tr, const CUtensorMap& tr_lo, const CUtensorMap& tw,
                        const KParams& kp, long long max_tiles, cudaStream_t s) {
@@ -2276,8 +2283,8 @@ cudaError_t launch_grouped_gemm_decode_q8(const GroupedGemmArgs& a, int nt, cuda
     kp.cols_per_tile = 128;
   }
   kp.n_tiles = (a.N + kp.cols_per_tile - 1) / kp.cols_per_tile;
-  const long long max_tiles =
-      (static_cast<long long>((a.M + nt - 1) / nt) + a.G) * static_cast<long long>(kp.n_tiles);
+  const long long max_tiles = cap_grid(
+      (static_cast<long long>((a.M + nt - 1) / nt) + a.G) * static_cast<long long>(kp.n_tiles), a, false);
   if (a.epilogue == kEpiCombineF32)
     return one ? launch_dec<kEpiCombineF32, false, false, true>(tr, tr_lo, tw, kp, max_tiles, s)
                : launch_dec<kEpiCombineF32, true, false, true>(tr, tr_lo, tw, kp, max_tiles, s);
@@ -2348,8 +2355,8 @@ cudaError_t launch_grouped_gemm_decode(const GroupedGemmArgs& a, int nt, cudaStr
     kp.cols_per_tile = 128;
   }
   kp.n_tiles = (a.N + kp.cols_per_tile - 1) / kp.cols_per_tile;
-  const long long max_tiles =
-      (static_cast<long long>((a.M + nt - 1) / nt) + a.G) * static_cast<long long>(kp.n_tiles);
+  const long long max_tiles = cap_grid(
+      (static_cast<long long>((a.M + nt - 1) / nt) + a.G) * static_cast<long long>(kp.n_tiles), a, false);
   if (a.epilogue == kEpiGateUpAct)
     return a.b_fp8 ? launch_dec<kEpiGateUpAct, false, true>(tr, tr_lo, tw, kp, max_tiles, s)
                    : launch_dec<kEpiGateUpAct, false, false>(tr, tr_lo, tw, kp, max_tiles, s);
@@ -2470,8 +2477,8 @@ cudaError_t launch_grouped_gemm_q8(const GroupedGemmArgs& a, cudaStream_t s) {
     tb2_tail = tb_tail;
   }
   const int tile_m = pair ? 2 * BM : BM;
-  const long long max_tiles = (static_cast<long long>((a.M + tile_m - 1) / tile_m) + a.G) *
-                              static_cast<long long>(kp.n_tiles);
+  const long long max_tiles = cap_grid((static_cast<long long>((a.M + tile_m - 1) / tile_m) + a.G) *
+                                           static_cast<long long>(kp.n_tiles), a, pair);
   CUtensorMap tout = ta;
   make_out_map(a, kp, /*out_bf16=*/true, tout);
 #define MOE_LAUNCH_Q8(E_, S_, P_) \
@@ -2704,8 +2711,8 @@ cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s) {
       return cudaErrorInvalidValue;
   }
   const int tile_m = pair ? 2 * BM : BM;
-  const long long max_tiles = (static_cast<long long>((a.M + tile_m - 1) / tile_m) + a.G) *
-                              static_cast<long long>(kp.n_tiles) * kp.ksplit;
+  const long long max_tiles = cap_grid((static_cast<long long>((a.M + tile_m - 1) / tile_m) + a.G) *
+                                           static_cast<long long>(kp.n_tiles) * kp.ksplit, a, pair);
   CUtensorMap tout = ta;
   make_out_map(a, kp, /*out_bf16=*/a.b_fp8 != 0, tout);
   // (pair is never set for fp8 weights: their kernels exist on 1-CTA tiles only)

@@ -20,6 +20,7 @@ int g_fused_combine = 0;  // moe_set_option(MOE_OPT_FUSED_COMBINE, .)
 int g_shared_in_gemm = 0;  // moe_set_option(MOE_OPT_SHARED_IN_GEMM, .)
 int g_fused_routing = 1;  // moe_set_option(MOE_OPT_FUSED_ROUTING, .)
 int g_dynamic_tiles = 2;  // moe_set_option(MOE_OPT_DYNAMIC_TILES, .)
+int g_shared_ctas = 0;    // moe_set_option(MOE_OPT_SHARED_CTAS, .)
 
 // The shared expert depends on x alone, so moe_layer runs it on a second
 // stream of the library's own (one per device, created on first use) that
@@ -415,7 +416,7 @@ int do_ffn(const moe_config_t* c, const void* A, const float* a_row_scale, int M
            cudaStream_t s, const int32_t* a_gather = nullptr, int a_rows = 0,
            const int32_t* comb_rows = nullptr, const float* comb_w = nullptr, int sh_rows = 0,
            const void* W13s = nullptr, const float* s13s = nullptr, const void* W2s = nullptr,
-           const float* s2s = nullptr, int32_t* counters = nullptr) {
+           const float* s2s = nullptr, int32_t* counters = nullptr, int max_ctas = 0) {
   if (M <= 0) return MOE_OK;
   cudaError_t e;
   trace_mark(s);
@@ -471,6 +472,7 @@ int do_ffn(const moe_config_t* c, const void* A, const float* a_row_scale, int M
   // costs the short tiles of the down passes and decode-sized passes more
   // than it saves)
   a.tile_counter = (counters && dynamic_gate_up(c, M, G)) ? counters : nullptr;
+  a.max_ctas = max_ctas;  // (b copies it)
   e = launch_grouped_gemm(a, s);
   if (e != cudaSuccess) return e == cudaErrorNotSupported ? MOE_ERR_UNSUPPORTED : MOE_ERR_CUDA;
   if (fp8) {
@@ -729,7 +731,7 @@ int moe_layer(const moe_config_t* cfg, const void* x, const void* Wg, const floa
                          cfg->I_shared, h_s, s_out, fp8 ? ws_at(ws, L.hs16) : nullptr,
                          fp8 ? reinterpret_cast<float*>(ws_at(ws, L.hs_inv)) : nullptr, err, side,
                          nullptr, 0, nullptr, nullptr, 0, nullptr, nullptr, nullptr, nullptr,
-                         ctr ? ctr + 2 : nullptr);
+                         ctr ? ctr + 2 : nullptr, g_shared_ctas);
     if (r != MOE_OK) {
       side_join(side, s);
       side = nullptr;
@@ -868,6 +870,11 @@ int moe_set_option(int option, int value) {
     case MOE_OPT_TILE_ORDER: {
       const int old = g_tile_order;
       g_tile_order = value ? 1 : 0;
+      return old;
+    }
+    case MOE_OPT_SHARED_CTAS: {
+      const int old = g_shared_ctas;
+      g_shared_ctas = value < 0 ? 0 : value;
       return old;
     }
     case MOE_OPT_DYNAMIC_TILES: {

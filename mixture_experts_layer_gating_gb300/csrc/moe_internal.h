@@ -249,6 +249,8 @@ struct GroupedGemmArgs {
   // dynamic tile order (moe_set_option(MOE_OPT_DYNAMIC_TILES, 1)): a counter
   // that is zero when the launch starts; nullptr = static round-robin order
   int32_t* tile_counter;
+  // > 0: at most this many CTAs in the persistent grid (0: one per SM)
+  int max_ctas;
 };
 
 cudaError_t launch_grouped_gemm(const GroupedGemmArgs& a, cudaStream_t s);

@@ -163,6 +163,8 @@ def test_set_option_values():
         (moe.MOE_OPT_DYNAMIC_TILES, 3, 2),
         (moe.MOE_OPT_DYNAMIC_TILES, 1, 1),
         (moe.MOE_OPT_DYNAMIC_TILES, 0, 0),
+        (moe.MOE_OPT_SHARED_CTAS, 48, 48),
+        (moe.MOE_OPT_SHARED_CTAS, -5, 0),
         (moe.MOE_OPT_FUSED_ROUTING, 0, 0),
         (moe.MOE_OPT_FUSED_ROUTING, 2, 2),
         (moe.MOE_OPT_FUSED_ROUTING, 7, 2),

@@ -229,6 +229,25 @@ def test_layer_same_result_with_shared_expert_stream(case, fork):
         moe.moe_set_option(moe.MOE_OPT_SHARED_STREAM, old)
 
 
+@pytest.mark.parametrize("case", ["gemma4_T256", "qwen35_T1024", "ling_T1100_nk"])
+def test_layer_same_result_with_capped_shared_grid(case):
+    """MOE_OPT_SHARED_CTAS: the shared expert's side-stream GEMMs on at most 24
+    CTAs (2-CTA tiles: 12 clusters) give the layer bit for bit, forked either
+    way."""
+    shape, layout = SIDE_CASES[case]
+    inp = workloads.make_inputs(shape, seed=9, device="cuda")
+    old = moe.moe_set_option(moe.MOE_OPT_SHARED_STREAM, 0)
+    old_ctas = moe.moe_set_option(moe.MOE_OPT_SHARED_CTAS, 24)
+    try:
+        serial = run_layer(shape, inp, layout)["out"].clone()
+        for fork in (1, 2):
+            moe.moe_set_option(moe.MOE_OPT_SHARED_STREAM, fork)
+            assert torch.equal(run_layer(shape, inp, layout)["out"], serial)
+    finally:
+        moe.moe_set_option(moe.MOE_OPT_SHARED_STREAM, old)
+        moe.moe_set_option(moe.MOE_OPT_SHARED_CTAS, old_ctas)
+
+
 DYN_CASES = [
     # case, layout, pair-tile policy, gather policy
     ("qwen3_T512", "kn", 3, 3),         # bf16: cp.async row gather (one-CTA tiles), 2-CTA down pass
