@@ -231,13 +231,13 @@ def router_planes(T: int, E: int, D: int) -> int:
     return (kb + kbs - 1) // kbs
 
 
-def fused_router(T: int, E: int, D: int, k: int, act_dtype: str) -> bool:
+def fused_router(T: int, E: int, D: int, k: int, act_dtype: str, anywhere: bool = False) -> bool:
     """Whether moe_layer runs the router projection and the top-k softmax as
     one kernel: the library's rule (MOE_OPT_FUSED_ROUTING on, its default),
     restated -- bf16 activations, 64 <= E <= 512, E and D multiples of 8,
     k <= 32, not a batch the CUDA-core projection takes (at most 64 tokens
     and 2^25 multiply-adds, slices of D of at most 1024), and a fused grid of
-    at least 64 CTAs."""
+    at least 64 CTAs (not required with `anywhere`: options 2 and 3)."""
     if act_dtype != "bf16" or not 64 <= E <= 512 or E % 8 or D % 8 or k > 32:
         return False
     S = router_planes(T, E, D)
@@ -248,7 +248,7 @@ def fused_router(T: int, E: int, D: int, k: int, act_dtype: str) -> bool:
     ck = 1
     while 2 * ck <= want:
         ck *= 2
-    return not small and tiles * ck * nh >= 64
+    return not small and (anywhere or tiles * ck * nh >= 64)
 
 
 def memory_kernel_bytes(shape, name: str, rows_form_bytes: int, nk: bool = False):
@@ -363,6 +363,8 @@ def set_options(moe, args):
         moe.moe_set_option(moe.MOE_OPT_DYNAMIC_TILES, args.dynamic_tiles)
     if getattr(args, "split_routing", False):
         moe.moe_set_option(moe.MOE_OPT_FUSED_ROUTING, 0)
+    elif getattr(args, "cluster_sort", False):
+        moe.moe_set_option(moe.MOE_OPT_FUSED_ROUTING, 3)
     if args.lpt:
         moe.moe_set_option(moe.MOE_OPT_TILE_ORDER, 1)
     if args.shared_in_gemm:
@@ -398,18 +400,24 @@ def gather_mode(shape, opt: int, shared_in_gemm: bool) -> int:
     return 2 if (bf16 and shape.R >= 32 * shape.E) else 0
 
 
-def kernel_names(shape, nk, gather_a=3, a8=False, fused=False, shared_in_gemm=False, fused_routing=True):
-    """Names of the kernels one moe_layer call launches, in launch order."""
+def kernel_names(shape, nk, gather_a=3, a8=False, fused=False, shared_in_gemm=False, fused_routing=True,
+                 hist_sort=True):
+    """Names of the kernels one moe_layer call launches, in launch order.
+    hist_sort=False: MOE_OPT_FUSED_ROUTING 3 (the fused router wherever the
+    shape allows, init_routing without its histograms)."""
     fp8 = shape.w_dtype == "fp8_e4m3"
     rows = "e4m3" if a8 else "e4m3x2" if nk else "fp16"  # the A-row form of fp8 layers
     router = ["router_topk"] if fused_routing and fused_router(shape.T, shape.E, shape.D, shape.k,
-                                                                shape.act_dtype) \
+                                                                shape.act_dtype, not hist_sort) \
         else ["router_gemm", "topk_softmax"]
     names = ([f"x_to_{rows}"] if fp8 else []) + router
     if shape.R <= 8192:  # small batches: init_routing + gather in one kernel
         names += ["route_permute"]
     else:
-        names += ["route_sort"] if (fused_routing and shape.R <= 65536) else ["route_hist", "route_scan_scatter"]
+        # one launch: from the fused router's per-CTA histograms, or as one
+        # cluster up to 65536 rows
+        one = fused_routing and ((hist_sort and router == ["router_topk"]) or shape.R <= 65536)
+        names += ["route_sort"] if one else ["route_hist", "route_scan_scatter"]
         names += ["permute_gather"] if gather_mode(shape, gather_a, shared_in_gemm) == 0 else []
     names += ["w13_gate_up"]
     names += [f"h_to_{rows}"] if fp8 else []
@@ -494,15 +502,22 @@ def measure(args, world, rank, local, shape, primary: bool, layout: str):
     gather_opt = 3 if args.gather_a is None else args.gather_a
     in_gemm = (args.shared_in_gemm and shape.I_shared == shape.I and shape.I_shared > 0 and
                shape.act_dtype == "bf16" and (nk or not fp8) and gather_opt in (0, 3))
-    names = kernel_names(shape, nk, gather_opt, a8, fused, in_gemm, not args.split_routing)
+    names = kernel_names(shape, nk, gather_opt, a8, fused, in_gemm, not args.split_routing,
+                         not args.cluster_sort)
     assert len(names) == L
+    # the traced steps are enqueued back to back (one synchronisation at the
+    # end) so that the device, not the host's launch latency, sets each
+    # interval; the first one, enqueued on an idle device, is left out
     per = [[] for _ in range(L)]
-    for _ in range(args.steps):
+    traced = []
+    for _ in range(args.steps + 1):
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(L + 1)]
         moe.moe_set_trace_events(evs)
         step()
         moe.moe_set_trace_events(None)
-        torch.cuda.synchronize()
+        traced.append(evs)
+    torch.cuda.synchronize()
+    for evs in traced[1:]:
         for i in range(L):
             per[i].append(evs[i].elapsed_time(evs[i + 1]))
     kernels_us = {n: 1e3 * statistics.mean(v) for n, v in zip(names, per)}
@@ -751,6 +766,9 @@ def main():
     ap.add_argument("--split-routing", action="store_true",
                     help="router projection and top-k, histogram and scatter as separate launches "
                          "(MOE_OPT_FUSED_ROUTING 0)")
+    ap.add_argument("--cluster-sort", action="store_true",
+                    help="init_routing without the fused router's histograms: the 8-CTA cluster "
+                         "sort (two kernels above 65536 rows); MOE_OPT_FUSED_ROUTING 3")
     ap.add_argument("--fused-combine", action="store_true",
                     help="routed down pass adds weighted rows into [T, D] fp32 sums "
                          "(MOE_OPT_FUSED_COMBINE 1; the combine's summation order then varies)")

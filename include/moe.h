@@ -397,16 +397,20 @@ int moe_layer_launch_count(const moe_config_t* cfg);
  *   to 4 CTAs per 128 tokens splits the fp32 sum over D into consecutive
  *   slices on the tensor core and hands the partial rows through distributed
  *   shared memory to the CTA that adds them in slice order and takes the
- *   top-k; (b) for 8193 to 65536 expanded rows, the histogram, scan and
+ *   top-k; inside moe_layer each of its CTAs also counts its tokens' ids per
+ *   expert, and init_routing (above the one-launch size) is one kernel with
+ *   a CTA per router CTA that sorts that CTA's rows from those histograms;
+ *   (b) otherwise, for 8193 to 65536 expanded rows, the histogram, scan and
  *   stable scatter of init_routing are one cluster of 8 CTAs that exchange
  *   their expert histograms through distributed shared memory.
  *   (a) applies where its grid has at least 64 CTAs (prefill; decode batches
- *   take the split-K projection); 2 = (a) wherever the shape allows it
- *   (testing).  0 = a grouped-GEMM launch writing split-K planes, then the
- *   top-k kernel; a histogram kernel, then a scan + scatter kernel.  The logits may differ
- *   in the last bits between the two (another split of the fp32 sum over D);
- *   ids and weights follow from each one's own logits by the same rule, and
- *   the permutation is the same. */
+ *   take the split-K projection); 2 = (a) wherever the shape allows it, 3 =
+ *   the same without the histogram sort (testing).  0 = a grouped-GEMM launch
+ *   writing split-K planes, then the top-k kernel; a histogram kernel, then a
+ *   scan + scatter kernel.  The logits may differ in the last bits between
+ *   the two (another split of the fp32 sum over D); ids and weights follow
+ *   from each one's own logits by the same rule, and the permutation is the
+ *   same. */
 #define MOE_OPT_FUSED_ROUTING 10
 /*   MOE_OPT_B_PREFETCH: n > 0 = the grouped GEMMs' TMA producer also
  *   prefetches its weight box n k-blocks ahead into L2 (near the end of a

@@ -90,6 +90,9 @@ struct Layout {
   // fp8-weight layers: h (routed, shared) as fp16 rows with inverse scales
   size_t h16, h_inv, hs16, hs_inv;
   size_t seg_scratch;
+  // expert histogram of each fused-router CTA's rows (0 = the shape has no
+  // fused router)
+  size_t chunk_hist;
   size_t total;
 };
 
@@ -215,6 +218,11 @@ Layout make_layout(const moe_config_t* c) {
   L.off[MOE_WS_SORTED_ROWS] = take(R * 4);
   L.off[MOE_WS_DEST] = take(R * 4);
   L.seg_scratch = take(E * static_cast<size_t>(route_segments(static_cast<long long>(R))) * 4 + 4);
+  if (router_topk_ok(c->T, c->E, c->D, c->k)) {
+    int nchunks = 0, chunk_rows = 0;
+    router_topk_chunks(c->T, c->E, c->D, c->k, nchunks, chunk_rows);
+    L.chunk_hist = take(static_cast<size_t>(nchunks) * E * 4);
+  }
   L.off[MOE_WS_X_PERM] = take(Rx * D * ab);
   L.off[MOE_WS_H] = take(Rx * I * 4);        // fp32, bf16 (hi, lo) planes, or bf16
   L.off[MOE_WS_Y_PERM] = take(Rx * D * 4);   // fp32 (bf16 rows for fp8 layers)
@@ -283,19 +291,31 @@ int common_checks(const moe_config_t* cfg, void* ws, size_t ws_bytes) {
 
 // The router projection and top-k as one kernel (MOE_OPT_FUSED_ROUTING): bf16
 // activations, batches the CUDA-core projection does not take.
-// MOE_OPT_FUSED_ROUTING 2 takes it wherever the shape allows (testing).
+// MOE_OPT_FUSED_ROUTING 2 and 3 take it wherever the shape allows (testing).
 bool fused_router_on(const moe_config_t* c, int nsplit) {
   return g_fused_routing && c->act_dtype == MOE_BF16 && !router_small_ok(c->T, c->E, c->D, nsplit) &&
          router_topk_ok(c->T, c->E, c->D, c->k) &&
-         (g_fused_routing == 2 || router_topk_preferred(c->T, c->E, c->D));
+         (g_fused_routing >= 2 || router_topk_preferred(c->T, c->E, c->D));
+}
+
+// moe_layer sorts the rows by the fused router's per-CTA histograms (one CTA
+// per router CTA, launch_route_sort_chunks) instead of counting them again:
+// the router is fused and the batch is above the one-launch size.
+// MOE_OPT_FUSED_ROUTING 3 (testing): the fused router wherever the shape
+// allows, as 2, with the other init_routing kernels.
+bool chunk_sort_on(const moe_config_t* c) {
+  return g_fused_routing != 3 && fused_router_on(c, router_k_split(c->T, c->E, c->D)) &&
+         !small_route(static_cast<long long>(c->T) * c->k, c->E);
 }
 
 // ------------------------------------------------------------------ stages
 // `partials`: workspace room for the router's split-K planes (may be null when
 // the configuration does not split).
+// `chunk_hist`: where the fused router also writes its per-CTA expert
+// histograms (moe_layer with chunk_sort_on; null otherwise).
 int do_route(const moe_config_t* c, const void* x, const void* Wg, const float* bias,
              float* logits, int32_t* ids, float* w, float* partials, int32_t* err,
-             cudaStream_t s) {
+             cudaStream_t s, int32_t* chunk_hist = nullptr) {
   cudaError_t e = cudaSuccess;
   const float* src = logits;
   int nsplit = 1;
@@ -311,7 +331,7 @@ int do_route(const moe_config_t* c, const void* x, const void* Wg, const float* 
       if (fused_router_on(c, nsplit)) {
         // projection and top-k in one launch
         return cuda_status(launch_router_topk(x, Wg, bias, c->T, c->D, c->E, c->k, c->renormalize,
-                                              logits, ids, w, err, s));
+                                              logits, ids, w, err, s, chunk_hist));
       }
       if (router_small_ok(c->T, c->E, c->D, nsplit)) {
         // a few tokens: a matrix-vector product per token on the CUDA cores,
@@ -370,10 +390,13 @@ int do_permute_rows(const moe_config_t* c, const void* x, const int32_t* sorted_
 // row_bytes: bytes of one row of x (act_dtype rows, or moe_layer's fp8 row form)
 // extra_rows = T: x_perm rows R .. R+T-1 become copies of the tokens (the
 // shared expert's rows as the last group of the routed GEMMs).
+// chunk_hist: the fused router's per-CTA histograms of these ids (moe_layer
+// with chunk_sort_on), or null.
 int do_permute(const moe_config_t* c, const int32_t* ids, const void* x, int32_t* counts,
                int32_t* offsets, int32_t* sorted_rows, int32_t* dest, void* x_perm,
                int32_t* seg_scratch, int32_t* err, cudaStream_t s, size_t row_bytes,
-               const float* tok_scale = nullptr, float* row_scale = nullptr, int extra_rows = 0) {
+               const float* tok_scale = nullptr, float* row_scale = nullptr, int extra_rows = 0,
+               const int32_t* chunk_hist = nullptr) {
   const int R = c->T * c->k;
   if (small_route(R, c->E)) {  // one launch: sort + gather
     trace_mark(s);
@@ -384,11 +407,18 @@ int do_permute(const moe_config_t* c, const int32_t* ids, const void* x, int32_t
         row_scale, err, s, extra_rows));
   }
   cudaError_t e;
-  // histogram, scan and scatter as one 8-CTA cluster launch up to 65536
-  // expanded rows; above, the two-kernel sort spreads the scattered writes
-  // over one CTA per segment (Ling-style prefill, 131072 rows: 38 us in the
-  // cluster against 25 us in two kernels)
-  if (g_fused_routing && R > 0 && R <= kClusterSortRows && c->E <= 512) {
+  // after the fused router: one CTA per router CTA, from its histograms;
+  // otherwise histogram, scan and scatter as one 8-CTA cluster launch up to
+  // 65536 expanded rows, and above, the two-kernel sort that spreads the
+  // scattered writes over one CTA per segment (Ling-style prefill, 131072
+  // rows: 38 us in the cluster against 25 us in two kernels)
+  if (chunk_hist) {
+    int nchunks = 0, chunk_rows = 0;
+    router_topk_chunks(c->T, c->E, c->D, c->k, nchunks, chunk_rows);
+    trace_mark(s);
+    e = launch_route_sort_chunks(ids, R, c->E, nchunks, chunk_rows, chunk_hist, counts, offsets,
+                                 sorted_rows, dest, err, s);
+  } else if (g_fused_routing && R > 0 && R <= kClusterSortRows && c->E <= 512) {
     trace_mark(s);
     e = launch_route_sort_cluster(ids, R, c->E, counts, offsets, sorted_rows, dest, err, s);
   } else {
@@ -749,7 +779,9 @@ int moe_layer(const moe_config_t* cfg, const void* x, const void* Wg, const floa
     return code;
   };
   float* partials = L.router_partials ? reinterpret_cast<float*>(ws_at(ws, L.router_partials)) : nullptr;
-  st = do_route(cfg, x, Wg, logit_bias, logits, ids, w, partials, err, s);
+  int32_t* chunk_hist =
+      chunk_sort_on(cfg) ? reinterpret_cast<int32_t*>(ws_at(ws, L.chunk_hist)) : nullptr;
+  st = do_route(cfg, x, Wg, logit_bias, logits, ids, w, partials, err, s, chunk_hist);
   if (st != MOE_OK) return fail(st);
   // The routed gate/up pass reads its rows from a permuted copy of x (the
   // gather kernel streams at HBM speed), or gathers them from x itself
@@ -762,7 +794,7 @@ int moe_layer(const moe_config_t* cfg, const void* x, const void* Wg, const floa
   if (late_fork && !gather && !small_route(static_cast<long long>(cfg->T) * cfg->k, cfg->E)) {
     // init_routing, the fork, then the permutation beside the shared GEMMs
     st = do_permute(cfg, ids, nullptr, counts, offsets, sorted_rows, dest, nullptr, seg, err, s,
-                    layer_row_bytes(cfg));
+                    layer_row_bytes(cfg), nullptr, nullptr, 0, chunk_hist);
     if (st != MOE_OK) return fail(st);
     st = fork_shared();
     if (st != MOE_OK) return fail(st);
@@ -771,7 +803,7 @@ int moe_layer(const moe_config_t* cfg, const void* x, const void* Wg, const floa
   } else {
     st = do_permute(cfg, ids, gather ? nullptr : x_rows, counts, offsets, sorted_rows, dest,
                     gather ? nullptr : x_perm, seg, err, s, layer_row_bytes(cfg), tok_inv, row_inv,
-                    in_gemm ? cfg->T : 0);
+                    in_gemm ? cfg->T : 0, chunk_hist);
     if (st == MOE_OK && late_fork) st = fork_shared();
   }
   if (st != MOE_OK) return fail(st);
@@ -889,7 +921,7 @@ int moe_set_option(int option, int value) {
     }
     case MOE_OPT_FUSED_ROUTING: {
       const int old = g_fused_routing;
-      g_fused_routing = value <= 0 ? 0 : value >= 2 ? 2 : 1;
+      g_fused_routing = value <= 0 ? 0 : value >= 3 ? 3 : value;
       return old;
     }
     case MOE_OPT_FUSED_COMBINE: {
@@ -922,9 +954,12 @@ int moe_layer_launch_count(const moe_config_t* cfg) {
   if (small_route(static_cast<long long>(cfg->T) * cfg->k, cfg->E)) {
     n += 1;  // init_routing + permutation gather in one kernel
   } else {
-    // histogram, scan + stable scatter (one cluster launch when fused, up to
-    // kClusterSortRows expanded rows)
-    n += (g_fused_routing && static_cast<long long>(cfg->T) * cfg->k <= kClusterSortRows) ? 1 : 2;
+    // histogram, scan + stable scatter: one launch after the fused router
+    // (from its histograms), or as one cluster up to kClusterSortRows rows
+    n += (chunk_sort_on(cfg) ||
+          (g_fused_routing && static_cast<long long>(cfg->T) * cfg->k <= kClusterSortRows))
+             ? 1
+             : 2;
     if (gather_mode(cfg) == 0) n += 1;  // permutation gather
   }
   n += 2;  // routed gate/up, down

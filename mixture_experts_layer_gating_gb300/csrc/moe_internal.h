@@ -114,9 +114,21 @@ bool router_topk_ok(int T, int E, int D, int k);
 // Whether the fused kernel is the faster choice for the shape (>= 64 CTAs).
 bool router_topk_preferred(int T, int E, int D);
 void router_topk_split(int T, int E, int D, int& ck, int& nh);
+// Its CTAs, in launch order, and the expanded rows of each one's tokens
+// (128 / (ck nh) tokens times k): CTA b's rows are [b chunk_rows, (b + 1)
+// chunk_rows).  With chunk_hist (16-byte aligned, nchunks x E int32) the
+// kernel also writes each CTA's expert histogram of those rows there.
+void router_topk_chunks(int T, int E, int D, int k, int& nchunks, int& chunk_rows);
 cudaError_t launch_router_topk(const void* x, const void* Wg, const float* bias, int T, int D,
                                int E, int k, int renorm, float* logits, int32_t* ids, float* w,
-                               int32_t* err, cudaStream_t s);
+                               int32_t* err, cudaStream_t s, int32_t* chunk_hist = nullptr);
+// init_routing from those histograms: a CTA per few chunks, no cluster (E <= 512,
+// E % 4 == 0, chunk_rows <= 8192).  Same results as the other init_routing
+// kernels when the histograms count the ids.
+cudaError_t launch_route_sort_chunks(const int32_t* ids, int R, int E, int nchunks, int chunk_rows,
+                                     const int32_t* chunk_hist, int32_t* counts, int32_t* offsets,
+                                     int32_t* sorted_rows, int32_t* dest, int32_t* err,
+                                     cudaStream_t s);
 
 // Split-K factor of the router projection (a pure function of the shape, so
 // the workspace size does not depend on the device).

@@ -72,7 +72,20 @@ struct RtCtrl {
   int abort;
 };
 
-constexpr size_t rt_smem_bytes() { return 1024 + RT_RING_BYTES + sizeof(RtCtrl); }
+// outputs of the warm-up pass (below): one dummy token for each of warps 6..9;
+// and the CTA's expert histogram of its tokens' ids
+constexpr int RT_WARM_WARPS = 4;
+struct RtWarm {
+  float logits[RT_WARM_WARPS][512];
+  int32_t ids[RT_WARM_WARPS][32];
+  float w[RT_WARM_WARPS][32];
+  int32_t err;
+  int32_t hist[512];
+};
+
+constexpr size_t rt_smem_bytes() {
+  return 1024 + RT_RING_BYTES + sizeof(RtCtrl) + sizeof(RtWarm);
+}
 static_assert(rt_smem_bytes() <= 227 * 1024, "shared memory budget");
 
 struct RtParams {
@@ -84,6 +97,9 @@ struct RtParams {
   int32_t* ids;
   float* w;
   int32_t* err;
+  // optional [gridDim.x][E]: row b = expert counts of the ids of CTA b's
+  // tokens (the tokens [b * 128 / C, (b + 1) * 128 / C), C CTAs per cluster)
+  int32_t* chunk_hist;
 };
 
 // NB: experts per CTA (the MMA N); EPL: logits per lane in the top-k warp.
@@ -99,6 +115,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   RtCtrl* ctrl = reinterpret_cast<RtCtrl*>(base + RT_RING_BYTES);
+  RtWarm* warm_out = reinterpret_cast<RtWarm*>(base + RT_RING_BYTES + sizeof(RtCtrl));
   float* red = reinterpret_cast<float*>(base);  // partial rows, after the products
   volatile int* abort_flag = &ctrl->abort;
 
@@ -116,6 +133,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
   const int ld = p.nh * NB + 4;      // floats per partial row
   const int e0 = hx * NB;            // first expert of this CTA
 
+  for (int e = threadIdx.x; e < p.E; e += RT_THREADS) warm_out->hist[e] = 0;
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&ctrl->full[s], 1);
@@ -214,67 +232,90 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
     __syncwarp();
   }
 
-  // ---------------------------------------------------------- accumulator
-  bool have_acc = false;
-  if (warp >= 2 && warp < 6) {
-    have_acc = mbar_wait(&ctrl->tfull, 0, abort_flag);
-    if (!have_acc && lane == 0) {
-      ctrl->abort = 1;
-      atomicOr(p.err, MOE_DEV_WAIT_TIMEOUT);
-    }
-    __syncwarp();
-    tc_fence_after_sync();
-  }
-  // every CTA of the cluster has finished its products: the rings may be overwritten
-  tc_fence_before_sync();
-  cluster_sync();
-  tc_fence_after_sync();
-  if (warp >= 2 && warp < 6) {
-    const int quarter = warp & 3;  // TMEM lanes [32 quarter, 32 quarter + 32)
-    const int r = quarter * 32 + lane;
-    const int owner = r / rpo, local = r - owner * rpo;
-    const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
-    float* row = red + static_cast<size_t>(sl * rpo + local) * ld + e0;
-    const uint32_t dst = mapa_shared(row, static_cast<uint32_t>(owner));
-    for (int c = 0; c < nbox * 64; c += 32) {
-      uint32_t v[32];
-      tmem_ld_32x32b_x32(taddr + c, v);
-      tc_wait_ld();
-      if (!have_acc) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = 0u;
+  // Two passes through one loop body, so that both run the same code.  Pass 0:
+  // warps 6..9 (one per SM sub-partition) take the top-k of one dummy token
+  // (rows of the stage ring as they happen to be, results to shared scratch)
+  // while the products run, which brings the routine's code into the SM's
+  // instruction caches: fetched cold once the partial rows are in, it cost
+  // ~3 us per launch (the GEMMs of the layer stream their weights through
+  // the L2 in between).  Pass 1: the hand-over and the real tokens.
+#pragma unroll 1
+  for (int pass = 0; pass < 2; ++pass) {
+    const bool warm = pass == 0;
+    if (!warm) {
+      // ---------------------------------------------------------- accumulator
+      bool have_acc = false;
+      if (warp >= 2 && warp < 6) {
+        have_acc = mbar_wait(&ctrl->tfull, 0, abort_flag);
+        if (!have_acc && lane == 0) {
+          ctrl->abort = 1;
+          atomicOr(p.err, MOE_DEV_WAIT_TIMEOUT);
+        }
+        __syncwarp();
+        tc_fence_after_sync();
       }
+      // every CTA of the cluster has finished its products: the rings may be overwritten
+      tc_fence_before_sync();
+      cluster_sync();
+      tc_fence_after_sync();
+      if (warp >= 2 && warp < 6) {
+        const int quarter = warp & 3;  // TMEM lanes [32 quarter, 32 quarter + 32)
+        const int r = quarter * 32 + lane;
+        const int owner = r / rpo, local = r - owner * rpo;
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+        float* row = red + static_cast<size_t>(sl * rpo + local) * ld + e0;
+        const uint32_t dst = mapa_shared(row, static_cast<uint32_t>(owner));
+        for (int c = 0; c < nbox * 64; c += 32) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(taddr + c, v);
+          tc_wait_ld();
+          if (!have_acc) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        st_cluster_v4(dst + static_cast<uint32_t>((c + 4 * j) * 4), v[4 * j], v[4 * j + 1],
-                      v[4 * j + 2], v[4 * j + 3]);
+            for (int j = 0; j < 32; ++j) v[j] = 0u;
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            st_cluster_v4(dst + static_cast<uint32_t>((c + 4 * j) * 4), v[4 * j], v[4 * j + 1],
+                          v[4 * j + 2], v[4 * j + 3]);
+        }
+      }
+      // every partial row has arrived at its finishing CTA
+      tc_fence_before_sync();
+      cluster_sync();
+      tc_fence_after_sync();
+      if (warp == 1) tmem_dealloc(tmem_base, NB);
     }
-  }
-  // every partial row has arrived at its finishing CTA
-  tc_fence_before_sync();
-  cluster_sync();
-  tc_fence_after_sync();
-  if (warp == 1) tmem_dealloc(tmem_base, NB);
 
-  // ---------------------------------------------------------- top-k softmax
-  for (int i = warp; i < rpo; i += RT_WARPS) {
-    const int t = m0 + q * rpo + i;
-    if (t >= p.T) break;  // tokens grow with i
-    float v[EPL];
+    // -------------------------------------------------------- top-k softmax
+    int i = warm ? (warp >= 6 && warp < 6 + RT_WARM_WARPS ? 0 : rpo) : warp;
+    for (; i < (warm ? 1 : rpo); i += RT_WARPS) {
+      const int t = m0 + q * rpo + i;
+      if (!warm && t >= p.T) break;  // tokens grow with i
+      float v[EPL];
 #pragma unroll
-    for (int j = 0; j < EPL; ++j) {
-      const int e = lane + 32 * j;
-      float s = 0.0f;
-      if (e < p.E) {
-        s = red[static_cast<size_t>(i) * ld + e];
-        for (int z = 1; z < p.ck; ++z) s += red[static_cast<size_t>(z * rpo + i) * ld + e];
+      for (int j = 0; j < EPL; ++j) {
+        const int e = lane + 32 * j;
+        float s = 0.0f;
+        if (e < p.E) {
+          s = red[static_cast<size_t>(i) * ld + e];
+          for (int z = 1; z < p.ck; ++z) s += red[static_cast<size_t>(z * rpo + i) * ld + e];
+        }
+        v[j] = s;
       }
-      v[j] = s;
+      const int ww = warp - 6;
+      const int id = warp_topk_softmax<EPL>(
+          v, lane, p.E, p.k, p.renorm, p.bias,
+          warm ? warm_out->logits[ww] : p.logits + static_cast<size_t>(t) * p.E,
+          warm ? warm_out->ids[ww] : p.ids + static_cast<size_t>(t) * p.k,
+          warm ? warm_out->w[ww] : p.w + static_cast<size_t>(t) * p.k,
+          warm ? &warm_out->err : p.err);
+      if (!warm && id >= 0) atomicAdd(&warm_out->hist[id], 1);
     }
-    warp_topk_softmax<EPL>(v, lane, p.E, p.k, p.renorm, p.bias,
-                           p.logits + static_cast<size_t>(t) * p.E,
-                           p.ids + static_cast<size_t>(t) * p.k, p.w + static_cast<size_t>(t) * p.k,
-                           p.err);
+  }
+  if (p.chunk_hist) {
+    __syncthreads();
+    for (int e = threadIdx.x; e < p.E; e += RT_THREADS)
+      p.chunk_hist[static_cast<size_t>(blockIdx.x) * p.E + e] = warm_out->hist[e];
   }
 }
 
@@ -341,10 +382,19 @@ bool router_topk_preferred(int T, int E, int D) {
   return static_cast<long long>((T + RT_BM - 1) / RT_BM) * ck * nh >= 64;
 }
 
+void router_topk_chunks(int T, int E, int D, int k, int& nchunks, int& chunk_rows) {
+  int ck, nh;
+  router_topk_split(T, E, D, ck, nh);
+  nchunks = (T + RT_BM - 1) / RT_BM * ck * nh;
+  chunk_rows = RT_BM / (ck * nh) * k;
+}
+
 cudaError_t launch_router_topk(const void* x, const void* Wg, const float* bias, int T, int D,
                                int E, int k, int renorm, float* logits, int32_t* ids, float* w,
-                               int32_t* err, cudaStream_t s) {
-  if (!router_topk_ok(T, E, D, k) || !x || !Wg || !logits || !ids || !w) return cudaErrorInvalidValue;
+                               int32_t* err, cudaStream_t s, int32_t* chunk_hist) {
+  if (!router_topk_ok(T, E, D, k) || !x || !Wg || !logits || !ids || !w ||
+      (reinterpret_cast<uintptr_t>(chunk_hist) & 15))
+    return cudaErrorInvalidValue;
   RtParams p;
   p.T = T;
   p.D = D;
@@ -357,6 +407,7 @@ cudaError_t launch_router_topk(const void* x, const void* Wg, const float* bias,
   p.ids = ids;
   p.w = w;
   p.err = err;
+  p.chunk_hist = chunk_hist;
   CUtensorMap tx, tw;
   {
     const uint64_t dims[2] = {static_cast<uint64_t>(D), static_cast<uint64_t>(T)};

@@ -460,6 +460,153 @@ __global__ void __launch_bounds__(kSortWarps * 32, 1)
 }
 
 // ------------------------------------------------------------------------
+// init_routing after the fused router (router_sm103.cu), which also writes
+// the expert histogram of each of its CTAs' tokens: chunk_hist[b][e] = rows of
+// expert e among the rows [b * chunk_rows, (b + 1) * chunk_rows).  CTA b of
+// this grid takes the same rows: it adds, per expert, the histograms of the
+// chunks before it (its base position) and of all of them (counts), scans the
+// counts over experts (offsets; CTA 0 publishes both), and scatters its rows
+// in order as route_scatter_kernel does.  The same stable counting sort as
+// the other init_routing kernels, with no cluster or grid-wide wait.  A CTA
+// takes cpb consecutive chunks, so that the grid stays at about 32 CTAs:
+// with one CTA per chunk (64-128) the sort waited for SMs held by the shared
+// expert's GEMMs on the side stream (Gemma-4-style prefill: 460 -> 467 us a
+// layer).  A position outside [0, R) (histograms that do not match the ids)
+// is never written: the row gets dest = -1 and MOE_DEV_BAD_DEST is flagged.
+constexpr int kChunkThreads = 512;
+constexpr int kChunkWarps = kChunkThreads / 32;
+constexpr int kChunkCtas = 32;        // about this many CTAs
+constexpr int kChunkMaxRows = 8192;   // rows of one CTA (its ids in shared memory)
+
+size_t chunk_sort_smem(int E, int cta_rows) {
+  const int ngrp = kChunkThreads / (E / 4);
+  return (2 * static_cast<size_t>(ngrp) * E + static_cast<size_t>(kChunkWarps) * E + cta_rows) *
+         sizeof(int32_t);
+}
+
+__global__ void __launch_bounds__(kChunkThreads)
+    route_sort_chunks_kernel(const int32_t* __restrict__ ids, int R, int E, int nchunks,
+                             int chunk_rows, int cpb, const int32_t* __restrict__ chunk_hist,
+                             int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                             int32_t* __restrict__ sorted_rows, int32_t* __restrict__ dest,
+                             int32_t* err) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int b = blockIdx.x;
+  const int c0 = b * cpb;  // first chunk of this CTA
+  const long long r0 = static_cast<long long>(c0) * chunk_rows;
+  const int n = static_cast<int>(max(0LL, min(static_cast<long long>(cpb) * chunk_rows, R - r0)));
+  if (n == 0 && b != 0) return;  // nothing to sort (CTA 0 still publishes counts / offsets)
+  extern __shared__ int32_t sm[];
+  const int E4 = E >> 2;                  // 16-byte columns of a histogram row (E % 4 == 0)
+  const int ngrp = kChunkThreads / E4;    // >= 4 chunk groups (E <= 512)
+  int32_t* part = sm;                     // [2][ngrp][E]: partial sums before b / over all
+  int32_t* wcnt = part + 2 * ngrp * E;    // [kChunkWarps][E]: per-warp counts, then starts
+  int32_t* ids_s = wcnt + kChunkWarps * E;  // [cpb * chunk_rows]: this CTA's expert ids
+  __shared__ int32_t warp_sum[kChunkWarps];
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+
+  // (a) each thread sums four experts over every ngrp-th chunk (16-byte loads)
+  {
+    const int col = tid % E4, grp = tid / E4;
+    if (grp < ngrp) {
+      int4 pre = make_int4(0, 0, 0, 0), tot = make_int4(0, 0, 0, 0);
+#pragma unroll 8
+      for (int c = grp; c < nchunks; c += ngrp) {
+        const int4 v = __ldg(reinterpret_cast<const int4*>(chunk_hist + static_cast<size_t>(c) * E) + col);
+        tot.x += v.x; tot.y += v.y; tot.z += v.z; tot.w += v.w;
+        if (c < c0) {
+          pre.x += v.x; pre.y += v.y; pre.z += v.z; pre.w += v.w;
+        }
+      }
+      reinterpret_cast<int4*>(part + grp * E)[col] = pre;
+      reinterpret_cast<int4*>(part + (ngrp + grp) * E)[col] = tot;
+    }
+  }
+  for (int i = tid; i < n; i += kChunkThreads) ids_s[i] = ids[r0 + i];
+  for (int i = tid; i < kChunkWarps * E; i += kChunkThreads) wcnt[i] = 0;
+  __syncthreads();
+
+  // (b) per expert e = thread: base position and count; exclusive scan of
+  // the counts over experts
+  const int e = tid;
+  int pre = 0, tot = 0;
+  if (e < E) {
+    for (int g = 0; g < ngrp; ++g) {
+      pre += part[g * E + e];
+      tot += part[(ngrp + g) * E + e];
+    }
+  }
+  int incl = tot;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int y = __shfl_up_sync(FULL, incl, d);
+    if (lane >= d) incl += y;
+  }
+  if (lane == 31) warp_sum[wid] = incl;
+
+  // (c) warp w counts its piece of the chunk's rows per expert
+  const int piece = (n + kChunkWarps - 1) / kChunkWarps;
+  const int w0 = min(n, wid * piece), w1 = min(n, w0 + piece);
+  bool bad = false;
+  for (int r = w0 + lane; r < w1; r += 32) {
+    const int id = ids_s[r];
+    if (id >= 0 && id < E) atomicAdd(&wcnt[wid * E + id], 1);
+    else bad = true;
+  }
+  if (__syncthreads_or(bad) && tid == 0) atomicOr(err, MOE_DEV_BAD_EXPERT_ID);
+  int wbase = 0, all = 0;
+  for (int w = 0; w < kChunkWarps; ++w) {
+    const int t = warp_sum[w];
+    if (w < wid) wbase += t;
+    all += t;
+  }
+  if (e < E) {
+    const int excl = wbase + incl - tot;
+    if (b == 0) {
+      counts[e] = tot;
+      offsets[e] = excl;
+    }
+    // (d) start position of every warp's rows of expert e
+    int run = excl + pre;
+    for (int w = 0; w < kChunkWarps; ++w) {
+      const int cnt = wcnt[w * E + e];
+      wcnt[w * E + e] = run;
+      run += cnt;
+    }
+  }
+  if (b == 0 && tid == 0) offsets[E] = all;
+  __syncthreads();
+
+  // (e) ordered scatter, 32 consecutive rows per step; inside a step, equal
+  // ids are ranked by lane with __match_any_sync
+  int32_t* my = wcnt + wid * E;
+  const unsigned lt = (1u << lane) - 1u;
+  bool bad_pos = false;
+  for (int rb = w0; rb < w1; rb += 32) {
+    const int r = rb + lane;
+    const bool in = r < w1;
+    const int id = in ? ids_s[r] : -1;
+    const bool valid = in && id >= 0 && id < E;
+    const int key = valid ? id : -1 - lane;  // invalid rows never match anything
+    const unsigned peers = __match_any_sync(FULL, key);
+    if (valid) {
+      const int pos = my[id] + __popc(peers & lt);
+      const bool ok = pos >= 0 && pos < R;
+      if (ok) sorted_rows[pos] = static_cast<int32_t>(r0 + r);
+      dest[r0 + r] = ok ? pos : -1;
+      bad_pos |= !ok;
+    } else if (in) {
+      dest[r0 + r] = -1;
+    }
+    __syncwarp();
+    if (valid && (peers & lt) == 0) my[id] += __popc(peers);
+    __syncwarp();
+  }
+  if (__any_sync(FULL, bad_pos) && lane == 0) atomicOr(err, MOE_DEV_BAD_DEST);
+}
+
+// ------------------------------------------------------------------------
 // init_routing and the permutation gather in one launch, for small batches
 // (R <= kSmallRouteRows expanded rows; decode).  Every CTA loads all R expert
 // ids into shared memory and repeats the whole stable counting sort there --
@@ -1305,6 +1452,45 @@ cudaError_t launch_route_sort_cluster(const int32_t* ids, int R, int E, int32_t*
   cfg.numAttrs = 2;
   cudaError_t e = cudaLaunchKernelEx(&cfg, route_sort_cluster_kernel, ids, R, E, counts, offsets,
                                      sorted_rows, dest, err);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route_sort_chunks(const int32_t* ids, int R, int E, int nchunks, int chunk_rows,
+                                     const int32_t* chunk_hist, int32_t* counts, int32_t* offsets,
+                                     int32_t* sorted_rows, int32_t* dest, int32_t* err,
+                                     cudaStream_t s) {
+  if (R <= 0 || E < 8 || E > 512 || (E % 4) || nchunks <= 0 || chunk_rows <= 0 ||
+      chunk_rows > kChunkMaxRows || static_cast<long long>(nchunks) * chunk_rows < R || !chunk_hist ||
+      (reinterpret_cast<uintptr_t>(chunk_hist) & 15))
+    return cudaErrorInvalidValue;
+  const int cpb = std::max(1, std::min((nchunks + kChunkCtas - 1) / kChunkCtas,
+                                       kChunkMaxRows / chunk_rows));
+  const int ctas = (nchunks + cpb - 1) / cpb;
+  const size_t smem = chunk_sort_smem(E, cpb * chunk_rows);
+  static bool attr_done[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+  if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+    // the largest request: E = 512 (4 chunk groups), kChunkMaxRows rows
+    cudaError_t e = cudaFuncSetAttribute(route_sort_chunks_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(chunk_sort_smem(512, kChunkMaxRows)));
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_done[dev] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = g_pdl ? 1 : 0;
+  cfg.gridDim = dim3(ctas, 1, 1);
+  cfg.blockDim = dim3(kChunkThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, route_sort_chunks_kernel, ids, R, E, nchunks, chunk_rows,
+                                     cpb, chunk_hist, counts, offsets, sorted_rows, dest, err);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -23,9 +23,10 @@ namespace moe {
 //  4. writes ids_row[j] and w_row[j] for j < k: softmax over the k chosen
 //     logits (renorm) or the full-softmax probability of the chosen experts;
 //     a token whose every logit is non-finite gets weights 1 / k.
+// Returns ids_row[lane] on lanes below k, -1 on the others.
 // k <= 32 and E <= 32 * EPL.
 template <int EPL>
-__device__ __forceinline__ void warp_topk_softmax(float (&v)[EPL], int lane, int E, int k,
+__device__ __forceinline__ int warp_topk_softmax(float (&v)[EPL], int lane, int E, int k,
                                                   int renorm, const float* __restrict__ bias,
                                                   float* logits_row, int32_t* __restrict__ ids_row,
                                                   float* __restrict__ w_row, int32_t* err) {
@@ -100,6 +101,7 @@ __device__ __forceinline__ void warp_topk_softmax(float (&v)[EPL], int lane, int
     ids_row[lane] = my_e;
     w_row[lane] = z / denom;
   }
+  return lane < k ? my_e : -1;
 }
 
 }  // namespace moe

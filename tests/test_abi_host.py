@@ -47,13 +47,16 @@ def test_workspace_size_covers_intermediates(lib, name):
         # least 32 rows per expert, MOE_OPT_GATHER_A's default)
         gemm_gathers = shape.act_dtype == "bf16" and shape.w_dtype == "bf16" and \
             shape.T * shape.k >= 32 * shape.E
-        # (the cluster sort up to 65536 expanded rows, two kernels above)
-        routing = (1 if shape.T * shape.k <= 65536 else 2) + (0 if gemm_gathers else 1)
     # router projection and top-k as one kernel: bf16 activations, 64 <= E, and
     # more than the CUDA-core projection takes (64 tokens, 2^25 multiply-adds)
     # (and a grid of at least 64 CTAs: prefill batches; see bench.fused_router)
     fused = shape.act_dtype == "bf16" and shape.E >= 64 and not (
         shape.T <= 64 and shape.T * shape.D * shape.E <= 2 ** 25) and shape.T >= 2048
+    if shape.T * shape.k > 8192:
+        # the sort from the fused router's histograms, or the cluster sort up
+        # to 65536 expanded rows: one launch; two kernels otherwise
+        one = fused or shape.T * shape.k <= 65536
+        routing = (1 if one else 2) + (0 if gemm_gathers else 1)
     # router (+ top-k), 2 (+2 shared) GEMMs, finalize
     base = (6 if fused else 7) if shape.I_shared else (4 if fused else 5)
     assert moe.moe_layer_launch_count(cfg) == base + fp8_extra + routing
@@ -167,7 +170,8 @@ def test_set_option_values():
         (moe.MOE_OPT_SHARED_CTAS, -5, 0),
         (moe.MOE_OPT_FUSED_ROUTING, 0, 0),
         (moe.MOE_OPT_FUSED_ROUTING, 2, 2),
-        (moe.MOE_OPT_FUSED_ROUTING, 7, 2),
+        (moe.MOE_OPT_FUSED_ROUTING, 3, 3),
+        (moe.MOE_OPT_FUSED_ROUTING, 7, 3),
         (moe.MOE_OPT_FUSED_ROUTING, 1, 1),
     ]
     for opt, value, stored in cases:
@@ -188,8 +192,8 @@ def test_fused_router_launch_count(T, E, D, k, fused):
     """moe_layer makes one launch fewer where the router projection and the
     top-k run as one kernel (MOE_OPT_FUSED_ROUTING), none fewer for them where
     that kernel does not apply, and one more fewer where init_routing's
-    histogram and scatter run as one cluster launch (more than 8192 expanded
-    rows)."""
+    histogram and scatter run as one launch (more than 8192 expanded rows:
+    from the fused router's histograms, or as one cluster up to 65536 rows)."""
     ensure_library()
     cfg = moe.make_config(T, D, E, k, 768)
     old = moe.moe_set_option(moe.MOE_OPT_FUSED_ROUTING, 1)
@@ -202,7 +206,9 @@ def test_fused_router_launch_count(T, E, D, k, fused):
     if D % 8:
         assert n_on == n_off == 0  # invalid configuration
     else:
-        assert n_on == n_off - (1 if fused else 0) - (1 if 8192 < T * k <= 65536 else 0)
+        R = T * k
+        one_sort = R > 8192 and (fused or R <= 65536)
+        assert n_on == n_off - (1 if fused else 0) - (1 if one_sort else 0)
 
 
 def test_fp8_nk_layout_host_logic(lib):

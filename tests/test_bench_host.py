@@ -149,6 +149,12 @@ def test_bench_kernel_names_match_launch_count(name, layout):
             moe.moe_layer_launch_count(cfg)
     finally:
         moe.moe_set_option(moe.MOE_OPT_FUSED_ROUTING, old)
+    old = moe.moe_set_option(moe.MOE_OPT_FUSED_ROUTING, 3)
+    try:
+        assert len(bench.kernel_names(shape, nk, hist_sort=False)) == \
+            moe.moe_layer_launch_count(cfg)
+    finally:
+        moe.moe_set_option(moe.MOE_OPT_FUSED_ROUTING, old)
 
 
 def test_bench_percentiles():

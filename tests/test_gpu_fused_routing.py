@@ -174,3 +174,60 @@ def test_cluster_sort_against_oracle(T, E, k, pattern, fused):
     assert np.array_equal(sorted_rows.cpu().numpy(), o["sorted_rows"])
     assert np.array_equal(dest.cpu().numpy(), o["dest"])
     assert torch.equal(x_perm.cpu(), x[torch.from_numpy(o["sorted_rows"] // k)])
+
+
+LAYER_CASES = [
+    # T, E, k, D: the fused router's CTAs (chunks) and rows per chunk in the comment
+    (4096, 128, 8, 2048),   # Qwen3-MoE prefill shape: 128 chunks of 256 rows
+    (1100, 64, 8, 512),     # 18 chunks of 512 rows, the last one short
+    (2100, 320, 8, 1024),   # two expert halves: 68 chunks of 256 rows
+    (700, 96, 16, 256),     # one CTA per tile: 6 chunks of 2048 rows
+    (1040, 200, 16, 136),   # k = 16 (moe_layer's largest): 9 chunks of 2048 rows, E % 32 != 0
+    (9000, 512, 8, 512),    # 72000 rows (past the 8-CTA cluster sort): 142 chunks
+]
+
+
+def _layer_routing(T, E, k, D, mode):
+    gen = torch.Generator(device="cuda").manual_seed(T + 3 * E + k + D)
+    I = 64
+    x = torch.randn((T, D), generator=gen, device="cuda").to(torch.bfloat16)
+    Wg = (0.05 * torch.randn((D, E), generator=gen, device="cuda")).to(torch.bfloat16)
+    W13 = (0.02 * torch.randn((E, D, 2 * I), generator=gen, device="cuda")).to(torch.bfloat16)
+    W2 = (0.02 * torch.randn((E, I, D), generator=gen, device="cuda")).to(torch.bfloat16)
+    cfg = moe.make_config(T, D, E, k, I)
+    ws = moe.alloc_workspace(cfg)
+    out = torch.empty((T, D), dtype=torch.bfloat16, device="cuda")
+    old = moe.moe_set_option(moe.MOE_OPT_FUSED_ROUTING, mode)
+    try:
+        moe.moe_layer(cfg, x, Wg, None, W13, None, W2, None, None, None, None, None, out, ws)
+        torch.cuda.synchronize()
+    finally:
+        moe.moe_set_option(moe.MOE_OPT_FUSED_ROUTING, old)
+    R = T * k
+    view = lambda slot, n: moe.workspace_view(ws, cfg, slot, (n,), torch.int32).cpu().numpy()  # noqa: E731
+    got = {"ids": view("topk_ids", R), "counts": view("counts", E), "offsets": view("offsets", E + 1),
+           "sorted_rows": view("sorted_rows", R), "dest": view("dest", R)}
+    return got, out.cpu(), moe.moe_read_device_status(ws)
+
+
+@pytest.mark.parametrize("T,E,k,D", LAYER_CASES)
+def test_layer_sorts_by_router_histograms(T, E, k, D):
+    """moe_layer after the fused router: init_routing from the router's
+    per-CTA histograms (MOE_OPT_FUSED_ROUTING 2: the fused router wherever the
+    shape allows) against the oracle's stable counting sort of the GPU's own
+    ids, bit-exact; the layer output bit-identical to the run that sorts with
+    the other init_routing kernels (option 3: same router, same permutation)."""
+    ensure_library()
+    got, out, status = _layer_routing(T, E, k, D, 2)
+    assert status == 0
+    ids = got["ids"].reshape(T, k)
+    assert ((ids >= 0) & (ids < E)).all()
+    o = oracle.init_routing(ids, E)
+    for key in ("counts", "offsets", "sorted_rows", "dest"):
+        assert np.array_equal(got[key], o[key]), key
+    got3, out3, status3 = _layer_routing(T, E, k, D, 3)
+    assert status3 == 0
+    assert np.array_equal(got3["ids"], got["ids"])
+    for key in ("counts", "offsets", "sorted_rows", "dest"):
+        assert np.array_equal(got3[key], got[key]), key
+    assert torch.equal(out3, out)
