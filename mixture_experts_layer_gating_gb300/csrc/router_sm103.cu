@@ -23,7 +23,9 @@
 // then all 16 warps of the CTA finish its 128 / C tokens: the ck partial rows
 // added in slice order, the bias added last, the final logits written, and the
 // top-k and softmax taken by one warp per token with the same routine as the
-// stand-alone top-k kernel.  Two cluster barriers order the hand-over: one
+// stand-alone top-k kernel; on request (chunk_hist) each CTA also writes the
+// expert histogram of its tokens' ids, from which init_routing sorts the rows
+// without counting them again.  Two cluster barriers order the hand-over: one
 // after every CTA's products (its ring may be overwritten), one after every
 // partial row has arrived.  Every mbarrier wait is bounded; a CTA that gives
 // up flags MOE_DEV_WAIT_TIMEOUT and still takes part in both barriers.
@@ -72,20 +74,8 @@ struct RtCtrl {
   int abort;
 };
 
-// outputs of the warm-up pass (below): one dummy token for each of warps 6..9;
-// and the CTA's expert histogram of its tokens' ids
-constexpr int RT_WARM_WARPS = 4;
-struct RtWarm {
-  float logits[RT_WARM_WARPS][512];
-  int32_t ids[RT_WARM_WARPS][32];
-  float w[RT_WARM_WARPS][32];
-  int32_t err;
-  int32_t hist[512];
-};
-
-constexpr size_t rt_smem_bytes() {
-  return 1024 + RT_RING_BYTES + sizeof(RtCtrl) + sizeof(RtWarm);
-}
+// after the ctrl block: the CTA's expert histogram of its tokens' ids (E <= 512)
+constexpr size_t rt_smem_bytes() { return 1024 + RT_RING_BYTES + sizeof(RtCtrl) + 512 * sizeof(int32_t); }
 static_assert(rt_smem_bytes() <= 227 * 1024, "shared memory budget");
 
 struct RtParams {
@@ -115,7 +105,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   RtCtrl* ctrl = reinterpret_cast<RtCtrl*>(base + RT_RING_BYTES);
-  RtWarm* warm_out = reinterpret_cast<RtWarm*>(base + RT_RING_BYTES + sizeof(RtCtrl));
+  int32_t* hist = reinterpret_cast<int32_t*>(base + RT_RING_BYTES + sizeof(RtCtrl));
   float* red = reinterpret_cast<float*>(base);  // partial rows, after the products
   volatile int* abort_flag = &ctrl->abort;
 
@@ -133,7 +123,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
   const int ld = p.nh * NB + 4;      // floats per partial row
   const int e0 = hx * NB;            // first expert of this CTA
 
-  for (int e = threadIdx.x; e < p.E; e += RT_THREADS) warm_out->hist[e] = 0;
+  for (int e = threadIdx.x; e < p.E; e += RT_THREADS) hist[e] = 0;
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&ctrl->full[s], 1);
@@ -232,90 +222,73 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
     __syncwarp();
   }
 
-  // Two passes through one loop body, so that both run the same code.  Pass 0:
-  // warps 6..9 (one per SM sub-partition) take the top-k of one dummy token
-  // (rows of the stage ring as they happen to be, results to shared scratch)
-  // while the products run, which brings the routine's code into the SM's
-  // instruction caches: fetched cold once the partial rows are in, it cost
-  // ~3 us per launch (the GEMMs of the layer stream their weights through
-  // the L2 in between).  Pass 1: the hand-over and the real tokens.
-#pragma unroll 1
-  for (int pass = 0; pass < 2; ++pass) {
-    const bool warm = pass == 0;
-    if (!warm) {
-      // ---------------------------------------------------------- accumulator
-      bool have_acc = false;
-      if (warp >= 2 && warp < 6) {
-        have_acc = mbar_wait(&ctrl->tfull, 0, abort_flag);
-        if (!have_acc && lane == 0) {
-          ctrl->abort = 1;
-          atomicOr(p.err, MOE_DEV_WAIT_TIMEOUT);
-        }
-        __syncwarp();
-        tc_fence_after_sync();
-      }
-      // every CTA of the cluster has finished its products: the rings may be overwritten
-      tc_fence_before_sync();
-      cluster_sync();
-      tc_fence_after_sync();
-      if (warp >= 2 && warp < 6) {
-        const int quarter = warp & 3;  // TMEM lanes [32 quarter, 32 quarter + 32)
-        const int r = quarter * 32 + lane;
-        const int owner = r / rpo, local = r - owner * rpo;
-        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
-        float* row = red + static_cast<size_t>(sl * rpo + local) * ld + e0;
-        const uint32_t dst = mapa_shared(row, static_cast<uint32_t>(owner));
-        for (int c = 0; c < nbox * 64; c += 32) {
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(taddr + c, v);
-          tc_wait_ld();
-          if (!have_acc) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = 0u;
-          }
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            st_cluster_v4(dst + static_cast<uint32_t>((c + 4 * j) * 4), v[4 * j], v[4 * j + 1],
-                          v[4 * j + 2], v[4 * j + 3]);
-        }
-      }
-      // every partial row has arrived at its finishing CTA
-      tc_fence_before_sync();
-      cluster_sync();
-      tc_fence_after_sync();
-      if (warp == 1) tmem_dealloc(tmem_base, NB);
+  // ---------------------------------------------------------- accumulator
+  bool have_acc = false;
+  if (warp >= 2 && warp < 6) {
+    have_acc = mbar_wait(&ctrl->tfull, 0, abort_flag);
+    if (!have_acc && lane == 0) {
+      ctrl->abort = 1;
+      atomicOr(p.err, MOE_DEV_WAIT_TIMEOUT);
     }
+    __syncwarp();
+    tc_fence_after_sync();
+  }
+  // every CTA of the cluster has finished its products: the rings may be overwritten
+  tc_fence_before_sync();
+  cluster_sync();
+  tc_fence_after_sync();
+  if (warp >= 2 && warp < 6) {
+    const int quarter = warp & 3;  // TMEM lanes [32 quarter, 32 quarter + 32)
+    const int r = quarter * 32 + lane;
+    const int owner = r / rpo, local = r - owner * rpo;
+    const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+    float* row = red + static_cast<size_t>(sl * rpo + local) * ld + e0;
+    const uint32_t dst = mapa_shared(row, static_cast<uint32_t>(owner));
+    for (int c = 0; c < nbox * 64; c += 32) {
+      uint32_t v[32];
+      tmem_ld_32x32b_x32(taddr + c, v);
+      tc_wait_ld();
+      if (!have_acc) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = 0u;
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        st_cluster_v4(dst + static_cast<uint32_t>((c + 4 * j) * 4), v[4 * j], v[4 * j + 1],
+                      v[4 * j + 2], v[4 * j + 3]);
+    }
+  }
+  // every partial row has arrived at its finishing CTA
+  tc_fence_before_sync();
+  cluster_sync();
+  tc_fence_after_sync();
+  if (warp == 1) tmem_dealloc(tmem_base, NB);
 
-    // -------------------------------------------------------- top-k softmax
-    int i = warm ? (warp >= 6 && warp < 6 + RT_WARM_WARPS ? 0 : rpo) : warp;
-    for (; i < (warm ? 1 : rpo); i += RT_WARPS) {
-      const int t = m0 + q * rpo + i;
-      if (!warm && t >= p.T) break;  // tokens grow with i
-      float v[EPL];
+  // ---------------------------------------------------------- top-k softmax
+  for (int i = warp; i < rpo; i += RT_WARPS) {
+    const int t = m0 + q * rpo + i;
+    if (t >= p.T) break;  // tokens grow with i
+    float v[EPL];
 #pragma unroll
-      for (int j = 0; j < EPL; ++j) {
-        const int e = lane + 32 * j;
-        float s = 0.0f;
-        if (e < p.E) {
-          s = red[static_cast<size_t>(i) * ld + e];
-          for (int z = 1; z < p.ck; ++z) s += red[static_cast<size_t>(z * rpo + i) * ld + e];
-        }
-        v[j] = s;
+    for (int j = 0; j < EPL; ++j) {
+      const int e = lane + 32 * j;
+      float s = 0.0f;
+      if (e < p.E) {
+        s = red[static_cast<size_t>(i) * ld + e];
+        for (int z = 1; z < p.ck; ++z) s += red[static_cast<size_t>(z * rpo + i) * ld + e];
       }
-      const int ww = warp - 6;
-      const int id = warp_topk_softmax<EPL>(
-          v, lane, p.E, p.k, p.renorm, p.bias,
-          warm ? warm_out->logits[ww] : p.logits + static_cast<size_t>(t) * p.E,
-          warm ? warm_out->ids[ww] : p.ids + static_cast<size_t>(t) * p.k,
-          warm ? warm_out->w[ww] : p.w + static_cast<size_t>(t) * p.k,
-          warm ? &warm_out->err : p.err);
-      if (!warm && id >= 0) atomicAdd(&warm_out->hist[id], 1);
+      v[j] = s;
     }
+    const int id = warp_topk_softmax<EPL>(v, lane, p.E, p.k, p.renorm, p.bias,
+                                          p.logits + static_cast<size_t>(t) * p.E,
+                                          p.ids + static_cast<size_t>(t) * p.k,
+                                          p.w + static_cast<size_t>(t) * p.k, p.err);
+    if (id >= 0) atomicAdd(&hist[id], 1);
   }
   if (p.chunk_hist) {
     __syncthreads();
     for (int e = threadIdx.x; e < p.E; e += RT_THREADS)
-      p.chunk_hist[static_cast<size_t>(blockIdx.x) * p.E + e] = warm_out->hist[e];
+      p.chunk_hist[static_cast<size_t>(blockIdx.x) * p.E + e] = hist[e];
   }
 }
 
