@@ -102,8 +102,12 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
   constexpr int STAGES = RtCfg<NB>::kStages;
   constexpr int STAGE_BYTES = RtCfg<NB>::kStageBytes;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* base = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  // 1024-byte aligned start, formed as smem_raw + offset (not through an
+  // integer round trip) so that the compiler keeps it a shared-memory pointer:
+  // the partial rows' loads and the histogram's atomics are then shared-space
+  // accesses, not generic ones ordered behind the tokens' global stores
+  const uint32_t s_raw = smem_u32(smem_raw);
+  uint8_t* base = smem_raw + (((s_raw + 1023u) & ~1023u) - s_raw);
   RtCtrl* ctrl = reinterpret_cast<RtCtrl*>(base + RT_RING_BYTES);
   int32_t* hist = reinterpret_cast<int32_t*>(base + RT_RING_BYTES + sizeof(RtCtrl));
   float* red = reinterpret_cast<float*>(base);  // partial rows, after the products
